@@ -1,0 +1,214 @@
+"""KDA oracle: slow, plain, fp64 CPU statements of what the KDA core computes.
+
+TEST INFRASTRUCTURE ONLY.  The CUDA library never imports, links or calls
+anything here, and nothing here imports the library.  Only ``tests/``, the
+smoke check and the benchmark's CPU-baseline leg use this package.
+
+Two independent statements of the same mathematics:
+
+* ``recurrence`` -- the token-by-token recurrence (C, fp64, ``kda_oracle.c``),
+  as defined on the nnterp "kimi_linear" page (paragraph on Kimi Delta
+  Attention: channel-wise decay before each delta-rule update, L2 norm of q
+  and k inside the kernel) with the L2 norm and scale of the Ascend model
+  file's ``_l2_normalize`` / ``_torch_chunk_kda``.  This is THE oracle.
+* ``chunked_form`` -- the chunk-parallel (WY/UT) form restated, step by step
+  and in the same order, from ``_torch_chunk_kda`` in the Ascend model file
+  (tail padding, per-chunk cumulative log-decay, strictly-lower interaction
+  matrix, forward substitution, corrected keys/values, causal intra-chunk
+  scores, inter-chunk state pass).  Pure numpy, fp64, exact pairwise
+  exponentials; used only to cross-check the recurrence on tiny inputs.
+
+``step`` is one decode token of the recurrence on rows of a state pool picked
+by slot indices (the model file's ``_decode_gdr`` / ``_decode_fused_kda``
+semantics: the pool is updated in place).
+
+State orientation: the oracle works in the mathematical K x V orientation.
+The library stores states as [.., V, K]; callers transpose when comparing.
+
+Parity status of each function is recorded with its pins in
+``tests/test_oracle_pins.py``; every function here is pinned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libkda_oracle.so")
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile the C recurrence with the host gcc (portable flags, no fast-math)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            dp = ctypes.POINTER(ctypes.c_double)
+            lib.kda_oracle_recurrence.argtypes = [
+                dp, dp, dp, dp, dp, ctypes.POINTER(ctypes.c_int64),
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                dp, dp, dp, ctypes.c_int]
+            lib.kda_oracle_recurrence.restype = ctypes.c_int
+            lib.kda_oracle_max_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def max_threads() -> int:
+    return int(_load().kda_oracle_max_threads())
+
+
+def _f64(x) -> np.ndarray:
+    """Widen to a contiguous fp64 numpy array (exact for bf16 and fp32 values)."""
+    if hasattr(x, "detach"):  # torch tensor on the CPU
+        x = x.detach().cpu().float().numpy() if str(x.dtype) == "torch.bfloat16" else x.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def recurrence(q, k, v, g, beta, cu_seqlens=None, initial_state=None, scale=None,
+               n_threads: int = 0):
+    """Token recurrence in fp64.
+
+    q, k, g: [T, H, K]; v: [T, H, V]; beta: [T, H]  (T = all tokens, packed);
+    cu_seqlens: [N+1] sequence offsets, or None for one sequence;
+    initial_state: [N, H, K, V] (math orientation) or None for zeros.
+    Returns (o [T, H, V], final_state [N, H, K, V]), both fp64.
+    """
+    q, k, v, g, beta = (_f64(t) for t in (q, k, v, g, beta))
+    T, H, K = q.shape
+    V = v.shape[-1]
+    if cu_seqlens is None:
+        cu = np.array([0, T], dtype=np.int64)
+    else:
+        cu = np.ascontiguousarray(np.asarray(
+            cu_seqlens.cpu().numpy() if hasattr(cu_seqlens, "cpu") else cu_seqlens,
+            dtype=np.int64))
+    n = len(cu) - 1
+    if scale is None:
+        scale = K ** -0.5
+    o = np.zeros((T, H, V), dtype=np.float64)
+    sf = np.zeros((n, H, K, V), dtype=np.float64)
+    s0 = None if initial_state is None else _f64(initial_state)
+    if s0 is not None and s0.shape != (n, H, K, V):
+        raise ValueError(f"initial_state shape {s0.shape} != {(n, H, K, V)}")
+    rc = _load().kda_oracle_recurrence(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+        cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n, H, K, V, float(scale),
+        _ptr(s0) if s0 is not None else None, _ptr(o), _ptr(sf), int(n_threads))
+    if rc != 0:
+        raise RuntimeError("kda_oracle_recurrence failed (bad arguments or out of memory)")
+    return o, sf
+
+
+def step(q, k, v, g, beta, pool, state_indices=None, scale=None):
+    """One decode token per sequence on a state pool, in fp64.
+
+    q, k, g: [N, H, K]; v: [N, H, V]; beta: [N, H]; pool: [slots, H, K, V]
+    (math orientation, NOT modified); state_indices: [N] slot per sequence or
+    None for slot n.  Returns (o [N, H, V], new_pool) with the picked slots
+    advanced by one token and every other slot unchanged.
+    """
+    q = _f64(q)
+    N = q.shape[0]
+    pool = _f64(pool).copy()
+    idx = np.arange(N) if state_indices is None else np.asarray(
+        state_indices.cpu().numpy() if hasattr(state_indices, "cpu") else state_indices, dtype=np.int64)
+    cu = np.arange(N + 1, dtype=np.int64)
+    o, sf = recurrence(q, k, v, g, beta, cu_seqlens=cu, initial_state=pool[idx], scale=scale)
+    pool[idx] = sf
+    return o, pool
+
+
+def _l2_normalize(x: np.ndarray) -> np.ndarray:
+    # eps 1e-6 added to the sum of squares, inside the root (model file, _l2_normalize)
+    return x / np.sqrt((x * x).sum(axis=-1, keepdims=True) + 1e-6)
+
+
+def chunked_form(q, k, v, g, beta, initial_state=None, chunk: int = 64, scale=None):
+    """Chunk-parallel KDA for ONE sequence, in fp64 (model file, _torch_chunk_kda).
+
+    q, k, g: [T, H, K]; v: [T, H, V]; beta: [T, H]; initial_state: [H, K, V]
+    or None.  Returns (o [T, H, V], final_state [H, K, V]).
+    """
+    q, k, v, g, beta = (_f64(t) for t in (q, k, v, g, beta))
+    T, H, K = q.shape
+    V = v.shape[-1]
+    if scale is None:
+        scale = K ** -0.5
+    S_all = np.zeros((H, K, V)) if initial_state is None else _f64(initial_state).copy()
+
+    # 1. right-pad to a multiple of the chunk: zero q/k/v, zero log-decay (no
+    #    decay) and zero beta (no write), so padded tokens leave the state alone.
+    pad = (-T) % chunk
+    if pad:
+        zk = np.zeros((pad, H, K))
+        q, k, g = (np.concatenate([t, zk]) for t in (q, k, g))
+        v = np.concatenate([v, np.zeros((pad, H, V))])
+        beta = np.concatenate([beta, np.zeros((pad, H))])
+    n_chunks = q.shape[0] // chunk
+
+    # 2. L2-normalise q and k over the key dim; fold the scale into q.
+    qn = _l2_normalize(q) * scale
+    kn = _l2_normalize(k)
+
+    o = np.zeros((n_chunks * chunk, H, V))
+    for h in range(H):
+        S = S_all[h]
+        for c in range(n_chunks):
+            rows = slice(c * chunk, (c + 1) * chunk)
+            Q, Kc, Vc = qn[rows, h], kn[rows, h], v[rows, h]
+            b = beta[rows, h]
+            # 3. cumulative log-decay inside the chunk
+            G = np.cumsum(g[rows, h], axis=0)
+            # 4. strictly-lower interaction matrix, rows scaled by beta:
+            #    M[r, j] = beta_r * sum_d k_r,d k_j,d exp(G_r,d - G_j,d), j < r
+            M = np.zeros((chunk, chunk))
+            for r in range(chunk):
+                for j in range(r):
+                    M[r, j] = b[r] * np.sum(Kc[r] * Kc[j] * np.exp(G[r] - G[j]))
+            # 5. forward substitution: X = (I + M)^-1 built row by row, then
+            #    columns scaled by beta: Tm = (I + M)^-1 diag(beta)
+            X = np.zeros((chunk, chunk))
+            for r in range(chunk):
+                X[r] = -(M[r, :r] @ X[:r]) if r else 0.0
+                X[r, r] += 1.0
+            Tm = X * b[None, :]
+            # 6. corrected keys and values
+            W = Tm @ (np.exp(G) * Kc)
+            U = Tm @ Vc
+            # 7. causal intra-chunk scores, diagonal kept
+            A = np.zeros((chunk, chunk))
+            for r in range(chunk):
+                for j in range(r + 1):
+                    A[r, j] = np.sum(Q[r] * np.exp(G[r] - G[j]) * Kc[j])
+            # 8. inter-chunk pass: new values, output, state carried to the next chunk
+            Vnew = U - W @ S
+            o[rows, h] = (Q * np.exp(G)) @ S + A @ Vnew
+            GC = G[-1]
+            S = np.exp(GC)[:, None] * S + (np.exp(GC[None, :] - G) * Kc).T @ Vnew
+        S_all[h] = S
+    return o[:T], S_all

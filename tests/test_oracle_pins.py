@@ -1,0 +1,290 @@
+"""Pins of the fp64 oracle to facts fixed by the pages and by mathematics.
+
+None of these re-types the oracle's loop: each checks a closed form, an
+invariant, a special case that reduces to a textbook result, or a brute-force
+hand expansion.  Together they are chosen so that a plausible slip in the
+oracle (decay applied after the read, read-out before the write, eps outside
+the root, a transposed state, a wrong sign in the residual, a dropped decay
+factor in the chunked form) fails at least one of them.
+
+Sources: nnterp "kimi_linear" page (definition of Kimi Delta Attention: the
+state decays channel by channel before each delta-rule update; L2 norm of q
+and k in the kernel); Ascend model file, ``_l2_normalize`` (eps 1e-6 on the
+sum of squares, inside the root) and ``_torch_chunk_kda`` (scale 1/sqrt(K) on
+the normalised query, chunked form, zero padding of the tail).
+"""
+import numpy as np
+import pytest
+
+import oracle
+
+EPS = 1e-6
+
+
+def _rand(rng, T, H, K, V, g_lo=-0.3, g_hi=-0.01):
+    q = rng.standard_normal((T, H, K))
+    k = rng.standard_normal((T, H, K))
+    v = rng.standard_normal((T, H, V))
+    g = rng.uniform(g_lo, g_hi, (T, H, K))
+    beta = 1 / (1 + np.exp(-rng.standard_normal((T, H))))
+    return q, k, v, g, beta
+
+
+def _unit(x):
+    return x / np.sqrt((x * x).sum(-1, keepdims=True) + EPS)
+
+
+# ---- L2 norm and scale ------------------------------------------------------
+
+def test_eps_inside_root_on_sum_of_squares():
+    # q = 1e-3 e_1, k = e_1, S0 = 0, one token, beta = 1, g = 0:
+    #   k_hat = 1/sqrt(1 + 1e-6) e_1, q_hat = 1e-3/sqrt(1e-6 + 1e-6) e_1 = e_1/sqrt(2)
+    #   o = scale * beta * (k_hat . q_hat) * v
+    K, V = 4, 3
+    q = np.zeros((1, 1, K)); q[0, 0, 0] = 1e-3
+    k = np.zeros((1, 1, K)); k[0, 0, 0] = 1.0
+    v = np.array([[[1.0, -2.0, 0.5]]])
+    g = np.zeros((1, 1, K)); beta = np.ones((1, 1))
+    o, S = oracle.recurrence(q, k, v, g, beta, scale=0.5)
+    kq = (1 / np.sqrt(1 + 1e-6)) * (1 / np.sqrt(2.0))
+    np.testing.assert_allclose(o[0, 0], 0.5 * kq * v[0, 0], rtol=1e-13)
+    # eps outside the root would give ~0.999 instead of 1/sqrt(2)
+    assert abs(o[0, 0, 0] / (0.5 * v[0, 0, 0]) - 0.70710643) < 1e-6
+
+
+def test_default_scale_is_inverse_sqrt_K():
+    rng = np.random.default_rng(1)
+    q, k, v, g, b = _rand(rng, 5, 1, 16, 3)
+    o1, _ = oracle.recurrence(q, k, v, g, b)
+    o2, _ = oracle.recurrence(q, k, v, g, b, scale=0.25)
+    np.testing.assert_allclose(o1, o2, rtol=1e-14)
+
+
+# ---- closed forms -----------------------------------------------------------
+
+def test_beta_zero_is_pure_channel_decay():
+    # beta = 0: no writes. S_T = diag(exp(sum_t g_t)) S0 and
+    # o_t = scale * (diag(exp(G_t)) S0)^T q_hat_t, G_t = sum_{s<=t} g_s.
+    rng = np.random.default_rng(2)
+    T, H, K, V = 37, 2, 5, 3
+    q, k, v, g, _ = _rand(rng, T, H, K, V)
+    beta = np.zeros((T, H))
+    s0 = rng.standard_normal((1, H, K, V))
+    o, S = oracle.recurrence(q, k, v, g, beta, initial_state=s0, scale=0.7)
+    G = np.cumsum(g, axis=0)                          # [T, H, K]
+    np.testing.assert_allclose(S[0], np.exp(G[-1])[:, :, None] * s0[0], rtol=1e-12)
+    qh = _unit(q)
+    for t in range(T):
+        for h in range(H):
+            expect = 0.7 * (np.exp(G[t, h])[:, None] * s0[0, h]).T @ qh[t, h]
+            np.testing.assert_allclose(o[t, h], expect, rtol=1e-11, atol=1e-14)
+
+
+def test_single_token_from_zero_is_one_delta_write():
+    # S0 = 0, one token: the decay acts on zero, u = beta v, S = beta k_hat v^T,
+    # o = scale * beta (k_hat . q_hat) v.  K != V catches a transposed state.
+    rng = np.random.default_rng(3)
+    K, V = 6, 4
+    q, k, v, g, beta = _rand(rng, 1, 1, K, V)
+    o, S = oracle.recurrence(q, k, v, g, beta, scale=0.3)
+    kh, qh = _unit(k[0, 0]), _unit(q[0, 0])
+    np.testing.assert_allclose(S[0, 0], beta[0, 0] * np.outer(kh, v[0, 0]), rtol=1e-13)
+    np.testing.assert_allclose(o[0, 0], 0.3 * beta[0, 0] * (kh @ qh) * v[0, 0], rtol=1e-12)
+
+
+def test_associative_recall_orthonormal_keys():
+    # beta = 1, g = 0, S0 = 0, keys orthonormal: every write stores v_i exactly
+    # under k_i.  With unit keys k_hat = c k, c^2 = 1/(1+eps); querying with
+    # q_t = k_t gives o_t = scale * c^2 * v_t and S_T^T k_i = c * v_i.
+    rng = np.random.default_rng(4)
+    K, V, T = 16, 7, 12
+    Qm, _ = np.linalg.qr(rng.standard_normal((K, K)))
+    keys = Qm[:T]                                  # T orthonormal rows
+    k = keys[:, None, :]
+    q = k.copy()
+    v = rng.standard_normal((T, 1, V))
+    g = np.zeros((T, 1, K)); beta = np.ones((T, 1))
+    o, S = oracle.recurrence(q, k, v, g, beta, scale=0.2)
+    c2 = 1.0 / (1.0 + EPS)
+    np.testing.assert_allclose(o[:, 0], 0.2 * c2 * v[:, 0], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(S[0, 0].T @ keys.T, np.sqrt(c2) * v[:, 0].T, rtol=1e-10, atol=1e-12)
+
+
+def test_two_tokens_hand_expanded_K3_V2():
+    # Brute force, T = 2, K = 3, V = 2, S0 = 0, written out by hand:
+    #   S1 = b1 k1 v1^T,   o1 = s b1 (k1.q1) v1
+    #   D  = diag(exp(g2)),  u2 = b2 (v2 - b1 (k1^T D k2) v1)
+    #   o2 = s [ b1 (k1^T D q2) v1 + (k2.q2) u2 ]      (hats on q, k)
+    q = np.array([[[0.3, -1.2, 0.8]], [[1.1, 0.4, -0.2]]])
+    k = np.array([[[-0.5, 0.9, 1.3]], [[0.7, 0.7, -0.6]]])
+    v = np.array([[[2.0, -1.0]], [[0.5, 3.0]]])
+    g = np.array([[[-0.1, -0.2, -0.3]], [[-0.4, -0.05, -1.5]]])
+    b = np.array([[0.6], [0.9]])
+    s = 0.45
+    o, S = oracle.recurrence(q, k, v, g, b, scale=s)
+    k1, k2 = _unit(k[0, 0]), _unit(k[1, 0])
+    q1, q2 = _unit(q[0, 0]), _unit(q[1, 0])
+    v1, v2 = v[0, 0], v[1, 0]
+    b1, b2 = b[0, 0], b[1, 0]
+    d = np.exp(g[1, 0])
+    o1 = s * b1 * (k1 @ q1) * v1
+    u2 = b2 * (v2 - b1 * np.sum(k1 * d * k2) * v1)
+    o2 = s * (b1 * np.sum(k1 * d * q2) * v1 + (k2 @ q2) * u2)
+    S2 = b1 * np.outer(d * k1, v1) + np.outer(k2, u2)
+    np.testing.assert_allclose(o[0, 0], o1, rtol=1e-13)
+    np.testing.assert_allclose(o[1, 0], o2, rtol=1e-13)
+    np.testing.assert_allclose(S[0, 0], S2, rtol=1e-13)
+
+
+# ---- invariants -------------------------------------------------------------
+
+def test_joint_linearity_in_values_and_initial_state():
+    rng = np.random.default_rng(5)
+    T, H, K, V = 29, 2, 8, 5
+    q, k, v1, g, b = _rand(rng, T, H, K, V)
+    v2 = rng.standard_normal((T, H, V))
+    s1 = rng.standard_normal((1, H, K, V)); s2 = rng.standard_normal((1, H, K, V))
+    a = -1.7
+    o1, f1 = oracle.recurrence(q, k, v1, g, b, initial_state=s1)
+    o2, f2 = oracle.recurrence(q, k, v2, g, b, initial_state=s2)
+    o3, f3 = oracle.recurrence(q, k, v1 + a * v2, g, b, initial_state=s1 + a * s2)
+    np.testing.assert_allclose(o3, o1 + a * o2, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(f3, f1 + a * f2, rtol=1e-10, atol=1e-12)
+
+
+def test_value_columns_and_key_channels_are_equivariant():
+    rng = np.random.default_rng(6)
+    T, H, K, V = 23, 1, 7, 6
+    q, k, v, g, b = _rand(rng, T, H, K, V)
+    s0 = rng.standard_normal((1, H, K, V))
+    o, S = oracle.recurrence(q, k, v, g, b, initial_state=s0)
+    pv = rng.permutation(V)
+    o2, S2 = oracle.recurrence(q, k, v[..., pv], g, b, initial_state=s0[..., pv])
+    np.testing.assert_allclose(o2, o[..., pv], rtol=1e-12)
+    np.testing.assert_allclose(S2, S[..., pv], rtol=1e-12)
+    pk = rng.permutation(K)
+    o3, S3 = oracle.recurrence(q[..., pk], k[..., pk], v, g[..., pk], b,
+                               initial_state=s0[:, :, pk, :])
+    np.testing.assert_allclose(o3, o, rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(S3, S[:, :, pk, :], rtol=1e-11, atol=1e-13)
+
+
+def test_heads_and_sequences_are_independent():
+    rng = np.random.default_rng(7)
+    lens = [5, 0, 17, 9]
+    T, H, K, V = sum(lens), 3, 6, 4
+    q, k, v, g, b = _rand(rng, T, H, K, V)
+    s0 = rng.standard_normal((len(lens), H, K, V))
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    o, S = oracle.recurrence(q, k, v, g, b, cu_seqlens=cu, initial_state=s0)
+    for n in range(len(lens)):
+        sl = slice(cu[n], cu[n + 1])
+        for h in range(H):
+            oh, Sh = oracle.recurrence(q[sl, h:h + 1], k[sl, h:h + 1], v[sl, h:h + 1],
+                                       g[sl, h:h + 1], b[sl, h:h + 1],
+                                       initial_state=s0[n:n + 1, h:h + 1])
+            np.testing.assert_allclose(o[sl, h:h + 1], oh, rtol=1e-13)
+            np.testing.assert_allclose(S[n, h], Sh[0, 0], rtol=1e-13)
+    # an empty sequence hands back its initial state unchanged
+    np.testing.assert_array_equal(S[1], s0[1])
+
+
+@pytest.mark.parametrize("split", [1, 63, 64, 65, 100])
+def test_split_and_handoff(split):
+    rng = np.random.default_rng(8)
+    T, H, K, V = 130, 2, 8, 8
+    q, k, v, g, b = _rand(rng, T, H, K, V)
+    s0 = rng.standard_normal((1, H, K, V))
+    o, S = oracle.recurrence(q, k, v, g, b, initial_state=s0)
+    a, c = slice(0, split), slice(split, T)
+    oa, Sa = oracle.recurrence(q[a], k[a], v[a], g[a], b[a], initial_state=s0)
+    ob, Sb = oracle.recurrence(q[c], k[c], v[c], g[c], b[c], initial_state=Sa)
+    np.testing.assert_allclose(np.concatenate([oa, ob]), o, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(Sb, S, rtol=1e-12, atol=1e-13)
+
+
+def test_contraction_without_inputs():
+    # v = 0, g <= 0, beta in [0, 1], |k_hat| < 1: each step is
+    # S <- (I - beta k k^T) D S, a product of contractions in Frobenius norm.
+    rng = np.random.default_rng(9)
+    T, K, V = 40, 8, 5
+    q, k, _, g, b = _rand(rng, T, 1, K, V, g_lo=-0.2, g_hi=0.0)
+    v = np.zeros((T, 1, V))
+    S = rng.standard_normal((1, 1, K, V))
+    prev = np.linalg.norm(S)
+    for t in range(T):
+        _, S = oracle.recurrence(q[t:t + 1], k[t:t + 1], v[t:t + 1], g[t:t + 1], b[t:t + 1],
+                                 initial_state=S)
+        cur = np.linalg.norm(S)
+        assert cur <= prev * (1 + 1e-14)
+        prev = cur
+
+
+def test_query_and_key_magnitude_only_enter_through_eps():
+    rng = np.random.default_rng(10)
+    q, k, v, g, b = _rand(rng, 20, 2, 16, 4)
+    o, S = oracle.recurrence(q, k, v, g, b)
+    o2, S2 = oracle.recurrence(3.0 * q, 0.5 * k, v, g, b)
+    # |q|^2, |k|^2 ~ 16 >> eps: relative change O(eps / |x|^2)
+    np.testing.assert_allclose(o2, o, rtol=2e-6, atol=1e-7)
+    np.testing.assert_allclose(S2, S, rtol=2e-6, atol=1e-7)
+
+
+# ---- the chunked form against the recurrence --------------------------------
+
+@pytest.mark.parametrize("chunk", [1, 4, 16, 64])
+def test_chunked_form_equals_recurrence(chunk):
+    rng = np.random.default_rng(11 + chunk)
+    T, H, K, V = 77, 2, 8, 6          # ragged tail for every chunk size
+    q, k, v, g, b = _rand(rng, T, H, K, V, g_lo=-0.5, g_hi=-0.001)
+    s0 = rng.standard_normal((H, K, V))
+    o, S = oracle.recurrence(q, k, v, g, b, initial_state=s0[None], scale=0.35)
+    oc, Sc = oracle.chunked_form(q, k, v, g, b, initial_state=s0, chunk=chunk, scale=0.35)
+    np.testing.assert_allclose(oc, o, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(Sc, S[0], rtol=1e-11, atol=1e-12)
+
+
+def test_chunked_form_strong_decay():
+    # per-token decays down to -3 (the long-prefill mix): exact pairwise exps in fp64
+    rng = np.random.default_rng(12)
+    T, H, K, V = 70, 1, 8, 4
+    q, k, v, g, b = _rand(rng, T, H, K, V)
+    strong = rng.uniform(-3, -1, g.shape)
+    g = np.where(rng.uniform(size=g.shape) < 0.3, strong, g)
+    o, S = oracle.recurrence(q, k, v, g, b)
+    oc, Sc = oracle.chunked_form(q, k, v, g, b, chunk=64)
+    np.testing.assert_allclose(oc, o, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(Sc, S[0], rtol=1e-10, atol=1e-12)
+
+
+# ---- the decode step --------------------------------------------------------
+
+def test_step_advances_only_the_picked_slots():
+    rng = np.random.default_rng(13)
+    N, H, K, V, slots = 3, 2, 6, 5, 7
+    q, k, v, g, b = _rand(rng, N, H, K, V)
+    pool = rng.standard_normal((slots, H, K, V))
+    idx = np.array([5, 0, 3])
+    o, new = oracle.step(q, k, v, g, b, pool, state_indices=idx)
+    untouched = [s for s in range(slots) if s not in idx]
+    np.testing.assert_array_equal(new[untouched], pool[untouched])
+    for n in range(N):
+        on, Sn = oracle.recurrence(q[n:n + 1], k[n:n + 1], v[n:n + 1], g[n:n + 1], b[n:n + 1],
+                                   initial_state=pool[idx[n]][None])
+        np.testing.assert_allclose(o[n], on[0], rtol=1e-13)
+        np.testing.assert_allclose(new[idx[n]], Sn[0], rtol=1e-13)
+
+
+def test_steps_compose_to_the_sequence_recurrence():
+    rng = np.random.default_rng(14)
+    T, H, K, V = 9, 2, 5, 4
+    q, k, v, g, b = _rand(rng, T, H, K, V)
+    pool = rng.standard_normal((2, H, K, V))
+    o_seq, S_seq = oracle.recurrence(q, k, v, g, b, initial_state=pool[1][None])
+    p = pool
+    for t in range(T):
+        o_t, p = oracle.step(q[t:t + 1], k[t:t + 1], v[t:t + 1], g[t:t + 1], b[t:t + 1], p,
+                             state_indices=[1])
+        np.testing.assert_allclose(o_t[0], o_seq[t], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(p[1], S_seq[0], rtol=1e-12, atol=1e-13)
+    np.testing.assert_array_equal(p[0], pool[0])
