@@ -1,0 +1,448 @@
+#!/usr/bin/env python3
+"""Benchmark of the KDA core (libkda) on GB300.
+
+A step is one chunked KDA prefill of the 4k workload (B=1, T=4096, H=32,
+K=V=128, bf16 q/k/v, fp32 g/beta, zero initial state, output + final fp32
+state) through the C ABI: kda_chunk_intra then kda_chunk_scan on one stream.
+Inputs are resident in HBM when the timed region starts; they (plus the
+workspace) exceed the 129 MB L2, so no flush is needed between steps.  The
+same line also carries the decode half of the metric: the 256 x 32 decode
+step (512 MiB fp32 state pool, 64 consecutive steps), in microseconds.
+
+Prints ONE JSON line on rank 0.  ``--impl reference`` times the fp64 CPU
+oracle instead (a bounded sample of the same workload on the host cores).
+
+Multi-GPU (torchrun, one rank per GPU): each rank runs its own copy of the
+workload (independent sequences; the KDA core needs no exchange), so the
+scaling is weak and there is no collective on the data path; only the
+timing barrier and a max-reduction of the times.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import kda_inputs  # noqa: E402
+
+METRIC = "KDA prefill tokens/s (T=4096,H=32,K=V=128) & decode step us; % roofline"
+T_4K, H, K, V = 4096, 32, 128, 128
+DEC_N, DEC_STEPS = 256, 64
+L2_BYTES = 129 * 1024 * 1024
+KERNELS_PER_PREFILL = 3   # chunk index, intra-chunk, state scan
+KERNELS_PER_DECODE = 1
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--precise", action="store_true", help="fp32 CUDA-core chunk path")
+    return p.parse_args()
+
+
+# ---- distributed plumbing --------------------------------------------------
+
+def dist_setup(backend):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend=backend)
+    return rank, ws
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws, device=None):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---- peaks, clocks, profiles ----------------------------------------------
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+class Clocks:
+    """nvidia-smi sampled every 50 ms while the benchmark runs; the samples
+    inside a wall-clock window are summarised afterwards."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.t0 = time.time()
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                       "-i", str(gpu_index), "-lms", "50"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.p = None
+
+    def stop(self):
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = []
+        for line in self.f.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append(dict(t=ts + frac, sm=float(parts[2]), smax=float(parts[3]),
+                                 power=float(parts[4]) if parts[4] not in ("[N/A]", "N/A") else None,
+                                 reasons=parts[5], hw=parts[6], hwt=parts[7], swt=parts[8],
+                                 swp=parts[9]))
+            except (ValueError, IndexError):
+                continue
+        self.rows = rows
+        os.unlink(self.f.name)
+        return rows
+
+    def summary(self, t_start, t_end):
+        rows = getattr(self, "rows", [])
+        win = [r for r in rows if t_start - 0.06 <= r["t"] <= t_end + 0.06]
+        if not win and rows:  # the window was shorter than one sample period
+            mid = 0.5 * (t_start + t_end)
+            win = sorted(rows, key=lambda r: abs(r["t"] - mid))[:2]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        reasons = set()
+        for r in win:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in win),
+                "sm_max_mhz": max(r["smax"] for r in win), "reasons": sorted(reasons),
+                "samples": len(win),
+                "power_w_max": max((r["power"] for r in win if r["power"] is not None), default=None)}
+
+
+def traffic_from_profiles(kernel_key):
+    """Per-launch DRAM bytes of a kernel from the committed ncu summary, or
+    None if there is none or the kernel's source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path)).get(kernel_key)
+    except (ValueError, OSError):
+        return None
+    if not d:
+        return None
+    import hashlib
+    src = os.path.join(ROOT, d["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != d["source_sha"]:
+        return None
+    return float(d["bytes_per_launch"])
+
+
+# ---- algorithmic bytes -----------------------------------------------------
+
+def prefill_bytes(T, H, elem=2):
+    qkv = 3 * T * H * K * elem
+    g = T * H * K * 4
+    beta = T * H * 4
+    o = T * H * V * elem
+    state = H * V * K * 4          # final state written (zero initial state not read)
+    return dict(intra=qkv + g + beta, scan=o + state, step=qkv + g + beta + o + state)
+
+
+def decode_bytes(N, H, elem=2):
+    state = 2 * N * H * V * K * 4  # read + write
+    io = N * H * (2 * K * elem + V * elem + K * 4 + 4 + V * elem)
+    return state + io
+
+
+# ---- our arm ---------------------------------------------------------------
+
+def run_ours(args, rank, ws):
+    import kimi_delta_attention_07_gb300 as kda
+    kda.load()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    pk = peaks()
+
+    x = kda_inputs.prefill_4k()
+    d = {n: x[n].to(dev) for n in ("q", "k", "v", "g", "beta")}
+    flags = kda.KDA_CHUNK_PRECISE if args.precise else 0
+    ws_bytes = kda.kda_chunk_workspace_bytes(T_4K, 1, H, K, V, kda.KDA_BF16, flags)
+    work = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    o = torch.empty((T_4K, H, V), dtype=torch.bfloat16, device=dev)
+    sf = torch.empty((1, H, V, K), dtype=torch.float32, device=dev)
+    kw = dict(o=o, final_state=sf, workspace=work, precise=args.precise, stream=stream)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], phase="intra", **kw)
+        if ev is not None:
+            ev[1].record(stream)
+        kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], phase="scan", **kw)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+
+    clocks = Clocks(dev.index) if rank == 0 else None
+    time.sleep(0.15)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(ws)
+    total_ms = start.elapsed_time(end)
+    intra_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    scan_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    total_ms = max_over_ranks(total_ms, ws, dev)
+    ms_per_step = total_ms / args.steps
+    tokens = T_4K * args.steps * ws
+    value = tokens / (total_ms / 1e3)
+
+    nb = prefill_bytes(T_4K, H)
+    kernels = {
+        "kda_chunk_intra": dict(ms=intra_ms, algorithmic_bytes=nb["intra"],
+                                gbs=nb["intra"] / (intra_ms * 1e-3) / 1e9),
+        "kda_chunk_scan": dict(ms=scan_ms, algorithmic_bytes=nb["scan"],
+                               gbs=nb["scan"] / (scan_ms * 1e-3) / 1e9),
+    }
+    tot = intra_ms + scan_ms
+    for v_ in kernels.values():
+        v_["share"] = v_["ms"] / tot
+    dom = max(kernels, key=lambda n: kernels[n]["ms"])
+    dk = kernels[dom]
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": round(dk["gbs"], 1),
+                "peak": pk["hbm"], "unit": "GB/s", "frac": round(dk["gbs"] / pk["hbm"], 4),
+                "traffic": traffic_from_profiles(dom + ("_precise" if args.precise else "")),
+                "peak_source": pk["source"] + " (burst HBM copy)"}
+    step_gbs = nb["step"] / (ms_per_step * 1e-3) / 1e9
+    step_roofline = {"bound": "hbm", "algorithmic_bytes": nb["step"], "achieved": round(step_gbs, 1),
+                     "peak": pk["hbm"], "unit": "GB/s", "frac": round(step_gbs / pk["hbm"], 4)}
+
+    if rank == 0:
+        clocks.stop()
+        clk = clocks.summary(t_wall0, t_wall1)
+    else:
+        clk = None
+
+    e2e = run_e2e(args, kda, x, dev, stream, work, flags, ws)
+    dec = None if args.no_decode else run_decode(args, kda, dev, stream, pk, ws)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(x, sample_heads=H)
+
+    launches = KERNELS_PER_PREFILL * args.steps
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp32" if args.precise else "bf16",
+            "data": "synthetic (seeded, torch.Generator on CPU)",
+            "config": {"workload": "prefill_4k", "B": 1, "T": T_4K, "H": H, "K": K, "V": V,
+                       "chunk": 64, "io_dtype": "bf16", "g_beta_state": "fp32",
+                       "global_batch_tokens": T_4K * ws, "parallelism": f"replicas{ws}",
+                       "l2": "inputs + workspace > 129 MB L2, no flush",
+                       "path": "fp32 CUDA-core (precise)" if args.precise else "default"},
+            "roofline": roofline, "step_roofline": step_roofline, "kernels": kernels,
+            "e2e": e2e, "gpu_launches": launches, "clocks": clk,
+            "decode": dec, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, kda, x, dev, stream, work, flags, ws):
+    """Same metric through the public call with HOST buffers: pinned host
+    inputs copied in, the chunked forward, output and final state copied out,
+    all inside the timed region."""
+    names = ("q", "k", "v", "g", "beta")
+    host = {n: x[n].pin_memory() for n in names}
+    d = {n: torch.empty_like(host[n], device=dev) for n in names}
+    o_h = torch.empty((T_4K, H, V), dtype=torch.bfloat16).pin_memory()
+    s_h = torch.empty((1, H, V, K), dtype=torch.float32).pin_memory()
+    o = torch.empty((T_4K, H, V), dtype=torch.bfloat16, device=dev)
+    sf = torch.empty((1, H, V, K), dtype=torch.float32, device=dev)
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = o_h.numel() * 2 + s_h.numel() * 4
+
+    def one():
+        for n in names:
+            d[n].copy_(host[n], non_blocking=True)
+        kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], o=o, final_state=sf,
+                          workspace=work, precise=bool(flags), stream=stream)
+        o_h.copy_(o, non_blocking=True)
+        s_h.copy_(sf, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    steps = max(1, min(args.steps, 20))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b), ws, dev)
+    return {"value": round(T_4K * steps * ws / (ms / 1e3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def run_decode(args, kda, dev, stream, pk, ws):
+    """256 sequences x 32 heads, 512 MiB fp32 state pool, 64 consecutive decode
+    steps with fresh bf16 tokens each step (all inputs pre-staged on the device)."""
+    pool = kda_inputs.decode_pool(DEC_N, H=H, seed=3).to(dev)
+    toks = [kda_inputs.decode_tokens(DEC_N, H=H, seed=3, step=t) for t in range(DEC_STEPS)]
+    toks = [{n: t[n].to(dev) for n in ("q", "k", "v", "g", "beta")} for t in toks]
+    o = torch.empty((DEC_N, H, V), dtype=torch.bfloat16, device=dev)
+    for t in range(3):  # warm-up on a scratch copy so the timed 64 steps start from the seed pool
+        scratch = pool.clone()
+        kda.kda_recurrent_step(*(toks[t][n] for n in ("q", "k", "v", "g", "beta")), scratch, o=o,
+                               stream=stream)
+        del scratch
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(DEC_STEPS)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    for t in range(DEC_STEPS):
+        evs[t][0].record(stream)
+        kda.kda_recurrent_step(*(toks[t][n] for n in ("q", "k", "v", "g", "beta")), pool, o=o,
+                               stream=stream)
+        evs[t][1].record(stream)
+    torch.cuda.synchronize()
+    us = [a.elapsed_time(b) * 1e3 for a, b in evs]
+    med = max_over_ranks(statistics.median(us), ws, dev)
+    nbytes = decode_bytes(DEC_N, H)
+    gbs = nbytes / (med * 1e-6) / 1e9
+    return {"workload": "decode_256", "us_per_step": round(med, 2),
+            "us_min": round(min(us), 2), "tokens_per_s": round(DEC_N * ws / (med * 1e-6), 1),
+            "steps": DEC_STEPS, "launches": DEC_STEPS * KERNELS_PER_DECODE,
+            "roofline": {"kernel": "recurrent_step_kernel", "bound": "hbm",
+                         "algorithmic_bytes": nbytes, "achieved": round(gbs, 1),
+                         "peak": pk["hbm"], "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
+                         "traffic": traffic_from_profiles("recurrent_step_kernel")}}
+
+
+# ---- the oracle as the CPU baseline / reference arm ------------------------
+
+def cpu_baseline(x, sample_heads):
+    import oracle
+    heads = list(range(sample_heads))
+    sub = {n: x[n][:, heads].contiguous() for n in ("q", "k", "v", "g", "beta")}
+    cores = oracle.max_threads()
+    t = time.perf_counter()
+    oracle.recurrence(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], n_threads=cores)
+    dt = time.perf_counter() - t
+    tokens = x["q"].shape[0] * len(heads) / H  # in units of full (all-head) tokens
+    return {"value": round(tokens / dt, 1), "unit": "tokens/s", "cores": min(cores, len(heads)),
+            "kind": "oracle", "seconds": round(dt, 3),
+            "sample": f"prefill_4k, {len(heads)} of {H} heads x {x['q'].shape[0]} tokens, fp64 "
+                      f"token recurrence, OpenMP over heads"}
+
+
+def run_reference(args, rank, ws):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    x = kda_inputs.prefill_4k()
+    cores = oracle.max_threads()
+    heads = list(range(min(H, max(cores, 1))))
+    sub = {n: x[n][:, heads].contiguous() for n in ("q", "k", "v", "g", "beta")}
+
+    def step():
+        oracle.recurrence(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], n_threads=cores)
+
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t
+    tokens = T_4K * len(heads) / H * args.steps
+    value = tokens / dt
+    sample = (f"prefill_4k, {len(heads)} of {H} heads x {T_4K} tokens per step, fp64 token "
+              f"recurrence (the oracle), OpenMP over heads")
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": "prefill_4k", "B": 1, "T": T_4K, "H": H, "K": K, "V": V},
+            "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s",
+                             "cores": min(cores, len(heads)), "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        rank, ws = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+        run_reference(args, rank, ws)
+        return
+    rank, ws = dist_setup("nccl")
+    try:
+        run_ours(args, rank, ws)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

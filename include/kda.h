@@ -1,0 +1,193 @@
+/*
+ * kda.h -- C ABI of libkda, the GB300 (sm_103a) Kimi Delta Attention core.
+ *
+ * Kimi Delta Attention (KDA) is a gated DeltaNet whose decay is per key
+ * channel (nnterp "kimi_linear" page, paragraph defining Kimi Delta
+ * Attention).  Per (sequence, head), with q and k L2-normalised inside the
+ * library (eps 1e-6 added to the sum of squares, inside the root; Ascend
+ * model file, _l2_normalize) and an fp32 K x V state S:
+ *
+ *     S   <- diag(exp(g_t)) S                      decay each key channel
+ *     S   <- S + beta_t k_t (v_t - S^T k_t)^T      delta-rule write
+ *     o_t  = scale * S^T q_t                       read-out, updated state
+ *
+ * Two forms are exported, as on that page: a chunked form for prompts
+ * (kda_chunk_fwd, chunk 64; Ascend model file, _torch_chunk_kda and
+ * _prefill_flash_kda / _prefill_torch_kda for the per-request loop) and a
+ * token step for decode on a pooled state (kda_recurrent_step; Ascend model
+ * file, _decode_fused_kda / _decode_gdr).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Pointers are DEVICE pointers unless stated.  All tensors are dense,
+ * row-major (C order), without padding.  Nothing is allocated: the caller
+ * owns every buffer, including the chunk workspace.  Nothing is kept
+ * between calls.  Work is enqueued on `stream` (a cudaStream_t passed as
+ * void*; NULL = the legacy default stream) and the call returns without
+ * synchronising; the host never reads device memory.
+ *
+ * Layouts (T = tokens, H = heads, K = key dim, V = value dim, N = sequences):
+ *   q, k, g : [T, H, K]     v, o : [T, H, V]     beta : [T, H]
+ *   states  : [N, H, V, K]  fp32, key dim contiguous.  This is the transpose
+ *             of the mathematical K x V state, the orientation the model
+ *             file's recurrent-state cache uses.
+ * Element types: q, k, v and o are all `dtype` (kda_dtype); g, beta and the
+ * states are always fp32.  g is the log-decay (<= 0 for a contraction; any
+ * finite value is accepted), beta is the already-activated write strength.
+ * The supported head dims are K = V = 128.
+ *
+ * Errors: arguments are validated before anything is enqueued; a failing
+ * call returns a kda_status other than KDA_OK and enqueues nothing.  A
+ * failed kernel launch returns KDA_ERR_CUDA (the CUDA error is cleared).
+ * Errors that only the device can see (bad cu_seqlens, a slot index out of
+ * range) never cause an out-of-bounds access; they are reported as stated
+ * per entry point.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad dtype, ... */
+    KDA_ERR_UNSUPPORTED = 2, /* valid request outside what is built (K, V != 128) */
+    KDA_ERR_WORKSPACE = 3,   /* workspace NULL, too small or misaligned */
+    KDA_ERR_CUDA = 4         /* a CUDA runtime call or kernel launch failed */
+} kda_status;
+
+typedef enum {
+    KDA_F32 = 0,  /* q, k, v, o in fp32 */
+    KDA_BF16 = 1  /* q, k, v, o in bf16 */
+} kda_dtype;
+
+/* kda_chunk_fwd flags */
+#define KDA_CHUNK_PRECISE 1 /* fp32 CUDA-core chunk path also for bf16 inputs */
+
+/* Chunk length of the chunked form (Ascend model file, _KDA_CHUNK_SIZE). */
+#define KDA_CHUNK 64
+
+/* Human-readable name of a kda_status value (static string, never NULL). */
+const char *kda_status_string(int status);
+
+/* ABI version of this library: 100 * major + minor. */
+int kda_version(void);
+
+/*
+ * Bytes of device workspace kda_chunk_fwd needs for these sizes (0 on
+ * invalid sizes).  The workspace holds the sequence/chunk index and the
+ * per-chunk intra-chunk products handed from the intra-chunk kernel to the
+ * state-scan kernel.  It must be 256-byte aligned.
+ */
+size_t kda_chunk_workspace_bytes(int64_t total_tokens, int n_seqs, int H, int K, int V,
+                                 int dtype, int flags);
+
+/*
+ * Chunked KDA forward over N packed sequences (prefill).
+ *
+ *   q, k        [T, H, K] dtype     v [T, H, V] dtype     g [T, H, K] fp32
+ *   beta        [T, H] fp32
+ *   o           [T, H, V] dtype     (output, written for every real token)
+ *   cu_seqlens  device int32 [N+1], non-decreasing, cu_seqlens[0] = 0,
+ *               cu_seqlens[N] = T; sequence n owns tokens [cu[n], cu[n+1]).
+ *               NULL = N sequences of equal length T / N (N must divide T),
+ *               i.e. a dense [B, T/B, H, *] batch.
+ *   state_indices  NULL: initial_state and final_state are [N, H, V, K].
+ *               Otherwise device int32 [N], distinct values in [0, n_slots):
+ *               initial_state / final_state are pools [n_slots, H, V, K] and
+ *               sequence n reads its initial state from, and writes its
+ *               final state to, slot state_indices[n] (the hand-off of a
+ *               prefill's final state into the decode state pool; model
+ *               file, update_mamba_cache).
+ *   initial_state  NULL = zero initial states.
+ *   final_state    NULL = final states are not written.  May alias
+ *               initial_state (each slot is read before it is written).
+ *   scale       multiplies the normalised query (the model uses 1/sqrt(K)).
+ *   dtype       kda_dtype of q, k, v, o.
+ *   flags       0 or KDA_CHUNK_PRECISE.  Without the flag, bf16 inputs take
+ *               the tensor-core path (bf16 operands, fp32 accumulation,
+ *               fp32 state); fp32 inputs always take the fp32 path.
+ *   workspace   device, 256-byte aligned, kda_chunk_workspace_bytes(...)
+ *               bytes; its contents are scratch and may be anything.
+ *
+ * A zero-length sequence hands back its initial state (or zeros) as its
+ * final state.  Device-side argument errors (cu_seqlens decreasing, out of
+ * [0, T], or a slot index out of range) skip the offending sequence
+ * (nothing of it is read or written) and set a flag that
+ * kda_workspace_status() reports.
+ */
+int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
+                  const float *beta, const float *initial_state, float *final_state,
+                  const int32_t *state_indices, int64_t n_slots, void *o,
+                  const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens, int H, int K,
+                  int V, float scale, int dtype, int flags, void *workspace,
+                  size_t workspace_bytes, void *stream);
+
+/*
+ * The two phases of kda_chunk_fwd, for callers that schedule or time them
+ * separately.  kda_chunk_fwd(args) == kda_chunk_intra(args) followed, on the
+ * same stream and with the same workspace, by kda_chunk_scan(args).
+ *
+ * kda_chunk_intra: builds the sequence/chunk index from cu_seqlens (and
+ *   checks state_indices), then computes, for every (chunk, head), the
+ *   intra-chunk products -- L2 norms, cumulative log-decay, the UT transform
+ *   (I + L)^-1 diag(beta) by forward substitution, the WY products W and U,
+ *   the causal scores -- into the workspace.  Reads q, k, v, g, beta.
+ * kda_chunk_scan: the sequential inter-chunk state pass; reads the
+ *   workspace and the initial states, writes o and the final states.
+ * Both take exactly the arguments of kda_chunk_fwd and validate them the
+ * same way; q, k, v, g, beta are not read by the scan and o, states are not
+ * touched by the intra phase.
+ */
+int kda_chunk_intra(const void *q, const void *k, const void *v, const float *g,
+                    const float *beta, const float *initial_state, float *final_state,
+                    const int32_t *state_indices, int64_t n_slots, void *o,
+                    const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens, int H, int K,
+                    int V, float scale, int dtype, int flags, void *workspace,
+                    size_t workspace_bytes, void *stream);
+int kda_chunk_scan(const void *q, const void *k, const void *v, const float *g,
+                   const float *beta, const float *initial_state, float *final_state,
+                   const int32_t *state_indices, int64_t n_slots, void *o,
+                   const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens, int H, int K,
+                   int V, float scale, int dtype, int flags, void *workspace,
+                   size_t workspace_bytes, void *stream);
+
+/*
+ * Device-side error flags of the last kda_chunk_fwd that used this
+ * workspace: 0 = none, bit 0 = bad cu_seqlens, bit 1 = slot index out of
+ * range.  Synchronises `stream` and copies 4 bytes to the host.
+ * Returns KDA_OK or KDA_ERR_CUDA / KDA_ERR_INVALID_ARG.
+ */
+int kda_workspace_status(const void *workspace, int *flags_out, void *stream);
+
+/*
+ * One decode token for each of N sequences, on a pooled state, in place
+ * (model file, _decode_gdr / _decode_fused_kda with one token per sequence).
+ *
+ *   q, k, g     [N, H, K] (q, k dtype; g fp32)   v [N, H, V] dtype
+ *   beta        [N, H] fp32
+ *   state_pool  [n_slots, H, V, K] fp32, read and updated in place
+ *   state_indices  device int32 [N], distinct slots; NULL = slot n for
+ *               sequence n (then n_slots >= N).  A slot outside
+ *               [0, n_slots) leaves the pool untouched and writes NaN to
+ *               that sequence's o rows.
+ *   o           [N, H, V] dtype
+ *
+ * The state is streamed once from HBM and written back once; N = 0 is a
+ * no-op.
+ */
+int kda_recurrent_step(const void *q, const void *k, const void *v, const float *g,
+                       const float *beta, float *state_pool, const int32_t *state_indices,
+                       int64_t n_slots, void *o, int N, int H, int K, int V, float scale,
+                       int dtype, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

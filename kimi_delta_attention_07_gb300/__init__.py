@@ -1,0 +1,213 @@
+"""Python binding of libkda, the GB300 (sm_103a) Kimi Delta Attention core.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libkda.so`` behind the C ABI declared in ``include/kda.h``.
+PyTorch provides device memory and the stream.  There is no fallback: if
+the library is missing, every call raises.
+
+Entry points (same names as the C ABI):
+  kda_chunk_fwd        chunked prefill over packed (varlen) sequences
+  kda_recurrent_step   one decode token per sequence on a pooled state
+  kda_chunk_workspace_bytes, kda_workspace_status, kda_status_string
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA = range(5)
+KDA_F32, KDA_BF16 = 0, 1
+KDA_CHUNK_PRECISE = 1
+CHUNK = 64
+
+EXPORTS = ("kda_status_string", "kda_version", "kda_chunk_workspace_bytes", "kda_chunk_fwd",
+           "kda_chunk_intra", "kda_chunk_scan", "kda_workspace_status", "kda_recurrent_step")
+
+_lib = None
+_lock = threading.Lock()
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {kda_status_string(status)}")
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Load libkda (built by ``__graft_entry__.build()``); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or _build.LIB
+        if not os.path.exists(path):
+            raise ImportError(f"libkda is not built ({path} missing); run __graft_entry__.build()")
+        L = ctypes.CDLL(path)
+        vp, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                  ctypes.c_float, ctypes.c_size_t)
+        L.kda_status_string.argtypes = [i32]
+        L.kda_status_string.restype = ctypes.c_char_p
+        L.kda_version.restype = i32
+        L.kda_chunk_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, i32, i32]
+        L.kda_chunk_workspace_bytes.restype = sz
+        for name in ("kda_chunk_fwd", "kda_chunk_intra", "kda_chunk_scan"):
+            fn = getattr(L, name)
+            fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, vp, vp, i32, i64, i32, i32, i32,
+                           f32, i32, i32, vp, sz, vp]
+            fn.restype = i32
+        L.kda_workspace_status.argtypes = [vp, ctypes.POINTER(i32), vp]
+        L.kda_workspace_status.restype = i32
+        L.kda_recurrent_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, vp, i32, i32, i32, i32,
+                                         f32, i32, vp]
+        L.kda_recurrent_step.restype = i32
+        _lib = L
+        return L
+
+
+def kda_status_string(status: int) -> str:
+    return load().kda_status_string(int(status)).decode()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_F32
+    raise TypeError(f"q/k/v must be bf16 or fp32, got {t.dtype}")
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(t, name, dtype=None, shape=None, device=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} shape {tuple(t.shape)} != {tuple(shape)}")
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def kda_chunk_workspace_bytes(total_tokens: int, n_seqs: int, H: int, K: int = 128,
+                              V: int = 128, dtype: int = KDA_BF16, flags: int = 0) -> int:
+    return int(load().kda_chunk_workspace_bytes(total_tokens, n_seqs, H, K, V, dtype, flags))
+
+
+def kda_chunk_fwd(q, k, v, g, beta, *, cu_seqlens=None, n_seqs=None, initial_state=None,
+                  final_state=None, state_indices=None, n_slots=None, scale=None,
+                  precise=False, output_final_state=True, o=None, workspace=None, stream=None,
+                  phase="fwd"):
+    """Chunked KDA forward.
+
+    q, k, g: [T, H, K]; v: [T, H, V]; beta: [T, H] (all CUDA, contiguous).
+    cu_seqlens: int32 [N+1] or None (then n_seqs equal-length sequences,
+    default 1).  Without state_indices, initial_state / final_state are
+    [N, H, V, K]; with state_indices (int32 [N]) they are slot pools
+    [slots, H, V, K] and final_state may be the same tensor as
+    initial_state (in-place hand-off).  Returns (o, final_state).
+    """
+    T, H, K = q.shape
+    V = v.shape[-1]
+    dt = _dtype_code(q)
+    if cu_seqlens is not None:
+        N = cu_seqlens.numel() - 1
+    else:
+        N = 1 if n_seqs is None else int(n_seqs)
+    for name, t, dtype_, shape in (("q", q, q.dtype, (T, H, K)), ("k", k, q.dtype, (T, H, K)),
+                                   ("v", v, q.dtype, (T, H, V)),
+                                   ("g", g, torch.float32, (T, H, K)),
+                                   ("beta", beta, torch.float32, (T, H)),
+                                   ("cu_seqlens", cu_seqlens, torch.int32, None),
+                                   ("state_indices", state_indices, torch.int32, (N,)),
+                                   ("initial_state", initial_state, torch.float32, None)):
+        _check(t, name, dtype_, shape)
+    if state_indices is None:
+        slots = 0
+        if initial_state is not None and tuple(initial_state.shape) != (N, H, V, K):
+            raise ValueError(f"initial_state must be [{N}, {H}, {V}, {K}]")
+        if final_state is None and output_final_state:
+            final_state = torch.empty((N, H, V, K), dtype=torch.float32, device=q.device)
+    else:
+        if final_state is None:
+            raise ValueError("with state_indices, final_state must be the destination pool")
+        slots = final_state.shape[0] if n_slots is None else int(n_slots)
+        if initial_state is not None and initial_state.shape[0] < slots:
+            raise ValueError("initial_state pool has fewer slots than final_state")
+    _check(final_state, "final_state", torch.float32)
+    if o is None:
+        o = torch.empty((T, H, V), dtype=q.dtype, device=q.device)
+    _check(o, "o", q.dtype, (T, H, V))
+    flags = KDA_CHUNK_PRECISE if precise else 0
+    need = kda_chunk_workspace_bytes(T, N, H, K, V, dt, flags)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace", torch.uint8)
+    if scale is None:
+        scale = K ** -0.5
+    name = {"fwd": "kda_chunk_fwd", "intra": "kda_chunk_intra", "scan": "kda_chunk_scan"}[phase]
+    st = getattr(load(), name)(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(initial_state),
+                               _p(final_state), _p(state_indices), slots, _p(o), _p(cu_seqlens),
+                               N, T, H, K, V, float(scale), dt, flags, _p(workspace),
+                               workspace.numel(), _stream(stream))
+    if st != KDA_OK:
+        raise KdaError(st, name)
+    return o, final_state
+
+
+def kda_workspace_status(workspace, stream=None) -> int:
+    out = ctypes.c_int(0)
+    st = load().kda_workspace_status(_p(workspace), ctypes.byref(out), _stream(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_workspace_status")
+    return int(out.value)
+
+
+def kda_recurrent_step(q, k, v, g, beta, state_pool, *, state_indices=None, scale=None, o=None,
+                       stream=None):
+    """One decode token per sequence, updating ``state_pool`` [slots, H, V, K] in place.
+
+    q, k, g: [N, H, K]; v: [N, H, V]; beta: [N, H]; state_indices int32 [N]
+    or None (slot n).  Returns o [N, H, V].
+    """
+    N, H, K = q.shape
+    V = v.shape[-1]
+    dt = _dtype_code(q)
+    for name, t, dtype_, shape in (("q", q, q.dtype, (N, H, K)), ("k", k, q.dtype, (N, H, K)),
+                                   ("v", v, q.dtype, (N, H, V)),
+                                   ("g", g, torch.float32, (N, H, K)),
+                                   ("beta", beta, torch.float32, (N, H)),
+                                   ("state_pool", state_pool, torch.float32, None),
+                                   ("state_indices", state_indices, torch.int32, (N,))):
+        _check(t, name, dtype_, shape)
+    if state_pool.dim() != 4 or tuple(state_pool.shape[1:]) != (H, V, K):
+        raise ValueError(f"state_pool must be [slots, {H}, {V}, {K}]")
+    if o is None:
+        o = torch.empty((N, H, V), dtype=q.dtype, device=q.device)
+    _check(o, "o", q.dtype, (N, H, V))
+    if scale is None:
+        scale = K ** -0.5
+    st = load().kda_recurrent_step(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(state_pool),
+                                   _p(state_indices), state_pool.shape[0], _p(o), N, H, K, V,
+                                   float(scale), dt, _stream(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_recurrent_step")
+    return o

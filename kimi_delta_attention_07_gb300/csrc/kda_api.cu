@@ -1,0 +1,164 @@
+// C ABI of libkda: argument validation and kernel sequencing.
+#include <string.h>
+
+#include "kda_internal.cuh"
+
+using namespace kda;
+
+namespace {
+
+inline bool valid_dtype(int dt) { return dt == KDA_F32 || dt == KDA_BF16; }
+
+inline size_t elem_bytes(int dt) { return dt == KDA_BF16 ? 2 : 4; }
+
+inline bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// The chunk path a call takes: the tensor-core path for bf16 inputs unless
+// the precise path is requested.
+inline bool use_tensor_cores(int dtype, int flags) {
+    (void)dtype;
+    (void)flags;
+    return false;
+}
+
+inline size_t record_bytes(int dtype, int flags) {
+    (void)dtype;
+    (void)flags;
+    return F32Rec::bytes;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kda_status_string(int status) {
+    switch (status) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: only K = V = 128 is built";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace missing, too small or misaligned";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA: a CUDA call or kernel launch failed";
+        default: return "KDA: unknown status";
+    }
+}
+
+int kda_version(void) { return 100; }
+
+size_t kda_chunk_workspace_bytes(int64_t total_tokens, int n_seqs, int H, int K, int V,
+                                 int dtype, int flags) {
+    if (total_tokens < 0 || n_seqs <= 0 || H <= 0 || K != kHeadDim || V != kHeadDim ||
+        !valid_dtype(dtype))
+        return 0;
+    return ws_layout(total_tokens, n_seqs, H, record_bytes(dtype, flags)).total;
+}
+
+}  // extern "C"
+
+namespace {
+
+enum Phase { kIntra = 1, kScan = 2, kBoth = 3 };
+
+int chunk_call(int phase, const void *q, const void *k, const void *v, const float *g,
+               const float *beta, const float *initial_state, float *final_state,
+               const int32_t *state_indices, int64_t n_slots, void *o, const int32_t *cu_seqlens,
+               int n_seqs, int64_t total_tokens, int H, int K, int V, float scale, int dtype,
+               int flags, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!valid_dtype(dtype) || n_seqs <= 0 || H <= 0 || K <= 0 || V <= 0 || total_tokens < 0 ||
+        total_tokens > INT32_MAX || (flags & ~KDA_CHUNK_PRECISE))
+        return KDA_ERR_INVALID_ARG;
+    if (K != kHeadDim || V != kHeadDim) return KDA_ERR_UNSUPPORTED;
+    if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens && total_tokens % n_seqs != 0) return KDA_ERR_INVALID_ARG;
+    if (state_indices && n_slots <= 0) return KDA_ERR_INVALID_ARG;
+    if (!state_indices && n_slots < 0) return KDA_ERR_INVALID_ARG;
+    // vector loads need 16-byte (fp32) / 8-byte (bf16) aligned rows
+    const size_t ea = 4 * elem_bytes(dtype);
+    if ((q && !aligned(q, ea)) || (k && !aligned(k, ea)) || (v && !aligned(v, ea)) ||
+        (o && !aligned(o, ea)) || (g && !aligned(g, 16)) || (beta && !aligned(beta, 4)) ||
+        (initial_state && !aligned(initial_state, 16)) || (final_state && !aligned(final_state, 16)))
+        return KDA_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256)) return KDA_ERR_WORKSPACE;
+    const size_t need = kda_chunk_workspace_bytes(total_tokens, n_seqs, H, K, V, dtype, flags);
+    if (workspace_bytes < need) return KDA_ERR_WORKSPACE;
+    if (!isfinite(scale)) return KDA_ERR_INVALID_ARG;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaGetLastError();  // clear a stale error so the checks below see only ours
+    cudaError_t e = cudaSuccess;
+    if (phase & kIntra) {
+        e = launch_chunk_index(cu_seqlens, n_seqs, total_tokens, state_indices, n_slots,
+                               workspace, s);
+        if (e == cudaSuccess)
+            e = launch_chunk_prep_f32(q, k, v, g, beta, dtype, n_seqs, total_tokens, H, scale,
+                                      workspace, s);
+    }
+    if (e == cudaSuccess && (phase & kScan))
+        e = launch_chunk_scan_f32(initial_state, final_state, state_indices, o, dtype, n_seqs,
+                                  total_tokens, H, workspace, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+#define KDA_CHUNK_ARGS                                                                        \
+    const void *q, const void *k, const void *v, const float *g, const float *beta,           \
+        const float *initial_state, float *final_state, const int32_t *state_indices,          \
+        int64_t n_slots, void *o, const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens, \
+        int H, int K, int V, float scale, int dtype, int flags, void *workspace,               \
+        size_t workspace_bytes, void *stream
+#define KDA_CHUNK_PASS                                                                       \
+    q, k, v, g, beta, initial_state, final_state, state_indices, n_slots, o, cu_seqlens,      \
+        n_seqs, total_tokens, H, K, V, scale, dtype, flags, workspace, workspace_bytes, stream
+
+int kda_chunk_fwd(KDA_CHUNK_ARGS) { return chunk_call(kBoth, KDA_CHUNK_PASS); }
+int kda_chunk_intra(KDA_CHUNK_ARGS) { return chunk_call(kIntra, KDA_CHUNK_PASS); }
+int kda_chunk_scan(KDA_CHUNK_ARGS) { return chunk_call(kScan, KDA_CHUNK_PASS); }
+
+int kda_workspace_status(const void *workspace, int *flags_out, void *stream) {
+    if (!workspace || !flags_out) return KDA_ERR_INVALID_ARG;
+    int32_t st = 0;
+    cudaError_t e = cudaMemcpyAsync(&st, workspace, sizeof(st), cudaMemcpyDeviceToHost,
+                                    (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    *flags_out = st;
+    return KDA_OK;
+}
+
+int kda_recurrent_step(const void *q, const void *k, const void *v, const float *g,
+                       const float *beta, float *state_pool, const int32_t *state_indices,
+                       int64_t n_slots, void *o, int N, int H, int K, int V, float scale,
+                       int dtype, void *stream) {
+    if (!valid_dtype(dtype) || N < 0 || H <= 0 || K <= 0 || V <= 0 || n_slots < 0)
+        return KDA_ERR_INVALID_ARG;
+    if (K != kHeadDim || V != kHeadDim) return KDA_ERR_UNSUPPORTED;
+    if (N == 0) return KDA_OK;
+    if (!q || !k || !v || !g || !beta || !state_pool || !o) return KDA_ERR_INVALID_ARG;
+    if (!state_indices && n_slots < N) return KDA_ERR_INVALID_ARG;
+    if ((int64_t)N * H > INT32_MAX) return KDA_ERR_INVALID_ARG;
+    const size_t ea = 4 * elem_bytes(dtype);
+    if (!aligned(q, ea) || !aligned(k, ea) || !aligned(v, ea) || !aligned(o, elem_bytes(dtype)) ||
+        !aligned(g, 16) || !aligned(beta, 4) || !aligned(state_pool, 16))
+        return KDA_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return KDA_ERR_INVALID_ARG;
+    cudaGetLastError();
+    const cudaError_t e = launch_recurrent_step(q, k, v, g, beta, state_pool, state_indices,
+                                                n_slots, o, N, H, scale, dtype,
+                                                (cudaStream_t)stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
+}  // extern "C"

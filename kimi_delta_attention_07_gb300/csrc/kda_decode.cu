@@ -1,0 +1,121 @@
+// Decode step of Kimi Delta Attention on a pooled fp32 state, in place.
+//
+// One token per sequence (Ascend model file, KimiDeltaAttention._decode_gdr
+// and _decode_fused_kda; nnterp "kimi_linear" page, the token-by-token form).
+// For each (sequence n, head h) and each state row v (the pool stores S^T,
+// [V][K], key dim contiguous):
+//
+//   s      = S^T[v, :] * exp(g)                 decayed row
+//   a      = s . k_hat,   b = s . q_hat          (q_hat carries the scale)
+//   u      = beta * (v_v - a)
+//   S^T[v] = s + u * k_hat                       written back
+//   o_v    = b + u * (k_hat . q_hat)            = (S_new^T q_hat)_v
+//
+// The state is streamed once in and once out (HBM bound): each warp owns
+// whole 512-byte rows, a lane holds 4 consecutive key channels (one 128-bit
+// load and one 128-bit store per lane per row), and the two dot products are
+// warp-shuffle reductions.  Rows of one head are split over CTAs when there
+// are too few (sequence, head) pairs to fill the GPU.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kDecodeThreads = 256;  // 8 warps
+constexpr int kRowsInFlight = 8;     // rows a warp loads before reducing
+
+template <typename T>
+__global__ void __launch_bounds__(kDecodeThreads)
+    recurrent_step_kernel(const T *__restrict__ q, const T *__restrict__ k,
+                          const T *__restrict__ v, const float *__restrict__ g,
+                          const float *__restrict__ beta, float *__restrict__ pool,
+                          const int32_t *__restrict__ state_indices, int64_t n_slots,
+                          T *__restrict__ o, int H, int rows_per_cta, float scale) {
+    const int pair = blockIdx.x;  // n * H + h
+    const int n = pair / H;
+    const int h = pair - n * H;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int row0 = blockIdx.y * rows_per_cta;
+
+    const int64_t slot = state_indices ? (int64_t)state_indices[n] : (int64_t)n;
+    const int64_t io_k = (int64_t)pair * kHeadDim;  // offset of q/k/g/v/o rows of (n, h)
+
+    if (slot < 0 || slot >= n_slots) {
+        // invalid slot: the pool is not touched and this head's output is NaN
+        for (int r = threadIdx.x; r < rows_per_cta; r += kDecodeThreads)
+            o[io_k + row0 + r] = from_f32<T>(__int_as_float(0x7fc00000));
+        return;
+    }
+
+    // L2 norms of q and k over the key dim (eps inside the root), scale on q.
+    const float4 q4 = load4(q + io_k + 4 * lane);
+    const float4 k4 = load4(k + io_k + 4 * lane);
+    const float4 g4 = load4(g + io_k + 4 * lane);
+    const float sq = warp_sum(q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w);
+    const float sk = warp_sum(k4.x * k4.x + k4.y * k4.y + k4.z * k4.z + k4.w * k4.w);
+    const float rq = scale / sqrtf(sq + 1e-6f);
+    const float rk = 1.0f / sqrtf(sk + 1e-6f);
+    const float4 qh = make_float4(q4.x * rq, q4.y * rq, q4.z * rq, q4.w * rq);
+    const float4 kh = make_float4(k4.x * rk, k4.y * rk, k4.z * rk, k4.w * rk);
+    const float4 dec = make_float4(expf(g4.x), expf(g4.y), expf(g4.z), expf(g4.w));
+    const float kq = warp_sum(kh.x * qh.x + kh.y * qh.y + kh.z * qh.z + kh.w * qh.w);
+    const float b = beta[pair];
+
+    float *S = pool + ((slot * H + h) * (int64_t)kHeadDim) * kHeadDim;  // [V][K] of (slot, h)
+    const int warps = kDecodeThreads / 32;
+
+    for (int base = row0 + warp; base < row0 + rows_per_cta; base += warps * kRowsInFlight) {
+        float4 s[kRowsInFlight];
+#pragma unroll
+        for (int j = 0; j < kRowsInFlight; ++j) {
+            const int r = base + j * warps;
+            if (r < row0 + rows_per_cta)
+                s[j] = *reinterpret_cast<const float4 *>(S + (int64_t)r * kHeadDim + 4 * lane);
+        }
+#pragma unroll
+        for (int j = 0; j < kRowsInFlight; ++j) {
+            const int r = base + j * warps;
+            if (r >= row0 + rows_per_cta) break;
+            float4 x = s[j];
+            x.x *= dec.x; x.y *= dec.y; x.z *= dec.z; x.w *= dec.w;
+            float a = x.x * kh.x + x.y * kh.y + x.z * kh.z + x.w * kh.w;
+            float c = x.x * qh.x + x.y * qh.y + x.z * qh.z + x.w * qh.w;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                a += __shfl_xor_sync(0xffffffffu, a, off);
+                c += __shfl_xor_sync(0xffffffffu, c, off);
+            }
+            const float u = b * (to_f32(v[io_k + r]) - a);
+            x.x += u * kh.x; x.y += u * kh.y; x.z += u * kh.z; x.w += u * kh.w;
+            *reinterpret_cast<float4 *>(S + (int64_t)r * kHeadDim + 4 * lane) = x;
+            if (lane == 0) o[io_k + r] = from_f32<T>(c + u * kq);
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_recurrent_step(const void *q, const void *k, const void *v, const float *g,
+                                  const float *beta, float *pool, const int32_t *state_indices,
+                                  int64_t n_slots, void *o, int N, int H, float scale, int dtype,
+                                  cudaStream_t stream) {
+    const int64_t pairs = (int64_t)N * H;
+    // Split a head's 128 rows over more CTAs when there are few heads in flight,
+    // so that at least ~4 CTAs per SM are resident.
+    int rows = kHeadDim;
+    while (rows > 16 && pairs * (kHeadDim / rows) < 152 * 8) rows >>= 1;
+    const dim3 grid((unsigned)pairs, kHeadDim / rows);
+    if (dtype == KDA_BF16) {
+        recurrent_step_kernel<__nv_bfloat16><<<grid, kDecodeThreads, 0, stream>>>(
+            (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, g,
+            beta, pool, state_indices, n_slots, (__nv_bfloat16 *)o, H, rows, scale);
+    } else {
+        recurrent_step_kernel<float><<<grid, kDecodeThreads, 0, stream>>>(
+            (const float *)q, (const float *)k, (const float *)v, g, beta, pool, state_indices,
+            n_slots, (float *)o, H, rows, scale);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -1,0 +1,135 @@
+// Internal helpers and the workspace layout shared by the libkda kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+constexpr int kChunk = KDA_CHUNK;  // 64 tokens per chunk
+constexpr int kHeadDim = 128;      // K = V = 128 is what is built
+
+// ---- element access -------------------------------------------------------
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// Four consecutive elements starting at p (p 8-byte aligned for bf16,
+// 16-byte aligned for fp32).
+__device__ __forceinline__ float4 load4(const float *p) {
+    return *reinterpret_cast<const float4 *>(p);
+}
+__device__ __forceinline__ float4 load4(const __nv_bfloat16 *p) {
+    const uint2 raw = *reinterpret_cast<const uint2 *>(p);
+    const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
+    const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
+    const float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// ---- workspace layout -----------------------------------------------------
+//
+//   [0, 256)      status word (int32, StatusBits) + padding
+//   [256, ...)    seq_start[N] int32 (-1 = sequence skipped), seq_len[N] int32,
+//                 chunk_off[N+1] int32 (exclusive prefix sum of chunks per seq)
+//   aligned(256)  per-(chunk, head) records, index chunk * H + head
+//
+// The record contents depend on the chunk path (fp32 CUDA-core path or bf16
+// tensor-core path); each path defines its record size.
+
+enum StatusBits : int { kBadSeqlens = 1, kBadSlot = 2 };
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline int64_t max_chunks(int64_t total_tokens, int n_seqs) {
+    // Sum over sequences of ceil(len / 64) <= floor(T / 64) + N.
+    return total_tokens / kChunk + n_seqs;
+}
+
+struct WsLayout {
+    size_t status_off, seq_start_off, seq_len_off, chunk_off_off, records_off, record_bytes,
+        total;
+};
+
+__host__ __device__ inline WsLayout ws_layout(int64_t total_tokens, int n_seqs, int H,
+                                              size_t record_bytes) {
+    WsLayout L;
+    const size_t arr = align_up(sizeof(int32_t) * (size_t)(n_seqs + 1), 16);
+    L.status_off = 0;
+    L.seq_start_off = 256;
+    L.seq_len_off = L.seq_start_off + arr;
+    L.chunk_off_off = L.seq_len_off + arr;
+    L.records_off = align_up(L.chunk_off_off + arr, 256);
+    L.record_bytes = record_bytes;
+    L.total = L.records_off + (size_t)max_chunks(total_tokens, n_seqs) * (size_t)H * record_bytes;
+    return L;
+}
+
+template <typename P>
+__host__ __device__ inline P *ws_at(void *ws, size_t off) {
+    return reinterpret_cast<P *>(reinterpret_cast<char *>(ws) + off);
+}
+
+// fp32 CUDA-core path: per (chunk, head) record, all fp32
+//   W [64][K], U [64][V], QG [64][K], KD [64][K], A [64][64], gC [K]
+struct F32Rec {
+    static constexpr size_t W = 0;
+    static constexpr size_t U = W + kChunk * kHeadDim;
+    static constexpr size_t QG = U + kChunk * kHeadDim;
+    static constexpr size_t KD = QG + kChunk * kHeadDim;
+    static constexpr size_t A = KD + kChunk * kHeadDim;
+    static constexpr size_t GC = A + kChunk * kChunk;
+    static constexpr size_t floats = GC + kHeadDim;
+    static constexpr size_t bytes = floats * sizeof(float);
+};
+
+// ---- launchers (return cudaGetLastError() of the launch) ------------------
+
+cudaError_t launch_chunk_index(const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens,
+                               const int32_t *state_indices, int64_t n_slots, void *workspace,
+                               cudaStream_t stream);
+
+cudaError_t launch_chunk_prep_f32(const void *q, const void *k, const void *v, const float *g,
+                                  const float *beta, int dtype, int n_seqs, int64_t total_tokens,
+                                  int H, float scale, void *workspace, cudaStream_t stream);
+
+cudaError_t launch_chunk_scan_f32(const float *initial_state, float *final_state,
+                                  const int32_t *state_indices, void *o, int dtype, int n_seqs,
+                                  int64_t total_tokens, int H, void *workspace,
+                                  cudaStream_t stream);
+
+// Block-wide helper used by the chunk kernels: find the sequence that owns
+// global chunk `c` (largest n with chunk_off[n] <= c; chunk_off non-decreasing).
+__device__ __forceinline__ int owner_of_chunk(const int32_t *chunk_off, int n_seqs, int c) {
+    int lo = 0, hi = n_seqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (chunk_off[mid] <= c) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+cudaError_t launch_recurrent_step(const void *q, const void *k, const void *v, const float *g,
+                                  const float *beta, float *pool, const int32_t *state_indices,
+                                  int64_t n_slots, void *o, int N, int H, float scale, int dtype,
+                                  cudaStream_t stream);
+
+}  // namespace kda

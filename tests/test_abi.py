@@ -1,0 +1,128 @@
+"""libkda C ABI on the host: the library loads, exports every function that
+include/kda.h declares, and rejects bad arguments before touching the GPU.
+No call here launches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import kimi_delta_attention_07_gb300 as kda
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(kda_\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from kimi_delta_attention_07_gb300 import _build
+    _build.build()
+    return kda.load()
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("kda_chunk_fwd", "kda_chunk_intra", "kda_chunk_scan", "kda_recurrent_step", "kda_chunk_workspace_bytes",
+              "kda_workspace_status", "kda_status_string", "kda_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(kda.lib_path())
+    for n in _declared_functions():
+        assert hasattr(raw, n), f"libkda does not export {n}"
+    assert set(kda.EXPORTS) <= set(_declared_functions())
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert kda.kda_status_string(s).startswith("KDA_")
+    assert "unknown" in kda.kda_status_string(99)
+    assert lib.kda_version() == 100
+
+
+def test_workspace_bytes(lib):
+    f = kda.kda_chunk_workspace_bytes
+    assert f(4096, 1, 32) > 0
+    assert f(4096, 1, 32, 64, 128) == 0          # only K = V = 128 is built
+    assert f(-1, 1, 32) == 0 and f(10, 0, 32) == 0 and f(10, 1, 0) == 0
+    assert f(10, 1, 32, dtype=7) == 0
+    # grows with tokens, sequences and heads; covers one record per (chunk, head)
+    assert f(8192, 1, 32) > f(4096, 1, 32)
+    assert f(4096, 4, 32) > f(4096, 1, 32)
+    assert f(4096, 1, 32) >= (4096 // 64) * 32 * 64 * 128 * 2
+
+
+def _chunk(lib, **kw):
+    a = dict(q=8, k=8, v=8, g=16, beta=16, s0=None, sf=None, idx=None, slots=0, o=8, cu=None,
+             N=1, T=64, H=1, K=128, V=128, scale=0.1, dt=kda.KDA_BF16, flags=0, ws=256,
+             wsb=1 << 30, stream=None)
+    a.update(kw)
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.kda_chunk_fwd(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]),
+                             vp(a["s0"]), vp(a["sf"]), vp(a["idx"]), a["slots"], vp(a["o"]),
+                             vp(a["cu"]), a["N"], a["T"], a["H"], a["K"], a["V"], a["scale"],
+                             a["dt"], a["flags"], vp(a["ws"]), a["wsb"], None)
+
+
+def test_chunk_fwd_rejects_bad_arguments_without_launching(lib):
+    # fake, never-dereferenced addresses: validation fails before any launch
+    base = 1 << 20
+    ok = dict(q=base, k=base, v=base, g=base, beta=base, o=base, ws=base)
+    assert _chunk(lib, **{**ok, "dt": 5}) == kda.KDA_ERR_INVALID_ARG
+    assert _chunk(lib, **{**ok, "K": 64}) == kda.KDA_ERR_UNSUPPORTED
+    assert _chunk(lib, **{**ok, "q": None}) == kda.KDA_ERR_INVALID_ARG
+    assert _chunk(lib, **{**ok, "N": 0}) == kda.KDA_ERR_INVALID_ARG
+    assert _chunk(lib, **{**ok, "T": -1}) == kda.KDA_ERR_INVALID_ARG
+    assert _chunk(lib, **{**ok, "N": 3, "T": 64}) == kda.KDA_ERR_INVALID_ARG  # 3 does not divide 64
+    assert _chunk(lib, **{**ok, "flags": 8}) == kda.KDA_ERR_INVALID_ARG
+    assert _chunk(lib, **{**ok, "q": base + 2}) == kda.KDA_ERR_INVALID_ARG   # misaligned row
+    assert _chunk(lib, **{**ok, "ws": None}) == kda.KDA_ERR_WORKSPACE
+    assert _chunk(lib, **{**ok, "ws": base + 16}) == kda.KDA_ERR_WORKSPACE   # not 256-aligned
+    assert _chunk(lib, **{**ok, "wsb": 1024}) == kda.KDA_ERR_WORKSPACE
+    assert _chunk(lib, **{**ok, "idx": base, "slots": 0}) == kda.KDA_ERR_INVALID_ARG
+    assert _chunk(lib, **{**ok, "scale": float("nan")}) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_recurrent_step_rejects_bad_arguments_without_launching(lib):
+    base = 1 << 20
+    vp = ctypes.c_void_p
+
+    def step(**kw):
+        a = dict(q=base, k=base, v=base, g=base, beta=base, pool=base, idx=None, slots=4, o=base,
+                 N=4, H=2, K=128, V=128, scale=0.1, dt=kda.KDA_F32)
+        a.update(kw)
+        p = lambda x: None if x is None else vp(x)
+        return lib.kda_recurrent_step(p(a["q"]), p(a["k"]), p(a["v"]), p(a["g"]), p(a["beta"]),
+                                      p(a["pool"]), p(a["idx"]), a["slots"], p(a["o"]), a["N"],
+                                      a["H"], a["K"], a["V"], a["scale"], a["dt"], None)
+
+    assert step(N=0) == kda.KDA_OK                         # empty batch: nothing to do
+    assert step(V=64) == kda.KDA_ERR_UNSUPPORTED
+    assert step(pool=None) == kda.KDA_ERR_INVALID_ARG
+    assert step(slots=3) == kda.KDA_ERR_INVALID_ARG         # identity slots need slots >= N
+    assert step(N=-1) == kda.KDA_ERR_INVALID_ARG
+    assert step(dt=3) == kda.KDA_ERR_INVALID_ARG
+    assert step(g=base + 4) == kda.KDA_ERR_INVALID_ARG      # g rows must be 16-byte aligned
+
+
+def test_product_path_does_not_touch_the_oracle():
+    # the library package and its sources never import or name the oracle
+    pkg = os.path.join(ROOT, "kimi_delta_attention_07_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        if "_build" in dirpath:
+            continue
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert "import oracle" not in text and "from oracle" not in text, fn
+                assert "kda_oracle" not in text, fn

@@ -1,0 +1,278 @@
+"""CUDA path vs the fp64 oracle, through the C ABI, on seeded synthetic inputs.
+
+Tolerances (relative L2 error over a whole tensor, per the acceptance bar of
+the KDA core): 1e-4 for fp32 inputs, 1e-2 for bf16 q/k/v.  Outputs of bf16
+calls are bf16, so their o is held to the bf16 bar even on the precise path;
+fp32 states are always compared at their own precision.
+"""
+import numpy as np
+import pytest
+import torch
+
+import kda_inputs
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL_F32 = 1e-4
+TOL_BF16 = 1e-2
+
+
+@pytest.fixture(scope="module")
+def kda():
+    import kimi_delta_attention_07_gb300 as m
+    m.load()  # raises if libkda is missing: no fallback
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    return m
+
+
+def rel_l2(x, ref):
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    return float(np.linalg.norm(x - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+def to_np(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def vk_to_kv(s):
+    """library state [.., V, K] -> oracle orientation [.., K, V]"""
+    return np.swapaxes(to_np(s), -1, -2)
+
+
+def dev(x, names=("q", "k", "v", "g", "beta", "cu_seqlens", "initial_state")):
+    return {n: (x[n].cuda() if x.get(n) is not None else None) for n in names}
+
+
+def oracle_prefill(x, heads=None):
+    """Oracle on all heads (or the listed ones).  Returns o [T,h,V], S [N,h,K,V]."""
+    sel = slice(None) if heads is None else list(heads)
+    s0 = x["initial_state"]
+    s0 = None if s0 is None else np.swapaxes(s0.double().numpy(), -1, -2)[:, sel]
+    return oracle.recurrence(x["q"][:, sel], x["k"][:, sel], x["v"][:, sel], x["g"][:, sel],
+                             x["beta"][:, sel], cu_seqlens=x["cu_seqlens"].numpy(),
+                             initial_state=s0)
+
+
+def run_chunk(kda, x, precise=False, **kw):
+    d = dev(x)
+    o, sf = kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                              cu_seqlens=d["cu_seqlens"], initial_state=d["initial_state"],
+                              precise=precise, **kw)
+    torch.cuda.synchronize()
+    return o, sf
+
+
+# ---------------------------------------------------------------------------
+# decode step
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_step_small_with_slot_indices(kda, dtype):
+    N, H, slots = 5, 3, 9
+    pool = kda_inputs.decode_pool(slots, H=H, seed=21)
+    tok = kda_inputs.decode_tokens(N, H=H, dtype=dtype, seed=21)
+    idx = torch.tensor([7, 2, 0, 8, 4], dtype=torch.int32)
+    pool_d = pool.cuda()
+    o = kda.kda_recurrent_step(*(tok[n].cuda() for n in ("q", "k", "v", "g", "beta")), pool_d,
+                               state_indices=idx.cuda())
+    torch.cuda.synchronize()
+    o_ref, pool_ref = oracle.step(tok["q"], tok["k"], tok["v"], tok["g"], tok["beta"],
+                                  np.swapaxes(pool.double().numpy(), -1, -2), state_indices=idx.numpy())
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    assert rel_l2(to_np(o), o_ref) < tol
+    assert rel_l2(vk_to_kv(pool_d), pool_ref) < TOL_F32
+    untouched = [s for s in range(slots) if s not in idx.tolist()]
+    assert torch.equal(pool_d.cpu()[untouched], pool[untouched])
+
+
+def test_step_identity_slots_and_many_steps_fp32(kda):
+    N, H = 4, 2
+    pool = kda_inputs.decode_pool(N, H=H, seed=22)
+    pool_d = pool.cuda()
+    ref = np.swapaxes(pool.double().numpy(), -1, -2)
+    for t in range(20):
+        tok = kda_inputs.decode_tokens(N, H=H, dtype=torch.float32, seed=22, step=t)
+        o = kda.kda_recurrent_step(*(tok[n].cuda() for n in ("q", "k", "v", "g", "beta")), pool_d)
+        o_ref, ref = oracle.step(tok["q"], tok["k"], tok["v"], tok["g"], tok["beta"], ref)
+        assert rel_l2(to_np(o), o_ref) < TOL_F32
+    assert rel_l2(vk_to_kv(pool_d), ref) < TOL_F32
+
+
+def test_step_invalid_slot_writes_nan_and_leaves_pool(kda):
+    N, H, slots = 3, 2, 4
+    pool = kda_inputs.decode_pool(slots, H=H, seed=23)
+    tok = kda_inputs.decode_tokens(N, H=H, dtype=torch.float32, seed=23)
+    idx = torch.tensor([1, 9, -1], dtype=torch.int32)  # 9 and -1 are out of range
+    pool_d = pool.cuda()
+    o = kda.kda_recurrent_step(*(tok[n].cuda() for n in ("q", "k", "v", "g", "beta")), pool_d,
+                               state_indices=idx.cuda())
+    torch.cuda.synchronize()
+    o = o.cpu()
+    assert torch.isnan(o[1]).all() and torch.isnan(o[2]).all()
+    assert torch.isfinite(o[0]).all()
+    assert torch.equal(pool_d.cpu()[[0, 2, 3]], pool[[0, 2, 3]])
+    o_ref, pool_ref = oracle.step(tok["q"][:1], tok["k"][:1], tok["v"][:1], tok["g"][:1],
+                                  tok["beta"][:1], np.swapaxes(pool.double().numpy(), -1, -2),
+                                  state_indices=[1])
+    assert rel_l2(to_np(o[:1]), o_ref) < TOL_F32
+
+
+def test_step_decode_256_full_size_sampled(kda):
+    """The 256 x 32 decode workload, 64 steps, in the bench's launch
+    configuration; the oracle follows a sample of (sequence, head) pairs."""
+    N, H, steps = 256, 32, 64
+    pool = kda_inputs.decode_pool(N, H=H, seed=3)
+    pool_d = pool.cuda()
+    rng = np.random.default_rng(0)
+    seqs = rng.choice(N, 6, replace=False)
+    heads = rng.choice(H, 3, replace=False)
+    ref = np.swapaxes(pool[seqs][:, heads].double().numpy(), -1, -2)
+    for t in range(steps):
+        tok = kda_inputs.decode_tokens(N, H=H, seed=3, step=t)
+        o = kda.kda_recurrent_step(*(tok[n].cuda() for n in ("q", "k", "v", "g", "beta")), pool_d)
+        if t % 16 == 15 or t == 0:
+            torch.cuda.synchronize()
+        sub = {n: tok[n][seqs][:, heads] for n in ("q", "k", "v", "g", "beta")}
+        o_ref, ref = oracle.step(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], ref)
+        if t in (0, steps - 1):
+            assert rel_l2(to_np(o[seqs][:, heads]), o_ref) < TOL_BF16
+    got = vk_to_kv(pool_d[seqs][:, heads])
+    assert rel_l2(got, ref) < TOL_F32
+    assert torch.isfinite(pool_d).all()
+
+
+# ---------------------------------------------------------------------------
+# chunked prefill
+# ---------------------------------------------------------------------------
+
+def test_chunk_recurrence_small_fp32(kda):
+    """B=1 H=2 T=256 fp32 (seed 0): the fp32 path meets the 1e-4 bar."""
+    x = kda_inputs.recurrence_small()
+    o, sf = run_chunk(kda, x)
+    o_ref, s_ref = oracle_prefill(x)
+    assert rel_l2(to_np(o), o_ref) < TOL_F32
+    assert rel_l2(vk_to_kv(sf), s_ref) < TOL_F32
+
+
+@pytest.mark.parametrize("lengths", [[1], [63], [64], [65], [127, 64, 1, 200], [0, 70, 0]])
+def test_chunk_ragged_and_edge_lengths_fp32(kda, lengths):
+    x = kda_inputs.prefill(lengths, H=2, dtype=torch.float32, seed=31, init_std=0.02)
+    o, sf = run_chunk(kda, x)
+    o_ref, s_ref = oracle_prefill(x)
+    if sum(lengths):
+        assert rel_l2(to_np(o), o_ref) < TOL_F32
+    assert rel_l2(vk_to_kv(sf), s_ref) < TOL_F32
+
+
+@pytest.mark.parametrize("precise", [False, True])
+def test_chunk_varlen_bf16(kda, precise):
+    x = kda_inputs.prefill([300, 64, 129, 5], H=3, dtype=torch.bfloat16, seed=32, init_std=0.02)
+    o, sf = run_chunk(kda, x, precise=precise)
+    o_ref, s_ref = oracle_prefill(x)
+    assert rel_l2(to_np(o), o_ref) < TOL_BF16
+    assert rel_l2(vk_to_kv(sf), s_ref) < (TOL_F32 if precise else TOL_BF16)
+
+
+def test_chunk_strong_decay_fp32(kda):
+    """The long-prefill decay mix (10% of channels at -3..-1 per token)."""
+    x = kda_inputs.prefill([257], H=2, dtype=torch.float32, seed=33, g_mixed=True)
+    o, sf = run_chunk(kda, x)
+    o_ref, s_ref = oracle_prefill(x)
+    assert rel_l2(to_np(o), o_ref) < TOL_F32
+    assert rel_l2(vk_to_kv(sf), s_ref) < TOL_F32
+
+
+def test_chunk_dense_batch_without_cu_seqlens(kda):
+    x = kda_inputs.prefill([96, 96, 96], H=2, dtype=torch.float32, seed=34)
+    d = dev(x)
+    o, sf = kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], n_seqs=3)
+    torch.cuda.synchronize()
+    o_ref, s_ref = oracle_prefill(x)
+    assert rel_l2(to_np(o), o_ref) < TOL_F32
+    assert rel_l2(vk_to_kv(sf), s_ref) < TOL_F32
+
+
+def test_chunk_handoff_into_pool_then_decode(kda):
+    """Prefill final states scattered into pool slots (in place, initial state
+    read from the same slots), then decode steps continue from them."""
+    H, slots = 2, 6
+    x = kda_inputs.prefill([90, 33], H=H, dtype=torch.float32, seed=35)
+    pool = kda_inputs.decode_pool(slots, H=H, seed=35)
+    idx = torch.tensor([4, 1], dtype=torch.int32)
+    pool_d = pool.cuda()
+    d = dev(x)
+    o, _ = kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], cu_seqlens=d["cu_seqlens"],
+                             initial_state=pool_d, final_state=pool_d, state_indices=idx.cuda())
+    s0 = np.swapaxes(pool.double().numpy(), -1, -2)[idx.numpy()]
+    o_ref, s_ref = oracle.recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                                     cu_seqlens=x["cu_seqlens"].numpy(), initial_state=s0)
+    torch.cuda.synchronize()
+    assert rel_l2(to_np(o), o_ref) < TOL_F32
+    got = vk_to_kv(pool_d)
+    assert rel_l2(got[idx.numpy()], s_ref) < TOL_F32
+    others = [s for s in range(slots) if s not in idx.tolist()]
+    assert torch.equal(pool_d.cpu()[others], pool[others])
+    ref_pool = got.copy()
+    ref_pool[idx.numpy()] = s_ref
+    for t in range(4):
+        tok = kda_inputs.decode_tokens(2, H=H, dtype=torch.float32, seed=36, step=t)
+        o2 = kda.kda_recurrent_step(*(tok[n].cuda() for n in ("q", "k", "v", "g", "beta")), pool_d,
+                                    state_indices=idx.cuda())
+        o2_ref, ref_pool = oracle.step(tok["q"], tok["k"], tok["v"], tok["g"], tok["beta"],
+                                       ref_pool, state_indices=idx.numpy())
+        assert rel_l2(to_np(o2), o2_ref) < TOL_F32
+    assert rel_l2(vk_to_kv(pool_d), ref_pool) < TOL_F32
+
+
+def test_chunk_bad_cu_seqlens_are_flagged_and_skipped(kda):
+    x = kda_inputs.prefill([64, 64], H=1, dtype=torch.float32, seed=37)
+    d = dev(x)
+    bad = torch.tensor([0, 100, 64], dtype=torch.int32, device="cuda")  # decreasing
+    ws = torch.zeros(kda.kda_chunk_workspace_bytes(128, 2, 1, dtype=kda.KDA_F32),
+                     dtype=torch.uint8, device="cuda")
+    sf = torch.full((2, 1, 128, 128), 7.0, device="cuda")
+    kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], cu_seqlens=bad, final_state=sf,
+                      workspace=ws)
+    assert kda.kda_workspace_status(ws) & 1
+    assert (sf[1] == 7.0).all()  # the bad sequence is skipped, not written
+
+
+def test_chunked_and_recurrent_gpu_paths_agree_fp32(kda):
+    """Same inputs through kda_chunk_fwd and through T kda_recurrent_step calls."""
+    x = kda_inputs.recurrence_small()
+    o_c, s_c = run_chunk(kda, x)
+    H = x["H"]
+    pool = torch.zeros((1, H, 128, 128), device="cuda")
+    outs = []
+    for t in range(x["q"].shape[0]):
+        sl = slice(t, t + 1)
+        outs.append(kda.kda_recurrent_step(x["q"][sl].cuda(), x["k"][sl].cuda(), x["v"][sl].cuda(),
+                                           x["g"][sl].cuda(), x["beta"][sl].cuda(), pool))
+    o_r = torch.cat(outs)
+    torch.cuda.synchronize()
+    assert rel_l2(to_np(o_c), to_np(o_r)) < TOL_F32
+    assert rel_l2(to_np(s_c), to_np(pool)) < TOL_F32
+
+
+def test_chunk_prefill_4k_full_size_sampled_heads(kda):
+    """B=1 H=32 T=4096 bf16 (seed 1) in the bench's launch configuration; the
+    oracle checks a sample of heads (heads are independent)."""
+    x = kda_inputs.prefill_4k()
+    o, sf = run_chunk(kda, x)
+    heads = [0, 13, 31]
+    o_ref, s_ref = oracle_prefill(x, heads)
+    assert rel_l2(to_np(o[:, heads]), o_ref) < TOL_BF16
+    assert rel_l2(vk_to_kv(sf[:, heads]), s_ref) < TOL_BF16
+    assert torch.isfinite(o).all() and torch.isfinite(sf).all()
+
+
+def test_chunk_varlen_8_full_size_sampled_heads(kda):
+    x = kda_inputs.varlen_8()
+    o, sf = run_chunk(kda, x)
+    heads = [5, 22]
+    o_ref, s_ref = oracle_prefill(x, heads)
+    assert rel_l2(to_np(o[:, heads]), o_ref) < TOL_BF16
+    assert rel_l2(vk_to_kv(sf[:, heads]), s_ref) < TOL_BF16
+    assert torch.isfinite(o).all()
