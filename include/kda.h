@@ -186,6 +186,43 @@ int kda_recurrent_step(const void *q, const void *k, const void *v, const float 
                        int64_t n_slots, void *o, int N, int H, int K, int V, float scale,
                        int dtype, void *stream);
 
+/*
+ * Size of the fixed scratch array behind kda_chunk_fwd_noalloc: 64 MiB.
+ */
+#define KDA_NOALLOC_WORKSPACE_BYTES (64u * 1024u * 1024u)
+
+/*
+ * kda_chunk_fwd for callers that cannot allocate device memory.  (The pages
+ * describing KDA have no counterpart of this call; it exists for library
+ * users.)  Some hosts give a kernel library only its input and output
+ * buffers -- an inference server's plugin interface that owns all device
+ * memory through its own pool, or a latency-critical path where a
+ * cudaMalloc, which can synchronise the device, is not allowed.  This call
+ * takes the arguments of kda_chunk_fwd minus the workspace and allocates
+ * nothing: its scratch space is a fixed array of
+ * KDA_NOALLOC_WORKSPACE_BYTES inside the library's device image, which every
+ * GPU that loads the library holds until the process exits.
+ *
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address once (cudaGetSymbolAddress); make that first
+ *     call before any stream capture on that device.
+ *   - Sizes whose kda_chunk_workspace_bytes(...) exceeds
+ *     KDA_NOALLOC_WORKSPACE_BYTES return KDA_ERR_WORKSPACE and enqueue
+ *     nothing; other argument errors are those of kda_chunk_fwd.
+ *   - Every call, from any stream or thread, uses the same array.  Calls
+ *     whose work overlaps on the GPU race and corrupt each other's results:
+ *     order them (one stream, or events).  Nothing needs clearing between
+ *     calls.
+ *   - kda_workspace_status() is not available for this call (the workspace
+ *     is not visible to the caller); bad cu_seqlens or slots still skip the
+ *     offending sequences.
+ */
+int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, const float *initial_state, float *final_state,
+                          const int32_t *state_indices, int64_t n_slots, void *o,
+                          const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens, int H,
+                          int K, int V, float scale, int dtype, int flags, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -26,7 +26,9 @@ KDA_CHUNK_PRECISE = 1
 CHUNK = 64
 
 EXPORTS = ("kda_status_string", "kda_version", "kda_chunk_workspace_bytes", "kda_chunk_fwd",
-           "kda_chunk_intra", "kda_chunk_scan", "kda_workspace_status", "kda_recurrent_step")
+           "kda_chunk_intra", "kda_chunk_scan", "kda_workspace_status", "kda_recurrent_step",
+           "kda_chunk_fwd_noalloc")
+NOALLOC_WORKSPACE_BYTES = 64 * 1024 * 1024
 
 _lib = None
 _lock = threading.Lock()
@@ -64,6 +66,9 @@ def load(path: str | None = None):
             fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, vp, vp, i32, i64, i32, i32, i32,
                            f32, i32, i32, vp, sz, vp]
             fn.restype = i32
+        L.kda_chunk_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, vp, vp, i32, i64,
+                                            i32, i32, i32, f32, i32, i32, vp]
+        L.kda_chunk_fwd_noalloc.restype = i32
         L.kda_workspace_status.argtypes = [vp, ctypes.POINTER(i32), vp]
         L.kda_workspace_status.restype = i32
         L.kda_recurrent_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, vp, i32, i32, i32, i32,
@@ -211,3 +216,34 @@ def kda_recurrent_step(q, k, v, g, beta, state_pool, *, state_indices=None, scal
     if st != KDA_OK:
         raise KdaError(st, "kda_recurrent_step")
     return o
+
+
+def kda_chunk_fwd_noalloc(q, k, v, g, beta, *, cu_seqlens=None, n_seqs=None, initial_state=None,
+                          final_state=None, state_indices=None, n_slots=None, scale=None,
+                          precise=False, o=None, stream=None):
+    """kda_chunk_fwd without a workspace argument, for hosts that cannot
+    allocate device memory: the library serves the scratch space from a
+    fixed 64 MiB array of its own (see include/kda.h).  ``o`` and
+    ``final_state`` must then be supplied by the caller as well, since this
+    wrapper allocates nothing either.  Returns (o, final_state)."""
+    T, H, K = q.shape
+    V = v.shape[-1]
+    dt = _dtype_code(q)
+    N = cu_seqlens.numel() - 1 if cu_seqlens is not None else (1 if n_seqs is None else int(n_seqs))
+    if o is None:
+        raise ValueError("kda_chunk_fwd_noalloc allocates nothing: pass o")
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("o", o),
+                    ("cu_seqlens", cu_seqlens), ("state_indices", state_indices),
+                    ("initial_state", initial_state), ("final_state", final_state)):
+        _check(t, name)
+    slots = 0 if state_indices is None else (final_state.shape[0] if n_slots is None else int(n_slots))
+    flags = KDA_CHUNK_PRECISE if precise else 0
+    if scale is None:
+        scale = K ** -0.5
+    st = load().kda_chunk_fwd_noalloc(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(initial_state),
+                                      _p(final_state), _p(state_indices), slots, _p(o),
+                                      _p(cu_seqlens), N, T, H, K, V, float(scale), dt, flags,
+                                      _stream(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_chunk_fwd_noalloc")
+    return o, final_state
