@@ -16,15 +16,11 @@ inline bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 // The chunk path a call takes: the tensor-core path for bf16 inputs unless
 // the precise path is requested.
 inline bool use_tensor_cores(int dtype, int flags) {
-    (void)dtype;
-    (void)flags;
-    return false;
+    return dtype == KDA_BF16 && !(flags & KDA_CHUNK_PRECISE);
 }
 
 inline size_t record_bytes(int dtype, int flags) {
-    (void)dtype;
-    (void)flags;
-    return F32Rec::bytes;
+    return use_tensor_cores(dtype, flags) ? (size_t)TcRec::bytes : F32Rec::bytes;
 }
 
 }  // namespace
@@ -85,16 +81,21 @@ int chunk_call(int phase, const void *q, const void *k, const void *v, const flo
     cudaStream_t s = (cudaStream_t)stream;
     cudaGetLastError();  // clear a stale error so the checks below see only ours
     cudaError_t e = cudaSuccess;
+    const bool tc = use_tensor_cores(dtype, flags);
     if (phase & kIntra) {
         e = launch_chunk_index(cu_seqlens, n_seqs, total_tokens, state_indices, n_slots,
                                workspace, s);
         if (e == cudaSuccess)
-            e = launch_chunk_prep_f32(q, k, v, g, beta, dtype, n_seqs, total_tokens, H, scale,
-                                      workspace, s);
+            e = tc ? launch_chunk_prep_tc(q, k, v, g, beta, n_seqs, total_tokens, H, scale,
+                                          workspace, s)
+                   : launch_chunk_prep_f32(q, k, v, g, beta, dtype, n_seqs, total_tokens, H,
+                                           scale, workspace, s);
     }
     if (e == cudaSuccess && (phase & kScan))
-        e = launch_chunk_scan_f32(initial_state, final_state, state_indices, o, dtype, n_seqs,
-                                  total_tokens, H, workspace, s);
+        e = tc ? launch_chunk_scan_tc(initial_state, final_state, state_indices, o, n_seqs,
+                                      total_tokens, H, workspace, s)
+               : launch_chunk_scan_f32(initial_state, final_state, state_indices, o, dtype,
+                                       n_seqs, total_tokens, H, workspace, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return KDA_ERR_CUDA;

@@ -101,6 +101,24 @@ struct F32Rec {
     static constexpr size_t bytes = floats * sizeof(float);
 };
 
+// bf16 tensor-core path: per (chunk, head) record.  The first kStage bytes
+// (WQ | KDT | A | gC) are the scan's shared-memory image of the chunk, in the
+// 128-byte-swizzled K-major operand layout; U follows, row-major.
+//   WQ  [128 rows][128 K] bf16: rows 0..63 W, rows 64..127 QG        32 KB
+//   KDT [128 rows (key)][64 K (chunk row)] bf16: KD^T                16 KB
+//   A   [64][64] bf16: causal scores (directly after KDT)             8 KB
+//   gC  [128] fp32: exp(G_last)
+//   U   [64][128] bf16 row-major                                     16 KB
+struct TcRec {
+    static constexpr uint32_t WQ = 0;
+    static constexpr uint32_t KDT = 32768;
+    static constexpr uint32_t A = KDT + 16384;
+    static constexpr uint32_t GC = A + 8192;
+    static constexpr uint32_t U = GC + 512;
+    static constexpr uint32_t bytes = 74752;  // U + 16384, rounded up to 1024
+};
+static_assert(TcRec::U + 16384 <= TcRec::bytes, "TcRec layout");
+
 // ---- launchers (return cudaGetLastError() of the launch) ------------------
 
 cudaError_t launch_chunk_index(const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens,
@@ -115,6 +133,15 @@ cudaError_t launch_chunk_scan_f32(const float *initial_state, float *final_state
                                   const int32_t *state_indices, void *o, int dtype, int n_seqs,
                                   int64_t total_tokens, int H, void *workspace,
                                   cudaStream_t stream);
+
+cudaError_t launch_chunk_prep_tc(const void *q, const void *k, const void *v, const float *g,
+                                 const float *beta, int n_seqs, int64_t total_tokens, int H,
+                                 float scale, void *workspace, cudaStream_t stream);
+
+cudaError_t launch_chunk_scan_tc(const float *initial_state, float *final_state,
+                                 const int32_t *state_indices, void *o, int n_seqs,
+                                 int64_t total_tokens, int H, void *workspace,
+                                 cudaStream_t stream);
 
 // Block-wide helper used by the chunk kernels: find the sequence that owns
 // global chunk `c` (largest n with chunk_off[n] <= c; chunk_off non-decreasing).
