@@ -51,6 +51,7 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--precise", action="store_true", help="fp32 CUDA-core chunk path")
     return p.parse_args()
 
@@ -275,7 +276,7 @@ def run_ours(args, rank, ws):
     else:
         clk = None
 
-    e2e = run_e2e(args, kda, x, dev, stream, work, flags, ws)
+    e2e = None if args.no_e2e else run_e2e(args, kda, x, dev, stream, work, flags, ws)
     dec = None if args.no_decode else run_decode(args, kda, dev, stream, pk, ws)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:

@@ -36,6 +36,11 @@
  * finite value is accepted), beta is the already-activated write strength.
  * The supported head dims are K = V = 128.
  *
+ * Alignment: row pointers must be 16-byte aligned for fp32 tensors and for
+ * bf16 tensors on the tensor-core chunk path, 8-byte aligned for other bf16
+ * uses; the workspace 256-byte aligned.  (Tensors from cudaMalloc or
+ * PyTorch's allocator always are.)
+ *
  * Errors: arguments are validated before anything is enqueued; a failing
  * call returns a kda_status other than KDA_OK and enqueues nothing.  A
  * failed kernel launch returns KDA_ERR_CUDA (the CUDA error is cleared).

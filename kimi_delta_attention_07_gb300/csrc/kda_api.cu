@@ -67,8 +67,9 @@ int chunk_call(int phase, const void *q, const void *k, const void *v, const flo
     if (!cu_seqlens && total_tokens % n_seqs != 0) return KDA_ERR_INVALID_ARG;
     if (state_indices && n_slots <= 0) return KDA_ERR_INVALID_ARG;
     if (!state_indices && n_slots < 0) return KDA_ERR_INVALID_ARG;
-    // vector loads need 16-byte (fp32) / 8-byte (bf16) aligned rows
-    const size_t ea = 4 * elem_bytes(dtype);
+    // vector loads need 16-byte (fp32) / 8-byte (bf16) aligned rows; the
+    // tensor-core path moves rows with 16-byte bulk copies and vector stores
+    const size_t ea = use_tensor_cores(dtype, flags) ? 16 : 4 * elem_bytes(dtype);
     if ((q && !aligned(q, ea)) || (k && !aligned(k, ea)) || (v && !aligned(v, ea)) ||
         (o && !aligned(o, ea)) || (g && !aligned(g, 16)) || (beta && !aligned(beta, 4)) ||
         (initial_state && !aligned(initial_state, 16)) || (final_state && !aligned(final_state, 16)))

@@ -3,32 +3,35 @@
 //
 // Same two phases as the fp32 path (chunked form of the Ascend model file's
 // _torch_chunk_kda), with every dense contraction on the 5th-generation
-// tensor cores:
+// tensor cores.
 //
-// prep, one CTA per (chunk, head), 8 warps:
+// prep -- persistent, one CTA per SM walking the (chunk, head) items; the raw
+// q, k, v, g rows of the next item are bulk-copied into a second shared
+// buffer while the current item is computed:
 //   * q_hat = scale * l2norm(q), k_hat = l2norm(k) (fp32), G = cumsum(g).
+//   * G is replaced in place by l_r = exp(G_r - G_{16 br}) (br = r's 16-row
+//     block) and per-channel block factors rho_b = exp(G_{16b}) and
+//     tau_{br,b} = exp(G_{16br} - G_{16b}); every exponent is <= 0, and
+//     exp(G_r - G_{16b}) = l_r * tau_{br,b}, exp(G_r) = l_r * rho_br.
 //   * Causal scores A[r,j] and the interaction matrix L[r,j] as ONE M=128 MMA
-//     per 16-column block b of the chunk: rows 0..63 of the A operand are
-//     q_hat_r * exp(G_r - G_ref), rows 64..127 k_hat_r * exp(G_r - G_ref),
-//     the B operand is k_hat_j * exp(G_ref - G_j) for the 16 keys j of the
-//     block, with the reference G_ref = G at the block's first token.  For
-//     every kept pair (j <= r) the row factor is <= 1 and the column factor is
-//     at most exp(15 * max|g|), so the factorisation cannot overflow for
-//     per-token decays down to about -5.3 (the column exponent is clamped at
-//     80 beyond that, and only masked pairs can then be affected).
-//   * X = (I + beta L)^-1 by forward substitution in fp32; T = X diag(beta).
-//   * W^T = (exp(G) k_hat)^T T^T and U^T = v^T T^T as M=128 (key / value
-//     dim) x N=64 x K=64 MMAs.
-//   * The record handed to the scan holds the MMA operands of the scan,
-//     already in the 128-byte-swizzled K-major shared-memory layout, so the
-//     scan moves them with one bulk copy per chunk:
-//       WQ  [128][128]: rows 0..63 W, rows 64..127 QG = q_hat exp(G)
-//       KDT [128][64] : KD^T, KD = k_hat exp(G_last - G)
-//       A   [64][64]  : causal scores (scale folded into q_hat)
-//       gC  [128] fp32: exp(G_last);   U [64][128] bf16 row-major.
+//     per 16-column block b: rows 0..63 of the A operand are
+//     q_hat_r * exp(G_r - G_16b), rows 64..127 k_hat_r * exp(G_r - G_16b)
+//     (zero for r < 16b), the B operand is k_hat_j * exp(G_16b - G_j) for the
+//     16 keys of block b.  For every kept pair (j <= r) the row factor is
+//     <= 1 and the column factor at most exp(15 * max|g|); the column
+//     exponent is clamped at 80, which only matters for per-token decays
+//     below about -5.3 and then only for masked pairs.
+//   * X = (I + beta L)^-1 blockwise in fp32 (16x16 diagonal blocks by forward
+//     substitution, one warp each, then three levels of 16x16 products);
+//     T = X diag(beta).
+//   * W = T (exp(G) k_hat) and U = T v as M=128 x N=128 x K=64 MMAs whose A
+//     operand is [T ; scratch] (rows 64..127 unused), so each thread of
+//     TMEM lanes 0..63 holds whole rows of W and U.
+//   * Record written with 16-byte stores, laid out as the scan's shared-
+//     memory image (128-byte-swizzled K-major operands), see TcRec.
 //
-// scan, one CTA per (sequence, head, 32 value columns), 4 warps:
-//   per chunk (records double-buffered by cp.async.bulk):
+// scan, one CTA per (sequence, head, 32 value columns), 4 warps, records in a
+// 3-stage cp.async.bulk ring:
 //     D1  = WQ * S            (M=128, N=32, K=128)  rows 0..63: W S
 //     Vn  = U - D1[0:64]      (fp32, written as a bf16 K-major operand)
 //     D1 += [* ; A] * Vn      (rows 64..127 become o = QG S + A Vn)
@@ -37,6 +40,8 @@
 //   The 128-row A operand of the second MMA starts 8 KB before the A tile in
 //   the staged record (its rows 0..63 are the tail of KD^T and only feed D1
 //   rows that were already consumed).
+#include <algorithm>
+
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
 
@@ -49,247 +54,469 @@ constexpr int C = kChunk;    // 64
 constexpr int D = kHeadDim;  // 128
 constexpr int kStatusTimeout = 4;
 
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&p);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
+    return make_uint4(pack2(x[0], x[1]), pack2(x[2], x[3]), pack2(x[4], x[5]), pack2(x[6], x[7]));
+}
+
+// 8 consecutive bf16 (16 bytes) -> fp32
+__device__ __forceinline__ void unpack8(uint4 raw, float (&x)[8]) {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162 *>(&w[i]);
+        const float2 f = __bfloat1622float2(p);
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+    }
+}
+
+__device__ __forceinline__ void load8f(const float *p, float (&x)[8]) {
+    const float4 a = *reinterpret_cast<const float4 *>(p);
+    const float4 b = *reinterpret_cast<const float4 *>(p + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+__device__ __forceinline__ void store8f(float *p, const float (&x)[8]) {
+    *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
+    *reinterpret_cast<float4 *>(p + 4) = make_float4(x[4], x[5], x[6], x[7]);
+}
+
 // ---------------------------------------------------------------------------
 // prep
 // ---------------------------------------------------------------------------
 constexpr int kPrepThreads = 256;
-constexpr uint32_t kPrepTmemCols = 128;
-// shared memory plan (offsets from a 1024-aligned base)
-constexpr int P_G = 0;                    // fp32 [64][128] cumulative log-decay   32 KB
-constexpr int P_Z = P_G + C * D * 4;      // 32 KB: A_b operand -> L,X fp32 -> E^T,V^T operands
-constexpr int P_C = P_Z + 32768;          // 4 x [16][128] bf16 column-factor operands 16 KB
-constexpr int P_T = P_C + 16384;          // [64][64] bf16 T operand 8 KB
-constexpr int P_MISC = P_T + 8192;        // rq, rk, beta (fp32 x 64 each), barrier, tmem base
-constexpr int P_BYTES = P_MISC + 3 * 64 * 4 + 64;
-constexpr int P_SMEM = P_BYTES + 1024;    // slack for 1024-byte alignment
+constexpr uint32_t kPrepTmemCols = 256;
+// one item's raw rows (double-buffered)
+constexpr int R_Q = 0;          // bf16 [64][128]; after the A/L MMAs: X fp32 [64][64]
+constexpr int R_K = 16384;      // bf16 [64][128]
+constexpr int R_V = 32768;      // bf16 [64][128]
+constexpr int R_G = 49152;      // fp32 [64][128]: g -> G -> l
+constexpr int R_BYTES = 81920;
+constexpr int P_Z = 2 * R_BYTES;          // 32 KB: A_b operand | L fp32 (stride 68) | E^T, V^T
+constexpr int P_C = P_Z + 32768;          // 16 KB: column-factor operands | [T ; temps]
+constexpr int P_RQ = P_C + 16384;         // fp32 [64]
+constexpr int P_RK = P_RQ + 256;          // fp32 [64]
+constexpr int P_BETA = P_RK + 256;        // fp32 [64]
+constexpr int P_GREF = P_BETA + 256;      // fp32 [5][128]: G at rows 0, 16, 32, 48, 63
+constexpr int P_RHO = P_GREF + 5 * 512;   // fp32 [4][128]: exp(G_16b)
+constexpr int P_TAU = P_RHO + 4 * 512;    // fp32 [6][128]: exp(G_16br - G_16b), br > b
+constexpr int P_BAR = P_TAU + 6 * 512;    // full[2], mma barrier, tmem slot
+constexpr int P_BYTES = P_BAR + 64;
+constexpr int P_SMEM = P_BYTES + 1024;
+constexpr int LSTRIDE = 68;               // row stride (floats) of L in shared memory
+static_assert(C * LSTRIDE * 4 <= 32768, "L does not fit");
 
-__device__ __forceinline__ void st_bf16(unsigned char *base, uint32_t off, float x) {
-    *reinterpret_cast<__nv_bfloat16 *>(base + off) = __float2bfloat16_rn(x);
+__device__ __forceinline__ int tau_index(int br, int b) { return br * (br - 1) / 2 + b; }
+
+struct PrepItem {
+    int64_t tok0;
+    int valid, h, c;
+};
+
+__device__ __forceinline__ PrepItem prep_item(int item, int H, const int32_t *chunk_off,
+                                              const int32_t *seq_start, const int32_t *seq_len,
+                                              int n_seqs) {
+    PrepItem it;
+    it.c = item / H;
+    it.h = item - it.c * H;
+    const int n = owner_of_chunk(chunk_off, n_seqs, it.c);
+    const int jc = it.c - chunk_off[n];
+    it.tok0 = (int64_t)seq_start[n] + (int64_t)jc * C;
+    it.valid = min(C, seq_len[n] - jc * C);
+    return it;
 }
 
-__global__ void __launch_bounds__(kPrepThreads, 2)
+__global__ void __launch_bounds__(kPrepThreads, 1)
     chunk_prep_tc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                          const __nv_bfloat16 *__restrict__ v, const float *__restrict__ g,
                          const float *__restrict__ beta, int n_seqs, int H, float scale,
                          void *workspace, WsLayout L) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    float *sG = reinterpret_cast<float *>(sm + P_G);
     unsigned char *sZ = sm + P_Z;
     unsigned char *sC = sm + P_C;
-    unsigned char *sT = sm + P_T;
-    float *sRq = reinterpret_cast<float *>(sm + P_MISC);
-    float *sRk = sRq + 64;
-    float *sB = sRk + 64;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sB + 64);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 1);
+    float *sRq = reinterpret_cast<float *>(sm + P_RQ);
+    float *sRk = reinterpret_cast<float *>(sm + P_RK);
+    float *sB = reinterpret_cast<float *>(sm + P_BETA);
+    float *sGref = reinterpret_cast<float *>(sm + P_GREF);
+    float *sRho = reinterpret_cast<float *>(sm + P_RHO);
+    float *sTau = reinterpret_cast<float *>(sm + P_TAU);
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + P_BAR);
+    uint64_t *mbar = full + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 1);
 
     const int32_t *chunk_off = ws_at<const int32_t>(workspace, L.chunk_off_off);
-    const int c = blockIdx.x, h = blockIdx.y;
-    if (c >= chunk_off[n_seqs]) return;
-    const int n = owner_of_chunk(chunk_off, n_seqs, c);
-    const int jc = c - chunk_off[n];
-    const int64_t tok0 = (int64_t)ws_at<const int32_t>(workspace, L.seq_start_off)[n] + (int64_t)jc * C;
-    const int valid = min(C, ws_at<const int32_t>(workspace, L.seq_len_off)[n] - jc * C);
-    unsigned char *rec = ws_at<unsigned char>(workspace, L.records_off + ((size_t)c * H + h) * TcRec::bytes);
+    const int32_t *seq_start = ws_at<const int32_t>(workspace, L.seq_start_off);
+    const int32_t *seq_len = ws_at<const int32_t>(workspace, L.seq_len_off);
     int32_t *status = ws_at<int32_t>(workspace, L.status_off);
+    const int n_items = chunk_off[n_seqs] * H;
+    if ((int)blockIdx.x >= n_items) return;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (warp == 0) tmem_alloc(tmem_slot, kPrepTmemCols);
     if (tid == 32) {
-        mbar_init(bar, 1);
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        mbar_init(mbar, 1);
         fence_mbar_init();
-    }
-
-    // 1. cumulative log-decay (threads 0..127, one key channel each) and the
-    //    row norms of q and k (warps 4..7), beta.
-    if (tid < D) {
-        float run = 0.0f;
-        const float *gp = g + (tok0 * H + h) * (int64_t)D + tid;
-#pragma unroll 8
-        for (int r = 0; r < C; ++r) {
-            run += (r < valid) ? gp[(int64_t)r * H * D] : 0.0f;
-            sG[r * D + tid] = run;
-        }
-    } else {
-        for (int r = warp - 4; r < C; r += 4) {
-            float4 q4 = make_float4(0, 0, 0, 0), k4 = q4;
-            if (r < valid) {
-                const int64_t off = ((tok0 + r) * H + h) * (int64_t)D + 4 * lane;
-                q4 = load4(q + off);
-                k4 = load4(k + off);
-            }
-            const float sq = warp_sum(q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w);
-            const float sk = warp_sum(k4.x * k4.x + k4.y * k4.y + k4.z * k4.z + k4.w * k4.w);
-            if (lane == 0) {
-                sRq[r] = scale / sqrtf(sq + 1e-6f);
-                sRk[r] = 1.0f / sqrtf(sk + 1e-6f);
-            }
-        }
-        if (tid - D < C) {
-            const int r = tid - D;
-            sB[r] = r < valid ? beta[(tok0 + r) * H + h] : 0.0f;
-        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // 2. QG (WQ rows 64..127), KD^T, column-factor operands, gC.
-    {
-        const int d = tid & (D - 1);
-        const float Gl = sG[(C - 1) * D + d];
-        for (int r = tid >> 7; r < C; r += 2) {
-            float qv = 0.0f, kv = 0.0f;
-            if (r < valid) {
-                const int64_t off = ((tok0 + r) * H + h) * (int64_t)D + d;
-                qv = __bfloat162float(q[off]);
-                kv = __bfloat162float(k[off]);
-            }
-            const float qh = qv * sRq[r], kh = kv * sRk[r];
-            const float G = sG[r * D + d];
-            const float Gb = sG[(r & ~15) * D + d];
-            st_bf16(rec, TcRec::WQ + sw128_off(64 + r, d, 128), qh * __expf(G));
-            st_bf16(rec, TcRec::KDT + sw128_off(d, r, 128), kh * __expf(Gl - G));
-            st_bf16(sC, (uint32_t)((r >> 4) * 4096) + sw128_off(r & 15, d, 16),
-                    kh * __expf(fminf(Gb - G, 80.0f)));
-        }
-        if (tid < D) reinterpret_cast<float *>(rec + TcRec::GC)[tid] = __expf(Gl);
+    // first item: expect its bytes, then rows 0..valid-1 are copied by threads 0..63
+    PrepItem nxt = prep_item(blockIdx.x, H, chunk_off, seq_start, seq_len, n_seqs);
+    if (tid == 0) mbar_arrive_expect_tx(&full[0], (uint32_t)nxt.valid * 1280u);
+    __syncthreads();
+    float beta_next = 0.0f;
+    if (tid < nxt.valid) {
+        const int64_t row = (nxt.tok0 + tid) * H + nxt.h;
+        bulk_g2s(sm + R_Q + tid * 256, q + row * D, 256, &full[0]);
+        bulk_g2s(sm + R_K + tid * 256, k + row * D, 256, &full[0]);
+        bulk_g2s(sm + R_V + tid * 256, v + row * D, 256, &full[0]);
+        bulk_g2s(sm + R_G + tid * 512, g + row * D, 512, &full[0]);
+        beta_next = beta[(nxt.tok0 + tid) * H + nxt.h];
     }
 
-    // 3. A and L, one 16-column block at a time (A operand rebuilt in Z).
+    uint32_t mphase = 0;
     bool ok = true;
-    uint32_t phase = 0;
-    for (int b = 0; b < 4; ++b) {
-        const int d = tid & (D - 1);
-        for (int r = tid >> 7; r < C; r += 2) {
-            float qa = 0.0f, ka = 0.0f;
-            if (r >= 16 * b && r < valid) {
-                const int64_t off = ((tok0 + r) * H + h) * (int64_t)D + d;
-                const float e = __expf(sG[r * D + d] - sG[16 * b * D + d]);
-                qa = __bfloat162float(q[off]) * sRq[r] * e;
-                ka = __bfloat162float(k[off]) * sRk[r] * e;
-            }
-            st_bf16(sZ, sw128_off(r, d, 128), qa);
-            st_bf16(sZ, sw128_off(64 + r, d, 128), ka);
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
-            mma_tile<128, 16, 128>(tmem + 16 * b, smem_u32(sZ), 128, smem_u32(sC + b * 4096), 16,
-                                   false);
-            mma_commit(bar);
-        }
-        ok = mbar_wait(bar, phase) && ok;
-        phase ^= 1;
-        tc_fence_after();
-    }
-    if (!__syncthreads_and(ok)) {
-        if (tid == 0) atomicOr(status, kStatusTimeout);
-        goto done;
-    }
+    int m = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++m) {
+        const PrepItem cur = nxt;
+        const int buf = m & 1;
+        unsigned char *raw = sm + buf * R_BYTES;
+        const __nv_bfloat16 *sQr = reinterpret_cast<const __nv_bfloat16 *>(raw + R_Q);
+        const __nv_bfloat16 *sKr = reinterpret_cast<const __nv_bfloat16 *>(raw + R_K);
+        const __nv_bfloat16 *sVr = reinterpret_cast<const __nv_bfloat16 *>(raw + R_V);
+        float *sG = reinterpret_cast<float *>(raw + R_G);
+        float *sX = reinterpret_cast<float *>(raw + R_Q);  // after the q rows are consumed
+        unsigned char *rec = ws_at<unsigned char>(workspace, L.records_off + ((size_t)cur.c * H + cur.h) * TcRec::bytes);
+        const int valid = cur.valid;
+        if (tid < C) sB[tid] = tid < valid ? beta_next : 0.0f;
 
-    // 4. read A (lanes 0..63) to the record and L (lanes 64..127) to shared fp32.
-    {
-        float *sL = reinterpret_cast<float *>(sZ);
-        const int quarter = warp & 3, col0 = (warp >> 2) * 32;
-        const int row = 32 * quarter + lane;
-        float x[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + col0, x);
-        tmem_ld_wait();
-        if (row < C) {
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int j = col0 + jj;
-                st_bf16(rec, TcRec::A + sw128_off(row, j, 64), j <= row ? x[jj] : 0.0f);
-            }
-        } else {
-            const int r = row - C;
-            const float br = sB[r];
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int j = col0 + jj;
-                sL[r * C + j] = j < r ? br * x[jj] : 0.0f;
+        const int nitem = item + gridDim.x;
+        if (nitem < n_items) {
+            nxt = prep_item(nitem, H, chunk_off, seq_start, seq_len, n_seqs);
+            if (tid == 0) mbar_arrive_expect_tx(&full[buf ^ 1], (uint32_t)nxt.valid * 1280u);
+        }
+        ok = mbar_wait(&full[buf], (m >> 1) & 1) && ok;
+        // zero the rows past the end of the sequence (not copied)
+        for (int i = tid; i < (C - valid) * 16; i += kPrepThreads) {
+            const int r = valid + i / 16, c16 = i % 16;
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(raw + R_Q + r * 256 + c16 * 16) = z;
+            *reinterpret_cast<uint4 *>(raw + R_K + r * 256 + c16 * 16) = z;
+            *reinterpret_cast<uint4 *>(raw + R_V + r * 256 + c16 * 16) = z;
+            *reinterpret_cast<uint4 *>(raw + R_G + r * 512 + c16 * 32) = z;
+            *reinterpret_cast<uint4 *>(raw + R_G + r * 512 + c16 * 32 + 16) = z;
+        }
+        if (!__syncthreads_and(ok)) break;
+        // prefetch the next item into the other buffer (its last reader was item m-1)
+        if (nitem < n_items && tid < nxt.valid) {
+            fence_async_smem();
+            const int64_t row = (nxt.tok0 + tid) * H + nxt.h;
+            unsigned char *nb = sm + (buf ^ 1) * R_BYTES;
+            bulk_g2s(nb + R_Q + tid * 256, q + row * D, 256, &full[buf ^ 1]);
+            bulk_g2s(nb + R_K + tid * 256, k + row * D, 256, &full[buf ^ 1]);
+            bulk_g2s(nb + R_V + tid * 256, v + row * D, 256, &full[buf ^ 1]);
+            bulk_g2s(nb + R_G + tid * 512, g + row * D, 512, &full[buf ^ 1]);
+            beta_next = beta[(nxt.tok0 + tid) * H + nxt.h];
+        }
+
+        // 1. row norms of q and k; cumulative log-decay in place (two halves).
+        for (int r = warp; r < C; r += 8) {
+            float a[8];
+            const uint2 qa = *reinterpret_cast<const uint2 *>(sQr + r * D + 4 * lane);
+            const uint2 ka = *reinterpret_cast<const uint2 *>(sKr + r * D + 4 * lane);
+            unpack8(make_uint4(qa.x, qa.y, ka.x, ka.y), a);
+            const float sq = warp_sum(a[0] * a[0] + a[1] * a[1] + a[2] * a[2] + a[3] * a[3]);
+            const float sk = warp_sum(a[4] * a[4] + a[5] * a[5] + a[6] * a[6] + a[7] * a[7]);
+            if (lane == 0) {
+                sRq[r] = scale / sqrtf(sq + 1e-6f);
+                sRk[r] = 1.0f / sqrtf(sk + 1e-6f);
             }
         }
-    }
-    tc_fence_before();
-    __syncthreads();
-
-    // 5. X = (I + L)^-1 row by row; T = X diag(beta) as a bf16 operand.
-    {
-        const float *sL = reinterpret_cast<const float *>(sZ);
-        float *sX = reinterpret_cast<float *>(sZ) + C * C;
-        const int col = tid >> 2, part = tid & 3;
-        for (int r = 0; r < C; ++r) {
-            float acc = 0.0f;
-            for (int m = col + part; m < r; m += 4) acc = fmaf(sL[r * C + m], sX[m * C + col], acc);
-            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-            if (part == 0) sX[r * C + col] = (col == r) ? 1.0f : (col < r ? -acc : 0.0f);
+        {
+            const int d = tid & (D - 1), r0 = (tid >> 7) * 32;
+            float x[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] = sG[(r0 + i) * D + d];
+#pragma unroll
+            for (int i = 1; i < 32; ++i) x[i] += x[i - 1];
+            if (!r0) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) sG[i * D + d] = x[i];
+            }
             __syncthreads();
-        }
-        for (int i = tid; i < C * C; i += kPrepThreads) {
-            const int r = i / C, cc = i % C;
-            st_bf16(sT, sw128_off(r, cc, 64), sX[r * C + cc] * sB[cc]);
-        }
-    }
-    __syncthreads();
-
-    // 6. E^T = (exp(G) k_hat)^T and V^T operands (in Z), then W^T, U^T MMAs.
-    {
-        unsigned char *sE = sZ, *sV = sZ + 16384;
-        const int d = tid & (D - 1);
-        for (int j = tid >> 7; j < C; j += 2) {
-            float kv = 0.0f, vv = 0.0f;
-            if (j < valid) {
-                const int64_t off = ((tok0 + j) * H + h) * (int64_t)D + d;
-                kv = __bfloat162float(k[off]);
-                vv = __bfloat162float(v[off]);
+            if (r0) {
+                const float base = sG[31 * D + d];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) sG[(r0 + i) * D + d] = x[i] + base;
             }
-            st_bf16(sE, sw128_off(d, j, 128), kv * sRk[j] * __expf(sG[j * D + d]));
-            st_bf16(sV, sw128_off(d, j, 128), vv);
+        }
+        __syncthreads();
+        // reference rows and block factors (threads 0..127: one key channel each)
+        if (tid < D) {
+            const int d = tid;
+            float gb[4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                gb[b] = sG[16 * b * D + d];
+                sGref[b * D + d] = gb[b];
+                sRho[b * D + d] = __expf(gb[b]);
+            }
+            sGref[4 * D + d] = sG[(C - 1) * D + d];
+#pragma unroll
+            for (int br = 1; br < 4; ++br)
+#pragma unroll
+                for (int b = 0; b < br; ++b) sTau[tau_index(br, b) * D + d] = __expf(gb[br] - gb[b]);
+            reinterpret_cast<float *>(rec + TcRec::GC)[d] = __expf(sG[(C - 1) * D + d]);
+        }
+        __syncthreads();
+
+        // 2a. KD^T = (k_hat exp(G_last - G))^T, in 16-byte chunks of 8 chunk rows.
+        for (int qi = tid; qi < 8 * D; qi += kPrepThreads) {
+            const int c8 = qi >> 7, d = qi & (D - 1);
+            const float gl = sGref[4 * D + d];
+            float x[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int r = 8 * c8 + t;
+                x[t] = __bfloat162float(sKr[r * D + d]) * sRk[r] * __expf(gl - sG[r * D + d]);
+            }
+            *reinterpret_cast<uint4 *>(rec + TcRec::KDT + sw128_off(d, 8 * c8, 128)) = pack8(x);
+        }
+        __syncthreads();
+        // 2b. per (row, 8 channels): QG, column factors, then G -> l in place.
+        for (int qi = tid; qi < C * 16; qi += kPrepThreads) {
+            const int r = qi >> 4, d0 = (qi & 15) * 8, br = r >> 4;
+            float G8[8], Gb8[8], rho8[8], qv[8], kv[8];
+            load8f(sG + r * D + d0, G8);
+            load8f(sGref + br * D + d0, Gb8);
+            load8f(sRho + br * D + d0, rho8);
+            unpack8(*reinterpret_cast<const uint4 *>(sQr + r * D + d0), qv);
+            unpack8(*reinterpret_cast<const uint4 *>(sKr + r * D + d0), kv);
+            const float rq = sRq[r], rk = sRk[r];
+            float qg[8], cf[8], l8[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                l8[t] = __expf(G8[t] - Gb8[t]);
+                qg[t] = qv[t] * rq * l8[t] * rho8[t];
+                cf[t] = kv[t] * rk * __expf(fminf(Gb8[t] - G8[t], 80.0f));
+            }
+            *reinterpret_cast<uint4 *>(rec + TcRec::WQ + sw128_off(64 + r, d0, 128)) = pack8(qg);
+            *reinterpret_cast<uint4 *>(sC + br * 4096 + sw128_off(r & 15, d0, 16)) = pack8(cf);
+            store8f(sG + r * D + d0, l8);
+        }
+
+        // 3. A and L: one M=128 x N=16 x K=128 MMA per 16-column block.
+        for (int b = 0; b < 4; ++b) {
+            __syncthreads();  // l complete (b = 0) / previous MMA done with Z (b > 0)
+            for (int qi = tid; qi < C * 16; qi += kPrepThreads) {
+                const int r = qi >> 4, d0 = (qi & 15) * 8, br = r >> 4;
+                float qa[8], ka[8];
+                if (r < 16 * b) {
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) qa[t] = ka[t] = 0.0f;
+                } else {
+                    float l8[8], qv[8], kv[8];
+                    load8f(sG + r * D + d0, l8);
+                    if (br != b) {
+                        float t8[8];
+                        load8f(sTau + tau_index(br, b) * D + d0, t8);
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) l8[t] *= t8[t];
+                    }
+                    unpack8(*reinterpret_cast<const uint4 *>(sQr + r * D + d0), qv);
+                    unpack8(*reinterpret_cast<const uint4 *>(sKr + r * D + d0), kv);
+                    const float rq = sRq[r], rk = sRk[r];
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        qa[t] = qv[t] * rq * l8[t];
+                        ka[t] = kv[t] * rk * l8[t];
+                    }
+                }
+                *reinterpret_cast<uint4 *>(sZ + sw128_off(r, d0, 128)) = pack8(qa);
+                *reinterpret_cast<uint4 *>(sZ + sw128_off(64 + r, d0, 128)) = pack8(ka);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            if (tid == 0) {
+                tc_fence_after();
+                mma_tile<128, 16, 128>(tmem + 16 * b, smem_u32(sZ), 128, smem_u32(sC + b * 4096),
+                                       16, false);
+                mma_commit(mbar);
+            }
+            ok = mbar_wait(mbar, mphase) && ok;
+            mphase ^= 1;
+            tc_fence_after();
+        }
+        if (!__syncthreads_and(ok)) break;
+
+        // 4. A rows (TMEM lanes 0..63) to the record; beta-scaled L rows
+        //    (lanes 64..127) to shared fp32.
+        {
+            float *sL = reinterpret_cast<float *>(sZ);
+            const int quarter = warp & 3, col0 = (warp >> 2) * 32;
+            const int row = 32 * quarter + lane;
+            float x[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + col0, x);
+            tmem_ld_wait();
+            if (row < C) {
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    float y[8];
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) y[t] = (col0 + 8 * c8 + t <= row) ? x[8 * c8 + t] : 0.0f;
+                    *reinterpret_cast<uint4 *>(rec + TcRec::A + sw128_off(row, col0 + 8 * c8, 64)) = pack8(y);
+                }
+            } else {
+                const int r = row - C;
+                const float bet = sB[r];
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    float4 y;
+                    const int j = col0 + 4 * c4;
+                    y.x = (j + 0 < r) ? bet * x[4 * c4 + 0] : 0.0f;
+                    y.y = (j + 1 < r) ? bet * x[4 * c4 + 1] : 0.0f;
+                    y.z = (j + 2 < r) ? bet * x[4 * c4 + 2] : 0.0f;
+                    y.w = (j + 3 < r) ? bet * x[4 * c4 + 3] : 0.0f;
+                    *reinterpret_cast<float4 *>(sL + r * LSTRIDE + j) = y;
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+
+        // 5. X = (I + L)^-1 blockwise; T = X diag(beta) -> bf16 operand at sC.
+        {
+            const float *sL = reinterpret_cast<const float *>(sZ);
+            float *tmp = reinterpret_cast<float *>(sC + 8192);  // 3 x [16][16] fp32
+            if (warp < 4) {  // diagonal blocks: forward substitution, one warp each
+                const int o = 16 * warp, c = lane & 15, part = lane >> 4;
+                for (int r = 0; r < 16; ++r) {
+                    float acc = 0.0f;
+                    for (int mm = c + part; mm < r; mm += 2)
+                        acc = fmaf(sL[(o + r) * LSTRIDE + o + mm], sX[(o + mm) * C + o + c], acc);
+                    acc += __shfl_xor_sync(0xffffffffu, acc, 16);
+                    if (part == 0) sX[(o + r) * C + o + c] = (c == r) ? 1.0f : (c < r ? -acc : 0.0f);
+                    __syncwarp();
+                }
+            }
+            __syncthreads();
+            const int er = tid >> 4, ec = tid & 15;
+            // level by level: X_ab = -X_aa * sum_{m=b}^{a-1} L_am X_mb
+            for (int lvl = 1; lvl < 4; ++lvl) {
+                const int nblk = 4 - lvl;
+                for (int t = 0; t < nblk; ++t) {
+                    const int a = t + lvl, b = t;
+                    float acc = 0.0f;
+                    for (int mb = b; mb < a; ++mb) {
+#pragma unroll 4
+                        for (int x = 0; x < 16; ++x)
+                            acc = fmaf(sL[(16 * a + er) * LSTRIDE + 16 * mb + x],
+                                       sX[(16 * mb + x) * C + 16 * b + ec], acc);
+                    }
+                    tmp[t * 256 + er * 16 + ec] = acc;
+                }
+                __syncthreads();
+                for (int t = 0; t < nblk; ++t) {
+                    const int a = t + lvl, b = t;
+                    float acc = 0.0f;
+                    for (int x = 0; x <= er; ++x)
+                        acc = fmaf(sX[(16 * a + er) * C + 16 * a + x], tmp[t * 256 + x * 16 + ec], acc);
+                    sX[(16 * a + er) * C + 16 * b + ec] = -acc;
+                }
+                __syncthreads();
+            }
+            // T = X diag(beta), lower triangle, as a K-major [i][j] bf16 operand
+            for (int qi = tid; qi < C * 8; qi += kPrepThreads) {
+                const int i = qi >> 3, j0 = (qi & 7) * 8;
+                float y[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) y[t] = (j0 + t <= i) ? sX[i * C + j0 + t] * sB[j0 + t] : 0.0f;
+                *reinterpret_cast<uint4 *>(sC + sw128_off(i, j0, 64)) = pack8(y);
+            }
+        }
+        __syncthreads();
+
+        // 6. E^T = (exp(G) k_hat)^T and V^T operands in Z; W = T E, U = T V.
+        for (int qi = tid; qi < 8 * D; qi += kPrepThreads) {
+            const int c8 = qi >> 7, d = qi & (D - 1);
+            const float rho = sRho[(c8 >> 1) * D + d];
+            float e[8], vv[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int j = 8 * c8 + t;
+                e[t] = __bfloat162float(sKr[j * D + d]) * sRk[j] * sG[j * D + d] * rho;
+                vv[t] = __bfloat162float(sVr[j * D + d]);
+            }
+            *reinterpret_cast<uint4 *>(sZ + sw128_off(d, 8 * c8, 128)) = pack8(e);
+            *reinterpret_cast<uint4 *>(sZ + 16384 + sw128_off(d, 8 * c8, 128)) = pack8(vv);
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
         if (tid == 0) {
             tc_fence_after();
-            mma_tile<128, 64, 64>(tmem + 0, smem_u32(sE), 128, smem_u32(sT), 64, false);
-            mma_tile<128, 64, 64>(tmem + 64, smem_u32(sV), 128, smem_u32(sT), 64, false);
-            mma_commit(bar);
+            mma_tile<128, 128, 64>(tmem + 0, smem_u32(sC), 128, smem_u32(sZ), 128, false);
+            mma_tile<128, 128, 64>(tmem + 128, smem_u32(sC), 128, smem_u32(sZ + 16384), 128, false);
+            mma_commit(mbar);
         }
-        ok = mbar_wait(bar, phase);
+        ok = mbar_wait(mbar, mphase) && ok;
+        mphase ^= 1;
         tc_fence_after();
-    }
-    if (!__syncthreads_and(ok)) {
-        if (tid == 0) atomicOr(status, kStatusTimeout);
-        goto done;
-    }
+        if (!__syncthreads_and(ok)) break;
 
-    // 7. W (WQ rows 0..63) and U to the record.
-    {
-        const int quarter = warp & 3, col0 = (warp >> 2) * 32;
-        const int lrow = 32 * quarter + lane;  // key dim d for W, value dim for U
-        const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16);
-        float x[32];
-        tmem_ld32(ta + col0, x);
-        tmem_ld_wait();
+        // 7. W rows (WQ rows 0..63) and U to the record: TMEM lanes 0..63.
+        if ((warp & 3) < 2) {
+            const int i = 32 * (warp & 3) + lane, half = warp >> 2;
+            const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
 #pragma unroll
-        for (int ii = 0; ii < 32; ++ii) st_bf16(rec, TcRec::WQ + sw128_off(col0 + ii, lrow, 128), x[ii]);
-        tmem_ld32(ta + 64 + col0, x);
-        tmem_ld_wait();
-        __nv_bfloat16 *U = reinterpret_cast<__nv_bfloat16 *>(rec + TcRec::U);
+            for (int part = 0; part < 2; ++part) {
+                float x[32];
+                const int c0 = 64 * half + 32 * part;
+                tmem_ld32(ta + c0, x);
+                tmem_ld_wait();
 #pragma unroll
-        for (int ii = 0; ii < 32; ++ii) U[(col0 + ii) * D + lrow] = __float2bfloat16_rn(x[ii]);
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    float y[8];
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) y[t] = x[8 * c8 + t];
+                    *reinterpret_cast<uint4 *>(rec + TcRec::WQ + sw128_off(i, c0 + 8 * c8, 128)) = pack8(y);
+                }
+                tmem_ld32(ta + 128 + c0, x);
+                tmem_ld_wait();
+                unsigned char *ub = rec + TcRec::U + (c0 >> 5) * TcRec::UBLK + i * 64;
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    float y[8];
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) y[t] = x[8 * c8 + t];
+                    *reinterpret_cast<uint4 *>(ub + 16 * c8) = pack8(y);
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
     }
-
-done:
-    tc_fence_before();
-    __syncthreads();
+    if (!ok) {
+        if (tid == 0) {
+            atomicOr(status, kStatusTimeout);
+            // let copies still in flight land before the shared memory is released
+            mbar_wait(&full[0], 0, 400000000LL) || mbar_wait(&full[0], 1, 400000000LL);
+            mbar_wait(&full[1], 0, 400000000LL) || mbar_wait(&full[1], 1, 400000000LL);
+        }
+        __syncthreads();
+    }
     if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
 }
 
@@ -299,15 +526,33 @@ done:
 constexpr int kScanThreads = 128;
 constexpr int BV = 32;
 constexpr uint32_t kScanTmemCols = 64;
-constexpr uint32_t kStageBytes = TcRec::U;  // WQ | KDT | A | gC, copied in one piece
-constexpr int S_STAGE = 58368;              // kStageBytes rounded up to 1024
-constexpr int S_SOP = 2 * S_STAGE;          // S^T operand [32][128] bf16, 8 KB
-constexpr int S_VOP = S_SOP + 8192;         // Vn^T operand [32][64] bf16, 4 KB
-constexpr int S_BAR = S_VOP + 4096;         // full[2], mma
+constexpr int kStages = 3;
+constexpr uint32_t kImageBytes = TcRec::U;                   // WQ | KDT | A | gC
+constexpr uint32_t kStageBytes = kImageBytes + TcRec::UBLK;  // + this CTA's U block
+constexpr int S_STAGE = 62464;                               // kStageBytes rounded up to 1024
+constexpr int S_SOP = kStages * S_STAGE;                     // S^T operand [32][128] bf16, 8 KB
+constexpr int S_VOP = S_SOP + 8192;                          // Vn^T operand [32][64] bf16, 4 KB
+constexpr int S_BAR = S_VOP + 4096;                          // full[kStages], mma
 constexpr int S_BYTES = S_BAR + 64;
 constexpr int S_SMEM = S_BYTES + 1024;
 static_assert(kStageBytes <= (uint32_t)S_STAGE, "stage too small");
-static_assert(kStageBytes % 16 == 0, "bulk copy size");
+static_assert(kImageBytes % 16 == 0 && TcRec::UBLK % 16 == 0, "bulk copy size");
+
+// Write this thread's 32 values x[v] as column `col` of a K-major SW128 bf16
+// operand with 32 rows: neighbouring lanes (col even / odd) swap one value so
+// that each 32-bit store holds two adjacent columns of one row.  Whole warps.
+__device__ __forceinline__ void store_col_pairs(unsigned char *op, int col, const float (&x)[32]) {
+    const bool odd = col & 1;
+    const int ce = col & ~1;
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        const float send = odd ? x[2 * m] : x[2 * m + 1];
+        const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+        const float lo = odd ? recv : x[2 * m];
+        const float hi = odd ? x[2 * m + 1] : recv;
+        *reinterpret_cast<uint32_t *>(op + sw128_off(2 * m + (odd ? 1 : 0), ce, 32)) = pack2(lo, hi);
+    }
+}
 
 __global__ void __launch_bounds__(kScanThreads, 1)
     chunk_scan_tc_kernel(const float *__restrict__ initial_state, float *__restrict__ final_state,
@@ -318,10 +563,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     unsigned char *sS = sm + S_SOP;
     unsigned char *sVn = sm + S_VOP;
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + S_BAR);
-    uint64_t *mbar = full + 2;
+    uint64_t *mbar = full + kStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 1);
 
-    const int n = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * BV;
+    const int n = blockIdx.x, h = blockIdx.y, vb = blockIdx.z, v0 = vb * BV;
     const int tid = threadIdx.x, warp = tid >> 5;
     const int32_t start = ws_at<const int32_t>(workspace, L.seq_start_off)[n];
     if (start < 0) return;  // sequence skipped (bad cu_seqlens or slot)
@@ -333,11 +578,17 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     int32_t *status = ws_at<int32_t>(workspace, L.status_off);
     const unsigned char *recs = ws_at<const unsigned char>(workspace, L.records_off);
     auto rec_of = [&](int ck) { return recs + ((size_t)(c0 + ck) * H + h) * TcRec::bytes; };
+    auto issue = [&](int ck) {  // thread 0
+        const int s = ck % kStages;
+        unsigned char *dst = sm + s * S_STAGE;
+        mbar_arrive_expect_tx(&full[s], kStageBytes);
+        bulk_g2s(dst, rec_of(ck), kImageBytes, &full[s]);
+        bulk_g2s(dst + kImageBytes, rec_of(ck) + TcRec::U + vb * TcRec::UBLK, TcRec::UBLK, &full[s]);
+    };
 
     if (warp == 0) tmem_alloc(tmem_slot, kScanTmemCols);
     if (tid == 0) {
-        mbar_init(&full[0], 1);
-        mbar_init(&full[1], 1);
+        for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
         mbar_init(mbar, 1);
         fence_mbar_init();
     }
@@ -346,8 +597,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 #pragma unroll
     for (int x = 0; x < BV; ++x)
         S[x] = initial_state ? initial_state[st_off + (int64_t)(v0 + x) * D + tid] : 0.0f;
-#pragma unroll
-    for (int x = 0; x < BV; ++x) st_bf16(sS, sw128_off(x, tid, BV), S[x]);
+    store_col_pairs(sS, tid, S);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -356,33 +606,18 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     const uint32_t tD1 = tmem, tD3 = tmem + 32;
     const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
 
-    bool issued[2] = {false, false};
-    if (tid == 0 && nck > 0) {
-        mbar_arrive_expect_tx(&full[0], kStageBytes);
-        bulk_g2s(sm, rec_of(0), kStageBytes, &full[0]);
-        issued[0] = true;
+    if (tid == 0) {
+        for (int ck = 0; ck < kStages - 1 && ck < nck; ++ck) issue(ck);
     }
     uint32_t mphase = 0;
     bool ok = true;
     for (int ck = 0; ck < nck; ++ck) {
-        const int stage = ck & 1;
+        const int stage = ck % kStages;
         unsigned char *st = sm + stage * S_STAGE;
-        if (tid == 0 && ck + 1 < nck) {  // the other stage was released at the end of ck-1
-            mbar_arrive_expect_tx(&full[stage ^ 1], kStageBytes);
-            bulk_g2s(sm + (stage ^ 1) * S_STAGE, rec_of(ck + 1), kStageBytes, &full[stage ^ 1]);
-            issued[stage ^ 1] = true;
-        }
+        if (tid == 0 && ck + kStages - 1 < nck) issue(ck + kStages - 1);  // its stage was freed by ck-1
         const int valid = min(C, len - ck * C);
         const int64_t tok0 = (int64_t)start + (int64_t)ck * C;
-        // U row for this thread's chunk row (threads 0..63), fetched while waiting
-        uint4 u4[4];
-        if (tid < C) {
-            const uint4 *up = reinterpret_cast<const uint4 *>(rec_of(ck) + TcRec::U + (tid * D + v0) * 2);
-#pragma unroll
-            for (int x = 0; x < 4; ++x) u4[x] = up[x];
-        }
-        ok = mbar_wait(&full[stage], (ck >> 1) & 1) && ok;
-        if (tid == 0) issued[stage] = false;
+        ok = mbar_wait(&full[stage], (uint32_t)((ck / kStages) & 1)) && ok;
         if (!__syncthreads_and(ok)) break;
 
         // D1 = WQ * S
@@ -395,13 +630,20 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         mphase ^= 1;
         tc_fence_after();
         if (warp < 2) {  // rows 0..63: Vn = U - W S
-            float x[32];
+            float x[32], u[32];
             tmem_ld32(tD1 + lane_base, x);
-            tmem_ld_wait();
-            const __nv_bfloat16 *ub = reinterpret_cast<const __nv_bfloat16 *>(u4);
+            const uint4 *up = reinterpret_cast<const uint4 *>(st + kImageBytes + tid * 64);
 #pragma unroll
-            for (int vv = 0; vv < BV; ++vv)
-                st_bf16(sVn, sw128_off(vv, tid, BV), __bfloat162float(ub[vv]) - x[vv]);
+            for (int c8 = 0; c8 < 4; ++c8) {
+                float y[8];
+                unpack8(up[c8], y);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) u[8 * c8 + t] = y[t];
+            }
+            tmem_ld_wait();
+#pragma unroll
+            for (int vv = 0; vv < BV; ++vv) x[vv] = u[vv] - x[vv];
+            store_col_pairs(sVn, tid, x);
         }
         fence_async_smem();
         tc_fence_before();
@@ -423,25 +665,24 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             tmem_ld_wait();
             const int r = tid - 64;
             if (r < valid) {
-                uint4 pk[4];
-                __nv_bfloat16 *pb = reinterpret_cast<__nv_bfloat16 *>(pk);
-#pragma unroll
-                for (int vv = 0; vv < BV; ++vv) pb[vv] = __float2bfloat16_rn(x[vv]);
                 uint4 *op = reinterpret_cast<uint4 *>(o + ((tok0 + r) * H + h) * (int64_t)D + v0);
 #pragma unroll
-                for (int x4 = 0; x4 < 4; ++x4) op[x4] = pk[x4];
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    float y[8];
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) y[t] = x[8 * c8 + t];
+                    op[c8] = pack8(y);
+                }
             }
         }
         {  // S = diag(gC) S + KD^T Vn
             float x[32];
             tmem_ld32(tD3 + lane_base, x);
-            tmem_ld_wait();
             const float gc = reinterpret_cast<const float *>(st + TcRec::GC)[tid];
+            tmem_ld_wait();
 #pragma unroll
-            for (int vv = 0; vv < BV; ++vv) {
-                S[vv] = fmaf(gc, S[vv], x[vv]);
-                st_bf16(sS, sw128_off(vv, tid, BV), S[vv]);
-            }
+            for (int vv = 0; vv < BV; ++vv) S[vv] = fmaf(gc, S[vv], x[vv]);
+            store_col_pairs(sS, tid, S);
         }
         fence_async_smem();
         tc_fence_before();
@@ -451,8 +692,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         if (tid == 0) {
             atomicOr(status, kStatusTimeout);
             // let copies still in flight land before the shared memory is released
-            for (int s = 0; s < 2; ++s)
-                if (issued[s]) mbar_wait(&full[s], 0, 400000000LL) || mbar_wait(&full[s], 1, 400000000LL);
+            for (int s = 0; s < kStages; ++s)
+                mbar_wait(&full[s], 0, 400000000LL) || mbar_wait(&full[s], 1, 400000000LL);
         }
     } else if (final_state) {
 #pragma unroll
@@ -463,13 +704,26 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     if (warp == 0) tmem_dealloc(tmem, kScanTmemCols);
 }
 
+int sm_count() {
+    static int count[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!count[dev]) {
+        int c = 0;
+        cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
+        count[dev] = c > 0 ? c : 148;
+    }
+    return count[dev];
+}
+
 }  // namespace
 
 cudaError_t launch_chunk_prep_tc(const void *q, const void *k, const void *v, const float *g,
                                  const float *beta, int n_seqs, int64_t total_tokens, int H,
                                  float scale, void *workspace, cudaStream_t stream) {
     const WsLayout L = ws_layout(total_tokens, n_seqs, H, TcRec::bytes);
-    const dim3 grid((unsigned)max_chunks(total_tokens, n_seqs), (unsigned)H);
+    const int64_t items_max = max_chunks(total_tokens, n_seqs) * (int64_t)H;
+    const int grid = (int)std::min<int64_t>(items_max, (int64_t)sm_count());
     cudaFuncSetAttribute(chunk_prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
     chunk_prep_tc_kernel<<<grid, kPrepThreads, P_SMEM, stream>>>(
         (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, g, beta,

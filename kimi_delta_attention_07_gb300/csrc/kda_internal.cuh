@@ -101,23 +101,25 @@ struct F32Rec {
     static constexpr size_t bytes = floats * sizeof(float);
 };
 
-// bf16 tensor-core path: per (chunk, head) record.  The first kStage bytes
-// (WQ | KDT | A | gC) are the scan's shared-memory image of the chunk, in the
-// 128-byte-swizzled K-major operand layout; U follows, row-major.
+// bf16 tensor-core path: per (chunk, head) record.  WQ | KDT | A | gC is the
+// scan's shared-memory image of the chunk, in the 128-byte-swizzled K-major
+// operand layout; U follows, split in four 32-column blocks so that the scan
+// CTA of value block vb copies its 4 KB piece with one bulk copy.
 //   WQ  [128 rows][128 K] bf16: rows 0..63 W, rows 64..127 QG        32 KB
 //   KDT [128 rows (key)][64 K (chunk row)] bf16: KD^T                16 KB
 //   A   [64][64] bf16: causal scores (directly after KDT)             8 KB
 //   gC  [128] fp32: exp(G_last)
-//   U   [64][128] bf16 row-major                                     16 KB
+//   U   [4 value blocks][64 rows][32] bf16                           16 KB
 struct TcRec {
     static constexpr uint32_t WQ = 0;
     static constexpr uint32_t KDT = 32768;
     static constexpr uint32_t A = KDT + 16384;
     static constexpr uint32_t GC = A + 8192;
     static constexpr uint32_t U = GC + 512;
-    static constexpr uint32_t bytes = 74752;  // U + 16384, rounded up to 1024
+    static constexpr uint32_t UBLK = 64 * 32 * 2;  // one 32-column block of U
+    static constexpr uint32_t bytes = 74752;       // U + 16384, rounded up to 1024
 };
-static_assert(TcRec::U + 16384 <= TcRec::bytes, "TcRec layout");
+static_assert(TcRec::U + 4 * TcRec::UBLK <= TcRec::bytes, "TcRec layout");
 
 // ---- launchers (return cudaGetLastError() of the launch) ------------------
 
