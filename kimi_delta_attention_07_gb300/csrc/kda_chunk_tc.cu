@@ -40,7 +40,11 @@
 //   The 128-row A operand of the second MMA starts 8 KB before the A tile in
 //   the staged record (its rows 0..63 are the tail of KD^T and only feed D1
 //   rows that were already consumed).
+#include <cuda.h>  // CUtensorMap (the encoder is fetched through the runtime)
+#include <cudaTypedefs.h>
+
 #include <algorithm>
+#include <mutex>
 
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
@@ -110,7 +114,7 @@ constexpr int P_BAR = P_TAU + 6 * 512;    // full[2], mma barrier, tmem slot
 constexpr int P_BYTES = P_BAR + 64;
 constexpr int P_SMEM = P_BYTES + 1024;
 constexpr int LSTRIDE = 68;               // row stride (floats) of L in shared memory
-static_assert(C * LSTRIDE * 4 <= 32768, "L does not fit");
+static_assert(C * LSTRIDE * 4 <= 17408 && 22528 + 6 * 16 * 20 * 4 <= 32768, "Z scratch does not fit");
 
 __device__ __forceinline__ int tau_index(int br, int b) { return br * (br - 1) / 2 + b; }
 
@@ -132,11 +136,47 @@ __device__ __forceinline__ PrepItem prep_item(int item, int H, const int32_t *ch
     return it;
 }
 
+
+// Raw rows of one (chunk, head) item: q, k, v ([T, H, 128] bf16) and g
+// ([T, H, 128] fp32) through 3-D tensor maps {128, H, T}; one 128 x 1 x 64
+// box each, rows past the end of the tensor arrive as zeros.
+struct RawMaps {
+    CUtensorMap q, k, v, g;
+};
+
+__device__ __forceinline__ void load_raw(unsigned char *buf, const RawMaps &m, int h, int64_t tok0,
+                                         uint64_t *bar) {
+    mbar_arrive_expect_tx(bar, (uint32_t)R_BYTES);
+    tma_load_3d(buf + R_Q, &m.q, 0, h, (int)tok0, bar);
+    tma_load_3d(buf + R_K, &m.k, 0, h, (int)tok0, bar);
+    tma_load_3d(buf + R_V, &m.v, 0, h, (int)tok0, bar);
+    tma_load_3d(buf + R_G, &m.g, 0, h, (int)tok0, bar);
+}
+
+// 16x16 fp32 matrices of the inverse live with a row stride of 20 floats
+// (16-byte aligned rows, conflict-free row reads across 8 rows).
+constexpr int MS = 20;
+constexpr int MBLK = 16 * MS;  // floats per 16x16 matrix
+
+// Four outputs (row i, columns 4cg..4cg+3) of P = A * B for 16x16 matrices;
+// A read with stride lda, B with stride MS.
+__device__ __forceinline__ float4 mm16_row4(const float *A, int lda, const float *B, int i, int cg) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+        const float a = A[i * lda + kk];
+        const float4 b = *reinterpret_cast<const float4 *>(B + kk * MS + 4 * cg);
+        acc.x = fmaf(a, b.x, acc.x);
+        acc.y = fmaf(a, b.y, acc.y);
+        acc.z = fmaf(a, b.z, acc.z);
+        acc.w = fmaf(a, b.w, acc.w);
+    }
+    return acc;
+}
+
 __global__ void __launch_bounds__(kPrepThreads, 1)
-    chunk_prep_tc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-                         const __nv_bfloat16 *__restrict__ v, const float *__restrict__ g,
-                         const float *__restrict__ beta, int n_seqs, int H, float scale,
-                         void *workspace, WsLayout L) {
+    chunk_prep_tc_kernel(const __grid_constant__ RawMaps maps, const float *__restrict__ beta,
+                         int n_seqs, int H, float scale, void *workspace, WsLayout L) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     unsigned char *sZ = sm + P_Z;
@@ -171,23 +211,16 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // first item: expect its bytes, then rows 0..valid-1 are copied by threads 0..63
+    // first item
     PrepItem nxt = prep_item(blockIdx.x, H, chunk_off, seq_start, seq_len, n_seqs);
-    if (tid == 0) mbar_arrive_expect_tx(&full[0], (uint32_t)nxt.valid * 1280u);
-    __syncthreads();
+    if (tid == 0) load_raw(sm, maps, nxt.h, nxt.tok0, &full[0]);
     float beta_next = 0.0f;
-    if (tid < nxt.valid) {
-        const int64_t row = (nxt.tok0 + tid) * H + nxt.h;
-        bulk_g2s(sm + R_Q + tid * 256, q + row * D, 256, &full[0]);
-        bulk_g2s(sm + R_K + tid * 256, k + row * D, 256, &full[0]);
-        bulk_g2s(sm + R_V + tid * 256, v + row * D, 256, &full[0]);
-        bulk_g2s(sm + R_G + tid * 512, g + row * D, 512, &full[0]);
-        beta_next = beta[(nxt.tok0 + tid) * H + nxt.h];
-    }
+    if (tid < nxt.valid) beta_next = beta[(nxt.tok0 + tid) * H + nxt.h];
 
     uint32_t mphase = 0;
     bool ok = true;
     int m = 0;
+    KDA_PHASE_START();
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++m) {
         const PrepItem cur = nxt;
         const int buf = m & 1;
@@ -202,10 +235,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         if (tid < C) sB[tid] = tid < valid ? beta_next : 0.0f;
 
         const int nitem = item + gridDim.x;
-        if (nitem < n_items) {
-            nxt = prep_item(nitem, H, chunk_off, seq_start, seq_len, n_seqs);
-            if (tid == 0) mbar_arrive_expect_tx(&full[buf ^ 1], (uint32_t)nxt.valid * 1280u);
-        }
+        if (nitem < n_items) nxt = prep_item(nitem, H, chunk_off, seq_start, seq_len, n_seqs);
         ok = mbar_wait(&full[buf], (m >> 1) & 1) && ok;
         // zero the rows past the end of the sequence (not copied)
         for (int i = tid; i < (C - valid) * 16; i += kPrepThreads) {
@@ -218,27 +248,37 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             *reinterpret_cast<uint4 *>(raw + R_G + r * 512 + c16 * 32 + 16) = z;
         }
         if (!__syncthreads_and(ok)) break;
+        KDA_PHASE(0, 0);
         // prefetch the next item into the other buffer (its last reader was item m-1)
-        if (nitem < n_items && tid < nxt.valid) {
-            fence_async_smem();
-            const int64_t row = (nxt.tok0 + tid) * H + nxt.h;
-            unsigned char *nb = sm + (buf ^ 1) * R_BYTES;
-            bulk_g2s(nb + R_Q + tid * 256, q + row * D, 256, &full[buf ^ 1]);
-            bulk_g2s(nb + R_K + tid * 256, k + row * D, 256, &full[buf ^ 1]);
-            bulk_g2s(nb + R_V + tid * 256, v + row * D, 256, &full[buf ^ 1]);
-            bulk_g2s(nb + R_G + tid * 512, g + row * D, 512, &full[buf ^ 1]);
-            beta_next = beta[(nxt.tok0 + tid) * H + nxt.h];
+        if (nitem < n_items) {
+            if (tid == 0) {
+                fence_async_smem();
+                load_raw(sm + (buf ^ 1) * R_BYTES, maps, nxt.h, nxt.tok0, &full[buf ^ 1]);
+            }
+            if (tid < nxt.valid) beta_next = beta[(nxt.tok0 + tid) * H + nxt.h];
         }
 
-        // 1. row norms of q and k; cumulative log-decay in place (two halves).
-        for (int r = warp; r < C; r += 8) {
-            float a[8];
-            const uint2 qa = *reinterpret_cast<const uint2 *>(sQr + r * D + 4 * lane);
-            const uint2 ka = *reinterpret_cast<const uint2 *>(sKr + r * D + 4 * lane);
-            unpack8(make_uint4(qa.x, qa.y, ka.x, ka.y), a);
-            const float sq = warp_sum(a[0] * a[0] + a[1] * a[1] + a[2] * a[2] + a[3] * a[3]);
-            const float sk = warp_sum(a[4] * a[4] + a[5] * a[5] + a[6] * a[6] + a[7] * a[7]);
-            if (lane == 0) {
+        KDA_PHASE(0, 1);
+        // 1. row norms of q and k (16 lanes per row, 8 channels each); cumulative
+        //    log-decay in place (two halves).
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int r = 16 * it + (tid >> 4), c16 = tid & 15;
+            float a[8], b[8];
+            unpack8(*reinterpret_cast<const uint4 *>(sQr + r * D + 8 * c16), a);
+            unpack8(*reinterpret_cast<const uint4 *>(sKr + r * D + 8 * c16), b);
+            float sq = 0.f, sk = 0.f;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                sq = fmaf(a[t], a[t], sq);
+                sk = fmaf(b[t], b[t], sk);
+            }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            }
+            if (c16 == 0) {
                 sRq[r] = scale / sqrtf(sq + 1e-6f);
                 sRk[r] = 1.0f / sqrtf(sk + 1e-6f);
             }
@@ -281,6 +321,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
         __syncthreads();
 
+        KDA_PHASE(0, 2);
         // 2a. KD^T = (k_hat exp(G_last - G))^T, in 16-byte chunks of 8 chunk rows.
         for (int qi = tid; qi < 8 * D; qi += kPrepThreads) {
             const int c8 = qi >> 7, d = qi & (D - 1);
@@ -294,6 +335,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             *reinterpret_cast<uint4 *>(rec + TcRec::KDT + sw128_off(d, 8 * c8, 128)) = pack8(x);
         }
         __syncthreads();
+        KDA_PHASE(0, 3);
         // 2b. per (row, 8 channels): QG, column factors, then G -> l in place.
         for (int qi = tid; qi < C * 16; qi += kPrepThreads) {
             const int r = qi >> 4, d0 = (qi & 15) * 8, br = r >> 4;
@@ -316,6 +358,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             store8f(sG + r * D + d0, l8);
         }
 
+        KDA_PHASE(0, 4);
         // 3. A and L: one M=128 x N=16 x K=128 MMA per 16-column block.
         for (int b = 0; b < 4; ++b) {
             __syncthreads();  // l complete (b = 0) / previous MMA done with Z (b > 0)
@@ -351,8 +394,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             __syncthreads();
             if (tid == 0) {
                 tc_fence_after();
-                mma_tile<128, 16, 128>(tmem + 16 * b, smem_u32(sZ), 128, smem_u32(sC + b * 4096),
-                                       16, false);
+                mma_tile<128, 16, 128, 128, 16>(tmem + 16 * b, smem_u32(sZ), smem_u32(sC + b * 4096), false);
                 mma_commit(mbar);
             }
             ok = mbar_wait(mbar, mphase) && ok;
@@ -361,6 +403,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
         if (!__syncthreads_and(ok)) break;
 
+        KDA_PHASE(0, 5);
         // 4. A rows (TMEM lanes 0..63) to the record; beta-scaled L rows
         //    (lanes 64..127) to shared fp32.
         {
@@ -396,58 +439,144 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         tc_fence_before();
         __syncthreads();
 
-        // 5. X = (I + L)^-1 blockwise; T = X diag(beta) -> bf16 operand at sC.
+        KDA_PHASE(0, 6);
+        // 5. X = (I + L)^-1, L strictly lower (beta-scaled rows), in 16x16 blocks:
+        //    diagonal blocks X_bb = (I + N)^-1 = (I - N)(I + N^2)(I + N^4)(I + N^8)
+        //    (N = L_bb is nilpotent); then with M = X_D L_off (strictly block
+        //    lower, M^4 = 0): (I + L)^-1 = (I - M + M^2 - M^3) X_D.
+        //    T = X diag(beta) -> bf16 operand at sC.
         {
             const float *sL = reinterpret_cast<const float *>(sZ);
-            float *tmp = reinterpret_cast<float *>(sC + 8192);  // 3 x [16][16] fp32
-            if (warp < 4) {  // diagonal blocks: forward substitution, one warp each
-                const int o = 16 * warp, c = lane & 15, part = lane >> 4;
-                for (int r = 0; r < 16; ++r) {
-                    float acc = 0.0f;
-                    for (int mm = c + part; mm < r; mm += 2)
-                        acc = fmaf(sL[(o + r) * LSTRIDE + o + mm], sX[(o + mm) * C + o + c], acc);
-                    acc += __shfl_xor_sync(0xffffffffu, acc, 16);
-                    if (part == 0) sX[(o + r) * C + o + c] = (c == r) ? 1.0f : (c < r ? -acc : 0.0f);
-                    __syncwarp();
-                }
+            float *T1 = reinterpret_cast<float *>(sC);              // 4 blocks each (5 KB)
+            float *T2 = T1 + 4 * MBLK;
+            float *T3 = T2 + 4 * MBLK;
+            float *T4 = reinterpret_cast<float *>(sZ) + 64 * LSTRIDE;  // after L in Z
+            const int bb = tid >> 6, i = (tid & 63) >> 2, cg = tid & 3;
+            const int o = 16 * bb;
+            const float *N = sL + o * LSTRIDE + o;                   // L_bb, stride LSTRIDE
+            auto put = [](float *M_, int i_, int cg_, float4 x) {
+                *reinterpret_cast<float4 *>(M_ + i_ * MS + 4 * cg_) = x;
+            };
+            auto get = [](const float *M_, int i_, int cg_) {
+                return *reinterpret_cast<const float4 *>(M_ + i_ * MS + 4 * cg_);
+            };
+            // P2 = N N  -> T1 ; N as a MS-stride copy -> T4 (for products with N on the right)
+            {
+                float4 nn;
+                nn.x = N[i * LSTRIDE + 4 * cg + 0]; nn.y = N[i * LSTRIDE + 4 * cg + 1];
+                nn.z = N[i * LSTRIDE + 4 * cg + 2]; nn.w = N[i * LSTRIDE + 4 * cg + 3];
+                put(T4 + bb * MBLK, i, cg, nn);
             }
             __syncthreads();
-            const int er = tid >> 4, ec = tid & 15;
-            // level by level: X_ab = -X_aa * sum_{m=b}^{a-1} L_am X_mb
-            for (int lvl = 1; lvl < 4; ++lvl) {
-                const int nblk = 4 - lvl;
-                for (int t = 0; t < nblk; ++t) {
-                    const int a = t + lvl, b = t;
-                    float acc = 0.0f;
-                    for (int mb = b; mb < a; ++mb) {
-#pragma unroll 4
-                        for (int x = 0; x < 16; ++x)
-                            acc = fmaf(sL[(16 * a + er) * LSTRIDE + 16 * mb + x],
-                                       sX[(16 * mb + x) * C + 16 * b + ec], acc);
-                    }
-                    tmp[t * 256 + er * 16 + ec] = acc;
-                }
-                __syncthreads();
-                for (int t = 0; t < nblk; ++t) {
-                    const int a = t + lvl, b = t;
-                    float acc = 0.0f;
-                    for (int x = 0; x <= er; ++x)
-                        acc = fmaf(sX[(16 * a + er) * C + 16 * a + x], tmp[t * 256 + x * 16 + ec], acc);
-                    sX[(16 * a + er) * C + 16 * b + ec] = -acc;
-                }
-                __syncthreads();
+            put(T1 + bb * MBLK, i, cg, mm16_row4(N, LSTRIDE, T4 + bb * MBLK, i, cg));
+            __syncthreads();
+            // P4 = P2 P2 -> T2 ;  Y1 = I - N + P2 - N P2 -> T3
+            {
+                const float4 p4 = mm16_row4(T1 + bb * MBLK, MS, T1 + bb * MBLK, i, cg);
+                const float4 np2 = mm16_row4(N, LSTRIDE, T1 + bb * MBLK, i, cg);
+                const float4 p2 = get(T1 + bb * MBLK, i, cg);
+                const float4 n4 = get(T4 + bb * MBLK, i, cg);
+                float4 y;
+                y.x = (i == 4 * cg + 0 ? 1.f : 0.f) - n4.x + p2.x - np2.x;
+                y.y = (i == 4 * cg + 1 ? 1.f : 0.f) - n4.y + p2.y - np2.y;
+                y.z = (i == 4 * cg + 2 ? 1.f : 0.f) - n4.z + p2.z - np2.z;
+                y.w = (i == 4 * cg + 3 ? 1.f : 0.f) - n4.w + p2.w - np2.w;
+                put(T2 + bb * MBLK, i, cg, p4);
+                put(T3 + bb * MBLK, i, cg, y);
             }
+            __syncthreads();
+            // P8 = P4 P4 -> T1 ;  Y2 = Y1 + Y1 P4 -> T4
+            {
+                const float4 p8 = mm16_row4(T2 + bb * MBLK, MS, T2 + bb * MBLK, i, cg);
+                const float4 yp = mm16_row4(T3 + bb * MBLK, MS, T2 + bb * MBLK, i, cg);
+                const float4 y1 = get(T3 + bb * MBLK, i, cg);
+                put(T1 + bb * MBLK, i, cg, p8);
+                put(T4 + bb * MBLK, i, cg, make_float4(y1.x + yp.x, y1.y + yp.y, y1.z + yp.z, y1.w + yp.w));
+            }
+            __syncthreads();
+            // X_bb = Y2 + Y2 P8 -> sX diagonal block (stride 64) and T2 (stride MS)
+            {
+                const float4 yp = mm16_row4(T4 + bb * MBLK, MS, T1 + bb * MBLK, i, cg);
+                const float4 y2 = get(T4 + bb * MBLK, i, cg);
+                const float4 xd = make_float4(y2.x + yp.x, y2.y + yp.y, y2.z + yp.z, y2.w + yp.w);
+                *reinterpret_cast<float4 *>(sX + (o + i) * C + o + 4 * cg) = xd;
+                put(T2 + bb * MBLK, i, cg, xd);
+            }
+            __syncthreads();
+            KDA_PHASE(0, 7);
+            // Off-diagonal part.  Block pairs (a, b), a > b, indexed p = 0..5:
+            // (1,0) (2,0) (2,1) (3,0) (3,1) (3,2).  X_D blocks are in T2 (stride MS).
+            // Scratch: Z holds L in bytes [0, 17408) and the Y2 blocks in
+            // [17408, 22528); M goes after them, [22528, 30208).
+            const float *XD = T2;
+            float *Mb = reinterpret_cast<float *>(sZ + 22528);  // M_ab = X_aa L_ab, 6 blocks
+            float *M2 = T1;          // (M^2)_ab for (2,0) (3,1) (3,0)
+            float *M3 = T3;          // (M^3)_30
+            auto pair_a = [](int p) { return p < 1 ? 1 : (p < 3 ? 2 : 3); };
+            auto pair_b = [](int p, int a) { return p - a * (a - 1) / 2; };
+            for (int sl = tid; sl < 6 * 64; sl += kPrepThreads) {
+                const int p = sl >> 6, ii = (sl & 63) >> 2, cc = sl & 3;
+                const int a = pair_a(p), b = pair_b(p, a);
+                // X_aa (stride MS) times L_ab (stride LSTRIDE, needs a MS copy of B):
+                // compute directly: sum_k X_aa[ii][k] L[16a+k][16b + 4cc..]
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk) {
+                    const float x = XD[a * MBLK + ii * MS + kk];
+                    const float4 l = *reinterpret_cast<const float4 *>(sL + (16 * a + kk) * LSTRIDE + 16 * b + 4 * cc);
+                    acc.x = fmaf(x, l.x, acc.x); acc.y = fmaf(x, l.y, acc.y);
+                    acc.z = fmaf(x, l.z, acc.z); acc.w = fmaf(x, l.w, acc.w);
+                }
+                put(Mb + p * MBLK, ii, cc, acc);
+            }
+            __syncthreads();
+            // M^2: (2,0) = M21 M10 ; (3,1) = M32 M21 ; (3,0) = M31 M10 + M32 M20
+            for (int sl = tid; sl < 3 * 64; sl += kPrepThreads) {
+                const int p = sl >> 6, ii = (sl & 63) >> 2, cc = sl & 3;
+                float4 acc;
+                if (p == 0) acc = mm16_row4(Mb + 2 * MBLK, MS, Mb + 0 * MBLK, ii, cc);
+                else if (p == 1) acc = mm16_row4(Mb + 5 * MBLK, MS, Mb + 2 * MBLK, ii, cc);
+                else {
+                    const float4 a1 = mm16_row4(Mb + 4 * MBLK, MS, Mb + 0 * MBLK, ii, cc);
+                    const float4 a2 = mm16_row4(Mb + 5 * MBLK, MS, Mb + 1 * MBLK, ii, cc);
+                    acc = make_float4(a1.x + a2.x, a1.y + a2.y, a1.z + a2.z, a1.w + a2.w);
+                }
+                put(M2 + p * MBLK, ii, cc, acc);
+            }
+            __syncthreads();
+            // M^3: (3,0) = M32 (M^2)_20
+            if (tid < 64) put(M3, (tid & 63) >> 2, tid & 3, mm16_row4(Mb + 5 * MBLK, MS, M2 + 0 * MBLK, (tid & 63) >> 2, tid & 3));
+            __syncthreads();
+            // X_ab = (-M + M^2 - M^3)_ab X_bb
+            for (int sl = tid; sl < 6 * 64; sl += kPrepThreads) {
+                const int p = sl >> 6, ii = (sl & 63) >> 2, cc = sl & 3;
+                const int a = pair_a(p), b = pair_b(p, a);
+                const int p2 = (p == 1) ? 0 : (p == 4) ? 1 : (p == 3) ? 2 : -1;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk) {
+                    float z = -Mb[p * MBLK + ii * MS + kk];
+                    if (p2 >= 0) z += M2[p2 * MBLK + ii * MS + kk];
+                    if (p == 3) z -= M3[ii * MS + kk];
+                    const float4 xb = *reinterpret_cast<const float4 *>(XD + b * MBLK + kk * MS + 4 * cc);
+                    acc.x = fmaf(z, xb.x, acc.x); acc.y = fmaf(z, xb.y, acc.y);
+                    acc.z = fmaf(z, xb.z, acc.z); acc.w = fmaf(z, xb.w, acc.w);
+                }
+                *reinterpret_cast<float4 *>(sX + (16 * a + ii) * C + 16 * b + 4 * cc) = acc;
+            }
+            __syncthreads();
             // T = X diag(beta), lower triangle, as a K-major [i][j] bf16 operand
             for (int qi = tid; qi < C * 8; qi += kPrepThreads) {
-                const int i = qi >> 3, j0 = (qi & 7) * 8;
+                const int ri = qi >> 3, j0 = (qi & 7) * 8;
                 float y[8];
 #pragma unroll
-                for (int t = 0; t < 8; ++t) y[t] = (j0 + t <= i) ? sX[i * C + j0 + t] * sB[j0 + t] : 0.0f;
-                *reinterpret_cast<uint4 *>(sC + sw128_off(i, j0, 64)) = pack8(y);
+                for (int t = 0; t < 8; ++t) y[t] = (j0 + t <= ri) ? sX[ri * C + j0 + t] * sB[j0 + t] : 0.0f;
+                *reinterpret_cast<uint4 *>(sC + sw128_off(ri, j0, 64)) = pack8(y);
             }
         }
         __syncthreads();
 
+        KDA_PHASE(0, 8);
         // 6. E^T = (exp(G) k_hat)^T and V^T operands in Z; W = T E, U = T V.
         for (int qi = tid; qi < 8 * D; qi += kPrepThreads) {
             const int c8 = qi >> 7, d = qi & (D - 1);
@@ -467,8 +596,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         __syncthreads();
         if (tid == 0) {
             tc_fence_after();
-            mma_tile<128, 128, 64>(tmem + 0, smem_u32(sC), 128, smem_u32(sZ), 128, false);
-            mma_tile<128, 128, 64>(tmem + 128, smem_u32(sC), 128, smem_u32(sZ + 16384), 128, false);
+            mma_tile<128, 128, 64, 128, 128>(tmem + 0, smem_u32(sC), smem_u32(sZ), false);
+            mma_tile<128, 128, 64, 128, 128>(tmem + 128, smem_u32(sC), smem_u32(sZ + 16384), false);
             mma_commit(mbar);
         }
         ok = mbar_wait(mbar, mphase) && ok;
@@ -476,6 +605,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         tc_fence_after();
         if (!__syncthreads_and(ok)) break;
 
+        KDA_PHASE(0, 9);
         // 7. W rows (WQ rows 0..63) and U to the record: TMEM lanes 0..63.
         if ((warp & 3) < 2) {
             const int i = 32 * (warp & 3) + lane, half = warp >> 2;
@@ -507,6 +637,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
         tc_fence_before();
         __syncthreads();
+        KDA_PHASE(0, 10);
     }
     if (!ok) {
         if (tid == 0) {
@@ -542,15 +673,21 @@ static_assert(kImageBytes % 16 == 0 && TcRec::UBLK % 16 == 0, "bulk copy size");
 // operand with 32 rows: neighbouring lanes (col even / odd) swap one value so
 // that each 32-bit store holds two adjacent columns of one row.  Whole warps.
 __device__ __forceinline__ void store_col_pairs(unsigned char *op, int col, const float (&x)[32]) {
-    const bool odd = col & 1;
+    const int odd = col & 1;
     const int ce = col & ~1;
+    const int kk = ce & 63;
+    // element (row, ce) of the 32-row tile sits at
+    //   (ce / 64) * 4096 + row * 128 + (((kk / 8) ^ (row % 8)) * 16) + (kk % 8) * 2;
+    // for row = 2m + odd, (row % 8) = ((2m) % 8) | odd, hence the hoisted terms
+    unsigned char *base = op + (ce >> 6) * 4096 + odd * 128 + ((kk & 7) << 1);
+    const int cx = (kk >> 3) ^ odd;
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
         const float send = odd ? x[2 * m] : x[2 * m + 1];
         const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
         const float lo = odd ? recv : x[2 * m];
         const float hi = odd ? x[2 * m + 1] : recv;
-        *reinterpret_cast<uint32_t *>(op + sw128_off(2 * m + (odd ? 1 : 0), ce, 32)) = pack2(lo, hi);
+        *reinterpret_cast<uint32_t *>(base + 256 * m + ((cx ^ ((2 * m) & 7)) << 4)) = pack2(lo, hi);
     }
 }
 
@@ -578,7 +715,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     int32_t *status = ws_at<int32_t>(workspace, L.status_off);
     const unsigned char *recs = ws_at<const unsigned char>(workspace, L.records_off);
     auto rec_of = [&](int ck) { return recs + ((size_t)(c0 + ck) * H + h) * TcRec::bytes; };
-    auto issue = [&](int ck) {  // thread 0
+    auto issue = [&](int ck) {  // thread 32 (not the MMA-issuing thread)
         const int s = ck % kStages;
         unsigned char *dst = sm + s * S_STAGE;
         mbar_arrive_expect_tx(&full[s], kStageBytes);
@@ -606,29 +743,34 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     const uint32_t tD1 = tmem, tD3 = tmem + 32;
     const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
 
-    if (tid == 0) {
+    if (tid == 32) {
         for (int ck = 0; ck < kStages - 1 && ck < nck; ++ck) issue(ck);
     }
     uint32_t mphase = 0;
     bool ok = true;
+    KDA_PHASE_START();
     for (int ck = 0; ck < nck; ++ck) {
         const int stage = ck % kStages;
         unsigned char *st = sm + stage * S_STAGE;
-        if (tid == 0 && ck + kStages - 1 < nck) issue(ck + kStages - 1);  // its stage was freed by ck-1
+        if (tid == 32 && ck + kStages - 1 < nck) issue(ck + kStages - 1);  // its stage was freed by ck-1
         const int valid = min(C, len - ck * C);
         const int64_t tok0 = (int64_t)start + (int64_t)ck * C;
+        KDA_PHASE(1, 0);
         ok = mbar_wait(&full[stage], (uint32_t)((ck / kStages) & 1)) && ok;
         if (!__syncthreads_and(ok)) break;
+        KDA_PHASE(1, 1);
 
         // D1 = WQ * S
         if (tid == 0) {
             tc_fence_after();
-            mma_tile<128, BV, 128>(tD1, smem_u32(st + TcRec::WQ), 128, smem_u32(sS), BV, false);
+            mma_tile<128, BV, 128, 128, BV>(tD1, smem_u32(st + TcRec::WQ), smem_u32(sS), false);
             mma_commit(mbar);
         }
+        KDA_PHASE(1, 2);
         ok = mbar_wait(mbar, mphase) && ok;
         mphase ^= 1;
         tc_fence_after();
+        KDA_PHASE(1, 3);
         if (warp < 2) {  // rows 0..63: Vn = U - W S
             float x[32], u[32];
             tmem_ld32(tD1 + lane_base, x);
@@ -645,20 +787,24 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             for (int vv = 0; vv < BV; ++vv) x[vv] = u[vv] - x[vv];
             store_col_pairs(sVn, tid, x);
         }
+        KDA_PHASE(1, 4);
         fence_async_smem();
         tc_fence_before();
         if (!__syncthreads_and(ok)) break;
+        KDA_PHASE(1, 5);
 
         // D1 += [* ; A] * Vn ;  D3 = KD^T * Vn
         if (tid == 0) {
             tc_fence_after();
-            mma_tile<128, BV, 64>(tD1, smem_u32(st + TcRec::A) - 8192, 128, smem_u32(sVn), BV, true);
-            mma_tile<128, BV, 64>(tD3, smem_u32(st + TcRec::KDT), 128, smem_u32(sVn), BV, false);
+            mma_tile<128, BV, 64, 128, BV>(tD1, smem_u32(st + TcRec::A) - 8192, smem_u32(sVn), true);
+            mma_tile<128, BV, 64, 128, BV>(tD3, smem_u32(st + TcRec::KDT), smem_u32(sVn), false);
             mma_commit(mbar);
         }
+        KDA_PHASE(1, 6);
         ok = mbar_wait(mbar, mphase) && ok;
         mphase ^= 1;
         tc_fence_after();
+        KDA_PHASE(1, 7);
         if (warp >= 2) {  // rows 64..127: o
             float x[32];
             tmem_ld32(tD1 + lane_base, x);
@@ -684,12 +830,14 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             for (int vv = 0; vv < BV; ++vv) S[vv] = fmaf(gc, S[vv], x[vv]);
             store_col_pairs(sS, tid, S);
         }
+        KDA_PHASE(1, 8);
         fence_async_smem();
         tc_fence_before();
         if (!__syncthreads_and(ok)) break;
+        KDA_PHASE(1, 9);
     }
     if (!ok) {
-        if (tid == 0) {
+        if (tid == 32) {
             atomicOr(status, kStatusTimeout);
             // let copies still in flight land before the shared memory is released
             for (int s = 0; s < kStages; ++s)
@@ -718,16 +866,57 @@ int sm_count() {
 
 }  // namespace
 
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+// 3-D map {128, H, T} over a [T, H, 128] tensor; box 128 x 1 x 64.
+bool encode_rows(CUtensorMap *m, const void *base, CUtensorMapDataType dt, size_t elem, int H,
+                 int64_t T) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {(cuuint64_t)(D * elem), (cuuint64_t)(D * elem) * (cuuint64_t)H};
+    const cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)C};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 cudaError_t launch_chunk_prep_tc(const void *q, const void *k, const void *v, const float *g,
                                  const float *beta, int n_seqs, int64_t total_tokens, int H,
                                  float scale, void *workspace, cudaStream_t stream) {
     const WsLayout L = ws_layout(total_tokens, n_seqs, H, TcRec::bytes);
     const int64_t items_max = max_chunks(total_tokens, n_seqs) * (int64_t)H;
     const int grid = (int)std::min<int64_t>(items_max, (int64_t)sm_count());
+    RawMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    if (total_tokens > 0) {
+        if (!encode_rows(&maps.q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, total_tokens) ||
+            !encode_rows(&maps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, total_tokens) ||
+            !encode_rows(&maps.v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, total_tokens) ||
+            !encode_rows(&maps.g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, total_tokens))
+            return cudaErrorInvalidValue;
+    }
     cudaFuncSetAttribute(chunk_prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
-    chunk_prep_tc_kernel<<<grid, kPrepThreads, P_SMEM, stream>>>(
-        (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, g, beta,
-        n_seqs, H, scale, workspace, L);
+    chunk_prep_tc_kernel<<<grid, kPrepThreads, P_SMEM, stream>>>(maps, beta, n_seqs, H, scale,
+                                                                  workspace, L);
     return cudaGetLastError();
 }
 
@@ -744,3 +933,13 @@ cudaError_t launch_chunk_scan_tc(const float *initial_state, float *final_state,
 }
 
 }  // namespace kda
+
+#ifdef KDA_PHASE_TRACE
+extern "C" int kda_phase_read(unsigned long long *out) {
+    return (int)cudaMemcpyFromSymbol(out, kda_phase_cycles, sizeof(unsigned long long) * 64);
+}
+extern "C" int kda_phase_reset() {
+    unsigned long long z[64] = {0};
+    return (int)cudaMemcpyToSymbol(kda_phase_cycles, z, sizeof(z));
+}
+#endif

@@ -6,6 +6,29 @@
 
 #include <stdint.h>
 
+// Phase markers for cycle accounting of the first CTA's thread 0.  They
+// compile to nothing unless KDA_PHASE_TRACE is defined (this header is then
+// included by a single translation unit, which owns the counters).
+#ifdef KDA_PHASE_TRACE
+__device__ unsigned long long kda_phase_cycles[2][32];
+#define KDA_PHASE_START() long long kda_tprev_ = clock64()
+#define KDA_PHASE(kind, idx)                                                              \
+    do {                                                                                  \
+        if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0) {  \
+            const long long t_ = clock64();                                               \
+            kda_phase_cycles[kind][idx] += (unsigned long long)(t_ - kda_tprev_);         \
+            kda_tprev_ = t_;                                                              \
+        }                                                                                 \
+    } while (0)
+#else
+#define KDA_PHASE_START() \
+    do {                  \
+    } while (0)
+#define KDA_PHASE(kind, idx) \
+    do {                     \
+    } while (0)
+#endif
+
 namespace kda {
 namespace tc {
 
@@ -58,6 +81,18 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
             smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// ---- TMA tensor copy (3-D tile, global -> shared, completes on an mbarrier) ----------
+// tmap: generic address of a CUtensorMap kernel parameter; c0 (innermost) must
+// keep the copied row 16-byte aligned (here always 0).
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int c0, int c1, int c2,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
         : "memory");
 }
 
@@ -158,17 +193,28 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// High 32 bits of every SW128 K-major descriptor used here (stride byte
+// offset 1024, tcgen05 version bit, 128-byte swizzle); see sw128_desc.
+constexpr uint32_t kDescHi = (uint32_t)(1024 >> 4) | (1u << 14) | (2u << 29);
+
+__device__ __forceinline__ uint32_t sw128_desc_lo(uint32_t saddr) {
+    return ((saddr & 0x3FFFFu) >> 4) | (1u << 16);
+}
+
 // D[M x N] (+)= A[M x K] * B[N x K]^T, both operands K-major SW128 tiles with
-// a_rows / b_rows rows per K-block; issued by one thread.
-template <int M, int N, int K>
-__device__ __forceinline__ void mma_tile(uint32_t d_tmem, uint32_t a_saddr, int a_rows,
-                                         uint32_t b_saddr, int b_rows, bool accumulate) {
+// AROWS / BROWS rows per K-block; issued by one thread.  The descriptors of
+// the K steps differ only in their low word (start address), by constants.
+template <int M, int N, int K, int AROWS, int BROWS>
+__device__ __forceinline__ void mma_tile(uint32_t d_tmem, uint32_t a_saddr, uint32_t b_saddr,
+                                         bool accumulate) {
     constexpr uint32_t idesc = idesc_bf16(M, N);
+    const uint32_t alo = sw128_desc_lo(a_saddr), blo = sw128_desc_lo(b_saddr);
 #pragma unroll
     for (int s = 0; s < K / 16; ++s) {
-        const uint32_t kb = (uint32_t)(s >> 2), within = (uint32_t)((s & 3) * 32);
-        const uint64_t ad = sw128_desc(a_saddr + kb * (uint32_t)a_rows * 128u + within);
-        const uint64_t bd = sw128_desc(b_saddr + kb * (uint32_t)b_rows * 128u + within);
+        const uint32_t ka = (uint32_t)((s >> 2) * AROWS * 8 + (s & 3) * 2);
+        const uint32_t kb = (uint32_t)((s >> 2) * BROWS * 8 + (s & 3) * 2);
+        const uint64_t ad = ((uint64_t)kDescHi << 32) | (uint64_t)(alo + ka);
+        const uint64_t bd = ((uint64_t)kDescHi << 32) | (uint64_t)(blo + kb);
         mma_bf16(d_tmem, ad, bd, idesc, (accumulate || s > 0) ? 1u : 0u);
     }
 }
