@@ -5,25 +5,29 @@
 // _torch_chunk_kda), with every dense contraction on the 5th-generation
 // tensor cores.
 //
-// prep -- persistent, one CTA per SM walking the (chunk, head) items; the raw
-// q, k, v, g rows of the next item are bulk-copied into a second shared
-// buffer while the current item is computed:
+// prep -- persistent, one CTA (16 warps) per SM walking the (chunk, head)
+// items; the raw q, k, v, g tiles of an item arrive by TMA, and the next
+// item's tiles are requested as soon as the current ones are consumed:
 //   * q_hat = scale * l2norm(q), k_hat = l2norm(k) (fp32), G = cumsum(g).
 //   * G is replaced in place by l_r = exp(G_r - G_{16 br}) (br = r's 16-row
-//     block) and per-channel block factors rho_b = exp(G_{16b}) and
-//     tau_{br,b} = exp(G_{16br} - G_{16b}); every exponent is <= 0, and
-//     exp(G_r - G_{16b}) = l_r * tau_{br,b}, exp(G_r) = l_r * rho_br.
-//   * Causal scores A[r,j] and the interaction matrix L[r,j] as ONE M=128 MMA
-//     per 16-column block b: rows 0..63 of the A operand are
-//     q_hat_r * exp(G_r - G_16b), rows 64..127 k_hat_r * exp(G_r - G_16b)
-//     (zero for r < 16b), the B operand is k_hat_j * exp(G_16b - G_j) for the
-//     16 keys of block b.  For every kept pair (j <= r) the row factor is
-//     <= 1 and the column factor at most exp(15 * max|g|); the column
-//     exponent is clamped at 80, which only matters for per-token decays
-//     below about -5.3 and then only for masked pairs.
-//   * X = (I + beta L)^-1 blockwise in fp32 (16x16 diagonal blocks by forward
-//     substitution, one warp each, then three levels of 16x16 products);
-//     T = X diag(beta).
+//     block); rho_b = exp(G_{16b}), so exp(G_r) = l_r * rho_br.  Every
+//     exponent here is <= 0.
+//   * Causal scores A[r,j] and the interaction matrix L[r,j] come from ONE
+//     M=128 x N=160 x K=128 MMA: the A operand is [q_hat l ; k_hat l] (row
+//     r referenced to its own block start), the B operand stacks, for the
+//     10 (row block br, column block b) pairs with br >= b, the 16 rows
+//     k_hat_j * exp(G_{16br} - G_j), j in block b.  Row r of block br finds
+//     its columns j < 16(br+1) side by side.  Off the block diagonal both
+//     factors are <= 1; on it the column factor is at most exp(15 max|g|),
+//     its exponent clamped at 80 (only reached for per-token decays below
+//     about -5.3, and then only for masked pairs).
+//   * X = (I + beta L)^-1 blockwise in fp32: 16x16 diagonal blocks by
+//     forward substitution (one column per lane), the rest as
+//     (I - M + M^2 - M^3) X_D with M = X_D L_off; T = X diag(beta).
+//   * The stacked column operand and T enter their MMAs as hi + lo bf16
+//     pairs (two accumulating MMAs), which keeps the WY transform accurate
+//     when keys are strongly correlated and the later subtraction U - W S
+//     cancels.
 //   * W = T (exp(G) k_hat) and U = T v as M=128 x N=128 x K=64 MMAs whose A
 //     operand is [T ; scratch] (rows 64..127 unused), so each thread of
 //     TMEM lanes 0..63 holds whole rows of W and U.
@@ -94,29 +98,40 @@ __device__ __forceinline__ void store8f(float *p, const float (&x)[8]) {
 // ---------------------------------------------------------------------------
 // prep
 // ---------------------------------------------------------------------------
-constexpr int kPrepThreads = 256;
+constexpr int kPrepThreads = 512;
 constexpr uint32_t kPrepTmemCols = 256;
-// one item's raw rows (double-buffered)
-constexpr int R_Q = 0;          // bf16 [64][128]; after the A/L MMAs: X fp32 [64][64]
+constexpr int NPAIR = 10;      // (row block br, column block b) pairs with br >= b
+constexpr int NST = 16 * NPAIR;  // 160 = N of the stacked A/L MMA
+// shared memory plan (offsets from a 1024-aligned base)
+constexpr int R_Q = 0;          // bf16 [64][128]; after the A/L MMA: X fp32 [64][64]
 constexpr int R_K = 16384;      // bf16 [64][128]
 constexpr int R_V = 32768;      // bf16 [64][128]
 constexpr int R_G = 49152;      // fp32 [64][128]: g -> G -> l
 constexpr int R_BYTES = 81920;
-constexpr int P_Z = 2 * R_BYTES;          // 32 KB: A_b operand | L fp32 (stride 68) | E^T, V^T
-constexpr int P_C = P_Z + 32768;          // 16 KB: column-factor operands | [T ; temps]
-constexpr int P_RQ = P_C + 16384;         // fp32 [64]
+constexpr int P_XL = R_BYTES;             // 32 KB: [q_hat l ; k_hat l] | L fp32 + scratch | E^T, V^T
+constexpr int P_BS = P_XL + 32768;        // 40 KB: stacked column operand | inverse scratch, T
+constexpr int P_T = P_BS + 16384;         // T operand [64][64] bf16; the MMA reads 16 KB from here
+constexpr int P_RQ = P_BS + 40960;        // fp32 [64]
 constexpr int P_RK = P_RQ + 256;          // fp32 [64]
 constexpr int P_BETA = P_RK + 256;        // fp32 [64]
 constexpr int P_GREF = P_BETA + 256;      // fp32 [5][128]: G at rows 0, 16, 32, 48, 63
 constexpr int P_RHO = P_GREF + 5 * 512;   // fp32 [4][128]: exp(G_16b)
 constexpr int P_TAU = P_RHO + 4 * 512;    // fp32 [6][128]: exp(G_16br - G_16b), br > b
-constexpr int P_BAR = P_TAU + 6 * 512;    // full[2], mma barrier, tmem slot
-constexpr int P_BYTES = P_BAR + 64;
+constexpr int P_QSUM = P_TAU + 6 * 512;   // fp32 [4][128]: per-quarter sums of g
+constexpr int P_BAR = P_QSUM + 4 * 512;   // full, mma barrier, tmem slot
+constexpr int P_BS2 = (P_BAR + 64 + 1023) / 1024 * 1024;  // 40 KB: low part of the stacked operand
+constexpr int P_BYTES = P_BS2 + 40960;
 constexpr int P_SMEM = P_BYTES + 1024;
 constexpr int LSTRIDE = 68;               // row stride (floats) of L in shared memory
-static_assert(C * LSTRIDE * 4 <= 17408 && 22528 + 6 * 16 * 20 * 4 <= 32768, "Z scratch does not fit");
+constexpr int MS = 20;                    // row stride (floats) of 16x16 scratch matrices
+constexpr int MBLK = 16 * MS;             // floats per 16x16 scratch matrix
+static_assert(P_T + 8192 + 16384 <= P_BS + 40960, "T_hi / T_lo operand windows");
+static_assert(3 * 4 * MBLK * 4 <= P_T - P_BS, "inverse scratch vs T");
+static_assert(C * LSTRIDE * 4 + 4 * MBLK * 4 + 6 * MBLK * 4 <= 32768, "XL scratch");
 
 __device__ __forceinline__ int tau_index(int br, int b) { return br * (br - 1) / 2 + b; }
+// first column of row block br in the stacked A/L result (pairs (br, 0..br) are consecutive)
+__device__ __forceinline__ int pair_col0(int br) { return 8 * br * (br + 1); }
 
 struct PrepItem {
     int64_t tok0;
@@ -136,7 +151,6 @@ __device__ __forceinline__ PrepItem prep_item(int item, int H, const int32_t *ch
     return it;
 }
 
-
 // Raw rows of one (chunk, head) item: q, k, v ([T, H, 128] bf16) and g
 // ([T, H, 128] fp32) through 3-D tensor maps {128, H, T}; one 128 x 1 x 64
 // box each, rows past the end of the tensor arrive as zeros.
@@ -153,25 +167,34 @@ __device__ __forceinline__ void load_raw(unsigned char *buf, const RawMaps &m, i
     tma_load_3d(buf + R_G, &m.g, 0, h, (int)tok0, bar);
 }
 
-// 16x16 fp32 matrices of the inverse live with a row stride of 20 floats
-// (16-byte aligned rows, conflict-free row reads across 8 rows).
-constexpr int MS = 20;
-constexpr int MBLK = 16 * MS;  // floats per 16x16 matrix
+// Row i of a 16x16 fp32 matrix (row stride lda floats, 16-byte aligned rows).
+__device__ __forceinline__ void row16(const float *A, int lda, int i, float (&a)[16]) {
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+        const float4 x = *reinterpret_cast<const float4 *>(A + i * lda + 4 * q4);
+        a[4 * q4] = x.x; a[4 * q4 + 1] = x.y; a[4 * q4 + 2] = x.z; a[4 * q4 + 3] = x.w;
+    }
+}
 
-// Four outputs (row i, columns 4cg..4cg+3) of P = A * B for 16x16 matrices;
-// A read with stride lda, B with stride MS.
-__device__ __forceinline__ float4 mm16_row4(const float *A, int lda, const float *B, int i, int cg) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+// Two outputs (row a[], columns 2c2, 2c2+1) of a * B, B a 16x16 matrix with
+// stride MS; every load is issued before the first FMA.
+__device__ __forceinline__ float2 row_times(const float (&a)[16], const float *B, int c2) {
+    float2 b[16];
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) b[kk] = *reinterpret_cast<const float2 *>(B + kk * MS + 2 * c2);
+    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) {
-        const float a = A[i * lda + kk];
-        const float4 b = *reinterpret_cast<const float4 *>(B + kk * MS + 4 * cg);
-        acc.x = fmaf(a, b.x, acc.x);
-        acc.y = fmaf(a, b.y, acc.y);
-        acc.z = fmaf(a, b.z, acc.z);
-        acc.w = fmaf(a, b.w, acc.w);
+        acc.x = fmaf(a[kk], b[kk].x, acc.x);
+        acc.y = fmaf(a[kk], b[kk].y, acc.y);
     }
     return acc;
+}
+
+__device__ __forceinline__ float2 mm16_row2(const float *A, int lda, const float *B, int i, int c2) {
+    float a[16];
+    row16(A, lda, i, a);
+    return row_times(a, B, c2);
 }
 
 __global__ void __launch_bounds__(kPrepThreads, 1)
@@ -179,17 +202,25 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                          int n_seqs, int H, float scale, void *workspace, WsLayout L) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    unsigned char *sZ = sm + P_Z;
-    unsigned char *sC = sm + P_C;
+    unsigned char *sXL = sm + P_XL;
+    unsigned char *sBS = sm + P_BS;
+    unsigned char *sT = sm + P_T;          // T_hi; T_lo follows 8 KB later
+    unsigned char *sBS2 = sm + P_BS2;
     float *sRq = reinterpret_cast<float *>(sm + P_RQ);
     float *sRk = reinterpret_cast<float *>(sm + P_RK);
     float *sB = reinterpret_cast<float *>(sm + P_BETA);
     float *sGref = reinterpret_cast<float *>(sm + P_GREF);
     float *sRho = reinterpret_cast<float *>(sm + P_RHO);
     float *sTau = reinterpret_cast<float *>(sm + P_TAU);
+    float *sQsum = reinterpret_cast<float *>(sm + P_QSUM);
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + P_BAR);
-    uint64_t *mbar = full + 2;
+    uint64_t *mbar = full + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 1);
+    const __nv_bfloat16 *sQr = reinterpret_cast<const __nv_bfloat16 *>(sm + R_Q);
+    const __nv_bfloat16 *sKr = reinterpret_cast<const __nv_bfloat16 *>(sm + R_K);
+    const __nv_bfloat16 *sVr = reinterpret_cast<const __nv_bfloat16 *>(sm + R_V);
+    float *sG = reinterpret_cast<float *>(sm + R_G);
+    float *sX = reinterpret_cast<float *>(sm + R_Q);  // after the q rows are consumed
 
     const int32_t *chunk_off = ws_at<const int32_t>(workspace, L.chunk_off_off);
     const int32_t *seq_start = ws_at<const int32_t>(workspace, L.seq_start_off);
@@ -201,8 +232,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (warp == 0) tmem_alloc(tmem_slot, kPrepTmemCols);
     if (tid == 32) {
-        mbar_init(&full[0], 1);
-        mbar_init(&full[1], 1);
+        mbar_init(full, 1);
         mbar_init(mbar, 1);
         fence_mbar_init();
     }
@@ -211,59 +241,47 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // first item
-    PrepItem nxt = prep_item(blockIdx.x, H, chunk_off, seq_start, seq_len, n_seqs);
-    if (tid == 0) load_raw(sm, maps, nxt.h, nxt.tok0, &full[0]);
-    float beta_next = 0.0f;
-    if (tid < nxt.valid) beta_next = beta[(nxt.tok0 + tid) * H + nxt.h];
+    // item metadata runs one item ahead of the loads, which run one item ahead
+    // of the compute
+    int item = blockIdx.x;
+    PrepItem cur = prep_item(item, H, chunk_off, seq_start, seq_len, n_seqs);
+    if (tid == 0) load_raw(sm, maps, cur.h, cur.tok0, full);
+    float beta_cur = tid < cur.valid ? beta[(cur.tok0 + tid) * H + cur.h] : 0.0f;
+    PrepItem nxt = cur;
+    if (item + (int)gridDim.x < n_items)
+        nxt = prep_item(item + gridDim.x, H, chunk_off, seq_start, seq_len, n_seqs);
 
-    uint32_t mphase = 0;
+    uint32_t fphase = 0, mphase = 0;
     bool ok = true;
-    int m = 0;
     KDA_PHASE_START();
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++m) {
-        const PrepItem cur = nxt;
-        const int buf = m & 1;
-        unsigned char *raw = sm + buf * R_BYTES;
-        const __nv_bfloat16 *sQr = reinterpret_cast<const __nv_bfloat16 *>(raw + R_Q);
-        const __nv_bfloat16 *sKr = reinterpret_cast<const __nv_bfloat16 *>(raw + R_K);
-        const __nv_bfloat16 *sVr = reinterpret_cast<const __nv_bfloat16 *>(raw + R_V);
-        float *sG = reinterpret_cast<float *>(raw + R_G);
-        float *sX = reinterpret_cast<float *>(raw + R_Q);  // after the q rows are consumed
+    for (; item < n_items; item += gridDim.x) {
+        const bool has_next = item + (int)gridDim.x < n_items;
         unsigned char *rec = ws_at<unsigned char>(workspace, L.records_off + ((size_t)cur.c * H + cur.h) * TcRec::bytes);
         const int valid = cur.valid;
-        if (tid < C) sB[tid] = tid < valid ? beta_next : 0.0f;
+        if (tid < C) sB[tid] = tid < valid ? beta_cur : 0.0f;
+        float beta_nxt = 0.0f;
+        PrepItem nn = nxt;
 
-        const int nitem = item + gridDim.x;
-        if (nitem < n_items) nxt = prep_item(nitem, H, chunk_off, seq_start, seq_len, n_seqs);
-        ok = mbar_wait(&full[buf], (m >> 1) & 1) && ok;
-        // zero the rows past the end of the sequence (not copied)
+        ok = mbar_wait(full, fphase) && ok;
+        fphase ^= 1;
+        // rows past the end of the sequence: zero (the tensor map only zero-fills past T)
         for (int i = tid; i < (C - valid) * 16; i += kPrepThreads) {
             const int r = valid + i / 16, c16 = i % 16;
             const uint4 z = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4 *>(raw + R_Q + r * 256 + c16 * 16) = z;
-            *reinterpret_cast<uint4 *>(raw + R_K + r * 256 + c16 * 16) = z;
-            *reinterpret_cast<uint4 *>(raw + R_V + r * 256 + c16 * 16) = z;
-            *reinterpret_cast<uint4 *>(raw + R_G + r * 512 + c16 * 32) = z;
-            *reinterpret_cast<uint4 *>(raw + R_G + r * 512 + c16 * 32 + 16) = z;
+            *reinterpret_cast<uint4 *>(sm + R_Q + r * 256 + c16 * 16) = z;
+            *reinterpret_cast<uint4 *>(sm + R_K + r * 256 + c16 * 16) = z;
+            *reinterpret_cast<uint4 *>(sm + R_V + r * 256 + c16 * 16) = z;
+            *reinterpret_cast<uint4 *>(sm + R_G + r * 512 + c16 * 32) = z;
+            *reinterpret_cast<uint4 *>(sm + R_G + r * 512 + c16 * 32 + 16) = z;
         }
         if (!__syncthreads_and(ok)) break;
         KDA_PHASE(0, 0);
-        // prefetch the next item into the other buffer (its last reader was item m-1)
-        if (nitem < n_items) {
-            if (tid == 0) {
-                fence_async_smem();
-                load_raw(sm + (buf ^ 1) * R_BYTES, maps, nxt.h, nxt.tok0, &full[buf ^ 1]);
-            }
-            if (tid < nxt.valid) beta_next = beta[(nxt.tok0 + tid) * H + nxt.h];
-        }
 
-        KDA_PHASE(0, 1);
-        // 1. row norms of q and k (16 lanes per row, 8 channels each); cumulative
-        //    log-decay in place (two halves).
+        // 1. row norms of q and k (16 lanes per row, 8 channels each) and the
+        //    cumulative log-decay (4 row quarters per channel, then offsets).
 #pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int r = 16 * it + (tid >> 4), c16 = tid & 15;
+        for (int it = 0; it < 2; ++it) {
+            const int r = 32 * it + (tid >> 4), c16 = tid & 15;
             float a[8], b[8];
             unpack8(*reinterpret_cast<const uint4 *>(sQr + r * D + 8 * c16), a);
             unpack8(*reinterpret_cast<const uint4 *>(sKr + r * D + 8 * c16), b);
@@ -284,26 +302,21 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             }
         }
         {
-            const int d = tid & (D - 1), r0 = (tid >> 7) * 32;
-            float x[32];
+            const int d = tid & (D - 1), qtr = tid >> 7, r0 = 16 * qtr;
+            float x[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) x[i] = sG[(r0 + i) * D + d];
+            for (int i = 0; i < 16; ++i) x[i] = sG[(r0 + i) * D + d];
 #pragma unroll
-            for (int i = 1; i < 32; ++i) x[i] += x[i - 1];
-            if (!r0) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) sG[i * D + d] = x[i];
-            }
+            for (int i = 1; i < 16; ++i) x[i] += x[i - 1];
+            sQsum[qtr * D + d] = x[15];
             __syncthreads();
-            if (r0) {
-                const float base = sG[31 * D + d];
+            float off = 0.0f;
+            for (int q2 = 0; q2 < qtr; ++q2) off += sQsum[q2 * D + d];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) sG[(r0 + i) * D + d] = x[i] + base;
-            }
+            for (int i = 0; i < 16; ++i) sG[(r0 + i) * D + d] = x[i] + off;
         }
         __syncthreads();
-        // reference rows and block factors (threads 0..127: one key channel each)
-        if (tid < D) {
+        if (tid < D) {  // reference rows and block factors, one key channel each
             const int d = tid;
             float gb[4];
 #pragma unroll
@@ -312,17 +325,19 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                 sGref[b * D + d] = gb[b];
                 sRho[b * D + d] = __expf(gb[b]);
             }
-            sGref[4 * D + d] = sG[(C - 1) * D + d];
+            const float gl = sG[(C - 1) * D + d];
+            sGref[4 * D + d] = gl;
 #pragma unroll
             for (int br = 1; br < 4; ++br)
 #pragma unroll
                 for (int b = 0; b < br; ++b) sTau[tau_index(br, b) * D + d] = __expf(gb[br] - gb[b]);
-            reinterpret_cast<float *>(rec + TcRec::GC)[d] = __expf(sG[(C - 1) * D + d]);
+            reinterpret_cast<float *>(rec + TcRec::GC)[d] = __expf(gl);
         }
         __syncthreads();
+        KDA_PHASE(0, 1);
 
-        KDA_PHASE(0, 2);
-        // 2a. KD^T = (k_hat exp(G_last - G))^T, in 16-byte chunks of 8 chunk rows.
+        // 2. passes that read G itself: KD^T (column chunks) and the stacked
+        //    column operand k_hat_j * exp(G_16br - G_j) for the 10 pairs.
         for (int qi = tid; qi < 8 * D; qi += kPrepThreads) {
             const int c8 = qi >> 7, d = qi & (D - 1);
             const float gl = sGref[4 * D + d];
@@ -334,9 +349,30 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             }
             *reinterpret_cast<uint4 *>(rec + TcRec::KDT + sw128_off(d, 8 * c8, 128)) = pack8(x);
         }
+        for (int qi = tid; qi < NST * 16; qi += kPrepThreads) {
+            const int p = qi >> 8, jj = (qi >> 4) & 15, d0 = (qi & 15) * 8;
+            const int br = p >= 6 ? 3 : (p >= 3 ? 2 : (p >= 1 ? 1 : 0));
+            const int b = p - br * (br + 1) / 2, j = 16 * b + jj;
+            float G8[8], Gb8[8], kv[8], y[8];
+            load8f(sG + j * D + d0, G8);
+            load8f(sGref + br * D + d0, Gb8);
+            unpack8(*reinterpret_cast<const uint4 *>(sKr + j * D + d0), kv);
+            const float rk = sRk[j];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) y[t] = kv[t] * rk * __expf(fminf(Gb8[t] - G8[t], 80.0f));
+            // hi + lo bf16 parts: the MMA sees this operand to ~16 bits
+            const uint4 hi = pack8(y);
+            float lo[8];
+            unpack8(hi, lo);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) lo[t] = y[t] - lo[t];
+            *reinterpret_cast<uint4 *>(sBS + sw128_off(16 * p + jj, d0, NST)) = hi;
+            *reinterpret_cast<uint4 *>(sBS2 + sw128_off(16 * p + jj, d0, NST)) = pack8(lo);
+        }
         __syncthreads();
-        KDA_PHASE(0, 3);
-        // 2b. per (row, 8 channels): QG, column factors, then G -> l in place.
+        KDA_PHASE(0, 2);
+        // 3. per (row, 8 channels): l = exp(G - G_16br) in place, QG to the
+        //    record, and the row operand [q_hat l ; k_hat l].
         for (int qi = tid; qi < C * 16; qi += kPrepThreads) {
             const int r = qi >> 4, d0 = (qi & 15) * 8, br = r >> 4;
             float G8[8], Gb8[8], rho8[8], qv[8], kv[8];
@@ -346,238 +382,217 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             unpack8(*reinterpret_cast<const uint4 *>(sQr + r * D + d0), qv);
             unpack8(*reinterpret_cast<const uint4 *>(sKr + r * D + d0), kv);
             const float rq = sRq[r], rk = sRk[r];
-            float qg[8], cf[8], l8[8];
+            float qg[8], ql[8], kl[8], l8[8];
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
                 l8[t] = __expf(G8[t] - Gb8[t]);
-                qg[t] = qv[t] * rq * l8[t] * rho8[t];
-                cf[t] = kv[t] * rk * __expf(fminf(Gb8[t] - G8[t], 80.0f));
+                ql[t] = qv[t] * rq * l8[t];
+                kl[t] = kv[t] * rk * l8[t];
+                qg[t] = ql[t] * rho8[t];
             }
             *reinterpret_cast<uint4 *>(rec + TcRec::WQ + sw128_off(64 + r, d0, 128)) = pack8(qg);
-            *reinterpret_cast<uint4 *>(sC + br * 4096 + sw128_off(r & 15, d0, 16)) = pack8(cf);
+            *reinterpret_cast<uint4 *>(sXL + sw128_off(r, d0, 128)) = pack8(ql);
+            *reinterpret_cast<uint4 *>(sXL + sw128_off(64 + r, d0, 128)) = pack8(kl);
             store8f(sG + r * D + d0, l8);
         }
-
-        KDA_PHASE(0, 4);
-        // 3. A and L: one M=128 x N=16 x K=128 MMA per 16-column block.
-        for (int b = 0; b < 4; ++b) {
-            __syncthreads();  // l complete (b = 0) / previous MMA done with Z (b > 0)
-            for (int qi = tid; qi < C * 16; qi += kPrepThreads) {
-                const int r = qi >> 4, d0 = (qi & 15) * 8, br = r >> 4;
-                float qa[8], ka[8];
-                if (r < 16 * b) {
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) qa[t] = ka[t] = 0.0f;
-                } else {
-                    float l8[8], qv[8], kv[8];
-                    load8f(sG + r * D + d0, l8);
-                    if (br != b) {
-                        float t8[8];
-                        load8f(sTau + tau_index(br, b) * D + d0, t8);
-#pragma unroll
-                        for (int t = 0; t < 8; ++t) l8[t] *= t8[t];
-                    }
-                    unpack8(*reinterpret_cast<const uint4 *>(sQr + r * D + d0), qv);
-                    unpack8(*reinterpret_cast<const uint4 *>(sKr + r * D + d0), kv);
-                    const float rq = sRq[r], rk = sRk[r];
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) {
-                        qa[t] = qv[t] * rq * l8[t];
-                        ka[t] = kv[t] * rk * l8[t];
-                    }
-                }
-                *reinterpret_cast<uint4 *>(sZ + sw128_off(r, d0, 128)) = pack8(qa);
-                *reinterpret_cast<uint4 *>(sZ + sw128_off(64 + r, d0, 128)) = pack8(ka);
-            }
-            fence_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            if (tid == 0) {
-                tc_fence_after();
-                mma_tile<128, 16, 128, 128, 16>(tmem + 16 * b, smem_u32(sZ), smem_u32(sC + b * 4096), false);
-                mma_commit(mbar);
-            }
-            ok = mbar_wait(mbar, mphase) && ok;
-            mphase ^= 1;
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        KDA_PHASE(0, 3);
+        if (tid == 0) {
             tc_fence_after();
+            mma_tile<128, NST, 128, 128, NST>(tmem, smem_u32(sXL), smem_u32(sBS), false);
+            mma_tile<128, NST, 128, 128, NST>(tmem, smem_u32(sXL), smem_u32(sBS2), true);
+            mma_commit(mbar);
         }
+        // global loads for later items, their latency hidden under the MMA
+        if (has_next && tid < nxt.valid) beta_nxt = beta[(nxt.tok0 + tid) * H + nxt.h];
+        if (item + 2 * (int)gridDim.x < n_items)
+            nn = prep_item(item + 2 * gridDim.x, H, chunk_off, seq_start, seq_len, n_seqs);
+        ok = mbar_wait(mbar, mphase) && ok;
+        mphase ^= 1;
+        tc_fence_after();
         if (!__syncthreads_and(ok)) break;
+        KDA_PHASE(0, 4);
 
-        KDA_PHASE(0, 5);
-        // 4. A rows (TMEM lanes 0..63) to the record; beta-scaled L rows
-        //    (lanes 64..127) to shared fp32.
+        // 4. A rows (TMEM lanes 0..63) to the record, beta-scaled L rows
+        //    (lanes 64..127) to shared fp32.  Row r of block br finds column j
+        //    of its block pairs at TMEM column pair_col0(br) + j.
         {
-            float *sL = reinterpret_cast<float *>(sZ);
-            const int quarter = warp & 3, col0 = (warp >> 2) * 32;
-            const int row = 32 * quarter + lane;
-            float x[32];
-            tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + col0, x);
-            tmem_ld_wait();
-            if (row < C) {
+            float *sL = reinterpret_cast<float *>(sXL);
+            const int quarter = warp & 3, part = warp >> 2;
+            const int r = 32 * (quarter & 1) + lane;  // row inside A (quarters 0,1) or L (2,3)
+            const int br = r >> 4;
+            const bool lo_pair = (quarter & 1) == 0;  // rows of blocks 0,1: columns [0, 48)
+            const int ntile = lo_pair ? 3 : 7;
+            const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16);
+            for (int tile = part; tile < ntile; tile += 4) {
+                const int c0 = (lo_pair ? 0 : 48) + 16 * tile;
+                float x[16];
+                tmem_ld16(ta + c0, x);
+                tmem_ld_wait();
+                const int j0 = c0 - pair_col0(br);
+                if (j0 < 0 || j0 >= 16 * (br + 1)) continue;
+                if (quarter < 2) {
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    float y[8];
+                    for (int h8 = 0; h8 < 2; ++h8) {
+                        float y[8];
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) y[t] = (col0 + 8 * c8 + t <= row) ? x[8 * c8 + t] : 0.0f;
-                    *reinterpret_cast<uint4 *>(rec + TcRec::A + sw128_off(row, col0 + 8 * c8, 64)) = pack8(y);
+                        for (int t = 0; t < 8; ++t) y[t] = (j0 + 8 * h8 + t <= r) ? x[8 * h8 + t] : 0.0f;
+                        *reinterpret_cast<uint4 *>(rec + TcRec::A + sw128_off(r, j0 + 8 * h8, 64)) = pack8(y);
+                    }
+                } else {
+                    const float bet = sB[r];
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const int j = j0 + 4 * c4;
+                        float4 y;
+                        y.x = (j + 0 < r) ? bet * x[4 * c4 + 0] : 0.0f;
+                        y.y = (j + 1 < r) ? bet * x[4 * c4 + 1] : 0.0f;
+                        y.z = (j + 2 < r) ? bet * x[4 * c4 + 2] : 0.0f;
+                        y.w = (j + 3 < r) ? bet * x[4 * c4 + 3] : 0.0f;
+                        *reinterpret_cast<float4 *>(sL + r * LSTRIDE + j) = y;
+                    }
                 }
-            } else {
-                const int r = row - C;
-                const float bet = sB[r];
-#pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4) {
-                    float4 y;
-                    const int j = col0 + 4 * c4;
-                    y.x = (j + 0 < r) ? bet * x[4 * c4 + 0] : 0.0f;
-                    y.y = (j + 1 < r) ? bet * x[4 * c4 + 1] : 0.0f;
-                    y.z = (j + 2 < r) ? bet * x[4 * c4 + 2] : 0.0f;
-                    y.w = (j + 3 < r) ? bet * x[4 * c4 + 3] : 0.0f;
-                    *reinterpret_cast<float4 *>(sL + r * LSTRIDE + j) = y;
-                }
+            }
+            // A entries right of a row's block diagonal are zero
+            {
+                const int ra = tid >> 3, c8 = tid & 7;
+                if (c8 >= 2 * ((ra >> 4) + 1))
+                    *reinterpret_cast<uint4 *>(rec + TcRec::A + sw128_off(ra, 8 * c8, 64)) = make_uint4(0, 0, 0, 0);
             }
         }
         tc_fence_before();
         __syncthreads();
+        KDA_PHASE(0, 5);
 
-        KDA_PHASE(0, 6);
         // 5. X = (I + L)^-1, L strictly lower (beta-scaled rows), in 16x16 blocks:
-        //    diagonal blocks X_bb = (I + N)^-1 = (I - N)(I + N^2)(I + N^4)(I + N^8)
-        //    (N = L_bb is nilpotent); then with M = X_D L_off (strictly block
-        //    lower, M^4 = 0): (I + L)^-1 = (I - M + M^2 - M^3) X_D.
-        //    T = X diag(beta) -> bf16 operand at sC.
+        //    diagonal blocks X_bb = (I + L_bb)^-1 by forward substitution, one
+        //    column per lane (warps 0-1, no barriers); then with M = X_D L_off
+        //    (strictly block lower, M^4 = 0): (I + L)^-1 = (I - M + M^2 - M^3) X_D,
+        //    which is blocked forward substitution regrouped by levels.
+        //    T = X diag(beta) -> bf16 operand at sT.
         {
-            const float *sL = reinterpret_cast<const float *>(sZ);
-            float *T1 = reinterpret_cast<float *>(sC);              // 4 blocks each (5 KB)
+            const float *sL = reinterpret_cast<const float *>(sXL);
+            float *T1 = reinterpret_cast<float *>(sBS);  // 4 blocks each
             float *T2 = T1 + 4 * MBLK;
             float *T3 = T2 + 4 * MBLK;
-            float *T4 = reinterpret_cast<float *>(sZ) + 64 * LSTRIDE;  // after L in Z
-            const int bb = tid >> 6, i = (tid & 63) >> 2, cg = tid & 3;
-            const int o = 16 * bb;
-            const float *N = sL + o * LSTRIDE + o;                   // L_bb, stride LSTRIDE
-            auto put = [](float *M_, int i_, int cg_, float4 x) {
-                *reinterpret_cast<float4 *>(M_ + i_ * MS + 4 * cg_) = x;
+            float *T4 = reinterpret_cast<float *>(sXL) + C * LSTRIDE;  // after L
+            float *Mb = T4 + 4 * MBLK;                                  // 6 blocks
+            auto put = [](float *M_, int i_, int c_, float2 x) {
+                *reinterpret_cast<float2 *>(M_ + i_ * MS + 2 * c_) = x;
             };
-            auto get = [](const float *M_, int i_, int cg_) {
-                return *reinterpret_cast<const float4 *>(M_ + i_ * MS + 4 * cg_);
-            };
-            // P2 = N N  -> T1 ; N as a MS-stride copy -> T4 (for products with N on the right)
-            {
-                float4 nn;
-                nn.x = N[i * LSTRIDE + 4 * cg + 0]; nn.y = N[i * LSTRIDE + 4 * cg + 1];
-                nn.z = N[i * LSTRIDE + 4 * cg + 2]; nn.w = N[i * LSTRIDE + 4 * cg + 3];
-                put(T4 + bb * MBLK, i, cg, nn);
+            if (warp < 2) {
+                const int blk = tid >> 4, c = tid & 15, o = 16 * blk;
+                float x[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    float lr[16];
+                    row16(sL + o, LSTRIDE, o + r, lr);
+                    // two partial sums shorten the dependent chain
+                    float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+                    for (int m2 = 0; m2 < r; ++m2) {
+                        if (m2 & 1) a1 = fmaf(lr[m2], x[m2], a1);
+                        else a0 = fmaf(lr[m2], x[m2], a0);
+                    }
+                    x[r] = (r == c) ? 1.0f : (r < c ? 0.0f : -(a0 + a1));
+                }
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    sX[(o + r) * C + o + c] = x[r];
+                    T2[blk * MBLK + r * MS + c] = x[r];
+                }
             }
             __syncthreads();
-            put(T1 + bb * MBLK, i, cg, mm16_row4(N, LSTRIDE, T4 + bb * MBLK, i, cg));
-            __syncthreads();
-            // P4 = P2 P2 -> T2 ;  Y1 = I - N + P2 - N P2 -> T3
-            {
-                const float4 p4 = mm16_row4(T1 + bb * MBLK, MS, T1 + bb * MBLK, i, cg);
-                const float4 np2 = mm16_row4(N, LSTRIDE, T1 + bb * MBLK, i, cg);
-                const float4 p2 = get(T1 + bb * MBLK, i, cg);
-                const float4 n4 = get(T4 + bb * MBLK, i, cg);
-                float4 y;
-                y.x = (i == 4 * cg + 0 ? 1.f : 0.f) - n4.x + p2.x - np2.x;
-                y.y = (i == 4 * cg + 1 ? 1.f : 0.f) - n4.y + p2.y - np2.y;
-                y.z = (i == 4 * cg + 2 ? 1.f : 0.f) - n4.z + p2.z - np2.z;
-                y.w = (i == 4 * cg + 3 ? 1.f : 0.f) - n4.w + p2.w - np2.w;
-                put(T2 + bb * MBLK, i, cg, p4);
-                put(T3 + bb * MBLK, i, cg, y);
-            }
-            __syncthreads();
-            // P8 = P4 P4 -> T1 ;  Y2 = Y1 + Y1 P4 -> T4
-            {
-                const float4 p8 = mm16_row4(T2 + bb * MBLK, MS, T2 + bb * MBLK, i, cg);
-                const float4 yp = mm16_row4(T3 + bb * MBLK, MS, T2 + bb * MBLK, i, cg);
-                const float4 y1 = get(T3 + bb * MBLK, i, cg);
-                put(T1 + bb * MBLK, i, cg, p8);
-                put(T4 + bb * MBLK, i, cg, make_float4(y1.x + yp.x, y1.y + yp.y, y1.z + yp.z, y1.w + yp.w));
-            }
-            __syncthreads();
-            // X_bb = Y2 + Y2 P8 -> sX diagonal block (stride 64) and T2 (stride MS)
-            {
-                const float4 yp = mm16_row4(T4 + bb * MBLK, MS, T1 + bb * MBLK, i, cg);
-                const float4 y2 = get(T4 + bb * MBLK, i, cg);
-                const float4 xd = make_float4(y2.x + yp.x, y2.y + yp.y, y2.z + yp.z, y2.w + yp.w);
-                *reinterpret_cast<float4 *>(sX + (o + i) * C + o + 4 * cg) = xd;
-                put(T2 + bb * MBLK, i, cg, xd);
-            }
-            __syncthreads();
-            KDA_PHASE(0, 7);
+            KDA_PHASE(0, 6);
             // Off-diagonal part.  Block pairs (a, b), a > b, indexed p = 0..5:
-            // (1,0) (2,0) (2,1) (3,0) (3,1) (3,2).  X_D blocks are in T2 (stride MS).
-            // Scratch: Z holds L in bytes [0, 17408) and the Y2 blocks in
-            // [17408, 22528); M goes after them, [22528, 30208).
+            // (1,0) (2,0) (2,1) (3,0) (3,1) (3,2).  X_D blocks are in T2.
             const float *XD = T2;
-            float *Mb = reinterpret_cast<float *>(sZ + 22528);  // M_ab = X_aa L_ab, 6 blocks
-            float *M2 = T1;          // (M^2)_ab for (2,0) (3,1) (3,0)
-            float *M3 = T3;          // (M^3)_30
-            auto pair_a = [](int p) { return p < 1 ? 1 : (p < 3 ? 2 : 3); };
-            auto pair_b = [](int p, int a) { return p - a * (a - 1) / 2; };
-            for (int sl = tid; sl < 6 * 64; sl += kPrepThreads) {
-                const int p = sl >> 6, ii = (sl & 63) >> 2, cc = sl & 3;
-                const int a = pair_a(p), b = pair_b(p, a);
-                // X_aa (stride MS) times L_ab (stride LSTRIDE, needs a MS copy of B):
-                // compute directly: sum_k X_aa[ii][k] L[16a+k][16b + 4cc..]
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            float *M2 = T1;  // (M^2)_ab for (2,0) (3,1) (3,0)
+            float *M3 = T3;  // (M^3)_30
+            auto pair_a = [](int p_) { return p_ < 1 ? 1 : (p_ < 3 ? 2 : 3); };
+            for (int sl = tid; sl < 6 * 128; sl += kPrepThreads) {  // M_ab = X_aa L_ab
+                const int p_ = sl >> 7, ii = (sl >> 3) & 15, cc = sl & 7;
+                const int a = pair_a(p_), b = p_ - a * (a - 1) / 2;
+                float xa[16];
+                row16(XD + a * MBLK, MS, ii, xa);
+                float2 l[16];
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk)
+                    l[kk] = *reinterpret_cast<const float2 *>(sL + (16 * a + kk) * LSTRIDE + 16 * b + 2 * cc);
+                float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int kk = 0; kk < 16; ++kk) {
-                    const float x = XD[a * MBLK + ii * MS + kk];
-                    const float4 l = *reinterpret_cast<const float4 *>(sL + (16 * a + kk) * LSTRIDE + 16 * b + 4 * cc);
-                    acc.x = fmaf(x, l.x, acc.x); acc.y = fmaf(x, l.y, acc.y);
-                    acc.z = fmaf(x, l.z, acc.z); acc.w = fmaf(x, l.w, acc.w);
+                    acc.x = fmaf(xa[kk], l[kk].x, acc.x);
+                    acc.y = fmaf(xa[kk], l[kk].y, acc.y);
                 }
-                put(Mb + p * MBLK, ii, cc, acc);
+                put(Mb + p_ * MBLK, ii, cc, acc);
             }
             __syncthreads();
-            // M^2: (2,0) = M21 M10 ; (3,1) = M32 M21 ; (3,0) = M31 M10 + M32 M20
-            for (int sl = tid; sl < 3 * 64; sl += kPrepThreads) {
-                const int p = sl >> 6, ii = (sl & 63) >> 2, cc = sl & 3;
-                float4 acc;
-                if (p == 0) acc = mm16_row4(Mb + 2 * MBLK, MS, Mb + 0 * MBLK, ii, cc);
-                else if (p == 1) acc = mm16_row4(Mb + 5 * MBLK, MS, Mb + 2 * MBLK, ii, cc);
-                else {
-                    const float4 a1 = mm16_row4(Mb + 4 * MBLK, MS, Mb + 0 * MBLK, ii, cc);
-                    const float4 a2 = mm16_row4(Mb + 5 * MBLK, MS, Mb + 1 * MBLK, ii, cc);
-                    acc = make_float4(a1.x + a2.x, a1.y + a2.y, a1.z + a2.z, a1.w + a2.w);
+            if (tid < 3 * 128) {  // M^2: (2,0) = M21 M10 ; (3,1) = M32 M21 ; (3,0) = M31 M10 + M32 M20
+                const int p_ = tid >> 7, ii = (tid >> 3) & 15, cc = tid & 7;
+                float2 acc;
+                if (p_ == 0) {
+                    acc = mm16_row2(Mb + 2 * MBLK, MS, Mb + 0 * MBLK, ii, cc);
+                } else if (p_ == 1) {
+                    acc = mm16_row2(Mb + 5 * MBLK, MS, Mb + 2 * MBLK, ii, cc);
+                } else {
+                    const float2 a1 = mm16_row2(Mb + 4 * MBLK, MS, Mb + 0 * MBLK, ii, cc);
+                    const float2 a2 = mm16_row2(Mb + 5 * MBLK, MS, Mb + 1 * MBLK, ii, cc);
+                    acc = make_float2(a1.x + a2.x, a1.y + a2.y);
                 }
-                put(M2 + p * MBLK, ii, cc, acc);
+                put(M2 + p_ * MBLK, ii, cc, acc);
             }
             __syncthreads();
-            // M^3: (3,0) = M32 (M^2)_20
-            if (tid < 64) put(M3, (tid & 63) >> 2, tid & 3, mm16_row4(Mb + 5 * MBLK, MS, M2 + 0 * MBLK, (tid & 63) >> 2, tid & 3));
+            if (tid < 128) {  // M^3: (3,0) = M32 (M^2)_20
+                const int ii = (tid >> 3) & 15, cc = tid & 7;
+                put(M3, ii, cc, mm16_row2(Mb + 5 * MBLK, MS, M2 + 0 * MBLK, ii, cc));
+            }
             __syncthreads();
-            // X_ab = (-M + M^2 - M^3)_ab X_bb
-            for (int sl = tid; sl < 6 * 64; sl += kPrepThreads) {
-                const int p = sl >> 6, ii = (sl & 63) >> 2, cc = sl & 3;
-                const int a = pair_a(p), b = pair_b(p, a);
-                const int p2 = (p == 1) ? 0 : (p == 4) ? 1 : (p == 3) ? 2 : -1;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int sl = tid; sl < 6 * 128; sl += kPrepThreads) {  // X_ab = (-M + M^2 - M^3)_ab X_bb
+                const int p_ = sl >> 7, ii = (sl >> 3) & 15, cc = sl & 7;
+                const int a = pair_a(p_), b = p_ - a * (a - 1) / 2;
+                const int p2 = (p_ == 1) ? 0 : (p_ == 4) ? 1 : (p_ == 3) ? 2 : -1;
+                float z[16];
+                row16(Mb + p_ * MBLK, MS, ii, z);
+                if (p2 >= 0) {
+                    float m2[16];
+                    row16(M2 + p2 * MBLK, MS, ii, m2);
 #pragma unroll
-                for (int kk = 0; kk < 16; ++kk) {
-                    float z = -Mb[p * MBLK + ii * MS + kk];
-                    if (p2 >= 0) z += M2[p2 * MBLK + ii * MS + kk];
-                    if (p == 3) z -= M3[ii * MS + kk];
-                    const float4 xb = *reinterpret_cast<const float4 *>(XD + b * MBLK + kk * MS + 4 * cc);
-                    acc.x = fmaf(z, xb.x, acc.x); acc.y = fmaf(z, xb.y, acc.y);
-                    acc.z = fmaf(z, xb.z, acc.z); acc.w = fmaf(z, xb.w, acc.w);
+                    for (int kk = 0; kk < 16; ++kk) z[kk] = m2[kk] - z[kk];
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk) z[kk] = -z[kk];
                 }
-                *reinterpret_cast<float4 *>(sX + (16 * a + ii) * C + 16 * b + 4 * cc) = acc;
+                if (p_ == 3) {
+                    float m3[16];
+                    row16(M3, MS, ii, m3);
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk) z[kk] -= m3[kk];
+                }
+                *reinterpret_cast<float2 *>(sX + (16 * a + ii) * C + 16 * b + 2 * cc) =
+                    row_times(z, XD + b * MBLK, cc);
             }
             __syncthreads();
-            // T = X diag(beta), lower triangle, as a K-major [i][j] bf16 operand
-            for (int qi = tid; qi < C * 8; qi += kPrepThreads) {
-                const int ri = qi >> 3, j0 = (qi & 7) * 8;
-                float y[8];
+            {  // T = X diag(beta), lower triangle, as K-major [i][j] bf16 hi + lo operands
+                const int ri = tid >> 3, j0 = (tid & 7) * 8;
+                float y[8], lo[8];
 #pragma unroll
                 for (int t = 0; t < 8; ++t) y[t] = (j0 + t <= ri) ? sX[ri * C + j0 + t] * sB[j0 + t] : 0.0f;
-                *reinterpret_cast<uint4 *>(sC + sw128_off(ri, j0, 64)) = pack8(y);
+                const uint4 hi = pack8(y);
+                unpack8(hi, lo);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) lo[t] = y[t] - lo[t];
+                *reinterpret_cast<uint4 *>(sT + sw128_off(ri, j0, 64)) = hi;
+                *reinterpret_cast<uint4 *>(sT + 8192 + sw128_off(ri, j0, 64)) = pack8(lo);
             }
         }
         __syncthreads();
+        KDA_PHASE(0, 7);
 
-        KDA_PHASE(0, 8);
-        // 6. E^T = (exp(G) k_hat)^T and V^T operands in Z; W = T E, U = T V.
+        // 6. E^T = (exp(G) k_hat)^T and V^T operands (in XL); then the raw tiles
+        //    are dead and the next item's loads go out; W = T E, U = T V.
         for (int qi = tid; qi < 8 * D; qi += kPrepThreads) {
             const int c8 = qi >> 7, d = qi & (D - 1);
             const float rho = sRho[(c8 >> 1) * D + d];
@@ -588,63 +603,64 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                 e[t] = __bfloat162float(sKr[j * D + d]) * sRk[j] * sG[j * D + d] * rho;
                 vv[t] = __bfloat162float(sVr[j * D + d]);
             }
-            *reinterpret_cast<uint4 *>(sZ + sw128_off(d, 8 * c8, 128)) = pack8(e);
-            *reinterpret_cast<uint4 *>(sZ + 16384 + sw128_off(d, 8 * c8, 128)) = pack8(vv);
+            *reinterpret_cast<uint4 *>(sXL + sw128_off(d, 8 * c8, 128)) = pack8(e);
+            *reinterpret_cast<uint4 *>(sXL + 16384 + sw128_off(d, 8 * c8, 128)) = pack8(vv);
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
         if (tid == 0) {
+            if (has_next) load_raw(sm, maps, nxt.h, nxt.tok0, full);
             tc_fence_after();
-            mma_tile<128, 128, 64, 128, 128>(tmem + 0, smem_u32(sC), smem_u32(sZ), false);
-            mma_tile<128, 128, 64, 128, 128>(tmem + 128, smem_u32(sC), smem_u32(sZ + 16384), false);
+            mma_tile<128, 128, 64, 128, 128>(tmem + 0, smem_u32(sT), smem_u32(sXL), false);
+            mma_tile<128, 128, 64, 128, 128>(tmem + 0, smem_u32(sT + 8192), smem_u32(sXL), true);
+            mma_tile<128, 128, 64, 128, 128>(tmem + 128, smem_u32(sT), smem_u32(sXL + 16384), false);
+            mma_tile<128, 128, 64, 128, 128>(tmem + 128, smem_u32(sT + 8192), smem_u32(sXL + 16384), true);
             mma_commit(mbar);
         }
+        KDA_PHASE(0, 8);
         ok = mbar_wait(mbar, mphase) && ok;
         mphase ^= 1;
         tc_fence_after();
         if (!__syncthreads_and(ok)) break;
 
-        KDA_PHASE(0, 9);
         // 7. W rows (WQ rows 0..63) and U to the record: TMEM lanes 0..63.
         if ((warp & 3) < 2) {
-            const int i = 32 * (warp & 3) + lane, half = warp >> 2;
+            const int i = 32 * (warp & 3) + lane, part = warp >> 2;
             const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+            float x[32];
+            tmem_ld32(ta + 32 * part, x);
+            tmem_ld_wait();
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                float x[32];
-                const int c0 = 64 * half + 32 * part;
-                tmem_ld32(ta + c0, x);
-                tmem_ld_wait();
+            for (int c8 = 0; c8 < 4; ++c8) {
+                float y[8];
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    float y[8];
+                for (int t = 0; t < 8; ++t) y[t] = x[8 * c8 + t];
+                *reinterpret_cast<uint4 *>(rec + TcRec::WQ + sw128_off(i, 32 * part + 8 * c8, 128)) = pack8(y);
+            }
+            tmem_ld32(ta + 128 + 32 * part, x);
+            tmem_ld_wait();
+            unsigned char *ub = rec + TcRec::U + part * TcRec::UBLK + i * 64;
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) y[t] = x[8 * c8 + t];
-                    *reinterpret_cast<uint4 *>(rec + TcRec::WQ + sw128_off(i, c0 + 8 * c8, 128)) = pack8(y);
-                }
-                tmem_ld32(ta + 128 + c0, x);
-                tmem_ld_wait();
-                unsigned char *ub = rec + TcRec::U + (c0 >> 5) * TcRec::UBLK + i * 64;
+            for (int c8 = 0; c8 < 4; ++c8) {
+                float y[8];
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    float y[8];
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) y[t] = x[8 * c8 + t];
-                    *reinterpret_cast<uint4 *>(ub + 16 * c8) = pack8(y);
-                }
+                for (int t = 0; t < 8; ++t) y[t] = x[8 * c8 + t];
+                *reinterpret_cast<uint4 *>(ub + 16 * c8) = pack8(y);
             }
         }
         tc_fence_before();
         __syncthreads();
-        KDA_PHASE(0, 10);
+        KDA_PHASE(0, 9);
+        cur = nxt;
+        nxt = nn;
+        beta_cur = beta_nxt;
     }
     if (!ok) {
         if (tid == 0) {
             atomicOr(status, kStatusTimeout);
-            // let copies still in flight land before the shared memory is released
-            mbar_wait(&full[0], 0, 400000000LL) || mbar_wait(&full[0], 1, 400000000LL);
-            mbar_wait(&full[1], 0, 400000000LL) || mbar_wait(&full[1], 1, 400000000LL);
+            // let a copy still in flight land before the shared memory is released
+            mbar_wait(full, fphase, 400000000LL);
         }
         __syncthreads();
     }

@@ -184,6 +184,36 @@ def test_chunk_strong_decay_fp32(kda):
     assert rel_l2(vk_to_kv(sf), s_ref) < TOL_F32
 
 
+@pytest.mark.parametrize("g_lo,g_hi", [(-3.0, -1.0), (-5.0, -3.0)])
+def test_chunk_strong_decay_bf16_tensor_cores(kda, g_lo, g_hi):
+    """Every channel decaying hard, down to -5 per token: the tensor-core
+    path's per-16-column-block decay references stay in range."""
+    x = kda_inputs.prefill([150, 77], H=2, dtype=torch.bfloat16, seed=38, g_range=(g_lo, g_hi),
+                           init_std=0.02)
+    o, sf = run_chunk(kda, x)
+    o_ref, s_ref = oracle_prefill(x)
+    assert rel_l2(to_np(o), o_ref) < TOL_BF16
+    assert rel_l2(vk_to_kv(sf), s_ref) < TOL_BF16
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_chunk_nearly_parallel_keys(kda, dtype):
+    """Repeated tokens: keys within a few percent of one direction and beta
+    near 1, so every entry of the intra-chunk interaction matrix is near 1
+    (random keys keep it near 0).  Both chunk paths must stay on the oracle."""
+    x = kda_inputs.prefill([200, 64], H=2, dtype=dtype, seed=39)
+    gen = torch.Generator().manual_seed(39)
+    base = torch.randn(1, 2, 128, generator=gen)
+    noise = torch.randn(x["k"].shape, generator=gen)
+    x["k"] = (base + 0.03 * noise).to(dtype)
+    x["beta"] = torch.full_like(x["beta"], 0.97)
+    o, sf = run_chunk(kda, x)
+    o_ref, s_ref = oracle_prefill(x)
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    assert rel_l2(to_np(o), o_ref) < tol
+    assert rel_l2(vk_to_kv(sf), s_ref) < tol
+
+
 def test_chunk_dense_batch_without_cu_seqlens(kda):
     x = kda_inputs.prefill([96, 96, 96], H=2, dtype=torch.float32, seed=34)
     d = dev(x)
@@ -276,3 +306,35 @@ def test_chunk_varlen_8_full_size_sampled_heads(kda):
     assert rel_l2(to_np(o[:, heads]), o_ref) < TOL_BF16
     assert rel_l2(vk_to_kv(sf[:, heads]), s_ref) < TOL_BF16
     assert torch.isfinite(o).all()
+
+
+def test_long_131k_prefill_handoff_then_256_decode_steps(kda):
+    """B=1 H=32 T=131072 bf16 with the 90% weak / 10% strong (-3..-1) decay mix
+    (seed 4): the prefill's final state goes straight into a pool slot, then
+    256 decode steps continue from it.  The oracle follows one sampled head
+    through both phases."""
+    x = kda_inputs.long_131k()
+    H = x["H"]
+    head = 7
+    pool = torch.zeros((2, H, 128, 128), dtype=torch.float32, device="cuda")
+    idx = torch.tensor([1], dtype=torch.int32, device="cuda")
+    d = dev(x)
+    o, _ = kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], cu_seqlens=d["cu_seqlens"],
+                             final_state=pool, state_indices=idx)
+    torch.cuda.synchronize()
+    o_ref, s_ref = oracle_prefill(x, [head])
+    assert rel_l2(to_np(o[:, [head]]), o_ref) < TOL_BF16
+    assert rel_l2(vk_to_kv(pool[1, [head]]), s_ref[0]) < TOL_BF16
+    assert torch.isfinite(o).all() and torch.isfinite(pool).all()
+    assert (pool[0] == 0).all()
+    del d, o
+    ref = s_ref.copy()  # [1, 1, K, V]: the oracle continues from its own exact state
+    for t in range(256):
+        tok = kda_inputs.decode_tokens(1, H=H, seed=4, step=t, g_mixed=True)
+        o2 = kda.kda_recurrent_step(*(tok[n].cuda() for n in ("q", "k", "v", "g", "beta")), pool,
+                                    state_indices=idx)
+        sub = {n: tok[n][:, [head]] for n in ("q", "k", "v", "g", "beta")}
+        o2_ref, ref = oracle.step(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], ref)
+        if t in (0, 255):
+            assert rel_l2(to_np(o2[:, [head]]), o2_ref) < TOL_BF16
+    assert rel_l2(vk_to_kv(pool[1, [head]]), ref[0]) < TOL_BF16
