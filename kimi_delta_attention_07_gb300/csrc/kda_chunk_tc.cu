@@ -43,7 +43,9 @@
 //     S   = diag(gC) S + D3   (fp32, one key row per thread, in registers)
 //   The 128-row A operand of the second MMA starts 8 KB before the A tile in
 //   the staged record (its rows 0..63 are the tail of KD^T and only feed D1
-//   rows that were already consumed).
+//   rows that were already consumed).  D1 is double-buffered in TMEM so that
+//   the output rows of a chunk are stored while the next chunk's first MMA
+//   runs; only the MMA-issuing thread waits for a stage before that MMA.
 #include <cuda.h>  // CUtensorMap (the encoder is fetched through the runtime)
 #include <cudaTypedefs.h>
 
@@ -176,25 +178,33 @@ __device__ __forceinline__ void row16(const float *A, int lda, int i, float (&a)
     }
 }
 
-// Two outputs (row a[], columns 2c2, 2c2+1) of a * B, B a 16x16 matrix with
-// stride MS; every load is issued before the first FMA.
-__device__ __forceinline__ float2 row_times(const float (&a)[16], const float *B, int c2) {
-    float2 b[16];
+// Four outputs (row a[], columns 4c4..4c4+3) of a * B, B a 16x16 matrix with
+// row stride ldb (floats, 16-byte aligned rows).
+__device__ __forceinline__ float4 row4_times(const float (&a)[16], const float *B, int c4,
+                                             int ldb = MS) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk) b[kk] = *reinterpret_cast<const float2 *>(B + kk * MS + 2 * c2);
-    float2 acc = make_float2(0.f, 0.f);
+    for (int h8 = 0; h8 < 2; ++h8) {
+        float4 b[8];
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
-        acc.x = fmaf(a[kk], b[kk].x, acc.x);
-        acc.y = fmaf(a[kk], b[kk].y, acc.y);
+        for (int kk = 0; kk < 8; ++kk) b[kk] = *reinterpret_cast<const float4 *>(B + (8 * h8 + kk) * ldb + 4 * c4);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const float x = a[8 * h8 + kk];
+            acc.x = fmaf(x, b[kk].x, acc.x);
+            acc.y = fmaf(x, b[kk].y, acc.y);
+            acc.z = fmaf(x, b[kk].z, acc.z);
+            acc.w = fmaf(x, b[kk].w, acc.w);
+        }
     }
     return acc;
 }
 
-__device__ __forceinline__ float2 mm16_row2(const float *A, int lda, const float *B, int i, int c2) {
+__device__ __forceinline__ float4 mm16_row4(const float *A, int lda, const float *B, int ldb, int i,
+                                            int c4) {
     float a[16];
     row16(A, lda, i, a);
-    return row_times(a, B, c2);
+    return row4_times(a, B, c4, ldb);
 }
 
 __global__ void __launch_bounds__(kPrepThreads, 1)
@@ -336,8 +346,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         __syncthreads();
         KDA_PHASE(0, 1);
 
-        // 2. passes that read G itself: KD^T (column chunks) and the stacked
-        //    column operand k_hat_j * exp(G_16br - G_j) for the 10 pairs.
+        // 2. KD^T = (k_hat exp(G_last - G))^T, column chunks of 8 chunk rows.
         for (int qi = tid; qi < 8 * D; qi += kPrepThreads) {
             const int c8 = qi >> 7, d = qi & (D - 1);
             const float gl = sGref[4 * D + d];
@@ -349,50 +358,72 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             }
             *reinterpret_cast<uint4 *>(rec + TcRec::KDT + sw128_off(d, 8 * c8, 128)) = pack8(x);
         }
-        for (int qi = tid; qi < NST * 16; qi += kPrepThreads) {
-            const int p = qi >> 8, jj = (qi >> 4) & 15, d0 = (qi & 15) * 8;
-            const int br = p >= 6 ? 3 : (p >= 3 ? 2 : (p >= 1 ? 1 : 0));
-            const int b = p - br * (br + 1) / 2, j = 16 * b + jj;
-            float G8[8], Gb8[8], kv[8], y[8];
-            load8f(sG + j * D + d0, G8);
-            load8f(sGref + br * D + d0, Gb8);
-            unpack8(*reinterpret_cast<const uint4 *>(sKr + j * D + d0), kv);
-            const float rk = sRk[j];
-#pragma unroll
-            for (int t = 0; t < 8; ++t) y[t] = kv[t] * rk * __expf(fminf(Gb8[t] - G8[t], 80.0f));
-            // hi + lo bf16 parts: the MMA sees this operand to ~16 bits
-            const uint4 hi = pack8(y);
-            float lo[8];
-            unpack8(hi, lo);
-#pragma unroll
-            for (int t = 0; t < 8; ++t) lo[t] = y[t] - lo[t];
-            *reinterpret_cast<uint4 *>(sBS + sw128_off(16 * p + jj, d0, NST)) = hi;
-            *reinterpret_cast<uint4 *>(sBS2 + sw128_off(16 * p + jj, d0, NST)) = pack8(lo);
-        }
         __syncthreads();
         KDA_PHASE(0, 2);
-        // 3. per (row, 8 channels): l = exp(G - G_16br) in place, QG to the
-        //    record, and the row operand [q_hat l ; k_hat l].
+        // 3. one pass per (row j, 8 channels): l = exp(G_j - G_16bj) (stored over
+        //    G), QG to the record, the row operand [q_hat l ; k_hat l], and the
+        //    stacked column operand rows of j for every row block br >= bj:
+        //    k_hat_j exp(G_16br - G_j) = k_hat_j tau(br, bj) / l_j, with 1 / l_j
+        //    clamped at exp(80) on the block diagonal; where l_j < 1e-30 those
+        //    entries are taken as exponentials directly.
         for (int qi = tid; qi < C * 16; qi += kPrepThreads) {
-            const int r = qi >> 4, d0 = (qi & 15) * 8, br = r >> 4;
+            const int r = qi >> 4, d0 = (qi & 15) * 8, bj = r >> 4;
             float G8[8], Gb8[8], rho8[8], qv[8], kv[8];
             load8f(sG + r * D + d0, G8);
-            load8f(sGref + br * D + d0, Gb8);
-            load8f(sRho + br * D + d0, rho8);
+            load8f(sGref + bj * D + d0, Gb8);
+            load8f(sRho + bj * D + d0, rho8);
             unpack8(*reinterpret_cast<const uint4 *>(sQr + r * D + d0), qv);
             unpack8(*reinterpret_cast<const uint4 *>(sKr + r * D + d0), kv);
             const float rq = sRq[r], rk = sRk[r];
-            float qg[8], ql[8], kl[8], l8[8];
+            float ql[8], kl[8], l8[8], inv[8], kh[8];
+            bool tiny = false;
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
                 l8[t] = __expf(G8[t] - Gb8[t]);
+                kh[t] = kv[t] * rk;
                 ql[t] = qv[t] * rq * l8[t];
-                kl[t] = kv[t] * rk * l8[t];
-                qg[t] = ql[t] * rho8[t];
+                kl[t] = kh[t] * l8[t];
+                tiny |= l8[t] < 1e-30f;
+                inv[t] = __fdividef(1.0f, l8[t]);
+                qv[t] = ql[t] * rho8[t];  // QG = q_hat exp(G)
             }
-            *reinterpret_cast<uint4 *>(rec + TcRec::WQ + sw128_off(64 + r, d0, 128)) = pack8(qg);
+            *reinterpret_cast<uint4 *>(rec + TcRec::WQ + sw128_off(64 + r, d0, 128)) = pack8(qv);
             *reinterpret_cast<uint4 *>(sXL + sw128_off(r, d0, 128)) = pack8(ql);
             *reinterpret_cast<uint4 *>(sXL + sw128_off(64 + r, d0, 128)) = pack8(kl);
+            // hi + lo bf16 parts: the MMA sees this operand to ~16 bits
+            auto emit = [&](int b2, const float (&y)[8]) {
+                const uint4 hi = pack8(y);
+                float lo[8];
+                unpack8(hi, lo);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) lo[t] = y[t] - lo[t];
+                const int row = 16 * (b2 * (b2 + 1) / 2 + bj) + (r & 15);
+                *reinterpret_cast<uint4 *>(sBS + sw128_off(row, d0, NST)) = hi;
+                *reinterpret_cast<uint4 *>(sBS2 + sw128_off(row, d0, NST)) = pack8(lo);
+            };
+            if (!__builtin_expect(tiny, 0)) {
+                float y[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) y[t] = kh[t] * fminf(inv[t], 5.540622e34f);
+                emit(bj, y);
+                for (int b2 = bj + 1; b2 < 4; ++b2) {
+                    float t8[8];
+                    load8f(sTau + tau_index(b2, bj) * D + d0, t8);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) y[t] = kh[t] * t8[t] * inv[t];
+                    emit(b2, y);
+                }
+            } else {  // a decay of more than ~69 inside this 16-row block
+                float y[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) y[t] = kh[t] * __expf(fminf(Gb8[t] - G8[t], 80.0f));
+                emit(bj, y);
+                for (int b2 = bj + 1; b2 < 4; ++b2) {
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) y[t] = kh[t] * __expf(sGref[b2 * D + d0 + t] - G8[t]);
+                    emit(b2, y);
+                }
+            }
             store8f(sG + r * D + d0, l8);
         }
         fence_async_smem();
@@ -479,9 +510,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             float *T3 = T2 + 4 * MBLK;
             float *T4 = reinterpret_cast<float *>(sXL) + C * LSTRIDE;  // after L
             float *Mb = T4 + 4 * MBLK;                                  // 6 blocks
-            auto put = [](float *M_, int i_, int c_, float2 x) {
-                *reinterpret_cast<float2 *>(M_ + i_ * MS + 2 * c_) = x;
-            };
             if (warp < 2) {
                 const int blk = tid >> 4, c = tid & 15, o = 16 * blk;
                 float x[16];
@@ -507,72 +535,58 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             __syncthreads();
             KDA_PHASE(0, 6);
             // Off-diagonal part.  Block pairs (a, b), a > b, indexed p = 0..5:
-            // (1,0) (2,0) (2,1) (3,0) (3,1) (3,2).  X_D blocks are in T2.
+            // (1,0) (2,0) (2,1) (3,0) (3,1) (3,2).  X_D blocks are in T2.  Each
+            // level gives a thread at most one (row, 4 columns) slot.
             const float *XD = T2;
-            float *M2 = T1;  // (M^2)_ab for (2,0) (3,1) (3,0)
-            float *M3 = T3;  // (M^3)_30
+            float *M2 = T1;  // M21 M10, M32 M21, M31 M10, M32 M20
+            float *M3 = T3;  // (M^3)_30 = M32 (M21 M10)
             auto pair_a = [](int p_) { return p_ < 1 ? 1 : (p_ < 3 ? 2 : 3); };
-            for (int sl = tid; sl < 6 * 128; sl += kPrepThreads) {  // M_ab = X_aa L_ab
-                const int p_ = sl >> 7, ii = (sl >> 3) & 15, cc = sl & 7;
+            auto put4 = [](float *M_, int i_, int c_, float4 x) {
+                *reinterpret_cast<float4 *>(M_ + i_ * MS + 4 * c_) = x;
+            };
+            if (tid < 6 * 64) {  // M_ab = X_aa L_ab
+                const int p_ = tid >> 6, ii = (tid >> 2) & 15, c4 = tid & 3;
                 const int a = pair_a(p_), b = p_ - a * (a - 1) / 2;
-                float xa[16];
-                row16(XD + a * MBLK, MS, ii, xa);
-                float2 l[16];
-#pragma unroll
-                for (int kk = 0; kk < 16; ++kk)
-                    l[kk] = *reinterpret_cast<const float2 *>(sL + (16 * a + kk) * LSTRIDE + 16 * b + 2 * cc);
-                float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int kk = 0; kk < 16; ++kk) {
-                    acc.x = fmaf(xa[kk], l[kk].x, acc.x);
-                    acc.y = fmaf(xa[kk], l[kk].y, acc.y);
-                }
-                put(Mb + p_ * MBLK, ii, cc, acc);
+                put4(Mb + p_ * MBLK, ii, c4, mm16_row4(XD + a * MBLK, MS, sL + (16 * a) * LSTRIDE + 16 * b, LSTRIDE, ii, c4));
             }
             __syncthreads();
-            if (tid < 3 * 128) {  // M^2: (2,0) = M21 M10 ; (3,1) = M32 M21 ; (3,0) = M31 M10 + M32 M20
-                const int p_ = tid >> 7, ii = (tid >> 3) & 15, cc = tid & 7;
-                float2 acc;
-                if (p_ == 0) {
-                    acc = mm16_row2(Mb + 2 * MBLK, MS, Mb + 0 * MBLK, ii, cc);
-                } else if (p_ == 1) {
-                    acc = mm16_row2(Mb + 5 * MBLK, MS, Mb + 2 * MBLK, ii, cc);
-                } else {
-                    const float2 a1 = mm16_row2(Mb + 4 * MBLK, MS, Mb + 0 * MBLK, ii, cc);
-                    const float2 a2 = mm16_row2(Mb + 5 * MBLK, MS, Mb + 1 * MBLK, ii, cc);
-                    acc = make_float2(a1.x + a2.x, a1.y + a2.y);
-                }
-                put(M2 + p_ * MBLK, ii, cc, acc);
+            if (tid < 4 * 64) {
+                const int q_ = tid >> 6, ii = (tid >> 2) & 15, c4 = tid & 3;
+                const int pa_ = q_ == 0 ? 2 : (q_ == 2 ? 4 : 5);  // M21 M10, M32 M21, M31 M10, M32 M20
+                const int pb_ = q_ == 1 ? 2 : (q_ == 3 ? 1 : 0);
+                put4(M2 + q_ * MBLK, ii, c4, mm16_row4(Mb + pa_ * MBLK, MS, Mb + pb_ * MBLK, MS, ii, c4));
             }
             __syncthreads();
-            if (tid < 128) {  // M^3: (3,0) = M32 (M^2)_20
-                const int ii = (tid >> 3) & 15, cc = tid & 7;
-                put(M3, ii, cc, mm16_row2(Mb + 5 * MBLK, MS, M2 + 0 * MBLK, ii, cc));
+            if (tid < 64) {
+                const int ii = (tid >> 2) & 15, c4 = tid & 3;
+                put4(M3, ii, c4, mm16_row4(Mb + 5 * MBLK, MS, M2 + 0 * MBLK, MS, ii, c4));
             }
             __syncthreads();
-            for (int sl = tid; sl < 6 * 128; sl += kPrepThreads) {  // X_ab = (-M + M^2 - M^3)_ab X_bb
-                const int p_ = sl >> 7, ii = (sl >> 3) & 15, cc = sl & 7;
+            if (tid < 6 * 64) {  // X_ab = (-M + M^2 - M^3)_ab X_bb
+                const int p_ = tid >> 6, ii = (tid >> 2) & 15, c4 = tid & 3;
                 const int a = pair_a(p_), b = p_ - a * (a - 1) / 2;
-                const int p2 = (p_ == 1) ? 0 : (p_ == 4) ? 1 : (p_ == 3) ? 2 : -1;
-                float z[16];
+                float z[16], w[16];
                 row16(Mb + p_ * MBLK, MS, ii, z);
-                if (p2 >= 0) {
-                    float m2[16];
-                    row16(M2 + p2 * MBLK, MS, ii, m2);
 #pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) z[kk] = m2[kk] - z[kk];
-                } else {
+                for (int kk = 0; kk < 16; ++kk) z[kk] = -z[kk];
+                if (p_ == 1 || p_ == 4) {  // (2,0): M21 M10 ; (3,1): M32 M21
+                    row16(M2 + (p_ == 1 ? 0 : 1) * MBLK, MS, ii, w);
 #pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) z[kk] = -z[kk];
+                    for (int kk = 0; kk < 16; ++kk) z[kk] += w[kk];
                 }
-                if (p_ == 3) {
-                    float m3[16];
-                    row16(M3, MS, ii, m3);
+                if (p_ == 3) {  // (3,0): M31 M10 + M32 M20 - M32 M21 M10
+                    row16(M2 + 2 * MBLK, MS, ii, w);
 #pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) z[kk] -= m3[kk];
+                    for (int kk = 0; kk < 16; ++kk) z[kk] += w[kk];
+                    row16(M2 + 3 * MBLK, MS, ii, w);
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk) z[kk] += w[kk];
+                    row16(M3, MS, ii, w);
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk) z[kk] -= w[kk];
                 }
-                *reinterpret_cast<float2 *>(sX + (16 * a + ii) * C + 16 * b + 2 * cc) =
-                    row_times(z, XD + b * MBLK, cc);
+                *reinterpret_cast<float4 *>(sX + (16 * a + ii) * C + 16 * b + 4 * c4) =
+                    row4_times(z, XD + b * MBLK, c4);
             }
             __syncthreads();
             {  // T = X diag(beta), lower triangle, as K-major [i][j] bf16 hi + lo operands
@@ -664,6 +678,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
         __syncthreads();
     }
+    KDA_PHASE_FLUSH(0);
     if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
 }
 
@@ -672,7 +687,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
 // ---------------------------------------------------------------------------
 constexpr int kScanThreads = 128;
 constexpr int BV = 32;
-constexpr uint32_t kScanTmemCols = 64;
+constexpr uint32_t kScanTmemCols = 128;  // D1 double-buffered (2 x 32 columns), D3 (32)
 constexpr int kStages = 3;
 constexpr uint32_t kImageBytes = TcRec::U;                   // WQ | KDT | A | gC
 constexpr uint32_t kStageBytes = kImageBytes + TcRec::UBLK;  // + this CTA's U block
@@ -756,8 +771,28 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tD1 = tmem, tD3 = tmem + 32;
+    const uint32_t tD3 = tmem + 64;
     const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+
+    // Output rows of chunk ck (TMEM D1 buffer ck & 1, lanes 64..127) -> o.
+    // Runs in warps 2-3 while the next chunk's first MMA executes.
+    auto store_output = [&](int ck) {
+        float x[32];
+        tmem_ld32(tmem + 32 * (ck & 1) + lane_base, x);
+        tmem_ld_wait();
+        const int r = tid - 64;
+        if (r < min(C, len - ck * C)) {
+            const int64_t tok = (int64_t)start + (int64_t)ck * C + r;
+            uint4 *op = reinterpret_cast<uint4 *>(o + (tok * H + h) * (int64_t)D + v0);
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {
+                float y[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) y[t] = x[8 * c8 + t];
+                op[c8] = pack8(y);
+            }
+        }
+    };
 
     if (tid == 32) {
         for (int ck = 0; ck < kStages - 1 && ck < nck; ++ck) issue(ck);
@@ -767,25 +802,26 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     KDA_PHASE_START();
     for (int ck = 0; ck < nck; ++ck) {
         const int stage = ck % kStages;
+        const uint32_t fpar = (uint32_t)((ck / kStages) & 1);
         unsigned char *st = sm + stage * S_STAGE;
+        const uint32_t tD1 = tmem + 32 * (ck & 1);
         if (tid == 32 && ck + kStages - 1 < nck) issue(ck + kStages - 1);  // its stage was freed by ck-1
-        const int valid = min(C, len - ck * C);
-        const int64_t tok0 = (int64_t)start + (int64_t)ck * C;
         KDA_PHASE(1, 0);
-        ok = mbar_wait(&full[stage], (uint32_t)((ck / kStages) & 1)) && ok;
-        if (!__syncthreads_and(ok)) break;
-        KDA_PHASE(1, 1);
 
-        // D1 = WQ * S
+        // D1 = WQ * S  (only the issuing thread needs the stage before the MMA)
         if (tid == 0) {
+            ok = mbar_wait(&full[stage], fpar) && ok;
             tc_fence_after();
             mma_tile<128, BV, 128, 128, BV>(tD1, smem_u32(st + TcRec::WQ), smem_u32(sS), false);
             mma_commit(mbar);
         }
+        KDA_PHASE(1, 1);
+        if (ck > 0 && warp >= 2) store_output(ck - 1);
         KDA_PHASE(1, 2);
         ok = mbar_wait(mbar, mphase) && ok;
         mphase ^= 1;
         tc_fence_after();
+        if (tid != 0) ok = mbar_wait(&full[stage], fpar) && ok;  // U and gC of this stage
         KDA_PHASE(1, 3);
         if (warp < 2) {  // rows 0..63: Vn = U - W S
             float x[32], u[32];
@@ -806,7 +842,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         KDA_PHASE(1, 4);
         fence_async_smem();
         tc_fence_before();
-        if (!__syncthreads_and(ok)) break;
+        __syncthreads();
         KDA_PHASE(1, 5);
 
         // D1 += [* ; A] * Vn ;  D3 = KD^T * Vn
@@ -821,22 +857,6 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         mphase ^= 1;
         tc_fence_after();
         KDA_PHASE(1, 7);
-        if (warp >= 2) {  // rows 64..127: o
-            float x[32];
-            tmem_ld32(tD1 + lane_base, x);
-            tmem_ld_wait();
-            const int r = tid - 64;
-            if (r < valid) {
-                uint4 *op = reinterpret_cast<uint4 *>(o + ((tok0 + r) * H + h) * (int64_t)D + v0);
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    float y[8];
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) y[t] = x[8 * c8 + t];
-                    op[c8] = pack8(y);
-                }
-            }
-        }
         {  // S = diag(gC) S + KD^T Vn
             float x[32];
             tmem_ld32(tD3 + lane_base, x);
@@ -852,6 +872,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         if (!__syncthreads_and(ok)) break;
         KDA_PHASE(1, 9);
     }
+    if (ok && nck > 0 && warp >= 2) store_output(nck - 1);
     if (!ok) {
         if (tid == 32) {
             atomicOr(status, kStatusTimeout);
@@ -863,6 +884,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 #pragma unroll
         for (int x = 0; x < BV; ++x) final_state[st_off + (int64_t)(v0 + x) * D + tid] = S[x];
     }
+    KDA_PHASE_FLUSH(1);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kScanTmemCols);
