@@ -39,10 +39,10 @@
 //     D1  = WQ * S            (M=128, N=32, K=128)  rows 0..63: W S
 //     Vn  = U - D1[0:64]      (fp32, written as a bf16 K-major operand)
 //     D1 += [* ; A] * Vn      (rows 64..127 become o = QG S + A Vn)
-//     D3  = KD^T * Vn         (M=128, N=32, K=64)
+//     D3  = KD^T * Vn         (M=128, N=32, K=64; KD as an MN-major operand)
 //     S   = diag(gC) S + D3   (fp32, one key row per thread, in registers)
 //   The 128-row A operand of the second MMA starts 8 KB before the A tile in
-//   the staged record (its rows 0..63 are the tail of KD^T and only feed D1
+//   the staged record (its rows 0..63 are the tail of KD and only feed D1
 //   rows that were already consumed).  D1 is double-buffered in TMEM so that
 //   the output rows of a chunk are stored while the next chunk's first MMA
 //   runs; only the MMA-issuing thread waits for a stage before that MMA.
@@ -92,10 +92,6 @@ __device__ __forceinline__ void load8f(const float *p, float (&x)[8]) {
     x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
-__device__ __forceinline__ void store8f(float *p, const float (&x)[8]) {
-    *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
-    *reinterpret_cast<float4 *>(p + 4) = make_float4(x[4], x[5], x[6], x[7]);
-}
 
 // ---------------------------------------------------------------------------
 // prep
@@ -107,7 +103,7 @@ constexpr int NST = 16 * NPAIR;  // 160 = N of the stacked A/L MMA
 // shared memory plan (offsets from a 1024-aligned base)
 constexpr int R_Q = 0;          // bf16 [64][128]; after the A/L MMA: X fp32 [64][64]
 constexpr int R_K = 16384;      // bf16 [64][128]
-constexpr int R_V = 32768;      // bf16 [64][128]
+constexpr int R_V = 32768;      // bf16, two 128B-swizzled [64 rows][64] blocks (MN-major operand)
 constexpr int R_G = 49152;      // fp32 [64][128]: g -> G -> l
 constexpr int R_BYTES = 81920;
 constexpr int P_XL = R_BYTES;             // 32 KB: [q_hat l ; k_hat l] | L fp32 + scratch | E^T, V^T
@@ -120,10 +116,13 @@ constexpr int P_GREF = P_BETA + 256;      // fp32 [5][128]: G at rows 0, 16, 32,
 constexpr int P_RHO = P_GREF + 5 * 512;   // fp32 [4][128]: exp(G_16b)
 constexpr int P_TAU = P_RHO + 4 * 512;    // fp32 [6][128]: exp(G_16br - G_16b), br > b
 constexpr int P_QSUM = P_TAU + 6 * 512;   // fp32 [4][128]: per-quarter sums of g
-constexpr int P_BAR = P_QSUM + 4 * 512;   // full, mma barrier, tmem slot
+constexpr int P_PSI = P_QSUM + 4 * 512;   // fp32 [4][128]: exp(G_last - G_16b)
+constexpr int P_BAR = P_PSI + 4 * 512;    // full, mma barrier, tmem slot
 constexpr int P_BS2 = (P_BAR + 64 + 1023) / 1024 * 1024;  // 40 KB: low part of the stacked operand
-constexpr int P_BYTES = P_BS2 + 40960;
+constexpr int P_E = P_BS2 + 40960;        // 16 KB: E = k_hat exp(G), MN-major [j][d]
+constexpr int P_BYTES = P_E + 16384;
 constexpr int P_SMEM = P_BYTES + 1024;
+static_assert(P_SMEM <= 232448, "prep shared memory");
 constexpr int LSTRIDE = 68;               // row stride (floats) of L in shared memory
 constexpr int MS = 20;                    // row stride (floats) of 16x16 scratch matrices
 constexpr int MBLK = 16 * MS;             // floats per 16x16 scratch matrix
@@ -153,20 +152,29 @@ __device__ __forceinline__ PrepItem prep_item(int item, int H, const int32_t *ch
     return it;
 }
 
-// Raw rows of one (chunk, head) item: q, k, v ([T, H, 128] bf16) and g
-// ([T, H, 128] fp32) through 3-D tensor maps {128, H, T}; one 128 x 1 x 64
-// box each, rows past the end of the tensor arrive as zeros.
+// Raw tiles of one (chunk, head) item through 3-D tensor maps {128, H, T}
+// over the [T, H, 128] tensors: q, k (bf16) and g (fp32) as plain row-major
+// 128 x 1 x 64 boxes; v (bf16) as two 64 x 1 x 64 boxes with 128-byte
+// swizzle, i.e. already the MN-major operand layout of the U MMA.  Rows past
+// the end of the tensor arrive as zeros.  k and g are loaded as soon as the
+// previous item's row pass has consumed them, q and v after its last MMA.
 struct RawMaps {
     CUtensorMap q, k, v, g;
 };
 
-__device__ __forceinline__ void load_raw(unsigned char *buf, const RawMaps &m, int h, int64_t tok0,
-                                         uint64_t *bar) {
-    mbar_arrive_expect_tx(bar, (uint32_t)R_BYTES);
-    tma_load_3d(buf + R_Q, &m.q, 0, h, (int)tok0, bar);
+__device__ __forceinline__ void load_kg(unsigned char *buf, const RawMaps &m, int h, int64_t tok0,
+                                        uint64_t *bar) {
+    mbar_arrive_expect_tx(bar, 16384u + 32768u);
     tma_load_3d(buf + R_K, &m.k, 0, h, (int)tok0, bar);
-    tma_load_3d(buf + R_V, &m.v, 0, h, (int)tok0, bar);
     tma_load_3d(buf + R_G, &m.g, 0, h, (int)tok0, bar);
+}
+
+__device__ __forceinline__ void load_qv(unsigned char *buf, const RawMaps &m, int h, int64_t tok0,
+                                        uint64_t *bar) {
+    mbar_arrive_expect_tx(bar, 16384u + 16384u);
+    tma_load_3d(buf + R_Q, &m.q, 0, h, (int)tok0, bar);
+    tma_load_3d(buf + R_V, &m.v, 0, h, (int)tok0, bar);
+    tma_load_3d(buf + R_V + 8192, &m.v, 64, h, (int)tok0, bar);
 }
 
 // Row i of a 16x16 fp32 matrix (row stride lda floats, 16-byte aligned rows).
@@ -223,12 +231,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     float *sRho = reinterpret_cast<float *>(sm + P_RHO);
     float *sTau = reinterpret_cast<float *>(sm + P_TAU);
     float *sQsum = reinterpret_cast<float *>(sm + P_QSUM);
+    float *sPsi = reinterpret_cast<float *>(sm + P_PSI);
+    unsigned char *sE = sm + P_E;
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + P_BAR);
     uint64_t *mbar = full + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 1);
     const __nv_bfloat16 *sQr = reinterpret_cast<const __nv_bfloat16 *>(sm + R_Q);
     const __nv_bfloat16 *sKr = reinterpret_cast<const __nv_bfloat16 *>(sm + R_K);
-    const __nv_bfloat16 *sVr = reinterpret_cast<const __nv_bfloat16 *>(sm + R_V);
     float *sG = reinterpret_cast<float *>(sm + R_G);
     float *sX = reinterpret_cast<float *>(sm + R_Q);  // after the q rows are consumed
 
@@ -242,7 +251,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (warp == 0) tmem_alloc(tmem_slot, kPrepTmemCols);
     if (tid == 32) {
-        mbar_init(full, 1);
+        mbar_init(full, 2);  // two arrivals per item: the k/g half and the q/v half
         mbar_init(mbar, 1);
         fence_mbar_init();
     }
@@ -255,7 +264,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     // of the compute
     int item = blockIdx.x;
     PrepItem cur = prep_item(item, H, chunk_off, seq_start, seq_len, n_seqs);
-    if (tid == 0) load_raw(sm, maps, cur.h, cur.tok0, full);
+    if (tid == 0) {
+        load_kg(sm, maps, cur.h, cur.tok0, full);
+        load_qv(sm, maps, cur.h, cur.tok0, full);
+    }
     float beta_cur = tid < cur.valid ? beta[(cur.tok0 + tid) * H + cur.h] : 0.0f;
     PrepItem nxt = cur;
     if (item + (int)gridDim.x < n_items)
@@ -280,7 +292,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             const uint4 z = make_uint4(0, 0, 0, 0);
             *reinterpret_cast<uint4 *>(sm + R_Q + r * 256 + c16 * 16) = z;
             *reinterpret_cast<uint4 *>(sm + R_K + r * 256 + c16 * 16) = z;
-            *reinterpret_cast<uint4 *>(sm + R_V + r * 256 + c16 * 16) = z;
+            *reinterpret_cast<uint4 *>(sm + R_V + (c16 >> 3) * 8192 + r * 128 + (c16 & 7) * 16) = z;
             *reinterpret_cast<uint4 *>(sm + R_G + r * 512 + c16 * 32) = z;
             *reinterpret_cast<uint4 *>(sm + R_G + r * 512 + c16 * 32 + 16) = z;
         }
@@ -338,6 +350,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             const float gl = sG[(C - 1) * D + d];
             sGref[4 * D + d] = gl;
 #pragma unroll
+            for (int b = 0; b < 4; ++b) sPsi[b * D + d] = __expf(gl - gb[b]);
+#pragma unroll
             for (int br = 1; br < 4; ++br)
 #pragma unroll
                 for (int b = 0; b < br; ++b) sTau[tau_index(br, b) * D + d] = __expf(gb[br] - gb[b]);
@@ -346,22 +360,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         __syncthreads();
         KDA_PHASE(0, 1);
 
-        // 2. KD^T = (k_hat exp(G_last - G))^T, column chunks of 8 chunk rows.
-        for (int qi = tid; qi < 8 * D; qi += kPrepThreads) {
-            const int c8 = qi >> 7, d = qi & (D - 1);
-            const float gl = sGref[4 * D + d];
-            float x[8];
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const int r = 8 * c8 + t;
-                x[t] = __bfloat162float(sKr[r * D + d]) * sRk[r] * __expf(gl - sG[r * D + d]);
-            }
-            *reinterpret_cast<uint4 *>(rec + TcRec::KDT + sw128_off(d, 8 * c8, 128)) = pack8(x);
-        }
-        __syncthreads();
         KDA_PHASE(0, 2);
-        // 3. one pass per (row j, 8 channels): l = exp(G_j - G_16bj) (stored over
-        //    G), QG to the record, the row operand [q_hat l ; k_hat l], and the
+        // 3. one pass per (row j, 8 channels): l = exp(G_j - G_16bj), QG and KD to
+        //    the record, E, the row operand [q_hat l ; k_hat l], and the
         //    stacked column operand rows of j for every row block br >= bj:
         //    k_hat_j exp(G_16br - G_j) = k_hat_j tau(br, bj) / l_j, with 1 / l_j
         //    clamped at exp(80) on the block diagonal; where l_j < 1e-30 those
@@ -385,11 +386,26 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                 kl[t] = kh[t] * l8[t];
                 tiny |= l8[t] < 1e-30f;
                 inv[t] = __fdividef(1.0f, l8[t]);
-                qv[t] = ql[t] * rho8[t];  // QG = q_hat exp(G)
             }
-            *reinterpret_cast<uint4 *>(rec + TcRec::WQ + sw128_off(64 + r, d0, 128)) = pack8(qv);
+            {
+                float qg[8];  // QG = q_hat exp(G)
+#pragma unroll
+                for (int t = 0; t < 8; ++t) qg[t] = ql[t] * rho8[t];
+                *reinterpret_cast<uint4 *>(rec + TcRec::WQ + sw128_off(64 + r, d0, 128)) = pack8(qg);
+            }
             *reinterpret_cast<uint4 *>(sXL + sw128_off(r, d0, 128)) = pack8(ql);
             *reinterpret_cast<uint4 *>(sXL + sw128_off(64 + r, d0, 128)) = pack8(kl);
+            {  // E = k_hat exp(G) (MN-major [j][d] for W = T E) and KD = k_hat exp(G_last - G)
+                float ps8[8], e8[8], kd8[8];
+                load8f(sPsi + bj * D + d0, ps8);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    e8[t] = kl[t] * rho8[t];
+                    kd8[t] = tiny ? kh[t] * __expf(sGref[4 * D + d0 + t] - G8[t]) : kh[t] * ps8[t] * inv[t];
+                }
+                *reinterpret_cast<uint4 *>(sE + sw128_off(r, d0, 64)) = pack8(e8);
+                *reinterpret_cast<uint4 *>(rec + TcRec::KD + sw128_off(r, d0, 64)) = pack8(kd8);
+            }
             // hi + lo bf16 parts: the MMA sees this operand to ~16 bits
             auto emit = [&](int b2, const float (&y)[8]) {
                 const uint4 hi = pack8(y);
@@ -424,7 +440,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                     emit(b2, y);
                 }
             }
-            store8f(sG + r * D + d0, l8);
         }
         fence_async_smem();
         tc_fence_before();
@@ -436,6 +451,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             mma_tile<128, NST, 128, 128, NST>(tmem, smem_u32(sXL), smem_u32(sBS2), true);
             mma_commit(mbar);
         }
+        // the k and g tiles are consumed: the next item's k/g loads go out now
+        if (tid == 0 && has_next) load_kg(sm, maps, nxt.h, nxt.tok0, full);
         // global loads for later items, their latency hidden under the MMA
         if (has_next && tid < nxt.valid) beta_nxt = beta[(nxt.tok0 + tid) * H + nxt.h];
         if (item + 2 * (int)gridDim.x < n_items)
@@ -605,37 +622,28 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         __syncthreads();
         KDA_PHASE(0, 7);
 
-        // 6. E^T = (exp(G) k_hat)^T and V^T operands (in XL); then the raw tiles
-        //    are dead and the next item's loads go out; W = T E, U = T V.
-        for (int qi = tid; qi < 8 * D; qi += kPrepThreads) {
-            const int c8 = qi >> 7, d = qi & (D - 1);
-            const float rho = sRho[(c8 >> 1) * D + d];
-            float e[8], vv[8];
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const int j = 8 * c8 + t;
-                e[t] = __bfloat162float(sKr[j * D + d]) * sRk[j] * sG[j * D + d] * rho;
-                vv[t] = __bfloat162float(sVr[j * D + d]);
-            }
-            *reinterpret_cast<uint4 *>(sXL + sw128_off(d, 8 * c8, 128)) = pack8(e);
-            *reinterpret_cast<uint4 *>(sXL + 16384 + sw128_off(d, 8 * c8, 128)) = pack8(vv);
-        }
+        // 6. W = T E, U = T V (B operands MN-major: E from the row pass, V as
+        //    loaded); hi + lo parts of T.
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
         if (tid == 0) {
-            if (has_next) load_raw(sm, maps, nxt.h, nxt.tok0, full);
             tc_fence_after();
-            mma_tile<128, 128, 64, 128, 128>(tmem + 0, smem_u32(sT), smem_u32(sXL), false);
-            mma_tile<128, 128, 64, 128, 128>(tmem + 0, smem_u32(sT + 8192), smem_u32(sXL), true);
-            mma_tile<128, 128, 64, 128, 128>(tmem + 128, smem_u32(sT), smem_u32(sXL + 16384), false);
-            mma_tile<128, 128, 64, 128, 128>(tmem + 128, smem_u32(sT + 8192), smem_u32(sXL + 16384), true);
+            mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 0, smem_u32(sT), smem_u32(sE), false);
+            mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 0, smem_u32(sT + 8192), smem_u32(sE), true);
+            mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 128, smem_u32(sT), smem_u32(sm + R_V), false);
+            mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 128, smem_u32(sT + 8192), smem_u32(sm + R_V), true);
             mma_commit(mbar);
         }
         KDA_PHASE(0, 8);
         ok = mbar_wait(mbar, mphase) && ok;
         mphase ^= 1;
         tc_fence_after();
+        // q (inverse scratch) and v are consumed: the next item's q/v loads go out
+        if (tid == 0 && has_next) {
+            fence_async_smem();
+            load_qv(sm, maps, nxt.h, nxt.tok0, full);
+        }
         if (!__syncthreads_and(ok)) break;
 
         // 7. W rows (WQ rows 0..63) and U to the record: TMEM lanes 0..63.
@@ -689,7 +697,7 @@ constexpr int kScanThreads = 128;
 constexpr int BV = 32;
 constexpr uint32_t kScanTmemCols = 128;  // D1 double-buffered (2 x 32 columns), D3 (32)
 constexpr int kStages = 3;
-constexpr uint32_t kImageBytes = TcRec::U;                   // WQ | KDT | A | gC
+constexpr uint32_t kImageBytes = TcRec::U;                   // WQ | KD | A | gC
 constexpr uint32_t kStageBytes = kImageBytes + TcRec::UBLK;  // + this CTA's U block
 constexpr int S_STAGE = 62464;                               // kStageBytes rounded up to 1024
 constexpr int S_SOP = kStages * S_STAGE;                     // S^T operand [32][128] bf16, 8 KB
@@ -849,7 +857,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         if (tid == 0) {
             tc_fence_after();
             mma_tile<128, BV, 64, 128, BV>(tD1, smem_u32(st + TcRec::A) - 8192, smem_u32(sVn), true);
-            mma_tile<128, BV, 64, 128, BV>(tD3, smem_u32(st + TcRec::KDT), smem_u32(sVn), false);
+            mma_tile<128, BV, 64, 64, BV, true, false>(tD3, smem_u32(st + TcRec::KD), smem_u32(sVn), false);
             mma_commit(mbar);
         }
         KDA_PHASE(1, 6);
@@ -923,15 +931,16 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // 3-D map {128, H, T} over a [T, H, 128] tensor; box 128 x 1 x 64.
 bool encode_rows(CUtensorMap *m, const void *base, CUtensorMapDataType dt, size_t elem, int H,
-                 int64_t T) {
+                 int64_t T, bool swizzled64 = false) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
     const cuuint64_t strides[2] = {(cuuint64_t)(D * elem), (cuuint64_t)(D * elem) * (cuuint64_t)H};
-    const cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)C};
+    const cuuint32_t box[3] = {(cuuint32_t)(swizzled64 ? 64 : D), 1, (cuuint32_t)C};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_INTERLEAVE_NONE,
+               swizzled64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -948,7 +957,7 @@ cudaError_t launch_chunk_prep_tc(const void *q, const void *k, const void *v, co
     if (total_tokens > 0) {
         if (!encode_rows(&maps.q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, total_tokens) ||
             !encode_rows(&maps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, total_tokens) ||
-            !encode_rows(&maps.v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, total_tokens) ||
+            !encode_rows(&maps.v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, total_tokens, true) ||
             !encode_rows(&maps.g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, total_tokens))
             return cudaErrorInvalidValue;
     }

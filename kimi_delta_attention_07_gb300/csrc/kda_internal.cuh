@@ -101,19 +101,20 @@ struct F32Rec {
     static constexpr size_t bytes = floats * sizeof(float);
 };
 
-// bf16 tensor-core path: per (chunk, head) record.  WQ | KDT | A | gC is the
+// bf16 tensor-core path: per (chunk, head) record.  WQ | KD | A | gC is the
 // scan's shared-memory image of the chunk, in the 128-byte-swizzled K-major
 // operand layout; U follows, split in four 32-column blocks so that the scan
 // CTA of value block vb copies its 4 KB piece with one bulk copy.
 //   WQ  [128 rows][128 K] bf16: rows 0..63 W, rows 64..127 QG        32 KB
-//   KDT [128 rows (key)][64 K (chunk row)] bf16: KD^T                16 KB
+//   KD  [64 chunk rows][128 key] bf16, MN-major SW128 (two 64-key
+//       blocks of 64 rows x 128 B): the A operand KD^T of the state update 16 KB
 //   A   [64][64] bf16: causal scores (directly after KDT)             8 KB
 //   gC  [128] fp32: exp(G_last)
 //   U   [4 value blocks][64 rows][32] bf16                           16 KB
 struct TcRec {
     static constexpr uint32_t WQ = 0;
-    static constexpr uint32_t KDT = 32768;
-    static constexpr uint32_t A = KDT + 16384;
+    static constexpr uint32_t KD = 32768;
+    static constexpr uint32_t A = KD + 16384;
     static constexpr uint32_t GC = A + 8192;
     static constexpr uint32_t U = GC + 512;
     static constexpr uint32_t UBLK = 64 * 32 * 2;  // one 32-column block of U

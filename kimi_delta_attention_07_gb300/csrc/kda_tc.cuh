@@ -210,20 +210,34 @@ __device__ __forceinline__ uint32_t sw128_desc_lo(uint32_t saddr) {
     return ((saddr & 0x3FFFFu) >> 4) | (1u << 16);
 }
 
-// D[M x N] (+)= A[M x K] * B[N x K]^T, both operands K-major SW128 tiles with
-// AROWS / BROWS rows per K-block; issued by one thread.  The descriptors of
-// the K steps differ only in their low word (start address), by constants.
-template <int M, int N, int K, int AROWS, int BROWS>
+// Operands of mma_tile:
+//   K-major SW128: [rows][K] in K-blocks of 64 (see sw128_off); ROWS = rows of
+//     the tile; a K=16 step moves the start address by 32 bytes inside the
+//     swizzle atom (next K-block: +ROWS * 128 bytes).
+//   MN-major SW128: [K][MN] with MN split in 64-element blocks of K rows x 128
+//     bytes (the same byte formula as sw128_off(k, mn, K)); block stride
+//     (leading byte offset) = K * 128, 8-row groups 1024 bytes apart; a K=16
+//     step moves the start address by 2048 bytes.
+template <bool MN_MAJOR, int ROWS_OR_K>
+__device__ __forceinline__ uint32_t operand_lo(uint32_t saddr, int s) {
+    if (MN_MAJOR)
+        return (((saddr & 0x3FFFFu) >> 4) | ((uint32_t)((ROWS_OR_K * 128) >> 4) << 16)) + (uint32_t)(s * 128);
+    return sw128_desc_lo(saddr) + (uint32_t)((s >> 2) * ROWS_OR_K * 8 + (s & 3) * 2);
+}
+
+// D[M x N] (+)= A[M x K] * B[N x K]^T on SW128 tiles, issued by one thread.
+// AROWS / BROWS: rows of a K-major operand tile; for an MN-major operand
+// (A_MN / B_MN) pass K.  The descriptors of the K steps differ only in their
+// low word (start address), by constants.
+template <int M, int N, int K, int AROWS, int BROWS, bool A_MN = false, bool B_MN = false>
 __device__ __forceinline__ void mma_tile(uint32_t d_tmem, uint32_t a_saddr, uint32_t b_saddr,
                                          bool accumulate) {
-    constexpr uint32_t idesc = idesc_bf16(M, N);
-    const uint32_t alo = sw128_desc_lo(a_saddr), blo = sw128_desc_lo(b_saddr);
+    constexpr uint32_t idesc =
+        idesc_bf16(M, N) | (A_MN ? (1u << 15) : 0u) | (B_MN ? (1u << 16) : 0u);
 #pragma unroll
     for (int s = 0; s < K / 16; ++s) {
-        const uint32_t ka = (uint32_t)((s >> 2) * AROWS * 8 + (s & 3) * 2);
-        const uint32_t kb = (uint32_t)((s >> 2) * BROWS * 8 + (s & 3) * 2);
-        const uint64_t ad = ((uint64_t)kDescHi << 32) | (uint64_t)(alo + ka);
-        const uint64_t bd = ((uint64_t)kDescHi << 32) | (uint64_t)(blo + kb);
+        const uint64_t ad = ((uint64_t)kDescHi << 32) | (uint64_t)operand_lo<A_MN, AROWS>(a_saddr, s);
+        const uint64_t bd = ((uint64_t)kDescHi << 32) | (uint64_t)operand_lo<B_MN, BROWS>(b_saddr, s);
         mma_bf16(d_tmem, ad, bd, idesc, (accumulate || s > 0) ? 1u : 0u);
     }
 }
