@@ -30,7 +30,9 @@
 //     cancels.
 //   * W = T (exp(G) k_hat) and U = T v as M=128 x N=128 x K=64 MMAs whose A
 //     operand is [T ; scratch] (rows 64..127 unused), so each thread of
-//     TMEM lanes 0..63 holds whole rows of W and U.
+//     TMEM lanes 0..63 holds whole rows of W and U.  They sit in TMEM
+//     columns of their own and are written out while the next item's A/L
+//     MMA runs.
 //   * Record written with 16-byte stores, laid out as the scan's shared-
 //     memory image (128-byte-swizzled K-major operands), see TcRec.
 //
@@ -97,11 +99,12 @@ __device__ __forceinline__ void load8f(const float *p, float (&x)[8]) {
 // prep
 // ---------------------------------------------------------------------------
 constexpr int kPrepThreads = 512;
-constexpr uint32_t kPrepTmemCols = 256;
+constexpr int kLoader = 64;  // issues the TMA loads and the A/L MMA; its warp does no W/U readout
+constexpr uint32_t kPrepTmemCols = 256;  // A/L result 0..159; then W 0..127, U 128..255
 constexpr int NPAIR = 10;      // (row block br, column block b) pairs with br >= b
 constexpr int NST = 16 * NPAIR;  // 160 = N of the stacked A/L MMA
 // shared memory plan (offsets from a 1024-aligned base)
-constexpr int R_Q = 0;          // bf16 [64][128]; after the A/L MMA: X fp32 [64][64]
+constexpr int R_Q = 0;          // bf16 [64][128]
 constexpr int R_K = 16384;      // bf16 [64][128]
 constexpr int R_V = 32768;      // bf16, two 128B-swizzled [64 rows][64] blocks (MN-major operand)
 constexpr int R_G = 49152;      // fp32 [64][128]: g -> G -> l
@@ -117,7 +120,7 @@ constexpr int P_RHO = P_GREF + 5 * 512;   // fp32 [4][128]: exp(G_16b)
 constexpr int P_TAU = P_RHO + 4 * 512;    // fp32 [6][128]: exp(G_16br - G_16b), br > b
 constexpr int P_QSUM = P_TAU + 6 * 512;   // fp32 [4][128]: per-quarter sums of g
 constexpr int P_PSI = P_QSUM + 4 * 512;   // fp32 [4][128]: exp(G_last - G_16b)
-constexpr int P_BAR = P_PSI + 4 * 512;    // full, mma barrier, tmem slot
+constexpr int P_BAR = P_PSI + 4 * 512;    // q/k/g barrier, mma barrier, tmem slot, v barrier, metadata
 constexpr int P_BS2 = (P_BAR + 64 + 1023) / 1024 * 1024;  // 40 KB: low part of the stacked operand
 constexpr int P_E = P_BS2 + 40960;        // 16 KB: E = k_hat exp(G), MN-major [j][d]
 constexpr int P_BYTES = P_E + 16384;
@@ -139,6 +142,8 @@ struct PrepItem {
     int valid, h, c;
 };
 
+static_assert(32 + sizeof(PrepItem) <= 64, "barrier block");
+
 __device__ __forceinline__ PrepItem prep_item(int item, int H, const int32_t *chunk_off,
                                               const int32_t *seq_start, const int32_t *seq_len,
                                               int n_seqs) {
@@ -156,23 +161,23 @@ __device__ __forceinline__ PrepItem prep_item(int item, int H, const int32_t *ch
 // over the [T, H, 128] tensors: q, k (bf16) and g (fp32) as plain row-major
 // 128 x 1 x 64 boxes; v (bf16) as two 64 x 1 x 64 boxes with 128-byte
 // swizzle, i.e. already the MN-major operand layout of the U MMA.  Rows past
-// the end of the tensor arrive as zeros.  k and g are loaded as soon as the
-// previous item's row pass has consumed them, q and v after its last MMA.
+// the end of the tensor arrive as zeros.  q, k and g are loaded as soon as
+// the previous item's row pass has consumed them, v after its last MMA.
 struct RawMaps {
     CUtensorMap q, k, v, g;
 };
 
-__device__ __forceinline__ void load_kg(unsigned char *buf, const RawMaps &m, int h, int64_t tok0,
-                                        uint64_t *bar) {
-    mbar_arrive_expect_tx(bar, 16384u + 32768u);
+__device__ __forceinline__ void load_qkg(unsigned char *buf, const RawMaps &m, int h, int64_t tok0,
+                                         uint64_t *bar) {
+    mbar_arrive_expect_tx(bar, 16384u + 16384u + 32768u);
+    tma_load_3d(buf + R_Q, &m.q, 0, h, (int)tok0, bar);
     tma_load_3d(buf + R_K, &m.k, 0, h, (int)tok0, bar);
     tma_load_3d(buf + R_G, &m.g, 0, h, (int)tok0, bar);
 }
 
-__device__ __forceinline__ void load_qv(unsigned char *buf, const RawMaps &m, int h, int64_t tok0,
-                                        uint64_t *bar) {
-    mbar_arrive_expect_tx(bar, 16384u + 16384u);
-    tma_load_3d(buf + R_Q, &m.q, 0, h, (int)tok0, bar);
+__device__ __forceinline__ void load_v(unsigned char *buf, const RawMaps &m, int h, int64_t tok0,
+                                       uint64_t *bar) {
+    mbar_arrive_expect_tx(bar, 16384u);
     tma_load_3d(buf + R_V, &m.v, 0, h, (int)tok0, bar);
     tma_load_3d(buf + R_V + 8192, &m.v, 64, h, (int)tok0, bar);
 }
@@ -236,10 +241,12 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + P_BAR);
     uint64_t *mbar = full + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 1);
+    uint64_t *vfull = full + 3;
+    PrepItem *sNext = reinterpret_cast<PrepItem *>(sm + P_BAR + 32);  // metadata two items ahead
     const __nv_bfloat16 *sQr = reinterpret_cast<const __nv_bfloat16 *>(sm + R_Q);
     const __nv_bfloat16 *sKr = reinterpret_cast<const __nv_bfloat16 *>(sm + R_K);
     float *sG = reinterpret_cast<float *>(sm + R_G);
-    float *sX = reinterpret_cast<float *>(sm + R_Q);  // after the q rows are consumed
+    float *sX = reinterpret_cast<float *>(sm + P_BS2);  // X fp32 [64][64] once the A/L MMA is done
 
     const int32_t *chunk_off = ws_at<const int32_t>(workspace, L.chunk_off_off);
     const int32_t *seq_start = ws_at<const int32_t>(workspace, L.seq_start_off);
@@ -251,7 +258,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (warp == 0) tmem_alloc(tmem_slot, kPrepTmemCols);
     if (tid == 32) {
-        mbar_init(full, 2);  // two arrivals per item: the k/g half and the q/v half
+        mbar_init(full, 1);
+        mbar_init(vfull, 1);
         mbar_init(mbar, 1);
         fence_mbar_init();
     }
@@ -264,16 +272,19 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     // of the compute
     int item = blockIdx.x;
     PrepItem cur = prep_item(item, H, chunk_off, seq_start, seq_len, n_seqs);
-    if (tid == 0) {
-        load_kg(sm, maps, cur.h, cur.tok0, full);
-        load_qv(sm, maps, cur.h, cur.tok0, full);
+    if (tid == kLoader) {
+        load_qkg(sm, maps, cur.h, cur.tok0, full);
+        load_v(sm, maps, cur.h, cur.tok0, vfull);
     }
     float beta_cur = tid < cur.valid ? beta[(cur.tok0 + tid) * H + cur.h] : 0.0f;
     PrepItem nxt = cur;
     if (item + (int)gridDim.x < n_items)
         nxt = prep_item(item + gridDim.x, H, chunk_off, seq_start, seq_len, n_seqs);
 
-    uint32_t fphase = 0, mphase = 0;
+    // phases of the three barriers, and whether a phase is armed but not yet
+    // waited for (what must land before the shared memory is released)
+    uint32_t fphase = 0, vphase = 0, mphase = 0;
+    bool fpend = true, vpend = true, mpend = false;
     bool ok = true;
     KDA_PHASE_START();
     for (; item < n_items; item += gridDim.x) {
@@ -282,17 +293,19 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         const int valid = cur.valid;
         if (tid < C) sB[tid] = tid < valid ? beta_cur : 0.0f;
         float beta_nxt = 0.0f;
-        PrepItem nn = nxt;
 
-        ok = mbar_wait(full, fphase) && ok;
-        fphase ^= 1;
+        if (mbar_wait(full, fphase)) {
+            fphase ^= 1;
+            fpend = false;
+        } else {
+            ok = false;
+        }
         // rows past the end of the sequence: zero (the tensor map only zero-fills past T)
         for (int i = tid; i < (C - valid) * 16; i += kPrepThreads) {
             const int r = valid + i / 16, c16 = i % 16;
             const uint4 z = make_uint4(0, 0, 0, 0);
             *reinterpret_cast<uint4 *>(sm + R_Q + r * 256 + c16 * 16) = z;
             *reinterpret_cast<uint4 *>(sm + R_K + r * 256 + c16 * 16) = z;
-            *reinterpret_cast<uint4 *>(sm + R_V + (c16 >> 3) * 8192 + r * 128 + (c16 & 7) * 16) = z;
             *reinterpret_cast<uint4 *>(sm + R_G + r * 512 + c16 * 32) = z;
             *reinterpret_cast<uint4 *>(sm + R_G + r * 512 + c16 * 32 + 16) = z;
         }
@@ -357,6 +370,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                 for (int b = 0; b < br; ++b) sTau[tau_index(br, b) * D + d] = __expf(gb[br] - gb[b]);
             reinterpret_cast<float *>(rec + TcRec::GC)[d] = __expf(gl);
         }
+        if (tid == kLoader) bulk_wait_read();  // the previous item's W/U staging is read
         __syncthreads();
         KDA_PHASE(0, 1);
 
@@ -367,8 +381,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         //    k_hat_j exp(G_16br - G_j) = k_hat_j tau(br, bj) / l_j, with 1 / l_j
         //    clamped at exp(80) on the block diagonal; where l_j < 1e-30 those
         //    entries are taken as exponentials directly.
-        for (int qi = tid; qi < C * 16; qi += kPrepThreads) {
-            const int r = qi >> 4, d0 = (qi & 15) * 8, bj = r >> 4;
+        //    A thread takes rows r and 63 - r: five column blocks in total.
+#pragma unroll 1
+        for (int it = 0; it < 2; ++it) {
+            const int r = it == 0 ? (tid >> 4) : 63 - (tid >> 4), d0 = (tid & 15) * 8, bj = r >> 4;
             float G8[8], Gb8[8], rho8[8], qv[8], kv[8];
             load8f(sG + r * D + d0, G8);
             load8f(sGref + bj * D + d0, Gb8);
@@ -445,20 +461,30 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         tc_fence_before();
         __syncthreads();
         KDA_PHASE(0, 3);
-        if (tid == 0) {
+        if (tid == kLoader) {
             tc_fence_after();
             mma_tile<128, NST, 128, 128, NST>(tmem, smem_u32(sXL), smem_u32(sBS), false);
             mma_tile<128, NST, 128, 128, NST>(tmem, smem_u32(sXL), smem_u32(sBS2), true);
             mma_commit(mbar);
+            // the q, k and g tiles are consumed: the next item's loads go out now
+            if (has_next) load_qkg(sm, maps, nxt.h, nxt.tok0, full);
         }
-        // the k and g tiles are consumed: the next item's k/g loads go out now
-        if (tid == 0 && has_next) load_kg(sm, maps, nxt.h, nxt.tok0, full);
-        // global loads for later items, their latency hidden under the MMA
+        mpend = true;
+        fpend = has_next;
+        // global loads for later items, their latency hidden under the MMA:
+        // beta of the next item (used at its start), and the metadata of the
+        // item after it, fetched by one thread of a warp that does no TMEM
+        // readout (its dependent loads stall only that warp) and handed over
+        // in shared memory
         if (has_next && tid < nxt.valid) beta_nxt = beta[(nxt.tok0 + tid) * H + nxt.h];
-        if (item + 2 * (int)gridDim.x < n_items)
-            nn = prep_item(item + 2 * gridDim.x, H, chunk_off, seq_start, seq_len, n_seqs);
-        ok = mbar_wait(mbar, mphase) && ok;
-        mphase ^= 1;
+        if (tid == kPrepThreads - 32 && item + 2 * (int)gridDim.x < n_items)
+            *sNext = prep_item(item + 2 * gridDim.x, H, chunk_off, seq_start, seq_len, n_seqs);
+        if (mbar_wait(mbar, mphase)) {
+            mphase ^= 1;
+            mpend = false;
+        } else {
+            ok = false;
+        }
         tc_fence_after();
         if (!__syncthreads_and(ok)) break;
         KDA_PHASE(0, 4);
@@ -623,10 +649,22 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         KDA_PHASE(0, 7);
 
         // 6. W = T E, U = T V (B operands MN-major: E from the row pass, V as
-        //    loaded); hi + lo parts of T.
+        //    loaded); hi + lo parts of T.  The v tile was requested at the end
+        //    of the previous item; rows past the sequence end are zeroed.
+        if (mbar_wait(vfull, vphase)) {
+            vphase ^= 1;
+            vpend = false;
+        } else {
+            ok = false;
+        }
+        for (int i = tid; i < (C - valid) * 16; i += kPrepThreads) {
+            const int r = valid + i / 16, c16 = i % 16;
+            *reinterpret_cast<uint4 *>(sm + R_V + (c16 >> 3) * 8192 + r * 128 + (c16 & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+        }
         fence_async_smem();
         tc_fence_before();
-        __syncthreads();
+        if (!__syncthreads_and(ok)) break;
         if (tid == 0) {
             tc_fence_after();
             mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 0, smem_u32(sT), smem_u32(sE), false);
@@ -635,18 +673,26 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 128, smem_u32(sT + 8192), smem_u32(sm + R_V), true);
             mma_commit(mbar);
         }
+        mpend = true;
         KDA_PHASE(0, 8);
-        ok = mbar_wait(mbar, mphase) && ok;
-        mphase ^= 1;
-        tc_fence_after();
-        // q (inverse scratch) and v are consumed: the next item's q/v loads go out
-        if (tid == 0 && has_next) {
-            fence_async_smem();
-            load_qv(sm, maps, nxt.h, nxt.tok0, full);
+        if (mbar_wait(mbar, mphase)) {
+            mphase ^= 1;
+            mpend = false;
+        } else {
+            ok = false;
         }
-        if (!__syncthreads_and(ok)) break;
+        tc_fence_after();
+        // v is consumed: the next item's v load goes out
+        if (tid == kLoader && has_next) load_v(sm, maps, nxt.h, nxt.tok0, vfull);
+        vpend = has_next;
 
-        // 7. W rows (WQ rows 0..63) and U to the record: TMEM lanes 0..63.
+        // 7. W rows (WQ rows 0..63) and U: TMEM lanes 0..63 -> shared memory
+        //    (sXL, free since the T conversion) in the record's own layout ->
+        //    three bulk copies to the record.  U rows are stored with their
+        //    16-byte chunks rotated (chunk c of row i at c ^ ((i / 2) % 4)),
+        //    which keeps these writes and the scan's reads free of bank
+        //    conflicts.  The staging area is reused once the copies have read
+        //    it (checked before the next row pass).
         if ((warp & 3) < 2) {
             const int i = 32 * (warp & 3) + lane, part = warp >> 2;
             const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
@@ -658,31 +704,42 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                 float y[8];
 #pragma unroll
                 for (int t = 0; t < 8; ++t) y[t] = x[8 * c8 + t];
-                *reinterpret_cast<uint4 *>(rec + TcRec::WQ + sw128_off(i, 32 * part + 8 * c8, 128)) = pack8(y);
+                *reinterpret_cast<uint4 *>(sXL + sw128_off(i, 32 * part + 8 * c8, 64)) = pack8(y);
             }
             tmem_ld32(ta + 128 + 32 * part, x);
             tmem_ld_wait();
-            unsigned char *ub = rec + TcRec::U + part * TcRec::UBLK + i * 64;
+            unsigned char *ub = sXL + 16384 + part * TcRec::UBLK + i * 64;
 #pragma unroll
             for (int c8 = 0; c8 < 4; ++c8) {
                 float y[8];
 #pragma unroll
                 for (int t = 0; t < 8; ++t) y[t] = x[8 * c8 + t];
-                *reinterpret_cast<uint4 *>(ub + 16 * c8) = pack8(y);
+                *reinterpret_cast<uint4 *>(ub + ((c8 ^ ((i >> 1) & 3)) << 4)) = pack8(y);
             }
         }
+        fence_async_smem();
         tc_fence_before();
-        __syncthreads();
+        if (!__syncthreads_and(ok)) break;
+        if (tid == kLoader) {
+            bulk_s2g(rec + TcRec::WQ, sXL, 8192);                  // W, key columns 0..63
+            bulk_s2g(rec + TcRec::WQ + 16384, sXL + 8192, 8192);   // W, key columns 64..127
+            bulk_s2g(rec + TcRec::U, sXL + 16384, 4 * TcRec::UBLK);
+            bulk_commit();
+        }
         KDA_PHASE(0, 9);
         cur = nxt;
-        nxt = nn;
+        if (item + 2 * (int)gridDim.x < n_items) nxt = *sNext;
         beta_cur = beta_nxt;
     }
+    if (tid == kLoader) bulk_wait_all();  // the last record's W and U are written
     if (!ok) {
-        if (tid == 0) {
+        if (tid == kLoader) {
             atomicOr(status, kStatusTimeout);
-            // let a copy still in flight land before the shared memory is released
-            mbar_wait(full, fphase, 400000000LL);
+            // let copies and MMAs still in flight land before the shared memory
+            // and the TMEM are released
+            if (fpend) mbar_wait(full, fphase, 400000000LL);
+            if (vpend) mbar_wait(vfull, vphase, 400000000LL);
+            if (mpend) mbar_wait(mbar, mphase, 400000000LL);
         }
         __syncthreads();
     }
@@ -838,7 +895,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 #pragma unroll
             for (int c8 = 0; c8 < 4; ++c8) {
                 float y[8];
-                unpack8(up[c8], y);
+                unpack8(up[c8 ^ ((tid >> 1) & 3)], y);
 #pragma unroll
                 for (int t = 0; t < 8; ++t) u[8 * c8 + t] = y[t];
             }

@@ -110,7 +110,8 @@ struct F32Rec {
 //       blocks of 64 rows x 128 B): the A operand KD^T of the state update 16 KB
 //   A   [64][64] bf16: causal scores (directly after KDT)             8 KB
 //   gC  [128] fp32: exp(G_last)
-//   U   [4 value blocks][64 rows][32] bf16                           16 KB
+//   U   [4 value blocks][64 rows][32] bf16; the four 16-byte chunks   16 KB
+//       of row i rotated: chunk c at position c ^ ((i / 2) % 4)
 struct TcRec {
     static constexpr uint32_t WQ = 0;
     static constexpr uint32_t KD = 32768;

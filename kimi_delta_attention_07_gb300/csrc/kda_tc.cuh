@@ -93,6 +93,25 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// ---- bulk copy (shared -> global, bulk-group completion) -----------------------
+// dst, src 16-byte aligned; bytes a multiple of 16.  The issuing thread tracks
+// completion: bulk_wait_read() returns once every committed copy has read its
+// shared-memory source, bulk_wait_all() once the writes are done.
+__device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // ---- TMA tensor copy (3-D tile, global -> shared, completes on an mbarrier) ----------
 // tmap: generic address of a CUtensorMap kernel parameter; c0 (innermost) must
 // keep the copied row 16-byte aligned (here always 0).
