@@ -87,14 +87,6 @@ __device__ __forceinline__ void unpack8(uint4 raw, float (&x)[8]) {
     }
 }
 
-__device__ __forceinline__ void load8f(const float *p, float (&x)[8]) {
-    const float4 a = *reinterpret_cast<const float4 *>(p);
-    const float4 b = *reinterpret_cast<const float4 *>(p + 4);
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
-
-
 // ---------------------------------------------------------------------------
 // prep
 // ---------------------------------------------------------------------------
@@ -112,15 +104,16 @@ constexpr int R_BYTES = 81920;
 constexpr int P_XL = R_BYTES;             // 32 KB: [q_hat l ; k_hat l] | L fp32 + scratch | E^T, V^T
 constexpr int P_BS = P_XL + 32768;        // 40 KB: stacked column operand | inverse scratch, T
 constexpr int P_T = P_BS + 16384;         // T operand [64][64] bf16; the MMA reads 16 KB from here
-constexpr int P_RQ = P_BS + 40960;        // fp32 [64]
-constexpr int P_RK = P_RQ + 256;          // fp32 [64]
+constexpr int P_RQ = P_BS + 40960;        // fp32 [64]: scale / |q_r|
+constexpr int P_RK = P_RQ + 256;          // fp32 [64]: 1 / |k_r|
 constexpr int P_BETA = P_RK + 256;        // fp32 [64]
 constexpr int P_GREF = P_BETA + 256;      // fp32 [5][128]: G at rows 0, 16, 32, 48, 63
 constexpr int P_RHO = P_GREF + 5 * 512;   // fp32 [4][128]: exp(G_16b)
 constexpr int P_TAU = P_RHO + 4 * 512;    // fp32 [6][128]: exp(G_16br - G_16b), br > b
 constexpr int P_QSUM = P_TAU + 6 * 512;   // fp32 [4][128]: per-quarter sums of g
 constexpr int P_PSI = P_QSUM + 4 * 512;   // fp32 [4][128]: exp(G_last - G_16b)
-constexpr int P_BAR = P_PSI + 4 * 512;    // q/k/g barrier, mma barrier, tmem slot, v barrier, metadata
+constexpr int P_FIRST = P_PSI + 4 * 512;  // fp32 [4][128]: g at rows 0, 16, 32, 48
+constexpr int P_BAR = P_FIRST + 4 * 512;    // q/k/g barrier, mma barrier, tmem slot, v barrier, metadata
 constexpr int P_BS2 = (P_BAR + 64 + 1023) / 1024 * 1024;  // 40 KB: low part of the stacked operand
 constexpr int P_E = P_BS2 + 40960;        // 16 KB: E = k_hat exp(G), MN-major [j][d]
 constexpr int P_BYTES = P_E + 16384;
@@ -130,8 +123,8 @@ constexpr int LSTRIDE = 68;               // row stride (floats) of L in shared 
 constexpr int MS = 20;                    // row stride (floats) of 16x16 scratch matrices
 constexpr int MBLK = 16 * MS;             // floats per 16x16 scratch matrix
 static_assert(P_T + 8192 + 16384 <= P_BS + 40960, "T_hi / T_lo operand windows");
-static_assert(3 * 4 * MBLK * 4 <= P_T - P_BS, "inverse scratch vs T");
-static_assert(C * LSTRIDE * 4 + 4 * MBLK * 4 + 6 * MBLK * 4 <= 32768, "XL scratch");
+static_assert(12 * MBLK * 4 <= P_T - P_BS, "inverse scratch vs T");
+static_assert(C * LSTRIDE * 4 + 2 * MBLK * 4 <= 32768, "XL scratch");
 
 __device__ __forceinline__ int tau_index(int br, int b) { return br * (br - 1) / 2 + b; }
 // first column of row block br in the stacked A/L result (pairs (br, 0..br) are consecutive)
@@ -182,6 +175,20 @@ __device__ __forceinline__ void load_v(unsigned char *buf, const RawMaps &m, int
     tma_load_3d(buf + R_V + 8192, &m.v, 64, h, (int)tok0, bar);
 }
 
+// fp32 [rows][128] arrays that are read 8 channels per lane (16 lanes per
+// row): channel d is stored at swz(d), i.e. float4 unit u of a row at
+// u ^ ((u / 8) % 2), so that each group of 8 lanes covers all 32 banks.
+__device__ __forceinline__ int swz(int d) { return d ^ (((d >> 5) & 1) << 2); }
+
+// channels d0 .. d0+7 (d0 a multiple of 8) of a swizzled row
+__device__ __forceinline__ void load8s(const float *row, int d0, float (&x)[8]) {
+    const int f = ((d0 >> 5) & 1) << 2;
+    const float4 a = *reinterpret_cast<const float4 *>(row + (d0 ^ f));
+    const float4 b = *reinterpret_cast<const float4 *>(row + ((d0 + 4) ^ f));
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
 // Row i of a 16x16 fp32 matrix (row stride lda floats, 16-byte aligned rows).
 __device__ __forceinline__ void row16(const float *A, int lda, int i, float (&a)[16]) {
 #pragma unroll
@@ -229,14 +236,15 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     unsigned char *sBS = sm + P_BS;
     unsigned char *sT = sm + P_T;          // T_hi; T_lo follows 8 KB later
     unsigned char *sBS2 = sm + P_BS2;
-    float *sRq = reinterpret_cast<float *>(sm + P_RQ);
-    float *sRk = reinterpret_cast<float *>(sm + P_RK);
     float *sB = reinterpret_cast<float *>(sm + P_BETA);
     float *sGref = reinterpret_cast<float *>(sm + P_GREF);
     float *sRho = reinterpret_cast<float *>(sm + P_RHO);
     float *sTau = reinterpret_cast<float *>(sm + P_TAU);
     float *sQsum = reinterpret_cast<float *>(sm + P_QSUM);
     float *sPsi = reinterpret_cast<float *>(sm + P_PSI);
+    float *sRq = reinterpret_cast<float *>(sm + P_RQ);
+    float *sRk = reinterpret_cast<float *>(sm + P_RK);
+    float *sFirst = reinterpret_cast<float *>(sm + P_FIRST);
     unsigned char *sE = sm + P_E;
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + P_BAR);
     uint64_t *mbar = full + 1;
@@ -245,8 +253,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     PrepItem *sNext = reinterpret_cast<PrepItem *>(sm + P_BAR + 32);  // metadata two items ahead
     const __nv_bfloat16 *sQr = reinterpret_cast<const __nv_bfloat16 *>(sm + R_Q);
     const __nv_bfloat16 *sKr = reinterpret_cast<const __nv_bfloat16 *>(sm + R_K);
-    float *sG = reinterpret_cast<float *>(sm + R_G);
-    float *sX = reinterpret_cast<float *>(sm + P_BS2);  // X fp32 [64][64] once the A/L MMA is done
+    float *sG = reinterpret_cast<float *>(sm + R_G);  // g -> G_r - G_16b
 
     const int32_t *chunk_off = ws_at<const int32_t>(workspace, L.chunk_off_off);
     const int32_t *seq_start = ws_at<const int32_t>(workspace, L.seq_start_off);
@@ -312,72 +319,55 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         if (!__syncthreads_and(ok)) break;
         KDA_PHASE(0, 0);
 
-        // 1. row norms of q and k (16 lanes per row, 8 channels each) and the
-        //    cumulative log-decay (4 row quarters per channel, then offsets).
-#pragma unroll
-        for (int it = 0; it < 2; ++it) {
-            const int r = 32 * it + (tid >> 4), c16 = tid & 15;
-            float a[8], b[8];
-            unpack8(*reinterpret_cast<const uint4 *>(sQr + r * D + 8 * c16), a);
-            unpack8(*reinterpret_cast<const uint4 *>(sKr + r * D + 8 * c16), b);
-            float sq = 0.f, sk = 0.f;
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                sq = fmaf(a[t], a[t], sq);
-                sk = fmaf(b[t], b[t], sk);
-            }
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) {
-                sq += __shfl_xor_sync(0xffffffffu, sq, o);
-                sk += __shfl_xor_sync(0xffffffffu, sk, o);
-            }
-            if (c16 == 0) {
-                sRq[r] = scale / sqrtf(sq + 1e-6f);
-                sRk[r] = 1.0f / sqrtf(sk + 1e-6f);
-            }
-        }
+        // 1. cumulative log-decay, one key channel and one 16-row block per
+        //    thread: sG receives G_r - G_16b (b = r's block, so <= 0); the
+        //    block sums and first-row values then give every reference
+        //    quantity of the thread's block: G_16b, rho_b = exp(G_16b),
+        //    psi_b = exp(G_last - G_16b), tau(b, b') = exp(G_16b - G_16b'),
+        //    b' < b, and gC = exp(G_last).
         {
             const int d = tid & (D - 1), qtr = tid >> 7, r0 = 16 * qtr;
             float x[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] = sG[(r0 + i) * D + d];
+            for (int i = 0; i < 16; ++i) x[i] = sG[(r0 + i) * D + d];  // g, plain layout
 #pragma unroll
             for (int i = 1; i < 16; ++i) x[i] += x[i - 1];
             sQsum[qtr * D + d] = x[15];
-            __syncthreads();
-            float off = 0.0f;
-            for (int q2 = 0; q2 < qtr; ++q2) off += sQsum[q2 * D + d];
+            sFirst[qtr * D + d] = x[0];
+            const int ds = swz(d);  // a lane of this warp: its column was read above
+            __syncwarp();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) sG[(r0 + i) * D + d] = x[i] + off;
-        }
-        __syncthreads();
-        if (tid < D) {  // reference rows and block factors, one key channel each
-            const int d = tid;
-            float gb[4];
+            for (int i = 0; i < 16; ++i) sG[(r0 + i) * D + ds] = x[i] - x[0];
+            __syncthreads();
+            float off = 0.0f, gl = 0.0f, gfirst[3];  // gfirst[b] = G_16b, b < qtr
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
-                gb[b] = sG[16 * b * D + d];
-                sGref[b * D + d] = gb[b];
-                sRho[b * D + d] = __expf(gb[b]);
+                const float qs = sQsum[b * D + d];
+                if (b < qtr) {
+                    gfirst[b] = off + sFirst[b * D + d];
+                    off += qs;
+                }
+                gl += qs;
             }
-            const float gl = sG[(C - 1) * D + d];
-            sGref[4 * D + d] = gl;
+            const float gb = off + x[0];
 #pragma unroll
-            for (int b = 0; b < 4; ++b) sPsi[b * D + d] = __expf(gl - gb[b]);
-#pragma unroll
-            for (int br = 1; br < 4; ++br)
-#pragma unroll
-                for (int b = 0; b < br; ++b) sTau[tau_index(br, b) * D + d] = __expf(gb[br] - gb[b]);
-            reinterpret_cast<float *>(rec + TcRec::GC)[d] = __expf(gl);
+            for (int b = 0; b < 3; ++b)
+                if (b < qtr) sTau[tau_index(qtr, b) * D + ds] = __expf(gb - gfirst[b]);
+            sGref[qtr * D + ds] = gb;
+            sRho[qtr * D + ds] = __expf(gb);
+            sPsi[qtr * D + ds] = __expf(gl - gb);
+            if (qtr == 3) {
+                sGref[4 * D + ds] = gl;
+                reinterpret_cast<float *>(rec + TcRec::GC)[d] = __expf(gl);
+            }
         }
         if (tid == kLoader) bulk_wait_read();  // the previous item's W/U staging is read
         __syncthreads();
         KDA_PHASE(0, 1);
-
-        KDA_PHASE(0, 2);
-        // 3. one pass per (row j, 8 channels): l = exp(G_j - G_16bj), QG and KD to
-        //    the record, E, the row operand [q_hat l ; k_hat l], and the
-        //    stacked column operand rows of j for every row block br >= bj:
+        // 2. the operands of the A/L MMA, one pass per (row j, 8 channels):
+        //    the row norms of q and k (16 lanes per row), l = exp(G_j - G_16bj),
+        //    the row operand [q_hat l ; k_hat l], and the stacked column
+        //    operand rows of j for every row block br >= bj:
         //    k_hat_j exp(G_16br - G_j) = k_hat_j tau(br, bj) / l_j, with 1 / l_j
         //    clamped at exp(80) on the block diagonal; where l_j < 1e-30 those
         //    entries are taken as exponentials directly.
@@ -385,43 +375,39 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
 #pragma unroll 1
         for (int it = 0; it < 2; ++it) {
             const int r = it == 0 ? (tid >> 4) : 63 - (tid >> 4), d0 = (tid & 15) * 8, bj = r >> 4;
-            float G8[8], Gb8[8], rho8[8], qv[8], kv[8];
-            load8f(sG + r * D + d0, G8);
-            load8f(sGref + bj * D + d0, Gb8);
-            load8f(sRho + bj * D + d0, rho8);
+            float rel8[8], qv[8], kv[8];
+            load8s(sG + r * D, d0, rel8);
             unpack8(*reinterpret_cast<const uint4 *>(sQr + r * D + d0), qv);
             unpack8(*reinterpret_cast<const uint4 *>(sKr + r * D + d0), kv);
-            const float rq = sRq[r], rk = sRk[r];
+            float sq = 0.f, sk = 0.f;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                sq = fmaf(qv[t], qv[t], sq);
+                sk = fmaf(kv[t], kv[t], sk);
+            }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) {  // the 16 lanes of row r
+                sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            }
+            const float rq = scale * rsqrtf(sq + 1e-6f), rk = rsqrtf(sk + 1e-6f);
+            if ((tid & 15) == 0) {
+                sRq[r] = rq;
+                sRk[r] = rk;
+            }
             float ql[8], kl[8], l8[8], inv[8], kh[8];
             bool tiny = false;
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
-                l8[t] = __expf(G8[t] - Gb8[t]);
+                l8[t] = __expf(rel8[t]);
                 kh[t] = kv[t] * rk;
                 ql[t] = qv[t] * rq * l8[t];
                 kl[t] = kh[t] * l8[t];
                 tiny |= l8[t] < 1e-30f;
                 inv[t] = __fdividef(1.0f, l8[t]);
             }
-            {
-                float qg[8];  // QG = q_hat exp(G)
-#pragma unroll
-                for (int t = 0; t < 8; ++t) qg[t] = ql[t] * rho8[t];
-                *reinterpret_cast<uint4 *>(rec + TcRec::WQ + sw128_off(64 + r, d0, 128)) = pack8(qg);
-            }
             *reinterpret_cast<uint4 *>(sXL + sw128_off(r, d0, 128)) = pack8(ql);
             *reinterpret_cast<uint4 *>(sXL + sw128_off(64 + r, d0, 128)) = pack8(kl);
-            {  // E = k_hat exp(G) (MN-major [j][d] for W = T E) and KD = k_hat exp(G_last - G)
-                float ps8[8], e8[8], kd8[8];
-                load8f(sPsi + bj * D + d0, ps8);
-#pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    e8[t] = kl[t] * rho8[t];
-                    kd8[t] = tiny ? kh[t] * __expf(sGref[4 * D + d0 + t] - G8[t]) : kh[t] * ps8[t] * inv[t];
-                }
-                *reinterpret_cast<uint4 *>(sE + sw128_off(r, d0, 64)) = pack8(e8);
-                *reinterpret_cast<uint4 *>(rec + TcRec::KD + sw128_off(r, d0, 64)) = pack8(kd8);
-            }
             // hi + lo bf16 parts: the MMA sees this operand to ~16 bits
             auto emit = [&](int b2, const float (&y)[8]) {
                 const uint4 hi = pack8(y);
@@ -440,7 +426,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                 emit(bj, y);
                 for (int b2 = bj + 1; b2 < 4; ++b2) {
                     float t8[8];
-                    load8f(sTau + tau_index(b2, bj) * D + d0, t8);
+                    load8s(sTau + tau_index(b2, bj) * D, d0, t8);
 #pragma unroll
                     for (int t = 0; t < 8; ++t) y[t] = kh[t] * t8[t] * inv[t];
                     emit(b2, y);
@@ -448,11 +434,12 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             } else {  // a decay of more than ~69 inside this 16-row block
                 float y[8];
 #pragma unroll
-                for (int t = 0; t < 8; ++t) y[t] = kh[t] * __expf(fminf(Gb8[t] - G8[t], 80.0f));
+                for (int t = 0; t < 8; ++t) y[t] = kh[t] * __expf(fminf(-rel8[t], 80.0f));
                 emit(bj, y);
                 for (int b2 = bj + 1; b2 < 4; ++b2) {
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) y[t] = kh[t] * __expf(sGref[b2 * D + d0 + t] - G8[t]);
+                    for (int t = 0; t < 8; ++t)
+                        y[t] = kh[t] * __expf(sGref[b2 * D + swz(d0 + t)] - sGref[bj * D + swz(d0 + t)] - rel8[t]);
                     emit(b2, y);
                 }
             }
@@ -466,11 +453,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             mma_tile<128, NST, 128, 128, NST>(tmem, smem_u32(sXL), smem_u32(sBS), false);
             mma_tile<128, NST, 128, 128, NST>(tmem, smem_u32(sXL), smem_u32(sBS2), true);
             mma_commit(mbar);
-            // the q, k and g tiles are consumed: the next item's loads go out now
-            if (has_next) load_qkg(sm, maps, nxt.h, nxt.tok0, full);
         }
         mpend = true;
-        fpend = has_next;
         // global loads for later items, their latency hidden under the MMA:
         // beta of the next item (used at its start), and the metadata of the
         // item after it, fetched by one thread of a warp that does no TMEM
@@ -479,6 +463,41 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         if (has_next && tid < nxt.valid) beta_nxt = beta[(nxt.tok0 + tid) * H + nxt.h];
         if (tid == kPrepThreads - 32 && item + 2 * (int)gridDim.x < n_items)
             *sNext = prep_item(item + 2 * gridDim.x, H, chunk_off, seq_start, seq_len, n_seqs);
+
+        // While the MMA runs: QG = q_hat exp(G) and KD = k_hat exp(G_last - G)
+        // to the record, E = k_hat exp(G) (MN-major [j][d], for W = T E).
+#pragma unroll 1
+        for (int it = 0; it < 2; ++it) {
+            const int r = 32 * it + (tid >> 4), d0 = (tid & 15) * 8, bj = r >> 4;
+            float rel8[8], rho8[8], ps8[8], qv[8], kv[8];
+            load8s(sG + r * D, d0, rel8);
+            load8s(sRho + bj * D, d0, rho8);
+            load8s(sPsi + bj * D, d0, ps8);
+            unpack8(*reinterpret_cast<const uint4 *>(sQr + r * D + d0), qv);
+            unpack8(*reinterpret_cast<const uint4 *>(sKr + r * D + d0), kv);
+            const float rq = sRq[r], rk = sRk[r];
+            float qg[8], e8[8], kd8[8], kh[8], l8[8];
+            bool tiny = false;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                l8[t] = __expf(rel8[t]);
+                kh[t] = kv[t] * rk;
+                qg[t] = qv[t] * rq * l8[t] * rho8[t];
+                e8[t] = kh[t] * l8[t] * rho8[t];
+                tiny |= l8[t] < 1e-30f;
+            }
+            if (!__builtin_expect(tiny, 0)) {
+#pragma unroll
+                for (int t = 0; t < 8; ++t) kd8[t] = kh[t] * ps8[t] * __fdividef(1.0f, l8[t]);
+            } else {  // exp(G_last - G) directly where 1 / l would overflow
+#pragma unroll
+                for (int t = 0; t < 8; ++t)
+                    kd8[t] = kh[t] * __expf(sGref[4 * D + swz(d0 + t)] - sGref[bj * D + swz(d0 + t)] - rel8[t]);
+            }
+            *reinterpret_cast<uint4 *>(rec + TcRec::WQ + sw128_off(64 + r, d0, 128)) = pack8(qg);
+            *reinterpret_cast<uint4 *>(sE + sw128_off(r, d0, 64)) = pack8(e8);
+            *reinterpret_cast<uint4 *>(rec + TcRec::KD + sw128_off(r, d0, 64)) = pack8(kd8);
+        }
         if (mbar_wait(mbar, mphase)) {
             mphase ^= 1;
             mpend = false;
@@ -487,36 +506,33 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
         tc_fence_after();
         if (!__syncthreads_and(ok)) break;
+        // the q, k and g tiles are consumed: the next item's loads go out now
+        if (tid == kLoader && has_next) load_qkg(sm, maps, nxt.h, nxt.tok0, full);
+        fpend = has_next;
         KDA_PHASE(0, 4);
 
-        // 4. A rows (TMEM lanes 0..63) to the record, beta-scaled L rows
-        //    (lanes 64..127) to shared fp32.  Row r of block br finds column j
-        //    of its block pairs at TMEM column pair_col0(br) + j.
+        // 3. beta-scaled L rows (TMEM lanes 64..127) to shared fp32 by the
+        //    warps of lane quarters 2-3; A rows (lanes 0..63) to the record by
+        //    warps 4, 5, 8, 9, 12, 13, while the inverse starts as soon as L
+        //    is in place.  Row r of block br finds column j of its block pairs
+        //    at TMEM column pair_col0(br) + j.
         {
             float *sL = reinterpret_cast<float *>(sXL);
-            const int quarter = warp & 3, part = warp >> 2;
+            const int quarter = warp & 3;
             const int r = 32 * (quarter & 1) + lane;  // row inside A (quarters 0,1) or L (2,3)
             const int br = r >> 4;
             const bool lo_pair = (quarter & 1) == 0;  // rows of blocks 0,1: columns [0, 48)
             const int ntile = lo_pair ? 3 : 7;
             const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16);
-            for (int tile = part; tile < ntile; tile += 4) {
-                const int c0 = (lo_pair ? 0 : 48) + 16 * tile;
-                float x[16];
-                tmem_ld16(ta + c0, x);
-                tmem_ld_wait();
-                const int j0 = c0 - pair_col0(br);
-                if (j0 < 0 || j0 >= 16 * (br + 1)) continue;
-                if (quarter < 2) {
-#pragma unroll
-                    for (int h8 = 0; h8 < 2; ++h8) {
-                        float y[8];
-#pragma unroll
-                        for (int t = 0; t < 8; ++t) y[t] = (j0 + 8 * h8 + t <= r) ? x[8 * h8 + t] : 0.0f;
-                        *reinterpret_cast<uint4 *>(rec + TcRec::A + sw128_off(r, j0 + 8 * h8, 64)) = pack8(y);
-                    }
-                } else {
-                    const float bet = sB[r];
+            if (quarter >= 2) {
+                const float bet = sB[r];
+                for (int tile = warp >> 2; tile < ntile; tile += 4) {
+                    const int c0 = (lo_pair ? 0 : 48) + 16 * tile;
+                    float x[16];
+                    tmem_ld16(ta + c0, x);
+                    tmem_ld_wait();
+                    const int j0 = c0 - pair_col0(br);
+                    if (j0 < 0 || j0 >= 16 * (br + 1)) continue;
 #pragma unroll
                     for (int c4 = 0; c4 < 4; ++c4) {
                         const int j = j0 + 4 * c4;
@@ -528,38 +544,87 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                         *reinterpret_cast<float4 *>(sL + r * LSTRIDE + j) = y;
                     }
                 }
-            }
-            // A entries right of a row's block diagonal are zero
-            {
-                const int ra = tid >> 3, c8 = tid & 7;
-                if (c8 >= 2 * ((ra >> 4) + 1))
-                    *reinterpret_cast<uint4 *>(rec + TcRec::A + sw128_off(ra, 8 * c8, 64)) = make_uint4(0, 0, 0, 0);
+                tc_fence_before();
+                named_bar_sync(1, 320);
+            } else if (warp < 2) {
+                named_bar_sync(1, 320);
+            } else {
+                const int part = (warp >> 2) - 1;  // 0..2
+                for (int tile = part; tile < ntile; tile += 3) {
+                    const int c0 = (lo_pair ? 0 : 48) + 16 * tile;
+                    float x[16];
+                    tmem_ld16(ta + c0, x);
+                    tmem_ld_wait();
+                    const int j0 = c0 - pair_col0(br);
+                    if (j0 < 0 || j0 >= 16 * (br + 1)) continue;
+#pragma unroll
+                    for (int h8 = 0; h8 < 2; ++h8) {
+                        float y[8];
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) y[t] = (j0 + 8 * h8 + t <= r) ? x[8 * h8 + t] : 0.0f;
+                        *reinterpret_cast<uint4 *>(rec + TcRec::A + sw128_off(r, j0 + 8 * h8, 64)) = pack8(y);
+                    }
+                }
+                // A entries right of a row's block diagonal are zero
+                for (int i = 64 * part + 32 * (quarter & 1) + lane; i < C * 8; i += 192) {
+                    const int ra = i >> 3, c8 = i & 7;
+                    if (c8 >= 2 * ((ra >> 4) + 1))
+                        *reinterpret_cast<uint4 *>(rec + TcRec::A + sw128_off(ra, 8 * c8, 64)) = make_uint4(0, 0, 0, 0);
+                }
+                tc_fence_before();
             }
         }
-        tc_fence_before();
-        __syncthreads();
         KDA_PHASE(0, 5);
 
-        // 5. X = (I + L)^-1, L strictly lower (beta-scaled rows), in 16x16 blocks:
-        //    diagonal blocks X_bb = (I + L_bb)^-1 by forward substitution, one
-        //    column per lane (warps 0-1, no barriers); then with M = X_D L_off
-        //    (strictly block lower, M^4 = 0): (I + L)^-1 = (I - M + M^2 - M^3) X_D,
-        //    which is blocked forward substitution regrouped by levels.
-        //    T = X diag(beta) -> bf16 operand at sT.
+        // 4. X = (I + L)^-1 with L strictly lower (beta-scaled rows), in 16x16
+        //    blocks, and T = X diag(beta) written straight into the bf16 hi + lo
+        //    operand (K-major [i][j]) at sT.  Blocked forward substitution:
+        //      A: per diagonal block a, forward substitution with (I + L_aa),
+        //         one right-hand side per lane: the unit vectors give
+        //         X_aa = (I + L_aa)^-1, the columns of L_ab (b < a) give
+        //         M_ab = X_aa L_ab (160 lanes, no barriers);
+        //      B: X_10 = -M_10 X_00, X_21 = -M_21 X_11, X_32 = -M_32 X_22,
+        //         C30 = M_32 M_20 - M_30, C31 = M_32 M_21 - M_31; the
+        //         diagonal blocks of T;
+        //      C: X_20 = -(M_20 X_00 + M_21 X_10), X_31 = -(M_31 X_11 + M_32 X_21),
+        //         X_30 = C30 X_00 + C31 X_10 (= -(M_30 X_00 + M_31 X_10 + M_32 X_20));
+        //         zeros above the block diagonal.
+        //    Stages B and C give each thread one (row, 4 columns) slot.
         {
             const float *sL = reinterpret_cast<const float *>(sXL);
-            float *T1 = reinterpret_cast<float *>(sBS);  // 4 blocks each
-            float *T2 = T1 + 4 * MBLK;
-            float *T3 = T2 + 4 * MBLK;
-            float *T4 = reinterpret_cast<float *>(sXL) + C * LSTRIDE;  // after L
-            float *Mb = T4 + 4 * MBLK;                                  // 6 blocks
-            if (warp < 2) {
-                const int blk = tid >> 4, c = tid & 15, o = 16 * blk;
+            float *XD = reinterpret_cast<float *>(sBS);    // X_aa, a = 0..3
+            float *Mb = XD + 4 * MBLK;                     // M_ab, pairs p = 0..5
+            float *Cb = Mb + 6 * MBLK;                     // C30, C31
+            float *Xo = reinterpret_cast<float *>(sXL) + C * LSTRIDE;  // X_10, X_21
+            // Block pairs (a, b), a > b, index p: (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+            auto pair_a = [](int p_) { return p_ < 1 ? 1 : (p_ < 3 ? 2 : 3); };
+            // T block (a, b), rows i, columns 4c4..4c4+3 from X values x
+            auto put_t = [&](int a, int b, int i, int c4, float4 x) {
+                const int row = 16 * a + i, col = 16 * b + 4 * c4;
+                const float4 bt = *reinterpret_cast<const float4 *>(sB + col);
+                const float y0 = x.x * bt.x, y1 = x.y * bt.y, y2 = x.z * bt.z, y3 = x.w * bt.w;
+                const uint32_t h01 = pack2(y0, y1), h23 = pack2(y2, y3);
+                const float2 f01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&h01));
+                const float2 f23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&h23));
+                const uint32_t off = sw128_off(row, col, 64);
+                *reinterpret_cast<uint2 *>(sT + off) = make_uint2(h01, h23);
+                *reinterpret_cast<uint2 *>(sT + 8192 + off) =
+                    make_uint2(pack2(y0 - f01.x, y1 - f01.y), pack2(y2 - f23.x, y3 - f23.y));
+            };
+            const int sidx = warp < 4 ? warp : (warp == 6 ? 4 : 5);  // stage A: warps 0, 1, 2, 3, 6
+            if (sidx < 5) {
+                const int sl = 32 * sidx + lane;
+                const bool unit = sl < 64;
+                const int p_ = unit ? 0 : (sl - 64) >> 4;
+                const int a = unit ? sl >> 4 : pair_a(p_);
+                const int b = unit ? a : p_ - a * (a - 1) / 2;
+                const int c = sl & 15, o = 16 * a;
                 float x[16];
 #pragma unroll
                 for (int r = 0; r < 16; ++r) {
                     float lr[16];
                     row16(sL + o, LSTRIDE, o + r, lr);
+                    const float rhs = unit ? (r == c ? 1.0f : 0.0f) : sL[(o + r) * LSTRIDE + 16 * b + c];
                     // two partial sums shorten the dependent chain
                     float a0 = 0.0f, a1 = 0.0f;
 #pragma unroll
@@ -567,88 +632,78 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                         if (m2 & 1) a1 = fmaf(lr[m2], x[m2], a1);
                         else a0 = fmaf(lr[m2], x[m2], a0);
                     }
-                    x[r] = (r == c) ? 1.0f : (r < c ? 0.0f : -(a0 + a1));
+                    x[r] = rhs - (a0 + a1);
                 }
+                float *dst = unit ? XD + a * MBLK : Mb + p_ * MBLK;
 #pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    sX[(o + r) * C + o + c] = x[r];
-                    T2[blk * MBLK + r * MS + c] = x[r];
-                }
+                for (int r = 0; r < 16; ++r) dst[r * MS + c] = x[r];
             }
             __syncthreads();
             KDA_PHASE(0, 6);
-            // Off-diagonal part.  Block pairs (a, b), a > b, indexed p = 0..5:
-            // (1,0) (2,0) (2,1) (3,0) (3,1) (3,2).  X_D blocks are in T2.  Each
-            // level gives a thread at most one (row, 4 columns) slot.
-            const float *XD = T2;
-            float *M2 = T1;  // M21 M10, M32 M21, M31 M10, M32 M20
-            float *M3 = T3;  // (M^3)_30 = M32 (M21 M10)
-            auto pair_a = [](int p_) { return p_ < 1 ? 1 : (p_ < 3 ? 2 : 3); };
-            auto put4 = [](float *M_, int i_, int c_, float4 x) {
-                *reinterpret_cast<float4 *>(M_ + i_ * MS + 4 * c_) = x;
-            };
-            if (tid < 6 * 64) {  // M_ab = X_aa L_ab
-                const int p_ = tid >> 6, ii = (tid >> 2) & 15, c4 = tid & 3;
-                const int a = pair_a(p_), b = p_ - a * (a - 1) / 2;
-                put4(Mb + p_ * MBLK, ii, c4, mm16_row4(XD + a * MBLK, MS, sL + (16 * a) * LSTRIDE + 16 * b, LSTRIDE, ii, c4));
-            }
-            __syncthreads();
-            if (tid < 4 * 64) {
+            {
                 const int q_ = tid >> 6, ii = (tid >> 2) & 15, c4 = tid & 3;
-                const int pa_ = q_ == 0 ? 2 : (q_ == 2 ? 4 : 5);  // M21 M10, M32 M21, M31 M10, M32 M20
-                const int pb_ = q_ == 1 ? 2 : (q_ == 3 ? 1 : 0);
-                put4(M2 + q_ * MBLK, ii, c4, mm16_row4(Mb + pa_ * MBLK, MS, Mb + pb_ * MBLK, MS, ii, c4));
-            }
-            __syncthreads();
-            if (tid < 64) {
-                const int ii = (tid >> 2) & 15, c4 = tid & 3;
-                put4(M3, ii, c4, mm16_row4(Mb + 5 * MBLK, MS, M2 + 0 * MBLK, MS, ii, c4));
-            }
-            __syncthreads();
-            if (tid < 6 * 64) {  // X_ab = (-M + M^2 - M^3)_ab X_bb
-                const int p_ = tid >> 6, ii = (tid >> 2) & 15, c4 = tid & 3;
-                const int a = pair_a(p_), b = p_ - a * (a - 1) / 2;
-                float z[16], w[16];
-                row16(Mb + p_ * MBLK, MS, ii, z);
-#pragma unroll
-                for (int kk = 0; kk < 16; ++kk) z[kk] = -z[kk];
-                if (p_ == 1 || p_ == 4) {  // (2,0): M21 M10 ; (3,1): M32 M21
-                    row16(M2 + (p_ == 1 ? 0 : 1) * MBLK, MS, ii, w);
-#pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) z[kk] += w[kk];
+                if (q_ < 3) {  // X_{q+1,q} = -M_{q+1,q} X_qq
+                    const int pm = q_ == 0 ? 0 : (q_ == 1 ? 2 : 5);
+                    float4 x = mm16_row4(Mb + pm * MBLK, MS, XD + q_ * MBLK, MS, ii, c4);
+                    x = make_float4(-x.x, -x.y, -x.z, -x.w);
+                    if (q_ < 2) *reinterpret_cast<float4 *>(Xo + q_ * MBLK + ii * MS + 4 * c4) = x;
+                    put_t(q_ + 1, q_, ii, c4, x);
+                } else if (q_ < 5) {  // C30 = M_32 M_20 - M_30, C31 = M_32 M_21 - M_31
+                    const int k_ = q_ - 3;
+                    float4 x = mm16_row4(Mb + 5 * MBLK, MS, Mb + (k_ == 0 ? 1 : 2) * MBLK, MS, ii, c4);
+                    const float4 m = *reinterpret_cast<const float4 *>(Mb + (3 + k_) * MBLK + ii * MS + 4 * c4);
+                    *reinterpret_cast<float4 *>(Cb + k_ * MBLK + ii * MS + 4 * c4) =
+                        make_float4(x.x - m.x, x.y - m.y, x.z - m.z, x.w - m.w);
+                } else {  // diagonal blocks of T: 256 slots over the last 192 threads
+                    for (int sl = tid - 320; sl < 256; sl += 192) {
+                        const int a = sl >> 6, i = (sl >> 2) & 15, cc = sl & 3;
+                        put_t(a, a, i, cc, *reinterpret_cast<const float4 *>(XD + a * MBLK + i * MS + 4 * cc));
+                    }
                 }
-                if (p_ == 3) {  // (3,0): M31 M10 + M32 M20 - M32 M21 M10
-                    row16(M2 + 2 * MBLK, MS, ii, w);
-#pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) z[kk] += w[kk];
-                    row16(M2 + 3 * MBLK, MS, ii, w);
-#pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) z[kk] += w[kk];
-                    row16(M3, MS, ii, w);
-#pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) z[kk] -= w[kk];
-                }
-                *reinterpret_cast<float4 *>(sX + (16 * a + ii) * C + 16 * b + 4 * c4) =
-                    row4_times(z, XD + b * MBLK, c4);
             }
             __syncthreads();
-            {  // T = X diag(beta), lower triangle, as K-major [i][j] bf16 hi + lo operands
-                const int ri = tid >> 3, j0 = (tid & 7) * 8;
-                float y[8], lo[8];
-#pragma unroll
-                for (int t = 0; t < 8; ++t) y[t] = (j0 + t <= ri) ? sX[ri * C + j0 + t] * sB[j0 + t] : 0.0f;
-                const uint4 hi = pack8(y);
-                unpack8(hi, lo);
-#pragma unroll
-                for (int t = 0; t < 8; ++t) lo[t] = y[t] - lo[t];
-                *reinterpret_cast<uint4 *>(sT + sw128_off(ri, j0, 64)) = hi;
-                *reinterpret_cast<uint4 *>(sT + 8192 + sw128_off(ri, j0, 64)) = pack8(lo);
+            KDA_PHASE(0, 12);
+            {
+                const int q_ = tid >> 6, ii = (tid >> 2) & 15, c4 = tid & 3;
+                if (q_ < 3) {
+                    float a16[16];
+                    float4 x, y;
+                    if (q_ == 0) {         // X_20 = -(M_20 X_00 + M_21 X_10)
+                        row16(Mb + 1 * MBLK, MS, ii, a16);
+                        x = row4_times(a16, XD, c4);
+                        row16(Mb + 2 * MBLK, MS, ii, a16);
+                        y = row4_times(a16, Xo, c4);
+                        x = make_float4(-(x.x + y.x), -(x.y + y.y), -(x.z + y.z), -(x.w + y.w));
+                        put_t(2, 0, ii, c4, x);
+                    } else if (q_ == 1) {  // X_31 = -(M_31 X_11 + M_32 X_21)
+                        row16(Mb + 4 * MBLK, MS, ii, a16);
+                        x = row4_times(a16, XD + MBLK, c4);
+                        row16(Mb + 5 * MBLK, MS, ii, a16);
+                        y = row4_times(a16, Xo + MBLK, c4);
+                        x = make_float4(-(x.x + y.x), -(x.y + y.y), -(x.z + y.z), -(x.w + y.w));
+                        put_t(3, 1, ii, c4, x);
+                    } else {               // X_30 = C30 X_00 + C31 X_10
+                        row16(Cb, MS, ii, a16);
+                        x = row4_times(a16, XD, c4);
+                        row16(Cb + MBLK, MS, ii, a16);
+                        y = row4_times(a16, Xo, c4);
+                        put_t(3, 0, ii, c4, make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w));
+                    }
+                } else {  // zeros above the block diagonal: 6 blocks x 16 rows x 2 chunks x hi, lo
+                    for (int sl = tid - 192; sl < 384; sl += 320) {
+                        const int pz = sl >> 6, i = (sl >> 2) & 15, h = (sl >> 1) & 1, hl = sl & 1;
+                        const int a = pz < 3 ? 0 : (pz < 5 ? 1 : 2);
+                        const int b = pz < 3 ? pz + 1 : (pz < 5 ? pz - 1 : 3);
+                        *reinterpret_cast<uint4 *>(sT + hl * 8192 + sw128_off(16 * a + i, 16 * b + 8 * h, 64)) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                }
             }
         }
         __syncthreads();
         KDA_PHASE(0, 7);
 
-        // 6. W = T E, U = T V (B operands MN-major: E from the row pass, V as
+        // 5. W = T E, U = T V (B operands MN-major: E from the row pass, V as
         //    loaded); hi + lo parts of T.  The v tile was requested at the end
         //    of the previous item; rows past the sequence end are zeroed.
         if (mbar_wait(vfull, vphase)) {
@@ -686,7 +741,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         if (tid == kLoader && has_next) load_v(sm, maps, nxt.h, nxt.tok0, vfull);
         vpend = has_next;
 
-        // 7. W rows (WQ rows 0..63) and U: TMEM lanes 0..63 -> shared memory
+        // 6. W rows (WQ rows 0..63) and U: TMEM lanes 0..63 -> shared memory
         //    (sXL, free since the T conversion) in the record's own layout ->
         //    three bulk copies to the record.  U rows are stored with their
         //    16-byte chunks rotated (chunk c of row i at c ^ ((i / 2) % 4)),
