@@ -39,7 +39,7 @@
 // scan, one CTA per (sequence, head, 32 value columns), 4 warps, records in a
 // 3-stage cp.async.bulk ring:
 //     D1  = WQ * S            (M=128, N=32, K=128)  rows 0..63: W S
-//     Vn  = U - D1[0:64]      (fp32, written as a bf16 K-major operand)
+//     Vn  = U - D1[0:64]      (fp32, written as a bf16 MN-major operand)
 //     D1 += [* ; A] * Vn      (rows 64..127 become o = QG S + A Vn)
 //     D3  = KD^T * Vn         (M=128, N=32, K=64; KD as an MN-major operand)
 //     S   = diag(gC) S + D3   (fp32, one key row per thread, in registers)
@@ -809,36 +809,28 @@ constexpr int kScanThreads = 128;
 constexpr int BV = 32;
 constexpr uint32_t kScanTmemCols = 128;  // D1 double-buffered (2 x 32 columns), D3 (32)
 constexpr int kStages = 3;
+static_assert(BV == 32, "S and Vn are N = 32 operands");
 constexpr uint32_t kImageBytes = TcRec::U;                   // WQ | KD | A | gC
 constexpr uint32_t kStageBytes = kImageBytes + TcRec::UBLK;  // + this CTA's U block
 constexpr int S_STAGE = 62464;                               // kStageBytes rounded up to 1024
-constexpr int S_SOP = kStages * S_STAGE;                     // S^T operand [32][128] bf16, 8 KB
-constexpr int S_VOP = S_SOP + 8192;                          // Vn^T operand [32][64] bf16, 4 KB
+constexpr int S_SOP = kStages * S_STAGE;                     // S operand [128 keys][32] bf16, 8 KB
+constexpr int S_VOP = S_SOP + 8192;                          // Vn operand [64 rows][32] bf16, 4 KB
 constexpr int S_BAR = S_VOP + 4096;                          // full[kStages], mma
 constexpr int S_BYTES = S_BAR + 64;
 constexpr int S_SMEM = S_BYTES + 1024;
 static_assert(kStageBytes <= (uint32_t)S_STAGE, "stage too small");
 static_assert(kImageBytes % 16 == 0 && TcRec::UBLK % 16 == 0, "bulk copy size");
 
-// Write this thread's 32 values x[v] as column `col` of a K-major SW128 bf16
-// operand with 32 rows: neighbouring lanes (col even / odd) swap one value so
-// that each 32-bit store holds two adjacent columns of one row.  Whole warps.
-__device__ __forceinline__ void store_col_pairs(unsigned char *op, int col, const float (&x)[32]) {
-    const int odd = col & 1;
-    const int ce = col & ~1;
-    const int kk = ce & 63;
-    // element (row, ce) of the 32-row tile sits at
-    //   (ce / 64) * 4096 + row * 128 + (((kk / 8) ^ (row % 8)) * 16) + (kk % 8) * 2;
-    // for row = 2m + odd, (row % 8) = ((2m) % 8) | odd, hence the hoisted terms
-    unsigned char *base = op + (ce >> 6) * 4096 + odd * 128 + ((kk & 7) << 1);
-    const int cx = (kk >> 3) ^ odd;
+// This thread's 32 values x[v] as row k of an N = 32 operand (MN-major,
+// 64-byte swizzle, see sw64_off): four 16-byte stores, conflict-free across
+// a warp of consecutive rows.
+__device__ __forceinline__ void store_row_n32(unsigned char *op, int k, const float (&x)[32]) {
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-        const float send = odd ? x[2 * m] : x[2 * m + 1];
-        const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-        const float lo = odd ? recv : x[2 * m];
-        const float hi = odd ? x[2 * m + 1] : recv;
-        *reinterpret_cast<uint32_t *>(base + 256 * m + ((cx ^ ((2 * m) & 7)) << 4)) = pack2(lo, hi);
+    for (int c = 0; c < 4; ++c) {
+        float y[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) y[t] = x[8 * c + t];
+        *reinterpret_cast<uint4 *>(op + sw64_off(k, 8 * c)) = pack8(y);
     }
 }
 
@@ -885,7 +877,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 #pragma unroll
     for (int x = 0; x < BV; ++x)
         S[x] = initial_state ? initial_state[st_off + (int64_t)(v0 + x) * D + tid] : 0.0f;
-    store_col_pairs(sS, tid, S);
+    store_row_n32(sS, tid, S);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -932,7 +924,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         if (tid == 0) {
             ok = mbar_wait(&full[stage], fpar) && ok;
             tc_fence_after();
-            mma_tile<128, BV, 128, 128, BV>(tD1, smem_u32(st + TcRec::WQ), smem_u32(sS), false);
+            mma_tile_n32<128, 128, 128>(tD1, smem_u32(st + TcRec::WQ), smem_u32(sS), false);
             mma_commit(mbar);
         }
         KDA_PHASE(1, 1);
@@ -957,7 +949,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             tmem_ld_wait();
 #pragma unroll
             for (int vv = 0; vv < BV; ++vv) x[vv] = u[vv] - x[vv];
-            store_col_pairs(sVn, tid, x);
+            store_row_n32(sVn, tid, x);
         }
         KDA_PHASE(1, 4);
         fence_async_smem();
@@ -968,8 +960,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         // D1 += [* ; A] * Vn ;  D3 = KD^T * Vn
         if (tid == 0) {
             tc_fence_after();
-            mma_tile<128, BV, 64, 128, BV>(tD1, smem_u32(st + TcRec::A) - 8192, smem_u32(sVn), true);
-            mma_tile<128, BV, 64, 64, BV, true, false>(tD3, smem_u32(st + TcRec::KD), smem_u32(sVn), false);
+            mma_tile_n32<128, 64, 128>(tD1, smem_u32(st + TcRec::A) - 8192, smem_u32(sVn), true);
+            mma_tile_n32<128, 64, 64, true>(tD3, smem_u32(st + TcRec::KD), smem_u32(sVn), false);
             mma_commit(mbar);
         }
         KDA_PHASE(1, 6);
@@ -984,7 +976,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             tmem_ld_wait();
 #pragma unroll
             for (int vv = 0; vv < BV; ++vv) S[vv] = fmaf(gc, S[vv], x[vv]);
-            store_col_pairs(sS, tid, S);
+            store_row_n32(sS, tid, S);
         }
         KDA_PHASE(1, 8);
         fence_async_smem();

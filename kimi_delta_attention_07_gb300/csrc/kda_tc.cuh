@@ -267,6 +267,29 @@ __device__ __forceinline__ void mma_tile(uint32_t d_tmem, uint32_t a_saddr, uint
     }
 }
 
+// B operand with N = 32, MN-major, 64-byte swizzle: one 64-byte row per K
+// index, element (n, k) at sw64_off(k, n); 8-row groups 512 bytes apart, a K=16
+// step moves the start address by 1024 bytes.  Tiles start on a 1024-byte
+// boundary.
+__host__ __device__ __forceinline__ uint32_t sw64_off(int k, int n) {
+    return (uint32_t)(k * 64 + ((((n >> 3) ^ ((k >> 1) & 3))) << 4) + ((n & 7) << 1));
+}
+constexpr uint32_t kDescHiSw64 = (uint32_t)(512 >> 4) | (1u << 14) | (4u << 29);
+
+// D[M x 32] (+)= A[M x K] * B[32 x K]^T, A as in mma_tile, B as above.
+template <int M, int K, int AROWS, bool A_MN = false>
+__device__ __forceinline__ void mma_tile_n32(uint32_t d_tmem, uint32_t a_saddr, uint32_t b_saddr,
+                                             bool accumulate) {
+    constexpr uint32_t idesc = idesc_bf16(M, 32) | (A_MN ? (1u << 15) : 0u) | (1u << 16);
+    const uint32_t b_lo = (b_saddr & 0x3FFFFu) >> 4;
+#pragma unroll
+    for (int s = 0; s < K / 16; ++s) {
+        const uint64_t ad = ((uint64_t)kDescHi << 32) | (uint64_t)operand_lo<A_MN, AROWS>(a_saddr, s);
+        const uint64_t bd = ((uint64_t)kDescHiSw64 << 32) | (uint64_t)(b_lo + (uint32_t)(s * 64));
+        mma_bf16(d_tmem, ad, bd, idesc, (accumulate || s > 0) ? 1u : 0u);
+    }
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
