@@ -316,7 +316,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             *reinterpret_cast<uint4 *>(sm + R_G + r * 512 + c16 * 32) = z;
             *reinterpret_cast<uint4 *>(sm + R_G + r * 512 + c16 * 32 + 16) = z;
         }
-        if (!__syncthreads_and(ok)) break;
+        if (!__syncthreads_and(ok)) {
+            ok = false;  // uniform from here on: every thread takes the exit path
+            break;
+        }
         KDA_PHASE(0, 0);
 
         // 1. cumulative log-decay, one key channel and one 16-row block per
@@ -505,7 +508,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             ok = false;
         }
         tc_fence_after();
-        if (!__syncthreads_and(ok)) break;
+        if (!__syncthreads_and(ok)) {
+            ok = false;  // uniform from here on: every thread takes the exit path
+            break;
+        }
         // the q, k and g tiles are consumed: the next item's loads go out now
         if (tid == kLoader && has_next) load_qkg(sm, maps, nxt.h, nxt.tok0, full);
         fpend = has_next;
@@ -719,7 +725,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
         fence_async_smem();
         tc_fence_before();
-        if (!__syncthreads_and(ok)) break;
+        if (!__syncthreads_and(ok)) {
+            ok = false;  // uniform from here on: every thread takes the exit path
+            break;
+        }
         if (tid == 0) {
             tc_fence_after();
             mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 0, smem_u32(sT), smem_u32(sE), false);
@@ -774,7 +783,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
         fence_async_smem();
         tc_fence_before();
-        if (!__syncthreads_and(ok)) break;
+        if (!__syncthreads_and(ok)) {
+            ok = false;  // uniform from here on: every thread takes the exit path
+            break;
+        }
         if (tid == kLoader) {
             bulk_s2g(rec + TcRec::WQ, sXL, 8192);                  // W, key columns 0..63
             bulk_s2g(rec + TcRec::WQ + 16384, sXL + 8192, 8192);   // W, key columns 64..127
@@ -805,7 +817,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
 // ---------------------------------------------------------------------------
 // scan
 // ---------------------------------------------------------------------------
-constexpr int kScanThreads = 128;
+constexpr int kScanThreads = 160;  // warps 0-3: state rows, Vn, output rows; warp 4: MMAs and loads
+constexpr int kIssuer = 128;       // lane 0 of warp 4
 constexpr int BV = 32;
 constexpr uint32_t kScanTmemCols = 128;  // D1 double-buffered (2 x 32 columns), D3 (32)
 constexpr int kStages = 3;
@@ -815,11 +828,13 @@ constexpr uint32_t kStageBytes = kImageBytes + TcRec::UBLK;  // + this CTA's U b
 constexpr int S_STAGE = 62464;                               // kStageBytes rounded up to 1024
 constexpr int S_SOP = kStages * S_STAGE;                     // S operand [128 keys][32] bf16, 8 KB
 constexpr int S_VOP = S_SOP + 8192;                          // Vn operand [64 rows][32] bf16, 4 KB
-constexpr int S_BAR = S_VOP + 4096;                          // full[kStages], mma
+constexpr int S_BAR = S_VOP + 4096;                          // full[kStages], ws, d3, out, drain, tmem slot
 constexpr int S_BYTES = S_BAR + 64;
 constexpr int S_SMEM = S_BYTES + 1024;
 static_assert(kStageBytes <= (uint32_t)S_STAGE, "stage too small");
 static_assert(kImageBytes % 16 == 0 && TcRec::UBLK % 16 == 0, "bulk copy size");
+static_assert(8 * (kStages + 4) + 4 <= 64, "scan barrier block");
+constexpr uint32_t kBarS = 1, kBarV = 2;  // named barriers (160 threads): S operand ready, Vn ready
 
 // This thread's 32 values x[v] as row k of an N = 32 operand (MN-major,
 // 64-byte swizzle, see sw64_off): four 16-byte stores, conflict-free across
@@ -834,6 +849,14 @@ __device__ __forceinline__ void store_row_n32(unsigned char *op, int k, const fl
     }
 }
 
+// Per chunk ck (records staged by bulk copies, kStages deep), D1 = D1[ck & 1]:
+//   issuer:     D1 = [W ; QG] S                         after "S ready"
+//   warps 0-1:  Vn = U - D1[0:64] -> Vn operand          -> "Vn ready"
+//   warps 2-3:  output rows of chunk ck-1 from D1[(ck-1) & 1]
+//   issuer:     D3 = KD^T Vn, then D1[64:128] += A Vn    after "Vn ready"
+//   warps 0-3:  S = diag(gC) S + D3 -> S operand         -> "S ready"
+// A dedicated issuing warp keeps the (slow to issue) MMAs off the threads that
+// own state rows; the output MMA runs while the state is updated.
 __global__ void __launch_bounds__(kScanThreads, 1)
     chunk_scan_tc_kernel(const float *__restrict__ initial_state, float *__restrict__ final_state,
                          const int32_t *__restrict__ state_indices, __nv_bfloat16 *__restrict__ o,
@@ -843,11 +866,14 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     unsigned char *sS = sm + S_SOP;
     unsigned char *sVn = sm + S_VOP;
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + S_BAR);
-    uint64_t *mbar = full + kStages;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 1);
+    uint64_t *bar_ws = full + kStages;  // D1 = WQ S done
+    uint64_t *bar_d3 = bar_ws + 1;      // D3 = KD^T Vn done
+    uint64_t *bar_out = bar_d3 + 1;     // D1 += A Vn done: the chunk's output rows
+    uint64_t *bar_drain = bar_out + 1;  // exit path: every MMA issued so far is done
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_drain + 1);
 
     const int n = blockIdx.x, h = blockIdx.y, vb = blockIdx.z, v0 = vb * BV;
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t start = ws_at<const int32_t>(workspace, L.seq_start_off)[n];
     if (start < 0) return;  // sequence skipped (bad cu_seqlens or slot)
     const int len = ws_at<const int32_t>(workspace, L.seq_len_off)[n];
@@ -858,36 +884,41 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     int32_t *status = ws_at<int32_t>(workspace, L.status_off);
     const unsigned char *recs = ws_at<const unsigned char>(workspace, L.records_off);
     auto rec_of = [&](int ck) { return recs + ((size_t)(c0 + ck) * H + h) * TcRec::bytes; };
-    auto issue = [&](int ck) {  // thread 32 (not the MMA-issuing thread)
-        const int s = ck % kStages;
-        unsigned char *dst = sm + s * S_STAGE;
-        mbar_arrive_expect_tx(&full[s], kStageBytes);
-        bulk_g2s(dst, rec_of(ck), kImageBytes, &full[s]);
-        bulk_g2s(dst + kImageBytes, rec_of(ck) + TcRec::U + vb * TcRec::UBLK, TcRec::UBLK, &full[s]);
+    auto stage_of = [&](int ck) { return sm + (ck % kStages) * S_STAGE; };
+    auto issue = [&](int ck) {  // the issuing thread
+        unsigned char *dst = stage_of(ck);
+        uint64_t *b = &full[ck % kStages];
+        mbar_arrive_expect_tx(b, kStageBytes);
+        bulk_g2s(dst, rec_of(ck), kImageBytes, b);
+        bulk_g2s(dst + kImageBytes, rec_of(ck) + TcRec::U + vb * TcRec::UBLK, TcRec::UBLK, b);
     };
 
     if (warp == 0) tmem_alloc(tmem_slot, kScanTmemCols);
-    if (tid == 0) {
+    if (tid == kIssuer) {
         for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
-        mbar_init(mbar, 1);
+        mbar_init(bar_ws, 1);
+        mbar_init(bar_d3, 1);
+        mbar_init(bar_out, 1);
+        mbar_init(bar_drain, 1);
         fence_mbar_init();
     }
-    // state row d = tid, columns v0 .. v0+31, fp32 in registers
+    // state row d = tid (warps 0-3), columns v0 .. v0+31, fp32 in registers
     float S[BV];
+    if (tid < D) {
 #pragma unroll
-    for (int x = 0; x < BV; ++x)
-        S[x] = initial_state ? initial_state[st_off + (int64_t)(v0 + x) * D + tid] : 0.0f;
-    store_row_n32(sS, tid, S);
+        for (int x = 0; x < BV; ++x)
+            S[x] = initial_state ? initial_state[st_off + (int64_t)(v0 + x) * D + tid] : 0.0f;
+        store_row_n32(sS, tid, S);
+    }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tD3 = tmem + 64;
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
 
-    // Output rows of chunk ck (TMEM D1 buffer ck & 1, lanes 64..127) -> o.
-    // Runs in warps 2-3 while the next chunk's first MMA executes.
+    // Output rows of chunk ck (TMEM D1 buffer ck & 1, lanes 64..127) -> o (warps 2-3).
     auto store_output = [&](int ck) {
         float x[32];
         tmem_ld32(tmem + 32 * (ck & 1) + lane_base, x);
@@ -906,37 +937,40 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         }
     };
 
-    if (tid == 32) {
-        for (int ck = 0; ck < kStages - 1 && ck < nck; ++ck) issue(ck);
-    }
-    uint32_t mphase = 0;
+    // stage loads issued / waited for by the issuer, for the exit path
+    int loads_issued = 0, loads_done = 0;
+    if (tid == kIssuer)
+        for (int ck = 0; ck < kStages - 1 && ck < nck; ++ck, ++loads_issued) issue(ck);
     bool ok = true;
     KDA_PHASE_START();
     for (int ck = 0; ck < nck; ++ck) {
-        const int stage = ck % kStages;
-        const uint32_t fpar = (uint32_t)((ck / kStages) & 1);
-        unsigned char *st = sm + stage * S_STAGE;
+        const uint32_t fpar = (uint32_t)((ck / kStages) & 1), cpar = (uint32_t)(ck & 1);
+        unsigned char *st = stage_of(ck);
         const uint32_t tD1 = tmem + 32 * (ck & 1);
-        if (tid == 32 && ck + kStages - 1 < nck) issue(ck + kStages - 1);  // its stage was freed by ck-1
-        KDA_PHASE(1, 0);
-
-        // D1 = WQ * S  (only the issuing thread needs the stage before the MMA)
-        if (tid == 0) {
-            ok = mbar_wait(&full[stage], fpar) && ok;
+        if (tid == kIssuer) {
+            ok = mbar_wait(&full[ck % kStages], fpar) && ok;
+            if (ok) loads_done = ck + 1;
             tc_fence_after();
-            mma_tile_n32<128, 128, 128>(tD1, smem_u32(st + TcRec::WQ), smem_u32(sS), false);
-            mma_commit(mbar);
-        }
-        KDA_PHASE(1, 1);
-        if (ck > 0 && warp >= 2) store_output(ck - 1);
-        KDA_PHASE(1, 2);
-        ok = mbar_wait(mbar, mphase) && ok;
-        mphase ^= 1;
-        tc_fence_after();
-        if (tid != 0) ok = mbar_wait(&full[stage], fpar) && ok;  // U and gC of this stage
-        KDA_PHASE(1, 3);
-        if (warp < 2) {  // rows 0..63: Vn = U - W S
-            float x[32], u[32];
+            if (ok) {
+                mma_tile_n32<128, 128, 128>(tD1, smem_u32(st + TcRec::WQ), smem_u32(sS), false);
+                mma_commit(bar_ws);
+            }
+            // refill the stage of chunk ck-1 once its last MMA (D1 += A Vn) is done
+            const int t = ck + kStages - 1;
+            if (ok && t < nck) {
+                if (ck > 0) ok = mbar_wait(bar_out, cpar ^ 1) && ok;
+                if (ok) {
+                    issue(t);
+                    ++loads_issued;
+                }
+            }
+        } else if (warp < 2) {
+            KDA_PHASE(1, 0);
+            ok = mbar_wait(&full[ck % kStages], fpar) && ok;  // U of this stage
+            ok = mbar_wait(bar_ws, cpar) && ok;
+            tc_fence_after();
+            KDA_PHASE(1, 1);
+            float x[32], u[32];  // Vn = U - W S, row tid
             tmem_ld32(tD1 + lane_base, x);
             const uint4 *up = reinterpret_cast<const uint4 *>(st + kImageBytes + tid * 64);
 #pragma unroll
@@ -950,49 +984,67 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 #pragma unroll
             for (int vv = 0; vv < BV; ++vv) x[vv] = u[vv] - x[vv];
             store_row_n32(sVn, tid, x);
+            fence_async_smem();
+            tc_fence_before();
+            KDA_PHASE(1, 2);
+        } else if (warp < 4) {
+            ok = mbar_wait(&full[ck % kStages], fpar) && ok;  // gC of this stage
+            if (ck > 0) {
+                ok = mbar_wait(bar_out, cpar ^ 1) && ok;
+                tc_fence_after();
+                if (ok) store_output(ck - 1);
+            }
+            tc_fence_before();
         }
-        KDA_PHASE(1, 4);
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        KDA_PHASE(1, 5);
-
-        // D1 += [* ; A] * Vn ;  D3 = KD^T * Vn
-        if (tid == 0) {
+        if (!named_bar_and(kBarV, kScanThreads, ok)) {
+            ok = false;
+            break;
+        }
+        if (tid == kIssuer) {
             tc_fence_after();
-            mma_tile_n32<128, 64, 128>(tD1, smem_u32(st + TcRec::A) - 8192, smem_u32(sVn), true);
             mma_tile_n32<128, 64, 64, true>(tD3, smem_u32(st + TcRec::KD), smem_u32(sVn), false);
-            mma_commit(mbar);
-        }
-        KDA_PHASE(1, 6);
-        ok = mbar_wait(mbar, mphase) && ok;
-        mphase ^= 1;
-        tc_fence_after();
-        KDA_PHASE(1, 7);
-        {  // S = diag(gC) S + KD^T Vn
-            float x[32];
+            mma_commit(bar_d3);
+            mma_tile_n32<128, 64, 128>(tD1, smem_u32(st + TcRec::A) - 8192, smem_u32(sVn), true);
+            mma_commit(bar_out);
+        } else if (warp < 4) {
+            KDA_PHASE(1, 3);
+            ok = mbar_wait(bar_d3, cpar) && ok;
+            tc_fence_after();
+            KDA_PHASE(1, 4);
+            float x[32];  // S = diag(gC) S + KD^T Vn
             tmem_ld32(tD3 + lane_base, x);
             const float gc = reinterpret_cast<const float *>(st + TcRec::GC)[tid];
             tmem_ld_wait();
 #pragma unroll
             for (int vv = 0; vv < BV; ++vv) S[vv] = fmaf(gc, S[vv], x[vv]);
             store_row_n32(sS, tid, S);
+            fence_async_smem();
+            tc_fence_before();
+            KDA_PHASE(1, 5);
         }
-        KDA_PHASE(1, 8);
-        fence_async_smem();
-        tc_fence_before();
-        if (!__syncthreads_and(ok)) break;
-        KDA_PHASE(1, 9);
+        if (!named_bar_and(kBarS, kScanThreads, ok)) {
+            ok = false;
+            break;
+        }
+        KDA_PHASE(1, 6);
     }
-    if (ok && nck > 0 && warp >= 2) store_output(nck - 1);
+    if (ok && nck > 0 && (warp == 2 || warp == 3)) {
+        ok = mbar_wait(bar_out, (uint32_t)((nck - 1) & 1));
+        tc_fence_after();
+        if (ok) store_output(nck - 1);
+    }
+    ok = __syncthreads_and(ok);
     if (!ok) {
-        if (tid == 32) {
+        // let copies and MMAs still in flight land before the shared memory
+        // and the TMEM are released
+        if (tid == kIssuer) {
             atomicOr(status, kStatusTimeout);
-            // let copies still in flight land before the shared memory is released
-            for (int s = 0; s < kStages; ++s)
-                mbar_wait(&full[s], 0, 400000000LL) || mbar_wait(&full[s], 1, 400000000LL);
+            for (int t = loads_done; t < loads_issued; ++t)
+                mbar_wait(&full[t % kStages], (uint32_t)((t / kStages) & 1), 400000000LL);
+            mma_commit(bar_drain);
+            mbar_wait(bar_drain, 0, 400000000LL);
         }
-    } else if (final_state) {
+    } else if (final_state && tid < D) {
 #pragma unroll
         for (int x = 0; x < BV; ++x) final_state[st_off + (int64_t)(v0 + x) * D + tid] = S[x];
     }
