@@ -72,7 +72,9 @@ typedef enum {
 } kda_dtype;
 
 /* kda_chunk_fwd flags */
-#define KDA_CHUNK_PRECISE 1 /* fp32 CUDA-core chunk path also for bf16 inputs */
+#define KDA_CHUNK_PRECISE 1    /* fp32 CUDA-core chunk path also for bf16 inputs */
+#define KDA_CHUNK_SCAN_WIDE 2  /* tensor-core path: one scan CTA per (sequence, head) */
+#define KDA_CHUNK_SCAN_SPLIT 4 /* tensor-core path: four scan CTAs per (sequence, head) */
 
 /* Chunk length of the chunked form (Ascend model file, _KDA_CHUNK_SIZE). */
 #define KDA_CHUNK 64
@@ -114,9 +116,16 @@ size_t kda_chunk_workspace_bytes(int64_t total_tokens, int n_seqs, int H, int K,
  *               initial_state (each slot is read before it is written).
  *   scale       multiplies the normalised query (the model uses 1/sqrt(K)).
  *   dtype       kda_dtype of q, k, v, o.
- *   flags       0 or KDA_CHUNK_PRECISE.  Without the flag, bf16 inputs take
+ *   flags       0 or KDA_CHUNK_PRECISE.  Without it, bf16 inputs take
  *               the tensor-core path (bf16 operands, fp32 accumulation,
- *               fp32 state); fp32 inputs always take the fp32 path.
+ *               fp32 state); fp32 inputs always take the fp32 path.  On the
+ *               tensor-core path the state scan runs either as four CTAs per
+ *               (sequence, head), 32 value columns each, or as one CTA per
+ *               (sequence, head); by default the first when all of them fit
+ *               in one wave on the device, else the second.
+ *               KDA_CHUNK_SCAN_SPLIT / KDA_CHUNK_SCAN_WIDE force one (not
+ *               both; ignored on the fp32 path).  Results agree within
+ *               rounding of the summation order.
  *   workspace   device, 256-byte aligned, kda_chunk_workspace_bytes(...)
  *               bytes; its contents are scratch and may be anything.
  *

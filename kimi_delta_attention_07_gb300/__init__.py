@@ -23,6 +23,9 @@ from . import _build
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA = range(5)
 KDA_F32, KDA_BF16 = 0, 1
 KDA_CHUNK_PRECISE = 1
+KDA_CHUNK_SCAN_WIDE = 2
+KDA_CHUNK_SCAN_SPLIT = 4
+_SCAN_FLAGS = {"auto": 0, "wide": KDA_CHUNK_SCAN_WIDE, "split": KDA_CHUNK_SCAN_SPLIT}
 CHUNK = 64
 
 EXPORTS = ("kda_status_string", "kda_version", "kda_chunk_workspace_bytes", "kda_chunk_fwd",
@@ -120,7 +123,7 @@ def kda_chunk_workspace_bytes(total_tokens: int, n_seqs: int, H: int, K: int = 1
 def kda_chunk_fwd(q, k, v, g, beta, *, cu_seqlens=None, n_seqs=None, initial_state=None,
                   final_state=None, state_indices=None, n_slots=None, scale=None,
                   precise=False, output_final_state=True, o=None, workspace=None, stream=None,
-                  phase="fwd"):
+                  phase="fwd", scan="auto"):
     """Chunked KDA forward.
 
     q, k, g: [T, H, K]; v: [T, H, V]; beta: [T, H] (all CUDA, contiguous).
@@ -128,7 +131,9 @@ def kda_chunk_fwd(q, k, v, g, beta, *, cu_seqlens=None, n_seqs=None, initial_sta
     default 1).  Without state_indices, initial_state / final_state are
     [N, H, V, K]; with state_indices (int32 [N]) they are slot pools
     [slots, H, V, K] and final_state may be the same tensor as
-    initial_state (in-place hand-off).  Returns (o, final_state).
+    initial_state (in-place hand-off).  scan: "auto", "wide" or "split"
+    selects the tensor-core state-scan layout (see KDA_CHUNK_SCAN_*).
+    Returns (o, final_state).
     """
     T, H, K = q.shape
     V = v.shape[-1]
@@ -161,7 +166,7 @@ def kda_chunk_fwd(q, k, v, g, beta, *, cu_seqlens=None, n_seqs=None, initial_sta
     if o is None:
         o = torch.empty((T, H, V), dtype=q.dtype, device=q.device)
     _check(o, "o", q.dtype, (T, H, V))
-    flags = KDA_CHUNK_PRECISE if precise else 0
+    flags = (KDA_CHUNK_PRECISE if precise else 0) | _SCAN_FLAGS[scan]
     need = kda_chunk_workspace_bytes(T, N, H, K, V, dt, flags)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)

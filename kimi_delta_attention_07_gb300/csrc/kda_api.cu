@@ -60,7 +60,9 @@ int chunk_call(int phase, const void *q, const void *k, const void *v, const flo
                int n_seqs, int64_t total_tokens, int H, int K, int V, float scale, int dtype,
                int flags, void *workspace, size_t workspace_bytes, void *stream) {
     if (!valid_dtype(dtype) || n_seqs <= 0 || H <= 0 || K <= 0 || V <= 0 || total_tokens < 0 ||
-        total_tokens > INT32_MAX || (flags & ~KDA_CHUNK_PRECISE))
+        total_tokens > INT32_MAX ||
+        (flags & ~(KDA_CHUNK_PRECISE | KDA_CHUNK_SCAN_WIDE | KDA_CHUNK_SCAN_SPLIT)) ||
+        ((flags & KDA_CHUNK_SCAN_WIDE) && (flags & KDA_CHUNK_SCAN_SPLIT)))
         return KDA_ERR_INVALID_ARG;
     if (K != kHeadDim || V != kHeadDim) return KDA_ERR_UNSUPPORTED;
     if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
@@ -94,7 +96,7 @@ int chunk_call(int phase, const void *q, const void *k, const void *v, const flo
     }
     if (e == cudaSuccess && (phase & kScan))
         e = tc ? launch_chunk_scan_tc(initial_state, final_state, state_indices, o, n_seqs,
-                                      total_tokens, H, workspace, s)
+                                      total_tokens, H, flags, workspace, s)
                : launch_chunk_scan_f32(initial_state, final_state, state_indices, o, dtype,
                                        n_seqs, total_tokens, H, workspace, s);
     if (e != cudaSuccess) {

@@ -1054,6 +1054,233 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     if (warp == 0) tmem_dealloc(tmem, kScanTmemCols);
 }
 
+// ---------------------------------------------------------------------------
+// wide scan: one CTA per (sequence, head) covering all 128 value columns.
+// An MMA instruction costs the same for N = 32 and N = 128, so this does a
+// split scan's per-chunk MMA work for four times the columns; it is the
+// better choice once sequences x heads x 4 exceed the SM count.
+// ---------------------------------------------------------------------------
+constexpr int kWideThreads = 288;  // warps 0-7: (TMEM quarter, column half); warp 8: MMAs and loads
+constexpr int kWideIssuer = 256;
+constexpr int kWideStages = 2;
+constexpr uint32_t kWideTmemCols = 512;  // D1 double-buffered (2 x 128 columns), D3 (128)
+constexpr uint32_t kWideStageBytes = TcRec::U + 4 * TcRec::UBLK;  // the whole record
+constexpr int W_STAGE = 74752;                                    // rounded up to 1024
+constexpr int W_SOP = kWideStages * W_STAGE;  // S operand [128 keys][128] bf16, MN-major SW128, 32 KB
+constexpr int W_VOP = W_SOP + 32768;          // Vn operand [64 rows][128] bf16, MN-major SW128, 16 KB
+constexpr int W_BAR = W_VOP + 16384;          // full[kWideStages], ws, d3, out, drain, tmem slot
+constexpr int W_SMEM = W_BAR + 64 + 1024;
+static_assert(kWideStageBytes <= (uint32_t)W_STAGE && W_STAGE % 1024 == 0, "wide stage");
+static_assert(kWideStageBytes % 16 == 0, "bulk copy size");
+static_assert(W_SMEM <= 232448, "wide scan shared memory");
+
+__global__ void __launch_bounds__(kWideThreads, 1)
+    chunk_scan_wide_kernel(const float *__restrict__ initial_state, float *__restrict__ final_state,
+                           const int32_t *__restrict__ state_indices, __nv_bfloat16 *__restrict__ o,
+                           int n_seqs, int H, void *workspace, WsLayout L) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char *sS = sm + W_SOP;
+    unsigned char *sVn = sm + W_VOP;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + W_BAR);
+    uint64_t *bar_ws = full + kWideStages;  // D1 = WQ S done
+    uint64_t *bar_d3 = bar_ws + 1;          // D3 = KD^T Vn done
+    uint64_t *bar_out = bar_d3 + 1;         // D1 += A Vn done: the chunk's output rows
+    uint64_t *bar_drain = bar_out + 1;      // exit path: every MMA issued so far is done
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_drain + 1);
+
+    const int n = blockIdx.x, h = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q = warp & 3, half = (warp >> 2) & 1;  // TMEM lane quarter, value-column half
+    const int32_t start = ws_at<const int32_t>(workspace, L.seq_start_off)[n];
+    if (start < 0) return;  // sequence skipped (bad cu_seqlens or slot)
+    const int len = ws_at<const int32_t>(workspace, L.seq_len_off)[n];
+    const int c0 = ws_at<const int32_t>(workspace, L.chunk_off_off)[n];
+    const int nck = (len + C - 1) / C;
+    const int64_t slot = state_indices ? (int64_t)state_indices[n] : (int64_t)n;
+    const int64_t st_off = (slot * H + h) * (int64_t)D * D;  // [V][K] block of (slot, h)
+    int32_t *status = ws_at<int32_t>(workspace, L.status_off);
+    const unsigned char *recs = ws_at<const unsigned char>(workspace, L.records_off);
+    auto stage_of = [&](int ck) { return sm + (ck % kWideStages) * W_STAGE; };
+    auto issue = [&](int ck) {  // the issuing thread
+        uint64_t *b = &full[ck % kWideStages];
+        mbar_arrive_expect_tx(b, kWideStageBytes);
+        bulk_g2s(stage_of(ck), recs + ((size_t)(c0 + ck) * H + h) * TcRec::bytes, kWideStageBytes, b);
+    };
+
+    if (warp == 0) tmem_alloc(tmem_slot, kWideTmemCols);
+    if (tid == kWideIssuer) {
+        for (int s = 0; s < kWideStages; ++s) mbar_init(&full[s], 1);
+        mbar_init(bar_ws, 1);
+        mbar_init(bar_d3, 1);
+        mbar_init(bar_out, 1);
+        mbar_init(bar_drain, 1);
+        fence_mbar_init();
+    }
+    // state row d = 32 q + lane, value columns 64 half .. 64 half + 63, fp32
+    const int d = 32 * q + lane, vh = 64 * half;
+    float S[64];
+    auto store_s = [&]() {  // this thread's part of the S operand (MN-major [d][v])
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            float y[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) y[t] = S[8 * c + t];
+            *reinterpret_cast<uint4 *>(sS + sw128_off(d, vh + 8 * c, D)) = pack8(y);
+        }
+    };
+    if (warp < 8) {
+#pragma unroll
+        for (int x = 0; x < 64; ++x)
+            S[x] = initial_state ? initial_state[st_off + (int64_t)(vh + x) * D + d] : 0.0f;
+        store_s();
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tD3 = tmem + 256;
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+
+    // output rows 64 + 32 (q - 2) + lane of chunk ck (TMEM D1 buffer ck & 1), this half
+    auto store_output = [&](int ck) {
+        const int r = 32 * (q - 2) + lane;
+        const bool live = r < min(C, len - ck * C);
+        const int64_t tok = (int64_t)start + (int64_t)ck * C + r;
+        uint4 *op = reinterpret_cast<uint4 *>(o + (tok * H + h) * (int64_t)D + vh);
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            float x[32];
+            tmem_ld32(tmem + 128 * (ck & 1) + vh + 32 * p + lane_base, x);
+            tmem_ld_wait();
+            if (live) {
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    float y[8];
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) y[t] = x[8 * c8 + t];
+                    op[4 * p + c8] = pack8(y);
+                }
+            }
+        }
+    };
+
+    int loads_issued = 0, loads_done = 0;
+    if (tid == kWideIssuer && nck > 0) {
+        issue(0);
+        loads_issued = 1;
+    }
+    bool ok = true;
+    for (int ck = 0; ck < nck; ++ck) {
+        const uint32_t fpar = (uint32_t)((ck / kWideStages) & 1), cpar = (uint32_t)(ck & 1);
+        unsigned char *st = stage_of(ck);
+        const uint32_t tD1 = tmem + 128 * (ck & 1);
+        if (tid == kWideIssuer) {
+            ok = mbar_wait(&full[ck % kWideStages], fpar) && ok;
+            if (ok) loads_done = ck + 1;
+            tc_fence_after();
+            if (ok) {
+                mma_tile<128, 128, 128, 128, 128, false, true>(tD1, smem_u32(st + TcRec::WQ), smem_u32(sS), false);
+                mma_commit(bar_ws);
+            }
+            // next chunk into the other stage once chunk ck-1's last MMA is done
+            if (ok && ck + 1 < nck) {
+                if (ck > 0) ok = mbar_wait(bar_out, cpar ^ 1) && ok;
+                if (ok) {
+                    issue(ck + 1);
+                    ++loads_issued;
+                }
+            }
+        } else if (warp < 8) {
+            ok = mbar_wait(&full[ck % kWideStages], fpar) && ok;  // U and gC of this stage
+            if (q < 2) {  // Vn = U - W S, row j = d, this half of the columns
+                ok = mbar_wait(bar_ws, cpar) && ok;
+                tc_fence_after();
+                const int j = d;
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    float x[32], u[32];
+                    tmem_ld32(tD1 + vh + 32 * p + lane_base, x);
+                    const uint4 *up = reinterpret_cast<const uint4 *>(st + TcRec::U + (2 * half + p) * TcRec::UBLK + j * 64);
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        float y[8];
+                        unpack8(up[c8 ^ ((j >> 1) & 3)], y);
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) u[8 * c8 + t] = y[t];
+                    }
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        float y[8];
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) y[t] = u[8 * c8 + t] - x[8 * c8 + t];
+                        *reinterpret_cast<uint4 *>(sVn + sw128_off(j, vh + 32 * p + 8 * c8, C)) = pack8(y);
+                    }
+                }
+                fence_async_smem();
+            } else if (ck > 0) {  // output rows of the previous chunk
+                ok = mbar_wait(bar_out, cpar ^ 1) && ok;
+                tc_fence_after();
+                if (ok) store_output(ck - 1);
+            }
+            tc_fence_before();
+        }
+        if (!named_bar_and(kBarV, kWideThreads, ok)) {
+            ok = false;
+            break;
+        }
+        if (tid == kWideIssuer) {
+            tc_fence_after();
+            mma_tile<128, 128, 64, 64, 64, true, true>(tD3, smem_u32(st + TcRec::KD), smem_u32(sVn), false);
+            mma_commit(bar_d3);
+            mma_tile<128, 128, 64, 128, 64, false, true>(tD1, smem_u32(st + TcRec::A) - 8192, smem_u32(sVn), true);
+            mma_commit(bar_out);
+        } else if (warp < 8) {
+            ok = mbar_wait(bar_d3, cpar) && ok;
+            tc_fence_after();
+            const float gc = reinterpret_cast<const float *>(st + TcRec::GC)[d];
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {  // S = diag(gC) S + KD^T Vn
+                float x[32];
+                tmem_ld32(tD3 + vh + 32 * p + lane_base, x);
+                tmem_ld_wait();
+#pragma unroll
+                for (int vv = 0; vv < 32; ++vv) S[32 * p + vv] = fmaf(gc, S[32 * p + vv], x[vv]);
+            }
+            store_s();
+            fence_async_smem();
+            tc_fence_before();
+        }
+        if (!named_bar_and(kBarS, kWideThreads, ok)) {
+            ok = false;
+            break;
+        }
+    }
+    if (ok && nck > 0 && warp < 8 && q >= 2) {
+        ok = mbar_wait(bar_out, (uint32_t)((nck - 1) & 1));
+        tc_fence_after();
+        if (ok) store_output(nck - 1);
+    }
+    ok = __syncthreads_and(ok);
+    if (!ok) {
+        if (tid == kWideIssuer) {
+            atomicOr(status, kStatusTimeout);
+            for (int t = loads_done; t < loads_issued; ++t)
+                mbar_wait(&full[t % kWideStages], (uint32_t)((t / kWideStages) & 1), 400000000LL);
+            mma_commit(bar_drain);
+            mbar_wait(bar_drain, 0, 400000000LL);
+        }
+    } else if (final_state && warp < 8) {
+#pragma unroll
+        for (int x = 0; x < 64; ++x) final_state[st_off + (int64_t)(vh + x) * D + d] = S[x];
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kWideTmemCols);
+}
+
 int sm_count() {
     static int count[64] = {0};
     int dev = 0;
@@ -1125,13 +1352,23 @@ cudaError_t launch_chunk_prep_tc(const void *q, const void *k, const void *v, co
 
 cudaError_t launch_chunk_scan_tc(const float *initial_state, float *final_state,
                                  const int32_t *state_indices, void *o, int n_seqs,
-                                 int64_t total_tokens, int H, void *workspace,
+                                 int64_t total_tokens, int H, int flags, void *workspace,
                                  cudaStream_t stream) {
     const WsLayout L = ws_layout(total_tokens, n_seqs, H, TcRec::bytes);
-    const dim3 grid((unsigned)n_seqs, (unsigned)H, D / BV);
-    cudaFuncSetAttribute(chunk_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S_SMEM);
-    chunk_scan_tc_kernel<<<grid, kScanThreads, S_SMEM, stream>>>(
-        initial_state, final_state, state_indices, (__nv_bfloat16 *)o, n_seqs, H, workspace, L);
+    // wide scan once four CTAs per (sequence, head) would not fit in one wave
+    const bool wide = (flags & KDA_CHUNK_SCAN_WIDE) ||
+                      (!(flags & KDA_CHUNK_SCAN_SPLIT) && (int64_t)n_seqs * H * (D / BV) > sm_count());
+    if (wide) {
+        const dim3 grid((unsigned)n_seqs, (unsigned)H, 1);
+        cudaFuncSetAttribute(chunk_scan_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, W_SMEM);
+        chunk_scan_wide_kernel<<<grid, kWideThreads, W_SMEM, stream>>>(
+            initial_state, final_state, state_indices, (__nv_bfloat16 *)o, n_seqs, H, workspace, L);
+    } else {
+        const dim3 grid((unsigned)n_seqs, (unsigned)H, D / BV);
+        cudaFuncSetAttribute(chunk_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S_SMEM);
+        chunk_scan_tc_kernel<<<grid, kScanThreads, S_SMEM, stream>>>(
+            initial_state, final_state, state_indices, (__nv_bfloat16 *)o, n_seqs, H, workspace, L);
+    }
     return cudaGetLastError();
 }
 

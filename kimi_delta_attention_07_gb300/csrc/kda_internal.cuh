@@ -144,7 +144,7 @@ cudaError_t launch_chunk_prep_tc(const void *q, const void *k, const void *v, co
 
 cudaError_t launch_chunk_scan_tc(const float *initial_state, float *final_state,
                                  const int32_t *state_indices, void *o, int n_seqs,
-                                 int64_t total_tokens, int H, void *workspace,
+                                 int64_t total_tokens, int H, int flags, void *workspace,
                                  cudaStream_t stream);
 
 // Block-wide helper used by the chunk kernels: find the sequence that owns

@@ -85,6 +85,7 @@ def test_chunk_fwd_rejects_bad_arguments_without_launching(lib):
     assert _chunk(lib, **{**ok, "T": -1}) == kda.KDA_ERR_INVALID_ARG
     assert _chunk(lib, **{**ok, "N": 3, "T": 64}) == kda.KDA_ERR_INVALID_ARG  # 3 does not divide 64
     assert _chunk(lib, **{**ok, "flags": 8}) == kda.KDA_ERR_INVALID_ARG
+    assert _chunk(lib, **{**ok, "flags": kda.KDA_CHUNK_SCAN_WIDE | kda.KDA_CHUNK_SCAN_SPLIT}) == kda.KDA_ERR_INVALID_ARG
     assert _chunk(lib, **{**ok, "q": base + 2}) == kda.KDA_ERR_INVALID_ARG   # misaligned row
     assert _chunk(lib, **{**ok, "ws": None}) == kda.KDA_ERR_WORKSPACE
     assert _chunk(lib, **{**ok, "ws": base + 16}) == kda.KDA_ERR_WORKSPACE   # not 256-aligned

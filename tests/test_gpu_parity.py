@@ -166,10 +166,13 @@ def test_chunk_ragged_and_edge_lengths_fp32(kda, lengths):
     assert rel_l2(vk_to_kv(sf), s_ref) < TOL_F32
 
 
-@pytest.mark.parametrize("precise", [False, True])
-def test_chunk_varlen_bf16(kda, precise):
+SCANS = ["split", "wide"]  # the two tensor-core state-scan layouts
+
+
+@pytest.mark.parametrize("precise,scan", [(False, "split"), (False, "wide"), (True, "auto")])
+def test_chunk_varlen_bf16(kda, precise, scan):
     x = kda_inputs.prefill([300, 64, 129, 5], H=3, dtype=torch.bfloat16, seed=32, init_std=0.02)
-    o, sf = run_chunk(kda, x, precise=precise)
+    o, sf = run_chunk(kda, x, precise=precise, scan=scan)
     o_ref, s_ref = oracle_prefill(x)
     assert rel_l2(to_np(o), o_ref) < TOL_BF16
     assert rel_l2(vk_to_kv(sf), s_ref) < (TOL_F32 if precise else TOL_BF16)
@@ -184,20 +187,22 @@ def test_chunk_strong_decay_fp32(kda):
     assert rel_l2(vk_to_kv(sf), s_ref) < TOL_F32
 
 
+@pytest.mark.parametrize("scan", SCANS)
 @pytest.mark.parametrize("g_lo,g_hi", [(-3.0, -1.0), (-5.0, -3.0)])
-def test_chunk_strong_decay_bf16_tensor_cores(kda, g_lo, g_hi):
+def test_chunk_strong_decay_bf16_tensor_cores(kda, g_lo, g_hi, scan):
     """Every channel decaying hard, down to -5 per token: the tensor-core
     path's per-16-column-block decay references stay in range."""
     x = kda_inputs.prefill([150, 77], H=2, dtype=torch.bfloat16, seed=38, g_range=(g_lo, g_hi),
                            init_std=0.02)
-    o, sf = run_chunk(kda, x)
+    o, sf = run_chunk(kda, x, scan=scan)
     o_ref, s_ref = oracle_prefill(x)
     assert rel_l2(to_np(o), o_ref) < TOL_BF16
     assert rel_l2(vk_to_kv(sf), s_ref) < TOL_BF16
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-def test_chunk_nearly_parallel_keys(kda, dtype):
+@pytest.mark.parametrize("dtype,scan", [(torch.bfloat16, "split"), (torch.bfloat16, "wide"),
+                                        (torch.float32, "auto")])
+def test_chunk_nearly_parallel_keys(kda, dtype, scan):
     """Repeated tokens: keys within a few percent of one direction and beta
     near 1, so every entry of the intra-chunk interaction matrix is near 1
     (random keys keep it near 0).  Both chunk paths must stay on the oracle."""
@@ -207,7 +212,7 @@ def test_chunk_nearly_parallel_keys(kda, dtype):
     noise = torch.randn(x["k"].shape, generator=gen)
     x["k"] = (base + 0.03 * noise).to(dtype)
     x["beta"] = torch.full_like(x["beta"], 0.97)
-    o, sf = run_chunk(kda, x)
+    o, sf = run_chunk(kda, x, scan=scan)
     o_ref, s_ref = oracle_prefill(x)
     tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
     assert rel_l2(to_np(o), o_ref) < tol
@@ -256,6 +261,40 @@ def test_chunk_handoff_into_pool_then_decode(kda):
     assert rel_l2(vk_to_kv(pool_d), ref_pool) < TOL_F32
 
 
+@pytest.mark.parametrize("scan", SCANS)
+def test_chunk_handoff_into_pool_bf16_tensor_cores(kda, scan):
+    """bf16 prefill reading and writing the same pool slots (out of order,
+    one zero-length sequence), both scan layouts."""
+    H, slots = 3, 7
+    x = kda_inputs.prefill([140, 0, 64, 71], H=H, dtype=torch.bfloat16, seed=45)
+    pool = kda_inputs.decode_pool(slots, H=H, seed=45)
+    idx = torch.tensor([5, 0, 2, 6], dtype=torch.int32)
+    pool_d = pool.cuda()
+    d = dev(x)
+    o, _ = kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], cu_seqlens=d["cu_seqlens"],
+                             initial_state=pool_d, final_state=pool_d, state_indices=idx.cuda(),
+                             scan=scan)
+    torch.cuda.synchronize()
+    s0 = np.swapaxes(pool.double().numpy(), -1, -2)[idx.numpy()]
+    o_ref, s_ref = oracle.recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                                     cu_seqlens=x["cu_seqlens"].numpy(), initial_state=s0)
+    assert rel_l2(to_np(o), o_ref) < TOL_BF16
+    got = vk_to_kv(pool_d)
+    assert rel_l2(got[idx.numpy()], s_ref) < TOL_BF16
+    assert np.array_equal(got[0], s0[1])  # slot 0: the zero-length sequence keeps its state
+    others = [s for s in range(slots) if s not in idx.tolist()]
+    assert torch.equal(pool_d.cpu()[others], pool[others])
+
+
+def test_chunk_wide_and_split_scans_agree(kda):
+    """The two scan layouts differ only in summation order."""
+    x = kda_inputs.prefill([500, 3, 191], H=4, dtype=torch.bfloat16, seed=46, init_std=0.02)
+    o1, s1 = run_chunk(kda, x, scan="split")
+    o2, s2 = run_chunk(kda, x, scan="wide")
+    assert rel_l2(to_np(o2), to_np(o1)) < 2e-3
+    assert rel_l2(to_np(s2), to_np(s1)) < 2e-3
+
+
 def test_chunk_bad_cu_seqlens_are_flagged_and_skipped(kda):
     x = kda_inputs.prefill([64, 64], H=1, dtype=torch.float32, seed=37)
     d = dev(x)
@@ -286,11 +325,12 @@ def test_chunked_and_recurrent_gpu_paths_agree_fp32(kda):
     assert rel_l2(to_np(s_c), to_np(pool)) < TOL_F32
 
 
-def test_chunk_prefill_4k_full_size_sampled_heads(kda):
-    """B=1 H=32 T=4096 bf16 (seed 1) in the bench's launch configuration; the
-    oracle checks a sample of heads (heads are independent)."""
+@pytest.mark.parametrize("scan", ["auto", "wide"])
+def test_chunk_prefill_4k_full_size_sampled_heads(kda, scan):
+    """B=1 H=32 T=4096 bf16 (seed 1) in the bench's launch configuration
+    ("auto"); the oracle checks a sample of heads (heads are independent)."""
     x = kda_inputs.prefill_4k()
-    o, sf = run_chunk(kda, x)
+    o, sf = run_chunk(kda, x, scan=scan)
     heads = [0, 13, 31]
     o_ref, s_ref = oracle_prefill(x, heads)
     assert rel_l2(to_np(o[:, heads]), o_ref) < TOL_BF16
@@ -298,9 +338,10 @@ def test_chunk_prefill_4k_full_size_sampled_heads(kda):
     assert torch.isfinite(o).all() and torch.isfinite(sf).all()
 
 
-def test_chunk_varlen_8_full_size_sampled_heads(kda):
+@pytest.mark.parametrize("scan", ["auto", "split"])
+def test_chunk_varlen_8_full_size_sampled_heads(kda, scan):
     x = kda_inputs.varlen_8()
-    o, sf = run_chunk(kda, x)
+    o, sf = run_chunk(kda, x, scan=scan)
     heads = [5, 22]
     o_ref, s_ref = oracle_prefill(x, heads)
     assert rel_l2(to_np(o[:, heads]), o_ref) < TOL_BF16
