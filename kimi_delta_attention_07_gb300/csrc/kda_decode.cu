@@ -22,7 +22,8 @@ namespace kda {
 namespace {
 
 constexpr int kDecodeThreads = 256;  // 8 warps
-constexpr int kRowsInFlight = 8;     // rows a warp loads before reducing
+constexpr int kWarps = kDecodeThreads / 32;
+constexpr int kMaxRowsPerWarp = kHeadDim / kWarps;  // 16: a whole head per CTA
 
 template <typename T>
 __global__ void __launch_bounds__(kDecodeThreads)
@@ -37,6 +38,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int row0 = blockIdx.y * rows_per_cta;
+    const int rpw = rows_per_cta / kWarps;  // rows of this warp: row0 + warp + 8 j
 
     const int64_t slot = state_indices ? (int64_t)state_indices[n] : (int64_t)n;
     const int64_t io_k = (int64_t)pair * kHeadDim;  // offset of q/k/g/v/o rows of (n, h)
@@ -47,6 +49,16 @@ __global__ void __launch_bounds__(kDecodeThreads)
             o[io_k + row0 + r] = from_f32<T>(__int_as_float(0x7fc00000));
         return;
     }
+
+    // This warp's state rows are requested first, so that their latency
+    // overlaps the setup below; lane j also fetches v of the warp's row j.
+    float *S = pool + ((slot * H + h) * (int64_t)kHeadDim) * kHeadDim;  // [V][K] of (slot, h)
+    float4 s[kMaxRowsPerWarp];
+#pragma unroll
+    for (int j = 0; j < kMaxRowsPerWarp; ++j)
+        if (j < rpw)
+            s[j] = *reinterpret_cast<const float4 *>(S + (int64_t)(row0 + warp + kWarps * j) * kHeadDim + 4 * lane);
+    const float vrow = lane < rpw ? to_f32(v[io_k + row0 + warp + kWarps * lane]) : 0.0f;
 
     // L2 norms of q and k over the key dim (eps inside the root), scale on q.
     const float4 q4 = load4(q + io_k + 4 * lane);
@@ -62,35 +74,23 @@ __global__ void __launch_bounds__(kDecodeThreads)
     const float kq = warp_sum(kh.x * qh.x + kh.y * qh.y + kh.z * qh.z + kh.w * qh.w);
     const float b = beta[pair];
 
-    float *S = pool + ((slot * H + h) * (int64_t)kHeadDim) * kHeadDim;  // [V][K] of (slot, h)
-    const int warps = kDecodeThreads / 32;
-
-    for (int base = row0 + warp; base < row0 + rows_per_cta; base += warps * kRowsInFlight) {
-        float4 s[kRowsInFlight];
 #pragma unroll
-        for (int j = 0; j < kRowsInFlight; ++j) {
-            const int r = base + j * warps;
-            if (r < row0 + rows_per_cta)
-                s[j] = *reinterpret_cast<const float4 *>(S + (int64_t)r * kHeadDim + 4 * lane);
+    for (int j = 0; j < kMaxRowsPerWarp; ++j) {
+        if (j >= rpw) break;
+        const int r = row0 + warp + kWarps * j;
+        float4 x = s[j];
+        x.x *= dec.x; x.y *= dec.y; x.z *= dec.z; x.w *= dec.w;
+        float a = x.x * kh.x + x.y * kh.y + x.z * kh.z + x.w * kh.w;
+        float c = x.x * qh.x + x.y * qh.y + x.z * qh.z + x.w * qh.w;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            a += __shfl_xor_sync(0xffffffffu, a, off);
+            c += __shfl_xor_sync(0xffffffffu, c, off);
         }
-#pragma unroll
-        for (int j = 0; j < kRowsInFlight; ++j) {
-            const int r = base + j * warps;
-            if (r >= row0 + rows_per_cta) break;
-            float4 x = s[j];
-            x.x *= dec.x; x.y *= dec.y; x.z *= dec.z; x.w *= dec.w;
-            float a = x.x * kh.x + x.y * kh.y + x.z * kh.z + x.w * kh.w;
-            float c = x.x * qh.x + x.y * qh.y + x.z * qh.z + x.w * qh.w;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                a += __shfl_xor_sync(0xffffffffu, a, off);
-                c += __shfl_xor_sync(0xffffffffu, c, off);
-            }
-            const float u = b * (to_f32(v[io_k + r]) - a);
-            x.x += u * kh.x; x.y += u * kh.y; x.z += u * kh.z; x.w += u * kh.w;
-            *reinterpret_cast<float4 *>(S + (int64_t)r * kHeadDim + 4 * lane) = x;
-            if (lane == 0) o[io_k + r] = from_f32<T>(c + u * kq);
-        }
+        const float u = b * (__shfl_sync(0xffffffffu, vrow, j) - a);
+        x.x += u * kh.x; x.y += u * kh.y; x.z += u * kh.z; x.w += u * kh.w;
+        *reinterpret_cast<float4 *>(S + (int64_t)r * kHeadDim + 4 * lane) = x;
+        if (lane == 0) o[io_k + r] = from_f32<T>(c + u * kq);
     }
 }
 
@@ -103,7 +103,7 @@ cudaError_t launch_recurrent_step(const void *q, const void *k, const void *v, c
     const int64_t pairs = (int64_t)N * H;
     // Split a head's 128 rows over more CTAs when there are few heads in flight,
     // so that at least ~4 CTAs per SM are resident.
-    int rows = kHeadDim;
+    int rows = kHeadDim;  // a multiple of 8 warps, at most 16 rows per warp
     while (rows > 16 && pairs * (kHeadDim / rows) < 152 * 8) rows >>= 1;
     const dim3 grid((unsigned)pairs, kHeadDim / rows);
     if (dtype == KDA_BF16) {
