@@ -303,42 +303,76 @@ def run_ours(args, rank, ws):
 
 
 def run_e2e(args, kda, x, dev, stream, work, flags, ws):
-    """Same metric through the public call with HOST buffers: pinned host
-    inputs copied in, the chunked forward, output and final state copied out,
-    all inside the timed region."""
+    """Same metric through the public call with HOST buffers: every step copies
+    its inputs in from pinned host memory, runs the chunked forward and copies
+    the output and final state back, all inside the timed region.  Steps are
+    pipelined the way a serving loop would run them: the inputs of step i+1
+    are copied in (two copy streams) while step i computes and step i-1's
+    results are copied out (a third stream); device input buffers are
+    double-buffered."""
     names = ("q", "k", "v", "g", "beta")
     host = {n: x[n].pin_memory() for n in names}
-    d = {n: torch.empty_like(host[n], device=dev) for n in names}
+    nbuf = 2
+    d = [{n: torch.empty_like(host[n], device=dev) for n in names} for _ in range(nbuf)]
+    o = [torch.empty((T_4K, H, V), dtype=torch.bfloat16, device=dev) for _ in range(nbuf)]
+    sf = [torch.empty((1, H, V, K), dtype=torch.float32, device=dev) for _ in range(nbuf)]
     o_h = torch.empty((T_4K, H, V), dtype=torch.bfloat16).pin_memory()
     s_h = torch.empty((1, H, V, K), dtype=torch.float32).pin_memory()
-    o = torch.empty((T_4K, H, V), dtype=torch.bfloat16, device=dev)
-    sf = torch.empty((1, H, V, K), dtype=torch.float32, device=dev)
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
     d2h = o_h.numel() * 2 + s_h.numel() * 4
+    copy_in = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
+    copy_out = torch.cuda.Stream(device=dev)
+    lanes = (("q", "g"), ("k", "v", "beta"))  # bytes split about evenly over the copy streams
 
-    def one():
-        for n in names:
-            d[n].copy_(host[n], non_blocking=True)
-        kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], o=o, final_state=sf,
-                          workspace=work, precise=bool(flags), stream=stream)
-        o_h.copy_(o, non_blocking=True)
-        s_h.copy_(sf, non_blocking=True)
+    def ev():
+        return torch.cuda.Event(enable_timing=False)
 
-    for _ in range(3):
-        one()
+    def run(steps, start_ev=None, end_ev=None):
+        in_done = [[ev() for _ in copy_in] for _ in range(steps)]
+        done = [ev() for _ in range(steps)]
+        out_done = [ev() for _ in range(steps)]
+        if start_ev is not None:
+            start_ev.record(stream)
+            for cs in (*copy_in, copy_out):
+                cs.wait_stream(stream)
+        for i in range(steps):
+            b = i % nbuf
+            for li, cs in enumerate(copy_in):
+                if i >= nbuf:
+                    cs.wait_event(done[i - nbuf])  # buffer b is free again
+                with torch.cuda.stream(cs):
+                    for n in lanes[li]:
+                        d[b][n].copy_(host[n], non_blocking=True)
+                in_done[i][li].record(cs)
+            for e_ in in_done[i]:
+                stream.wait_event(e_)
+            if i >= nbuf:
+                stream.wait_event(out_done[i - nbuf])  # o / final state of buffer b read out
+            kda.kda_chunk_fwd(d[b]["q"], d[b]["k"], d[b]["v"], d[b]["g"], d[b]["beta"], o=o[b],
+                              final_state=sf[b], workspace=work, precise=bool(flags), stream=stream)
+            done[i].record(stream)
+            copy_out.wait_event(done[i])
+            with torch.cuda.stream(copy_out):
+                o_h.copy_(o[b], non_blocking=True)
+                s_h.copy_(sf[b], non_blocking=True)
+            out_done[i].record(copy_out)
+        if end_ev is not None:
+            for cs in (*copy_in, copy_out):
+                stream.wait_stream(cs)
+            end_ev.record(stream)
+
+    run(3)
     torch.cuda.synchronize()
     steps = max(1, min(args.steps, 20))
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(ws)
     torch.cuda.synchronize()
-    a.record(stream)
-    for _ in range(steps):
-        one()
-    b.record(stream)
+    run(steps, a, b)
     torch.cuda.synchronize()
     ms = max_over_ranks(a.elapsed_time(b), ws, dev)
     return {"value": round(T_4K * steps * ws / (ms / 1e3), 1), "unit": "tokens/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "pipelined": "copy-in of step i+1 and copy-out of step i-1 overlap step i"}
 
 
 def run_decode(args, kda, dev, stream, pk, ws):
