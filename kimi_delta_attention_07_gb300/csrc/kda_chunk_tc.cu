@@ -108,10 +108,9 @@ constexpr int P_RQ = P_BS + 40960;        // fp32 [64]: scale / |q_r|
 constexpr int P_RK = P_RQ + 256;          // fp32 [64]: 1 / |k_r|
 constexpr int P_BETA = P_RK + 256;        // fp32 [64]
 constexpr int P_GREF = P_BETA + 256;      // fp32 [5][128]: G at rows 0, 16, 32, 48, 63
-constexpr int P_RHO = P_GREF + 5 * 512;   // fp32 [4][128]: exp(G_16b)
-constexpr int P_TAU = P_RHO + 4 * 512;    // fp32 [6][128]: exp(G_16br - G_16b), br > b
+constexpr int P_TAU = P_GREF + 5 * 512;   // fp32 [6][128]: exp(G_16br - G_16b), br > b
 constexpr int P_QSUM = P_TAU + 6 * 512;   // fp32 [4][128]: per-quarter sums of g
-constexpr int P_PSI = P_QSUM + 4 * 512;   // fp32 [4][128]: exp(G_last - G_16b)
+constexpr int P_PSI = P_QSUM + 4 * 512;   // fp32 [4][128]: G_last - G_16b
 constexpr int P_FIRST = P_PSI + 4 * 512;  // fp32 [4][128]: g at rows 0, 16, 32, 48
 constexpr int P_BAR = P_FIRST + 4 * 512;    // q/k/g barrier, mma barrier, tmem slot, v barrier, metadata
 constexpr int P_BS2 = (P_BAR + 64 + 1023) / 1024 * 1024;  // 40 KB: low part of the stacked operand
@@ -238,7 +237,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     unsigned char *sBS2 = sm + P_BS2;
     float *sB = reinterpret_cast<float *>(sm + P_BETA);
     float *sGref = reinterpret_cast<float *>(sm + P_GREF);
-    float *sRho = reinterpret_cast<float *>(sm + P_RHO);
     float *sTau = reinterpret_cast<float *>(sm + P_TAU);
     float *sQsum = reinterpret_cast<float *>(sm + P_QSUM);
     float *sPsi = reinterpret_cast<float *>(sm + P_PSI);
@@ -325,9 +323,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         // 1. cumulative log-decay, one key channel and one 16-row block per
         //    thread: sG receives G_r - G_16b (b = r's block, so <= 0); the
         //    block sums and first-row values then give every reference
-        //    quantity of the thread's block: G_16b, rho_b = exp(G_16b),
-        //    psi_b = exp(G_last - G_16b), tau(b, b') = exp(G_16b - G_16b'),
-        //    b' < b, and gC = exp(G_last).
+        //    quantity of the thread's block: G_16b, G_last - G_16b,
+        //    tau(b, b') = exp(G_16b - G_16b'), b' < b, and gC = exp(G_last).
         {
             const int d = tid & (D - 1), qtr = tid >> 7, r0 = 16 * qtr;
             float x[16];
@@ -357,8 +354,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             for (int b = 0; b < 3; ++b)
                 if (b < qtr) sTau[tau_index(qtr, b) * D + ds] = __expf(gb - gfirst[b]);
             sGref[qtr * D + ds] = gb;
-            sRho[qtr * D + ds] = __expf(gb);
-            sPsi[qtr * D + ds] = __expf(gl - gb);
+            sPsi[qtr * D + ds] = gl - gb;
             if (qtr == 3) {
                 sGref[4 * D + ds] = gl;
                 reinterpret_cast<float *>(rec + TcRec::GC)[d] = __expf(gl);
@@ -407,7 +403,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                 ql[t] = qv[t] * rq * l8[t];
                 kl[t] = kh[t] * l8[t];
                 tiny |= l8[t] < 1e-30f;
-                inv[t] = __fdividef(1.0f, l8[t]);
+                inv[t] = __expf(-rel8[t]);  // 1 / l
             }
             *reinterpret_cast<uint4 *>(sXL + sw128_off(r, d0, 128)) = pack8(ql);
             *reinterpret_cast<uint4 *>(sXL + sw128_off(64 + r, d0, 128)) = pack8(kl);
@@ -468,34 +464,25 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             *sNext = prep_item(item + 2 * gridDim.x, H, chunk_off, seq_start, seq_len, n_seqs);
 
         // While the MMA runs: QG = q_hat exp(G) and KD = k_hat exp(G_last - G)
-        // to the record, E = k_hat exp(G) (MN-major [j][d], for W = T E).
+        // to the record, E = k_hat exp(G) (MN-major [j][d], for W = T E); both
+        // exponents are <= 0 and formed from the block-relative G.
 #pragma unroll 1
         for (int it = 0; it < 2; ++it) {
             const int r = 32 * it + (tid >> 4), d0 = (tid & 15) * 8, bj = r >> 4;
-            float rel8[8], rho8[8], ps8[8], qv[8], kv[8];
+            float rel8[8], gb8[8], lp8[8], qv[8], kv[8];
             load8s(sG + r * D, d0, rel8);
-            load8s(sRho + bj * D, d0, rho8);
-            load8s(sPsi + bj * D, d0, ps8);
+            load8s(sGref + bj * D, d0, gb8);
+            load8s(sPsi + bj * D, d0, lp8);
             unpack8(*reinterpret_cast<const uint4 *>(sQr + r * D + d0), qv);
             unpack8(*reinterpret_cast<const uint4 *>(sKr + r * D + d0), kv);
             const float rq = sRq[r], rk = sRk[r];
-            float qg[8], e8[8], kd8[8], kh[8], l8[8];
-            bool tiny = false;
+            float qg[8], e8[8], kd8[8];
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
-                l8[t] = __expf(rel8[t]);
-                kh[t] = kv[t] * rk;
-                qg[t] = qv[t] * rq * l8[t] * rho8[t];
-                e8[t] = kh[t] * l8[t] * rho8[t];
-                tiny |= l8[t] < 1e-30f;
-            }
-            if (!__builtin_expect(tiny, 0)) {
-#pragma unroll
-                for (int t = 0; t < 8; ++t) kd8[t] = kh[t] * ps8[t] * __fdividef(1.0f, l8[t]);
-            } else {  // exp(G_last - G) directly where 1 / l would overflow
-#pragma unroll
-                for (int t = 0; t < 8; ++t)
-                    kd8[t] = kh[t] * __expf(sGref[4 * D + swz(d0 + t)] - sGref[bj * D + swz(d0 + t)] - rel8[t]);
+                const float eg = __expf(gb8[t] + rel8[t]), kh = kv[t] * rk;
+                qg[t] = qv[t] * rq * eg;
+                e8[t] = kh * eg;
+                kd8[t] = kh * __expf(lp8[t] - rel8[t]);
             }
             *reinterpret_cast<uint4 *>(rec + TcRec::WQ + sw128_off(64 + r, d0, 128)) = pack8(qg);
             *reinterpret_cast<uint4 *>(sE + sw128_off(r, d0, 64)) = pack8(e8);
