@@ -19,6 +19,14 @@ Named workloads (seed in brackets):
   long_131k         B=1 H=32 T=131072 bf16, g per (t,h,k): 90% U[-0.01,-1e-5],
                     10% U[-3,-1]; then 256 decode steps                      [4]
 q, k, v ~ N(0, 1); beta = sigmoid(N(0, 1)) (already activated), fp32.
+
+Gated variants (the model's raw gates; the library activates them in-kernel):
+  raw_gate [T, H, K] and raw_beta [T, H] ~ N(0, 1) in the q/k/v dtype,
+  a_log [H] = log U[a_lo, a_hi] (the model initialises A_log = log U[1, 16]),
+  dt_bias [H, K] ~ U[b_lo, b_hi] fp32, and an optional lower bound
+  (the lower-bounded "safe" gate keeps every decay in (lower_bound, 0)).
+  prefill_4k_gated  prefill_4k's q/k/v with raw gates, A_log = log U[1, 16],
+                    dt_bias ~ U[-1, 1], lower bound -5                       [5]
 """
 from __future__ import annotations
 
@@ -107,6 +115,29 @@ def decode_tokens(N, H=32, K=K_DIM, V=V_DIM, dtype=torch.bfloat16, seed=3, step=
     return dict(q=q, k=k, v=v, g=g, beta=beta)
 
 
+def gate_params(H, K=K_DIM, seed=5, a_range=(1.0, 16.0), bias_range=(-1.0, 1.0)):
+    """a_log [H] = log U[a_range], dt_bias [H, K] ~ U[bias_range], fp32."""
+    gen = _gen(seed * 7 + 3)
+    a_log = torch.log(_uniform((H,), gen, *a_range))
+    dt_bias = _uniform((H, K), gen, *bias_range)
+    return a_log, dt_bias
+
+
+def with_raw_gates(x, seed=5, dtype=None, a_range=(1.0, 16.0), bias_range=(-1.0, 1.0),
+                   lower_bound=-5.0):
+    """Add raw gates and gate parameters to a prefill or decode input dict
+    (raw_gate like g, raw_beta like beta, in the q dtype unless given)."""
+    dtype = x["q"].dtype if dtype is None else dtype
+    gen = _gen(seed * 13 + 11)
+    y = dict(x)
+    y["raw_gate"] = _normal(tuple(x["g"].shape), gen, dtype=dtype)
+    y["raw_beta"] = _normal(tuple(x["beta"].shape), gen, dtype=dtype)
+    H, K = x["g"].shape[-2], x["g"].shape[-1]
+    y["a_log"], y["dt_bias"] = gate_params(H, K, seed, a_range, bias_range)
+    y["lower_bound"] = lower_bound
+    return y
+
+
 # ---- the named workloads ---------------------------------------------------
 
 def recurrence_small():
@@ -127,10 +158,15 @@ def long_131k(T=131072, H=32):
     return prefill([T], H=H, dtype=torch.bfloat16, seed=4, g_mixed=True)
 
 
+def prefill_4k_gated(T=4096, H=32):
+    return with_raw_gates(prefill_4k(T, H), seed=5)
+
+
 WORKLOADS = {
     "recurrence_small": "B=1 H=2 T=256 K=V=128 fp32, g~U[-0.2,-0.001], seed 0",
     "prefill_4k": "B=1 H=32 T=4096 K=V=128 bf16 q/k/v, g~U[-0.1,-0.0005], S0=0, seed 1",
     "varlen_8": "8 packed seqs, lengths U{512..8192}, H=32 bf16, S0~N(0,0.02^2), seed 2",
     "decode_256": "256 seqs x H=32, pool fp32 [256,32,128,128]~N(0,0.02^2), 64 bf16 steps, seed 3",
     "long_131k": "B=1 H=32 T=131072 bf16, g 90% U[-0.01,-1e-5] / 10% U[-3,-1], +256 decode steps, seed 4",
+    "prefill_4k_gated": "prefill_4k with raw bf16 gates ~N(0,1), A_log=log U[1,16], dt_bias~U[-1,1], lower bound -5, seed 5",
 }

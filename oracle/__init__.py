@@ -18,6 +18,13 @@ Two independent statements of the same mathematics:
   scores, inter-chunk state pass).  Pure numpy, fp64, exact pairwise
   exponentials; used only to cross-check the recurrence on tiny inputs.
 
+``gate_activation`` is the model's gate activation (raw decay gate plus
+per-channel bias, scaled by exp(A_log), through a lower-bounded sigmoid or a
+softplus; raw beta through a sigmoid), as written in the Ascend model file's
+``_prefill_torch_kda`` and decode branch; the gated entry points compute it
+in-kernel and are compared against ``gate_activation`` followed by the
+recurrence.
+
 ``step`` is one decode token of the recurrence on rows of a state pool picked
 by slot indices (the model file's ``_decode_gdr`` / ``_decode_fused_kda``
 semantics: the pool is updated in place).
@@ -212,3 +219,35 @@ def chunked_form(q, k, v, g, beta, initial_state=None, chunk: int = 64, scale=No
             S = np.exp(GC)[:, None] * S + (np.exp(GC[None, :] - G) * Kc).T @ Vnew
         S_all[h] = S
     return o[:T], S_all
+
+
+def _softplus(x: np.ndarray) -> np.ndarray:
+    """max(x, 0) + log1p(exp(-|x|)): the model file's ``_softplus``, in fp64."""
+    return np.maximum(x, 0.0) + np.log1p(np.exp(-np.abs(x)))
+
+
+def _sigmoid(x: np.ndarray) -> np.ndarray:
+    """1 / (1 + exp(-x)) without overflow for large |x| (fp64)."""
+    e = np.exp(-np.abs(x))
+    return np.where(x >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
+
+
+def gate_activation(raw_gate, raw_beta, a_log, dt_bias, lower_bound=None):
+    """The gate activation of the Ascend model file (``_prefill_torch_kda``; the
+    same formulas in the decode branch of ``KimiDeltaAttention.forward``):
+
+        x    = raw_gate + dt_bias[h, k]
+        g    = lower_bound * sigmoid(exp(a_log[h]) * x)   with a lower bound
+             = -exp(a_log[h]) * softplus(x)               without
+        beta = sigmoid(raw_beta)
+
+    raw_gate [T, H, K], raw_beta [T, H], a_log [H], dt_bias [H, K] (the model's
+    flat [H*K] parameter viewed per head).  Returns (g, beta) in fp64."""
+    x = _f64(raw_gate) + _f64(dt_bias)[None, :, :]
+    scale = np.exp(_f64(a_log))[None, :, None]
+    if lower_bound is None:
+        g = -scale * _softplus(x)
+    else:
+        g = float(lower_bound) * _sigmoid(scale * x)
+    return g, _sigmoid(_f64(raw_beta))
+

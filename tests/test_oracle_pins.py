@@ -288,3 +288,77 @@ def test_steps_compose_to_the_sequence_recurrence():
         np.testing.assert_allclose(o_t[0], o_seq[t], rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(p[1], S_seq[0], rtol=1e-12, atol=1e-13)
     np.testing.assert_array_equal(p[0], pool[0])
+
+
+# ---------------------------------------------------------------------------
+# gate activation (Ascend model file, _prefill_torch_kda / decode branch)
+# ---------------------------------------------------------------------------
+
+def _gate_params(rng, H, K):
+    a_log = np.log(rng.uniform(1.0, 16.0, H))   # the model's A_log initialisation
+    dt_bias = rng.standard_normal((H, K))
+    return a_log, dt_bias
+
+
+def test_gate_at_zero_input_is_log2_or_half_the_bound():
+    """x = raw + dt_bias = 0: softplus(0) = log 2, sigmoid(0) = 1/2."""
+    rng = np.random.default_rng(21)
+    T, H, K = 3, 4, 5
+    a_log, dt_bias = _gate_params(rng, H, K)
+    raw = np.broadcast_to(-dt_bias, (T, H, K))
+    g, beta = oracle.gate_activation(raw, np.zeros((T, H)), a_log, dt_bias)
+    np.testing.assert_allclose(g, np.broadcast_to(-np.exp(a_log)[None, :, None] * np.log(2.0), g.shape),
+                               rtol=1e-15)
+    np.testing.assert_array_equal(beta, 0.5)
+    g_lb, _ = oracle.gate_activation(raw, np.zeros((T, H)), a_log, dt_bias, lower_bound=-5.0)
+    np.testing.assert_allclose(g_lb, -2.5, rtol=1e-15)
+
+
+def test_gate_softplus_and_sigmoid_reflection_identities():
+    """softplus(x) - softplus(-x) = x  and  sigmoid(x) + sigmoid(-x) = 1, through
+    the full activation: g(x) - g(-x) = -exp(A_log) x ; g_lb(x) + g_lb(-x) = lb ;
+    beta(r) + beta(-r) = 1."""
+    rng = np.random.default_rng(22)
+    T, H, K = 6, 3, 7
+    a_log, dt_bias = _gate_params(rng, H, K)
+    x = rng.standard_normal((T, H, K)) * 4.0
+    r = rng.standard_normal((T, H)) * 6.0
+    g_p, b_p = oracle.gate_activation(x - dt_bias, r, a_log, dt_bias)
+    g_m, b_m = oracle.gate_activation(-x - dt_bias, -r, a_log, dt_bias)
+    np.testing.assert_allclose(g_p - g_m, -np.exp(a_log)[None, :, None] * x, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(b_p + b_m, 1.0, rtol=0, atol=1e-15)
+    lb = -3.5
+    gl_p, _ = oracle.gate_activation(x - dt_bias, r, a_log, dt_bias, lower_bound=lb)
+    gl_m, _ = oracle.gate_activation(-x - dt_bias, r, a_log, dt_bias, lower_bound=lb)
+    np.testing.assert_allclose(gl_p + gl_m, lb, rtol=1e-14)
+
+
+def test_gate_limits_and_ranges():
+    """Large positive x: softplus(x) = x to fp64 rounding; large negative x:
+    softplus(x) = exp(x) (first order); the lower-bounded gate lies in (lb, 0),
+    the softplus gate below 0, beta in (0, 1); per-head scale exp(A_log) and
+    per-(head, channel) bias are applied where they belong."""
+    H, K = 2, 3
+    a_log = np.log(np.array([2.0, 8.0]))
+    dt_bias = np.array([[0.0, 1.0, -1.0], [0.5, 0.0, 0.0]])
+    big = np.full((1, H, K), 60.0) - dt_bias
+    g, _ = oracle.gate_activation(big, np.zeros((1, H)), a_log, dt_bias)
+    np.testing.assert_allclose(g[0], -np.exp(a_log)[:, None] * 60.0 * np.ones((H, K)), rtol=1e-15)
+    small = np.full((1, H, K), -40.0) - dt_bias
+    g, _ = oracle.gate_activation(small, np.zeros((1, H)), a_log, dt_bias)
+    np.testing.assert_allclose(g[0], -np.exp(a_log)[:, None] * np.exp(-40.0) * np.ones((H, K)), rtol=1e-12)
+    rng = np.random.default_rng(23)
+    raw = rng.standard_normal((50, H, K)) * 5
+    rb = rng.standard_normal((50, H)) * 5
+    g_lb, beta = oracle.gate_activation(raw, rb, a_log, dt_bias, lower_bound=-5.0)
+    assert np.all(g_lb >= -5.0) and np.all(g_lb < 0.0)  # (lb, 0); lb itself once fp64 saturates
+    mid = np.abs(raw) < 0.2
+    assert np.all(g_lb[mid] > -5.0)
+    assert np.all(beta > 0.0) and np.all(beta < 1.0)
+    g_sp, _ = oracle.gate_activation(raw, rb, a_log, dt_bias)
+    assert np.all(g_sp < 0.0)
+    # channel 1 of head 0 has bias +1: the same raw value gives the input x + 1
+    raw1 = np.zeros((1, H, K))
+    g1, _ = oracle.gate_activation(raw1, np.zeros((1, H)), a_log, dt_bias)
+    np.testing.assert_allclose(g1[0, 0, 1], -np.exp(a_log[0]) * np.log1p(np.exp(1.0)), rtol=1e-15)
+    np.testing.assert_allclose(g1[0, 1, 0], -np.exp(a_log[1]) * np.log1p(np.exp(0.5)), rtol=1e-15)
