@@ -53,6 +53,7 @@ def parse():
     p.add_argument("--no-decode", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--precise", action="store_true", help="fp32 CUDA-core chunk path")
+    p.add_argument("--no-gated", action="store_true", help="skip the raw-gate prefill sub-run")
     return p.parse_args()
 
 
@@ -189,6 +190,52 @@ def prefill_bytes(T, H, elem=2):
     return dict(intra=qkv + g + beta, scan=o + state, step=qkv + g + beta + o + state)
 
 
+def gated_prefill_bytes(T, H, elem=2):
+    """Raw gates in the q/k/v dtype (plus A_log, dt_bias) instead of fp32 g, beta."""
+    qkv = 3 * T * H * K * elem
+    gate = T * H * K * elem + T * H * elem + H * 4 + H * K * 4
+    o = T * H * V * elem
+    state = H * V * K * 4
+    return qkv + gate + o + state
+
+
+def run_gated(args, kda, dev, stream, ws):
+    """The 4k prefill from the model's raw gates (bf16 raw gate and beta, lower
+    bound -5), activated in-kernel: one kda_chunk_fwd_gated call per step."""
+    y = kda_inputs.prefill_4k_gated()
+    d = {n: y[n].to(dev) for n in ("q", "k", "v", "raw_gate", "raw_beta", "a_log", "dt_bias")}
+    o = torch.empty((T_4K, H, V), dtype=torch.bfloat16, device=dev)
+    sf = torch.empty((1, H, V, K), dtype=torch.float32, device=dev)
+    need = kda.kda_chunk_workspace_bytes(T_4K, 1, H, flags=kda.KDA_CHUNK_GATED)
+    work = torch.empty(need, dtype=torch.uint8, device=dev)
+
+    def step():
+        kda.kda_chunk_fwd_gated(d["q"], d["k"], d["v"], d["raw_gate"], d["raw_beta"], d["a_log"],
+                                d["dt_bias"], lower_bound=y["lower_bound"], o=o, final_state=sf,
+                                workspace=work, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b), ws, dev) / args.steps
+    byt = gated_prefill_bytes(T_4K, H)
+    pk = peaks()
+    return {"workload": "prefill_4k_gated", "tokens_per_s": round(T_4K * ws / (ms / 1e3), 1),
+            "ms_per_step": round(ms, 4), "steps": args.steps,
+            "gate": "raw bf16 gate + dt_bias, exp(A_log) scale, lower bound -5; raw bf16 beta",
+            "roofline": {"bound": "hbm", "algorithmic_bytes": byt,
+                         "achieved": round(byt / (ms / 1e3) / 1e9, 1), "peak": pk["hbm"],
+                         "unit": "GB/s", "frac": round(byt / (ms / 1e3) / 1e9 / pk["hbm"], 4)}}
+
+
 def decode_bytes(N, H, elem=2):
     state = 2 * N * H * V * K * 4  # read + write
     io = N * H * (2 * K * elem + V * elem + K * 4 + 4 + V * elem)
@@ -278,6 +325,7 @@ def run_ours(args, rank, ws):
 
     e2e = None if args.no_e2e else run_e2e(args, kda, x, dev, stream, work, flags, ws)
     dec = None if args.no_decode else run_decode(args, kda, dev, stream, pk, ws)
+    gated = None if (args.no_gated or args.precise) else run_gated(args, kda, dev, stream, ws)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(x, sample_heads=H)
@@ -297,7 +345,7 @@ def run_ours(args, rank, ws):
                        "path": "fp32 CUDA-core (precise)" if args.precise else "default"},
             "roofline": roofline, "step_roofline": step_roofline, "kernels": kernels,
             "e2e": e2e, "gpu_launches": launches, "clocks": clk,
-            "decode": dec, "cpu_baseline": cpu,
+            "decode": dec, "gated": gated, "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
 

@@ -75,6 +75,7 @@ typedef enum {
 #define KDA_CHUNK_PRECISE 1    /* fp32 CUDA-core chunk path also for bf16 inputs */
 #define KDA_CHUNK_SCAN_WIDE 2  /* tensor-core path: one scan CTA per (sequence, head) */
 #define KDA_CHUNK_SCAN_SPLIT 4 /* tensor-core path: four scan CTAs per (sequence, head) */
+#define KDA_CHUNK_GATED 8      /* kda_chunk_workspace_bytes only: size for kda_chunk_fwd_gated */
 
 /* Chunk length of the chunked form (Ascend model file, _KDA_CHUNK_SIZE). */
 #define KDA_CHUNK 64
@@ -236,6 +237,46 @@ int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const flo
                           const int32_t *state_indices, int64_t n_slots, void *o,
                           const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens, int H,
                           int K, int V, float scale, int dtype, int flags, void *stream);
+
+/*
+ * Gated entry points: the model's gate activation computed in-kernel
+ * (Ascend model file, _prefill_torch_kda and the decode branch of
+ * KimiDeltaAttention.forward).  Instead of activated g and beta they take
+ *
+ *   raw_gate    [T, H, K] (prefill) / [N, H, K] (decode), in the q dtype
+ *   raw_beta    [T, H] / [N, H], in the q dtype
+ *   a_log       device fp32 [H]      (the model's A_log)
+ *   dt_bias     device fp32 [H, K]   (the model's flat dt_bias, per head)
+ *   lower_bound, use_lower_bound
+ *
+ * and use, per element,
+ *   x    = raw_gate + dt_bias[h][k]
+ *   g    = lower_bound * sigmoid(exp(a_log[h]) * x)   if use_lower_bound
+ *        = -exp(a_log[h]) * softplus(x)               otherwise
+ *   beta = sigmoid(raw_beta)
+ * with softplus(x) = max(x, 0) + log1p(exp(-|x|)).  Everything else --
+ * arguments, layouts, aliasing, errors -- is as for kda_chunk_fwd /
+ * kda_recurrent_step.  The tensor-core path reads the raw bf16 gate and
+ * activates it on chip (half the gate bytes of an fp32 g); the fp32 path
+ * activates it into the workspace first.  Size the workspace with
+ * kda_chunk_workspace_bytes(..., flags | KDA_CHUNK_GATED).  The tensor-core
+ * path's decay-range limit (per-token decays down to about -5.3) makes the
+ * lower-bounded gate with lower_bound >= -5 the form to use there, as the
+ * model's own fast path does.
+ */
+int kda_chunk_fwd_gated(const void *q, const void *k, const void *v, const void *raw_gate,
+                        const void *raw_beta, const float *a_log, const float *dt_bias,
+                        float lower_bound, int use_lower_bound, const float *initial_state,
+                        float *final_state, const int32_t *state_indices, int64_t n_slots,
+                        void *o, const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens,
+                        int H, int K, int V, float scale, int dtype, int flags, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+int kda_recurrent_step_gated(const void *q, const void *k, const void *v, const void *raw_gate,
+                             const void *raw_beta, const float *a_log, const float *dt_bias,
+                             float lower_bound, int use_lower_bound, float *state_pool,
+                             const int32_t *state_indices, int64_t n_slots, void *o, int N,
+                             int H, int K, int V, float scale, int dtype, void *stream);
 
 #ifdef __cplusplus
 }

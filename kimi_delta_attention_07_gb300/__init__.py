@@ -25,12 +25,13 @@ KDA_F32, KDA_BF16 = 0, 1
 KDA_CHUNK_PRECISE = 1
 KDA_CHUNK_SCAN_WIDE = 2
 KDA_CHUNK_SCAN_SPLIT = 4
+KDA_CHUNK_GATED = 8
 _SCAN_FLAGS = {"auto": 0, "wide": KDA_CHUNK_SCAN_WIDE, "split": KDA_CHUNK_SCAN_SPLIT}
 CHUNK = 64
 
 EXPORTS = ("kda_status_string", "kda_version", "kda_chunk_workspace_bytes", "kda_chunk_fwd",
            "kda_chunk_intra", "kda_chunk_scan", "kda_workspace_status", "kda_recurrent_step",
-           "kda_chunk_fwd_noalloc")
+           "kda_chunk_fwd_noalloc", "kda_chunk_fwd_gated", "kda_recurrent_step_gated")
 NOALLOC_WORKSPACE_BYTES = 64 * 1024 * 1024
 
 _lib = None
@@ -77,6 +78,12 @@ def load(path: str | None = None):
         L.kda_recurrent_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, vp, i32, i32, i32, i32,
                                          f32, i32, vp]
         L.kda_recurrent_step.restype = i32
+        L.kda_chunk_fwd_gated.argtypes = [vp, vp, vp, vp, vp, vp, vp, f32, i32, vp, vp, vp, i64, vp,
+                                          vp, i32, i64, i32, i32, i32, f32, i32, i32, vp, sz, vp]
+        L.kda_chunk_fwd_gated.restype = i32
+        L.kda_recurrent_step_gated.argtypes = [vp, vp, vp, vp, vp, vp, vp, f32, i32, vp, vp, i64,
+                                               vp, i32, i32, i32, i32, f32, i32, vp]
+        L.kda_recurrent_step_gated.restype = i32
         _lib = L
         return L
 
@@ -123,7 +130,7 @@ def kda_chunk_workspace_bytes(total_tokens: int, n_seqs: int, H: int, K: int = 1
 def kda_chunk_fwd(q, k, v, g, beta, *, cu_seqlens=None, n_seqs=None, initial_state=None,
                   final_state=None, state_indices=None, n_slots=None, scale=None,
                   precise=False, output_final_state=True, o=None, workspace=None, stream=None,
-                  phase="fwd", scan="auto"):
+                  phase="fwd", scan="auto", _gate=None):
     """Chunked KDA forward.
 
     q, k, g: [T, H, K]; v: [T, H, V]; beta: [T, H] (all CUDA, contiguous).
@@ -142,10 +149,11 @@ def kda_chunk_fwd(q, k, v, g, beta, *, cu_seqlens=None, n_seqs=None, initial_sta
         N = cu_seqlens.numel() - 1
     else:
         N = 1 if n_seqs is None else int(n_seqs)
+    gdt = q.dtype if _gate is not None else torch.float32  # raw gates come in the q dtype
     for name, t, dtype_, shape in (("q", q, q.dtype, (T, H, K)), ("k", k, q.dtype, (T, H, K)),
                                    ("v", v, q.dtype, (T, H, V)),
-                                   ("g", g, torch.float32, (T, H, K)),
-                                   ("beta", beta, torch.float32, (T, H)),
+                                   ("g", g, gdt, (T, H, K)),
+                                   ("beta", beta, gdt, (T, H)),
                                    ("cu_seqlens", cu_seqlens, torch.int32, None),
                                    ("state_indices", state_indices, torch.int32, (N,)),
                                    ("initial_state", initial_state, torch.float32, None)):
@@ -167,20 +175,83 @@ def kda_chunk_fwd(q, k, v, g, beta, *, cu_seqlens=None, n_seqs=None, initial_sta
         o = torch.empty((T, H, V), dtype=q.dtype, device=q.device)
     _check(o, "o", q.dtype, (T, H, V))
     flags = (KDA_CHUNK_PRECISE if precise else 0) | _SCAN_FLAGS[scan]
+    if _gate is not None:
+        flags |= KDA_CHUNK_GATED
     need = kda_chunk_workspace_bytes(T, N, H, K, V, dt, flags)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     _check(workspace, "workspace", torch.uint8)
     if scale is None:
         scale = K ** -0.5
-    name = {"fwd": "kda_chunk_fwd", "intra": "kda_chunk_intra", "scan": "kda_chunk_scan"}[phase]
-    st = getattr(load(), name)(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(initial_state),
-                               _p(final_state), _p(state_indices), slots, _p(o), _p(cu_seqlens),
-                               N, T, H, K, V, float(scale), dt, flags, _p(workspace),
-                               workspace.numel(), _stream(stream))
+    if _gate is not None:
+        if phase != "fwd":
+            raise ValueError("the gated forward runs as one call (phase='fwd')")
+        a_log, dt_bias, lower_bound = _gate
+        name = "kda_chunk_fwd_gated"
+        st = load().kda_chunk_fwd_gated(
+            _p(q), _p(k), _p(v), _p(g), _p(beta), _p(a_log), _p(dt_bias),
+            float(0.0 if lower_bound is None else lower_bound), int(lower_bound is not None),
+            _p(initial_state), _p(final_state), _p(state_indices), slots, _p(o), _p(cu_seqlens),
+            N, T, H, K, V, float(scale), dt, flags, _p(workspace), workspace.numel(),
+            _stream(stream))
+    else:
+        name = {"fwd": "kda_chunk_fwd", "intra": "kda_chunk_intra", "scan": "kda_chunk_scan"}[phase]
+        st = getattr(load(), name)(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(initial_state),
+                                   _p(final_state), _p(state_indices), slots, _p(o),
+                                   _p(cu_seqlens), N, T, H, K, V, float(scale), dt, flags,
+                                   _p(workspace), workspace.numel(), _stream(stream))
     if st != KDA_OK:
         raise KdaError(st, name)
     return o, final_state
+
+
+def _check_gate(a_log, dt_bias, H, K):
+    _check(a_log, "a_log", torch.float32, (H,))
+    _check(dt_bias, "dt_bias", torch.float32, (H, K))
+
+
+def kda_chunk_fwd_gated(q, k, v, raw_gate, raw_beta, a_log, dt_bias, *, lower_bound=None, **kw):
+    """Chunked KDA forward from the model's raw gates, activated in-kernel:
+    g = lower_bound * sigmoid(exp(a_log[h]) (raw_gate + dt_bias[h])) (or
+    -exp(a_log[h]) softplus(raw_gate + dt_bias[h]) without a lower bound),
+    beta = sigmoid(raw_beta).  raw_gate [T, H, K] and raw_beta [T, H] in the
+    q dtype; a_log [H] and dt_bias [H, K] fp32.  Other arguments as for
+    kda_chunk_fwd.  Returns (o, final_state)."""
+    H, K = q.shape[1], q.shape[2]
+    _check_gate(a_log, dt_bias, H, K)
+    return kda_chunk_fwd(q, k, v, raw_gate, raw_beta, _gate=(a_log, dt_bias, lower_bound), **kw)
+
+
+def kda_recurrent_step_gated(q, k, v, raw_gate, raw_beta, a_log, dt_bias, state_pool, *,
+                             lower_bound=None, state_indices=None, scale=None, o=None,
+                             stream=None):
+    """kda_recurrent_step from the model's raw gates (see kda_chunk_fwd_gated)."""
+    N, H, K = q.shape
+    V = v.shape[-1]
+    dt = _dtype_code(q)
+    for name, t, dtype_, shape in (("q", q, q.dtype, (N, H, K)), ("k", k, q.dtype, (N, H, K)),
+                                   ("v", v, q.dtype, (N, H, V)),
+                                   ("raw_gate", raw_gate, q.dtype, (N, H, K)),
+                                   ("raw_beta", raw_beta, q.dtype, (N, H)),
+                                   ("state_pool", state_pool, torch.float32, None),
+                                   ("state_indices", state_indices, torch.int32, (N,))):
+        _check(t, name, dtype_, shape)
+    _check_gate(a_log, dt_bias, H, K)
+    if state_pool.dim() != 4 or tuple(state_pool.shape[1:]) != (H, V, K):
+        raise ValueError(f"state_pool must be [slots, {H}, {V}, {K}]")
+    if o is None:
+        o = torch.empty((N, H, V), dtype=q.dtype, device=q.device)
+    _check(o, "o", q.dtype, (N, H, V))
+    if scale is None:
+        scale = K ** -0.5
+    st = load().kda_recurrent_step_gated(
+        _p(q), _p(k), _p(v), _p(raw_gate), _p(raw_beta), _p(a_log), _p(dt_bias),
+        float(0.0 if lower_bound is None else lower_bound), int(lower_bound is not None),
+        _p(state_pool), _p(state_indices), state_pool.shape[0], _p(o), N, H, K, V, float(scale),
+        dt, _stream(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_recurrent_step_gated")
+    return o
 
 
 def kda_workspace_status(workspace, stream=None) -> int:

@@ -45,7 +45,11 @@ size_t kda_chunk_workspace_bytes(int64_t total_tokens, int n_seqs, int H, int K,
     if (total_tokens < 0 || n_seqs <= 0 || H <= 0 || K != kHeadDim || V != kHeadDim ||
         !valid_dtype(dtype))
         return 0;
-    return ws_layout(total_tokens, n_seqs, H, record_bytes(dtype, flags)).total;
+    const WsLayout L = ws_layout(total_tokens, n_seqs, H, record_bytes(dtype, flags));
+    // a gated call on the fp32 path also holds the activated g and beta
+    if ((flags & KDA_CHUNK_GATED) && !use_tensor_cores(dtype, flags))
+        return ws_gate(L, total_tokens, H).total;
+    return L.total;
 }
 
 }  // extern "C"
@@ -54,18 +58,37 @@ namespace {
 
 enum Phase { kIntra = 1, kScan = 2, kBoth = 3 };
 
+// gate == nullptr: g and beta are the activated fp32 inputs; otherwise g and
+// beta are unused and the model's raw gates (*gate) are activated in-kernel.
 int chunk_call(int phase, const void *q, const void *k, const void *v, const float *g,
-               const float *beta, const float *initial_state, float *final_state,
-               const int32_t *state_indices, int64_t n_slots, void *o, const int32_t *cu_seqlens,
-               int n_seqs, int64_t total_tokens, int H, int K, int V, float scale, int dtype,
-               int flags, void *workspace, size_t workspace_bytes, void *stream) {
+               const float *beta, const GateArgs *gate, const float *initial_state,
+               float *final_state, const int32_t *state_indices, int64_t n_slots, void *o,
+               const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens, int H, int K, int V,
+               float scale, int dtype, int flags, void *workspace, size_t workspace_bytes,
+               void *stream) {
     if (!valid_dtype(dtype) || n_seqs <= 0 || H <= 0 || K <= 0 || V <= 0 || total_tokens < 0 ||
         total_tokens > INT32_MAX ||
-        (flags & ~(KDA_CHUNK_PRECISE | KDA_CHUNK_SCAN_WIDE | KDA_CHUNK_SCAN_SPLIT)) ||
+        (flags & ~(KDA_CHUNK_PRECISE | KDA_CHUNK_SCAN_WIDE | KDA_CHUNK_SCAN_SPLIT |
+                   KDA_CHUNK_GATED)) ||
         ((flags & KDA_CHUNK_SCAN_WIDE) && (flags & KDA_CHUNK_SCAN_SPLIT)))
         return KDA_ERR_INVALID_ARG;
+    flags = gate ? (flags | KDA_CHUNK_GATED) : (flags & ~KDA_CHUNK_GATED);
     if (K != kHeadDim || V != kHeadDim) return KDA_ERR_UNSUPPORTED;
-    if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
+    if (gate) {
+        if (!gate->a_log || !gate->dt_bias || !aligned(gate->dt_bias, 16) ||
+            (gate->use_lower_bound && !isfinite(gate->lower_bound)))
+            return KDA_ERR_INVALID_ARG;
+        if (total_tokens > 0 &&
+            (!gate->raw_gate || !gate->raw_beta ||
+             !aligned(gate->raw_gate, use_tensor_cores(dtype, flags) ? 16 : 4 * elem_bytes(dtype)) ||
+             !aligned(gate->raw_beta, elem_bytes(dtype))))
+            return KDA_ERR_INVALID_ARG;
+        g = nullptr;
+        beta = nullptr;
+    } else if (total_tokens > 0 && (!g || !beta)) {
+        return KDA_ERR_INVALID_ARG;
+    }
+    if (total_tokens > 0 && (!q || !k || !v || !o)) return KDA_ERR_INVALID_ARG;
     if (!cu_seqlens && total_tokens % n_seqs != 0) return KDA_ERR_INVALID_ARG;
     if (state_indices && n_slots <= 0) return KDA_ERR_INVALID_ARG;
     if (!state_indices && n_slots < 0) return KDA_ERR_INVALID_ARG;
@@ -88,8 +111,17 @@ int chunk_call(int phase, const void *q, const void *k, const void *v, const flo
     if (phase & kIntra) {
         e = launch_chunk_index(cu_seqlens, n_seqs, total_tokens, state_indices, n_slots,
                                workspace, s);
+        if (e == cudaSuccess && gate && !tc) {  // fp32 path: activate into the workspace
+            const WsGate W = ws_gate(ws_layout(total_tokens, n_seqs, H, record_bytes(dtype, flags)),
+                                     total_tokens, H);
+            float *g_act = ws_at<float>(workspace, W.g_off);
+            float *beta_act = ws_at<float>(workspace, W.beta_off);
+            e = launch_gate_activation(*gate, dtype, total_tokens, H, g_act, beta_act, s);
+            g = g_act;
+            beta = beta_act;
+        }
         if (e == cudaSuccess)
-            e = tc ? launch_chunk_prep_tc(q, k, v, g, beta, n_seqs, total_tokens, H, scale,
+            e = tc ? launch_chunk_prep_tc(q, k, v, g, beta, gate, n_seqs, total_tokens, H, scale,
                                           workspace, s)
                    : launch_chunk_prep_f32(q, k, v, g, beta, dtype, n_seqs, total_tokens, H,
                                            scale, workspace, s);
@@ -117,12 +149,26 @@ extern "C" {
         int H, int K, int V, float scale, int dtype, int flags, void *workspace,               \
         size_t workspace_bytes, void *stream
 #define KDA_CHUNK_PASS                                                                       \
-    q, k, v, g, beta, initial_state, final_state, state_indices, n_slots, o, cu_seqlens,      \
+    q, k, v, g, beta, nullptr, initial_state, final_state, state_indices, n_slots, o,         \
+        cu_seqlens,                                                                           \
         n_seqs, total_tokens, H, K, V, scale, dtype, flags, workspace, workspace_bytes, stream
 
 int kda_chunk_fwd(KDA_CHUNK_ARGS) { return chunk_call(kBoth, KDA_CHUNK_PASS); }
 int kda_chunk_intra(KDA_CHUNK_ARGS) { return chunk_call(kIntra, KDA_CHUNK_PASS); }
 int kda_chunk_scan(KDA_CHUNK_ARGS) { return chunk_call(kScan, KDA_CHUNK_PASS); }
+
+int kda_chunk_fwd_gated(const void *q, const void *k, const void *v, const void *raw_gate,
+                        const void *raw_beta, const float *a_log, const float *dt_bias,
+                        float lower_bound, int use_lower_bound, const float *initial_state,
+                        float *final_state, const int32_t *state_indices, int64_t n_slots,
+                        void *o, const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens,
+                        int H, int K, int V, float scale, int dtype, int flags, void *workspace,
+                        size_t workspace_bytes, void *stream) {
+    const GateArgs gate{raw_gate, raw_beta, a_log, dt_bias, lower_bound, use_lower_bound != 0};
+    return chunk_call(kBoth, q, k, v, nullptr, nullptr, &gate, initial_state, final_state,
+                      state_indices, n_slots, o, cu_seqlens, n_seqs, total_tokens, H, K, V, scale,
+                      dtype, flags, workspace, workspace_bytes, stream);
+}
 
 int kda_workspace_status(const void *workspace, int *flags_out, void *stream) {
     if (!workspace || !flags_out) return KDA_ERR_INVALID_ARG;
@@ -138,24 +184,36 @@ int kda_workspace_status(const void *workspace, int *flags_out, void *stream) {
     return KDA_OK;
 }
 
-int kda_recurrent_step(const void *q, const void *k, const void *v, const float *g,
-                       const float *beta, float *state_pool, const int32_t *state_indices,
-                       int64_t n_slots, void *o, int N, int H, int K, int V, float scale,
-                       int dtype, void *stream) {
+namespace {
+int step_call(const void *q, const void *k, const void *v, const float *g, const float *beta,
+              const GateArgs *gate, float *state_pool, const int32_t *state_indices,
+              int64_t n_slots, void *o, int N, int H, int K, int V, float scale, int dtype,
+              void *stream) {
     if (!valid_dtype(dtype) || N < 0 || H <= 0 || K <= 0 || V <= 0 || n_slots < 0)
         return KDA_ERR_INVALID_ARG;
     if (K != kHeadDim || V != kHeadDim) return KDA_ERR_UNSUPPORTED;
     if (N == 0) return KDA_OK;
-    if (!q || !k || !v || !g || !beta || !state_pool || !o) return KDA_ERR_INVALID_ARG;
+    if (gate) {
+        if (!gate->raw_gate || !gate->raw_beta || !gate->a_log || !gate->dt_bias ||
+            !aligned(gate->raw_gate, 4 * elem_bytes(dtype)) ||
+            !aligned(gate->raw_beta, elem_bytes(dtype)) || !aligned(gate->dt_bias, 16) ||
+            (gate->use_lower_bound && !isfinite(gate->lower_bound)))
+            return KDA_ERR_INVALID_ARG;
+        g = nullptr;
+        beta = nullptr;
+    } else if (!g || !beta || !aligned(g, 16) || !aligned(beta, 4)) {
+        return KDA_ERR_INVALID_ARG;
+    }
+    if (!q || !k || !v || !state_pool || !o) return KDA_ERR_INVALID_ARG;
     if (!state_indices && n_slots < N) return KDA_ERR_INVALID_ARG;
     if ((int64_t)N * H > INT32_MAX) return KDA_ERR_INVALID_ARG;
     const size_t ea = 4 * elem_bytes(dtype);
     if (!aligned(q, ea) || !aligned(k, ea) || !aligned(v, ea) || !aligned(o, elem_bytes(dtype)) ||
-        !aligned(g, 16) || !aligned(beta, 4) || !aligned(state_pool, 16))
+        !aligned(state_pool, 16))
         return KDA_ERR_INVALID_ARG;
     if (!isfinite(scale)) return KDA_ERR_INVALID_ARG;
     cudaGetLastError();
-    const cudaError_t e = launch_recurrent_step(q, k, v, g, beta, state_pool, state_indices,
+    const cudaError_t e = launch_recurrent_step(q, k, v, g, beta, gate, state_pool, state_indices,
                                                 n_slots, o, N, H, scale, dtype,
                                                 (cudaStream_t)stream);
     if (e != cudaSuccess) {
@@ -163,6 +221,25 @@ int kda_recurrent_step(const void *q, const void *k, const void *v, const float 
         return KDA_ERR_CUDA;
     }
     return KDA_OK;
+}
+}  // namespace
+
+int kda_recurrent_step(const void *q, const void *k, const void *v, const float *g,
+                       const float *beta, float *state_pool, const int32_t *state_indices,
+                       int64_t n_slots, void *o, int N, int H, int K, int V, float scale,
+                       int dtype, void *stream) {
+    return step_call(q, k, v, g, beta, nullptr, state_pool, state_indices, n_slots, o, N, H, K,
+                     V, scale, dtype, stream);
+}
+
+int kda_recurrent_step_gated(const void *q, const void *k, const void *v, const void *raw_gate,
+                             const void *raw_beta, const float *a_log, const float *dt_bias,
+                             float lower_bound, int use_lower_bound, float *state_pool,
+                             const int32_t *state_indices, int64_t n_slots, void *o, int N,
+                             int H, int K, int V, float scale, int dtype, void *stream) {
+    const GateArgs gate{raw_gate, raw_beta, a_log, dt_bias, lower_bound, use_lower_bound != 0};
+    return step_call(q, k, v, nullptr, nullptr, &gate, state_pool, state_indices, n_slots, o, N,
+                     H, K, V, scale, dtype, stream);
 }
 
 }  // extern "C"

@@ -87,6 +87,17 @@ __device__ __forceinline__ void unpack8(uint4 raw, float (&x)[8]) {
     }
 }
 
+// The model's gate (see gate_decay) with the SFU exponential, logarithm and
+// reciprocal (a few ulp, far below the bf16 operands of this path); log1p of
+// a small argument by its series, where 1 + e would round the argument away.
+__device__ __forceinline__ float gate_decay_fast(float x, float gscale, float lower_bound,
+                                                 bool use_lower_bound) {
+    if (use_lower_bound) return __fdividef(lower_bound, 1.0f + __expf(-gscale * x));
+    const float e = __expf(-fabsf(x));  // in (0, 1]
+    const float l1p = e < 1e-3f ? e * (1.0f - 0.5f * e) : __logf(1.0f + e);
+    return -gscale * (fmaxf(x, 0.0f) + l1p);
+}
+
 // ---------------------------------------------------------------------------
 // prep
 // ---------------------------------------------------------------------------
@@ -159,9 +170,10 @@ struct RawMaps {
     CUtensorMap q, k, v, g;
 };
 
+// g_bytes: 32 KB for an fp32 g tile, 16 KB for a raw bf16 gate tile
 __device__ __forceinline__ void load_qkg(unsigned char *buf, const RawMaps &m, int h, int64_t tok0,
-                                         uint64_t *bar) {
-    mbar_arrive_expect_tx(bar, 16384u + 16384u + 32768u);
+                                         uint64_t *bar, uint32_t g_bytes) {
+    mbar_arrive_expect_tx(bar, 16384u + 16384u + g_bytes);
     tma_load_3d(buf + R_Q, &m.q, 0, h, (int)tok0, bar);
     tma_load_3d(buf + R_K, &m.k, 0, h, (int)tok0, bar);
     tma_load_3d(buf + R_G, &m.g, 0, h, (int)tok0, bar);
@@ -226,9 +238,19 @@ __device__ __forceinline__ float4 mm16_row4(const float *A, int lda, const float
     return row4_times(a, B, c4, ldb);
 }
 
+// GATED: maps.g covers the model's raw bf16 gate and beta is unused; the
+// gate (GateArgs) is activated on chip.  Otherwise g and beta are activated.
+template <bool GATED>
 __global__ void __launch_bounds__(kPrepThreads, 1)
     chunk_prep_tc_kernel(const __grid_constant__ RawMaps maps, const float *__restrict__ beta,
-                         int n_seqs, int H, float scale, void *workspace, WsLayout L) {
+                         const GateArgs gate, int n_seqs, int H, float scale, void *workspace,
+                         WsLayout L) {
+    constexpr uint32_t kGBytes = GATED ? 16384u : 32768u;
+    auto beta_of = [&](int64_t tok, int hh) {
+        return GATED ? gate_beta(__bfloat162float(
+                           reinterpret_cast<const __nv_bfloat16 *>(gate.raw_beta)[tok * H + hh]))
+                     : beta[tok * H + hh];
+    };
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     unsigned char *sXL = sm + P_XL;
@@ -278,10 +300,16 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     int item = blockIdx.x;
     PrepItem cur = prep_item(item, H, chunk_off, seq_start, seq_len, n_seqs);
     if (tid == kLoader) {
-        load_qkg(sm, maps, cur.h, cur.tok0, full);
+        load_qkg(sm, maps, cur.h, cur.tok0, full, kGBytes);
         load_v(sm, maps, cur.h, cur.tok0, vfull);
     }
-    float beta_cur = tid < cur.valid ? beta[(cur.tok0 + tid) * H + cur.h] : 0.0f;
+    float beta_cur = tid < cur.valid ? beta_of(cur.tok0 + tid, cur.h) : 0.0f;
+    // gate parameters of this thread's key channel (tid % 128) for the current
+    // item's head, fetched one item ahead like beta (A_log raw: its exponential
+    // is taken where it is used, so the load's latency stalls nothing)
+    auto gate_bias = [&](int hh) { return GATED ? gate.dt_bias[hh * D + (tid & (D - 1))] : 0.0f; };
+    auto gate_alog = [&](int hh) { return GATED ? gate.a_log[hh] : 0.0f; };
+    float bias_cur = gate_bias(cur.h), alog_cur = gate_alog(cur.h);
     PrepItem nxt = cur;
     if (item + (int)gridDim.x < n_items)
         nxt = prep_item(item + gridDim.x, H, chunk_off, seq_start, seq_len, n_seqs);
@@ -297,7 +325,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         unsigned char *rec = ws_at<unsigned char>(workspace, L.records_off + ((size_t)cur.c * H + cur.h) * TcRec::bytes);
         const int valid = cur.valid;
         if (tid < C) sB[tid] = tid < valid ? beta_cur : 0.0f;
-        float beta_nxt = 0.0f;
+        float beta_nxt = 0.0f, bias_nxt = 0.0f, alog_nxt = 0.0f;
 
         if (mbar_wait(full, fphase)) {
             fphase ^= 1;
@@ -311,8 +339,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             const uint4 z = make_uint4(0, 0, 0, 0);
             *reinterpret_cast<uint4 *>(sm + R_Q + r * 256 + c16 * 16) = z;
             *reinterpret_cast<uint4 *>(sm + R_K + r * 256 + c16 * 16) = z;
-            *reinterpret_cast<uint4 *>(sm + R_G + r * 512 + c16 * 32) = z;
-            *reinterpret_cast<uint4 *>(sm + R_G + r * 512 + c16 * 32 + 16) = z;
+            if (!GATED) {  // a raw gate tile is masked row by row on activation instead
+                *reinterpret_cast<uint4 *>(sm + R_G + r * 512 + c16 * 32) = z;
+                *reinterpret_cast<uint4 *>(sm + R_G + r * 512 + c16 * 32 + 16) = z;
+            }
         }
         if (!__syncthreads_and(ok)) {
             ok = false;  // uniform from here on: every thread takes the exit path
@@ -328,17 +358,27 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         {
             const int d = tid & (D - 1), qtr = tid >> 7, r0 = 16 * qtr;
             float x[16];
+            if (GATED) {  // the model's gate: x = raw + dt_bias, through softplus or sigmoid
+                const __nv_bfloat16 *raw = reinterpret_cast<const __nv_bfloat16 *>(sm + R_G);
+                const float bias = bias_cur, gs = __expf(alog_cur);
+                const bool lb = gate.use_lower_bound != 0;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] = sG[(r0 + i) * D + d];  // g, plain layout
+                for (int i = 0; i < 16; ++i)
+                    x[i] = r0 + i < valid ? gate_decay_fast(__bfloat162float(raw[(r0 + i) * D + d]) + bias,
+                                                            gs, gate.lower_bound, lb)
+                                          : 0.0f;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) x[i] = sG[(r0 + i) * D + d];  // g, plain layout
+            }
 #pragma unroll
             for (int i = 1; i < 16; ++i) x[i] += x[i - 1];
             sQsum[qtr * D + d] = x[15];
             sFirst[qtr * D + d] = x[0];
-            const int ds = swz(d);  // a lane of this warp: its column was read above
-            __syncwarp();
+            const int ds = swz(d);
+            __syncthreads();  // every g (or raw gate) value is read: sG is overwritten below
 #pragma unroll
             for (int i = 0; i < 16; ++i) sG[(r0 + i) * D + ds] = x[i] - x[0];
-            __syncthreads();
             float off = 0.0f, gl = 0.0f, gfirst[3];  // gfirst[b] = G_16b, b < qtr
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
@@ -459,7 +499,11 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         // item after it, fetched by one thread of a warp that does no TMEM
         // readout (its dependent loads stall only that warp) and handed over
         // in shared memory
-        if (has_next && tid < nxt.valid) beta_nxt = beta[(nxt.tok0 + tid) * H + nxt.h];
+        if (has_next && tid < nxt.valid) beta_nxt = beta_of(nxt.tok0 + tid, nxt.h);
+        if (GATED && has_next) {
+            bias_nxt = gate_bias(nxt.h);
+            alog_nxt = gate_alog(nxt.h);
+        }
         if (tid == kPrepThreads - 32 && item + 2 * (int)gridDim.x < n_items)
             *sNext = prep_item(item + 2 * gridDim.x, H, chunk_off, seq_start, seq_len, n_seqs);
 
@@ -500,7 +544,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             break;
         }
         // the q, k and g tiles are consumed: the next item's loads go out now
-        if (tid == kLoader && has_next) load_qkg(sm, maps, nxt.h, nxt.tok0, full);
+        if (tid == kLoader && has_next) load_qkg(sm, maps, nxt.h, nxt.tok0, full, kGBytes);
         fpend = has_next;
         KDA_PHASE(0, 4);
 
@@ -784,6 +828,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         cur = nxt;
         if (item + 2 * (int)gridDim.x < n_items) nxt = *sNext;
         beta_cur = beta_nxt;
+        bias_cur = bias_nxt;
+        alog_cur = alog_nxt;
     }
     if (tid == kLoader) bulk_wait_all();  // the last record's W and U are written
     if (!ok) {
@@ -1317,8 +1363,9 @@ bool encode_rows(CUtensorMap *m, const void *base, CUtensorMapDataType dt, size_
 }  // namespace
 
 cudaError_t launch_chunk_prep_tc(const void *q, const void *k, const void *v, const float *g,
-                                 const float *beta, int n_seqs, int64_t total_tokens, int H,
-                                 float scale, void *workspace, cudaStream_t stream) {
+                                 const float *beta, const GateArgs *gate, int n_seqs,
+                                 int64_t total_tokens, int H, float scale, void *workspace,
+                                 cudaStream_t stream) {
     const WsLayout L = ws_layout(total_tokens, n_seqs, H, TcRec::bytes);
     const int64_t items_max = max_chunks(total_tokens, n_seqs) * (int64_t)H;
     const int grid = (int)std::min<int64_t>(items_max, (int64_t)sm_count());
@@ -1328,12 +1375,25 @@ cudaError_t launch_chunk_prep_tc(const void *q, const void *k, const void *v, co
         if (!encode_rows(&maps.q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, total_tokens) ||
             !encode_rows(&maps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, total_tokens) ||
             !encode_rows(&maps.v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, total_tokens, true) ||
-            !encode_rows(&maps.g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, total_tokens))
+            !(gate ? encode_rows(&maps.g, gate->raw_gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H,
+                                 total_tokens)
+                   : encode_rows(&maps.g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, total_tokens)))
             return cudaErrorInvalidValue;
     }
-    cudaFuncSetAttribute(chunk_prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
-    chunk_prep_tc_kernel<<<grid, kPrepThreads, P_SMEM, stream>>>(maps, beta, n_seqs, H, scale,
-                                                                  workspace, L);
+    GateArgs ga;
+    memset(&ga, 0, sizeof(ga));
+    if (gate) {
+        ga = *gate;
+        cudaFuncSetAttribute(chunk_prep_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             P_SMEM);
+        chunk_prep_tc_kernel<true><<<grid, kPrepThreads, P_SMEM, stream>>>(maps, beta, ga, n_seqs, H,
+                                                                           scale, workspace, L);
+    } else {
+        cudaFuncSetAttribute(chunk_prep_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             P_SMEM);
+        chunk_prep_tc_kernel<false><<<grid, kPrepThreads, P_SMEM, stream>>>(maps, beta, ga, n_seqs, H,
+                                                                            scale, workspace, L);
+    }
     return cudaGetLastError();
 }
 

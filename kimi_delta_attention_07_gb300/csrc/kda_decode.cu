@@ -15,7 +15,10 @@
 // whole 512-byte rows, a lane holds 4 consecutive key channels (one 128-bit
 // load and one 128-bit store per lane per row), and the two dot products are
 // warp-shuffle reductions.  Rows of one head are split over CTAs when there
-// are too few (sequence, head) pairs to fill the GPU.
+// are too few (sequence, head) pairs to fill the GPU.  The gated variant
+// activates the model's raw gate and beta on the way in (see GateArgs).
+#include <string.h>
+
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -25,13 +28,14 @@ constexpr int kDecodeThreads = 256;  // 8 warps
 constexpr int kWarps = kDecodeThreads / 32;
 constexpr int kMaxRowsPerWarp = kHeadDim / kWarps;  // 16: a whole head per CTA
 
-template <typename T>
+template <typename T, bool GATED>
 __global__ void __launch_bounds__(kDecodeThreads)
     recurrent_step_kernel(const T *__restrict__ q, const T *__restrict__ k,
                           const T *__restrict__ v, const float *__restrict__ g,
-                          const float *__restrict__ beta, float *__restrict__ pool,
-                          const int32_t *__restrict__ state_indices, int64_t n_slots,
-                          T *__restrict__ o, int H, int rows_per_cta, float scale) {
+                          const float *__restrict__ beta, const GateArgs gate,
+                          float *__restrict__ pool, const int32_t *__restrict__ state_indices,
+                          int64_t n_slots, T *__restrict__ o, int H, int rows_per_cta,
+                          float scale) {
     const int pair = blockIdx.x;  // n * H + h
     const int n = pair / H;
     const int h = pair - n * H;
@@ -63,7 +67,22 @@ __global__ void __launch_bounds__(kDecodeThreads)
     // L2 norms of q and k over the key dim (eps inside the root), scale on q.
     const float4 q4 = load4(q + io_k + 4 * lane);
     const float4 k4 = load4(k + io_k + 4 * lane);
-    const float4 g4 = load4(g + io_k + 4 * lane);
+    float4 g4;
+    float b;
+    if (GATED) {
+        const float4 r4 = load4(reinterpret_cast<const T *>(gate.raw_gate) + io_k + 4 * lane);
+        const float4 c4 = load4(gate.dt_bias + (int64_t)h * kHeadDim + 4 * lane);
+        const float gs = expf(gate.a_log[h]);
+        const bool lb = gate.use_lower_bound != 0;
+        g4 = make_float4(gate_decay(r4.x + c4.x, gs, gate.lower_bound, lb),
+                         gate_decay(r4.y + c4.y, gs, gate.lower_bound, lb),
+                         gate_decay(r4.z + c4.z, gs, gate.lower_bound, lb),
+                         gate_decay(r4.w + c4.w, gs, gate.lower_bound, lb));
+        b = gate_beta(to_f32(reinterpret_cast<const T *>(gate.raw_beta)[pair]));
+    } else {
+        g4 = load4(g + io_k + 4 * lane);
+        b = beta[pair];
+    }
     const float sq = warp_sum(q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w);
     const float sk = warp_sum(k4.x * k4.x + k4.y * k4.y + k4.z * k4.z + k4.w * k4.w);
     const float rq = scale / sqrtf(sq + 1e-6f);
@@ -72,7 +91,6 @@ __global__ void __launch_bounds__(kDecodeThreads)
     const float4 kh = make_float4(k4.x * rk, k4.y * rk, k4.z * rk, k4.w * rk);
     const float4 dec = make_float4(expf(g4.x), expf(g4.y), expf(g4.z), expf(g4.w));
     const float kq = warp_sum(kh.x * qh.x + kh.y * qh.y + kh.z * qh.z + kh.w * qh.w);
-    const float b = beta[pair];
 
 #pragma unroll
     for (int j = 0; j < kMaxRowsPerWarp; ++j) {
@@ -96,25 +114,40 @@ __global__ void __launch_bounds__(kDecodeThreads)
 
 }  // namespace
 
+template <typename T>
+void launch_step(bool gated, dim3 grid, const void *q, const void *k, const void *v,
+                 const float *g, const float *beta, const GateArgs &gate, float *pool,
+                 const int32_t *state_indices, int64_t n_slots, void *o, int H, int rows,
+                 float scale, cudaStream_t stream) {
+    if (gated)
+        recurrent_step_kernel<T, true><<<grid, kDecodeThreads, 0, stream>>>(
+            (const T *)q, (const T *)k, (const T *)v, g, beta, gate, pool, state_indices,
+            n_slots, (T *)o, H, rows, scale);
+    else
+        recurrent_step_kernel<T, false><<<grid, kDecodeThreads, 0, stream>>>(
+            (const T *)q, (const T *)k, (const T *)v, g, beta, gate, pool, state_indices,
+            n_slots, (T *)o, H, rows, scale);
+}
+
 cudaError_t launch_recurrent_step(const void *q, const void *k, const void *v, const float *g,
-                                  const float *beta, float *pool, const int32_t *state_indices,
-                                  int64_t n_slots, void *o, int N, int H, float scale, int dtype,
-                                  cudaStream_t stream) {
+                                  const float *beta, const GateArgs *gate, float *pool,
+                                  const int32_t *state_indices, int64_t n_slots, void *o, int N,
+                                  int H, float scale, int dtype, cudaStream_t stream) {
     const int64_t pairs = (int64_t)N * H;
     // Split a head's 128 rows over more CTAs when there are few heads in flight,
     // so that at least ~4 CTAs per SM are resident.
     int rows = kHeadDim;  // a multiple of 8 warps, at most 16 rows per warp
     while (rows > 16 && pairs * (kHeadDim / rows) < 152 * 8) rows >>= 1;
     const dim3 grid((unsigned)pairs, kHeadDim / rows);
-    if (dtype == KDA_BF16) {
-        recurrent_step_kernel<__nv_bfloat16><<<grid, kDecodeThreads, 0, stream>>>(
-            (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, g,
-            beta, pool, state_indices, n_slots, (__nv_bfloat16 *)o, H, rows, scale);
-    } else {
-        recurrent_step_kernel<float><<<grid, kDecodeThreads, 0, stream>>>(
-            (const float *)q, (const float *)k, (const float *)v, g, beta, pool, state_indices,
-            n_slots, (float *)o, H, rows, scale);
-    }
+    GateArgs ga;
+    memset(&ga, 0, sizeof(ga));
+    if (gate) ga = *gate;
+    if (dtype == KDA_BF16)
+        launch_step<__nv_bfloat16>(gate != nullptr, grid, q, k, v, g, beta, ga, pool,
+                                   state_indices, n_slots, o, H, rows, scale, stream);
+    else
+        launch_step<float>(gate != nullptr, grid, q, k, v, g, beta, ga, pool, state_indices,
+                           n_slots, o, H, rows, scale, stream);
     return cudaGetLastError();
 }
 

@@ -123,6 +123,39 @@ struct TcRec {
 };
 static_assert(TcRec::U + 4 * TcRec::UBLK <= TcRec::bytes, "TcRec layout");
 
+// ---- gate activation (the model's gate, computed in-kernel) ----------------
+// x = raw_gate + dt_bias[h][k];  g = lower_bound * sigmoid(exp(a_log[h]) x)
+// with a lower bound, else -exp(a_log[h]) softplus(x);  beta = sigmoid(raw_beta).
+struct GateArgs {
+    const void *raw_gate;  // [T, H, K] in the q dtype
+    const void *raw_beta;  // [T, H] in the q dtype
+    const float *a_log;    // [H]
+    const float *dt_bias;  // [H, K]
+    float lower_bound;
+    int use_lower_bound;
+};
+
+// g from x = raw + bias, with gscale = exp(a_log[h])
+__device__ __forceinline__ float gate_decay(float x, float gscale, float lower_bound,
+                                            bool use_lower_bound) {
+    if (use_lower_bound) return lower_bound / (1.0f + expf(-gscale * x));
+    return -gscale * (fmaxf(x, 0.0f) + log1pf(expf(-fabsf(x))));
+}
+__device__ __forceinline__ float gate_beta(float raw) { return 1.0f / (1.0f + expf(-raw)); }
+
+// Workspace of a gated call on the fp32 path: activated g [T, H, K] and beta
+// [T, H] (fp32) after the records.
+struct WsGate {
+    size_t g_off, beta_off, total;
+};
+__host__ __device__ inline WsGate ws_gate(const WsLayout &L, int64_t total_tokens, int H) {
+    WsGate W;
+    W.g_off = align_up(L.total, 256);
+    W.beta_off = align_up(W.g_off + (size_t)total_tokens * H * kHeadDim * sizeof(float), 256);
+    W.total = W.beta_off + (size_t)total_tokens * H * sizeof(float);
+    return W;
+}
+
 // ---- launchers (return cudaGetLastError() of the launch) ------------------
 
 cudaError_t launch_chunk_index(const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens,
@@ -138,9 +171,16 @@ cudaError_t launch_chunk_scan_f32(const float *initial_state, float *final_state
                                   int64_t total_tokens, int H, void *workspace,
                                   cudaStream_t stream);
 
+// gate == nullptr: g, beta are activated fp32; otherwise g, beta are unused
+// and the raw gates of *gate are activated on chip.
 cudaError_t launch_chunk_prep_tc(const void *q, const void *k, const void *v, const float *g,
-                                 const float *beta, int n_seqs, int64_t total_tokens, int H,
-                                 float scale, void *workspace, cudaStream_t stream);
+                                 const float *beta, const GateArgs *gate, int n_seqs,
+                                 int64_t total_tokens, int H, float scale, void *workspace,
+                                 cudaStream_t stream);
+
+// Activated g and beta of a gated call into fp32 buffers (the fp32 path).
+cudaError_t launch_gate_activation(const GateArgs &gate, int dtype, int64_t total_tokens, int H,
+                                   float *g_out, float *beta_out, cudaStream_t stream);
 
 cudaError_t launch_chunk_scan_tc(const float *initial_state, float *final_state,
                                  const int32_t *state_indices, void *o, int n_seqs,
@@ -158,9 +198,10 @@ __device__ __forceinline__ int owner_of_chunk(const int32_t *chunk_off, int n_se
     return lo;
 }
 
+// gate == nullptr: g, beta are activated fp32; otherwise raw gates (*gate).
 cudaError_t launch_recurrent_step(const void *q, const void *k, const void *v, const float *g,
-                                  const float *beta, float *pool, const int32_t *state_indices,
-                                  int64_t n_slots, void *o, int N, int H, float scale, int dtype,
-                                  cudaStream_t stream);
+                                  const float *beta, const GateArgs *gate, float *pool,
+                                  const int32_t *state_indices, int64_t n_slots, void *o, int N,
+                                  int H, float scale, int dtype, cudaStream_t stream);
 
 }  // namespace kda

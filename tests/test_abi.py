@@ -32,7 +32,8 @@ def lib():
 def test_header_declares_the_entry_points():
     names = _declared_functions()
     for n in ("kda_chunk_fwd", "kda_chunk_intra", "kda_chunk_scan", "kda_recurrent_step", "kda_chunk_workspace_bytes",
-              "kda_workspace_status", "kda_status_string", "kda_version"):
+              "kda_workspace_status", "kda_status_string", "kda_version", "kda_chunk_fwd_gated",
+              "kda_recurrent_step_gated"):
         assert n in names
 
 
@@ -84,7 +85,7 @@ def test_chunk_fwd_rejects_bad_arguments_without_launching(lib):
     assert _chunk(lib, **{**ok, "N": 0}) == kda.KDA_ERR_INVALID_ARG
     assert _chunk(lib, **{**ok, "T": -1}) == kda.KDA_ERR_INVALID_ARG
     assert _chunk(lib, **{**ok, "N": 3, "T": 64}) == kda.KDA_ERR_INVALID_ARG  # 3 does not divide 64
-    assert _chunk(lib, **{**ok, "flags": 8}) == kda.KDA_ERR_INVALID_ARG
+    assert _chunk(lib, **{**ok, "flags": 16}) == kda.KDA_ERR_INVALID_ARG
     assert _chunk(lib, **{**ok, "flags": kda.KDA_CHUNK_SCAN_WIDE | kda.KDA_CHUNK_SCAN_SPLIT}) == kda.KDA_ERR_INVALID_ARG
     assert _chunk(lib, **{**ok, "q": base + 2}) == kda.KDA_ERR_INVALID_ARG   # misaligned row
     assert _chunk(lib, **{**ok, "ws": None}) == kda.KDA_ERR_WORKSPACE
@@ -92,6 +93,47 @@ def test_chunk_fwd_rejects_bad_arguments_without_launching(lib):
     assert _chunk(lib, **{**ok, "wsb": 1024}) == kda.KDA_ERR_WORKSPACE
     assert _chunk(lib, **{**ok, "idx": base, "slots": 0}) == kda.KDA_ERR_INVALID_ARG
     assert _chunk(lib, **{**ok, "scale": float("nan")}) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_gated_entry_points_reject_bad_arguments_without_launching(lib):
+    base = 1 << 20
+    vp = ctypes.c_void_p
+    p = lambda x: None if x is None else vp(x)
+
+    def chunk(**kw):
+        a = dict(q=base, k=base, v=base, rg=base, rb=base, alog=base, bias=base, lb=-5.0, use_lb=1,
+                 o=base, N=1, T=64, H=1, dt=kda.KDA_BF16, flags=0, ws=base, wsb=1 << 30)
+        a.update(kw)
+        return lib.kda_chunk_fwd_gated(p(a["q"]), p(a["k"]), p(a["v"]), p(a["rg"]), p(a["rb"]),
+                                       p(a["alog"]), p(a["bias"]), a["lb"], a["use_lb"], None, None,
+                                       None, 0, p(a["o"]), None, a["N"], a["T"], a["H"], 128, 128,
+                                       0.1, a["dt"], a["flags"], p(a["ws"]), a["wsb"], None)
+
+    def step(**kw):
+        a = dict(q=base, k=base, v=base, rg=base, rb=base, alog=base, bias=base, lb=-5.0, use_lb=1,
+                 pool=base, o=base, N=2, H=2, dt=kda.KDA_F32)
+        a.update(kw)
+        return lib.kda_recurrent_step_gated(p(a["q"]), p(a["k"]), p(a["v"]), p(a["rg"]), p(a["rb"]),
+                                            p(a["alog"]), p(a["bias"]), a["lb"], a["use_lb"],
+                                            p(a["pool"]), None, 4, p(a["o"]), a["N"], a["H"], 128,
+                                            128, 0.1, a["dt"], None)
+
+    for f in (chunk, step):
+        assert f(alog=None) == kda.KDA_ERR_INVALID_ARG
+        assert f(bias=None) == kda.KDA_ERR_INVALID_ARG
+        assert f(bias=base + 4) == kda.KDA_ERR_INVALID_ARG      # dt_bias rows: 16-byte aligned
+        assert f(rg=None) == kda.KDA_ERR_INVALID_ARG
+        assert f(rb=None) == kda.KDA_ERR_INVALID_ARG
+        assert f(lb=float("nan")) == kda.KDA_ERR_INVALID_ARG    # a lower bound must be finite
+        assert f(dt=4) == kda.KDA_ERR_INVALID_ARG
+    assert chunk(rg=base + 8) == kda.KDA_ERR_INVALID_ARG        # tensor-core path: 16-byte rows
+    assert chunk(ws=None) == kda.KDA_ERR_WORKSPACE
+    # the fp32 path keeps the activated gate in the workspace: it needs more room
+    f32 = kda.kda_chunk_workspace_bytes(4096, 1, 32, dtype=kda.KDA_F32)
+    f32_gated = kda.kda_chunk_workspace_bytes(4096, 1, 32, dtype=kda.KDA_F32, flags=kda.KDA_CHUNK_GATED)
+    assert f32_gated >= f32 + 4096 * 32 * (128 + 1) * 4
+    assert (kda.kda_chunk_workspace_bytes(4096, 1, 32, flags=kda.KDA_CHUNK_GATED)
+            == kda.kda_chunk_workspace_bytes(4096, 1, 32))          # tensor-core path: on chip
 
 
 def test_recurrent_step_rejects_bad_arguments_without_launching(lib):

@@ -379,3 +379,100 @@ def test_long_131k_prefill_handoff_then_256_decode_steps(kda):
         if t in (0, 255):
             assert rel_l2(to_np(o2[:, [head]]), o2_ref) < TOL_BF16
     assert rel_l2(vk_to_kv(pool[1, [head]]), ref[0]) < TOL_BF16
+
+
+# ---------------------------------------------------------------------------
+# gated entry points: the model's raw gates activated in-kernel
+# ---------------------------------------------------------------------------
+
+# lower-bounded gate (decays in (-5, 0)) and softplus gate with moderate decays
+GATES = {"lower_bound": dict(lower_bound=-5.0),
+         "softplus": dict(lower_bound=None, a_range=(1.0, 4.0), bias_range=(-6.0, -4.0))}
+
+
+def _gated(x, seed, gate):
+    kw = dict(GATES[gate])
+    lb = kw.pop("lower_bound")
+    y = kda_inputs.with_raw_gates(x, seed=seed, lower_bound=lb, **kw)
+    g_ref, b_ref = oracle.gate_activation(y["raw_gate"], y["raw_beta"], y["a_log"], y["dt_bias"],
+                                          lower_bound=lb)
+    return y, g_ref, b_ref
+
+
+@pytest.mark.parametrize("gate", list(GATES))
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_gated_step_matches_oracle(kda, dtype, gate):
+    H, slots = 3, 6
+    tok = kda_inputs.decode_tokens(4, H=H, dtype=dtype, seed=51)
+    y, g_ref, b_ref = _gated(tok, 51, gate)
+    pool = kda_inputs.decode_pool(slots, H=H, seed=51)
+    idx = torch.tensor([5, 2, 0, 3], dtype=torch.int32)
+    pool_d = pool.cuda()
+    o = kda.kda_recurrent_step_gated(*(y[n].cuda() for n in ("q", "k", "v", "raw_gate", "raw_beta",
+                                                              "a_log", "dt_bias")),
+                                     pool_d, lower_bound=y["lower_bound"], state_indices=idx.cuda())
+    torch.cuda.synchronize()
+    o_ref, pool_ref = oracle.step(y["q"], y["k"], y["v"], g_ref, b_ref,
+                                  np.swapaxes(pool.double().numpy(), -1, -2), state_indices=idx.numpy())
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    assert rel_l2(to_np(o), o_ref) < tol
+    assert rel_l2(vk_to_kv(pool_d), pool_ref) < TOL_F32
+
+
+@pytest.mark.parametrize("gate", list(GATES))
+@pytest.mark.parametrize("dtype,precise,scan", [(torch.bfloat16, False, "split"),
+                                                (torch.bfloat16, False, "wide"),
+                                                (torch.bfloat16, True, "auto"),
+                                                (torch.float32, False, "auto")])
+def test_gated_chunk_matches_oracle(kda, dtype, precise, scan, gate):
+    x = kda_inputs.prefill([190, 64, 0, 77], H=3, dtype=dtype, seed=52, init_std=0.02)
+    y, g_ref, b_ref = _gated(x, 52, gate)
+    d = dev(y, names=("q", "k", "v", "raw_gate", "raw_beta", "a_log", "dt_bias", "cu_seqlens",
+                      "initial_state"))
+    o, sf = kda.kda_chunk_fwd_gated(d["q"], d["k"], d["v"], d["raw_gate"], d["raw_beta"], d["a_log"],
+                                    d["dt_bias"], lower_bound=y["lower_bound"],
+                                    cu_seqlens=d["cu_seqlens"], initial_state=d["initial_state"],
+                                    precise=precise, scan=scan)
+    torch.cuda.synchronize()
+    s0 = np.swapaxes(y["initial_state"].double().numpy(), -1, -2)
+    o_ref, s_ref = oracle.recurrence(y["q"], y["k"], y["v"], g_ref, b_ref,
+                                     cu_seqlens=y["cu_seqlens"].numpy(), initial_state=s0)
+    tol_o = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    tol_s = TOL_F32 if (dtype == torch.float32 or precise) else TOL_BF16
+    assert rel_l2(to_np(o), o_ref) < tol_o
+    assert rel_l2(vk_to_kv(sf), s_ref) < tol_s
+
+
+def test_gated_chunk_equals_the_explicitly_activated_call(kda):
+    """fp32 inputs: the gated forward and kda_chunk_fwd fed the activation
+    (the oracle's, rounded to fp32) differ only by the activation's rounding."""
+    x = kda_inputs.prefill([150, 45], H=2, dtype=torch.float32, seed=53)
+    y, g_ref, b_ref = _gated(x, 53, "lower_bound")
+    d = dev(y, names=("q", "k", "v", "raw_gate", "raw_beta", "a_log", "dt_bias", "cu_seqlens"))
+    o1, s1 = kda.kda_chunk_fwd_gated(d["q"], d["k"], d["v"], d["raw_gate"], d["raw_beta"], d["a_log"],
+                                     d["dt_bias"], lower_bound=y["lower_bound"],
+                                     cu_seqlens=d["cu_seqlens"])
+    g = torch.from_numpy(g_ref).float().cuda()
+    b = torch.from_numpy(b_ref).float().cuda()
+    o2, s2 = kda.kda_chunk_fwd(d["q"], d["k"], d["v"], g, b, cu_seqlens=d["cu_seqlens"])
+    torch.cuda.synchronize()
+    assert rel_l2(to_np(o1), to_np(o2)) < 1e-5
+    assert rel_l2(to_np(s1), to_np(s2)) < 1e-5
+
+
+def test_gated_prefill_4k_full_size_sampled_heads(kda):
+    """The bench's gated workload (raw bf16 gates, lower bound -5) at full size."""
+    y = kda_inputs.prefill_4k_gated()
+    d = dev(y, names=("q", "k", "v", "raw_gate", "raw_beta", "a_log", "dt_bias", "cu_seqlens"))
+    o, sf = kda.kda_chunk_fwd_gated(d["q"], d["k"], d["v"], d["raw_gate"], d["raw_beta"], d["a_log"],
+                                    d["dt_bias"], lower_bound=y["lower_bound"],
+                                    cu_seqlens=d["cu_seqlens"])
+    torch.cuda.synchronize()
+    heads = [2, 29]
+    g_ref, b_ref = oracle.gate_activation(y["raw_gate"][:, heads], y["raw_beta"][:, heads],
+                                          y["a_log"][heads], y["dt_bias"][heads], y["lower_bound"])
+    o_ref, s_ref = oracle.recurrence(y["q"][:, heads], y["k"][:, heads], y["v"][:, heads], g_ref,
+                                     b_ref, cu_seqlens=y["cu_seqlens"].numpy())
+    assert rel_l2(to_np(o[:, heads]), o_ref) < TOL_BF16
+    assert rel_l2(vk_to_kv(sf[:, heads]), s_ref) < TOL_BF16
+    assert torch.isfinite(o).all()
