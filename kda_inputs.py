@@ -27,6 +27,8 @@ Gated variants (the model's raw gates; the library activates them in-kernel):
   (the lower-bounded "safe" gate keeps every decay in (lower_bound, 0)).
   prefill_4k_gated  prefill_4k's q/k/v with raw gates, A_log = log U[1, 16],
                     dt_bias ~ U[-1, 1], lower bound -5                       [5]
+Output epilogue inputs: out_gate [T, H, V] ~ N(0, 1) in the q dtype, o_norm
+weight [V] ~ U[0.5, 1.5] fp32, eps 1e-5.
 """
 from __future__ import annotations
 
@@ -135,6 +137,17 @@ def with_raw_gates(x, seed=5, dtype=None, a_range=(1.0, 16.0), bias_range=(-1.0,
     H, K = x["g"].shape[-2], x["g"].shape[-1]
     y["a_log"], y["dt_bias"] = gate_params(H, K, seed, a_range, bias_range)
     y["lower_bound"] = lower_bound
+    return y
+
+
+def with_output_gate(x, seed=6, dtype=None, eps=1e-5):
+    """Add the output epilogue's inputs: out_gate like v, o_norm weight [V], eps."""
+    dtype = x["q"].dtype if dtype is None else dtype
+    gen = _gen(seed * 17 + 5)
+    y = dict(x)
+    y["out_gate"] = _normal(tuple(x["v"].shape), gen, dtype=dtype)
+    y["norm_weight"] = _uniform((x["v"].shape[-1],), gen, 0.5, 1.5)
+    y["norm_eps"] = eps
     return y
 
 

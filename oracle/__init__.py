@@ -25,6 +25,9 @@ softplus; raw beta through a sigmoid), as written in the Ascend model file's
 in-kernel and are compared against ``gate_activation`` followed by the
 recurrence.
 
+``output_gate_norm`` is the model's output epilogue (RMSNorm over the value
+dim, its weight, times sigmoid of the output gate; ``_project_out``).
+
 ``step`` is one decode token of the recurrence on rows of a state pool picked
 by slot indices (the model file's ``_decode_gdr`` / ``_decode_fused_kda``
 semantics: the pool is updated in place).
@@ -251,3 +254,17 @@ def gate_activation(raw_gate, raw_beta, a_log, dt_bias, lower_bound=None):
         g = float(lower_bound) * _sigmoid(scale * x)
     return g, _sigmoid(_f64(raw_beta))
 
+
+
+def output_gate_norm(o, gate, weight, eps):
+    """The output epilogue of the model (Ascend model file,
+    ``KimiDeltaAttention._project_out``): RMSNorm over the value dim of each
+    (token, head) row, times its weight, times sigmoid of the output gate,
+
+        out[t, h, v] = o[t, h, v] / sqrt(mean_v o[t, h, :]^2 + eps) * weight[v]
+                       * sigmoid(gate[t, h, v])
+
+    o, gate [.., H, V]; weight [V].  fp64."""
+    x = _f64(o)
+    r = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + float(eps))
+    return x * r * _f64(weight) * _sigmoid(_f64(gate))

@@ -362,3 +362,51 @@ def test_gate_limits_and_ranges():
     g1, _ = oracle.gate_activation(raw1, np.zeros((1, H)), a_log, dt_bias)
     np.testing.assert_allclose(g1[0, 0, 1], -np.exp(a_log[0]) * np.log1p(np.exp(1.0)), rtol=1e-15)
     np.testing.assert_allclose(g1[0, 1, 0], -np.exp(a_log[1]) * np.log1p(np.exp(0.5)), rtol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# output epilogue (Ascend model file, KimiDeltaAttention._project_out)
+# ---------------------------------------------------------------------------
+
+def test_output_norm_of_a_constant_row_and_gate_zero():
+    """A row of equal entries c: RMS = |c| (eps = 0), so out = sign(c) w sigmoid(gate);
+    gate = 0 halves it."""
+    V = 8
+    w = np.linspace(0.5, 2.0, V)
+    o = np.full((1, 1, V), -3.0)
+    out = oracle.output_gate_norm(o, np.zeros((1, 1, V)), w, 0.0)
+    np.testing.assert_allclose(out[0, 0], -0.5 * w, rtol=1e-15)
+
+
+def test_output_norm_scale_invariance_and_unit_rms():
+    """out is unchanged when a row is scaled (eps -> 0); with weight 1 and a
+    large gate the row has unit RMS; eps enters as mean(o^2) + eps."""
+    rng = np.random.default_rng(31)
+    T, H, V = 5, 3, 16
+    o = rng.standard_normal((T, H, V))
+    gate = rng.standard_normal((T, H, V))
+    w = rng.uniform(0.5, 1.5, V)
+    a = oracle.output_gate_norm(o, gate, w, 0.0)
+    b = oracle.output_gate_norm(7.5 * o, gate, w, 0.0)
+    np.testing.assert_allclose(a, b, rtol=1e-13)
+    u = oracle.output_gate_norm(o, np.full((T, H, V), 60.0), np.ones(V), 0.0)
+    np.testing.assert_allclose(np.sqrt(np.mean(u * u, axis=-1)), 1.0, rtol=1e-13)
+    # eps: a row of ones with eps = 3 has RMS factor 1 / sqrt(1 + 3) = 1/2
+    e = oracle.output_gate_norm(np.ones((1, 1, V)), np.full((1, 1, V), 60.0), np.ones(V), 3.0)
+    np.testing.assert_allclose(e, 0.5, rtol=1e-13)
+
+
+def test_output_norm_rows_are_independent():
+    """Each (token, head) row is normalised on its own: changing one row leaves
+    every other output untouched."""
+    rng = np.random.default_rng(32)
+    o = rng.standard_normal((4, 2, 8))
+    gate = rng.standard_normal((4, 2, 8))
+    w = np.ones(8)
+    a = oracle.output_gate_norm(o, gate, w, 1e-6)
+    o2 = o.copy()
+    o2[2, 1] *= -4.0
+    b = oracle.output_gate_norm(o2, gate, w, 1e-6)
+    mask = np.ones((4, 2), bool)
+    mask[2, 1] = False
+    np.testing.assert_array_equal(a[mask], b[mask])
