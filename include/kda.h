@@ -263,10 +263,19 @@ int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const flo
  * path's decay-range limit (per-token decays down to about -5.3) makes the
  * lower-bounded gate with lower_bound >= -5 the form to use there, as the
  * model's own fast path does.
+ *
+ * Output epilogue (model file, KimiDeltaAttention._project_out), optional:
+ *   out_gate    [T, H, V] / [N, H, V] in the q dtype, or NULL for none
+ *   norm_weight device fp32 [V];  norm_eps > 0
+ * replaces each output row of V values by
+ *   o / sqrt(mean(o^2) + norm_eps) * norm_weight * sigmoid(out_gate).
+ * Decode applies it in the step; the chunked forward applies it as a final
+ * pass over o (kda_output_gate_norm).
  */
 int kda_chunk_fwd_gated(const void *q, const void *k, const void *v, const void *raw_gate,
                         const void *raw_beta, const float *a_log, const float *dt_bias,
-                        float lower_bound, int use_lower_bound, const float *initial_state,
+                        float lower_bound, int use_lower_bound, const void *out_gate,
+                        const float *norm_weight, float norm_eps, const float *initial_state,
                         float *final_state, const int32_t *state_indices, int64_t n_slots,
                         void *o, const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens,
                         int H, int K, int V, float scale, int dtype, int flags, void *workspace,
@@ -274,9 +283,21 @@ int kda_chunk_fwd_gated(const void *q, const void *k, const void *v, const void 
 
 int kda_recurrent_step_gated(const void *q, const void *k, const void *v, const void *raw_gate,
                              const void *raw_beta, const float *a_log, const float *dt_bias,
-                             float lower_bound, int use_lower_bound, float *state_pool,
+                             float lower_bound, int use_lower_bound, const void *out_gate,
+                             const float *norm_weight, float norm_eps, float *state_pool,
                              const int32_t *state_indices, int64_t n_slots, void *o, int N,
                              int H, int K, int V, float scale, int dtype, void *stream);
+
+/*
+ * The output epilogue alone, in place on o [rows, V] (rows = tokens x heads,
+ * V = 128, dtype as q): each row becomes
+ *   o / sqrt(mean(o^2) + eps) * weight * sigmoid(gate)
+ * with gate [rows, V] (same dtype) and weight [V] fp32 (model file,
+ * KimiDeltaAttention._project_out: o_norm, then the sigmoid gate).  The row
+ * statistics are taken in fp32 from the stored o.  rows = 0 is a no-op.
+ */
+int kda_output_gate_norm(void *o, const void *gate, const float *weight, float eps,
+                         int64_t rows, int V, int dtype, void *stream);
 
 #ifdef __cplusplus
 }

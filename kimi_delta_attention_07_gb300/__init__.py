@@ -31,7 +31,8 @@ CHUNK = 64
 
 EXPORTS = ("kda_status_string", "kda_version", "kda_chunk_workspace_bytes", "kda_chunk_fwd",
            "kda_chunk_intra", "kda_chunk_scan", "kda_workspace_status", "kda_recurrent_step",
-           "kda_chunk_fwd_noalloc", "kda_chunk_fwd_gated", "kda_recurrent_step_gated")
+           "kda_chunk_fwd_noalloc", "kda_chunk_fwd_gated", "kda_recurrent_step_gated",
+           "kda_output_gate_norm")
 NOALLOC_WORKSPACE_BYTES = 64 * 1024 * 1024
 
 _lib = None
@@ -78,12 +79,15 @@ def load(path: str | None = None):
         L.kda_recurrent_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, vp, i32, i32, i32, i32,
                                          f32, i32, vp]
         L.kda_recurrent_step.restype = i32
-        L.kda_chunk_fwd_gated.argtypes = [vp, vp, vp, vp, vp, vp, vp, f32, i32, vp, vp, vp, i64, vp,
-                                          vp, i32, i64, i32, i32, i32, f32, i32, i32, vp, sz, vp]
+        L.kda_chunk_fwd_gated.argtypes = [vp, vp, vp, vp, vp, vp, vp, f32, i32, vp, vp, f32, vp, vp,
+                                          vp, i64, vp, vp, i32, i64, i32, i32, i32, f32, i32, i32,
+                                          vp, sz, vp]
         L.kda_chunk_fwd_gated.restype = i32
-        L.kda_recurrent_step_gated.argtypes = [vp, vp, vp, vp, vp, vp, vp, f32, i32, vp, vp, i64,
-                                               vp, i32, i32, i32, i32, f32, i32, vp]
+        L.kda_recurrent_step_gated.argtypes = [vp, vp, vp, vp, vp, vp, vp, f32, i32, vp, vp, f32, vp,
+                                               vp, i64, vp, i32, i32, i32, i32, f32, i32, vp]
         L.kda_recurrent_step_gated.restype = i32
+        L.kda_output_gate_norm.argtypes = [vp, vp, vp, f32, i64, i32, i32, vp]
+        L.kda_output_gate_norm.restype = i32
         _lib = L
         return L
 
@@ -186,12 +190,12 @@ def kda_chunk_fwd(q, k, v, g, beta, *, cu_seqlens=None, n_seqs=None, initial_sta
     if _gate is not None:
         if phase != "fwd":
             raise ValueError("the gated forward runs as one call (phase='fwd')")
-        a_log, dt_bias, lower_bound = _gate
+        a_log, dt_bias, lower_bound, out_gate, norm_weight, norm_eps = _gate
         name = "kda_chunk_fwd_gated"
         st = load().kda_chunk_fwd_gated(
             _p(q), _p(k), _p(v), _p(g), _p(beta), _p(a_log), _p(dt_bias),
             float(0.0 if lower_bound is None else lower_bound), int(lower_bound is not None),
-            _p(initial_state), _p(final_state), _p(state_indices), slots, _p(o), _p(cu_seqlens),
+            _p(out_gate), _p(norm_weight), float(norm_eps), _p(initial_state), _p(final_state), _p(state_indices), slots, _p(o), _p(cu_seqlens),
             N, T, H, K, V, float(scale), dt, flags, _p(workspace), workspace.numel(),
             _stream(stream))
     else:
@@ -210,22 +214,48 @@ def _check_gate(a_log, dt_bias, H, K):
     _check(dt_bias, "dt_bias", torch.float32, (H, K))
 
 
-def kda_chunk_fwd_gated(q, k, v, raw_gate, raw_beta, a_log, dt_bias, *, lower_bound=None, **kw):
+def _check_epilogue(out_gate, norm_weight, shape, dtype):
+    if out_gate is None:
+        return
+    _check(out_gate, "out_gate", dtype, shape)
+    _check(norm_weight, "norm_weight", torch.float32, (shape[-1],))
+
+
+def kda_chunk_fwd_gated(q, k, v, raw_gate, raw_beta, a_log, dt_bias, *, lower_bound=None,
+                        out_gate=None, norm_weight=None, norm_eps=1e-6, **kw):
     """Chunked KDA forward from the model's raw gates, activated in-kernel:
     g = lower_bound * sigmoid(exp(a_log[h]) (raw_gate + dt_bias[h])) (or
     -exp(a_log[h]) softplus(raw_gate + dt_bias[h]) without a lower bound),
     beta = sigmoid(raw_beta).  raw_gate [T, H, K] and raw_beta [T, H] in the
-    q dtype; a_log [H] and dt_bias [H, K] fp32.  Other arguments as for
-    kda_chunk_fwd.  Returns (o, final_state)."""
-    H, K = q.shape[1], q.shape[2]
+    q dtype; a_log [H] and dt_bias [H, K] fp32.  With out_gate ([T, H, V], q
+    dtype) and norm_weight ([V] fp32), each output row becomes
+    o / sqrt(mean(o^2) + norm_eps) * norm_weight * sigmoid(out_gate).  Other
+    arguments as for kda_chunk_fwd.  Returns (o, final_state)."""
+    T, H, K = q.shape
     _check_gate(a_log, dt_bias, H, K)
-    return kda_chunk_fwd(q, k, v, raw_gate, raw_beta, _gate=(a_log, dt_bias, lower_bound), **kw)
+    _check_epilogue(out_gate, norm_weight, tuple(v.shape), q.dtype)
+    return kda_chunk_fwd(q, k, v, raw_gate, raw_beta,
+                         _gate=(a_log, dt_bias, lower_bound, out_gate, norm_weight, norm_eps), **kw)
+
+
+def kda_output_gate_norm(o, gate, weight, eps=1e-6, *, stream=None):
+    """In place on o [.., V]: o / sqrt(mean(o^2) + eps) * weight * sigmoid(gate)."""
+    _check(o, "o")
+    _check(gate, "gate", o.dtype, tuple(o.shape))
+    _check(weight, "weight", torch.float32, (o.shape[-1],))
+    st = load().kda_output_gate_norm(_p(o), _p(gate), _p(weight), float(eps),
+                                     o.numel() // o.shape[-1], o.shape[-1], _dtype_code(o),
+                                     _stream(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_output_gate_norm")
+    return o
 
 
 def kda_recurrent_step_gated(q, k, v, raw_gate, raw_beta, a_log, dt_bias, state_pool, *,
-                             lower_bound=None, state_indices=None, scale=None, o=None,
-                             stream=None):
-    """kda_recurrent_step from the model's raw gates (see kda_chunk_fwd_gated)."""
+                             lower_bound=None, out_gate=None, norm_weight=None, norm_eps=1e-6,
+                             state_indices=None, scale=None, o=None, stream=None):
+    """kda_recurrent_step from the model's raw gates, with the optional output
+    epilogue applied in the step (see kda_chunk_fwd_gated)."""
     N, H, K = q.shape
     V = v.shape[-1]
     dt = _dtype_code(q)
@@ -237,6 +267,7 @@ def kda_recurrent_step_gated(q, k, v, raw_gate, raw_beta, a_log, dt_bias, state_
                                    ("state_indices", state_indices, torch.int32, (N,))):
         _check(t, name, dtype_, shape)
     _check_gate(a_log, dt_bias, H, K)
+    _check_epilogue(out_gate, norm_weight, (N, H, V), q.dtype)
     if state_pool.dim() != 4 or tuple(state_pool.shape[1:]) != (H, V, K):
         raise ValueError(f"state_pool must be [slots, {H}, {V}, {K}]")
     if o is None:
@@ -247,8 +278,8 @@ def kda_recurrent_step_gated(q, k, v, raw_gate, raw_beta, a_log, dt_bias, state_
     st = load().kda_recurrent_step_gated(
         _p(q), _p(k), _p(v), _p(raw_gate), _p(raw_beta), _p(a_log), _p(dt_bias),
         float(0.0 if lower_bound is None else lower_bound), int(lower_bound is not None),
-        _p(state_pool), _p(state_indices), state_pool.shape[0], _p(o), N, H, K, V, float(scale),
-        dt, _stream(stream))
+        _p(out_gate), _p(norm_weight), float(norm_eps), _p(state_pool), _p(state_indices),
+        state_pool.shape[0], _p(o), N, H, K, V, float(scale), dt, _stream(stream))
     if st != KDA_OK:
         raise KdaError(st, "kda_recurrent_step_gated")
     return o

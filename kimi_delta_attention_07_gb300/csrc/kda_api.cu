@@ -58,10 +58,20 @@ namespace {
 
 enum Phase { kIntra = 1, kScan = 2, kBoth = 3 };
 
+// epilogue arguments: out_gate rows as aligned as o's vector loads, weight
+// rows 16-byte aligned, a positive finite eps
+bool epi_ok(const EpiArgs *epi, int dtype) {
+    if (!epi || !epi->out_gate) return true;
+    return epi->weight && aligned(epi->weight, 16) &&
+           aligned(epi->out_gate, dtype == KDA_BF16 ? 8 : 16) && isfinite(epi->eps) &&
+           epi->eps > 0.0f;
+}
+
 // gate == nullptr: g and beta are the activated fp32 inputs; otherwise g and
 // beta are unused and the model's raw gates (*gate) are activated in-kernel.
 int chunk_call(int phase, const void *q, const void *k, const void *v, const float *g,
-               const float *beta, const GateArgs *gate, const float *initial_state,
+               const float *beta, const GateArgs *gate, const EpiArgs *epi,
+               const float *initial_state,
                float *final_state, const int32_t *state_indices, int64_t n_slots, void *o,
                const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens, int H, int K, int V,
                float scale, int dtype, int flags, void *workspace, size_t workspace_bytes,
@@ -89,6 +99,7 @@ int chunk_call(int phase, const void *q, const void *k, const void *v, const flo
         return KDA_ERR_INVALID_ARG;
     }
     if (total_tokens > 0 && (!q || !k || !v || !o)) return KDA_ERR_INVALID_ARG;
+    if (!epi_ok(epi, dtype)) return KDA_ERR_INVALID_ARG;
     if (!cu_seqlens && total_tokens % n_seqs != 0) return KDA_ERR_INVALID_ARG;
     if (state_indices && n_slots <= 0) return KDA_ERR_INVALID_ARG;
     if (!state_indices && n_slots < 0) return KDA_ERR_INVALID_ARG;
@@ -131,6 +142,8 @@ int chunk_call(int phase, const void *q, const void *k, const void *v, const flo
                                       total_tokens, H, flags, workspace, s)
                : launch_chunk_scan_f32(initial_state, final_state, state_indices, o, dtype,
                                        n_seqs, total_tokens, H, workspace, s);
+    if (e == cudaSuccess && (phase & kScan) && epi && epi->out_gate)
+        e = launch_output_gate_norm(o, *epi, total_tokens * H, dtype, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return KDA_ERR_CUDA;
@@ -149,7 +162,7 @@ extern "C" {
         int H, int K, int V, float scale, int dtype, int flags, void *workspace,               \
         size_t workspace_bytes, void *stream
 #define KDA_CHUNK_PASS                                                                       \
-    q, k, v, g, beta, nullptr, initial_state, final_state, state_indices, n_slots, o,         \
+    q, k, v, g, beta, nullptr, nullptr, initial_state, final_state, state_indices, n_slots, o,\
         cu_seqlens,                                                                           \
         n_seqs, total_tokens, H, K, V, scale, dtype, flags, workspace, workspace_bytes, stream
 
@@ -159,13 +172,15 @@ int kda_chunk_scan(KDA_CHUNK_ARGS) { return chunk_call(kScan, KDA_CHUNK_PASS); }
 
 int kda_chunk_fwd_gated(const void *q, const void *k, const void *v, const void *raw_gate,
                         const void *raw_beta, const float *a_log, const float *dt_bias,
-                        float lower_bound, int use_lower_bound, const float *initial_state,
+                        float lower_bound, int use_lower_bound, const void *out_gate,
+                        const float *norm_weight, float norm_eps, const float *initial_state,
                         float *final_state, const int32_t *state_indices, int64_t n_slots,
                         void *o, const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens,
                         int H, int K, int V, float scale, int dtype, int flags, void *workspace,
                         size_t workspace_bytes, void *stream) {
     const GateArgs gate{raw_gate, raw_beta, a_log, dt_bias, lower_bound, use_lower_bound != 0};
-    return chunk_call(kBoth, q, k, v, nullptr, nullptr, &gate, initial_state, final_state,
+    const EpiArgs epi{out_gate, norm_weight, norm_eps};
+    return chunk_call(kBoth, q, k, v, nullptr, nullptr, &gate, &epi, initial_state, final_state,
                       state_indices, n_slots, o, cu_seqlens, n_seqs, total_tokens, H, K, V, scale,
                       dtype, flags, workspace, workspace_bytes, stream);
 }
@@ -186,7 +201,8 @@ int kda_workspace_status(const void *workspace, int *flags_out, void *stream) {
 
 namespace {
 int step_call(const void *q, const void *k, const void *v, const float *g, const float *beta,
-              const GateArgs *gate, float *state_pool, const int32_t *state_indices,
+              const GateArgs *gate, const EpiArgs *epi, float *state_pool,
+              const int32_t *state_indices,
               int64_t n_slots, void *o, int N, int H, int K, int V, float scale, int dtype,
               void *stream) {
     if (!valid_dtype(dtype) || N < 0 || H <= 0 || K <= 0 || V <= 0 || n_slots < 0)
@@ -205,6 +221,7 @@ int step_call(const void *q, const void *k, const void *v, const float *g, const
         return KDA_ERR_INVALID_ARG;
     }
     if (!q || !k || !v || !state_pool || !o) return KDA_ERR_INVALID_ARG;
+    if (!epi_ok(epi, dtype)) return KDA_ERR_INVALID_ARG;
     if (!state_indices && n_slots < N) return KDA_ERR_INVALID_ARG;
     if ((int64_t)N * H > INT32_MAX) return KDA_ERR_INVALID_ARG;
     const size_t ea = 4 * elem_bytes(dtype);
@@ -213,7 +230,7 @@ int step_call(const void *q, const void *k, const void *v, const float *g, const
         return KDA_ERR_INVALID_ARG;
     if (!isfinite(scale)) return KDA_ERR_INVALID_ARG;
     cudaGetLastError();
-    const cudaError_t e = launch_recurrent_step(q, k, v, g, beta, gate, state_pool, state_indices,
+    const cudaError_t e = launch_recurrent_step(q, k, v, g, beta, gate, epi, state_pool, state_indices,
                                                 n_slots, o, N, H, scale, dtype,
                                                 (cudaStream_t)stream);
     if (e != cudaSuccess) {
@@ -228,18 +245,37 @@ int kda_recurrent_step(const void *q, const void *k, const void *v, const float 
                        const float *beta, float *state_pool, const int32_t *state_indices,
                        int64_t n_slots, void *o, int N, int H, int K, int V, float scale,
                        int dtype, void *stream) {
-    return step_call(q, k, v, g, beta, nullptr, state_pool, state_indices, n_slots, o, N, H, K,
-                     V, scale, dtype, stream);
+    return step_call(q, k, v, g, beta, nullptr, nullptr, state_pool, state_indices, n_slots, o, N,
+                     H, K, V, scale, dtype, stream);
 }
 
 int kda_recurrent_step_gated(const void *q, const void *k, const void *v, const void *raw_gate,
                              const void *raw_beta, const float *a_log, const float *dt_bias,
-                             float lower_bound, int use_lower_bound, float *state_pool,
+                             float lower_bound, int use_lower_bound, const void *out_gate,
+                             const float *norm_weight, float norm_eps, float *state_pool,
                              const int32_t *state_indices, int64_t n_slots, void *o, int N,
                              int H, int K, int V, float scale, int dtype, void *stream) {
     const GateArgs gate{raw_gate, raw_beta, a_log, dt_bias, lower_bound, use_lower_bound != 0};
-    return step_call(q, k, v, nullptr, nullptr, &gate, state_pool, state_indices, n_slots, o, N,
-                     H, K, V, scale, dtype, stream);
+    const EpiArgs epi{out_gate, norm_weight, norm_eps};
+    return step_call(q, k, v, nullptr, nullptr, &gate, &epi, state_pool, state_indices, n_slots, o,
+                     N, H, K, V, scale, dtype, stream);
+}
+
+int kda_output_gate_norm(void *o, const void *gate, const float *weight, float eps,
+                         int64_t rows, int V, int dtype, void *stream) {
+    if (!valid_dtype(dtype) || rows < 0 || V <= 0) return KDA_ERR_INVALID_ARG;
+    if (V != kHeadDim) return KDA_ERR_UNSUPPORTED;
+    if (rows == 0) return KDA_OK;
+    const EpiArgs epi{gate, weight, eps};
+    if (!o || !gate || !aligned(o, dtype == KDA_BF16 ? 8 : 16) || !epi_ok(&epi, dtype))
+        return KDA_ERR_INVALID_ARG;
+    cudaGetLastError();
+    const cudaError_t e = launch_output_gate_norm(o, epi, rows, dtype, (cudaStream_t)stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
 }
 
 }  // extern "C"

@@ -16,7 +16,9 @@
 // load and one 128-bit store per lane per row), and the two dot products are
 // warp-shuffle reductions.  Rows of one head are split over CTAs when there
 // are too few (sequence, head) pairs to fill the GPU.  The gated variant
-// activates the model's raw gate and beta on the way in (see GateArgs).
+// activates the model's raw gate and beta on the way in (see GateArgs); the
+// epilogue variant (one CTA per head) normalises each head's output row and
+// applies the output gate before storing it (see EpiArgs).
 #include <string.h>
 
 #include "kda_internal.cuh"
@@ -28,14 +30,15 @@ constexpr int kDecodeThreads = 256;  // 8 warps
 constexpr int kWarps = kDecodeThreads / 32;
 constexpr int kMaxRowsPerWarp = kHeadDim / kWarps;  // 16: a whole head per CTA
 
-template <typename T, bool GATED>
+template <typename T, bool GATED, bool EPI>
 __global__ void __launch_bounds__(kDecodeThreads)
     recurrent_step_kernel(const T *__restrict__ q, const T *__restrict__ k,
                           const T *__restrict__ v, const float *__restrict__ g,
-                          const float *__restrict__ beta, const GateArgs gate,
+                          const float *__restrict__ beta, const GateArgs gate, const EpiArgs epi,
                           float *__restrict__ pool, const int32_t *__restrict__ state_indices,
                           int64_t n_slots, T *__restrict__ o, int H, int rows_per_cta,
                           float scale) {
+    __shared__ float s_part[kWarps];  // epilogue: per-warp sums of o^2
     const int pair = blockIdx.x;  // n * H + h
     const int n = pair / H;
     const int h = pair - n * H;
@@ -63,6 +66,12 @@ __global__ void __launch_bounds__(kDecodeThreads)
         if (j < rpw)
             s[j] = *reinterpret_cast<const float4 *>(S + (int64_t)(row0 + warp + kWarps * j) * kHeadDim + 4 * lane);
     const float vrow = lane < rpw ? to_f32(v[io_k + row0 + warp + kWarps * lane]) : 0.0f;
+    float gate_o = 0.0f, w_o = 0.0f;  // epilogue: output gate and norm weight of row `lane`
+    if (EPI && lane < rpw) {
+        const int r = row0 + warp + kWarps * lane;
+        gate_o = to_f32(reinterpret_cast<const T *>(epi.out_gate)[io_k + r]);
+        w_o = epi.weight[r];
+    }
 
     // L2 norms of q and k over the key dim (eps inside the root), scale on q.
     const float4 q4 = load4(q + io_k + 4 * lane);
@@ -92,6 +101,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
     const float4 dec = make_float4(expf(g4.x), expf(g4.y), expf(g4.z), expf(g4.w));
     const float kq = warp_sum(kh.x * qh.x + kh.y * qh.y + kh.z * qh.z + kh.w * qh.w);
 
+    float my_o = 0.0f, ss = 0.0f;  // epilogue: o of row `lane`, sum of o^2 over the warp's rows
 #pragma unroll
     for (int j = 0; j < kMaxRowsPerWarp; ++j) {
         if (j >= rpw) break;
@@ -108,46 +118,80 @@ __global__ void __launch_bounds__(kDecodeThreads)
         const float u = b * (__shfl_sync(0xffffffffu, vrow, j) - a);
         x.x += u * kh.x; x.y += u * kh.y; x.z += u * kh.z; x.w += u * kh.w;
         *reinterpret_cast<float4 *>(S + (int64_t)r * kHeadDim + 4 * lane) = x;
-        if (lane == 0) o[io_k + r] = from_f32<T>(c + u * kq);
+        const float ov = c + u * kq;
+        if (EPI) {
+            ss = fmaf(ov, ov, ss);
+            if (lane == j) my_o = ov;
+        } else if (lane == 0) {
+            o[io_k + r] = from_f32<T>(ov);
+        }
+    }
+    if (EPI) {  // rows_per_cta == 128: this CTA holds the head's whole output row
+        if (lane == 0) s_part[warp] = ss;
+        __syncthreads();
+        float tot = 0.0f;
+#pragma unroll
+        for (int w2 = 0; w2 < kWarps; ++w2) tot += s_part[w2];
+        const float rn = 1.0f / sqrtf(tot * (1.0f / kHeadDim) + epi.eps);
+        if (lane < rpw)
+            o[io_k + row0 + warp + kWarps * lane] = from_f32<T>(my_o * rn * w_o * gate_beta(gate_o));
     }
 }
 
 }  // namespace
 
-template <typename T>
-void launch_step(bool gated, dim3 grid, const void *q, const void *k, const void *v,
-                 const float *g, const float *beta, const GateArgs &gate, float *pool,
-                 const int32_t *state_indices, int64_t n_slots, void *o, int H, int rows,
-                 float scale, cudaStream_t stream) {
-    if (gated)
-        recurrent_step_kernel<T, true><<<grid, kDecodeThreads, 0, stream>>>(
-            (const T *)q, (const T *)k, (const T *)v, g, beta, gate, pool, state_indices,
+template <typename T, bool GATED>
+void launch_step2(bool epi_on, dim3 grid, const void *q, const void *k, const void *v,
+                  const float *g, const float *beta, const GateArgs &gate, const EpiArgs &epi,
+                  float *pool, const int32_t *state_indices, int64_t n_slots, void *o, int H,
+                  int rows, float scale, cudaStream_t stream) {
+    if (epi_on)
+        recurrent_step_kernel<T, GATED, true><<<grid, kDecodeThreads, 0, stream>>>(
+            (const T *)q, (const T *)k, (const T *)v, g, beta, gate, epi, pool, state_indices,
             n_slots, (T *)o, H, rows, scale);
     else
-        recurrent_step_kernel<T, false><<<grid, kDecodeThreads, 0, stream>>>(
-            (const T *)q, (const T *)k, (const T *)v, g, beta, gate, pool, state_indices,
+        recurrent_step_kernel<T, GATED, false><<<grid, kDecodeThreads, 0, stream>>>(
+            (const T *)q, (const T *)k, (const T *)v, g, beta, gate, epi, pool, state_indices,
             n_slots, (T *)o, H, rows, scale);
 }
 
+template <typename T>
+void launch_step(bool gated, bool epi_on, dim3 grid, const void *q, const void *k,
+                 const void *v, const float *g, const float *beta, const GateArgs &gate,
+                 const EpiArgs &epi, float *pool, const int32_t *state_indices, int64_t n_slots,
+                 void *o, int H, int rows, float scale, cudaStream_t stream) {
+    if (gated)
+        launch_step2<T, true>(epi_on, grid, q, k, v, g, beta, gate, epi, pool, state_indices,
+                              n_slots, o, H, rows, scale, stream);
+    else
+        launch_step2<T, false>(epi_on, grid, q, k, v, g, beta, gate, epi, pool, state_indices,
+                               n_slots, o, H, rows, scale, stream);
+}
+
 cudaError_t launch_recurrent_step(const void *q, const void *k, const void *v, const float *g,
-                                  const float *beta, const GateArgs *gate, float *pool,
-                                  const int32_t *state_indices, int64_t n_slots, void *o, int N,
-                                  int H, float scale, int dtype, cudaStream_t stream) {
+                                  const float *beta, const GateArgs *gate, const EpiArgs *epi,
+                                  float *pool, const int32_t *state_indices, int64_t n_slots,
+                                  void *o, int N, int H, float scale, int dtype,
+                                  cudaStream_t stream) {
     const int64_t pairs = (int64_t)N * H;
     // Split a head's 128 rows over more CTAs when there are few heads in flight,
     // so that at least ~4 CTAs per SM are resident.
     int rows = kHeadDim;  // a multiple of 8 warps, at most 16 rows per warp
-    while (rows > 16 && pairs * (kHeadDim / rows) < 152 * 8) rows >>= 1;
+    const bool epi_on = epi && epi->out_gate;
+    while (!epi_on && rows > 16 && pairs * (kHeadDim / rows) < 152 * 8) rows >>= 1;
     const dim3 grid((unsigned)pairs, kHeadDim / rows);
     GateArgs ga;
     memset(&ga, 0, sizeof(ga));
     if (gate) ga = *gate;
+    EpiArgs ea;
+    memset(&ea, 0, sizeof(ea));
+    if (epi_on) ea = *epi;
     if (dtype == KDA_BF16)
-        launch_step<__nv_bfloat16>(gate != nullptr, grid, q, k, v, g, beta, ga, pool,
+        launch_step<__nv_bfloat16>(gate != nullptr, epi_on, grid, q, k, v, g, beta, ga, ea, pool,
                                    state_indices, n_slots, o, H, rows, scale, stream);
     else
-        launch_step<float>(gate != nullptr, grid, q, k, v, g, beta, ga, pool, state_indices,
-                           n_slots, o, H, rows, scale, stream);
+        launch_step<float>(gate != nullptr, epi_on, grid, q, k, v, g, beta, ga, ea, pool,
+                           state_indices, n_slots, o, H, rows, scale, stream);
     return cudaGetLastError();
 }
 

@@ -143,6 +143,13 @@ __device__ __forceinline__ float gate_decay(float x, float gscale, float lower_b
 }
 __device__ __forceinline__ float gate_beta(float raw) { return 1.0f / (1.0f + expf(-raw)); }
 
+// Output epilogue: o / sqrt(mean(o^2) + eps) * weight * sigmoid(gate) per row.
+struct EpiArgs {
+    const void *out_gate;  // [rows, V] in the o dtype; nullptr = no epilogue
+    const float *weight;   // [V]
+    float eps;
+};
+
 // Workspace of a gated call on the fp32 path: activated g [T, H, K] and beta
 // [T, H] (fp32) after the records.
 struct WsGate {
@@ -199,9 +206,16 @@ __device__ __forceinline__ int owner_of_chunk(const int32_t *chunk_off, int n_se
 }
 
 // gate == nullptr: g, beta are activated fp32; otherwise raw gates (*gate).
+// epi == nullptr (or epi->out_gate == nullptr): plain o; otherwise the output
+// epilogue is applied in the step.
 cudaError_t launch_recurrent_step(const void *q, const void *k, const void *v, const float *g,
-                                  const float *beta, const GateArgs *gate, float *pool,
-                                  const int32_t *state_indices, int64_t n_slots, void *o, int N,
-                                  int H, float scale, int dtype, cudaStream_t stream);
+                                  const float *beta, const GateArgs *gate, const EpiArgs *epi,
+                                  float *pool, const int32_t *state_indices, int64_t n_slots,
+                                  void *o, int N, int H, float scale, int dtype,
+                                  cudaStream_t stream);
+
+// The output epilogue in place on o [rows, 128].
+cudaError_t launch_output_gate_norm(void *o, const EpiArgs &epi, int64_t rows, int dtype,
+                                    cudaStream_t stream);
 
 }  // namespace kda

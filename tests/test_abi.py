@@ -102,21 +102,23 @@ def test_gated_entry_points_reject_bad_arguments_without_launching(lib):
 
     def chunk(**kw):
         a = dict(q=base, k=base, v=base, rg=base, rb=base, alog=base, bias=base, lb=-5.0, use_lb=1,
-                 o=base, N=1, T=64, H=1, dt=kda.KDA_BF16, flags=0, ws=base, wsb=1 << 30)
+                 og=None, nw=base, eps=1e-6, o=base, N=1, T=64, H=1, dt=kda.KDA_BF16, flags=0,
+                 ws=base, wsb=1 << 30)
         a.update(kw)
         return lib.kda_chunk_fwd_gated(p(a["q"]), p(a["k"]), p(a["v"]), p(a["rg"]), p(a["rb"]),
-                                       p(a["alog"]), p(a["bias"]), a["lb"], a["use_lb"], None, None,
-                                       None, 0, p(a["o"]), None, a["N"], a["T"], a["H"], 128, 128,
-                                       0.1, a["dt"], a["flags"], p(a["ws"]), a["wsb"], None)
+                                       p(a["alog"]), p(a["bias"]), a["lb"], a["use_lb"], p(a["og"]),
+                                       p(a["nw"]), a["eps"], None, None, None, 0, p(a["o"]), None,
+                                       a["N"], a["T"], a["H"], 128, 128, 0.1, a["dt"], a["flags"],
+                                       p(a["ws"]), a["wsb"], None)
 
     def step(**kw):
         a = dict(q=base, k=base, v=base, rg=base, rb=base, alog=base, bias=base, lb=-5.0, use_lb=1,
-                 pool=base, o=base, N=2, H=2, dt=kda.KDA_F32)
+                 og=None, nw=base, eps=1e-6, pool=base, o=base, N=2, H=2, dt=kda.KDA_F32)
         a.update(kw)
         return lib.kda_recurrent_step_gated(p(a["q"]), p(a["k"]), p(a["v"]), p(a["rg"]), p(a["rb"]),
                                             p(a["alog"]), p(a["bias"]), a["lb"], a["use_lb"],
-                                            p(a["pool"]), None, 4, p(a["o"]), a["N"], a["H"], 128,
-                                            128, 0.1, a["dt"], None)
+                                            p(a["og"]), p(a["nw"]), a["eps"], p(a["pool"]), None, 4,
+                                            p(a["o"]), a["N"], a["H"], 128, 128, 0.1, a["dt"], None)
 
     for f in (chunk, step):
         assert f(alog=None) == kda.KDA_ERR_INVALID_ARG
@@ -126,6 +128,11 @@ def test_gated_entry_points_reject_bad_arguments_without_launching(lib):
         assert f(rb=None) == kda.KDA_ERR_INVALID_ARG
         assert f(lb=float("nan")) == kda.KDA_ERR_INVALID_ARG    # a lower bound must be finite
         assert f(dt=4) == kda.KDA_ERR_INVALID_ARG
+        # output epilogue: weight needed, 16-byte aligned, positive finite eps
+        assert f(og=base, nw=None) == kda.KDA_ERR_INVALID_ARG
+        assert f(og=base, nw=base + 4) == kda.KDA_ERR_INVALID_ARG
+        assert f(og=base, eps=0.0) == kda.KDA_ERR_INVALID_ARG
+        assert f(og=base, eps=float("inf")) == kda.KDA_ERR_INVALID_ARG
     assert chunk(rg=base + 8) == kda.KDA_ERR_INVALID_ARG        # tensor-core path: 16-byte rows
     assert chunk(ws=None) == kda.KDA_ERR_WORKSPACE
     # the fp32 path keeps the activated gate in the workspace: it needs more room
@@ -134,6 +141,24 @@ def test_gated_entry_points_reject_bad_arguments_without_launching(lib):
     assert f32_gated >= f32 + 4096 * 32 * (128 + 1) * 4
     assert (kda.kda_chunk_workspace_bytes(4096, 1, 32, flags=kda.KDA_CHUNK_GATED)
             == kda.kda_chunk_workspace_bytes(4096, 1, 32))          # tensor-core path: on chip
+
+
+def test_output_gate_norm_rejects_bad_arguments_without_launching(lib):
+    base = 1 << 20
+    vp = ctypes.c_void_p
+    f = lambda o=base, g=base, w=base, eps=1e-6, rows=10, V=128, dt=kda.KDA_BF16: \
+        lib.kda_output_gate_norm(None if o is None else vp(o), None if g is None else vp(g),
+                                 None if w is None else vp(w), eps, rows, V, dt, None)
+    assert f(rows=0) == kda.KDA_OK                      # nothing to do
+    assert f(V=64) == kda.KDA_ERR_UNSUPPORTED
+    assert f(rows=-1) == kda.KDA_ERR_INVALID_ARG
+    assert f(o=None) == kda.KDA_ERR_INVALID_ARG
+    assert f(g=None) == kda.KDA_ERR_INVALID_ARG
+    assert f(w=None) == kda.KDA_ERR_INVALID_ARG
+    assert f(w=base + 8) == kda.KDA_ERR_INVALID_ARG
+    assert f(eps=-1.0) == kda.KDA_ERR_INVALID_ARG
+    assert f(o=base + 4) == kda.KDA_ERR_INVALID_ARG      # bf16 rows: 8-byte aligned
+    assert f(dt=kda.KDA_F32, g=base + 8) == kda.KDA_ERR_INVALID_ARG
 
 
 def test_recurrent_step_rejects_bad_arguments_without_launching(lib):

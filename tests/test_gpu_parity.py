@@ -476,3 +476,67 @@ def test_gated_prefill_4k_full_size_sampled_heads(kda):
     assert rel_l2(to_np(o[:, heads]), o_ref) < TOL_BF16
     assert rel_l2(vk_to_kv(sf[:, heads]), s_ref) < TOL_BF16
     assert torch.isfinite(o).all()
+
+
+# ---------------------------------------------------------------------------
+# output epilogue: RMSNorm(o) * weight * sigmoid(out_gate)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_gated_step_with_output_epilogue(kda, dtype):
+    H, slots = 4, 5
+    tok = kda_inputs.decode_tokens(3, H=H, dtype=dtype, seed=61)
+    y, g_ref, b_ref = _gated(tok, 61, "lower_bound")
+    y = kda_inputs.with_output_gate(y, seed=61)
+    pool = kda_inputs.decode_pool(slots, H=H, seed=61)
+    idx = torch.tensor([4, 1, 2], dtype=torch.int32)
+    pool_d = pool.cuda()
+    o = kda.kda_recurrent_step_gated(*(y[n].cuda() for n in ("q", "k", "v", "raw_gate", "raw_beta",
+                                                              "a_log", "dt_bias")),
+                                     pool_d, lower_bound=y["lower_bound"], out_gate=y["out_gate"].cuda(),
+                                     norm_weight=y["norm_weight"].cuda(), norm_eps=y["norm_eps"],
+                                     state_indices=idx.cuda())
+    torch.cuda.synchronize()
+    o_ref, pool_ref = oracle.step(y["q"], y["k"], y["v"], g_ref, b_ref,
+                                  np.swapaxes(pool.double().numpy(), -1, -2), state_indices=idx.numpy())
+    out_ref = oracle.output_gate_norm(o_ref, y["out_gate"], y["norm_weight"], y["norm_eps"])
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    assert rel_l2(to_np(o), out_ref) < tol
+    assert rel_l2(vk_to_kv(pool_d), pool_ref) < TOL_F32
+
+
+@pytest.mark.parametrize("dtype,precise,scan", [(torch.bfloat16, False, "split"),
+                                                (torch.bfloat16, False, "wide"),
+                                                (torch.float32, False, "auto")])
+def test_gated_chunk_with_output_epilogue(kda, dtype, precise, scan):
+    x = kda_inputs.prefill([130, 0, 65], H=2, dtype=dtype, seed=62, init_std=0.02)
+    y, g_ref, b_ref = _gated(x, 62, "lower_bound")
+    y = kda_inputs.with_output_gate(y, seed=62)
+    d = dev(y, names=("q", "k", "v", "raw_gate", "raw_beta", "a_log", "dt_bias", "cu_seqlens",
+                      "initial_state", "out_gate", "norm_weight"))
+    o, sf = kda.kda_chunk_fwd_gated(d["q"], d["k"], d["v"], d["raw_gate"], d["raw_beta"], d["a_log"],
+                                    d["dt_bias"], lower_bound=y["lower_bound"], out_gate=d["out_gate"],
+                                    norm_weight=d["norm_weight"], norm_eps=y["norm_eps"],
+                                    cu_seqlens=d["cu_seqlens"], initial_state=d["initial_state"],
+                                    precise=precise, scan=scan)
+    torch.cuda.synchronize()
+    s0 = np.swapaxes(y["initial_state"].double().numpy(), -1, -2)
+    o_ref, s_ref = oracle.recurrence(y["q"], y["k"], y["v"], g_ref, b_ref,
+                                     cu_seqlens=y["cu_seqlens"].numpy(), initial_state=s0)
+    out_ref = oracle.output_gate_norm(o_ref, y["out_gate"], y["norm_weight"], y["norm_eps"])
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    assert rel_l2(to_np(o), out_ref) < tol
+    assert rel_l2(vk_to_kv(sf), s_ref) < tol
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_output_gate_norm_standalone(kda, dtype):
+    gen = torch.Generator().manual_seed(63)
+    o = (torch.randn((257, 3, 128), generator=gen) * 3).to(dtype)
+    gate = torch.randn((257, 3, 128), generator=gen).to(dtype)
+    w = torch.rand(128, generator=gen) + 0.5
+    od = o.cuda()
+    kda.kda_output_gate_norm(od, gate.cuda(), w.cuda(), 1e-5)
+    torch.cuda.synchronize()
+    ref = oracle.output_gate_norm(o, gate, w, 1e-5)
+    assert rel_l2(to_np(od), ref) < (1e-6 if dtype == torch.float32 else 5e-3)
