@@ -209,27 +209,39 @@ def run_gated(args, kda, dev, stream, ws):
     need = kda.kda_chunk_workspace_bytes(T_4K, 1, H, flags=kda.KDA_CHUNK_GATED)
     work = torch.empty(need, dtype=torch.uint8, device=dev)
 
-    def step():
+    ye = kda_inputs.with_output_gate(y, seed=6)
+    og, nw = ye["out_gate"].to(dev), ye["norm_weight"].to(dev)
+
+    def step(epi=False):
         kda.kda_chunk_fwd_gated(d["q"], d["k"], d["v"], d["raw_gate"], d["raw_beta"], d["a_log"],
                                 d["dt_bias"], lower_bound=y["lower_bound"], o=o, final_state=sf,
-                                workspace=work, stream=stream)
+                                workspace=work, stream=stream,
+                                out_gate=og if epi else None, norm_weight=nw if epi else None,
+                                norm_eps=ye["norm_eps"])
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(ws)
-    torch.cuda.synchronize()
-    a.record(stream)
-    for _ in range(args.steps):
-        step()
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = max_over_ranks(a.elapsed_time(b), ws, dev) / args.steps
+    def timed(epi):
+        for _ in range(max(3, args.warmup)):
+            step(epi)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(ws)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(args.steps):
+            step(epi)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(a.elapsed_time(b), ws, dev) / args.steps
+
+    ms = timed(False)
+    ms_epi = timed(True)
     byt = gated_prefill_bytes(T_4K, H)
     pk = peaks()
     return {"workload": "prefill_4k_gated", "tokens_per_s": round(T_4K * ws / (ms / 1e3), 1),
             "ms_per_step": round(ms, 4), "steps": args.steps,
+            "with_output_epilogue": {"tokens_per_s": round(T_4K * ws / (ms_epi / 1e3), 1),
+                                     "ms_per_step": round(ms_epi, 4),
+                                     "epilogue": "RMSNorm(o) * weight * sigmoid(out_gate), eps 1e-5"},
             "gate": "raw bf16 gate + dt_bias, exp(A_log) scale, lower bound -5; raw bf16 beta",
             "roofline": {"bound": "hbm", "algorithmic_bytes": byt,
                          "achieved": round(byt / (ms / 1e3) / 1e9, 1), "peak": pk["hbm"],
@@ -450,7 +462,30 @@ def run_decode(args, kda, dev, stream, pk, ws):
     med = max_over_ranks(statistics.median(us), ws, dev)
     nbytes = decode_bytes(DEC_N, H)
     gbs = nbytes / (med * 1e-6) / 1e9
+    # the model's decode path: raw gates in, output epilogue out (same pool, continued)
+    gtoks = [kda_inputs.with_output_gate(kda_inputs.with_raw_gates(
+        kda_inputs.decode_tokens(DEC_N, H=H, seed=3, step=DEC_STEPS + t), seed=5), seed=6)
+        for t in range(8)]
+    names = ("q", "k", "v", "raw_gate", "raw_beta", "a_log", "dt_bias")
+    gd = [{n: t[n].to(dev) for n in names + ("out_gate", "norm_weight")} for t in gtoks]
+
+    def gstep(t):
+        kda.kda_recurrent_step_gated(*(gd[t][n] for n in names), pool, lower_bound=-5.0,
+                                     out_gate=gd[t]["out_gate"], norm_weight=gd[t]["norm_weight"],
+                                     norm_eps=1e-5, o=o, stream=stream)
+
+    gstep(0)
+    torch.cuda.synchronize()
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(8)]
+    for t in range(8):
+        gev[t][0].record(stream)
+        gstep(t)
+        gev[t][1].record(stream)
+    torch.cuda.synchronize()
+    gus = statistics.median([a.elapsed_time(b) * 1e3 for a, b in gev])
     return {"workload": "decode_256", "us_per_step": round(med, 2),
+            "gated_epilogue_us_per_step": round(gus, 2),
             "us_min": round(min(us), 2), "tokens_per_s": round(DEC_N * ws / (med * 1e-6), 1),
             "steps": DEC_STEPS, "launches": DEC_STEPS * KERNELS_PER_DECODE,
             "roofline": {"kernel": "recurrent_step_kernel", "bound": "hbm",
