@@ -27,6 +27,8 @@ Gated variants (the model's raw gates; the library activates them in-kernel):
   (the lower-bounded "safe" gate keeps every decay in (lower_bound, 0)).
   prefill_4k_gated  prefill_4k's q/k/v with raw gates, A_log = log U[1, 16],
                     dt_bias ~ U[-1, 1], lower bound -5                       [5]
+Speculative decode: S draft tokens per sequence, q, k, g [N, S, H, K],
+v [N, S, H, V], beta [N, S, H], drawn like decode tokens.
 Output epilogue inputs: out_gate [T, H, V] ~ N(0, 1) in the q dtype, o_norm
 weight [V] ~ U[0.5, 1.5] fp32, eps 1e-5.
 """
@@ -149,6 +151,19 @@ def with_output_gate(x, seed=6, dtype=None, eps=1e-5):
     y["norm_weight"] = _uniform((x["v"].shape[-1],), gen, 0.5, 1.5)
     y["norm_eps"] = eps
     return y
+
+
+def spec_tokens(N, S, H=32, K=K_DIM, V=V_DIM, dtype=torch.bfloat16, seed=7, step=0,
+                g_range=(-0.1, -0.0005)):
+    """S draft tokens per sequence for speculative decode: q, k, g [N, S, H, K],
+    v [N, S, H, V], beta [N, S, H] (activated)."""
+    gen = _gen(seed * 100019 + 104729 * (step + 1))
+    q = _normal((N, S, H, K), gen, dtype=dtype)
+    k = _normal((N, S, H, K), gen, dtype=dtype)
+    v = _normal((N, S, H, V), gen, dtype=dtype)
+    g = decay_uniform((N, S, H, K), gen, *g_range)
+    beta = _beta((N, S, H), gen)
+    return dict(q=q, k=k, v=v, g=g, beta=beta)
 
 
 # ---- the named workloads ---------------------------------------------------

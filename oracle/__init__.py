@@ -28,6 +28,10 @@ recurrence.
 ``output_gate_norm`` is the model's output epilogue (RMSNorm over the value
 dim, its weight, times sigmoid of the output gate; ``_project_out``).
 
+``multi_step`` is speculative decode with a verify width of S tokens per
+sequence: per-token state slots, and the initial state picked by the number of
+tokens accepted in the previous step.
+
 ``step`` is one decode token of the recurrence on rows of a state pool picked
 by slot indices (the model file's ``_decode_gdr`` / ``_decode_fused_kda``
 semantics: the pool is updated in place).
@@ -268,3 +272,33 @@ def output_gate_norm(o, gate, weight, eps):
     x = _f64(o)
     r = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + float(eps))
     return x * r * _f64(weight) * _sigmoid(_f64(gate))
+
+
+def multi_step(q, k, v, g, beta, pool, state_indices, num_accepted=None, scale=None):
+    """Speculative (multi-token) decode on a state pool, as the model's
+    ``_decode_fused_kda`` / ``_decode_gdr`` call it with a verify width S
+    (``ssm_state_indices`` of batch x S entries, ``num_accepted_tokens``).
+    Reading of the call: sequence n starts from slot
+    state_indices[n, num_accepted[n] - 1] (from state_indices[n, 0] when
+    num_accepted is None), runs its S tokens in order through the
+    recurrence, and the state after token t is written to slot
+    state_indices[n, t].
+
+    q, k, g [N, S, H, K]; v [N, S, H, V]; beta [N, S, H]; pool [slots, H, K, V]
+    (oracle orientation); state_indices [N, S]; num_accepted [N] or None.
+    Returns (o [N, S, H, V], new pool), fp64."""
+    q, k, v, g, b = (_f64(t) for t in (q, k, v, g, beta))
+    idx = np.asarray(state_indices, dtype=np.int64)
+    N, S = idx.shape
+    out_pool = _f64(pool).copy()
+    o = np.zeros(v.shape, dtype=np.float64)
+    for n in range(N):
+        a = 1 if num_accepted is None else int(num_accepted[n])
+        state = out_pool[idx[n, a - 1]].copy()
+        for t in range(S):
+            o_t, s_t = recurrence(q[n, t:t + 1], k[n, t:t + 1], v[n, t:t + 1], g[n, t:t + 1],
+                                  b[n, t:t + 1], initial_state=state[None], scale=scale)
+            o[n, t] = o_t[0]
+            state = s_t[0]
+            out_pool[idx[n, t]] = state
+    return o, out_pool

@@ -410,3 +410,49 @@ def test_output_norm_rows_are_independent():
     mask = np.ones((4, 2), bool)
     mask[2, 1] = False
     np.testing.assert_array_equal(a[mask], b[mask])
+
+
+# ---------------------------------------------------------------------------
+# speculative (multi-token) decode
+# ---------------------------------------------------------------------------
+
+def _multi_inputs(rng, N, S, H, K, V):
+    q = rng.standard_normal((N, S, H, K))
+    k = rng.standard_normal((N, S, H, K))
+    v = rng.standard_normal((N, S, H, V))
+    g = -rng.uniform(0.01, 0.5, (N, S, H, K))
+    b = rng.uniform(0.1, 0.9, (N, S, H))
+    return q, k, v, g, b
+
+
+def test_multi_step_with_one_token_is_the_step():
+    rng = np.random.default_rng(41)
+    N, H, K, V, slots = 3, 2, 6, 5, 6
+    q, k, v, g, b = _multi_inputs(rng, N, 1, H, K, V)
+    pool = rng.standard_normal((slots, H, K, V))
+    idx = np.array([[4], [0], [2]])
+    o, new = oracle.multi_step(q, k, v, g, b, pool, idx)
+    o1, new1 = oracle.step(q[:, 0], k[:, 0], v[:, 0], g[:, 0], b[:, 0], pool, state_indices=idx[:, 0])
+    np.testing.assert_allclose(o[:, 0], o1, rtol=1e-13)
+    np.testing.assert_allclose(new, new1, rtol=1e-13)
+
+
+def test_multi_step_writes_every_prefix_state_and_reads_the_accepted_slot():
+    """Slot idx[n, t] receives the recurrence over tokens 0..t, started from
+    slot idx[n, a - 1]; outputs are the recurrence's; other slots untouched."""
+    rng = np.random.default_rng(42)
+    N, S, H, K, V, slots = 2, 4, 2, 5, 3, 12
+    q, k, v, g, b = _multi_inputs(rng, N, S, H, K, V)
+    pool = rng.standard_normal((slots, H, K, V))
+    idx = np.array([[3, 7, 1, 9], [10, 2, 5, 0]])
+    acc = np.array([3, 1])
+    o, new = oracle.multi_step(q, k, v, g, b, pool, idx, num_accepted=acc)
+    for n in range(N):
+        s0 = pool[idx[n, acc[n] - 1]]
+        for t in range(S):
+            o_r, s_r = oracle.recurrence(q[n, :t + 1], k[n, :t + 1], v[n, :t + 1], g[n, :t + 1],
+                                         b[n, :t + 1], initial_state=s0[None])
+            np.testing.assert_allclose(new[idx[n, t]], s_r[0], rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(o[n, t], o_r[t], rtol=1e-12, atol=1e-13)
+    untouched = [s for s in range(slots) if s not in idx]
+    np.testing.assert_array_equal(new[untouched], pool[untouched])
