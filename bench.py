@@ -484,14 +484,53 @@ def run_decode(args, kda, dev, stream, pk, ws):
         gev[t][1].record(stream)
     torch.cuda.synchronize()
     gus = statistics.median([a.elapsed_time(b) * 1e3 for a, b in gev])
+    del gd, gtoks
+    spec = run_spec_decode(kda, dev, stream, pk)
     return {"workload": "decode_256", "us_per_step": round(med, 2),
-            "gated_epilogue_us_per_step": round(gus, 2),
+            "gated_epilogue_us_per_step": round(gus, 2), "speculative": spec,
             "us_min": round(min(us), 2), "tokens_per_s": round(DEC_N * ws / (med * 1e-6), 1),
             "steps": DEC_STEPS, "launches": DEC_STEPS * KERNELS_PER_DECODE,
             "roofline": {"kernel": "recurrent_step_kernel", "bound": "hbm",
                          "algorithmic_bytes": nbytes, "achieved": round(gbs, 1),
                          "peak": pk["hbm"], "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
                          "traffic": traffic_from_profiles("recurrent_step_kernel")}}
+
+
+def run_spec_decode(kda, dev, stream, pk, S=4, steps=16):
+    """Speculative decode with a verify width of S: 256 sequences x 32 heads,
+    S draft tokens each, per-token slots in a pool of 256 S slots, accepted
+    counts cycling 1..S.  The state is read once and written S times."""
+    slots = DEC_N * S
+    pool = kda_inputs.decode_pool(slots, H=H, seed=73).to(dev)
+    idx = torch.arange(slots, dtype=torch.int32, device=dev).view(DEC_N, S)
+    acc = (torch.arange(DEC_N, dtype=torch.int32, device=dev) % S) + 1
+    toks = [{n: t.to(dev) for n, t in kda_inputs.spec_tokens(DEC_N, S, H=H, seed=73, step=i).items()}
+            for i in range(4)]
+    o = torch.empty((DEC_N, S, H, V), dtype=torch.bfloat16, device=dev)
+
+    def one(i):
+        t = toks[i % len(toks)]
+        kda.kda_recurrent_multi_step(t["q"], t["k"], t["v"], t["g"], t["beta"], pool, idx,
+                                     num_accepted=acc, o=o, stream=stream)
+
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for i in range(steps):
+        evs[i][0].record(stream)
+        one(i)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    us = statistics.median([a.elapsed_time(b) * 1e3 for a, b in evs])
+    nbytes = (1 + S) * DEC_N * H * V * K * 4 + S * DEC_N * H * (3 * K * 2 + K * 4 + 4 + V * 2)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    del pool
+    return {"verify_width": S, "us_per_step": round(us, 2),
+            "tokens_per_s": round(DEC_N * S / (us * 1e-6), 1),
+            "roofline": {"bound": "hbm", "algorithmic_bytes": nbytes, "achieved": round(gbs, 1),
+                         "peak": pk["hbm"], "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4)}}
 
 
 # ---- the oracle as the CPU baseline / reference arm ------------------------

@@ -239,6 +239,30 @@ int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const flo
                           int K, int V, float scale, int dtype, int flags, void *stream);
 
 /*
+ * Speculative (multi-token) decode: S tokens per sequence run in order
+ * through the recurrence (the model's decode call with a verify width S:
+ * model file, _decode_fused_kda / _decode_gdr with ssm_state_indices of
+ * batch x S entries and num_accepted_tokens).
+ *
+ *   q, k, g       [N, S, H, K]   v, o [N, S, H, V]   beta [N, S, H]
+ *   state_indices device int32 [N, S]: the state after token t of sequence
+ *                 n is written to slot state_indices[n][t]
+ *   num_accepted  device int32 [N] or NULL: sequence n starts from slot
+ *                 state_indices[n][num_accepted[n] - 1] (NULL: from
+ *                 state_indices[n][0]), the state left by the previous
+ *                 verify step after its last accepted token
+ *
+ * A sequence with a slot outside [0, n_slots) or num_accepted outside
+ * [1, S] leaves the pool untouched and gets NaN outputs.  Slots of
+ * different sequences must not overlap.  S = 1 with num_accepted = NULL is
+ * kda_recurrent_step.  The state is read once and written S times.
+ */
+int kda_recurrent_multi_step(const void *q, const void *k, const void *v, const float *g,
+                             const float *beta, float *state_pool, const int32_t *state_indices,
+                             const int32_t *num_accepted, int64_t n_slots, void *o, int N, int S,
+                             int H, int K, int V, float scale, int dtype, void *stream);
+
+/*
  * Gated entry points: the model's gate activation computed in-kernel
  * (Ascend model file, _prefill_torch_kda and the decode branch of
  * KimiDeltaAttention.forward).  Instead of activated g and beta they take

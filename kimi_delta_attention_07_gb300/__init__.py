@@ -32,7 +32,7 @@ CHUNK = 64
 EXPORTS = ("kda_status_string", "kda_version", "kda_chunk_workspace_bytes", "kda_chunk_fwd",
            "kda_chunk_intra", "kda_chunk_scan", "kda_workspace_status", "kda_recurrent_step",
            "kda_chunk_fwd_noalloc", "kda_chunk_fwd_gated", "kda_recurrent_step_gated",
-           "kda_output_gate_norm")
+           "kda_output_gate_norm", "kda_recurrent_multi_step")
 NOALLOC_WORKSPACE_BYTES = 64 * 1024 * 1024
 
 _lib = None
@@ -88,6 +88,9 @@ def load(path: str | None = None):
         L.kda_recurrent_step_gated.restype = i32
         L.kda_output_gate_norm.argtypes = [vp, vp, vp, f32, i64, i32, i32, vp]
         L.kda_output_gate_norm.restype = i32
+        L.kda_recurrent_multi_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, vp, i32, i32,
+                                               i32, i32, i32, f32, i32, vp]
+        L.kda_recurrent_multi_step.restype = i32
         _lib = L
         return L
 
@@ -322,6 +325,41 @@ def kda_recurrent_step(q, k, v, g, beta, state_pool, *, state_indices=None, scal
                                    float(scale), dt, _stream(stream))
     if st != KDA_OK:
         raise KdaError(st, "kda_recurrent_step")
+    return o
+
+
+def kda_recurrent_multi_step(q, k, v, g, beta, state_pool, state_indices, *, num_accepted=None,
+                             scale=None, o=None, stream=None):
+    """Speculative decode: S tokens per sequence through the recurrence.
+
+    q, k, g [N, S, H, K]; v [N, S, H, V]; beta [N, S, H]; state_indices int32
+    [N, S] (the state after token t goes to slot state_indices[n, t]);
+    num_accepted int32 [N] or None (start from slot state_indices[n, a - 1],
+    else [n, 0]).  Updates state_pool in place; returns o [N, S, H, V].
+    """
+    N, S, H, K = q.shape
+    V = v.shape[-1]
+    dt = _dtype_code(q)
+    for name, t, dtype_, shape in (("q", q, q.dtype, (N, S, H, K)), ("k", k, q.dtype, (N, S, H, K)),
+                                   ("v", v, q.dtype, (N, S, H, V)),
+                                   ("g", g, torch.float32, (N, S, H, K)),
+                                   ("beta", beta, torch.float32, (N, S, H)),
+                                   ("state_pool", state_pool, torch.float32, None),
+                                   ("state_indices", state_indices, torch.int32, (N, S)),
+                                   ("num_accepted", num_accepted, torch.int32, (N,))):
+        _check(t, name, dtype_, shape)
+    if state_pool.dim() != 4 or tuple(state_pool.shape[1:]) != (H, V, K):
+        raise ValueError(f"state_pool must be [slots, {H}, {V}, {K}]")
+    if o is None:
+        o = torch.empty((N, S, H, V), dtype=q.dtype, device=q.device)
+    _check(o, "o", q.dtype, (N, S, H, V))
+    if scale is None:
+        scale = K ** -0.5
+    st = load().kda_recurrent_multi_step(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(state_pool),
+                                         _p(state_indices), _p(num_accepted), state_pool.shape[0],
+                                         _p(o), N, S, H, K, V, float(scale), dt, _stream(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_recurrent_multi_step")
     return o
 
 

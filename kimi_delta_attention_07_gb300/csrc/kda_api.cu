@@ -202,13 +202,15 @@ int kda_workspace_status(const void *workspace, int *flags_out, void *stream) {
 namespace {
 int step_call(const void *q, const void *k, const void *v, const float *g, const float *beta,
               const GateArgs *gate, const EpiArgs *epi, float *state_pool,
-              const int32_t *state_indices,
+              const int32_t *state_indices, const int32_t *num_accepted, int S,
               int64_t n_slots, void *o, int N, int H, int K, int V, float scale, int dtype,
               void *stream) {
-    if (!valid_dtype(dtype) || N < 0 || H <= 0 || K <= 0 || V <= 0 || n_slots < 0)
+    if (!valid_dtype(dtype) || N < 0 || S < 1 || H <= 0 || K <= 0 || V <= 0 || n_slots < 0)
         return KDA_ERR_INVALID_ARG;
     if (K != kHeadDim || V != kHeadDim) return KDA_ERR_UNSUPPORTED;
     if (N == 0) return KDA_OK;
+    if (S > 1 && !state_indices) return KDA_ERR_INVALID_ARG;  // per-token slots are required
+    if ((int64_t)N * S * H > INT32_MAX) return KDA_ERR_INVALID_ARG;
     if (gate) {
         if (!gate->raw_gate || !gate->raw_beta || !gate->a_log || !gate->dt_bias ||
             !aligned(gate->raw_gate, 4 * elem_bytes(dtype)) ||
@@ -230,9 +232,9 @@ int step_call(const void *q, const void *k, const void *v, const float *g, const
         return KDA_ERR_INVALID_ARG;
     if (!isfinite(scale)) return KDA_ERR_INVALID_ARG;
     cudaGetLastError();
-    const cudaError_t e = launch_recurrent_step(q, k, v, g, beta, gate, epi, state_pool, state_indices,
-                                                n_slots, o, N, H, scale, dtype,
-                                                (cudaStream_t)stream);
+    const cudaError_t e = launch_recurrent_step(q, k, v, g, beta, gate, epi, state_pool,
+                                                state_indices, num_accepted, n_slots, o, N, S, H,
+                                                scale, dtype, (cudaStream_t)stream);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return KDA_ERR_CUDA;
@@ -245,8 +247,16 @@ int kda_recurrent_step(const void *q, const void *k, const void *v, const float 
                        const float *beta, float *state_pool, const int32_t *state_indices,
                        int64_t n_slots, void *o, int N, int H, int K, int V, float scale,
                        int dtype, void *stream) {
-    return step_call(q, k, v, g, beta, nullptr, nullptr, state_pool, state_indices, n_slots, o, N,
-                     H, K, V, scale, dtype, stream);
+    return step_call(q, k, v, g, beta, nullptr, nullptr, state_pool, state_indices, nullptr, 1,
+                     n_slots, o, N, H, K, V, scale, dtype, stream);
+}
+
+int kda_recurrent_multi_step(const void *q, const void *k, const void *v, const float *g,
+                             const float *beta, float *state_pool, const int32_t *state_indices,
+                             const int32_t *num_accepted, int64_t n_slots, void *o, int N, int S,
+                             int H, int K, int V, float scale, int dtype, void *stream) {
+    return step_call(q, k, v, g, beta, nullptr, nullptr, state_pool, state_indices, num_accepted,
+                     S, n_slots, o, N, H, K, V, scale, dtype, stream);
 }
 
 int kda_recurrent_step_gated(const void *q, const void *k, const void *v, const void *raw_gate,
@@ -257,8 +267,8 @@ int kda_recurrent_step_gated(const void *q, const void *k, const void *v, const 
                              int H, int K, int V, float scale, int dtype, void *stream) {
     const GateArgs gate{raw_gate, raw_beta, a_log, dt_bias, lower_bound, use_lower_bound != 0};
     const EpiArgs epi{out_gate, norm_weight, norm_eps};
-    return step_call(q, k, v, nullptr, nullptr, &gate, &epi, state_pool, state_indices, n_slots, o,
-                     N, H, K, V, scale, dtype, stream);
+    return step_call(q, k, v, nullptr, nullptr, &gate, &epi, state_pool, state_indices, nullptr, 1,
+                     n_slots, o, N, H, K, V, scale, dtype, stream);
 }
 
 int kda_output_gate_norm(void *o, const void *gate, const float *weight, float eps,

@@ -30,6 +30,7 @@ constexpr int kDecodeThreads = 256;  // 8 warps
 constexpr int kWarps = kDecodeThreads / 32;
 constexpr int kMaxRowsPerWarp = kHeadDim / kWarps;  // 16: a whole head per CTA
 
+// One token per sequence (the common decode step).
 template <typename T, bool GATED, bool EPI>
 __global__ void __launch_bounds__(kDecodeThreads)
     recurrent_step_kernel(const T *__restrict__ q, const T *__restrict__ k,
@@ -138,41 +139,205 @@ __global__ void __launch_bounds__(kDecodeThreads)
     }
 }
 
+// Speculative decode: S tokens per sequence, per-token destination slots,
+// the starting slot picked by the accepted count (see launch_recurrent_step).
+template <typename T, bool GATED, bool EPI>
+__global__ void __launch_bounds__(kDecodeThreads)
+    recurrent_multi_step_kernel(const T *__restrict__ q, const T *__restrict__ k,
+                                const T *__restrict__ v, const float *__restrict__ g,
+                                const float *__restrict__ beta, const GateArgs gate,
+                                const EpiArgs epi, float *__restrict__ pool,
+                                const int32_t *__restrict__ state_indices,
+                                const int32_t *__restrict__ num_accepted, int64_t n_slots,
+                                T *__restrict__ o, int S, int H, int rows_per_cta, float scale) {
+    __shared__ float s_part[kWarps];  // epilogue: per-warp sums of o^2
+    const int pair = blockIdx.x;  // n * H + h
+    const int n = pair / H;
+    const int h = pair - n * H;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int row0 = blockIdx.y * rows_per_cta;
+    const int rpw = rows_per_cta / kWarps;  // rows of this warp: row0 + warp + 8 j
+    // token t of sequence n, head h: q/k/g/v/o rows at ((n S + t) H + h) * K
+    auto io_of = [&](int t) { return ((int64_t)(n * S + t) * H + h) * kHeadDim; };
+    auto slot_of = [&](int t) {  // the slot the state after token t goes to
+        return state_indices ? (int64_t)state_indices[(int64_t)n * S + t] : (int64_t)n;
+    };
+
+    // Every slot of the sequence, and the number of accepted tokens, is checked
+    // before anything is written.
+    const int acc = num_accepted ? num_accepted[n] : 1;
+    bool valid = acc >= 1 && acc <= S;
+    for (int t = 0; t < S && valid; ++t) {
+        const int64_t sl = slot_of(t);
+        valid = sl >= 0 && sl < n_slots;
+    }
+    if (!valid) {
+        // the pool is not touched and this head's outputs are NaN
+        for (int t = 0; t < S; ++t)
+            for (int r = threadIdx.x; r < rows_per_cta; r += kDecodeThreads)
+                o[io_of(t) + row0 + r] = from_f32<T>(__int_as_float(0x7fc00000));
+        return;
+    }
+    const int64_t slot_in = slot_of(acc - 1);
+
+    // This warp's state rows are requested first, so that their latency
+    // overlaps the setup below; they stay in registers across the tokens.
+    const float *S0 = pool + ((slot_in * H + h) * (int64_t)kHeadDim) * kHeadDim;  // [V][K]
+    float4 s[kMaxRowsPerWarp];
+#pragma unroll
+    for (int j = 0; j < kMaxRowsPerWarp; ++j)
+        if (j < rpw)
+            s[j] = *reinterpret_cast<const float4 *>(S0 + (int64_t)(row0 + warp + kWarps * j) * kHeadDim + 4 * lane);
+
+    // A token's inputs, fetched one token ahead so that their latency overlaps
+    // the previous token's row updates.
+    struct TokIn {
+        float4 q4, k4, g4;  // g4: raw gate + dt_bias when GATED, else g
+        float vrow, b;      // vrow: v of the warp's row `lane`; b: beta (raw when GATED)
+        float gate_o, w_o;  // epilogue: output gate and norm weight of row `lane`
+    };
+    auto fetch = [&](int t) {
+        TokIn in;
+        const int64_t io_k = io_of(t);
+        const int64_t pt = (int64_t)(n * S + t) * H + h;  // beta / raw beta index
+        in.vrow = lane < rpw ? to_f32(v[io_k + row0 + warp + kWarps * lane]) : 0.0f;
+        in.gate_o = 0.0f;
+        in.w_o = 0.0f;
+        if (EPI && lane < rpw) {
+            const int r = row0 + warp + kWarps * lane;
+            in.gate_o = to_f32(reinterpret_cast<const T *>(epi.out_gate)[io_k + r]);
+            in.w_o = epi.weight[r];
+        }
+        in.q4 = load4(q + io_k + 4 * lane);
+        in.k4 = load4(k + io_k + 4 * lane);
+        if (GATED) {
+            const float4 r4 = load4(reinterpret_cast<const T *>(gate.raw_gate) + io_k + 4 * lane);
+            const float4 c4 = load4(gate.dt_bias + (int64_t)h * kHeadDim + 4 * lane);
+            in.g4 = make_float4(r4.x + c4.x, r4.y + c4.y, r4.z + c4.z, r4.w + c4.w);
+            in.b = to_f32(reinterpret_cast<const T *>(gate.raw_beta)[pt]);
+        } else {
+            in.g4 = load4(g + io_k + 4 * lane);
+            in.b = beta[pt];
+        }
+        return in;
+    };
+    TokIn nxt = fetch(0);
+    for (int t = 0; t < S; ++t) {
+        const TokIn cur = nxt;
+        if (t + 1 < S) nxt = fetch(t + 1);
+        const int64_t io_k = io_of(t);
+        const float vrow = cur.vrow, gate_o = cur.gate_o, w_o = cur.w_o;
+        const float4 q4 = cur.q4, k4 = cur.k4;
+        float4 g4;
+        float b;
+        if (GATED) {
+            const float gs = expf(gate.a_log[h]);
+            const bool lb = gate.use_lower_bound != 0;
+            g4 = make_float4(gate_decay(cur.g4.x, gs, gate.lower_bound, lb),
+                             gate_decay(cur.g4.y, gs, gate.lower_bound, lb),
+                             gate_decay(cur.g4.z, gs, gate.lower_bound, lb),
+                             gate_decay(cur.g4.w, gs, gate.lower_bound, lb));
+            b = gate_beta(cur.b);
+        } else {
+            g4 = cur.g4;
+            b = cur.b;
+        }
+        const float sq = warp_sum(q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w);
+        const float sk = warp_sum(k4.x * k4.x + k4.y * k4.y + k4.z * k4.z + k4.w * k4.w);
+        const float rq = scale / sqrtf(sq + 1e-6f);
+        const float rk = 1.0f / sqrtf(sk + 1e-6f);
+        const float4 qh = make_float4(q4.x * rq, q4.y * rq, q4.z * rq, q4.w * rq);
+        const float4 kh = make_float4(k4.x * rk, k4.y * rk, k4.z * rk, k4.w * rk);
+        const float4 dec = make_float4(expf(g4.x), expf(g4.y), expf(g4.z), expf(g4.w));
+        const float kq = warp_sum(kh.x * qh.x + kh.y * qh.y + kh.z * qh.z + kh.w * qh.w);
+
+        float *Sd = pool + ((slot_of(t) * H + h) * (int64_t)kHeadDim) * kHeadDim;  // destination
+        float my_o = 0.0f, ss = 0.0f;  // epilogue: o of row `lane`, sum of o^2 over the warp's rows
+#pragma unroll
+        for (int j = 0; j < kMaxRowsPerWarp; ++j) {
+            if (j >= rpw) break;
+            const int r = row0 + warp + kWarps * j;
+            float4 x = s[j];
+            x.x *= dec.x; x.y *= dec.y; x.z *= dec.z; x.w *= dec.w;
+            float a = x.x * kh.x + x.y * kh.y + x.z * kh.z + x.w * kh.w;
+            float c = x.x * qh.x + x.y * qh.y + x.z * qh.z + x.w * qh.w;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                a += __shfl_xor_sync(0xffffffffu, a, off);
+                c += __shfl_xor_sync(0xffffffffu, c, off);
+            }
+            const float u = b * (__shfl_sync(0xffffffffu, vrow, j) - a);
+            x.x += u * kh.x; x.y += u * kh.y; x.z += u * kh.z; x.w += u * kh.w;
+            s[j] = x;
+            *reinterpret_cast<float4 *>(Sd + (int64_t)r * kHeadDim + 4 * lane) = x;
+            const float ov = c + u * kq;
+            if (EPI) {
+                ss = fmaf(ov, ov, ss);
+                if (lane == j) my_o = ov;
+            } else if (lane == 0) {
+                o[io_k + r] = from_f32<T>(ov);
+            }
+        }
+        if (EPI) {  // rows_per_cta == 128: this CTA holds the head's whole output row
+            if (lane == 0) s_part[warp] = ss;
+            __syncthreads();
+            float tot = 0.0f;
+#pragma unroll
+            for (int w2 = 0; w2 < kWarps; ++w2) tot += s_part[w2];
+            const float rn = 1.0f / sqrtf(tot * (1.0f / kHeadDim) + epi.eps);
+            if (lane < rpw)
+                o[io_k + row0 + warp + kWarps * lane] = from_f32<T>(my_o * rn * w_o * gate_beta(gate_o));
+            __syncthreads();  // s_part is rewritten by the next token
+        }
+    }
+}
+
 }  // namespace
 
-template <typename T, bool GATED>
-void launch_step2(bool epi_on, dim3 grid, const void *q, const void *k, const void *v,
-                  const float *g, const float *beta, const GateArgs &gate, const EpiArgs &epi,
-                  float *pool, const int32_t *state_indices, int64_t n_slots, void *o, int H,
-                  int rows, float scale, cudaStream_t stream) {
-    if (epi_on)
-        recurrent_step_kernel<T, GATED, true><<<grid, kDecodeThreads, 0, stream>>>(
-            (const T *)q, (const T *)k, (const T *)v, g, beta, gate, epi, pool, state_indices,
-            n_slots, (T *)o, H, rows, scale);
+struct StepLaunch {
+    dim3 grid;
+    const void *q, *k, *v;
+    const float *g, *beta;
+    GateArgs gate;
+    EpiArgs epi;
+    float *pool;
+    const int32_t *state_indices, *num_accepted;
+    int64_t n_slots;
+    void *o;
+    int S, H, rows;
+    float scale;
+    cudaStream_t stream;
+};
+
+template <typename T, bool GATED, bool EPI>
+void launch_step3(const StepLaunch &a) {
+    if (a.S == 1 && !a.num_accepted)
+        recurrent_step_kernel<T, GATED, EPI><<<a.grid, kDecodeThreads, 0, a.stream>>>(
+            (const T *)a.q, (const T *)a.k, (const T *)a.v, a.g, a.beta, a.gate, a.epi, a.pool,
+            a.state_indices, a.n_slots, (T *)a.o, a.H, a.rows, a.scale);
     else
-        recurrent_step_kernel<T, GATED, false><<<grid, kDecodeThreads, 0, stream>>>(
-            (const T *)q, (const T *)k, (const T *)v, g, beta, gate, epi, pool, state_indices,
-            n_slots, (T *)o, H, rows, scale);
+        recurrent_multi_step_kernel<T, GATED, EPI><<<a.grid, kDecodeThreads, 0, a.stream>>>(
+            (const T *)a.q, (const T *)a.k, (const T *)a.v, a.g, a.beta, a.gate, a.epi, a.pool,
+            a.state_indices, a.num_accepted, a.n_slots, (T *)a.o, a.S, a.H, a.rows, a.scale);
 }
 
 template <typename T>
-void launch_step(bool gated, bool epi_on, dim3 grid, const void *q, const void *k,
-                 const void *v, const float *g, const float *beta, const GateArgs &gate,
-                 const EpiArgs &epi, float *pool, const int32_t *state_indices, int64_t n_slots,
-                 void *o, int H, int rows, float scale, cudaStream_t stream) {
-    if (gated)
-        launch_step2<T, true>(epi_on, grid, q, k, v, g, beta, gate, epi, pool, state_indices,
-                              n_slots, o, H, rows, scale, stream);
-    else
-        launch_step2<T, false>(epi_on, grid, q, k, v, g, beta, gate, epi, pool, state_indices,
-                               n_slots, o, H, rows, scale, stream);
+void launch_step(bool gated, bool epi_on, const StepLaunch &a) {
+    if (gated) {
+        if (epi_on) launch_step3<T, true, true>(a);
+        else launch_step3<T, true, false>(a);
+    } else {
+        if (epi_on) launch_step3<T, false, true>(a);
+        else launch_step3<T, false, false>(a);
+    }
 }
 
 cudaError_t launch_recurrent_step(const void *q, const void *k, const void *v, const float *g,
                                   const float *beta, const GateArgs *gate, const EpiArgs *epi,
-                                  float *pool, const int32_t *state_indices, int64_t n_slots,
-                                  void *o, int N, int H, float scale, int dtype,
-                                  cudaStream_t stream) {
+                                  float *pool, const int32_t *state_indices,
+                                  const int32_t *num_accepted, int64_t n_slots, void *o, int N,
+                                  int S, int H, float scale, int dtype, cudaStream_t stream) {
     const int64_t pairs = (int64_t)N * H;
     // Split a head's 128 rows over more CTAs when there are few heads in flight,
     // so that at least ~4 CTAs per SM are resident.
@@ -180,18 +345,22 @@ cudaError_t launch_recurrent_step(const void *q, const void *k, const void *v, c
     const bool epi_on = epi && epi->out_gate;
     while (!epi_on && rows > 16 && pairs * (kHeadDim / rows) < 152 * 8) rows >>= 1;
     const dim3 grid((unsigned)pairs, kHeadDim / rows);
-    GateArgs ga;
-    memset(&ga, 0, sizeof(ga));
-    if (gate) ga = *gate;
-    EpiArgs ea;
-    memset(&ea, 0, sizeof(ea));
-    if (epi_on) ea = *epi;
-    if (dtype == KDA_BF16)
-        launch_step<__nv_bfloat16>(gate != nullptr, epi_on, grid, q, k, v, g, beta, ga, ea, pool,
-                                   state_indices, n_slots, o, H, rows, scale, stream);
-    else
-        launch_step<float>(gate != nullptr, epi_on, grid, q, k, v, g, beta, ga, ea, pool,
-                           state_indices, n_slots, o, H, rows, scale, stream);
+    StepLaunch a;
+    memset(&a, 0, sizeof(a));
+    a.grid = grid;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+    if (gate) a.gate = *gate;
+    if (epi_on) a.epi = *epi;
+    a.pool = pool;
+    a.state_indices = state_indices;
+    a.num_accepted = num_accepted;
+    a.n_slots = n_slots;
+    a.o = o;
+    a.S = S; a.H = H; a.rows = rows;
+    a.scale = scale;
+    a.stream = stream;
+    if (dtype == KDA_BF16) launch_step<__nv_bfloat16>(gate != nullptr, epi_on, a);
+    else launch_step<float>(gate != nullptr, epi_on, a);
     return cudaGetLastError();
 }
 

@@ -208,11 +208,15 @@ __device__ __forceinline__ int owner_of_chunk(const int32_t *chunk_off, int n_se
 // gate == nullptr: g, beta are activated fp32; otherwise raw gates (*gate).
 // epi == nullptr (or epi->out_gate == nullptr): plain o; otherwise the output
 // epilogue is applied in the step.
+// S tokens per sequence (q/k/g/v/o [N, S, H, *], beta [N, S, H]); the state
+// after token t goes to slot state_indices[n S + t], the initial state comes
+// from slot state_indices[n S + num_accepted[n] - 1] (num_accepted == nullptr:
+// token 0's slot; state_indices == nullptr with S == 1: slot n).
 cudaError_t launch_recurrent_step(const void *q, const void *k, const void *v, const float *g,
                                   const float *beta, const GateArgs *gate, const EpiArgs *epi,
-                                  float *pool, const int32_t *state_indices, int64_t n_slots,
-                                  void *o, int N, int H, float scale, int dtype,
-                                  cudaStream_t stream);
+                                  float *pool, const int32_t *state_indices,
+                                  const int32_t *num_accepted, int64_t n_slots, void *o, int N,
+                                  int S, int H, float scale, int dtype, cudaStream_t stream);
 
 // The output epilogue in place on o [rows, 128].
 cudaError_t launch_output_gate_norm(void *o, const EpiArgs &epi, int64_t rows, int dtype,

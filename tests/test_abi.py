@@ -161,6 +161,28 @@ def test_output_gate_norm_rejects_bad_arguments_without_launching(lib):
     assert f(dt=kda.KDA_F32, g=base + 8) == kda.KDA_ERR_INVALID_ARG
 
 
+def test_multi_step_rejects_bad_arguments_without_launching(lib):
+    base = 1 << 20
+    vp = ctypes.c_void_p
+    p = lambda x: None if x is None else vp(x)
+
+    def f(**kw):
+        a = dict(q=base, k=base, v=base, g=base, b=base, pool=base, idx=base, acc=None, slots=8,
+                 o=base, N=2, S=3, H=2, dt=kda.KDA_BF16)
+        a.update(kw)
+        return lib.kda_recurrent_multi_step(p(a["q"]), p(a["k"]), p(a["v"]), p(a["g"]), p(a["b"]),
+                                            p(a["pool"]), p(a["idx"]), p(a["acc"]), a["slots"],
+                                            p(a["o"]), a["N"], a["S"], a["H"], 128, 128, 0.1, a["dt"],
+                                            None)
+
+    assert f(N=0) == kda.KDA_OK
+    assert f(S=0) == kda.KDA_ERR_INVALID_ARG
+    assert f(idx=None) == kda.KDA_ERR_INVALID_ARG       # per-token slots are required for S > 1
+    assert f(pool=None) == kda.KDA_ERR_INVALID_ARG
+    assert f(g=base + 4) == kda.KDA_ERR_INVALID_ARG
+    assert f(dt=2) == kda.KDA_ERR_INVALID_ARG
+
+
 def test_recurrent_step_rejects_bad_arguments_without_launching(lib):
     base = 1 << 20
     vp = ctypes.c_void_p

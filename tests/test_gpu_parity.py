@@ -540,3 +540,71 @@ def test_output_gate_norm_standalone(kda, dtype):
     torch.cuda.synchronize()
     ref = oracle.output_gate_norm(o, gate, w, 1e-5)
     assert rel_l2(to_np(od), ref) < (1e-6 if dtype == torch.float32 else 5e-3)
+
+
+# ---------------------------------------------------------------------------
+# speculative (multi-token) decode
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_multi_step_matches_oracle(kda, dtype):
+    """Four sequences, S = 3 draft tokens, per-token slots, accepted counts
+    1..3 picking the starting slot; one sequence with an invalid count gets NaN
+    outputs and leaves its slots alone."""
+    N, S, H, slots = 4, 3, 2, 16
+    tok = kda_inputs.spec_tokens(N, S, H=H, dtype=dtype, seed=71)
+    pool = kda_inputs.decode_pool(slots, H=H, seed=71)
+    idx = torch.tensor([[3, 8, 1], [0, 5, 12], [7, 2, 9], [4, 6, 10]], dtype=torch.int32)
+    acc = torch.tensor([2, 1, 3, 0], dtype=torch.int32)  # sequence 3: invalid (0 accepted)
+    pool_d = pool.cuda()
+    o = kda.kda_recurrent_multi_step(*(tok[n].cuda() for n in ("q", "k", "v", "g", "beta")), pool_d,
+                                     idx.cuda(), num_accepted=acc.cuda())
+    torch.cuda.synchronize()
+    good = [0, 1, 2]
+    p0 = np.swapaxes(pool.double().numpy(), -1, -2)
+    o_ref, pool_ref = oracle.multi_step(*(tok[n][good] for n in ("q", "k", "v", "g", "beta")), p0,
+                                        idx.numpy()[good], num_accepted=acc.numpy()[good])
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    assert rel_l2(to_np(o[good]), o_ref) < tol
+    assert rel_l2(vk_to_kv(pool_d), pool_ref) < TOL_F32
+    assert torch.isnan(o[3].float()).all()
+    bad_slots = idx[3].tolist()
+    assert torch.equal(pool_d.cpu()[bad_slots], pool[bad_slots])
+
+
+def test_multi_step_with_one_token_equals_the_step(kda):
+    N, H = 5, 3
+    tok = kda_inputs.decode_tokens(N, H=H, seed=72)
+    pool = kda_inputs.decode_pool(8, H=H, seed=72)
+    idx = torch.tensor([6, 1, 3, 0, 7], dtype=torch.int32)
+    p1, p2 = pool.cuda(), pool.cuda()
+    o1 = kda.kda_recurrent_step(*(tok[n].cuda() for n in ("q", "k", "v", "g", "beta")), p1,
+                                state_indices=idx.cuda())
+    o2 = kda.kda_recurrent_multi_step(*(tok[n].unsqueeze(1).cuda() for n in ("q", "k", "v", "g", "beta")),
+                                      p2, idx.view(N, 1).cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2[:, 0]) and torch.equal(p1, p2)
+
+
+def test_multi_step_decode_256_verify_width_4_sampled(kda):
+    """The 256 x 32 decode pool with a verify width of 4 (4 draft tokens per
+    sequence, per-token slots in a 4x larger pool, accepted counts 1..4)."""
+    N, S, H = 256, 4, 32
+    slots = N * S
+    pool = kda_inputs.decode_pool(slots, H=H, seed=73)
+    tok = kda_inputs.spec_tokens(N, S, H=H, seed=73)
+    idx = torch.arange(slots, dtype=torch.int32).view(N, S)
+    acc = (torch.arange(N, dtype=torch.int32) % S) + 1
+    pool_d = pool.cuda()
+    o = kda.kda_recurrent_multi_step(*(tok[n].cuda() for n in ("q", "k", "v", "g", "beta")), pool_d,
+                                     idx.cuda(), num_accepted=acc.cuda())
+    torch.cuda.synchronize()
+    seqs, heads = [0, 129, 255], [5, 30]
+    sub = {n: tok[n][seqs][:, :, heads] for n in ("q", "k", "v", "g", "beta")}
+    p0 = np.swapaxes(pool[:, heads].double().numpy(), -1, -2)
+    o_ref, pool_ref = oracle.multi_step(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], p0,
+                                        idx.numpy()[seqs], num_accepted=acc.numpy()[seqs])
+    assert rel_l2(to_np(o[seqs][:, :, heads]), o_ref) < TOL_BF16
+    touched = idx.numpy()[seqs].ravel()
+    assert rel_l2(vk_to_kv(pool_d[touched][:, heads]), pool_ref[touched]) < TOL_F32
+    assert torch.isfinite(o).all()
