@@ -29,6 +29,8 @@ Gated variants (the model's raw gates; the library activates them in-kernel):
                     dt_bias ~ U[-1, 1], lower bound -5                       [5]
 Speculative decode: S draft tokens per sequence, q, k, g [N, S, H, K],
 v [N, S, H, V], beta [N, S, H], drawn like decode tokens.
+Short convolution: x [T, D = 3 H K] ~ N(0, 1), weight [ks = 4, D] ~ U[-1/2, 1/2]
+(bf16 unless given); decode conv states [slots, ks - 1, D] ~ N(0, 1).
 Output epilogue inputs: out_gate [T, H, V] ~ N(0, 1) in the q dtype, o_norm
 weight [V] ~ U[0.5, 1.5] fp32, eps 1e-5.
 """
@@ -164,6 +166,19 @@ def spec_tokens(N, S, H=32, K=K_DIM, V=V_DIM, dtype=torch.bfloat16, seed=7, step
     g = decay_uniform((N, S, H, K), gen, *g_range)
     beta = _beta((N, S, H), gen)
     return dict(q=q, k=k, v=v, g=g, beta=beta)
+
+
+def conv_inputs(lengths, D=3 * 32 * K_DIM, ks=4, dtype=torch.bfloat16, seed=8):
+    """Short-conv inputs: x [T, D] ~ N(0, 1) (the fused q/k/v projection, D =
+    3 H K), weight [ks, D] ~ U[-1/2, 1/2] (the model's kaiming-uniform bound for
+    a fan-in of ks = 4), cu_seqlens [N+1] int32."""
+    lengths = [int(t) for t in lengths]
+    gen = _gen(seed * 31 + 17)
+    x = _normal((sum(lengths), D), gen, dtype=dtype)
+    w = _uniform((ks, D), gen, -0.5, 0.5).to(dtype)
+    cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
+    return dict(x=x, weight=w, cu_seqlens=cu, lengths=lengths, ks=ks, D=D)
 
 
 # ---- the named workloads ---------------------------------------------------

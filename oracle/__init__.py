@@ -32,6 +32,10 @@ dim, its weight, times sigmoid of the output gate; ``_project_out``).
 sequence: per-token state slots, and the initial state picked by the number of
 tokens accepted in the previous step.
 
+``short_conv_prefill`` / ``short_conv_update`` are the model's depthwise causal
+short convolution on the fused q/k/v projection (``KimiShortConvolution``),
+over packed sequences and one decode token at a time, with its state cache.
+
 ``step`` is one decode token of the recurrence on rows of a state pool picked
 by slot indices (the model file's ``_decode_gdr`` / ``_decode_fused_kda``
 semantics: the pool is updated in place).
@@ -302,3 +306,53 @@ def multi_step(q, k, v, g, beta, pool, state_indices, num_accepted=None, scale=N
             state = s_t[0]
             out_pool[idx[n, t]] = state
     return o, out_pool
+
+
+def _act(y: np.ndarray, activation: str) -> np.ndarray:
+    if activation == "silu":
+        return y * _sigmoid(y)
+    if activation in (None, "none"):
+        return y
+    raise ValueError(activation)
+
+
+def short_conv_prefill(x, weight, cu_seqlens, activation="silu", initial_states=None):
+    """Depthwise causal convolution over packed sequences (Ascend model file,
+    ``KimiShortConvolution``, prefill branch: ``causal_conv1d_fn``):
+
+        y[t, d] = act( sum_{i<ks} weight[i, d] * x[t - (ks - 1) + i, d] )
+
+    where positions before the sequence start read its initial state (the
+    ks - 1 previous inputs; zeros when ``initial_states`` is None, as the model
+    passes has_initial_state = 0).  x [T, D]; weight [ks, D] (the model's
+    ``_conv_weight``); initial_states [N, ks - 1, D] or None.
+    Returns y [T, D] and the final states [N, ks - 1, D] (each sequence's last
+    ks - 1 inputs, reaching into its initial state when it is shorter), fp64."""
+    x = _f64(x)
+    w = _f64(weight)
+    ks, D = w.shape
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    N = len(cu) - 1
+    y = np.zeros_like(x)
+    finals = np.zeros((N, ks - 1, D))
+    for n in range(N):
+        s, e = cu[n], cu[n + 1]
+        init = np.zeros((ks - 1, D)) if initial_states is None else _f64(initial_states)[n]
+        ext = np.concatenate([init, x[s:e]], axis=0)  # rows: ks - 1 history, then the sequence
+        for t in range(e - s):
+            y[s + t] = _act(np.sum(w * ext[t:t + ks], axis=0), activation)
+        finals[n] = ext[len(ext) - (ks - 1):]
+    return y, finals
+
+
+def short_conv_update(x, weight, state, activation="silu"):
+    """One decode token per sequence (the update branch:
+    ``causal_conv1d_update``): y[n, d] = act(sum_i weight[i, d] * window[i, d])
+    with window = [state[n] ; x[n]], and the state shifts by one token.
+    x [N, D]; weight [ks, D]; state [N, ks - 1, D].  Returns (y, new state)."""
+    x = _f64(x)
+    w = _f64(weight)
+    st = _f64(state)
+    win = np.concatenate([st, x[:, None, :]], axis=1)  # [N, ks, D]
+    y = _act(np.sum(w[None] * win, axis=1), activation)
+    return y, win[:, 1:].copy()

@@ -456,3 +456,72 @@ def test_multi_step_writes_every_prefix_state_and_reads_the_accepted_slot():
             np.testing.assert_allclose(o[n, t], o_r[t], rtol=1e-12, atol=1e-13)
     untouched = [s for s in range(slots) if s not in idx]
     np.testing.assert_array_equal(new[untouched], pool[untouched])
+
+
+# ---------------------------------------------------------------------------
+# short causal convolution (Ascend model file, KimiShortConvolution)
+# ---------------------------------------------------------------------------
+
+def test_conv_unit_tap_is_the_activation_and_shifted_taps_delay():
+    """weight = e_{ks-1} gives y = act(x); weight = e_{ks-1-j} delays x by j
+    (zeros before the sequence start); silu(x) = x sigmoid(x)."""
+    rng = np.random.default_rng(51)
+    T, D, ks = 9, 6, 4
+    x = rng.standard_normal((T, D))
+    w = np.zeros((ks, D))
+    w[ks - 1] = 1.0
+    y, _ = oracle.short_conv_prefill(x, w, [0, T], activation="silu")
+    np.testing.assert_allclose(y, x / (1.0 + np.exp(-x)), rtol=1e-14)
+    for j in range(ks):
+        w = np.zeros((ks, D))
+        w[ks - 1 - j] = 1.0
+        y, _ = oracle.short_conv_prefill(x, w, [0, T], activation="none")
+        ref = np.zeros_like(x)
+        ref[j:] = x[:T - j]
+        np.testing.assert_array_equal(y, ref)
+
+
+def test_conv_matches_numpy_convolve_per_channel():
+    """Without activation each channel is the causal part of a full 1-D
+    convolution with the reversed taps (numpy.convolve)."""
+    rng = np.random.default_rng(52)
+    T, D, ks = 13, 5, 4
+    x = rng.standard_normal((T, D))
+    w = rng.standard_normal((ks, D))
+    y, fin = oracle.short_conv_prefill(x, w, [0, T], activation="none")
+    for d in range(D):
+        np.testing.assert_allclose(y[:, d], np.convolve(x[:, d], w[::-1, d])[:T], rtol=1e-12, atol=1e-13)
+    np.testing.assert_array_equal(fin[0], x[T - (ks - 1):])
+
+
+def test_conv_sequences_are_independent_and_short_ones_keep_history():
+    rng = np.random.default_rng(53)
+    D, ks = 4, 4
+    lens = [5, 2, 0, 7]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    x = rng.standard_normal((cu[-1], D))
+    w = rng.standard_normal((ks, D))
+    init = rng.standard_normal((len(lens), ks - 1, D))
+    y, fin = oracle.short_conv_prefill(x, w, cu, initial_states=init)
+    for n, L in enumerate(lens):
+        yn, fn = oracle.short_conv_prefill(x[cu[n]:cu[n + 1]], w, [0, L], initial_states=init[n:n + 1])
+        np.testing.assert_array_equal(y[cu[n]:cu[n + 1]], yn)
+        np.testing.assert_array_equal(fin[n], fn[0])
+    np.testing.assert_array_equal(fin[2], init[2])                            # empty: unchanged
+    np.testing.assert_array_equal(fin[1], np.concatenate([init[1][2:], x[cu[1]:cu[2]]]))  # 2 < ks - 1
+
+
+def test_conv_prefill_then_updates_equal_the_longer_prefill():
+    """Prefill T1 tokens, then one update per remaining token from the final
+    state, reproduces the prefill of all T tokens (outputs and state)."""
+    rng = np.random.default_rng(54)
+    T, T1, D, ks = 11, 6, 3, 4
+    x = rng.standard_normal((T, D))
+    w = rng.standard_normal((ks, D))
+    y_all, fin_all = oracle.short_conv_prefill(x, w, [0, T])
+    y1, st = oracle.short_conv_prefill(x[:T1], w, [0, T1])
+    np.testing.assert_array_equal(y1, y_all[:T1])
+    for t in range(T1, T):
+        yt, st = oracle.short_conv_update(x[t:t + 1], w, st)
+        np.testing.assert_allclose(yt[0], y_all[t], rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(st[0], fin_all[0], rtol=0, atol=0)
