@@ -54,6 +54,7 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--precise", action="store_true", help="fp32 CUDA-core chunk path")
     p.add_argument("--no-gated", action="store_true", help="skip the raw-gate prefill sub-run")
+    p.add_argument("--no-conv", action="store_true", help="skip the short-convolution sub-run")
     return p.parse_args()
 
 
@@ -248,6 +249,81 @@ def run_gated(args, kda, dev, stream, ws):
                          "unit": "GB/s", "frac": round(byt / (ms / 1e3) / 1e9 / pk["hbm"], 4)}}
 
 
+def _graph_us(fn, n, stream, reps=5):
+    """Per-call device time of fn(0..n-1) captured in one CUDA graph and
+    replayed: no host launch gaps inside the timed region."""
+    g = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream()  # capture needs a side stream
+    cs.wait_stream(stream)
+    with torch.cuda.graph(g, stream=cs):
+        for i in range(n):
+            fn(i, cs)
+    times = []
+    with torch.cuda.stream(stream):
+        g.replay()
+        torch.cuda.synchronize()
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b) * 1e3 / n)
+    del g
+    return statistics.median(times)
+
+
+def run_conv(args, kda, dev, stream, pk):
+    """The short causal convolution on the fused q/k/v projection (D = 3 x 32
+    x 128 = 12288 channels, ks = 4, SiLU, bf16): prefill over the 4k sequence
+    (x and y 96 MiB each, above L2) and one decode update for 256 sequences,
+    rotating over 8 input/pool sets (about 250 MB) so that no step finds its
+    data in L2.  Both are timed as CUDA-graph replays of 16 / 32 calls (the
+    decode update is shorter than a host launch)."""
+    c = kda_inputs.conv_inputs([T_4K], seed=83)
+    D, ks = c["D"], c["ks"]
+    x, w, cu = c["x"].to(dev), c["weight"].to(dev), c["cu_seqlens"].to(dev)
+    y = torch.empty_like(x)
+    fin = torch.empty((1, ks - 1, D), dtype=x.dtype, device=dev)
+
+    def pre(i, st=stream):
+        kda.kda_short_conv_fwd(x, w, cu_seqlens=cu, final_states=fin, y=y, stream=st)
+
+    for i in range(3):
+        pre(i)
+    torch.cuda.synchronize()
+    us_pre = _graph_us(pre, 16, stream)
+    b_pre = 2 * T_4K * D * 2 + ks * D * 2 + (ks - 1) * D * 2
+    del x, y
+    sets = []
+    for j in range(8):
+        g = torch.Generator().manual_seed(8300 + j)
+        sets.append((torch.randn((DEC_N, D), generator=g).to(torch.bfloat16).to(dev),
+                     torch.randn((DEC_N, ks - 1, D), generator=g).to(torch.bfloat16).to(dev),
+                     torch.empty((DEC_N, D), dtype=torch.bfloat16, device=dev)))
+
+    def upd(i, st=stream):
+        xt, pool, yt = sets[i % len(sets)]
+        kda.kda_short_conv_update(xt, w, pool, y=yt, stream=st)
+
+    for i in range(8):
+        upd(i)
+    torch.cuda.synchronize()
+    us_upd = _graph_us(upd, 32, stream)
+    b_upd = DEC_N * D * 2 * 2 + 2 * DEC_N * (ks - 1) * D * 2 + ks * D * 2
+    del sets
+    roof = lambda b, us: {"bound": "hbm", "algorithmic_bytes": b,
+                          "achieved": round(b / (us * 1e-6) / 1e9, 1), "peak": pk["hbm"],
+                          "unit": "GB/s", "frac": round(b / (us * 1e-6) / 1e9 / pk["hbm"], 4)}
+    return {"workload": "short_conv_qkv", "D": D, "ks": ks, "activation": "silu", "dtype": "bf16",
+            "timing": "CUDA graph replay, per call",
+            "prefill": {"T": T_4K, "us_per_call": round(us_pre, 2), "launches_per_call": 1,
+                        "tokens_per_s": round(T_4K / (us_pre * 1e-6), 1),
+                        "roofline": roof(b_pre, us_pre)},
+            "decode_update": {"N": DEC_N, "us_per_call": round(us_upd, 2), "launches_per_call": 1,
+                              "roofline": roof(b_upd, us_upd)}}
+
+
 def decode_bytes(N, H, elem=2):
     state = 2 * N * H * V * K * 4  # read + write
     io = N * H * (2 * K * elem + V * elem + K * 4 + 4 + V * elem)
@@ -338,6 +414,7 @@ def run_ours(args, rank, ws):
     e2e = None if args.no_e2e else run_e2e(args, kda, x, dev, stream, work, flags, ws)
     dec = None if args.no_decode else run_decode(args, kda, dev, stream, pk, ws)
     gated = None if (args.no_gated or args.precise) else run_gated(args, kda, dev, stream, ws)
+    conv = None if args.no_conv else run_conv(args, kda, dev, stream, pk)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(x, sample_heads=H)
@@ -357,7 +434,7 @@ def run_ours(args, rank, ws):
                        "path": "fp32 CUDA-core (precise)" if args.precise else "default"},
             "roofline": roofline, "step_roofline": step_roofline, "kernels": kernels,
             "e2e": e2e, "gpu_launches": launches, "clocks": clk,
-            "decode": dec, "gated": gated, "cpu_baseline": cpu,
+            "decode": dec, "gated": gated, "short_conv": conv, "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
 

@@ -239,6 +239,43 @@ int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const flo
                           int K, int V, float scale, int dtype, int flags, void *stream);
 
 /*
+ * Short causal convolution of the fused q/k/v projection (model file,
+ * KimiShortConvolution: causal_conv1d_fn in prefill, causal_conv1d_update
+ * in decode).  Depthwise over D channels with ks taps (2 <= ks <= 8):
+ *   y[t, d] = act( sum_{i<ks} weight[i, d] * x[t - (ks - 1) + i, d] )
+ * where positions before a sequence's start read its conv state (its ks - 1
+ * previous inputs; zeros without an initial state).  act is SiLU
+ * (KDA_CONV_SILU, x * sigmoid(x)) or none (KDA_CONV_NONE).
+ *
+ *   x, y        [T, D] (prefill) / [N, D] (update), dtype; D % 8 == 0
+ *   weight      [ks, D] dtype (the model's conv weight, tap-major)
+ *   conv states [N or slots, ks - 1, D] dtype: per sequence, or slots of a
+ *               pool picked by state_indices (int32 [N])
+ *
+ * Prefill: cu_seqlens int32 [N+1] (or NULL: N equal-length sequences);
+ * initial_states NULL = zeros (the model passes has_initial_state = 0);
+ * final_states (NULL = not written) receives each sequence's last ks - 1
+ * inputs and may be the same pool as initial_states.  cu_seqlens must be
+ * non-decreasing within [0, T]; malformed entries give undefined outputs for
+ * those tokens but no access outside the buffers, and leave the state alone.
+ * Update: one token per sequence; the window is [state ; x] and the state
+ * shifts by one token in place; a slot outside [0, n_slots) gives NaN
+ * outputs and leaves the pool untouched.  y must not overlap x or a state;
+ * sequences must not share a slot.  x, y, weight and the states are 16-byte
+ * aligned.  A prefill whose staged copy never lands (a bounded wait expired)
+ * writes NaN to the affected outputs.
+ */
+#define KDA_CONV_NONE 0
+#define KDA_CONV_SILU 1
+int kda_short_conv_fwd(const void *x, const void *weight, void *y, const int32_t *cu_seqlens,
+                       int n_seqs, int64_t total_tokens, int D, int ks, int activation,
+                       const void *initial_states, void *final_states,
+                       const int32_t *state_indices, int64_t n_slots, int dtype, void *stream);
+int kda_short_conv_update(const void *x, const void *weight, void *y, void *state_pool,
+                          const int32_t *state_indices, int64_t n_slots, int N, int D, int ks,
+                          int activation, int dtype, void *stream);
+
+/*
  * Speculative (multi-token) decode: S tokens per sequence run in order
  * through the recurrence (the model's decode call with a verify width S:
  * model file, _decode_fused_kda / _decode_gdr with ssm_state_indices of

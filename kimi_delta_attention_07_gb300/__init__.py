@@ -26,13 +26,17 @@ KDA_CHUNK_PRECISE = 1
 KDA_CHUNK_SCAN_WIDE = 2
 KDA_CHUNK_SCAN_SPLIT = 4
 KDA_CHUNK_GATED = 8
+KDA_CONV_NONE = 0
+KDA_CONV_SILU = 1
+_CONV_ACT = {"silu": KDA_CONV_SILU, "none": KDA_CONV_NONE, None: KDA_CONV_NONE}
 _SCAN_FLAGS = {"auto": 0, "wide": KDA_CHUNK_SCAN_WIDE, "split": KDA_CHUNK_SCAN_SPLIT}
 CHUNK = 64
 
 EXPORTS = ("kda_status_string", "kda_version", "kda_chunk_workspace_bytes", "kda_chunk_fwd",
            "kda_chunk_intra", "kda_chunk_scan", "kda_workspace_status", "kda_recurrent_step",
            "kda_chunk_fwd_noalloc", "kda_chunk_fwd_gated", "kda_recurrent_step_gated",
-           "kda_output_gate_norm", "kda_recurrent_multi_step")
+           "kda_output_gate_norm", "kda_recurrent_multi_step", "kda_short_conv_fwd",
+           "kda_short_conv_update")
 NOALLOC_WORKSPACE_BYTES = 64 * 1024 * 1024
 
 _lib = None
@@ -91,6 +95,11 @@ def load(path: str | None = None):
         L.kda_recurrent_multi_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, vp, i32, i32,
                                                i32, i32, i32, f32, i32, vp]
         L.kda_recurrent_multi_step.restype = i32
+        L.kda_short_conv_fwd.argtypes = [vp, vp, vp, vp, i32, i64, i32, i32, i32, vp, vp, vp, i64,
+                                         i32, vp]
+        L.kda_short_conv_fwd.restype = i32
+        L.kda_short_conv_update.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, vp]
+        L.kda_short_conv_update.restype = i32
         _lib = L
         return L
 
@@ -361,6 +370,67 @@ def kda_recurrent_multi_step(q, k, v, g, beta, state_pool, state_indices, *, num
     if st != KDA_OK:
         raise KdaError(st, "kda_recurrent_multi_step")
     return o
+
+
+def kda_short_conv_fwd(x, weight, *, cu_seqlens=None, n_seqs=None, activation="silu",
+                       initial_states=None, final_states=None, state_indices=None, n_slots=None,
+                       y=None, stream=None):
+    """Short causal convolution over packed sequences (prefill).
+
+    x [T, D]; weight [ks, D] (same dtype); cu_seqlens int32 [N+1] or None
+    (n_seqs equal lengths, default 1); activation "silu" or "none".  Conv
+    states are [N, ks-1, D] per sequence, or pools [slots, ks-1, D] picked by
+    state_indices (int32 [N]); initial_states None = zeros; final_states None =
+    not written (may be the initial pool, updated in place).  Returns
+    (y [T, D], final_states).
+    """
+    T, D = x.shape
+    ks = weight.shape[0]
+    dt = _dtype_code(x)
+    N = cu_seqlens.numel() - 1 if cu_seqlens is not None else (1 if n_seqs is None else int(n_seqs))
+    for name, t, dtype_, shape in (("x", x, x.dtype, (T, D)), ("weight", weight, x.dtype, (ks, D)),
+                                   ("cu_seqlens", cu_seqlens, torch.int32, (N + 1,)),
+                                   ("state_indices", state_indices, torch.int32, (N,)),
+                                   ("initial_states", initial_states, x.dtype, None),
+                                   ("final_states", final_states, x.dtype, None)):
+        _check(t, name, dtype_, shape)
+    if y is None:
+        y = torch.empty_like(x)
+    _check(y, "y", x.dtype, (T, D))
+    pool = final_states if final_states is not None else initial_states
+    slots = 0
+    if state_indices is not None:
+        slots = pool.shape[0] if n_slots is None else int(n_slots)
+    st = load().kda_short_conv_fwd(_p(x), _p(weight), _p(y), _p(cu_seqlens), N, T, D, ks,
+                                   _CONV_ACT[activation], _p(initial_states), _p(final_states),
+                                   _p(state_indices), slots, dt, _stream(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_short_conv_fwd")
+    return y, final_states
+
+
+def kda_short_conv_update(x, weight, state_pool, *, state_indices=None, activation="silu", y=None,
+                          stream=None):
+    """One decode token per sequence: x [N, D]; state_pool [slots, ks-1, D]
+    (slot n, or state_indices int32 [N]) shifted in place.  Returns y [N, D]."""
+    N, D = x.shape
+    ks = weight.shape[0]
+    dt = _dtype_code(x)
+    for name, t, dtype_, shape in (("x", x, x.dtype, (N, D)), ("weight", weight, x.dtype, (ks, D)),
+                                   ("state_pool", state_pool, x.dtype, None),
+                                   ("state_indices", state_indices, torch.int32, (N,))):
+        _check(t, name, dtype_, shape)
+    if state_pool.dim() != 3 or tuple(state_pool.shape[1:]) != (ks - 1, D):
+        raise ValueError(f"state_pool must be [slots, {ks - 1}, {D}]")
+    if y is None:
+        y = torch.empty_like(x)
+    _check(y, "y", x.dtype, (N, D))
+    st = load().kda_short_conv_update(_p(x), _p(weight), _p(y), _p(state_pool), _p(state_indices),
+                                      state_pool.shape[0], N, D, ks, _CONV_ACT[activation], dt,
+                                      _stream(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_short_conv_update")
+    return y
 
 
 def kda_chunk_fwd_noalloc(q, k, v, g, beta, *, cu_seqlens=None, n_seqs=None, initial_state=None,

@@ -271,6 +271,56 @@ int kda_recurrent_step_gated(const void *q, const void *k, const void *v, const 
                      n_slots, o, N, H, K, V, scale, dtype, stream);
 }
 
+int kda_short_conv_fwd(const void *x, const void *weight, void *y, const int32_t *cu_seqlens,
+                       int n_seqs, int64_t total_tokens, int D, int ks, int activation,
+                       const void *initial_states, void *final_states,
+                       const int32_t *state_indices, int64_t n_slots, int dtype, void *stream) {
+    if (!valid_dtype(dtype) || n_seqs <= 0 || total_tokens < 0 || D <= 0 || D % 8 != 0 ||
+        ks < 2 || ks > 8 || (activation != KDA_CONV_NONE && activation != KDA_CONV_SILU))
+        return KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens && total_tokens % n_seqs != 0) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!x || !weight || !y)) return KDA_ERR_INVALID_ARG;
+    if (state_indices ? n_slots <= 0 : n_slots < 0) return KDA_ERR_INVALID_ARG;
+    const int64_t slots = state_indices ? n_slots : n_seqs;
+    const size_t ea = 8 * elem_bytes(dtype) >= 16 ? 16 : 8 * elem_bytes(dtype);
+    if ((x && !aligned(x, ea)) || (weight && !aligned(weight, ea)) || (y && !aligned(y, ea)) ||
+        (initial_states && !aligned(initial_states, ea)) || (final_states && !aligned(final_states, ea)))
+        return KDA_ERR_INVALID_ARG;
+    cudaGetLastError();
+    const cudaError_t e = launch_short_conv_prefill(x, weight, y, cu_seqlens, n_seqs, total_tokens,
+                                                    D, ks, activation, initial_states, final_states,
+                                                    state_indices, slots, dtype,
+                                                    (cudaStream_t)stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
+int kda_short_conv_update(const void *x, const void *weight, void *y, void *state_pool,
+                          const int32_t *state_indices, int64_t n_slots, int N, int D, int ks,
+                          int activation, int dtype, void *stream) {
+    if (!valid_dtype(dtype) || N < 0 || D <= 0 || D % 8 != 0 || ks < 2 || ks > 8 ||
+        n_slots < 0 || (activation != KDA_CONV_NONE && activation != KDA_CONV_SILU))
+        return KDA_ERR_INVALID_ARG;
+    if (N == 0) return KDA_OK;
+    if (!x || !weight || !y || !state_pool) return KDA_ERR_INVALID_ARG;
+    if (!state_indices && n_slots < N) return KDA_ERR_INVALID_ARG;
+    const size_t ea = 8 * elem_bytes(dtype) >= 16 ? 16 : 8 * elem_bytes(dtype);
+    if (!aligned(x, ea) || !aligned(weight, ea) || !aligned(y, ea) || !aligned(state_pool, ea))
+        return KDA_ERR_INVALID_ARG;
+    cudaGetLastError();
+    const cudaError_t e = launch_short_conv_update(x, weight, y, state_pool, state_indices, n_slots,
+                                                   N, D, ks, activation, dtype,
+                                                   (cudaStream_t)stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
 int kda_output_gate_norm(void *o, const void *gate, const float *weight, float eps,
                          int64_t rows, int V, int dtype, void *stream) {
     if (!valid_dtype(dtype) || rows < 0 || V <= 0) return KDA_ERR_INVALID_ARG;

@@ -1314,18 +1314,6 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     if (warp == 0) tmem_dealloc(tmem, kWideTmemCols);
 }
 
-int sm_count() {
-    static int count[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (!count[dev]) {
-        int c = 0;
-        cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
-        count[dev] = c > 0 ? c : 148;
-    }
-    return count[dev];
-}
-
 }  // namespace
 
 namespace {

@@ -123,6 +123,19 @@ struct TcRec {
 };
 static_assert(TcRec::U + 4 * TcRec::UBLK <= TcRec::bytes, "TcRec layout");
 
+// SM count of the current device (cached per device; host only)
+inline int sm_count() {
+    static int count[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!count[dev]) {
+        int c = 0;
+        cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
+        count[dev] = c > 0 ? c : 148;
+    }
+    return count[dev];
+}
+
 // ---- gate activation (the model's gate, computed in-kernel) ----------------
 // x = raw_gate + dt_bias[h][k];  g = lower_bound * sigmoid(exp(a_log[h]) x)
 // with a lower bound, else -exp(a_log[h]) softplus(x);  beta = sigmoid(raw_beta).
@@ -212,6 +225,16 @@ __device__ __forceinline__ int owner_of_chunk(const int32_t *chunk_off, int n_se
 // after token t goes to slot state_indices[n S + t], the initial state comes
 // from slot state_indices[n S + num_accepted[n] - 1] (num_accepted == nullptr:
 // token 0's slot; state_indices == nullptr with S == 1: slot n).
+// Short causal convolution (x, weight, y, states all in `dtype`).
+cudaError_t launch_short_conv_prefill(const void *x, const void *weight, void *y,
+                                      const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens,
+                                      int D, int ks, int activation, const void *initial_states,
+                                      void *final_states, const int32_t *state_indices,
+                                      int64_t n_slots, int dtype, cudaStream_t stream);
+cudaError_t launch_short_conv_update(const void *x, const void *weight, void *y, void *pool,
+                                     const int32_t *state_indices, int64_t n_slots, int N, int D,
+                                     int ks, int activation, int dtype, cudaStream_t stream);
+
 cudaError_t launch_recurrent_step(const void *q, const void *k, const void *v, const float *g,
                                   const float *beta, const GateArgs *gate, const EpiArgs *epi,
                                   float *pool, const int32_t *state_indices,

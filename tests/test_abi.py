@@ -183,6 +183,41 @@ def test_multi_step_rejects_bad_arguments_without_launching(lib):
     assert f(dt=2) == kda.KDA_ERR_INVALID_ARG
 
 
+def test_short_conv_rejects_bad_arguments_without_launching(lib):
+    base = 1 << 20
+    vp = ctypes.c_void_p
+    p = lambda x: None if x is None else vp(x)
+
+    def fwd(**kw):
+        a = dict(x=base, w=base, y=base, cu=None, N=1, T=64, D=256, ks=4, act=1, s0=None, sf=None,
+                 idx=None, slots=0, dt=kda.KDA_BF16)
+        a.update(kw)
+        return lib.kda_short_conv_fwd(p(a["x"]), p(a["w"]), p(a["y"]), p(a["cu"]), a["N"], a["T"],
+                                      a["D"], a["ks"], a["act"], p(a["s0"]), p(a["sf"]), p(a["idx"]),
+                                      a["slots"], a["dt"], None)
+
+    def upd(**kw):
+        a = dict(x=base, w=base, y=base, pool=base, idx=None, slots=4, N=4, D=256, ks=4, act=1,
+                 dt=kda.KDA_BF16)
+        a.update(kw)
+        return lib.kda_short_conv_update(p(a["x"]), p(a["w"]), p(a["y"]), p(a["pool"]), p(a["idx"]),
+                                         a["slots"], a["N"], a["D"], a["ks"], a["act"], a["dt"], None)
+
+    for f in (fwd, upd):
+        assert f(ks=1) == kda.KDA_ERR_INVALID_ARG
+        assert f(ks=9) == kda.KDA_ERR_INVALID_ARG
+        assert f(D=100) == kda.KDA_ERR_INVALID_ARG      # D a multiple of 8
+        assert f(act=2) == kda.KDA_ERR_INVALID_ARG
+        assert f(dt=3) == kda.KDA_ERR_INVALID_ARG
+        assert f(x=None) == kda.KDA_ERR_INVALID_ARG
+        assert f(x=base + 8) == kda.KDA_ERR_INVALID_ARG  # bf16 rows of 8 channels: 16 bytes
+    assert fwd(N=3, T=64) == kda.KDA_ERR_INVALID_ARG     # 3 does not divide 64
+    assert fwd(idx=base, slots=0) == kda.KDA_ERR_INVALID_ARG
+    assert upd(N=0) == kda.KDA_OK
+    assert upd(slots=3) == kda.KDA_ERR_INVALID_ARG       # identity slots need slots >= N
+    assert upd(pool=None) == kda.KDA_ERR_INVALID_ARG
+
+
 def test_recurrent_step_rejects_bad_arguments_without_launching(lib):
     base = 1 << 20
     vp = ctypes.c_void_p

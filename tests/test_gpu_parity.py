@@ -608,3 +608,102 @@ def test_multi_step_decode_256_verify_width_4_sampled(kda):
     touched = idx.numpy()[seqs].ravel()
     assert rel_l2(vk_to_kv(pool_d[touched][:, heads]), pool_ref[touched]) < TOL_F32
     assert torch.isfinite(o).all()
+
+
+# ---------------------------------------------------------------------------
+# short causal convolution (f4)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("activation", ["silu", "none"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_short_conv_prefill_into_pool_then_updates(kda, dtype, activation):
+    """Packed sequences (one empty, one shorter than ks - 1) from pool slots,
+    final states written back in place, then decode updates continue."""
+    ks, D, slots = 4, 96, 7
+    c = kda_inputs.conv_inputs([40, 0, 2, 65], D=D, ks=ks, dtype=dtype, seed=81)
+    gen = torch.Generator().manual_seed(81)
+    pool = torch.randn((slots, ks - 1, D), generator=gen).to(dtype)
+    idx = torch.tensor([5, 0, 2, 6], dtype=torch.int32)
+    pool_d = pool.cuda()
+    y, _ = kda.kda_short_conv_fwd(c["x"].cuda(), c["weight"].cuda(), cu_seqlens=c["cu_seqlens"].cuda(),
+                                  activation=activation, initial_states=pool_d, final_states=pool_d,
+                                  state_indices=idx.cuda())
+    torch.cuda.synchronize()
+    init = pool.double().numpy()[idx.numpy()]
+    y_ref, fin_ref = oracle.short_conv_prefill(c["x"], c["weight"], c["cu_seqlens"].numpy(),
+                                               activation=activation, initial_states=init)
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    assert rel_l2(to_np(y), y_ref) < tol
+    got = pool_d.double().cpu().numpy()
+    assert rel_l2(got[idx.numpy()], fin_ref) < tol
+    others = [s for s in range(slots) if s not in idx.tolist()]
+    assert torch.equal(pool_d.cpu()[others], pool[others])
+    st_ref = got[idx.numpy()]
+    for t in range(3):
+        xt = torch.randn((4, D), generator=gen).to(dtype)
+        yt = kda.kda_short_conv_update(xt.cuda(), c["weight"].cuda(), pool_d, state_indices=idx.cuda(),
+                                       activation=activation)
+        yt_ref, st_ref = oracle.short_conv_update(xt, c["weight"], st_ref, activation=activation)
+        torch.cuda.synchronize()
+        assert rel_l2(to_np(yt), yt_ref) < tol
+    assert rel_l2(pool_d.double().cpu().numpy()[idx.numpy()], st_ref) < tol
+
+
+def test_short_conv_update_invalid_slot_and_dense_batch(kda):
+    ks, D = 3, 64
+    c = kda_inputs.conv_inputs([32, 32, 32], D=D, ks=ks, dtype=torch.float32, seed=82)
+    y, fin = kda.kda_short_conv_fwd(c["x"].cuda(), c["weight"].cuda(), n_seqs=3,
+                                    final_states=torch.empty((3, ks - 1, D), device="cuda"))
+    y_ref, fin_ref = oracle.short_conv_prefill(c["x"], c["weight"], c["cu_seqlens"].numpy())
+    torch.cuda.synchronize()
+    assert rel_l2(to_np(y), y_ref) < TOL_F32 and rel_l2(to_np(fin), fin_ref) < TOL_F32
+    pool = fin.clone()
+    bad = torch.tensor([1, 9], dtype=torch.int32, device="cuda")  # slot 9 is out of range
+    yu = kda.kda_short_conv_update(torch.ones((2, D), device="cuda"), c["weight"].cuda(), pool,
+                                   state_indices=bad)
+    torch.cuda.synchronize()
+    assert torch.isnan(yu[1]).all() and torch.isfinite(yu[0]).all()
+    assert torch.equal(pool[0], fin[0]) and torch.equal(pool[2], fin[2])
+
+
+def test_short_conv_prefill_4k_qkv_full_size_sampled_channels(kda):
+    """The fused q/k/v projection of the 4k workload: T = 4096, D = 3 x 32 x 128, bf16."""
+    c = kda_inputs.conv_inputs([4096], seed=83)
+    fin = torch.empty((1, 3, c["D"]), dtype=torch.bfloat16, device="cuda")
+    y, _ = kda.kda_short_conv_fwd(c["x"].cuda(), c["weight"].cuda(), cu_seqlens=c["cu_seqlens"].cuda(),
+                                  final_states=fin)
+    torch.cuda.synchronize()
+    ch = list(range(0, c["D"], 97))
+    y_ref, fin_ref = oracle.short_conv_prefill(c["x"][:, ch], c["weight"][:, ch], c["cu_seqlens"].numpy())
+    assert rel_l2(to_np(y[:, ch]), y_ref) < TOL_BF16
+    assert rel_l2(to_np(fin[:, :, ch]), fin_ref) < TOL_BF16
+
+
+@pytest.mark.parametrize("ks", [2, 6, 7, 8])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_short_conv_many_short_sequences_inside_one_tile(kda, dtype, ks):
+    """Sequences shorter than a thread's token run and than the window (so one
+    run crosses several sequence starts, each reading its own conv state), and
+    every tap count that has its own kernel instance."""
+    lengths = [1, 1, 3, 0, 9, 2, 17, 5, 0, 6, 1, 24]
+    D = 40
+    c = kda_inputs.conv_inputs(lengths, D=D, ks=ks, dtype=dtype, seed=84 + ks)
+    gen = torch.Generator().manual_seed(85 + ks)
+    init = torch.randn((len(lengths), ks - 1, D), generator=gen).to(dtype)
+    fin = torch.empty_like(init).cuda()
+    y, _ = kda.kda_short_conv_fwd(c["x"].cuda(), c["weight"].cuda(), cu_seqlens=c["cu_seqlens"].cuda(),
+                                  initial_states=init.cuda(), final_states=fin)
+    torch.cuda.synchronize()
+    y_ref, fin_ref = oracle.short_conv_prefill(c["x"], c["weight"], c["cu_seqlens"].numpy(),
+                                               initial_states=init)
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    assert rel_l2(to_np(y), y_ref) < tol
+    assert rel_l2(to_np(fin), fin_ref) < tol
+    # decode update with the same tap count, identity slots
+    xt = torch.randn((len(lengths), D), generator=gen).to(dtype)
+    pool = fin.clone()
+    yt = kda.kda_short_conv_update(xt.cuda(), c["weight"].cuda(), pool)
+    yt_ref, st_ref = oracle.short_conv_update(xt, c["weight"], fin_ref)
+    torch.cuda.synchronize()
+    assert rel_l2(to_np(yt), yt_ref) < tol
+    assert rel_l2(to_np(pool), st_ref) < tol
