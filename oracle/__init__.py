@@ -356,3 +356,32 @@ def short_conv_update(x, weight, state, activation="silu"):
     win = np.concatenate([st, x[:, None, :]], axis=1)  # [N, ks, D]
     y = _act(np.sum(w[None] * win, axis=1), activation)
     return y, win[:, 1:].copy()
+
+
+def short_conv_multi_update(x, weight, pool, state_indices, num_accepted=None, activation="silu"):
+    """Speculative decode through the short conv: the model's update branch
+    with a verify width S > 1 (the flattened [batch x S] tokens,
+    ``conv_state_indices`` from the per-sequence state blocks and
+    ``num_accepted_tokens``).  Reading of the call, the one taken for the
+    core's multi-token decode: sequence n starts from the conv state in slot
+    state_indices[n, num_accepted[n] - 1] (slot state_indices[n, 0] when
+    num_accepted is None), runs its S tokens in order through the one-token
+    update, and the state after token t is written to slot
+    state_indices[n, t].
+
+    x [N, S, D]; weight [ks, D]; pool [slots, ks - 1, D]; state_indices
+    [N, S]; num_accepted [N] or None.  Returns (y [N, S, D], new pool), fp64."""
+    x = _f64(x)
+    idx = np.asarray(state_indices, dtype=np.int64)
+    N, S = idx.shape
+    out_pool = _f64(pool).copy()
+    y = np.zeros(x.shape, dtype=np.float64)
+    for n in range(N):
+        a = 1 if num_accepted is None else int(num_accepted[n])
+        state = out_pool[idx[n, a - 1]].copy()
+        for t in range(S):
+            yt, st = short_conv_update(x[n, t:t + 1], weight, state[None], activation=activation)
+            y[n, t] = yt[0]
+            state = st[0]
+            out_pool[idx[n, t]] = state
+    return y, out_pool

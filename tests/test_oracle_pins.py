@@ -525,3 +525,33 @@ def test_conv_prefill_then_updates_equal_the_longer_prefill():
         yt, st = oracle.short_conv_update(x[t:t + 1], w, st)
         np.testing.assert_allclose(yt[0], y_all[t], rtol=1e-14, atol=1e-15)
     np.testing.assert_allclose(st[0], fin_all[0], rtol=0, atol=0)
+
+
+def test_conv_multi_update_is_a_prefill_from_the_accepted_slot():
+    """Each sequence's S outputs are the prefill of its S tokens from the
+    conv state in its accepted slot (pinned above), the state written after
+    token t is that prefill's final state over tokens 0..t, and S = 1 without
+    counts is the one-token update; slots of no sequence are untouched."""
+    rng = np.random.default_rng(55)
+    N, S, D, ks, slots = 3, 4, 5, 4, 14
+    x = rng.standard_normal((N, S, D))
+    w = rng.standard_normal((ks, D))
+    pool = rng.standard_normal((slots, ks - 1, D))
+    idx = np.array([[0, 1, 2, 3], [7, 8, 9, 10], [4, 5, 6, 13]])
+    acc = np.array([1, 3, 4])
+    for act in ("silu", "none"):
+        y, new = oracle.short_conv_multi_update(x, w, pool, idx, acc, activation=act)
+        for n in range(N):
+            start = pool[idx[n, acc[n] - 1]]
+            y_r, _ = oracle.short_conv_prefill(x[n], w, [0, S], activation=act, initial_states=start[None])
+            np.testing.assert_allclose(y[n], y_r, rtol=1e-13, atol=1e-14)
+            for t in range(S):
+                _, f_t = oracle.short_conv_prefill(x[n, :t + 1], w, [0, t + 1], activation=act,
+                                                   initial_states=start[None])
+                np.testing.assert_array_equal(new[idx[n, t]], f_t[0])
+        untouched = [s_ for s_ in range(slots) if s_ not in idx]
+        np.testing.assert_array_equal(new[untouched], pool[untouched])
+    y1, new1 = oracle.short_conv_multi_update(x[:, :1], w, pool, idx[:, :1])
+    y_u, st_u = oracle.short_conv_update(x[:, 0], w, pool[idx[:, 0]])
+    np.testing.assert_array_equal(y1[:, 0], y_u)
+    np.testing.assert_array_equal(new1[idx[:, 0]], st_u)
