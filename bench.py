@@ -311,7 +311,27 @@ def run_conv(args, kda, dev, stream, pk):
     torch.cuda.synchronize()
     us_upd = _graph_us(upd, 32, stream)
     b_upd = DEC_N * D * 2 * 2 + 2 * DEC_N * (ks - 1) * D * 2 + ks * D * 2
-    del sets
+    # speculative verify width 4: per-token state slots, accepted counts 1..4
+    SV = 4
+    spec = []
+    for j in range(4):
+        g = torch.Generator().manual_seed(8400 + j)
+        spec.append((torch.randn((DEC_N, SV, D), generator=g).to(torch.bfloat16).to(dev),
+                     torch.randn((DEC_N * SV, ks - 1, D), generator=g).to(torch.bfloat16).to(dev),
+                     torch.empty((DEC_N, SV, D), dtype=torch.bfloat16, device=dev)))
+    sidx = torch.arange(DEC_N * SV, dtype=torch.int32, device=dev).view(DEC_N, SV)
+    sacc = (torch.arange(DEC_N, dtype=torch.int32, device=dev) % SV) + 1
+
+    def spec_upd(i, st=stream):
+        xt, pool, yt = spec[i % len(spec)]
+        kda.kda_short_conv_multi_update(xt, w, pool, sidx, num_accepted=sacc, y=yt, stream=st)
+
+    for i in range(4):
+        spec_upd(i)
+    torch.cuda.synchronize()
+    us_spec = _graph_us(spec_upd, 32, stream)
+    b_spec = DEC_N * SV * D * 2 * 2 + (1 + SV) * DEC_N * (ks - 1) * D * 2 + ks * D * 2
+    del sets, spec
     roof = lambda b, us: {"bound": "hbm", "algorithmic_bytes": b,
                           "achieved": round(b / (us * 1e-6) / 1e9, 1), "peak": pk["hbm"],
                           "unit": "GB/s", "frac": round(b / (us * 1e-6) / 1e9 / pk["hbm"], 4)}
@@ -321,7 +341,9 @@ def run_conv(args, kda, dev, stream, pk):
                         "tokens_per_s": round(T_4K / (us_pre * 1e-6), 1),
                         "roofline": roof(b_pre, us_pre)},
             "decode_update": {"N": DEC_N, "us_per_call": round(us_upd, 2), "launches_per_call": 1,
-                              "roofline": roof(b_upd, us_upd)}}
+                              "roofline": roof(b_upd, us_upd)},
+            "speculative_update": {"N": DEC_N, "verify_width": SV, "us_per_call": round(us_spec, 2),
+                                   "launches_per_call": 1, "roofline": roof(b_spec, us_spec)}}
 
 
 def decode_bytes(N, H, elem=2):

@@ -276,6 +276,29 @@ int kda_short_conv_update(const void *x, const void *weight, void *y, void *stat
                           int activation, int dtype, void *stream);
 
 /*
+ * Short conv with a speculative verify width (the model's update branch with
+ * S > 1 tokens per sequence, conv_state_indices from the per-sequence state
+ * blocks and num_accepted_tokens: Ascend model file,
+ * KimiShortConvolution.forward and KimiDeltaAttention._forward_core).
+ *
+ *   x, y          [N, S, D] dtype;  weight [ks, D];  state_pool [slots, ks - 1, D]
+ *   state_indices device int32 [N, S]: the conv state after token t of
+ *                 sequence n is written to slot state_indices[n][t]
+ *   num_accepted  device int32 [N] or NULL: sequence n starts from slot
+ *                 state_indices[n][num_accepted[n] - 1] (NULL: [n][0])
+ *
+ * The same slot convention as kda_recurrent_multi_step.  A count outside
+ * [1, S] or a slot outside [0, n_slots) gives the sequence NaN outputs and
+ * leaves the pool untouched; slots of different sequences must not overlap.
+ * S = 1 with num_accepted = NULL is kda_short_conv_update with
+ * state_indices.
+ */
+int kda_short_conv_multi_update(const void *x, const void *weight, void *y, void *state_pool,
+                                const int32_t *state_indices, const int32_t *num_accepted,
+                                int64_t n_slots, int N, int S, int D, int ks, int activation,
+                                int dtype, void *stream);
+
+/*
  * Speculative (multi-token) decode: S tokens per sequence run in order
  * through the recurrence (the model's decode call with a verify width S:
  * model file, _decode_fused_kda / _decode_gdr with ssm_state_indices of

@@ -36,7 +36,7 @@ EXPORTS = ("kda_status_string", "kda_version", "kda_chunk_workspace_bytes", "kda
            "kda_chunk_intra", "kda_chunk_scan", "kda_workspace_status", "kda_recurrent_step",
            "kda_chunk_fwd_noalloc", "kda_chunk_fwd_gated", "kda_recurrent_step_gated",
            "kda_output_gate_norm", "kda_recurrent_multi_step", "kda_short_conv_fwd",
-           "kda_short_conv_update")
+           "kda_short_conv_update", "kda_short_conv_multi_update")
 NOALLOC_WORKSPACE_BYTES = 64 * 1024 * 1024
 
 _lib = None
@@ -100,6 +100,9 @@ def load(path: str | None = None):
         L.kda_short_conv_fwd.restype = i32
         L.kda_short_conv_update.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, vp]
         L.kda_short_conv_update.restype = i32
+        L.kda_short_conv_multi_update.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32,
+                                                  i32, vp]
+        L.kda_short_conv_multi_update.restype = i32
         _lib = L
         return L
 
@@ -430,6 +433,35 @@ def kda_short_conv_update(x, weight, state_pool, *, state_indices=None, activati
                                       _stream(stream))
     if st != KDA_OK:
         raise KdaError(st, "kda_short_conv_update")
+    return y
+
+
+def kda_short_conv_multi_update(x, weight, state_pool, state_indices, *, num_accepted=None,
+                                activation="silu", y=None, stream=None):
+    """S tokens per sequence through the conv: x [N, S, D]; state_pool
+    [slots, ks-1, D]; state_indices int32 [N, S] (state after token t to
+    slot [n][t]); num_accepted int32 [N] or None (start slot [n][a-1], else
+    [n][0]).  Returns y [N, S, D]."""
+    N, S, D = x.shape
+    ks = weight.shape[0]
+    dt = _dtype_code(x)
+    for name, t, dtype_, shape in (("x", x, x.dtype, (N, S, D)), ("weight", weight, x.dtype, (ks, D)),
+                                   ("state_pool", state_pool, x.dtype, None),
+                                   ("state_indices", state_indices, torch.int32, (N, S)),
+                                   ("num_accepted", num_accepted, torch.int32, (N,))):
+        _check(t, name, dtype_, shape)
+    if state_indices is None:
+        raise ValueError("state_indices is required")
+    if state_pool.dim() != 3 or tuple(state_pool.shape[1:]) != (ks - 1, D):
+        raise ValueError(f"state_pool must be [slots, {ks - 1}, {D}]")
+    if y is None:
+        y = torch.empty_like(x)
+    _check(y, "y", x.dtype, (N, S, D))
+    st = load().kda_short_conv_multi_update(_p(x), _p(weight), _p(y), _p(state_pool),
+                                            _p(state_indices), _p(num_accepted), state_pool.shape[0],
+                                            N, S, D, ks, _CONV_ACT[activation], dt, _stream(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_short_conv_multi_update")
     return y
 
 

@@ -321,6 +321,29 @@ int kda_short_conv_update(const void *x, const void *weight, void *y, void *stat
     return KDA_OK;
 }
 
+int kda_short_conv_multi_update(const void *x, const void *weight, void *y, void *state_pool,
+                                const int32_t *state_indices, const int32_t *num_accepted,
+                                int64_t n_slots, int N, int S, int D, int ks, int activation,
+                                int dtype, void *stream) {
+    if (!valid_dtype(dtype) || N < 0 || S < 1 || D <= 0 || D % 8 != 0 || ks < 2 || ks > 8 ||
+        n_slots <= 0 || (activation != KDA_CONV_NONE && activation != KDA_CONV_SILU))
+        return KDA_ERR_INVALID_ARG;
+    if (N == 0) return KDA_OK;
+    if (!x || !weight || !y || !state_pool || !state_indices) return KDA_ERR_INVALID_ARG;
+    const size_t ea = 8 * elem_bytes(dtype) >= 16 ? 16 : 8 * elem_bytes(dtype);
+    if (!aligned(x, ea) || !aligned(weight, ea) || !aligned(y, ea) || !aligned(state_pool, ea))
+        return KDA_ERR_INVALID_ARG;
+    cudaGetLastError();
+    const cudaError_t e = launch_short_conv_multi_update(x, weight, y, state_pool, state_indices,
+                                                         num_accepted, n_slots, N, S, D, ks,
+                                                         activation, dtype, (cudaStream_t)stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
 int kda_output_gate_norm(void *o, const void *gate, const float *weight, float eps,
                          int64_t rows, int V, int dtype, void *stream) {
     if (!valid_dtype(dtype) || rows < 0 || V <= 0) return KDA_ERR_INVALID_ARG;

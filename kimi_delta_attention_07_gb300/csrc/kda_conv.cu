@@ -511,6 +511,73 @@ __global__ void __launch_bounds__(kConvThreads)
     }
 }
 
+// S tokens per sequence (a speculative verify width): the window starts from
+// the conv state in slot idx[n][a - 1] (a = the sequence's accepted count, 1
+// without counts) and the state after token t goes to slot idx[n][t].  The
+// start state is in registers before the first write, so it may be one of the
+// destination slots.  A count outside [1, S] or a slot outside [0, n_slots)
+// gives the sequence NaN outputs and leaves the pool untouched.
+template <typename T, int KS>
+__global__ void __launch_bounds__(kConvThreads)
+    conv_multi_update_kernel(const T *__restrict__ x, const T *__restrict__ w, T *__restrict__ y,
+                             T *__restrict__ pool, const int32_t *__restrict__ idx,
+                             const int32_t *__restrict__ accepted, int64_t n_slots, int N, int S,
+                             int D, int activation) {
+    const int chunks = D / 8;
+    const int64_t total = (int64_t)N * chunks;
+    for (int64_t i = blockIdx.x * (int64_t)kConvThreads + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * kConvThreads) {
+        const int n = (int)(i / chunks);
+        const int d0 = (int)(i - (int64_t)n * chunks) * 8;
+        const int32_t *sl = idx + (int64_t)n * S;
+        const int a = accepted ? accepted[n] : 1;
+        bool valid = a >= 1 && a <= S;
+        for (int t = 0; t < S; ++t) valid = valid && sl[t] >= 0 && sl[t] < n_slots;
+        if (!valid) {
+            float nan8[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) nan8[c] = __int_as_float(0x7fc00000);
+            for (int t = 0; t < S; ++t) store8(y + ((int64_t)n * S + t) * D + d0, nan8);
+            continue;
+        }
+        Row8<T> raw[KS - 1], wr[KS];
+        const T *st0 = pool + (int64_t)sl[a - 1] * (KS - 1) * D + d0;
+#pragma unroll
+        for (int r = 0; r < KS - 1; ++r) raw[r].load(st0 + (int64_t)r * D);
+#pragma unroll
+        for (int k = 0; k < KS; ++k) wr[k].load(w + (int64_t)k * D + d0);
+        float win[KS - 1][8], wt[KS][8];
+#pragma unroll
+        for (int r = 0; r < KS - 1; ++r) raw[r].to_f32(win[r]);
+#pragma unroll
+        for (int k = 0; k < KS; ++k) wr[k].to_f32(wt[k]);
+        for (int t = 0; t < S; ++t) {
+            float cur[8], acc[8];
+            load8(x + ((int64_t)n * S + t) * D + d0, cur);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[c] = 0.0f;
+#pragma unroll
+            for (int k = 0; k < KS - 1; ++k)  // oldest tap first, as the one-token update
+#pragma unroll
+                for (int c = 0; c < 8; ++c) acc[c] = fmaf(wt[k][c], win[k][c], acc[c]);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[c] = fmaf(wt[KS - 1][c], cur[c], acc[c]);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[c] = conv_act(acc[c], activation);
+            store8(y + ((int64_t)n * S + t) * D + d0, acc);
+#pragma unroll
+            for (int k = 0; k + 1 < KS - 1; ++k)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) win[k][c] = win[k + 1][c];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) win[KS - 2][c] = cur[c];
+            T *dst = pool + (int64_t)sl[t] * (KS - 1) * D + d0;
+#pragma unroll
+            for (int r = 0; r < KS - 1; ++r) store8(dst + (int64_t)r * D, win[r]);
+        }
+    }
+}
+
 template <int V_>
 struct KsTag {
     static constexpr int value = V_;
@@ -594,6 +661,26 @@ cudaError_t launch_short_conv_update(const void *x, const void *weight, void *y,
             conv_update_kernel<float, KS><<<grid, kConvThreads, 0, stream>>>(
                 (const float *)x, (const float *)weight, (float *)y, (float *)pool, state_indices,
                 n_slots, N, D, activation);
+    };
+    dispatch_ks(ks, go);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_short_conv_multi_update(const void *x, const void *weight, void *y, void *pool,
+                                           const int32_t *state_indices, const int32_t *num_accepted,
+                                           int64_t n_slots, int N, int S, int D, int ks, int activation,
+                                           int dtype, cudaStream_t stream) {
+    const int grid = grid_for((int64_t)N * (D / 8));
+    auto go = [&](auto ks_tag) {
+        constexpr int KS = decltype(ks_tag)::value;
+        if (dtype == KDA_BF16)
+            conv_multi_update_kernel<__nv_bfloat16, KS><<<grid, kConvThreads, 0, stream>>>(
+                (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)weight, (__nv_bfloat16 *)y,
+                (__nv_bfloat16 *)pool, state_indices, num_accepted, n_slots, N, S, D, activation);
+        else
+            conv_multi_update_kernel<float, KS><<<grid, kConvThreads, 0, stream>>>(
+                (const float *)x, (const float *)weight, (float *)y, (float *)pool, state_indices,
+                num_accepted, n_slots, N, S, D, activation);
     };
     dispatch_ks(ks, go);
     return cudaGetLastError();

@@ -234,6 +234,10 @@ cudaError_t launch_short_conv_prefill(const void *x, const void *weight, void *y
 cudaError_t launch_short_conv_update(const void *x, const void *weight, void *y, void *pool,
                                      const int32_t *state_indices, int64_t n_slots, int N, int D,
                                      int ks, int activation, int dtype, cudaStream_t stream);
+cudaError_t launch_short_conv_multi_update(const void *x, const void *weight, void *y, void *pool,
+                                           const int32_t *state_indices, const int32_t *num_accepted,
+                                           int64_t n_slots, int N, int S, int D, int ks, int activation,
+                                           int dtype, cudaStream_t stream);
 
 cudaError_t launch_recurrent_step(const void *q, const void *k, const void *v, const float *g,
                                   const float *beta, const GateArgs *gate, const EpiArgs *epi,

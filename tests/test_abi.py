@@ -218,6 +218,20 @@ def test_short_conv_rejects_bad_arguments_without_launching(lib):
     assert upd(pool=None) == kda.KDA_ERR_INVALID_ARG
 
 
+    def multi(**kw):
+        a = dict(x=base, w=base, y=base, pool=base, idx=base, acc=None, slots=16, N=4, S=4, D=256,
+                 ks=4, act=1, dt=kda.KDA_BF16)
+        a.update(kw)
+        return lib.kda_short_conv_multi_update(p(a["x"]), p(a["w"]), p(a["y"]), p(a["pool"]),
+                                               p(a["idx"]), p(a["acc"]), a["slots"], a["N"], a["S"],
+                                               a["D"], a["ks"], a["act"], a["dt"], None)
+
+    assert multi(N=0) == kda.KDA_OK
+    for bad in (dict(S=0), dict(idx=None), dict(slots=0), dict(ks=9), dict(D=12), dict(act=5),
+                dict(dt=7), dict(y=base + 4), dict(pool=None)):
+        assert multi(**bad) == kda.KDA_ERR_INVALID_ARG, bad
+
+
 def test_recurrent_step_rejects_bad_arguments_without_launching(lib):
     base = 1 << 20
     vp = ctypes.c_void_p

@@ -707,3 +707,36 @@ def test_short_conv_many_short_sequences_inside_one_tile(kda, dtype, ks):
     torch.cuda.synchronize()
     assert rel_l2(to_np(yt), yt_ref) < tol
     assert rel_l2(to_np(pool), st_ref) < tol
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_short_conv_multi_update_accepted_slot_start(kda, dtype):
+    """Verify width S = 4: start from the accepted slot, per-token state
+    slots, accepted counts 1..S, one sequence with a count of 0 (NaN, pool
+    untouched), against the oracle; then S = 1 equals the one-token update."""
+    N, S, D, ks = 6, 4, 72, 4
+    slots = N * S + 3
+    gen = torch.Generator().manual_seed(86)
+    x = torch.randn((N, S, D), generator=gen).to(dtype)
+    w = (torch.rand((ks, D), generator=gen) - 0.5).to(dtype)
+    pool = torch.randn((slots, ks - 1, D), generator=gen).to(dtype)
+    perm = torch.randperm(slots, generator=gen)[:N * S].to(torch.int32).view(N, S)
+    acc = torch.tensor([1, 2, 3, 4, 0, 2], dtype=torch.int32)
+    pool_d = pool.cuda()
+    y = kda.kda_short_conv_multi_update(x.cuda(), w.cuda(), pool_d, perm.cuda(), num_accepted=acc.cuda())
+    torch.cuda.synchronize()
+    good = [n for n in range(N) if 1 <= acc[n] <= S]
+    y_ref, pool_ref = oracle.short_conv_multi_update(x[good], w, pool, perm[good].numpy(), acc[good].numpy())
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    assert rel_l2(to_np(y[good]), y_ref) < tol
+    assert rel_l2(pool_d.double().cpu().numpy(), pool_ref) < tol
+    assert torch.isnan(y[4]).all()
+    bad_slots = perm[4].long()
+    assert torch.equal(pool_d.cpu()[bad_slots], pool[bad_slots])
+    # S = 1 without counts == the one-token update through state_indices
+    p1, p2 = pool.cuda(), pool.cuda()
+    idx1 = perm[:, :1].contiguous().cuda()
+    y1 = kda.kda_short_conv_multi_update(x[:, :1].contiguous().cuda(), w.cuda(), p1, idx1)
+    y2 = kda.kda_short_conv_update(x[:, 0].contiguous().cuda(), w.cuda(), p2, state_indices=idx1.view(N))
+    torch.cuda.synchronize()
+    assert torch.equal(y1[:, 0], y2) and torch.equal(p1, p2)
