@@ -906,7 +906,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_drain + 1);
 
     const int n = blockIdx.x, h = blockIdx.y, vb = blockIdx.z, v0 = vb * BV;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int32_t start = ws_at<const int32_t>(workspace, L.seq_start_off)[n];
     if (start < 0) return;  // sequence skipped (bad cu_seqlens or slot)
     const int len = ws_at<const int32_t>(workspace, L.seq_len_off)[n];
