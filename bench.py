@@ -335,11 +335,13 @@ def run_conv(args, kda, dev, stream, pk):
     roof = lambda b, us: {"bound": "hbm", "algorithmic_bytes": b,
                           "achieved": round(b / (us * 1e-6) / 1e9, 1), "peak": pk["hbm"],
                           "unit": "GB/s", "frac": round(b / (us * 1e-6) / 1e9 / pk["hbm"], 4)}
+    pre_roof = dict(roof(b_pre, us_pre), kernel="conv_prefill_kernel",
+                    traffic=traffic_from_profiles("conv_prefill"))
     return {"workload": "short_conv_qkv", "D": D, "ks": ks, "activation": "silu", "dtype": "bf16",
             "timing": "CUDA graph replay, per call",
             "prefill": {"T": T_4K, "us_per_call": round(us_pre, 2), "launches_per_call": 1,
                         "tokens_per_s": round(T_4K / (us_pre * 1e-6), 1),
-                        "roofline": roof(b_pre, us_pre)},
+                        "roofline": pre_roof},
             "decode_update": {"N": DEC_N, "us_per_call": round(us_upd, 2), "launches_per_call": 1,
                               "roofline": roof(b_upd, us_upd)},
             "speculative_update": {"N": DEC_N, "verify_width": SV, "us_per_call": round(us_spec, 2),
