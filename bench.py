@@ -638,8 +638,8 @@ def run_spec_decode(kda, dev, stream, pk, S=4, steps=16):
 
 def cpu_baseline(x, sample_heads, min_seconds=1.0, max_reps=8):
     """The oracle on the host cores: the whole 4k workload (all heads), run
-    until at least min_seconds of wall time (about 10-30 core-seconds on the
-    GPU machine's host)."""
+    until at least min_seconds of wall time (about 10-30 core-seconds on a
+    16-core Grace host)."""
     import oracle
     heads = list(range(sample_heads))
     sub = {n: x[n][:, heads].contiguous() for n in ("q", "k", "v", "g", "beta")}
