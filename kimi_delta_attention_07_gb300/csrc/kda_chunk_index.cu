@@ -18,6 +18,7 @@ __global__ void __launch_bounds__(kIndexThreads)
     chunk_index_kernel(const int32_t *__restrict__ cu_seqlens, int n_seqs, int64_t total_tokens,
                        const int32_t *__restrict__ state_indices, int64_t n_slots,
                        void *workspace, WsLayout L) {
+    griddep_launch_dependents();  // the prep may be scheduled now; it waits for this grid to finish
     int32_t *seq_start = ws_at<int32_t>(workspace, L.seq_start_off);
     int32_t *seq_len = ws_at<int32_t>(workspace, L.seq_len_off);
     int32_t *chunk_off = ws_at<int32_t>(workspace, L.chunk_off_off);

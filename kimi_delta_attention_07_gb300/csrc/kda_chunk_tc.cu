@@ -246,6 +246,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                          const GateArgs gate, int n_seqs, int H, float scale, void *workspace,
                          WsLayout L) {
     constexpr uint32_t kGBytes = GATED ? 16384u : 32768u;
+    griddep_wait();  // the chunk index (previous kernel) is complete
     auto beta_of = [&](int64_t tok, int hh) {
         return GATED ? gate_beta(__bfloat162float(
                            reinterpret_cast<const __nv_bfloat16 *>(gate.raw_beta)[tok * H + hh]))
@@ -322,6 +323,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     KDA_PHASE_START();
     for (; item < n_items; item += gridDim.x) {
         const bool has_next = item + (int)gridDim.x < n_items;
+        if (!has_next) griddep_launch_dependents();  // last item: the scan may be scheduled
         unsigned char *rec = ws_at<unsigned char>(workspace, L.records_off + ((size_t)cur.c * H + cur.h) * TcRec::bytes);
         const int valid = cur.valid;
         if (tid < C) sB[tid] = tid < valid ? beta_cur : 0.0f;
@@ -904,6 +906,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     uint64_t *bar_out = bar_d3 + 1;     // D1 += A Vn done: the chunk's output rows
     uint64_t *bar_drain = bar_out + 1;  // exit path: every MMA issued so far is done
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_drain + 1);
+    griddep_wait();  // the records (previous kernel) are complete
 
     const int n = blockIdx.x, h = blockIdx.y, vb = blockIdx.z, v0 = vb * BV;
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -1111,6 +1114,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     chunk_scan_wide_kernel(const float *__restrict__ initial_state, float *__restrict__ final_state,
                            const int32_t *__restrict__ state_indices, __nv_bfloat16 *__restrict__ o,
                            int n_seqs, int H, void *workspace, WsLayout L) {
+    griddep_wait();  // the records (previous kernel) are complete
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     unsigned char *sS = sm + W_SOP;
@@ -1374,13 +1378,17 @@ cudaError_t launch_chunk_prep_tc(const void *q, const void *k, const void *v, co
         ga = *gate;
         cudaFuncSetAttribute(chunk_prep_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              P_SMEM);
-        chunk_prep_tc_kernel<true><<<grid, kPrepThreads, P_SMEM, stream>>>(maps, beta, ga, n_seqs, H,
-                                                                           scale, workspace, L);
+        const cudaError_t e = launch_dependent(chunk_prep_tc_kernel<true>, dim3(grid), dim3(kPrepThreads),
+                                               P_SMEM, stream, maps, beta, ga, n_seqs, H, scale,
+                                               workspace, L);
+        if (e != cudaSuccess) return e;
     } else {
         cudaFuncSetAttribute(chunk_prep_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              P_SMEM);
-        chunk_prep_tc_kernel<false><<<grid, kPrepThreads, P_SMEM, stream>>>(maps, beta, ga, n_seqs, H,
-                                                                            scale, workspace, L);
+        const cudaError_t e = launch_dependent(chunk_prep_tc_kernel<false>, dim3(grid),
+                                               dim3(kPrepThreads), P_SMEM, stream, maps, beta, ga,
+                                               n_seqs, H, scale, workspace, L);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
@@ -1396,13 +1404,17 @@ cudaError_t launch_chunk_scan_tc(const float *initial_state, float *final_state,
     if (wide) {
         const dim3 grid((unsigned)n_seqs, (unsigned)H, 1);
         cudaFuncSetAttribute(chunk_scan_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, W_SMEM);
-        chunk_scan_wide_kernel<<<grid, kWideThreads, W_SMEM, stream>>>(
-            initial_state, final_state, state_indices, (__nv_bfloat16 *)o, n_seqs, H, workspace, L);
+        const cudaError_t e = launch_dependent(chunk_scan_wide_kernel, grid, dim3(kWideThreads), W_SMEM,
+                                               stream, initial_state, final_state, state_indices,
+                                               (__nv_bfloat16 *)o, n_seqs, H, workspace, L);
+        if (e != cudaSuccess) return e;
     } else {
         const dim3 grid((unsigned)n_seqs, (unsigned)H, D / BV);
         cudaFuncSetAttribute(chunk_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S_SMEM);
-        chunk_scan_tc_kernel<<<grid, kScanThreads, S_SMEM, stream>>>(
-            initial_state, final_state, state_indices, (__nv_bfloat16 *)o, n_seqs, H, workspace, L);
+        const cudaError_t e = launch_dependent(chunk_scan_tc_kernel, grid, dim3(kScanThreads), S_SMEM,
+                                               stream, initial_state, final_state, state_indices,
+                                               (__nv_bfloat16 *)o, n_seqs, H, workspace, L);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

@@ -123,6 +123,32 @@ struct TcRec {
 };
 static_assert(TcRec::U + 4 * TcRec::UBLK <= TcRec::bytes, "TcRec layout");
 
+// Programmatic dependent launch.  A kernel launched with launch_dependent()
+// may be scheduled while the previous kernel on its stream is finishing; it
+// calls griddep_wait() before its first global-memory access, which returns
+// once that kernel has completed and its writes are visible (a no-op for a
+// kernel launched normally).  griddep_launch_dependents() lets the next such
+// kernel be scheduled before this one exits.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // SM count of the current device (cached per device; host only)
 inline int sm_count() {
     static int count[64] = {0};
