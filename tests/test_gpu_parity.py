@@ -308,6 +308,58 @@ def test_chunk_bad_cu_seqlens_are_flagged_and_skipped(kda):
     assert (sf[1] == 7.0).all()  # the bad sequence is skipped, not written
 
 
+@pytest.mark.parametrize("scan", ["split", "wide"])
+def test_chunk_back_to_back_calls_share_one_workspace(kda, scan):
+    """Two bf16 forwards enqueued back to back on one stream with one
+    workspace and different sequence layouts: the second call's chunk index
+    must not overwrite the first call's while the first scan still reads it
+    (the index kernel is the one launch of a call that is never overlapped
+    with the previous kernel).  Each result equals the same call run alone."""
+    x1 = kda_inputs.prefill([700, 64, 333], H=4, seed=47, init_std=0.02)
+    x2 = kda_inputs.prefill([65, 1, 900, 128, 200], H=4, seed=48, init_std=0.02)
+    d1, d2 = dev(x1), dev(x2)
+    T_max = max(sum(x1["lengths"]), sum(x2["lengths"]))
+    work = torch.empty(kda.kda_chunk_workspace_bytes(T_max, 5, 4), dtype=torch.uint8, device="cuda")
+    call = lambda d: kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], cu_seqlens=d["cu_seqlens"],
+                                       initial_state=d["initial_state"], workspace=work, scan=scan)
+    alone = []
+    for d in (d1, d2):
+        o, sf = call(d)
+        torch.cuda.synchronize()
+        alone.append((o.clone(), sf.clone()))
+    outs = [call(d) for d in (d1, d2, d1, d2)]  # no synchronisation in between
+    torch.cuda.synchronize()
+    for i, (o, sf) in enumerate(outs):
+        assert torch.equal(o, alone[i % 2][0]) and torch.equal(sf, alone[i % 2][1]), i
+
+
+def test_chunk_forward_replays_from_a_cuda_graph(kda):
+    """The tensor-core forward (three kernels, two of them launched as
+    programmatic dependents) captured in a CUDA graph and replayed gives the
+    eager results, for new input values written into the captured buffers."""
+    x = kda_inputs.prefill([300, 129], H=4, seed=49)
+    y = kda_inputs.prefill([300, 129], H=4, seed=50)
+    d = dev(x)
+    work = torch.empty(kda.kda_chunk_workspace_bytes(429, 2, 4), dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(d["v"])
+    sf = torch.empty((2, 4, 128, 128), dtype=torch.float32, device="cuda")
+    kw = dict(cu_seqlens=d["cu_seqlens"], o=o, final_state=sf, workspace=work)
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], stream=cs, **kw)  # warm-up, off capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cs):
+        kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], stream=cs, **kw)
+    for src in (y, x):
+        for n in ("q", "k", "v", "g", "beta"):
+            d[n].copy_(src[n].cuda())
+        graph.replay()
+        torch.cuda.synchronize()
+        o_ref, s_ref = run_chunk(kda, src)
+        assert torch.equal(o, o_ref) and torch.equal(sf, s_ref)
+
+
 def test_chunked_and_recurrent_gpu_paths_agree_fp32(kda):
     """Same inputs through kda_chunk_fwd and through T kda_recurrent_step calls."""
     x = kda_inputs.recurrence_small()
