@@ -581,6 +581,53 @@ def test_gated_chunk_with_output_epilogue(kda, dtype, precise, scan):
     assert rel_l2(vk_to_kv(sf), s_ref) < tol
 
 
+def test_gated_prefill_4k_with_output_epilogue(kda):
+    """The bench's gated 4k workload with the output epilogue (split-layout
+    scan): sampled heads against the oracle, and every head equal, within bf16
+    rounding of o, to the forward without the epilogue followed by the
+    standalone pass (a fused epilogue would normalise the unrounded o)."""
+    y = kda_inputs.with_output_gate(kda_inputs.prefill_4k_gated(), seed=6)
+    d = dev(y, names=("q", "k", "v", "raw_gate", "raw_beta", "a_log", "dt_bias", "cu_seqlens",
+                      "out_gate", "norm_weight"))
+    args = (d["q"], d["k"], d["v"], d["raw_gate"], d["raw_beta"], d["a_log"], d["dt_bias"])
+    kw = dict(lower_bound=y["lower_bound"], cu_seqlens=d["cu_seqlens"], scan="split")
+    o, sf = kda.kda_chunk_fwd_gated(*args, out_gate=d["out_gate"], norm_weight=d["norm_weight"],
+                                    norm_eps=y["norm_eps"], **kw)
+    o2, sf2 = kda.kda_chunk_fwd_gated(*args, **kw)
+    kda.kda_output_gate_norm(o2, d["out_gate"], d["norm_weight"], y["norm_eps"])
+    torch.cuda.synchronize()
+    assert torch.equal(sf, sf2)
+    assert rel_l2(to_np(o), to_np(o2)) < 4e-3  # unrounded vs bf16-rounded o before the norm
+    heads = [5, 30]
+    g_ref, b_ref = oracle.gate_activation(y["raw_gate"][:, heads], y["raw_beta"][:, heads],
+                                          y["a_log"][heads], y["dt_bias"][heads], y["lower_bound"])
+    o_ref, _ = oracle.recurrence(y["q"][:, heads], y["k"][:, heads], y["v"][:, heads], g_ref, b_ref,
+                                 cu_seqlens=y["cu_seqlens"].numpy())
+    out_ref = oracle.output_gate_norm(o_ref, y["out_gate"][:, heads], y["norm_weight"], y["norm_eps"])
+    assert rel_l2(to_np(o[:, heads]), out_ref) < TOL_BF16
+
+
+@pytest.mark.parametrize("lengths", [[200, 1, 64, 129], [63, 0, 650]])
+def test_gated_chunk_epilogue_split_scan_ragged(kda, lengths):
+    x = kda_inputs.prefill(lengths, H=3, seed=63, init_std=0.02)
+    y, g_ref, b_ref = _gated(x, 63, "lower_bound")
+    y = kda_inputs.with_output_gate(y, seed=63)
+    d = dev(y, names=("q", "k", "v", "raw_gate", "raw_beta", "a_log", "dt_bias", "cu_seqlens",
+                      "initial_state", "out_gate", "norm_weight"))
+    o, sf = kda.kda_chunk_fwd_gated(d["q"], d["k"], d["v"], d["raw_gate"], d["raw_beta"], d["a_log"],
+                                    d["dt_bias"], lower_bound=y["lower_bound"], out_gate=d["out_gate"],
+                                    norm_weight=d["norm_weight"], norm_eps=y["norm_eps"],
+                                    cu_seqlens=d["cu_seqlens"], initial_state=d["initial_state"],
+                                    scan="split")
+    torch.cuda.synchronize()
+    s0 = np.swapaxes(y["initial_state"].double().numpy(), -1, -2)
+    o_ref, s_ref = oracle.recurrence(y["q"], y["k"], y["v"], g_ref, b_ref,
+                                     cu_seqlens=y["cu_seqlens"].numpy(), initial_state=s0)
+    out_ref = oracle.output_gate_norm(o_ref, y["out_gate"], y["norm_weight"], y["norm_eps"])
+    assert rel_l2(to_np(o), out_ref) < TOL_BF16
+    assert rel_l2(vk_to_kv(sf), s_ref) < TOL_BF16
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_output_gate_norm_standalone(kda, dtype):
     gen = torch.Generator().manual_seed(63)
