@@ -413,7 +413,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         //    clamped at exp(80) on the block diagonal; where l_j < 1e-30 those
         //    entries are taken as exponentials directly.
         //    A thread takes rows r and 63 - r: five column blocks in total.
-#pragma unroll 1
+#pragma unroll  // both rows in one body: their shuffles and exponentials interleave
         for (int it = 0; it < 2; ++it) {
             const int r = it == 0 ? (tid >> 4) : 63 - (tid >> 4), d0 = (tid & 15) * 8, bj = r >> 4;
             float rel8[8], qv[8], kv[8];
