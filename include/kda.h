@@ -373,6 +373,23 @@ int kda_recurrent_step_gated(const void *q, const void *k, const void *v, const 
                              int H, int K, int V, float scale, int dtype, void *stream);
 
 /*
+ * kda_recurrent_multi_step from the model's raw gates, with the optional
+ * output epilogue: the speculative decode as the model's fused decode runs it
+ * (raw decay and beta, num_accepted_tokens, per-token state slots).
+ *   raw_gate [N, S, H, K] and raw_beta [N, S, H] in the q dtype;
+ *   out_gate [N, S, H, V] in the q dtype or NULL.
+ * The gate and the epilogue are as for kda_recurrent_step_gated, the slots
+ * and counts as for kda_recurrent_multi_step.
+ */
+int kda_recurrent_multi_step_gated(const void *q, const void *k, const void *v,
+                                   const void *raw_gate, const void *raw_beta, const float *a_log,
+                                   const float *dt_bias, float lower_bound, int use_lower_bound,
+                                   const void *out_gate, const float *norm_weight, float norm_eps,
+                                   float *state_pool, const int32_t *state_indices,
+                                   const int32_t *num_accepted, int64_t n_slots, void *o, int N,
+                                   int S, int H, int K, int V, float scale, int dtype, void *stream);
+
+/*
  * The output epilogue alone, in place on o [rows, V] (rows = tokens x heads,
  * V = 128, dtype as q): each row becomes
  *   o / sqrt(mean(o^2) + eps) * weight * sigmoid(gate)

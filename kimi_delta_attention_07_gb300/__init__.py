@@ -36,7 +36,7 @@ EXPORTS = ("kda_status_string", "kda_version", "kda_chunk_workspace_bytes", "kda
            "kda_chunk_intra", "kda_chunk_scan", "kda_workspace_status", "kda_recurrent_step",
            "kda_chunk_fwd_noalloc", "kda_chunk_fwd_gated", "kda_recurrent_step_gated",
            "kda_output_gate_norm", "kda_recurrent_multi_step", "kda_short_conv_fwd",
-           "kda_short_conv_update", "kda_short_conv_multi_update")
+           "kda_short_conv_update", "kda_short_conv_multi_update", "kda_recurrent_multi_step_gated")
 NOALLOC_WORKSPACE_BYTES = 64 * 1024 * 1024
 
 _lib = None
@@ -95,6 +95,10 @@ def load(path: str | None = None):
         L.kda_recurrent_multi_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, vp, i32, i32,
                                                i32, i32, i32, f32, i32, vp]
         L.kda_recurrent_multi_step.restype = i32
+        L.kda_recurrent_multi_step_gated.argtypes = [vp, vp, vp, vp, vp, vp, vp, f32, i32, vp, vp, f32,
+                                                     vp, vp, vp, i64, vp, i32, i32, i32, i32, i32, f32,
+                                                     i32, vp]
+        L.kda_recurrent_multi_step_gated.restype = i32
         L.kda_short_conv_fwd.argtypes = [vp, vp, vp, vp, i32, i64, i32, i32, i32, vp, vp, vp, i64,
                                          i32, vp]
         L.kda_short_conv_fwd.restype = i32
@@ -372,6 +376,44 @@ def kda_recurrent_multi_step(q, k, v, g, beta, state_pool, state_indices, *, num
                                          _p(o), N, S, H, K, V, float(scale), dt, _stream(stream))
     if st != KDA_OK:
         raise KdaError(st, "kda_recurrent_multi_step")
+    return o
+
+
+def kda_recurrent_multi_step_gated(q, k, v, raw_gate, raw_beta, a_log, dt_bias, state_pool,
+                                   state_indices, *, num_accepted=None, lower_bound=None,
+                                   out_gate=None, norm_weight=None, norm_eps=1e-6, scale=None,
+                                   o=None, stream=None):
+    """kda_recurrent_multi_step from the model's raw gates (raw_gate
+    [N, S, H, K], raw_beta [N, S, H], q dtype), with the optional output
+    epilogue (out_gate [N, S, H, V]); see kda_recurrent_step_gated."""
+    N, S, H, K = q.shape
+    V = v.shape[-1]
+    dt = _dtype_code(q)
+    for name, t, dtype_, shape in (("q", q, q.dtype, (N, S, H, K)), ("k", k, q.dtype, (N, S, H, K)),
+                                   ("v", v, q.dtype, (N, S, H, V)),
+                                   ("raw_gate", raw_gate, q.dtype, (N, S, H, K)),
+                                   ("raw_beta", raw_beta, q.dtype, (N, S, H)),
+                                   ("state_pool", state_pool, torch.float32, None),
+                                   ("state_indices", state_indices, torch.int32, (N, S)),
+                                   ("num_accepted", num_accepted, torch.int32, (N,))):
+        _check(t, name, dtype_, shape)
+    _check_gate(a_log, dt_bias, H, K)
+    _check_epilogue(out_gate, norm_weight, (N, S, H, V), q.dtype)
+    if state_pool.dim() != 4 or tuple(state_pool.shape[1:]) != (H, V, K):
+        raise ValueError(f"state_pool must be [slots, {H}, {V}, {K}]")
+    if o is None:
+        o = torch.empty((N, S, H, V), dtype=q.dtype, device=q.device)
+    _check(o, "o", q.dtype, (N, S, H, V))
+    if scale is None:
+        scale = K ** -0.5
+    st = load().kda_recurrent_multi_step_gated(
+        _p(q), _p(k), _p(v), _p(raw_gate), _p(raw_beta), _p(a_log), _p(dt_bias),
+        float(0.0 if lower_bound is None else lower_bound), int(lower_bound is not None),
+        _p(out_gate), _p(norm_weight), float(norm_eps), _p(state_pool), _p(state_indices),
+        _p(num_accepted), state_pool.shape[0], _p(o), N, S, H, K, V, float(scale), dt,
+        _stream(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_recurrent_multi_step_gated")
     return o
 
 

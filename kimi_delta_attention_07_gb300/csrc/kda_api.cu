@@ -271,6 +271,19 @@ int kda_recurrent_step_gated(const void *q, const void *k, const void *v, const 
                      n_slots, o, N, H, K, V, scale, dtype, stream);
 }
 
+int kda_recurrent_multi_step_gated(const void *q, const void *k, const void *v,
+                                   const void *raw_gate, const void *raw_beta, const float *a_log,
+                                   const float *dt_bias, float lower_bound, int use_lower_bound,
+                                   const void *out_gate, const float *norm_weight, float norm_eps,
+                                   float *state_pool, const int32_t *state_indices,
+                                   const int32_t *num_accepted, int64_t n_slots, void *o, int N,
+                                   int S, int H, int K, int V, float scale, int dtype, void *stream) {
+    const GateArgs gate{raw_gate, raw_beta, a_log, dt_bias, lower_bound, use_lower_bound != 0};
+    const EpiArgs epi{out_gate, norm_weight, norm_eps};
+    return step_call(q, k, v, nullptr, nullptr, &gate, &epi, state_pool, state_indices, num_accepted,
+                     S, n_slots, o, N, H, K, V, scale, dtype, stream);
+}
+
 int kda_short_conv_fwd(const void *x, const void *weight, void *y, const int32_t *cu_seqlens,
                        int n_seqs, int64_t total_tokens, int D, int ks, int activation,
                        const void *initial_states, void *final_states,

@@ -182,6 +182,24 @@ def test_multi_step_rejects_bad_arguments_without_launching(lib):
     assert f(g=base + 4) == kda.KDA_ERR_INVALID_ARG
     assert f(dt=2) == kda.KDA_ERR_INVALID_ARG
 
+    def fg(**kw):  # the gated form: raw gates, gate parameters, optional epilogue
+        a = dict(q=base, k=base, v=base, rg=base, rb=base, alog=base, bias=base, lb=-5.0, og=None,
+                 nw=None, eps=1e-6, pool=base, idx=base, acc=None, slots=8, o=base, N=2, S=3, H=2,
+                 dt=kda.KDA_BF16)
+        a.update(kw)
+        return lib.kda_recurrent_multi_step_gated(
+            p(a["q"]), p(a["k"]), p(a["v"]), p(a["rg"]), p(a["rb"]), p(a["alog"]), p(a["bias"]),
+            a["lb"], 1, p(a["og"]), p(a["nw"]), a["eps"], p(a["pool"]), p(a["idx"]), p(a["acc"]),
+            a["slots"], p(a["o"]), a["N"], a["S"], a["H"], 128, 128, 0.1, a["dt"], None)
+
+    assert fg(N=0) == kda.KDA_OK
+    assert fg(S=0) == kda.KDA_ERR_INVALID_ARG
+    assert fg(idx=None) == kda.KDA_ERR_INVALID_ARG
+    assert fg(rg=None) == kda.KDA_ERR_INVALID_ARG
+    assert fg(alog=None) == kda.KDA_ERR_INVALID_ARG
+    assert fg(og=base, nw=None) == kda.KDA_ERR_INVALID_ARG   # an epilogue needs its weight
+    assert fg(og=base, nw=base, eps=0.0) == kda.KDA_ERR_INVALID_ARG
+
 
 def test_short_conv_rejects_bad_arguments_without_launching(lib):
     base = 1 << 20

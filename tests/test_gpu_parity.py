@@ -671,6 +671,37 @@ def test_multi_step_matches_oracle(kda, dtype):
     assert torch.equal(pool_d.cpu()[bad_slots], pool[bad_slots])
 
 
+@pytest.mark.parametrize("epilogue", [False, True])
+@pytest.mark.parametrize("gate", list(GATES))
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_gated_multi_step_matches_oracle(kda, dtype, gate, epilogue):
+    """The speculative decode from the model's raw gates (both gate forms),
+    with and without the output epilogue: the oracle's gate activation, then
+    its multi-token step from the accepted slot, then its output epilogue."""
+    N, S, H, slots = 4, 3, 2, 16
+    tok = kda_inputs.spec_tokens(N, S, H=H, dtype=dtype, seed=72)
+    y, g_ref, b_ref = _gated(tok, 72, gate)
+    y = kda_inputs.with_output_gate(y, seed=72)
+    pool = kda_inputs.decode_pool(slots, H=H, seed=72)
+    idx = torch.tensor([[3, 8, 1], [0, 5, 12], [7, 2, 9], [4, 6, 10]], dtype=torch.int32)
+    acc = torch.tensor([2, 1, 3, 3], dtype=torch.int32)
+    pool_d = pool.cuda()
+    names = ("q", "k", "v", "raw_gate", "raw_beta", "a_log", "dt_bias")
+    o = kda.kda_recurrent_multi_step_gated(
+        *(y[n].cuda() for n in names), pool_d, idx.cuda(), num_accepted=acc.cuda(),
+        lower_bound=y["lower_bound"], out_gate=y["out_gate"].cuda() if epilogue else None,
+        norm_weight=y["norm_weight"].cuda() if epilogue else None, norm_eps=y["norm_eps"])
+    torch.cuda.synchronize()
+    p0 = np.swapaxes(pool.double().numpy(), -1, -2)
+    o_ref, pool_ref = oracle.multi_step(y["q"], y["k"], y["v"], g_ref, b_ref, p0, idx.numpy(),
+                                        num_accepted=acc.numpy())
+    if epilogue:
+        o_ref = oracle.output_gate_norm(o_ref, y["out_gate"], y["norm_weight"], y["norm_eps"])
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    assert rel_l2(to_np(o), o_ref) < tol
+    assert rel_l2(vk_to_kv(pool_d), pool_ref) < TOL_F32
+
+
 def test_multi_step_with_one_token_equals_the_step(kda):
     N, H = 5, 3
     tok = kda_inputs.decode_tokens(N, H=H, seed=72)
