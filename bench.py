@@ -627,8 +627,32 @@ def run_spec_decode(kda, dev, stream, pk, S=4, steps=16):
     us = statistics.median([a.elapsed_time(b) * 1e3 for a, b in evs])
     nbytes = (1 + S) * DEC_N * H * V * K * 4 + S * DEC_N * H * (3 * K * 2 + K * 4 + 4 + V * 2)
     gbs = nbytes / (us * 1e-6) / 1e9
-    del pool
-    return {"verify_width": S, "us_per_step": round(us, 2),
+    # the model's form: raw gates in, output epilogue out (same pool, continued)
+    gtoks = [kda_inputs.with_output_gate(kda_inputs.with_raw_gates(t, seed=74), seed=75) for t in
+             (kda_inputs.spec_tokens(DEC_N, S, H=H, seed=74, step=i) for i in range(2))]
+    names = ("q", "k", "v", "raw_gate", "raw_beta", "a_log", "dt_bias")
+    gd = [{n: t[n].to(dev) for n in names + ("out_gate", "norm_weight")} for t in gtoks]
+
+    def gone(i):
+        t = gd[i % len(gd)]
+        kda.kda_recurrent_multi_step_gated(*(t[n] for n in names), pool, idx, num_accepted=acc,
+                                           lower_bound=-5.0, out_gate=t["out_gate"],
+                                           norm_weight=t["norm_weight"], norm_eps=1e-5, o=o,
+                                           stream=stream)
+
+    for i in range(2):
+        gone(i)
+    torch.cuda.synchronize()
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(8)]
+    for i in range(8):
+        gev[i][0].record(stream)
+        gone(i)
+        gev[i][1].record(stream)
+    torch.cuda.synchronize()
+    gus = statistics.median([a.elapsed_time(b) * 1e3 for a, b in gev])
+    del pool, gd, gtoks
+    return {"verify_width": S, "us_per_step": round(us, 2), "gated_epilogue_us_per_step": round(gus, 2),
             "tokens_per_s": round(DEC_N * S / (us * 1e-6), 1),
             "roofline": {"bound": "hbm", "algorithmic_bytes": nbytes, "achieved": round(gbs, 1),
                          "peak": pk["hbm"], "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4)}}
