@@ -151,6 +151,9 @@ __global__ void __launch_bounds__(kDecodeThreads)
                                 const int32_t *__restrict__ num_accepted, int64_t n_slots,
                                 T *__restrict__ o, int S, int H, int rows_per_cta, float scale) {
     __shared__ float s_part[kWarps];  // epilogue: per-warp sums of o^2
+    // GATED: the decay factors of token t in buffer t & 1, activated once per CTA
+    // (16 channels per warp) at the end of token t - 1
+    __shared__ __align__(16) float s_dec[2][kHeadDim];
     const int pair = blockIdx.x;  // n * H + h
     const int n = pair / H;
     const int h = pair - n * H;
@@ -193,7 +196,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
     // A token's inputs, fetched one token ahead so that their latency overlaps
     // the previous token's row updates.
     struct TokIn {
-        float4 q4, k4, g4;  // g4: raw gate + dt_bias when GATED, else g
+        float4 q4, k4, g4;  // g4: g (not GATED)
+        float gx;           // GATED: raw gate + dt_bias of channel 16 warp + lane (lanes 0-15)
         float vrow, b;      // vrow: v of the warp's row `lane`; b: beta (raw when GATED)
         float gate_o, w_o;  // epilogue: output gate and norm weight of row `lane`
     };
@@ -212,9 +216,9 @@ __global__ void __launch_bounds__(kDecodeThreads)
         in.q4 = load4(q + io_k + 4 * lane);
         in.k4 = load4(k + io_k + 4 * lane);
         if (GATED) {
-            const float4 r4 = load4(reinterpret_cast<const T *>(gate.raw_gate) + io_k + 4 * lane);
-            const float4 c4 = load4(gate.dt_bias + (int64_t)h * kHeadDim + 4 * lane);
-            in.g4 = make_float4(r4.x + c4.x, r4.y + c4.y, r4.z + c4.z, r4.w + c4.w);
+            const int c = 16 * warp + (lane & 15);
+            in.gx = to_f32(reinterpret_cast<const T *>(gate.raw_gate)[io_k + c]) +
+                    gate.dt_bias[(int64_t)h * kHeadDim + c];
             in.b = to_f32(reinterpret_cast<const T *>(gate.raw_beta)[pt]);
         } else {
             in.g4 = load4(g + io_k + 4 * lane);
@@ -223,24 +227,29 @@ __global__ void __launch_bounds__(kDecodeThreads)
         return in;
     };
     TokIn nxt = fetch(0);
+    const float gscale = GATED ? expf(gate.a_log[h]) : 0.0f;
+    auto activate = [&](const TokIn &in, int buf) {  // GATED: one channel per lane 0-15
+        if (lane < 16)
+            s_dec[buf][16 * warp + lane] =
+                expf(gate_decay(in.gx, gscale, gate.lower_bound, gate.use_lower_bound != 0));
+    };
+    if (GATED) {
+        activate(nxt, 0);
+        __syncthreads();
+    }
     for (int t = 0; t < S; ++t) {
         const TokIn cur = nxt;
         if (t + 1 < S) nxt = fetch(t + 1);
         const int64_t io_k = io_of(t);
         const float vrow = cur.vrow, gate_o = cur.gate_o, w_o = cur.w_o;
         const float4 q4 = cur.q4, k4 = cur.k4;
-        float4 g4;
+        float4 dec;
         float b;
         if (GATED) {
-            const float gs = expf(gate.a_log[h]);
-            const bool lb = gate.use_lower_bound != 0;
-            g4 = make_float4(gate_decay(cur.g4.x, gs, gate.lower_bound, lb),
-                             gate_decay(cur.g4.y, gs, gate.lower_bound, lb),
-                             gate_decay(cur.g4.z, gs, gate.lower_bound, lb),
-                             gate_decay(cur.g4.w, gs, gate.lower_bound, lb));
+            dec = *reinterpret_cast<const float4 *>(&s_dec[t & 1][4 * lane]);
             b = gate_beta(cur.b);
         } else {
-            g4 = cur.g4;
+            dec = make_float4(expf(cur.g4.x), expf(cur.g4.y), expf(cur.g4.z), expf(cur.g4.w));
             b = cur.b;
         }
         const float sq = warp_sum(q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w);
@@ -249,7 +258,6 @@ __global__ void __launch_bounds__(kDecodeThreads)
         const float rk = 1.0f / sqrtf(sk + 1e-6f);
         const float4 qh = make_float4(q4.x * rq, q4.y * rq, q4.z * rq, q4.w * rq);
         const float4 kh = make_float4(k4.x * rk, k4.y * rk, k4.z * rk, k4.w * rk);
-        const float4 dec = make_float4(expf(g4.x), expf(g4.y), expf(g4.z), expf(g4.w));
         const float kq = warp_sum(kh.x * qh.x + kh.y * qh.y + kh.z * qh.z + kh.w * qh.w);
 
         float *Sd = pool + ((slot_of(t) * H + h) * (int64_t)kHeadDim) * kHeadDim;  // destination
@@ -279,6 +287,9 @@ __global__ void __launch_bounds__(kDecodeThreads)
                 o[io_k + r] = from_f32<T>(ov);
             }
         }
+        // the next token's decays into the other buffer (read by every warp at the
+        // top of token t - 1, before the barrier that ended it)
+        if (GATED && t + 1 < S) activate(nxt, (t + 1) & 1);
         if (EPI) {  // rows_per_cta == 128: this CTA holds the head's whole output row
             if (lane == 0) s_part[warp] = ss;
             __syncthreads();
@@ -289,6 +300,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
             if (lane < rpw)
                 o[io_k + row0 + warp + kWarps * lane] = from_f32<T>(my_o * rn * w_o * gate_beta(gate_o));
             __syncthreads();  // s_part is rewritten by the next token
+        } else if (GATED && t + 1 < S) {
+            __syncthreads();  // the next token's decays are in place
         }
     }
 }
