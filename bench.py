@@ -31,6 +31,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 import kda_inputs  # noqa: E402
@@ -55,10 +56,31 @@ def parse():
     p.add_argument("--precise", action="store_true", help="fp32 CUDA-core chunk path")
     p.add_argument("--no-gated", action="store_true", help="skip the raw-gate prefill sub-run")
     p.add_argument("--no-conv", action="store_true", help="skip the short-convolution sub-run")
+    p.add_argument("--no-varlen", action="store_true", help="skip the varlen_8 prefill sub-run")
+    p.add_argument("--no-long", action="store_true",
+                   help="skip the long_131k prefill + hand-off decode sub-run")
     return p.parse_args()
 
 
 # ---- distributed plumbing --------------------------------------------------
+
+def free_port():
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def spawn_ranks(n, script, argv, env=None, timeout=None):
+    """Run `script argv` as n local ranks (one process per GPU) under
+    torch.distributed.run on 127.0.0.1; each rank reads RANK / LOCAL_RANK /
+    WORLD_SIZE / MASTER_* from its environment.  Returns the launcher's exit
+    code; the ranks' stdout (rank 0's JSON line) passes through."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes", "1",
+           "--nproc-per-node", str(n), "--master-addr", "127.0.0.1",
+           "--master-port", str(free_port()), script, *argv]
+    return subprocess.run(cmd, env=env, timeout=timeout).returncode
+
 
 def dist_setup(backend):
     ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -247,6 +269,152 @@ def run_gated(args, kda, dev, stream, ws):
             "roofline": {"bound": "hbm", "algorithmic_bytes": byt,
                          "achieved": round(byt / (ms / 1e3) / 1e9, 1), "peak": pk["hbm"],
                          "unit": "GB/s", "frac": round(byt / (ms / 1e3) / 1e9 / pk["hbm"], 4)}}
+
+
+def time_prefill(kda, d, cu, init, steps, warmup, stream, ws, fin=None, idx=None):
+    """Device time of the chunked forward on resident inputs: whole call and
+    its two phases (CUDA events on the launch stream), ms per call."""
+    T, Hh, _ = d["q"].shape
+    N = cu.numel() - 1
+    o = torch.empty((T, Hh, V), dtype=torch.bfloat16, device=d["q"].device)
+    if fin is None:
+        fin = torch.empty((N, Hh, V, K), dtype=torch.float32, device=d["q"].device)
+    need = kda.kda_chunk_workspace_bytes(T, N, Hh)
+    work = torch.empty(need, dtype=torch.uint8, device=d["q"].device)
+    kw = dict(cu_seqlens=cu, initial_state=init, o=o, final_state=fin, state_indices=idx,
+              workspace=work, stream=stream)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], phase="intra", **kw)
+        if ev is not None:
+            ev[1].record(stream)
+        kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], phase="scan", **kw)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(max(3, warmup)):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        step(evs[i])
+    torch.cuda.synchronize()
+    tot = [e[0].elapsed_time(e[2]) for e in evs]
+    intra = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    scan = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    ms = max_over_ranks(statistics.mean(tot), ws, d["q"].device)
+    status = kda.kda_workspace_status(work, stream)
+    del work
+    return ms, intra, scan, o, fin, status
+
+
+def _hbm_roof(nbytes, ms, pk):
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "algorithmic_bytes": int(nbytes), "achieved": round(gbs, 1),
+            "peak": pk["hbm"], "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4)}
+
+
+def _oracle_tokens_per_s(x, heads, t_max=None):
+    """The oracle (fp64 recurrence, OpenMP over sequence x head) on the listed
+    heads of the first t_max tokens of each sequence; all-head tokens/s."""
+    import oracle
+    oracle.build()
+    cu = x["cu_seqlens"].numpy()
+    if t_max is not None:
+        lens = [min(int(cu[i + 1] - cu[i]), t_max) for i in range(len(cu) - 1)]
+        rows = torch.cat([torch.arange(int(cu[i]), int(cu[i]) + lens[i]) for i in range(len(lens))])
+        sub_cu = torch.zeros(len(lens) + 1, dtype=torch.int64)
+        sub_cu[1:] = torch.cumsum(torch.tensor(lens), 0)
+    else:
+        rows, sub_cu = torch.arange(int(cu[-1])), torch.tensor(cu, dtype=torch.int64)
+    sub = {n: x[n][rows][:, heads].contiguous() for n in ("q", "k", "v", "g", "beta")}
+    s0 = x.get("initial_state")
+    s0 = None if s0 is None else torch.swapaxes(s0[:, heads], -1, -2).double().numpy()
+    cores = oracle.max_threads()
+    t = time.perf_counter()
+    oracle.recurrence(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"],
+                      cu_seqlens=sub_cu.numpy().astype(np.int32), initial_state=s0, n_threads=cores)
+    dt = time.perf_counter() - t
+    tokens = rows.numel() * len(heads) / x["H"]
+    return {"value": round(tokens / dt, 1), "unit": "tokens/s", "kind": "oracle",
+            "cores": min(cores, len(heads) * (len(sub_cu) - 1)), "seconds": round(dt, 3),
+            "sample": (f"{len(heads)} of {x['H']} heads x "
+                       f"{'all' if t_max is None else f'the first {t_max}'} tokens of each of "
+                       f"{len(sub_cu) - 1} sequence(s), fp64 token recurrence, OpenMP over "
+                       f"(sequence, head)")}
+
+
+def run_varlen(args, kda, dev, stream, pk, ws, rank):
+    """varlen_8: 8 packed sequences, lengths U{512..8192} (seeded), H=32, bf16,
+    nonzero fp32 initial states: one chunked forward over all of them."""
+    x = kda_inputs.varlen_8()
+    d = {n: x[n].to(dev) for n in ("q", "k", "v", "g", "beta")}
+    cu, s0 = x["cu_seqlens"].to(dev), x["initial_state"].to(dev)
+    T, N = int(x["cu_seqlens"][-1]), len(x["lengths"])
+    ms, intra, scan, o, fin, status = time_prefill(kda, d, cu, s0, args.steps, args.warmup,
+                                                   stream, ws)
+    nb = prefill_bytes(T, H)["intra"] + T * H * V * 2 + 2 * N * H * V * K * 4
+    wide = N * H * 4 > torch.cuda.get_device_properties(dev).multi_processor_count
+    out = {"workload": "varlen_8", "lengths": x["lengths"], "T": T, "H": H,
+           "tokens_per_s": round(T * ws / (ms * 1e-3), 1), "ms_per_step": round(ms, 4),
+           "kernels_ms": {"kda_chunk_intra": round(intra, 4), "kda_chunk_scan": round(scan, 4)},
+           "scan_layout": "wide (one CTA per sequence x head)" if wide else "split",
+           "roofline": dict(_hbm_roof(nb, ms, pk), note="q,k,v,g,beta,o + initial and final states"),
+           "workspace_status": status, "steps": args.steps}
+    del d, o, fin
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = _oracle_tokens_per_s(x, heads=[0, 1])
+    return out
+
+
+def run_long(args, kda, dev, stream, pk, ws, rank):
+    """long_131k: B=1, T=131072, H=32, bf16, decay mix 90% U[-0.01,-1e-5] /
+    10% U[-3,-1]; the final state is handed into slot 1 of a 2-slot pool and
+    256 decode steps continue from it (fresh seeded tokens per step, all
+    pre-staged on the device), replayed from one CUDA graph."""
+    x = kda_inputs.long_131k()
+    d = {n: x[n].to(dev) for n in ("q", "k", "v", "g", "beta")}
+    cu = x["cu_seqlens"].to(dev)
+    T = int(x["cu_seqlens"][-1])
+    pool = torch.zeros((2, H, V, K), dtype=torch.float32, device=dev)
+    idx = torch.tensor([1], dtype=torch.int32, device=dev)
+    steps = max(2, min(args.steps, 5))
+    ms, intra, scan, o, _, status = time_prefill(kda, d, cu, None, steps, min(args.warmup, 3),
+                                                 stream, ws, fin=pool, idx=idx)
+    nb = prefill_bytes(T, H)["step"]
+    del d, o
+    # hand-off decode: B=1, 32 heads, state slot 1 (2 MiB, resident in L2)
+    toks = [kda_inputs.decode_tokens(1, H=H, seed=4, step=t, g_mixed=True) for t in range(256)]
+    toks = [{n: t[n].to(dev) for n in ("q", "k", "v", "g", "beta")} for t in toks]
+    o1 = torch.empty((256, 1, H, V), dtype=torch.bfloat16, device=dev)
+
+    def dstep(i, st):
+        t = toks[i]
+        kda.kda_recurrent_step(t["q"], t["k"], t["v"], t["g"], t["beta"], pool, state_indices=idx,
+                               o=o1[i], stream=st)
+
+    for i in range(3):
+        dstep(i, stream)
+    torch.cuda.synchronize()
+    us = _graph_us(dstep, 256, stream, reps=3)
+    out = {"workload": "long_131k", "T": T, "H": H,
+           "prefill": {"tokens_per_s": round(T * ws / (ms * 1e-3), 1), "ms_per_step": round(ms, 4),
+                       "kernels_ms": {"kda_chunk_intra": round(intra, 4),
+                                      "kda_chunk_scan": round(scan, 4)},
+                       "roofline": dict(_hbm_roof(nb, ms, pk),
+                                        note="bound in practice by 2048 sequential chunk steps per head"),
+                       "workspace_status": status, "steps": steps},
+           "handoff_decode": {"steps": 256, "us_per_step": round(us, 3),
+                              "timing": "256 steps from the handed-off pool slot, one CUDA graph replay",
+                              "l2_resident": "the 2 MiB state and 40 KB of inputs per step stay in L2",
+                              "launches_per_step": 1}}
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = _oracle_tokens_per_s(x, heads=list(range(16)), t_max=8192)
+    return out
 
 
 def _graph_us(fn, n, stream, reps=5):
@@ -439,6 +607,8 @@ def run_ours(args, rank, ws):
     dec = None if args.no_decode else run_decode(args, kda, dev, stream, pk, ws)
     gated = None if (args.no_gated or args.precise) else run_gated(args, kda, dev, stream, ws)
     conv = None if args.no_conv else run_conv(args, kda, dev, stream, pk)
+    varlen = None if (args.no_varlen or args.precise) else run_varlen(args, kda, dev, stream, pk, ws, rank)
+    long_ = None if (args.no_long or args.precise) else run_long(args, kda, dev, stream, pk, ws, rank)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(x, sample_heads=H)
@@ -458,7 +628,8 @@ def run_ours(args, rank, ws):
                        "path": "fp32 CUDA-core (precise)" if args.precise else "default"},
             "roofline": roofline, "step_roofline": step_roofline, "kernels": kernels,
             "e2e": e2e, "gpu_launches": launches, "clocks": clk,
-            "decode": dec, "gated": gated, "short_conv": conv, "cpu_baseline": cpu,
+            "decode": dec, "gated": gated, "short_conv": conv, "varlen_8": varlen,
+            "long_131k": long_, "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
 
@@ -720,6 +891,14 @@ def run_reference(args, rank, ws):
 
 def main():
     args = parse()
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # `bench.py --gpus N` started directly: launch the N ranks ourselves
+        if args.impl != "reference" and torch.cuda.device_count() < args.gpus:
+            sys.exit(f"bench.py: --gpus {args.gpus} but only {torch.cuda.device_count()} "
+                     f"CUDA device(s) are visible")
+        sys.exit(spawn_ranks(args.gpus, os.path.abspath(__file__), sys.argv[1:]))
+    if int(os.environ.get("WORLD_SIZE", "1")) != args.gpus:
+        sys.exit(f"bench.py: WORLD_SIZE={os.environ.get('WORLD_SIZE')} but --gpus {args.gpus}")
     if args.impl == "reference":
         rank, ws = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
         run_reference(args, rank, ws)

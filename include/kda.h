@@ -45,8 +45,15 @@
  * call returns a kda_status other than KDA_OK and enqueues nothing.  A
  * failed kernel launch returns KDA_ERR_CUDA (the CUDA error is cleared).
  * Errors that only the device can see (bad cu_seqlens, a slot index out of
- * range) never cause an out-of-bounds access; they are reported as stated
- * per entry point.
+ * range, a bounded wait that gave up) never cause an out-of-bounds access;
+ * they are reported as stated per entry point (the chunked forward: the
+ * KDA_WS_* bits of its workspace status word).
+ *
+ * Pending CUDA errors: before launching, every entry point reads and thereby
+ * clears the calling thread's pending (non-sticky) CUDA runtime error with
+ * cudaGetLastError(), so that a failed launch of its own is not mistaken for
+ * an earlier one.  A caller that needs its own pending error must read it
+ * (cudaGetLastError / cudaPeekAtLastError) before calling into libkda.
  */
 #ifndef KDA_H_
 #define KDA_H_
@@ -63,7 +70,8 @@ typedef enum {
     KDA_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad dtype, ... */
     KDA_ERR_UNSUPPORTED = 2, /* valid request outside what is built (K, V != 128) */
     KDA_ERR_WORKSPACE = 3,   /* workspace NULL, too small or misaligned */
-    KDA_ERR_CUDA = 4         /* a CUDA runtime call or kernel launch failed */
+    KDA_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+    KDA_ERR_DEVICE_TIMEOUT = 5 /* a bounded device-side wait gave up (see KDA_WS_TIMEOUT) */
 } kda_status;
 
 typedef enum {
@@ -133,7 +141,7 @@ size_t kda_chunk_workspace_bytes(int64_t total_tokens, int n_seqs, int H, int K,
  * A zero-length sequence hands back its initial state (or zeros) as its
  * final state.  Device-side argument errors (cu_seqlens decreasing, out of
  * [0, T], or a slot index out of range) skip the offending sequence
- * (nothing of it is read or written) and set a flag that
+ * (nothing of it is read or written) and set a KDA_WS_* bit that
  * kda_workspace_status() reports.
  */
 int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
@@ -173,10 +181,37 @@ int kda_chunk_scan(const void *q, const void *k, const void *v, const float *g,
                    size_t workspace_bytes, void *stream);
 
 /*
- * Device-side error flags of the last kda_chunk_fwd that used this
- * workspace: 0 = none, bit 0 = bad cu_seqlens, bit 1 = slot index out of
- * range.  Synchronises `stream` and copies 4 bytes to the host.
- * Returns KDA_OK or KDA_ERR_CUDA / KDA_ERR_INVALID_ARG.
+ * Workspace status word: the first int32 of a chunk workspace, rewritten by
+ * every kda_chunk_fwd / kda_chunk_intra that uses it and OR-ed into by the
+ * kernels of that call.
+ */
+#define KDA_WS_BAD_SEQLENS 1 /* cu_seqlens decreasing or outside [0, T]: those sequences skipped */
+#define KDA_WS_BAD_SLOT 2    /* a state_indices entry outside [0, n_slots): that sequence skipped */
+#define KDA_WS_TIMEOUT 4     /* a bounded wait of a kernel (a copy or an MMA that never
+                                completed, ~2 s) gave up: the CTA left its remaining chunks
+                                unwritten and exited; outputs of that call are incomplete */
+#define KDA_WS_EXACT_DECAY 8 /* informational, not an error: on the tensor-core path some
+                                (chunk, head) had a decay span outside the range of the
+                                factorised exponentials (a per-channel decay of more than 40
+                                within 16 tokens, or a positive g) and was computed with exact
+                                pairwise exponentials instead */
+
+/*
+ * The kda_status that a workspace status word stands for:
+ * KDA_ERR_DEVICE_TIMEOUT if KDA_WS_TIMEOUT is set, else KDA_ERR_INVALID_ARG
+ * if KDA_WS_BAD_SEQLENS or KDA_WS_BAD_SLOT is set, else KDA_OK (the
+ * informational KDA_WS_EXACT_DECAY is not an error).  Pure host function.
+ */
+int kda_status_from_workspace_flags(int flags);
+
+/*
+ * Status word of the last kda_chunk_fwd that used this workspace
+ * (KDA_WS_* bits, 0 = none) into *flags_out.  Synchronises `stream` and
+ * copies 4 bytes to the host.  Returns KDA_ERR_CUDA if that copy fails,
+ * KDA_ERR_INVALID_ARG for NULL arguments, and otherwise
+ * kda_status_from_workspace_flags(*flags_out): KDA_ERR_DEVICE_TIMEOUT after
+ * a bounded device-side wait gave up (the mirror of the model's own
+ * raise-on-bad-input convention for errors only the device can see).
  */
 int kda_workspace_status(const void *workspace, int *flags_out, void *stream);
 
@@ -219,11 +254,17 @@ int kda_recurrent_step(const void *q, const void *k, const void *v, const float 
  * GPU that loads the library holds until the process exits.
  *
  *   - The first call on a device (with that device current) looks up the
- *     array's device address once (cudaGetSymbolAddress); make that first
- *     call before any stream capture on that device.
+ *     array's device address (cudaGetSymbolAddress) and keeps it with the
+ *     CUDA context it was taken in; make that first call before any stream
+ *     capture on that device.  The lookup is repeated only when the current
+ *     context differs (a cudaDeviceReset gives the device a new primary
+ *     context, in which the array has a new address); after such a reset,
+ *     make one call before capturing again.
  *   - Sizes whose kda_chunk_workspace_bytes(...) exceeds
  *     KDA_NOALLOC_WORKSPACE_BYTES return KDA_ERR_WORKSPACE and enqueue
  *     nothing; other argument errors are those of kda_chunk_fwd.
+ *     KDA_CHUNK_GATED in flags is ignored (this is the forward from
+ *     activated g and beta).
  *   - Every call, from any stream or thread, uses the same array.  Calls
  *     whose work overlaps on the GPU race and corrupt each other's results:
  *     order them (one stream, or events).  Nothing needs clearing between

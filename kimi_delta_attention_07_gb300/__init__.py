@@ -20,7 +20,10 @@ import torch
 
 from . import _build
 
-KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA = range(5)
+(KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA,
+ KDA_ERR_DEVICE_TIMEOUT) = range(6)
+# bits of the chunk workspace's status word (kda_workspace_status)
+KDA_WS_BAD_SEQLENS, KDA_WS_BAD_SLOT, KDA_WS_TIMEOUT, KDA_WS_EXACT_DECAY = 1, 2, 4, 8
 KDA_F32, KDA_BF16 = 0, 1
 KDA_CHUNK_PRECISE = 1
 KDA_CHUNK_SCAN_WIDE = 2
@@ -36,7 +39,8 @@ EXPORTS = ("kda_status_string", "kda_version", "kda_chunk_workspace_bytes", "kda
            "kda_chunk_intra", "kda_chunk_scan", "kda_workspace_status", "kda_recurrent_step",
            "kda_chunk_fwd_noalloc", "kda_chunk_fwd_gated", "kda_recurrent_step_gated",
            "kda_output_gate_norm", "kda_recurrent_multi_step", "kda_short_conv_fwd",
-           "kda_short_conv_update", "kda_short_conv_multi_update", "kda_recurrent_multi_step_gated")
+           "kda_short_conv_update", "kda_short_conv_multi_update", "kda_recurrent_multi_step_gated",
+           "kda_status_from_workspace_flags")
 NOALLOC_WORKSPACE_BYTES = 64 * 1024 * 1024
 
 _lib = None
@@ -68,6 +72,8 @@ def load(path: str | None = None):
         L.kda_status_string.argtypes = [i32]
         L.kda_status_string.restype = ctypes.c_char_p
         L.kda_version.restype = i32
+        L.kda_status_from_workspace_flags.argtypes = [i32]
+        L.kda_status_from_workspace_flags.restype = i32
         L.kda_chunk_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, i32, i32]
         L.kda_chunk_workspace_bytes.restype = sz
         for name in ("kda_chunk_fwd", "kda_chunk_intra", "kda_chunk_scan"):
@@ -150,6 +156,48 @@ def kda_chunk_workspace_bytes(total_tokens: int, n_seqs: int, H: int, K: int = 1
     return int(load().kda_chunk_workspace_bytes(total_tokens, n_seqs, H, K, V, dtype, flags))
 
 
+def _chunk_args(q, k, v, g, beta, cu_seqlens, n_seqs, initial_state, final_state,
+                state_indices, n_slots, o, gate_dtype):
+    """Shape, dtype and pool checks shared by the chunked entry points.
+    Returns (T, H, K, V, N, dtype code, slots)."""
+    T, H, K = q.shape
+    V = v.shape[-1]
+    dt = _dtype_code(q)
+    if cu_seqlens is not None:
+        _check(cu_seqlens, "cu_seqlens", torch.int32)
+        if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+            raise ValueError("cu_seqlens must be int32 [N+1] with N >= 1")
+        N = cu_seqlens.numel() - 1
+    else:
+        N = 1 if n_seqs is None else int(n_seqs)
+    for name, t, dtype_, shape in (("q", q, q.dtype, (T, H, K)), ("k", k, q.dtype, (T, H, K)),
+                                   ("v", v, q.dtype, (T, H, V)),
+                                   ("g", g, gate_dtype, (T, H, K)),
+                                   ("beta", beta, gate_dtype, (T, H)),
+                                   ("state_indices", state_indices, torch.int32, (N,)),
+                                   ("o", o, q.dtype, (T, H, V))):
+        _check(t, name, dtype_, shape)
+    _check(initial_state, "initial_state", torch.float32)
+    _check(final_state, "final_state", torch.float32)
+    if state_indices is None:
+        slots = 0
+        for name, t in (("initial_state", initial_state), ("final_state", final_state)):
+            if t is not None and tuple(t.shape) != (N, H, V, K):
+                raise ValueError(f"{name} must be [{N}, {H}, {V}, {K}]")
+    else:
+        if final_state is None:
+            raise ValueError("with state_indices, final_state must be the destination pool")
+        slots = final_state.shape[0] if n_slots is None else int(n_slots)
+        for name, t in (("initial_state", initial_state), ("final_state", final_state)):
+            if t is None:
+                continue
+            if t.dim() != 4 or tuple(t.shape[1:]) != (H, V, K):
+                raise ValueError(f"{name} pool must be [slots, {H}, {V}, {K}]")
+            if t.shape[0] < slots:
+                raise ValueError(f"{name} pool has {t.shape[0]} slots, fewer than n_slots = {slots}")
+    return T, H, K, V, N, dt, slots
+
+
 def kda_chunk_fwd(q, k, v, g, beta, *, cu_seqlens=None, n_seqs=None, initial_state=None,
                   final_state=None, state_indices=None, n_slots=None, scale=None,
                   precise=False, output_final_state=True, o=None, workspace=None, stream=None,
@@ -165,38 +213,13 @@ def kda_chunk_fwd(q, k, v, g, beta, *, cu_seqlens=None, n_seqs=None, initial_sta
     selects the tensor-core state-scan layout (see KDA_CHUNK_SCAN_*).
     Returns (o, final_state).
     """
-    T, H, K = q.shape
-    V = v.shape[-1]
-    dt = _dtype_code(q)
-    if cu_seqlens is not None:
-        N = cu_seqlens.numel() - 1
-    else:
-        N = 1 if n_seqs is None else int(n_seqs)
     gdt = q.dtype if _gate is not None else torch.float32  # raw gates come in the q dtype
-    for name, t, dtype_, shape in (("q", q, q.dtype, (T, H, K)), ("k", k, q.dtype, (T, H, K)),
-                                   ("v", v, q.dtype, (T, H, V)),
-                                   ("g", g, gdt, (T, H, K)),
-                                   ("beta", beta, gdt, (T, H)),
-                                   ("cu_seqlens", cu_seqlens, torch.int32, None),
-                                   ("state_indices", state_indices, torch.int32, (N,)),
-                                   ("initial_state", initial_state, torch.float32, None)):
-        _check(t, name, dtype_, shape)
-    if state_indices is None:
-        slots = 0
-        if initial_state is not None and tuple(initial_state.shape) != (N, H, V, K):
-            raise ValueError(f"initial_state must be [{N}, {H}, {V}, {K}]")
-        if final_state is None and output_final_state:
-            final_state = torch.empty((N, H, V, K), dtype=torch.float32, device=q.device)
-    else:
-        if final_state is None:
-            raise ValueError("with state_indices, final_state must be the destination pool")
-        slots = final_state.shape[0] if n_slots is None else int(n_slots)
-        if initial_state is not None and initial_state.shape[0] < slots:
-            raise ValueError("initial_state pool has fewer slots than final_state")
-    _check(final_state, "final_state", torch.float32)
+    T, H, K, V, N, dt, slots = _chunk_args(q, k, v, g, beta, cu_seqlens, n_seqs, initial_state,
+                                           final_state, state_indices, n_slots, o, gdt)
+    if state_indices is None and final_state is None and output_final_state:
+        final_state = torch.empty((N, H, V, K), dtype=torch.float32, device=q.device)
     if o is None:
         o = torch.empty((T, H, V), dtype=q.dtype, device=q.device)
-    _check(o, "o", q.dtype, (T, H, V))
     flags = (KDA_CHUNK_PRECISE if precise else 0) | _SCAN_FLAGS[scan]
     if _gate is not None:
         flags |= KDA_CHUNK_GATED
@@ -304,11 +327,24 @@ def kda_recurrent_step_gated(q, k, v, raw_gate, raw_beta, a_log, dt_bias, state_
     return o
 
 
-def kda_workspace_status(workspace, stream=None) -> int:
+def kda_status_from_workspace_flags(flags: int) -> int:
+    """The kda_status a workspace status word stands for (pure host function)."""
+    return int(load().kda_status_from_workspace_flags(int(flags)))
+
+
+def kda_workspace_status(workspace, stream=None, check=False) -> int:
+    """Status word (KDA_WS_* bits) of the last chunked forward that used this
+    workspace; synchronises the stream.  With check=True a word that stands
+    for an error (a bounded device wait that gave up, bad cu_seqlens or
+    slots) raises KdaError with that status."""
+    if workspace is None:
+        raise ValueError("workspace is required")
     out = ctypes.c_int(0)
     st = load().kda_workspace_status(_p(workspace), ctypes.byref(out), _stream(stream))
-    if st != KDA_OK:
+    if st == KDA_ERR_CUDA:
         raise KdaError(st, "kda_workspace_status")
+    if check and st != KDA_OK:
+        raise KdaError(st, f"kda_workspace_status (flags {int(out.value):#x})")
     return int(out.value)
 
 
@@ -507,25 +543,20 @@ def kda_short_conv_multi_update(x, weight, state_pool, state_indices, *, num_acc
     return y
 
 
-def kda_chunk_fwd_noalloc(q, k, v, g, beta, *, cu_seqlens=None, n_seqs=None, initial_state=None,
-                          final_state=None, state_indices=None, n_slots=None, scale=None,
-                          precise=False, o=None, stream=None):
+def kda_chunk_fwd_noalloc(q, k, v, g, beta, *, o, final_state=None, cu_seqlens=None, n_seqs=None,
+                          initial_state=None, state_indices=None, n_slots=None, scale=None,
+                          precise=False, stream=None):
     """kda_chunk_fwd without a workspace argument, for hosts that cannot
     allocate device memory: the library serves the scratch space from a
-    fixed 64 MiB array of its own (see include/kda.h).  ``o`` and
-    ``final_state`` must then be supplied by the caller as well, since this
-    wrapper allocates nothing either.  Returns (o, final_state)."""
-    T, H, K = q.shape
-    V = v.shape[-1]
-    dt = _dtype_code(q)
-    N = cu_seqlens.numel() - 1 if cu_seqlens is not None else (1 if n_seqs is None else int(n_seqs))
+    fixed 64 MiB array of its own (see include/kda.h).  This wrapper
+    allocates nothing either, so ``o`` is required, and ``final_state`` is
+    written only when given (it is required, as the destination pool, with
+    state_indices).  Arguments are checked as for kda_chunk_fwd.  Returns
+    (o, final_state)."""
     if o is None:
         raise ValueError("kda_chunk_fwd_noalloc allocates nothing: pass o")
-    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("o", o),
-                    ("cu_seqlens", cu_seqlens), ("state_indices", state_indices),
-                    ("initial_state", initial_state), ("final_state", final_state)):
-        _check(t, name)
-    slots = 0 if state_indices is None else (final_state.shape[0] if n_slots is None else int(n_slots))
+    T, H, K, V, N, dt, slots = _chunk_args(q, k, v, g, beta, cu_seqlens, n_seqs, initial_state,
+                                           final_state, state_indices, n_slots, o, torch.float32)
     flags = KDA_CHUNK_PRECISE if precise else 0
     if scale is None:
         scale = K ** -0.5

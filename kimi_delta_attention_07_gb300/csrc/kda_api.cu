@@ -34,8 +34,16 @@ const char *kda_status_string(int status) {
         case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: only K = V = 128 is built";
         case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace missing, too small or misaligned";
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA: a CUDA call or kernel launch failed";
+        case KDA_ERR_DEVICE_TIMEOUT:
+            return "KDA_ERR_DEVICE_TIMEOUT: a bounded device-side wait gave up; outputs are incomplete";
         default: return "KDA: unknown status";
     }
+}
+
+int kda_status_from_workspace_flags(int flags) {
+    if (flags & KDA_WS_TIMEOUT) return KDA_ERR_DEVICE_TIMEOUT;
+    if (flags & (KDA_WS_BAD_SEQLENS | KDA_WS_BAD_SLOT)) return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
 }
 
 int kda_version(void) { return 100; }
@@ -196,7 +204,7 @@ int kda_workspace_status(const void *workspace, int *flags_out, void *stream) {
         return KDA_ERR_CUDA;
     }
     *flags_out = st;
-    return KDA_OK;
+    return kda_status_from_workspace_flags(st);
 }
 
 namespace {

@@ -64,7 +64,6 @@ using namespace tc;
 
 constexpr int C = kChunk;    // 64
 constexpr int D = kHeadDim;  // 128
-constexpr int kStatusTimeout = 4;
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);

@@ -55,7 +55,12 @@ __device__ __forceinline__ float warp_sum(float x) {
 // The record contents depend on the chunk path (fp32 CUDA-core path or bf16
 // tensor-core path); each path defines its record size.
 
-enum StatusBits : int { kBadSeqlens = 1, kBadSlot = 2 };
+enum StatusBits : int {
+    kBadSeqlens = KDA_WS_BAD_SEQLENS,
+    kBadSlot = KDA_WS_BAD_SLOT,
+    kStatusTimeout = KDA_WS_TIMEOUT,
+    kExactDecay = KDA_WS_EXACT_DECAY
+};
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

@@ -45,10 +45,40 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for s in range(5):
+    for s in range(6):
         assert kda.kda_status_string(s).startswith("KDA_")
+    assert "TIMEOUT" in kda.kda_status_string(kda.KDA_ERR_DEVICE_TIMEOUT)
     assert "unknown" in kda.kda_status_string(99)
     assert lib.kda_version() == 100
+
+
+def test_header_status_values_match_the_binding():
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    enum = dict(re.findall(r"^\s*(KDA_(?:OK|ERR_\w+))\s*=\s*(\d+)", text, flags=re.M))
+    assert {k: int(v) for k, v in enum.items()} == {
+        "KDA_OK": kda.KDA_OK, "KDA_ERR_INVALID_ARG": kda.KDA_ERR_INVALID_ARG,
+        "KDA_ERR_UNSUPPORTED": kda.KDA_ERR_UNSUPPORTED, "KDA_ERR_WORKSPACE": kda.KDA_ERR_WORKSPACE,
+        "KDA_ERR_CUDA": kda.KDA_ERR_CUDA, "KDA_ERR_DEVICE_TIMEOUT": kda.KDA_ERR_DEVICE_TIMEOUT}
+    bits = dict(re.findall(r"^#define\s+(KDA_WS_\w+)\s+(\d+)", text, flags=re.M))
+    assert {k: int(v) for k, v in bits.items()} == {
+        "KDA_WS_BAD_SEQLENS": kda.KDA_WS_BAD_SEQLENS, "KDA_WS_BAD_SLOT": kda.KDA_WS_BAD_SLOT,
+        "KDA_WS_TIMEOUT": kda.KDA_WS_TIMEOUT, "KDA_WS_EXACT_DECAY": kda.KDA_WS_EXACT_DECAY}
+
+
+@pytest.mark.parametrize("flags", range(16))
+def test_workspace_status_word_maps_to_a_status(lib, flags):
+    """Every combination of the status word's bits, as the kernels would leave
+    them in a workspace, decodes to the documented kda_status: a bounded wait
+    that gave up dominates, then the device-side argument errors; the
+    exact-decay bit is informational."""
+    st = kda.kda_status_from_workspace_flags(flags)
+    if flags & kda.KDA_WS_TIMEOUT:
+        assert st == kda.KDA_ERR_DEVICE_TIMEOUT
+    elif flags & (kda.KDA_WS_BAD_SEQLENS | kda.KDA_WS_BAD_SLOT):
+        assert st == kda.KDA_ERR_INVALID_ARG
+    else:
+        assert st == kda.KDA_OK
+    assert kda.kda_status_string(st).startswith("KDA_")
 
 
 def test_workspace_bytes(lib):
