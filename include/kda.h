@@ -33,7 +33,9 @@
  *             file's recurrent-state cache uses.
  * Element types: q, k, v and o are all `dtype` (kda_dtype); g, beta and the
  * states are always fp32.  g is the log-decay (<= 0 for a contraction; any
- * finite value is accepted), beta is the already-activated write strength.
+ * finite value is accepted, but on the bf16 tensor-core chunk path positive
+ * values are supported only while their sum over 16 tokens stays below 40),
+ * beta is the already-activated write strength.
  * The supported head dims are K = V = 128.
  *
  * Alignment: row pointers must be 16-byte aligned for fp32 tensors and for
@@ -191,16 +193,20 @@ int kda_chunk_scan(const void *q, const void *k, const void *v, const float *g,
                                 completed, ~2 s) gave up: the CTA left its remaining chunks
                                 unwritten and exited; outputs of that call are incomplete */
 #define KDA_WS_EXACT_DECAY 8 /* informational, not an error: on the tensor-core path some
-                                (chunk, head) had a decay span outside the range of the
-                                factorised exponentials (a per-channel decay of more than 40
-                                within 16 tokens, or a positive g) and was computed with exact
-                                pairwise exponentials instead */
+                                16-token block decayed by more than 75 in a key channel (per-token
+                                decays below about -5) and its diagonal 16 x 16 scores were
+                                computed with exact pairwise exponentials */
+#define KDA_WS_STRONG_DECAY 16 /* informational, not an error: on the tensor-core path some
+                                  (chunk, head) had |G_r - G_31| > 80 in a key channel (G the
+                                  cumulative log-decay inside the chunk) and was computed by the
+                                  strong-decay prep, with per-16-token decay references */
 
 /*
  * The kda_status that a workspace status word stands for:
  * KDA_ERR_DEVICE_TIMEOUT if KDA_WS_TIMEOUT is set, else KDA_ERR_INVALID_ARG
  * if KDA_WS_BAD_SEQLENS or KDA_WS_BAD_SLOT is set, else KDA_OK (the
- * informational KDA_WS_EXACT_DECAY is not an error).  Pure host function.
+ * informational KDA_WS_EXACT_DECAY and KDA_WS_STRONG_DECAY are not errors).
+ * Pure host function.
  */
 int kda_status_from_workspace_flags(int flags);
 
@@ -384,10 +390,11 @@ int kda_recurrent_multi_step(const void *q, const void *k, const void *v, const 
  * kda_recurrent_step.  The tensor-core path reads the raw bf16 gate and
  * activates it on chip (half the gate bytes of an fp32 g); the fp32 path
  * activates it into the workspace first.  Size the workspace with
- * kda_chunk_workspace_bytes(..., flags | KDA_CHUNK_GATED).  The tensor-core
- * path's decay-range limit (per-token decays down to about -5.3) makes the
- * lower-bounded gate with lower_bound >= -5 the form to use there, as the
- * model's own fast path does.
+ * kda_chunk_workspace_bytes(..., flags | KDA_CHUNK_GATED).  Any decay the
+ * gate produces is supported on every path: on the tensor-core path chunks
+ * with strong decay take the strong-decay prep and, beyond about -5 per
+ * token, exact pairwise exponentials on the diagonal (KDA_WS_STRONG_DECAY,
+ * KDA_WS_EXACT_DECAY).
  *
  * Output epilogue (model file, KimiDeltaAttention._project_out), optional:
  *   out_gate    [T, H, V] / [N, H, V] in the q dtype, or NULL for none

@@ -23,7 +23,8 @@ from . import _build
 (KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA,
  KDA_ERR_DEVICE_TIMEOUT) = range(6)
 # bits of the chunk workspace's status word (kda_workspace_status)
-KDA_WS_BAD_SEQLENS, KDA_WS_BAD_SLOT, KDA_WS_TIMEOUT, KDA_WS_EXACT_DECAY = 1, 2, 4, 8
+KDA_WS_BAD_SEQLENS, KDA_WS_BAD_SLOT, KDA_WS_TIMEOUT, KDA_WS_EXACT_DECAY, KDA_WS_STRONG_DECAY = (
+    1, 2, 4, 8, 16)
 KDA_F32, KDA_BF16 = 0, 1
 KDA_CHUNK_PRECISE = 1
 KDA_CHUNK_SCAN_WIDE = 2

@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(kIndexThreads)
     if (threadIdx.x == 0) {
         chunk_off[n_seqs] = carry;
         *ws_at<int32_t>(workspace, L.status_off) = status_s;
+        *ws_at<int32_t>(workspace, L.defer_count_off) = 0;  // no item deferred yet
     }
 }
 

@@ -5,36 +5,33 @@
 // _torch_chunk_kda), with every dense contraction on the 5th-generation
 // tensor cores.
 //
-// prep -- persistent, one CTA (16 warps) per SM walking the (chunk, head)
-// items; the raw q, k, v, g tiles of an item arrive by TMA, and the next
-// item's tiles are requested as soon as the current ones are consumed:
+// prep -- persistent, two CTAs (8 warps each) per SM walking the (chunk,
+// head) items, so that one CTA's barrier-separated phases overlap the
+// other's; the raw q, k, v tiles of an item arrive by TMA, g as a register
+// slice per thread fetched during the previous item:
 //   * q_hat = scale * l2norm(q), k_hat = l2norm(k) (fp32), G = cumsum(g).
-//   * G is replaced in place by l_r = exp(G_r - G_{16 br}) (br = r's 16-row
-//     block); rho_b = exp(G_{16b}), so exp(G_r) = l_r * rho_br.  Every
-//     exponent here is <= 0.
+//   * Every exponential is referenced to the chunk's middle token:
+//     x_r = exp(G_r - G_31) per key channel, so that
+//     exp(G_r - G_j) = x_r / x_j, exp(G_r) = x_r exp(G_31) and
+//     exp(G_63 - G_j) = exp(G_63 - G_31) / x_j.  A chunk with some
+//     |G_r - G_31| > 80 does not fit these factors; it is listed in the
+//     workspace and computed by the strong-decay prep (kda_chunk_tc_strong.cu,
+//     per-16-token references) right after.
 //   * Causal scores A[r,j] and the interaction matrix L[r,j] come from ONE
-//     M=128 x N=160 x K=128 MMA: the A operand is [q_hat l ; k_hat l] (row
-//     r referenced to its own block start), the B operand stacks, for the
-//     10 (row block br, column block b) pairs with br >= b, the 16 rows
-//     k_hat_j * exp(G_{16br} - G_j), j in block b.  Row r of block br finds
-//     its columns j < 16(br+1) side by side.  Off the block diagonal both
-//     factors are <= 1; on it the column factor is at most exp(15 max|g|),
-//     its exponent clamped at 80 (only reached for per-token decays below
-//     about -5.3, and then only for masked pairs).
+//     M=128 x N=64 x K=128 MMA: A operand [q_hat x ; k_hat x] (formed in
+//     place over the raw q, k tiles, which TMA delivers in that operand's
+//     layout), B operand k_hat / x as a hi + lo bf16 pair.
 //   * X = (I + beta L)^-1 blockwise in fp32: 16x16 diagonal blocks by
 //     forward substitution (one column per lane), the rest as
-//     (I - M + M^2 - M^3) X_D with M = X_D L_off; T = X diag(beta).
-//   * The stacked column operand and T enter their MMAs as hi + lo bf16
-//     pairs (two accumulating MMAs), which keeps the WY transform accurate
-//     when keys are strongly correlated and the later subtraction U - W S
-//     cancels.
+//     (I - M + M^2 - M^3) X_D with M = X_D L_off; T = X diag(beta), entered
+//     into its MMAs as a hi + lo bf16 pair, which keeps the WY transform
+//     accurate when keys are strongly correlated and the later subtraction
+//     U - W S cancels.
 //   * W = T (exp(G) k_hat) and U = T v as M=128 x N=128 x K=64 MMAs whose A
 //     operand is [T ; scratch] (rows 64..127 unused), so each thread of
-//     TMEM lanes 0..63 holds whole rows of W and U.  They sit in TMEM
-//     columns of their own and are written out while the next item's A/L
-//     MMA runs.
-//   * Record written with 16-byte stores, laid out as the scan's shared-
-//     memory image (128-byte-swizzled K-major operands), see TcRec.
+//     TMEM lanes 0..63 holds whole rows of W and U.
+//   * Record laid out as the scan's shared-memory image (128-byte-swizzled
+//     K-major operands), see TcRec; W and U leave by bulk copies.
 //
 // scan, one CTA per (sequence, head, 32 value columns), 4 warps, records in a
 // 3-stage cp.async.bulk ring:
@@ -48,14 +45,9 @@
 //   rows that were already consumed).  D1 is double-buffered in TMEM so that
 //   the output rows of a chunk are stored while the next chunk's first MMA
 //   runs; only the MMA-issuing thread waits for a stage before that MMA.
-#include <cuda.h>  // CUtensorMap (the encoder is fetched through the runtime)
-#include <cudaTypedefs.h>
-
 #include <algorithm>
-#include <mutex>
 
-#include "kda_internal.cuh"
-#include "kda_tc.cuh"
+#include "kda_chunk_tc.cuh"
 
 namespace kda {
 namespace {
@@ -65,86 +57,48 @@ using namespace tc;
 constexpr int C = kChunk;    // 64
 constexpr int D = kHeadDim;  // 128
 
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-    const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t *>(&p);
-}
-
-__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
-    return make_uint4(pack2(x[0], x[1]), pack2(x[2], x[3]), pack2(x[4], x[5]), pack2(x[6], x[7]));
-}
-
-// 8 consecutive bf16 (16 bytes) -> fp32
-__device__ __forceinline__ void unpack8(uint4 raw, float (&x)[8]) {
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162 *>(&w[i]);
-        const float2 f = __bfloat1622float2(p);
-        x[2 * i] = f.x;
-        x[2 * i + 1] = f.y;
-    }
-}
-
-// The model's gate (see gate_decay) with the SFU exponential, logarithm and
-// reciprocal (a few ulp, far below the bf16 operands of this path); log1p of
-// a small argument by its series, where 1 + e would round the argument away.
-__device__ __forceinline__ float gate_decay_fast(float x, float gscale, float lower_bound,
-                                                 bool use_lower_bound) {
-    if (use_lower_bound) return __fdividef(lower_bound, 1.0f + __expf(-gscale * x));
-    const float e = __expf(-fabsf(x));  // in (0, 1]
-    const float l1p = e < 1e-3f ? e * (1.0f - 0.5f * e) : __logf(1.0f + e);
-    return -gscale * (fmaxf(x, 0.0f) + l1p);
-}
 
 // ---------------------------------------------------------------------------
 // prep
 // ---------------------------------------------------------------------------
-constexpr int kPrepThreads = 512;
-constexpr int kLoader = 64;  // issues the TMA loads and the A/L MMA; its warp does no W/U readout
-constexpr uint32_t kPrepTmemCols = 256;  // A/L result 0..159; then W 0..127, U 128..255
-constexpr int NPAIR = 10;      // (row block br, column block b) pairs with br >= b
-constexpr int NST = 16 * NPAIR;  // 160 = N of the stacked A/L MMA
+constexpr int kPrepThreads = 256;
+constexpr int kPrepMinBlocks = 2;        // two CTAs per SM overlap each other's phases
+constexpr uint32_t kPrepTmemCols = 256;  // A/L result 0..63; then W 0..127, U 128..255
+constexpr float kLog2e = 1.4426950408889634f;
+// Largest |G_r - G_31| (natural log units) the factorised exponentials take:
+// both factors and every product of unmasked pairs stay inside fp32 / bf16
+// range with margin.  Chunks beyond it are deferred to the strong-decay prep.
+constexpr float kRelLimit2 = 80.0f * kLog2e;
 // shared memory plan (offsets from a 1024-aligned base)
-constexpr int R_Q = 0;          // bf16 [64][128]
-constexpr int R_K = 16384;      // bf16 [64][128]
-constexpr int R_V = 32768;      // bf16, two 128B-swizzled [64 rows][64] blocks (MN-major operand)
-constexpr int R_G = 49152;      // fp32 [64][128]: g -> G -> l
-constexpr int R_BYTES = 81920;
-constexpr int P_XL = R_BYTES;             // 32 KB: [q_hat l ; k_hat l] | L fp32 + scratch | E^T, V^T
-constexpr int P_BS = P_XL + 32768;        // 40 KB: stacked column operand | inverse scratch, T
-constexpr int P_T = P_BS + 16384;         // T operand [64][64] bf16; the MMA reads 16 KB from here
-constexpr int P_RQ = P_BS + 40960;        // fp32 [64]: scale / |q_r|
-constexpr int P_RK = P_RQ + 256;          // fp32 [64]: 1 / |k_r|
-constexpr int P_BETA = P_RK + 256;        // fp32 [64]
-constexpr int P_GREF = P_BETA + 256;      // fp32 [5][128]: G at rows 0, 16, 32, 48, 63
-constexpr int P_TAU = P_GREF + 5 * 512;   // fp32 [6][128]: exp(G_16br - G_16b), br > b
-constexpr int P_QSUM = P_TAU + 6 * 512;   // fp32 [4][128]: per-quarter sums of g
-constexpr int P_PSI = P_QSUM + 4 * 512;   // fp32 [4][128]: G_last - G_16b
-constexpr int P_FIRST = P_PSI + 4 * 512;  // fp32 [4][128]: g at rows 0, 16, 32, 48
-constexpr int P_BAR = P_FIRST + 4 * 512;    // q/k/g barrier, mma barrier, tmem slot, v barrier, metadata
-constexpr int P_BS2 = (P_BAR + 64 + 1023) / 1024 * 1024;  // 40 KB: low part of the stacked operand
-constexpr int P_E = P_BS2 + 40960;        // 16 KB: E = k_hat exp(G), MN-major [j][d]
-constexpr int P_BYTES = P_E + 16384;
+constexpr int P_XL = 0;             // 32 KB: raw [q ; k] (TMA) -> [q_hat x ; k_hat x]
+constexpr int P_COLH = 32768;       // 16 KB: k_hat / x, hi part (B operand of the A/L MMA)
+constexpr int P_COLL = 49152;       // 16 KB: its lo part
+constexpr int P_E = 65536;          // 16 KB: E = k_hat exp(G), MN-major [j][d]
+constexpr int P_V = 81920;          // 16 KB: v, MN-major (two 64-column boxes)
+constexpr int P_RQ = 98304;         // fp32 [64]: scale / |q_r|
+constexpr int P_RK = P_RQ + 256;    // fp32 [64]: 1 / |k_r|
+constexpr int P_BETA = P_RK + 256;  // fp32 [64]
+constexpr int P_QS = P_BETA + 256;  // fp32 [8][128]: per-octet sums of g (log2 units)
+constexpr int P_BAR = P_QS + 4096;  // q/k barrier, v barrier, mma barrier, tmem slot, metadata
+constexpr int P_BYTES = P_BAR + 128;
 constexpr int P_SMEM = P_BYTES + 1024;
-static_assert(P_SMEM <= 232448, "prep shared memory");
-constexpr int LSTRIDE = 68;               // row stride (floats) of L in shared memory
-constexpr int MS = 20;                    // row stride (floats) of 16x16 scratch matrices
-constexpr int MBLK = 16 * MS;             // floats per 16x16 scratch matrix
-static_assert(P_T + 8192 + 16384 <= P_BS + 40960, "T_hi / T_lo operand windows");
-static_assert(12 * MBLK * 4 <= P_T - P_BS, "inverse scratch vs T");
-static_assert(C * LSTRIDE * 4 + 2 * MBLK * 4 <= 32768, "XL scratch");
-
-__device__ __forceinline__ int tau_index(int br, int b) { return br * (br - 1) / 2 + b; }
-// first column of row block br in the stacked A/L result (pairs (br, 0..br) are consecutive)
-__device__ __forceinline__ int pair_col0(int br) { return 8 * br * (br + 1); }
+// reuse of [0, 64 KB) once the A/L MMA has read its operands
+constexpr int P_L = 0;              // fp32 [64][LSTRIDE]: beta-scaled L
+constexpr int P_SCR = 17408;        // inverse scratch: 14 16x16 fp32 blocks
+constexpr int P_T = 36864;          // T operand, hi (8 KB) and lo (8 KB)
+constexpr int P_STAGE = 32768;      // W and U staged for the record after the W/U MMA
+constexpr int LSTRIDE = 68;         // row stride (floats) of L in shared memory
+constexpr int MS = 20;              // row stride (floats) of 16x16 scratch matrices
+constexpr int MBLK = 16 * MS;       // floats per 16x16 scratch matrix
+static_assert(P_SMEM * kPrepMinBlocks + 2048 <= 233472, "two prep CTAs per SM");
+static_assert(P_L + C * LSTRIDE * 4 <= P_SCR && P_SCR + 14 * MBLK * 4 <= P_T, "L, scratch, T");
+static_assert(P_T + 16384 <= P_E && P_STAGE + 32768 <= P_E, "T and staging below E");
 
 struct PrepItem {
     int64_t tok0;
     int valid, h, c;
 };
-
-static_assert(32 + sizeof(PrepItem) <= 64, "barrier block");
+static_assert(32 + sizeof(PrepItem) <= 128, "barrier block");
 
 __device__ __forceinline__ PrepItem prep_item(int item, int H, const int32_t *chunk_off,
                                               const int32_t *seq_start, const int32_t *seq_len,
@@ -160,43 +114,28 @@ __device__ __forceinline__ PrepItem prep_item(int item, int H, const int32_t *ch
 }
 
 // Raw tiles of one (chunk, head) item through 3-D tensor maps {128, H, T}
-// over the [T, H, 128] tensors: q, k (bf16) and g (fp32) as plain row-major
-// 128 x 1 x 64 boxes; v (bf16) as two 64 x 1 x 64 boxes with 128-byte
-// swizzle, i.e. already the MN-major operand layout of the U MMA.  Rows past
-// the end of the tensor arrive as zeros.  q, k and g are loaded as soon as
-// the previous item's row pass has consumed them, v after its last MMA.
+// over the [T, H, 128] bf16 tensors, as 64-channel x 1 x 64-token boxes with
+// 128-byte swizzle: q and k land as the row blocks of the A/L MMA's K-major
+// A operand ([q ; k], 128 rows), v as the MN-major B operand of U = T V.
+// Rows past the end of the tensor arrive as zeros.
 struct RawMaps {
-    CUtensorMap q, k, v, g;
+    CUtensorMap q, k, v;
 };
 
-// g_bytes: 32 KB for an fp32 g tile, 16 KB for a raw bf16 gate tile
-__device__ __forceinline__ void load_qkg(unsigned char *buf, const RawMaps &m, int h, int64_t tok0,
-                                         uint64_t *bar, uint32_t g_bytes) {
-    mbar_arrive_expect_tx(bar, 16384u + 16384u + g_bytes);
-    tma_load_3d(buf + R_Q, &m.q, 0, h, (int)tok0, bar);
-    tma_load_3d(buf + R_K, &m.k, 0, h, (int)tok0, bar);
-    tma_load_3d(buf + R_G, &m.g, 0, h, (int)tok0, bar);
+__device__ __forceinline__ void load_qk(unsigned char *sm, const RawMaps &m, int h, int64_t tok0,
+                                        uint64_t *bar) {
+    mbar_arrive_expect_tx(bar, 32768u);
+    tma_load_3d(sm + P_XL, &m.q, 0, h, (int)tok0, bar);           // q, channels 0..63
+    tma_load_3d(sm + P_XL + 8192, &m.k, 0, h, (int)tok0, bar);    // k, channels 0..63
+    tma_load_3d(sm + P_XL + 16384, &m.q, 64, h, (int)tok0, bar);  // q, channels 64..127
+    tma_load_3d(sm + P_XL + 24576, &m.k, 64, h, (int)tok0, bar);  // k, channels 64..127
 }
 
-__device__ __forceinline__ void load_v(unsigned char *buf, const RawMaps &m, int h, int64_t tok0,
+__device__ __forceinline__ void load_v(unsigned char *sm, const RawMaps &m, int h, int64_t tok0,
                                        uint64_t *bar) {
     mbar_arrive_expect_tx(bar, 16384u);
-    tma_load_3d(buf + R_V, &m.v, 0, h, (int)tok0, bar);
-    tma_load_3d(buf + R_V + 8192, &m.v, 64, h, (int)tok0, bar);
-}
-
-// fp32 [rows][128] arrays that are read 8 channels per lane (16 lanes per
-// row): channel d is stored at swz(d), i.e. float4 unit u of a row at
-// u ^ ((u / 8) % 2), so that each group of 8 lanes covers all 32 banks.
-__device__ __forceinline__ int swz(int d) { return d ^ (((d >> 5) & 1) << 2); }
-
-// channels d0 .. d0+7 (d0 a multiple of 8) of a swizzled row
-__device__ __forceinline__ void load8s(const float *row, int d0, float (&x)[8]) {
-    const int f = ((d0 >> 5) & 1) << 2;
-    const float4 a = *reinterpret_cast<const float4 *>(row + (d0 ^ f));
-    const float4 b = *reinterpret_cast<const float4 *>(row + ((d0 + 4) ^ f));
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    tma_load_3d(sm + P_V, &m.v, 0, h, (int)tok0, bar);
+    tma_load_3d(sm + P_V + 8192, &m.v, 64, h, (int)tok0, bar);
 }
 
 // Row i of a 16x16 fp32 matrix (row stride lda floats, 16-byte aligned rows).
@@ -237,56 +176,99 @@ __device__ __forceinline__ float4 mm16_row4(const float *A, int lda, const float
     return row4_times(a, B, c4, ldb);
 }
 
-// GATED: maps.g covers the model's raw bf16 gate and beta is unused; the
-// gate (GateArgs) is activated on chip.  Otherwise g and beta are activated.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// 16 bytes of a global tensor through the non-coherent path, issued where
+// it stands (the inputs are read-only for the kernel's lifetime); the value
+// is consumed much later, so the load's latency hides under other phases.
+__device__ __forceinline__ uint4 ldg16_now(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint2 ldg8_now(const void *p) {
+    uint2 v;
+    asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+// g of one thread's (8 rows, 4 channels) slice, fetched into registers: the
+// activated fp32 g, or the model's raw bf16 gate (activated with the
+// cumulative sum).  Rows past the sequence end read nothing (zero decay).
 template <bool GATED>
-__global__ void __launch_bounds__(kPrepThreads, 1)
-    chunk_prep_tc_kernel(const __grid_constant__ RawMaps maps, const float *__restrict__ beta,
-                         const GateArgs gate, int n_seqs, int H, float scale, void *workspace,
-                         WsLayout L) {
-    constexpr uint32_t kGBytes = GATED ? 16384u : 32768u;
+struct GSlice {
+    uint4 v[8];
+};
+template <>
+struct GSlice<true> {
+    uint2 v[8];
+};
+
+template <bool GATED>
+__device__ __forceinline__ void load_gslice(GSlice<GATED> &s, const float *g, const GateArgs &gate,
+                                            int64_t tok0, int valid, int r0, int h, int H, int d) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = r0 + i;
+        const int64_t off = ((tok0 + r) * H + h) * (int64_t)D + d;
+        if constexpr (GATED)
+            s.v[i] = r < valid ? ldg8_now(reinterpret_cast<const __nv_bfloat16 *>(gate.raw_gate) + off)
+                               : make_uint2(0u, 0u);
+        else
+            s.v[i] = r < valid ? ldg16_now(g + off) : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// Main prep: every (chunk, head) item whose decay fits one chunk-wide
+// exponential reference; the others are listed for the strong-decay prep.
+// GATED: the raw gate of the model is activated on chip (gate.raw_gate /
+// raw_beta are read like g / beta).  Otherwise g and beta are the activated
+// fp32 inputs.
+template <bool GATED>
+__global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
+    chunk_prep_tc_kernel(const __grid_constant__ RawMaps maps, const float *__restrict__ g,
+                         const float *__restrict__ beta, const GateArgs gate, int n_seqs, int H,
+                         float scale, void *workspace, WsLayout L) {
     griddep_wait();  // the chunk index (previous kernel) is complete
-    auto beta_of = [&](int64_t tok, int hh) {
-        return GATED ? gate_beta(__bfloat162float(
-                           reinterpret_cast<const __nv_bfloat16 *>(gate.raw_beta)[tok * H + hh]))
-                     : beta[tok * H + hh];
-    };
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     unsigned char *sXL = sm + P_XL;
-    unsigned char *sBS = sm + P_BS;
-    unsigned char *sT = sm + P_T;          // T_hi; T_lo follows 8 KB later
-    unsigned char *sBS2 = sm + P_BS2;
-    float *sB = reinterpret_cast<float *>(sm + P_BETA);
-    float *sGref = reinterpret_cast<float *>(sm + P_GREF);
-    float *sTau = reinterpret_cast<float *>(sm + P_TAU);
-    float *sQsum = reinterpret_cast<float *>(sm + P_QSUM);
-    float *sPsi = reinterpret_cast<float *>(sm + P_PSI);
+    unsigned char *sE = sm + P_E;
+    unsigned char *sT = sm + P_T;  // T_hi; T_lo follows 8 KB later
     float *sRq = reinterpret_cast<float *>(sm + P_RQ);
     float *sRk = reinterpret_cast<float *>(sm + P_RK);
-    float *sFirst = reinterpret_cast<float *>(sm + P_FIRST);
-    unsigned char *sE = sm + P_E;
-    uint64_t *full = reinterpret_cast<uint64_t *>(sm + P_BAR);
-    uint64_t *mbar = full + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 1);
-    uint64_t *vfull = full + 3;
+    float *sB = reinterpret_cast<float *>(sm + P_BETA);
+    float *sQS = reinterpret_cast<float *>(sm + P_QS);
+    uint64_t *full_qk = reinterpret_cast<uint64_t *>(sm + P_BAR);
+    uint64_t *full_v = full_qk + 1;
+    uint64_t *mbar = full_qk + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(full_qk + 3);
     PrepItem *sNext = reinterpret_cast<PrepItem *>(sm + P_BAR + 32);  // metadata two items ahead
-    const __nv_bfloat16 *sQr = reinterpret_cast<const __nv_bfloat16 *>(sm + R_Q);
-    const __nv_bfloat16 *sKr = reinterpret_cast<const __nv_bfloat16 *>(sm + R_K);
-    float *sG = reinterpret_cast<float *>(sm + R_G);  // g -> G_r - G_16b
 
     const int32_t *chunk_off = ws_at<const int32_t>(workspace, L.chunk_off_off);
     const int32_t *seq_start = ws_at<const int32_t>(workspace, L.seq_start_off);
     const int32_t *seq_len = ws_at<const int32_t>(workspace, L.seq_len_off);
     int32_t *status = ws_at<int32_t>(workspace, L.status_off);
+    int32_t *defer_count = ws_at<int32_t>(workspace, L.defer_count_off);
+    int32_t *defer_list = ws_at<int32_t>(workspace, L.defer_off);
     const int n_items = chunk_off[n_seqs] * H;
     if ((int)blockIdx.x >= n_items) return;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // transform-pass slice of this thread: key channels d .. d+3 of the 8
+    // rows r0 .. r0+7 (one warp = all 128 channels of 8 rows)
+    const int d = 4 * lane, r0 = 8 * warp;
+    // its byte offsets in 128-byte-swizzled K-major tiles: K-block, chunk, half
+    const int kb = lane >> 4, cw = (lane & 15) >> 1, hb = (lane & 1) * 8;
     if (warp == 0) tmem_alloc(tmem_slot, kPrepTmemCols);
     if (tid == 32) {
-        mbar_init(full, 1);
-        mbar_init(vfull, 1);
+        mbar_init(full_qk, 1);
+        mbar_init(full_v, 1);
         mbar_init(mbar, 1);
         fence_mbar_init();
     }
@@ -295,244 +277,240 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // item metadata runs one item ahead of the loads, which run one item ahead
-    // of the compute
+    auto beta_of = [&](int64_t tok, int hh) {
+        return GATED ? gate_beta(__bfloat162float(
+                           reinterpret_cast<const __nv_bfloat16 *>(gate.raw_beta)[tok * H + hh]))
+                     : beta[tok * H + hh];
+    };
     int item = blockIdx.x;
     PrepItem cur = prep_item(item, H, chunk_off, seq_start, seq_len, n_seqs);
-    if (tid == kLoader) {
-        load_qkg(sm, maps, cur.h, cur.tok0, full, kGBytes);
-        load_v(sm, maps, cur.h, cur.tok0, vfull);
+    if (tid == 0) {
+        load_qk(sm, maps, cur.h, cur.tok0, full_qk);
+        load_v(sm, maps, cur.h, cur.tok0, full_v);
     }
+    GSlice<GATED> gs;
+    load_gslice<GATED>(gs, g, gate, cur.tok0, cur.valid, r0, cur.h, H, d);
     float beta_cur = tid < cur.valid ? beta_of(cur.tok0 + tid, cur.h) : 0.0f;
-    // gate parameters of this thread's key channel (tid % 128) for the current
-    // item's head, fetched one item ahead like beta (A_log raw: its exponential
-    // is taken where it is used, so the load's latency stalls nothing)
-    auto gate_bias = [&](int hh) { return GATED ? gate.dt_bias[hh * D + (tid & (D - 1))] : 0.0f; };
-    auto gate_alog = [&](int hh) { return GATED ? gate.a_log[hh] : 0.0f; };
-    float bias_cur = gate_bias(cur.h), alog_cur = gate_alog(cur.h);
+    float4 bias_cur = make_float4(0.f, 0.f, 0.f, 0.f);
+    float alog_cur = 0.0f;
+    if (GATED) {
+        bias_cur = *reinterpret_cast<const float4 *>(gate.dt_bias + cur.h * D + d);
+        alog_cur = gate.a_log[cur.h];
+    }
     PrepItem nxt = cur;
     if (item + (int)gridDim.x < n_items)
         nxt = prep_item(item + gridDim.x, H, chunk_off, seq_start, seq_len, n_seqs);
 
-    // phases of the three barriers, and whether a phase is armed but not yet
-    // waited for (what must land before the shared memory is released)
-    uint32_t fphase = 0, vphase = 0, mphase = 0;
-    bool fpend = true, vpend = true, mpend = false;
+    uint32_t qkphase = 0, vphase = 0, mphase = 0;
+    bool qkpend = true, vpend = true, mpend = false;
     bool ok = true;
     KDA_PHASE_START();
     for (; item < n_items; item += gridDim.x) {
         const bool has_next = item + (int)gridDim.x < n_items;
-        if (!has_next) griddep_launch_dependents();  // last item: the scan may be scheduled
+        if (!has_next) griddep_launch_dependents();  // last item: the next kernel may be scheduled
         unsigned char *rec = ws_at<unsigned char>(workspace, L.records_off + ((size_t)cur.c * H + cur.h) * TcRec::bytes);
         const int valid = cur.valid;
         if (tid < C) sB[tid] = tid < valid ? beta_cur : 0.0f;
-        float beta_nxt = 0.0f, bias_nxt = 0.0f, alog_nxt = 0.0f;
 
-        if (mbar_wait(full, fphase)) {
-            fphase ^= 1;
-            fpend = false;
+        // 1. cumulative log2-decay over this thread's 8 rows, per channel, in
+        //    registers: pre_i = log2(e) * sum of g over rows r0 .. r0+i.  The
+        //    8-row total goes to shared memory.
+        float4 pre[8];
+        {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float gsc = GATED ? __expf(alog_cur) : 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float4 gv;
+                if constexpr (GATED) {
+                    const float2 a = unpack2(gs.v[i].x), b = unpack2(gs.v[i].y);
+                    const bool live = r0 + i < valid;
+                    const float lb = gate.lower_bound;
+                    const bool ulb = gate.use_lower_bound != 0;
+                    gv.x = live ? gate_decay_fast(a.x + bias_cur.x, gsc, lb, ulb) : 0.0f;
+                    gv.y = live ? gate_decay_fast(a.y + bias_cur.y, gsc, lb, ulb) : 0.0f;
+                    gv.z = live ? gate_decay_fast(b.x + bias_cur.z, gsc, lb, ulb) : 0.0f;
+                    gv.w = live ? gate_decay_fast(b.y + bias_cur.w, gsc, lb, ulb) : 0.0f;
+                } else {
+                    gv = *reinterpret_cast<const float4 *>(&gs.v[i]);
+                }
+                acc.x = fmaf(gv.x, kLog2e, acc.x);
+                acc.y = fmaf(gv.y, kLog2e, acc.y);
+                acc.z = fmaf(gv.z, kLog2e, acc.z);
+                acc.w = fmaf(gv.w, kLog2e, acc.w);
+                pre[i] = acc;
+            }
+            *reinterpret_cast<float4 *>(sQS + warp * D + d) = acc;
+        }
+        KDA_PHASE(0, 0);
+        if (mbar_wait(full_qk, qkphase)) {
+            qkphase ^= 1;
+            qkpend = false;
         } else {
             ok = false;
         }
-        // rows past the end of the sequence: zero (the tensor map only zero-fills past T)
-        for (int i = tid; i < (C - valid) * 16; i += kPrepThreads) {
-            const int r = valid + i / 16, c16 = i % 16;
-            const uint4 z = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4 *>(sm + R_Q + r * 256 + c16 * 16) = z;
-            *reinterpret_cast<uint4 *>(sm + R_K + r * 256 + c16 * 16) = z;
-            if (!GATED) {  // a raw gate tile is masked row by row on activation instead
-                *reinterpret_cast<uint4 *>(sm + R_G + r * 512 + c16 * 32) = z;
-                *reinterpret_cast<uint4 *>(sm + R_G + r * 512 + c16 * 32 + 16) = z;
+        KDA_PHASE(0, 1);
+        // 2. row norms of q and k (raw tiles in the A operand's K-major
+        //    layout): one (row, 64-channel half) per thread, two threads per row
+        {
+            const int R = tid >> 1, half = tid & 1;  // R: 0..63 q rows, 64..127 k rows
+            const unsigned char *row = sXL + half * 16384 + R * 128;
+            float ss = 0.0f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                float x[8];
+                unpack8(*reinterpret_cast<const uint4 *>(row + (c << 4)), x);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) ss = fmaf(x[t], x[t], ss);
+            }
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            if (half == 0) {
+                if (R < C) sRq[R] = R < valid ? scale * rsqrtf(ss + 1e-6f) : 0.0f;
+                else sRk[R - C] = R - C < valid ? rsqrtf(ss + 1e-6f) : 0.0f;
             }
         }
+        if (tid == 0) bulk_wait_read();  // the previous item's W/U staging has been read
         if (!__syncthreads_and(ok)) {
             ok = false;  // uniform from here on: every thread takes the exit path
             break;
         }
-        KDA_PHASE(0, 0);
+        KDA_PHASE(0, 2);
 
-        // 1. cumulative log-decay, one key channel and one 16-row block per
-        //    thread: sG receives G_r - G_16b (b = r's block, so <= 0); the
-        //    block sums and first-row values then give every reference
-        //    quantity of the thread's block: G_16b, G_last - G_16b,
-        //    tau(b, b') = exp(G_16b - G_16b'), b' < b, and gC = exp(G_last).
+        // 3. per row of the slice: G_r - G_31 (the reference is row 31, the
+        //    middle of the chunk; log2 units), x = exp(G_r - G_31), and from
+        //    them the operands q_hat x, k_hat x (in place over the raw tiles),
+        //    k_hat / x (hi + lo), E = k_hat x e^{G_31}, QG = q_hat x e^{G_31}
+        //    and KD = (k_hat / x) e^{G_63 - G_31}.  A chunk with any
+        //    |G_r - G_31| beyond the limit is deferred as a whole (its outputs
+        //    here are discarded: the strong-decay prep rewrites its record).
+        bool wide = false;
         {
-            const int d = tid & (D - 1), qtr = tid >> 7, r0 = 16 * qtr;
-            float x[16];
-            if (GATED) {  // the model's gate: x = raw + dt_bias, through softplus or sigmoid
-                const __nv_bfloat16 *raw = reinterpret_cast<const __nv_bfloat16 *>(sm + R_G);
-                const float bias = bias_cur, gs = __expf(alog_cur);
-                const bool lb = gate.use_lower_bound != 0;
+            float4 before = make_float4(0.f, 0.f, 0.f, 0.f), c2 = before, tot = before;
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    x[i] = r0 + i < valid ? gate_decay_fast(__bfloat162float(raw[(r0 + i) * D + d]) + bias,
-                                                            gs, gate.lower_bound, lb)
-                                          : 0.0f;
-            } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) x[i] = sG[(r0 + i) * D + d];  // g, plain layout
-            }
-#pragma unroll
-            for (int i = 1; i < 16; ++i) x[i] += x[i - 1];
-            sQsum[qtr * D + d] = x[15];
-            sFirst[qtr * D + d] = x[0];
-            const int ds = swz(d);
-            __syncthreads();  // every g (or raw gate) value is read: sG is overwritten below
-#pragma unroll
-            for (int i = 0; i < 16; ++i) sG[(r0 + i) * D + ds] = x[i] - x[0];
-            float off = 0.0f, gl = 0.0f, gfirst[3];  // gfirst[b] = G_16b, b < qtr
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const float qs = sQsum[b * D + d];
-                if (b < qtr) {
-                    gfirst[b] = off + sFirst[b * D + d];
-                    off += qs;
+            for (int o = 0; o < 8; ++o) {
+                const float4 s = *reinterpret_cast<const float4 *>(sQS + o * D + d);
+                if (o < warp) {
+                    before.x += s.x; before.y += s.y; before.z += s.z; before.w += s.w;
                 }
-                gl += qs;
+                if (o < 4) {
+                    c2.x += s.x; c2.y += s.y; c2.z += s.z; c2.w += s.w;
+                }
+                tot.x += s.x; tot.y += s.y; tot.z += s.z; tot.w += s.w;
             }
-            const float gb = off + x[0];
+            const float4 off = make_float4(before.x - c2.x, before.y - c2.y, before.z - c2.z, before.w - c2.w);
+            const float4 tail = make_float4(tot.x - c2.x, tot.y - c2.y, tot.z - c2.z, tot.w - c2.w);
+            if (warp == 0)
+                *reinterpret_cast<float4 *>(rec + TcRec::GC + 4 * d) =
+                    make_float4(ex2(tot.x), ex2(tot.y), ex2(tot.z), ex2(tot.w));
+            const float ec[4] = {ex2(c2.x), ex2(c2.y), ex2(c2.z), ex2(c2.w)};
+            const float el[4] = {ex2(tail.x), ex2(tail.y), ex2(tail.z), ex2(tail.w)};
+            const float4 rq03 = *reinterpret_cast<const float4 *>(sRq + r0);
+            const float4 rq47 = *reinterpret_cast<const float4 *>(sRq + r0 + 4);
+            const float4 rk03 = *reinterpret_cast<const float4 *>(sRk + r0);
+            const float4 rk47 = *reinterpret_cast<const float4 *>(sRk + r0 + 4);
+            const float rqs[8] = {rq03.x, rq03.y, rq03.z, rq03.w, rq47.x, rq47.y, rq47.z, rq47.w};
+            const float rks[8] = {rk03.x, rk03.y, rk03.z, rk03.w, rk47.x, rk47.y, rk47.z, rk47.w};
+            // thread bases: XL (K-major, 128 rows), 64-row tiles (COL, E, KD), QG rows of WQ
+            unsigned char *xl = sXL + kb * 16384 + r0 * 128 + hb;
+            unsigned char *c64 = sm + P_COLH + kb * 8192 + r0 * 128 + hb;
+            unsigned char *qg = rec + TcRec::WQ + kb * 16384 + (C + r0) * 128 + hb;
+            unsigned char *kd = rec + TcRec::KD + kb * 8192 + r0 * 128 + hb;
+            float amax = 0.0f;
 #pragma unroll
-            for (int b = 0; b < 3; ++b)
-                if (b < qtr) sTau[tau_index(qtr, b) * D + ds] = __expf(gb - gfirst[b]);
-            sGref[qtr * D + ds] = gb;
-            sPsi[qtr * D + ds] = gl - gb;
-            if (qtr == 3) {
-                sGref[4 * D + ds] = gl;
-                reinterpret_cast<float *>(rec + TcRec::GC)[d] = __expf(gl);
+            for (int i = 0; i < 8; ++i) {
+                const int o16 = i * 128 + ((cw ^ i) << 4);  // row r0 + i, this thread's 8 bytes
+                const float rel[4] = {pre[i].x + off.x, pre[i].y + off.y, pre[i].z + off.z, pre[i].w + off.w};
+                const uint2 qraw = *reinterpret_cast<const uint2 *>(xl + o16);
+                const uint2 kraw = *reinterpret_cast<const uint2 *>(xl + 8192 + o16);
+                const bool live = r0 + i < valid;  // rows past the sequence end: zero
+                const float2 q01 = unpack2(live ? qraw.x : 0u), q23 = unpack2(live ? qraw.y : 0u);
+                const float2 k01 = unpack2(live ? kraw.x : 0u), k23 = unpack2(live ? kraw.y : 0u);
+                const float qv[4] = {q01.x, q01.y, q23.x, q23.y}, kv[4] = {k01.x, k01.y, k23.x, k23.y};
+                float qx[4], kx[4], col[4], lo[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    amax = fmaxf(amax, fabsf(rel[t]));
+                    const float x = ex2(rel[t]), ir = ex2(-rel[t]);
+                    const float kh = kv[t] * rks[i];
+                    qx[t] = qv[t] * rqs[i] * x;
+                    kx[t] = kh * x;
+                    col[t] = kh * ir;
+                }
+                const uint2 hi = make_uint2(pack2(col[0], col[1]), pack2(col[2], col[3]));
+                {
+                    const float2 h01 = unpack2(hi.x), h23 = unpack2(hi.y);
+                    lo[0] = col[0] - h01.x; lo[1] = col[1] - h01.y;
+                    lo[2] = col[2] - h23.x; lo[3] = col[3] - h23.y;
+                }
+                *reinterpret_cast<uint2 *>(xl + o16) = make_uint2(pack2(qx[0], qx[1]), pack2(qx[2], qx[3]));
+                *reinterpret_cast<uint2 *>(xl + 8192 + o16) = make_uint2(pack2(kx[0], kx[1]), pack2(kx[2], kx[3]));
+                *reinterpret_cast<uint2 *>(c64 + o16) = hi;
+                *reinterpret_cast<uint2 *>(c64 + 16384 + o16) = make_uint2(pack2(lo[0], lo[1]), pack2(lo[2], lo[3]));
+                *reinterpret_cast<uint2 *>(c64 + 32768 + o16) =
+                    make_uint2(pack2(kx[0] * ec[0], kx[1] * ec[1]), pack2(kx[2] * ec[2], kx[3] * ec[3]));
+                *reinterpret_cast<uint2 *>(qg + o16) =
+                    make_uint2(pack2(qx[0] * ec[0], qx[1] * ec[1]), pack2(qx[2] * ec[2], qx[3] * ec[3]));
+                *reinterpret_cast<uint2 *>(kd + o16) =
+                    make_uint2(pack2(col[0] * el[0], col[1] * el[1]), pack2(col[2] * el[2], col[3] * el[3]));
             }
+            wide = !(amax <= kRelLimit2);  // also catches a non-finite decay
         }
-        if (tid == kLoader) bulk_wait_read();  // the previous item's W/U staging is read
-        __syncthreads();
-        KDA_PHASE(0, 1);
-        // 2. the operands of the A/L MMA, one pass per (row j, 8 channels):
-        //    the row norms of q and k (16 lanes per row), l = exp(G_j - G_16bj),
-        //    the row operand [q_hat l ; k_hat l], and the stacked column
-        //    operand rows of j for every row block br >= bj:
-        //    k_hat_j exp(G_16br - G_j) = k_hat_j tau(br, bj) / l_j, with 1 / l_j
-        //    clamped at exp(80) on the block diagonal; where l_j < 1e-30 those
-        //    entries are taken as exponentials directly.
-        //    A thread takes rows r and 63 - r: five column blocks in total.
-#pragma unroll  // both rows in one body: their shuffles and exponentials interleave
-        for (int it = 0; it < 2; ++it) {
-            const int r = it == 0 ? (tid >> 4) : 63 - (tid >> 4), d0 = (tid & 15) * 8, bj = r >> 4;
-            float rel8[8], qv[8], kv[8];
-            load8s(sG + r * D, d0, rel8);
-            unpack8(*reinterpret_cast<const uint4 *>(sQr + r * D + d0), qv);
-            unpack8(*reinterpret_cast<const uint4 *>(sKr + r * D + d0), kv);
-            float sq = 0.f, sk = 0.f;
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                sq = fmaf(qv[t], qv[t], sq);
-                sk = fmaf(kv[t], kv[t], sk);
-            }
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) {  // the 16 lanes of row r
-                sq += __shfl_xor_sync(0xffffffffu, sq, o);
-                sk += __shfl_xor_sync(0xffffffffu, sk, o);
-            }
-            const float rq = scale * rsqrtf(sq + 1e-6f), rk = rsqrtf(sk + 1e-6f);
-            if ((tid & 15) == 0) {
-                sRq[r] = rq;
-                sRk[r] = rk;
-            }
-            float ql[8], kl[8], l8[8], inv[8], kh[8];
-            bool tiny = false;
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                l8[t] = __expf(rel8[t]);
-                kh[t] = kv[t] * rk;
-                ql[t] = qv[t] * rq * l8[t];
-                kl[t] = kh[t] * l8[t];
-                tiny |= l8[t] < 1e-30f;
-                inv[t] = __expf(-rel8[t]);  // 1 / l
-            }
-            *reinterpret_cast<uint4 *>(sXL + sw128_off(r, d0, 128)) = pack8(ql);
-            *reinterpret_cast<uint4 *>(sXL + sw128_off(64 + r, d0, 128)) = pack8(kl);
-            // hi + lo bf16 parts: the MMA sees this operand to ~16 bits
-            auto emit = [&](int b2, const float (&y)[8]) {
-                const uint4 hi = pack8(y);
-                float lo[8];
-                unpack8(hi, lo);
-#pragma unroll
-                for (int t = 0; t < 8; ++t) lo[t] = y[t] - lo[t];
-                const int row = 16 * (b2 * (b2 + 1) / 2 + bj) + (r & 15);
-                *reinterpret_cast<uint4 *>(sBS + sw128_off(row, d0, NST)) = hi;
-                *reinterpret_cast<uint4 *>(sBS2 + sw128_off(row, d0, NST)) = pack8(lo);
-            };
-            if (!__builtin_expect(tiny, 0)) {
-                float y[8];
-#pragma unroll
-                for (int t = 0; t < 8; ++t) y[t] = kh[t] * fminf(inv[t], 5.540622e34f);
-                emit(bj, y);
-                for (int b2 = bj + 1; b2 < 4; ++b2) {
-                    float t8[8];
-                    load8s(sTau + tau_index(b2, bj) * D, d0, t8);
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) y[t] = kh[t] * t8[t] * inv[t];
-                    emit(b2, y);
-                }
-            } else {  // a decay of more than ~69 inside this 16-row block
-                float y[8];
-#pragma unroll
-                for (int t = 0; t < 8; ++t) y[t] = kh[t] * __expf(fminf(-rel8[t], 80.0f));
-                emit(bj, y);
-                for (int b2 = bj + 1; b2 < 4; ++b2) {
-#pragma unroll
-                    for (int t = 0; t < 8; ++t)
-                        y[t] = kh[t] * __expf(sGref[b2 * D + swz(d0 + t)] - sGref[bj * D + swz(d0 + t)] - rel8[t]);
-                    emit(b2, y);
-                }
-            }
-        }
+        KDA_PHASE(0, 3);
         fence_async_smem();
         tc_fence_before();
-        __syncthreads();
-        KDA_PHASE(0, 3);
-        if (tid == kLoader) {
+        const bool defer = __syncthreads_or((int)wide) != 0;
+        KDA_PHASE(0, 4);
+        float beta_nxt = 0.0f, alog_nxt = 0.0f;
+        float4 bias_nxt = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (defer) {
+            // hand the item to the strong-decay prep; the next item's tiles go
+            // out at once (its v load once this item's v copy has landed)
+            if (tid == 0) {
+                defer_list[atomicAdd(defer_count, 1)] = item;
+                atomicOr(status, kStrongDecay);
+                if (has_next) load_qk(sm, maps, nxt.h, nxt.tok0, full_qk);
+            }
+            qkpend = has_next;
+            if (mbar_wait(full_v, vphase)) {
+                vphase ^= 1;
+                vpend = false;
+            } else {
+                ok = false;
+            }
+            if (tid == 0 && has_next && ok) load_v(sm, maps, nxt.h, nxt.tok0, full_v);
+            vpend = has_next && ok;
+            if (has_next) {
+                load_gslice<GATED>(gs, g, gate, nxt.tok0, nxt.valid, r0, nxt.h, H, d);
+                if (tid < nxt.valid) beta_nxt = beta_of(nxt.tok0 + tid, nxt.h);
+                if (GATED) {
+                    bias_nxt = *reinterpret_cast<const float4 *>(gate.dt_bias + nxt.h * D + d);
+                    alog_nxt = gate.a_log[nxt.h];
+                }
+            }
+            if (tid == kPrepThreads - 1 && item + 2 * (int)gridDim.x < n_items)
+                *sNext = prep_item(item + 2 * gridDim.x, H, chunk_off, seq_start, seq_len, n_seqs);
+            if (!__syncthreads_and(ok)) {
+                ok = false;
+                break;
+            }
+        } else {
+        if (tid == 0) {
             tc_fence_after();
-            mma_tile<128, NST, 128, 128, NST>(tmem, smem_u32(sXL), smem_u32(sBS), false);
-            mma_tile<128, NST, 128, 128, NST>(tmem, smem_u32(sXL), smem_u32(sBS2), true);
+            mma_tile<128, C, 128, 128, C>(tmem, smem_u32(sXL), smem_u32(sm + P_COLH), false);
+            mma_tile<128, C, 128, 128, C>(tmem, smem_u32(sXL), smem_u32(sm + P_COLL), true);
             mma_commit(mbar);
         }
         mpend = true;
-        // global loads for later items, their latency hidden under the MMA:
-        // beta of the next item (used at its start), and the metadata of the
-        // item after it, fetched by one thread of a warp that does no TMEM
-        // readout (its dependent loads stall only that warp) and handed over
-        // in shared memory
-        if (has_next && tid < nxt.valid) beta_nxt = beta_of(nxt.tok0 + tid, nxt.h);
-        if (GATED && has_next) {
-            bias_nxt = gate_bias(nxt.h);
-            alog_nxt = gate_alog(nxt.h);
-        }
-        if (tid == kPrepThreads - 32 && item + 2 * (int)gridDim.x < n_items)
+        // metadata of the item after next, fetched by one thread whose
+        // dependent loads stall only its own warp, handed over in shared memory
+        if (tid == kPrepThreads - 1 && item + 2 * (int)gridDim.x < n_items)
             *sNext = prep_item(item + 2 * gridDim.x, H, chunk_off, seq_start, seq_len, n_seqs);
 
-        // While the MMA runs: QG = q_hat exp(G) and KD = k_hat exp(G_last - G)
-        // to the record, E = k_hat exp(G) (MN-major [j][d], for W = T E); both
-        // exponents are <= 0 and formed from the block-relative G.
-#pragma unroll 1
-        for (int it = 0; it < 2; ++it) {
-            const int r = 32 * it + (tid >> 4), d0 = (tid & 15) * 8, bj = r >> 4;
-            float rel8[8], gb8[8], lp8[8], qv[8], kv[8];
-            load8s(sG + r * D, d0, rel8);
-            load8s(sGref + bj * D, d0, gb8);
-            load8s(sPsi + bj * D, d0, lp8);
-            unpack8(*reinterpret_cast<const uint4 *>(sQr + r * D + d0), qv);
-            unpack8(*reinterpret_cast<const uint4 *>(sKr + r * D + d0), kv);
-            const float rq = sRq[r], rk = sRk[r];
-            float qg[8], e8[8], kd8[8];
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const float eg = __expf(gb8[t] + rel8[t]), kh = kv[t] * rk;
-                qg[t] = qv[t] * rq * eg;
-                e8[t] = kh * eg;
-                kd8[t] = kh * __expf(lp8[t] - rel8[t]);
-            }
-            *reinterpret_cast<uint4 *>(rec + TcRec::WQ + sw128_off(64 + r, d0, 128)) = pack8(qg);
-            *reinterpret_cast<uint4 *>(sE + sw128_off(r, d0, 64)) = pack8(e8);
-            *reinterpret_cast<uint4 *>(rec + TcRec::KD + sw128_off(r, d0, 64)) = pack8(kd8);
-        }
+        // 4. causal scores A (j <= r, to the record) and the beta-scaled
+        //    strictly lower L (to shared fp32 for the inverse): TMEM lanes
+        //    0..63 hold A's rows, 64..127 L's; warp w reads the 32 lanes of
+        //    quarter w % 4 and columns 32 (w / 4) .. +31.
+        float *sL = reinterpret_cast<float *>(sm + P_L);
         if (mbar_wait(mbar, mphase)) {
             mphase ^= 1;
             mpend = false;
@@ -540,81 +518,44 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             ok = false;
         }
         tc_fence_after();
+        KDA_PHASE(0, 5);
+        {
+            const int quarter = warp & 3, j0 = 32 * (warp >> 2);
+            float x[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + j0, x);
+            tmem_ld_wait();
+            if (quarter < 2) {
+                const int r = 32 * quarter + lane;
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    float y[8];
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) y[t] = (j0 + 8 * c8 + t <= r) ? x[8 * c8 + t] : 0.0f;
+                    *reinterpret_cast<uint4 *>(rec + TcRec::A + sw128_off(r, j0 + 8 * c8, C)) = pack8(y);
+                }
+            } else {
+                const int r = 32 * (quarter - 2) + lane;
+                const float bet = sB[r];
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    const int j = j0 + 4 * c4;
+                    float4 y;
+                    y.x = (j + 0 < r) ? bet * x[4 * c4 + 0] : 0.0f;
+                    y.y = (j + 1 < r) ? bet * x[4 * c4 + 1] : 0.0f;
+                    y.z = (j + 2 < r) ? bet * x[4 * c4 + 2] : 0.0f;
+                    y.w = (j + 3 < r) ? bet * x[4 * c4 + 3] : 0.0f;
+                    *reinterpret_cast<float4 *>(sL + r * LSTRIDE + j) = y;
+                }
+            }
+            tc_fence_before();
+        }
         if (!__syncthreads_and(ok)) {
             ok = false;  // uniform from here on: every thread takes the exit path
             break;
         }
-        // the q, k and g tiles are consumed: the next item's loads go out now
-        if (tid == kLoader && has_next) load_qkg(sm, maps, nxt.h, nxt.tok0, full, kGBytes);
-        fpend = has_next;
-        KDA_PHASE(0, 4);
+        KDA_PHASE(0, 6);
 
-        // 3. beta-scaled L rows (TMEM lanes 64..127) to shared fp32 by the
-        //    warps of lane quarters 2-3; A rows (lanes 0..63) to the record by
-        //    warps 4, 5, 8, 9, 12, 13, while the inverse starts as soon as L
-        //    is in place.  Row r of block br finds column j of its block pairs
-        //    at TMEM column pair_col0(br) + j.
-        {
-            float *sL = reinterpret_cast<float *>(sXL);
-            const int quarter = warp & 3;
-            const int r = 32 * (quarter & 1) + lane;  // row inside A (quarters 0,1) or L (2,3)
-            const int br = r >> 4;
-            const bool lo_pair = (quarter & 1) == 0;  // rows of blocks 0,1: columns [0, 48)
-            const int ntile = lo_pair ? 3 : 7;
-            const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16);
-            if (quarter >= 2) {
-                const float bet = sB[r];
-                for (int tile = warp >> 2; tile < ntile; tile += 4) {
-                    const int c0 = (lo_pair ? 0 : 48) + 16 * tile;
-                    float x[16];
-                    tmem_ld16(ta + c0, x);
-                    tmem_ld_wait();
-                    const int j0 = c0 - pair_col0(br);
-                    if (j0 < 0 || j0 >= 16 * (br + 1)) continue;
-#pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        const int j = j0 + 4 * c4;
-                        float4 y;
-                        y.x = (j + 0 < r) ? bet * x[4 * c4 + 0] : 0.0f;
-                        y.y = (j + 1 < r) ? bet * x[4 * c4 + 1] : 0.0f;
-                        y.z = (j + 2 < r) ? bet * x[4 * c4 + 2] : 0.0f;
-                        y.w = (j + 3 < r) ? bet * x[4 * c4 + 3] : 0.0f;
-                        *reinterpret_cast<float4 *>(sL + r * LSTRIDE + j) = y;
-                    }
-                }
-                tc_fence_before();
-                named_bar_sync(1, 320);
-            } else if (warp < 2) {
-                named_bar_sync(1, 320);
-            } else {
-                const int part = (warp >> 2) - 1;  // 0..2
-                for (int tile = part; tile < ntile; tile += 3) {
-                    const int c0 = (lo_pair ? 0 : 48) + 16 * tile;
-                    float x[16];
-                    tmem_ld16(ta + c0, x);
-                    tmem_ld_wait();
-                    const int j0 = c0 - pair_col0(br);
-                    if (j0 < 0 || j0 >= 16 * (br + 1)) continue;
-#pragma unroll
-                    for (int h8 = 0; h8 < 2; ++h8) {
-                        float y[8];
-#pragma unroll
-                        for (int t = 0; t < 8; ++t) y[t] = (j0 + 8 * h8 + t <= r) ? x[8 * h8 + t] : 0.0f;
-                        *reinterpret_cast<uint4 *>(rec + TcRec::A + sw128_off(r, j0 + 8 * h8, 64)) = pack8(y);
-                    }
-                }
-                // A entries right of a row's block diagonal are zero
-                for (int i = 64 * part + 32 * (quarter & 1) + lane; i < C * 8; i += 192) {
-                    const int ra = i >> 3, c8 = i & 7;
-                    if (c8 >= 2 * ((ra >> 4) + 1))
-                        *reinterpret_cast<uint4 *>(rec + TcRec::A + sw128_off(ra, 8 * c8, 64)) = make_uint4(0, 0, 0, 0);
-                }
-                tc_fence_before();
-            }
-        }
-        KDA_PHASE(0, 5);
-
-        // 4. X = (I + L)^-1 with L strictly lower (beta-scaled rows), in 16x16
+        // 5. X = (I + L)^-1 with L strictly lower (beta-scaled rows), in 16x16
         //    blocks, and T = X diag(beta) written straight into the bf16 hi + lo
         //    operand (K-major [i][j]) at sT.  Blocked forward substitution:
         //      A: per diagonal block a, forward substitution with (I + L_aa),
@@ -627,13 +568,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         //      C: X_20 = -(M_20 X_00 + M_21 X_10), X_31 = -(M_31 X_11 + M_32 X_21),
         //         X_30 = C30 X_00 + C31 X_10 (= -(M_30 X_00 + M_31 X_10 + M_32 X_20));
         //         zeros above the block diagonal.
-        //    Stages B and C give each thread one (row, 4 columns) slot.
+        //    Stages B and C hand out (row, 4 columns) slots, 256 at a time.
         {
-            const float *sL = reinterpret_cast<const float *>(sXL);
-            float *XD = reinterpret_cast<float *>(sBS);    // X_aa, a = 0..3
-            float *Mb = XD + 4 * MBLK;                     // M_ab, pairs p = 0..5
-            float *Cb = Mb + 6 * MBLK;                     // C30, C31
-            float *Xo = reinterpret_cast<float *>(sXL) + C * LSTRIDE;  // X_10, X_21
+            const float *cL = sL;
+            float *XD = reinterpret_cast<float *>(sm + P_SCR);  // X_aa, a = 0..3
+            float *Mb = XD + 4 * MBLK;                         // M_ab, pairs p = 0..5
+            float *Cb = Mb + 6 * MBLK;                         // C30, C31
+            float *Xo = Cb + 2 * MBLK;                         // X_10, X_21
             // Block pairs (a, b), a > b, index p: (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
             auto pair_a = [](int p_) { return p_ < 1 ? 1 : (p_ < 3 ? 2 : 3); };
             // T block (a, b), rows i, columns 4c4..4c4+3 from X values x
@@ -642,16 +583,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                 const float4 bt = *reinterpret_cast<const float4 *>(sB + col);
                 const float y0 = x.x * bt.x, y1 = x.y * bt.y, y2 = x.z * bt.z, y3 = x.w * bt.w;
                 const uint32_t h01 = pack2(y0, y1), h23 = pack2(y2, y3);
-                const float2 f01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&h01));
-                const float2 f23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&h23));
+                const float2 f01 = unpack2(h01), f23 = unpack2(h23);
                 const uint32_t off = sw128_off(row, col, 64);
                 *reinterpret_cast<uint2 *>(sT + off) = make_uint2(h01, h23);
                 *reinterpret_cast<uint2 *>(sT + 8192 + off) =
                     make_uint2(pack2(y0 - f01.x, y1 - f01.y), pack2(y2 - f23.x, y3 - f23.y));
             };
-            const int sidx = warp < 4 ? warp : (warp == 6 ? 4 : 5);  // stage A: warps 0, 1, 2, 3, 6
-            if (sidx < 5) {
-                const int sl = 32 * sidx + lane;
+            if (warp < 5) {
+                const int sl = 32 * warp + lane;
                 const bool unit = sl < 64;
                 const int p_ = unit ? 0 : (sl - 64) >> 4;
                 const int a = unit ? sl >> 4 : pair_a(p_);
@@ -661,8 +600,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
 #pragma unroll
                 for (int r = 0; r < 16; ++r) {
                     float lr[16];
-                    row16(sL + o, LSTRIDE, o + r, lr);
-                    const float rhs = unit ? (r == c ? 1.0f : 0.0f) : sL[(o + r) * LSTRIDE + 16 * b + c];
+                    row16(cL + o, LSTRIDE, o + r, lr);
+                    const float rhs = unit ? (r == c ? 1.0f : 0.0f) : cL[(o + r) * LSTRIDE + 16 * b + c];
                     // two partial sums shorten the dependent chain
                     float a0 = 0.0f, a1 = 0.0f;
 #pragma unroll
@@ -677,33 +616,31 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                 for (int r = 0; r < 16; ++r) dst[r * MS + c] = x[r];
             }
             __syncthreads();
-            KDA_PHASE(0, 6);
-            {
-                const int q_ = tid >> 6, ii = (tid >> 2) & 15, c4 = tid & 3;
-                if (q_ < 3) {  // X_{q+1,q} = -M_{q+1,q} X_qq
+            KDA_PHASE(0, 7);
+            for (int s = tid; s < 576; s += kPrepThreads) {  // warp-uniform slot ranges
+                const int ii = (s >> 2) & 15, c4 = s & 3;
+                if (s < 192) {  // X_{q+1,q} = -M_{q+1,q} X_qq
+                    const int q_ = s >> 6;
                     const int pm = q_ == 0 ? 0 : (q_ == 1 ? 2 : 5);
                     float4 x = mm16_row4(Mb + pm * MBLK, MS, XD + q_ * MBLK, MS, ii, c4);
                     x = make_float4(-x.x, -x.y, -x.z, -x.w);
                     if (q_ < 2) *reinterpret_cast<float4 *>(Xo + q_ * MBLK + ii * MS + 4 * c4) = x;
                     put_t(q_ + 1, q_, ii, c4, x);
-                } else if (q_ < 5) {  // C30 = M_32 M_20 - M_30, C31 = M_32 M_21 - M_31
-                    const int k_ = q_ - 3;
+                } else if (s < 320) {  // C30 = M_32 M_20 - M_30, C31 = M_32 M_21 - M_31
+                    const int k_ = (s - 192) >> 6;
                     float4 x = mm16_row4(Mb + 5 * MBLK, MS, Mb + (k_ == 0 ? 1 : 2) * MBLK, MS, ii, c4);
                     const float4 m = *reinterpret_cast<const float4 *>(Mb + (3 + k_) * MBLK + ii * MS + 4 * c4);
                     *reinterpret_cast<float4 *>(Cb + k_ * MBLK + ii * MS + 4 * c4) =
                         make_float4(x.x - m.x, x.y - m.y, x.z - m.z, x.w - m.w);
-                } else {  // diagonal blocks of T: 256 slots over the last 192 threads
-                    for (int sl = tid - 320; sl < 256; sl += 192) {
-                        const int a = sl >> 6, i = (sl >> 2) & 15, cc = sl & 3;
-                        put_t(a, a, i, cc, *reinterpret_cast<const float4 *>(XD + a * MBLK + i * MS + 4 * cc));
-                    }
+                } else {  // diagonal blocks of T
+                    const int a = (s - 320) >> 6;
+                    put_t(a, a, ii, c4, *reinterpret_cast<const float4 *>(XD + a * MBLK + ii * MS + 4 * c4));
                 }
             }
             __syncthreads();
-            KDA_PHASE(0, 12);
-            {
-                const int q_ = tid >> 6, ii = (tid >> 2) & 15, c4 = tid & 3;
-                if (q_ < 3) {
+            for (int s = tid; s < 576; s += kPrepThreads) {
+                if (s < 192) {
+                    const int q_ = s >> 6, ii = (s >> 2) & 15, c4 = s & 3;
                     float a16[16];
                     float4 x, y;
                     if (q_ == 0) {         // X_20 = -(M_20 X_00 + M_21 X_10)
@@ -711,15 +648,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                         x = row4_times(a16, XD, c4);
                         row16(Mb + 2 * MBLK, MS, ii, a16);
                         y = row4_times(a16, Xo, c4);
-                        x = make_float4(-(x.x + y.x), -(x.y + y.y), -(x.z + y.z), -(x.w + y.w));
-                        put_t(2, 0, ii, c4, x);
+                        put_t(2, 0, ii, c4, make_float4(-(x.x + y.x), -(x.y + y.y), -(x.z + y.z), -(x.w + y.w)));
                     } else if (q_ == 1) {  // X_31 = -(M_31 X_11 + M_32 X_21)
                         row16(Mb + 4 * MBLK, MS, ii, a16);
                         x = row4_times(a16, XD + MBLK, c4);
                         row16(Mb + 5 * MBLK, MS, ii, a16);
                         y = row4_times(a16, Xo + MBLK, c4);
-                        x = make_float4(-(x.x + y.x), -(x.y + y.y), -(x.z + y.z), -(x.w + y.w));
-                        put_t(3, 1, ii, c4, x);
+                        put_t(3, 1, ii, c4, make_float4(-(x.x + y.x), -(x.y + y.y), -(x.z + y.z), -(x.w + y.w)));
                     } else {               // X_30 = C30 X_00 + C31 X_10
                         row16(Cb, MS, ii, a16);
                         x = row4_times(a16, XD, c4);
@@ -728,23 +663,19 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                         put_t(3, 0, ii, c4, make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w));
                     }
                 } else {  // zeros above the block diagonal: 6 blocks x 16 rows x 2 chunks x hi, lo
-                    for (int sl = tid - 192; sl < 384; sl += 320) {
-                        const int pz = sl >> 6, i = (sl >> 2) & 15, h = (sl >> 1) & 1, hl = sl & 1;
-                        const int a = pz < 3 ? 0 : (pz < 5 ? 1 : 2);
-                        const int b = pz < 3 ? pz + 1 : (pz < 5 ? pz - 1 : 3);
-                        *reinterpret_cast<uint4 *>(sT + hl * 8192 + sw128_off(16 * a + i, 16 * b + 8 * h, 64)) =
-                            make_uint4(0, 0, 0, 0);
-                    }
+                    const int sl = s - 192;
+                    const int pz = sl >> 6, i = (sl >> 2) & 15, h = (sl >> 1) & 1, hl = sl & 1;
+                    const int a = pz < 3 ? 0 : (pz < 5 ? 1 : 2);
+                    const int b = pz < 3 ? pz + 1 : (pz < 5 ? pz - 1 : 3);
+                    *reinterpret_cast<uint4 *>(sT + hl * 8192 + sw128_off(16 * a + i, 16 * b + 8 * h, 64)) =
+                        make_uint4(0, 0, 0, 0);
                 }
             }
         }
-        __syncthreads();
-        KDA_PHASE(0, 7);
-
-        // 5. W = T E, U = T V (B operands MN-major: E from the row pass, V as
-        //    loaded); hi + lo parts of T.  The v tile was requested at the end
-        //    of the previous item; rows past the sequence end are zeroed.
-        if (mbar_wait(vfull, vphase)) {
+        KDA_PHASE(0, 8);
+        // the v tile (requested with q and k, or at the end of the previous
+        // item): rows past the sequence end are zeroed
+        if (mbar_wait(full_v, vphase)) {
             vphase ^= 1;
             vpend = false;
         } else {
@@ -752,7 +683,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
         for (int i = tid; i < (C - valid) * 16; i += kPrepThreads) {
             const int r = valid + i / 16, c16 = i % 16;
-            *reinterpret_cast<uint4 *>(sm + R_V + (c16 >> 3) * 8192 + r * 128 + (c16 & 7) * 16) =
+            *reinterpret_cast<uint4 *>(sm + P_V + (c16 >> 3) * 8192 + r * 128 + (c16 & 7) * 16) =
                 make_uint4(0, 0, 0, 0);
         }
         fence_async_smem();
@@ -761,16 +692,29 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             ok = false;  // uniform from here on: every thread takes the exit path
             break;
         }
+        // 6. W = T E, U = T V (hi + lo T); the q and k tiles of the next item
+        //    go out now (L and the inverse scratch are consumed), and its g
+        //    slice and beta are fetched into registers while the MMA runs.
         if (tid == 0) {
             tc_fence_after();
             mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 0, smem_u32(sT), smem_u32(sE), false);
             mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 0, smem_u32(sT + 8192), smem_u32(sE), true);
-            mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 128, smem_u32(sT), smem_u32(sm + R_V), false);
-            mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 128, smem_u32(sT + 8192), smem_u32(sm + R_V), true);
+            mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 128, smem_u32(sT), smem_u32(sm + P_V), false);
+            mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 128, smem_u32(sT + 8192), smem_u32(sm + P_V), true);
             mma_commit(mbar);
+            if (has_next) load_qk(sm, maps, nxt.h, nxt.tok0, full_qk);
         }
         mpend = true;
-        KDA_PHASE(0, 8);
+        qkpend = has_next;
+        if (has_next) {
+            load_gslice<GATED>(gs, g, gate, nxt.tok0, nxt.valid, r0, nxt.h, H, d);
+            if (tid < nxt.valid) beta_nxt = beta_of(nxt.tok0 + tid, nxt.h);
+            if (GATED) {
+                bias_nxt = *reinterpret_cast<const float4 *>(gate.dt_bias + nxt.h * D + d);
+                alog_nxt = gate.a_log[nxt.h];
+            }
+        }
+        KDA_PHASE(0, 9);
         if (mbar_wait(mbar, mphase)) {
             mphase ^= 1;
             mpend = false;
@@ -779,38 +723,35 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
         tc_fence_after();
         // v is consumed: the next item's v load goes out
-        if (tid == kLoader && has_next) load_v(sm, maps, nxt.h, nxt.tok0, vfull);
+        if (tid == 0 && has_next) load_v(sm, maps, nxt.h, nxt.tok0, full_v);
         vpend = has_next;
+        KDA_PHASE(0, 10);
 
-        // 6. W rows (WQ rows 0..63) and U: TMEM lanes 0..63 -> shared memory
-        //    (sXL, free since the T conversion) in the record's own layout ->
-        //    three bulk copies to the record.  U rows are stored with their
-        //    16-byte chunks rotated (chunk c of row i at c ^ ((i / 2) % 4)),
-        //    which keeps these writes and the scan's reads free of bank
-        //    conflicts.  The staging area is reused once the copies have read
-        //    it (checked before the next row pass).
+        // 7. W rows and U: TMEM lanes 0..63 (warps of quarters 0, 1; warps
+        //    0, 1 take W, warps 4, 5 take U) -> shared memory in the record's
+        //    own layout -> three bulk copies to the record.  U rows are stored
+        //    with their 16-byte chunks rotated (chunk c of row i at
+        //    c ^ ((i / 2) % 4)), which keeps these writes and the scan's reads
+        //    free of bank conflicts.
+        unsigned char *stg = sm + P_STAGE;
         if ((warp & 3) < 2) {
             const int i = 32 * (warp & 3) + lane, part = warp >> 2;
-            const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-            float x[32];
-            tmem_ld32(ta + 32 * part, x);
-            tmem_ld_wait();
+            const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 128 * part;
+#pragma unroll 1
+            for (int cb = 0; cb < 4; ++cb) {
+                float x[32];
+                tmem_ld32(ta + 32 * cb, x);
+                tmem_ld_wait();
 #pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-                float y[8];
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    float y[8];
 #pragma unroll
-                for (int t = 0; t < 8; ++t) y[t] = x[8 * c8 + t];
-                *reinterpret_cast<uint4 *>(sXL + sw128_off(i, 32 * part + 8 * c8, 64)) = pack8(y);
-            }
-            tmem_ld32(ta + 128 + 32 * part, x);
-            tmem_ld_wait();
-            unsigned char *ub = sXL + 16384 + part * TcRec::UBLK + i * 64;
-#pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-                float y[8];
-#pragma unroll
-                for (int t = 0; t < 8; ++t) y[t] = x[8 * c8 + t];
-                *reinterpret_cast<uint4 *>(ub + ((c8 ^ ((i >> 1) & 3)) << 4)) = pack8(y);
+                    for (int t = 0; t < 8; ++t) y[t] = x[8 * c8 + t];
+                    unsigned char *dst = part == 0
+                        ? stg + sw128_off(i, 32 * cb + 8 * c8, 64)
+                        : stg + 16384 + cb * TcRec::UBLK + i * 64 + ((c8 ^ ((i >> 1) & 3)) << 4);
+                    *reinterpret_cast<uint4 *>(dst) = pack8(y);
+                }
             }
         }
         fence_async_smem();
@@ -819,32 +760,35 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             ok = false;  // uniform from here on: every thread takes the exit path
             break;
         }
-        if (tid == kLoader) {
-            bulk_s2g(rec + TcRec::WQ, sXL, 8192);                  // W, key columns 0..63
-            bulk_s2g(rec + TcRec::WQ + 16384, sXL + 8192, 8192);   // W, key columns 64..127
-            bulk_s2g(rec + TcRec::U, sXL + 16384, 4 * TcRec::UBLK);
+        if (tid == 0) {
+            bulk_s2g(rec + TcRec::WQ, stg, 8192);                  // W, key columns 0..63
+            bulk_s2g(rec + TcRec::WQ + 16384, stg + 8192, 8192);   // W, key columns 64..127
+            bulk_s2g(rec + TcRec::U, stg + 16384, 4 * TcRec::UBLK);
             bulk_commit();
         }
-        KDA_PHASE(0, 9);
+        }
+        KDA_PHASE(0, 11);
         cur = nxt;
         if (item + 2 * (int)gridDim.x < n_items) nxt = *sNext;
         beta_cur = beta_nxt;
         bias_cur = bias_nxt;
         alog_cur = alog_nxt;
     }
-    if (tid == kLoader) bulk_wait_all();  // the last record's W and U are written
+    if (tid == 0) bulk_wait_all();  // the last record's W and U are written
     if (!ok) {
-        if (tid == kLoader) {
+        if (tid == 0) {
             atomicOr(status, kStatusTimeout);
             // let copies and MMAs still in flight land before the shared memory
             // and the TMEM are released
-            if (fpend) mbar_wait(full, fphase, 400000000LL);
-            if (vpend) mbar_wait(vfull, vphase, 400000000LL);
+            if (qkpend) mbar_wait(full_qk, qkphase, 400000000LL);
+            if (vpend) mbar_wait(full_v, vphase, 400000000LL);
             if (mpend) mbar_wait(mbar, mphase, 400000000LL);
         }
         __syncthreads();
     }
     KDA_PHASE_FLUSH(0);
+    tc_fence_before();
+    __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
 }
 
@@ -1319,77 +1263,36 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 
 }  // namespace
 
-namespace {
-
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
-        cudaGetLastError();
-    });
-    return fn;
-}
-
-// 3-D map {128, H, T} over a [T, H, 128] tensor; box 128 x 1 x 64.
-bool encode_rows(CUtensorMap *m, const void *base, CUtensorMapDataType dt, size_t elem, int H,
-                 int64_t T, bool swizzled64 = false) {
-    auto enc = tensor_map_encoder();
-    if (!enc) return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
-    const cuuint64_t strides[2] = {(cuuint64_t)(D * elem), (cuuint64_t)(D * elem) * (cuuint64_t)H};
-    const cuuint32_t box[3] = {(cuuint32_t)(swizzled64 ? 64 : D), 1, (cuuint32_t)C};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE,
-               swizzled64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-}  // namespace
-
 cudaError_t launch_chunk_prep_tc(const void *q, const void *k, const void *v, const float *g,
                                  const float *beta, const GateArgs *gate, int n_seqs,
                                  int64_t total_tokens, int H, float scale, void *workspace,
                                  cudaStream_t stream) {
     const WsLayout L = ws_layout(total_tokens, n_seqs, H, TcRec::bytes);
     const int64_t items_max = max_chunks(total_tokens, n_seqs) * (int64_t)H;
-    const int grid = (int)std::min<int64_t>(items_max, (int64_t)sm_count());
+    const int grid = (int)std::min<int64_t>(items_max, (int64_t)kPrepMinBlocks * sm_count());
     RawMaps maps;
     memset(&maps, 0, sizeof(maps));
     if (total_tokens > 0) {
-        if (!encode_rows(&maps.q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, total_tokens) ||
-            !encode_rows(&maps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, total_tokens) ||
-            !encode_rows(&maps.v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, total_tokens, true) ||
-            !(gate ? encode_rows(&maps.g, gate->raw_gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H,
-                                 total_tokens)
-                   : encode_rows(&maps.g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, total_tokens)))
+        if (!encode_rows(&maps.q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, total_tokens, true) ||
+            !encode_rows(&maps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, total_tokens, true) ||
+            !encode_rows(&maps.v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, total_tokens, true))
             return cudaErrorInvalidValue;
     }
     GateArgs ga;
     memset(&ga, 0, sizeof(ga));
-    if (gate) {
-        ga = *gate;
-        cudaFuncSetAttribute(chunk_prep_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             P_SMEM);
-        const cudaError_t e = launch_dependent(chunk_prep_tc_kernel<true>, dim3(grid), dim3(kPrepThreads),
-                                               P_SMEM, stream, maps, beta, ga, n_seqs, H, scale,
-                                               workspace, L);
-        if (e != cudaSuccess) return e;
-    } else {
-        cudaFuncSetAttribute(chunk_prep_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             P_SMEM);
-        const cudaError_t e = launch_dependent(chunk_prep_tc_kernel<false>, dim3(grid),
-                                               dim3(kPrepThreads), P_SMEM, stream, maps, beta, ga,
-                                               n_seqs, H, scale, workspace, L);
-        if (e != cudaSuccess) return e;
-    }
-    return cudaGetLastError();
+    if (gate) ga = *gate;
+    auto kern = gate ? chunk_prep_tc_kernel<true> : chunk_prep_tc_kernel<false>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
+    cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
+    cudaError_t e = launch_dependent(kern, dim3(grid), dim3(kPrepThreads), P_SMEM, stream, maps, g,
+                                     beta, ga, n_seqs, H, scale, workspace, L);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    // the items deferred above (none in most workloads: its CTAs then exit at once)
+    if (e == cudaSuccess)
+        e = launch_chunk_prep_tc_strong(q, k, v, g, beta, gate, n_seqs, total_tokens, H, scale,
+                                        workspace, stream);
+    return e;
 }
 
 cudaError_t launch_chunk_scan_tc(const float *initial_state, float *final_state,

@@ -47,9 +47,12 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 // ---- workspace layout -----------------------------------------------------
 //
-//   [0, 256)      status word (int32, StatusBits) + padding
+//   [0, 256)      status word (int32, StatusBits), deferred-item count (int32,
+//                 tensor-core path) + padding
 //   [256, ...)    seq_start[N] int32 (-1 = sequence skipped), seq_len[N] int32,
 //                 chunk_off[N+1] int32 (exclusive prefix sum of chunks per seq)
+//   aligned(16)   deferred (chunk, head) items, int32 [max chunks * H]
+//                 (tensor-core path: the items handed to the strong-decay prep)
 //   aligned(256)  per-(chunk, head) records, index chunk * H + head
 //
 // The record contents depend on the chunk path (fp32 CUDA-core path or bf16
@@ -59,7 +62,8 @@ enum StatusBits : int {
     kBadSeqlens = KDA_WS_BAD_SEQLENS,
     kBadSlot = KDA_WS_BAD_SLOT,
     kStatusTimeout = KDA_WS_TIMEOUT,
-    kExactDecay = KDA_WS_EXACT_DECAY
+    kExactDecay = KDA_WS_EXACT_DECAY,
+    kStrongDecay = KDA_WS_STRONG_DECAY
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -70,8 +74,8 @@ __host__ __device__ inline int64_t max_chunks(int64_t total_tokens, int n_seqs) 
 }
 
 struct WsLayout {
-    size_t status_off, seq_start_off, seq_len_off, chunk_off_off, records_off, record_bytes,
-        total;
+    size_t status_off, defer_count_off, seq_start_off, seq_len_off, chunk_off_off, defer_off,
+        records_off, record_bytes, total;
 };
 
 __host__ __device__ inline WsLayout ws_layout(int64_t total_tokens, int n_seqs, int H,
@@ -79,12 +83,15 @@ __host__ __device__ inline WsLayout ws_layout(int64_t total_tokens, int n_seqs, 
     WsLayout L;
     const size_t arr = align_up(sizeof(int32_t) * (size_t)(n_seqs + 1), 16);
     L.status_off = 0;
+    L.defer_count_off = 4;
     L.seq_start_off = 256;
     L.seq_len_off = L.seq_start_off + arr;
     L.chunk_off_off = L.seq_len_off + arr;
-    L.records_off = align_up(L.chunk_off_off + arr, 256);
+    L.defer_off = L.chunk_off_off + arr;
+    const size_t items = (size_t)max_chunks(total_tokens, n_seqs) * (size_t)H;
+    L.records_off = align_up(L.defer_off + sizeof(int32_t) * items, 256);
     L.record_bytes = record_bytes;
-    L.total = L.records_off + (size_t)max_chunks(total_tokens, n_seqs) * (size_t)H * record_bytes;
+    L.total = L.records_off + items * record_bytes;
     return L;
 }
 
@@ -228,6 +235,14 @@ cudaError_t launch_chunk_prep_tc(const void *q, const void *k, const void *v, co
                                  const float *beta, const GateArgs *gate, int n_seqs,
                                  int64_t total_tokens, int H, float scale, void *workspace,
                                  cudaStream_t stream);
+
+// The strong-decay prep of the tensor-core path: the (chunk, head) items that
+// chunk_prep_tc deferred (listed in the workspace), with per-16-token decay
+// references.  Launched right after launch_chunk_prep_tc, same arguments.
+cudaError_t launch_chunk_prep_tc_strong(const void *q, const void *k, const void *v,
+                                        const float *g, const float *beta, const GateArgs *gate,
+                                        int n_seqs, int64_t total_tokens, int H, float scale,
+                                        void *workspace, cudaStream_t stream);
 
 // Activated g and beta of a gated call into fp32 buffers (the fp32 path).
 cudaError_t launch_gate_activation(const GateArgs &gate, int dtype, int64_t total_tokens, int H,

@@ -62,15 +62,16 @@ def test_header_status_values_match_the_binding():
     bits = dict(re.findall(r"^#define\s+(KDA_WS_\w+)\s+(\d+)", text, flags=re.M))
     assert {k: int(v) for k, v in bits.items()} == {
         "KDA_WS_BAD_SEQLENS": kda.KDA_WS_BAD_SEQLENS, "KDA_WS_BAD_SLOT": kda.KDA_WS_BAD_SLOT,
-        "KDA_WS_TIMEOUT": kda.KDA_WS_TIMEOUT, "KDA_WS_EXACT_DECAY": kda.KDA_WS_EXACT_DECAY}
+        "KDA_WS_TIMEOUT": kda.KDA_WS_TIMEOUT, "KDA_WS_EXACT_DECAY": kda.KDA_WS_EXACT_DECAY,
+        "KDA_WS_STRONG_DECAY": kda.KDA_WS_STRONG_DECAY}
 
 
-@pytest.mark.parametrize("flags", range(16))
+@pytest.mark.parametrize("flags", range(32))
 def test_workspace_status_word_maps_to_a_status(lib, flags):
     """Every combination of the status word's bits, as the kernels would leave
     them in a workspace, decodes to the documented kda_status: a bounded wait
-    that gave up dominates, then the device-side argument errors; the
-    exact-decay bit is informational."""
+    that gave up dominates, then the device-side argument errors; the two
+    decay bits are informational."""
     st = kda.kda_status_from_workspace_flags(flags)
     if flags & kda.KDA_WS_TIMEOUT:
         assert st == kda.KDA_ERR_DEVICE_TIMEOUT
