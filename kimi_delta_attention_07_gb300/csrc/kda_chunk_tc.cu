@@ -65,16 +65,16 @@ constexpr int kPrepThreads = 256;
 constexpr int kPrepMinBlocks = 2;        // two CTAs per SM overlap each other's phases
 constexpr uint32_t kPrepTmemCols = 256;  // A/L result 0..63; then W 0..127, U 128..255
 constexpr float kLog2e = 1.4426950408889634f;
-// Largest |G_r - G_31| (natural log units) the factorised exponentials take:
-// both factors and every product of unmasked pairs stay inside fp32 / bf16
-// range with margin.  Chunks beyond it are deferred to the strong-decay prep.
+// Largest |G_r - G_ref| (natural log units, ref = the reference row of r's
+// half) the factorised exponentials take: both factors stay inside fp32 /
+// bf16 range.  Chunks beyond it are deferred to the strong-decay prep.
 constexpr float kRelLimit2 = 80.0f * kLog2e;
+constexpr int NCOL = 96;  // B operand rows of the A/L MMA: 32 per (column half, reference)
 // shared memory plan (offsets from a 1024-aligned base)
 constexpr int P_XL = 0;             // 32 KB: raw [q ; k] (TMA) -> [q_hat x ; k_hat x]
-constexpr int P_COLH = 32768;       // 16 KB: k_hat / x, hi part (B operand of the A/L MMA)
-constexpr int P_COLL = 49152;       // 16 KB: its lo part
-constexpr int P_E = 65536;          // 16 KB: E = k_hat exp(G), MN-major [j][d]
-constexpr int P_V = 81920;          // 16 KB: v, MN-major (two 64-column boxes)
+constexpr int P_COLH = 32768;       // 24 KB: the column operand, hi part (B operand of A/L)
+constexpr int P_COLL = 57344;       // 24 KB: its lo part
+constexpr int P_E = 81920;          // 16 KB: E = k_hat exp(G), MN-major [j][d]
 constexpr int P_RQ = 98304;         // fp32 [64]: scale / |q_r|
 constexpr int P_RK = P_RQ + 256;    // fp32 [64]: 1 / |k_r|
 constexpr int P_BETA = P_RK + 256;  // fp32 [64]
@@ -86,13 +86,16 @@ constexpr int P_SMEM = P_BYTES + 1024;
 constexpr int P_L = 0;              // fp32 [64][LSTRIDE]: beta-scaled L
 constexpr int P_SCR = 17408;        // inverse scratch: 14 16x16 fp32 blocks
 constexpr int P_T = 36864;          // T operand, hi (8 KB) and lo (8 KB)
+constexpr int P_V = 53248;          // 16 KB: v, MN-major (two 64-column boxes), loaded after A/L
 constexpr int P_STAGE = 32768;      // W and U staged for the record after the W/U MMA
 constexpr int LSTRIDE = 68;         // row stride (floats) of L in shared memory
 constexpr int MS = 20;              // row stride (floats) of 16x16 scratch matrices
 constexpr int MBLK = 16 * MS;       // floats per 16x16 scratch matrix
 static_assert(P_SMEM * kPrepMinBlocks + 2048 <= 233472, "two prep CTAs per SM");
 static_assert(P_L + C * LSTRIDE * 4 <= P_SCR && P_SCR + 14 * MBLK * 4 <= P_T, "L, scratch, T");
-static_assert(P_T + 16384 <= P_E && P_STAGE + 32768 <= P_E, "T and staging below E");
+static_assert(P_T + 16384 <= P_V && P_V + 16384 <= P_E && P_STAGE + 32768 <= P_E,
+              "T, v and staging below E");
+static_assert(P_COLL + NCOL * 256 <= P_E, "column operand");
 
 struct PrepItem {
     int64_t tok0;
@@ -284,10 +287,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
     };
     int item = blockIdx.x;
     PrepItem cur = prep_item(item, H, chunk_off, seq_start, seq_len, n_seqs);
-    if (tid == 0) {
-        load_qk(sm, maps, cur.h, cur.tok0, full_qk);
-        load_v(sm, maps, cur.h, cur.tok0, full_v);
-    }
+    if (tid == 0) load_qk(sm, maps, cur.h, cur.tok0, full_qk);
     GSlice<GATED> gs;
     load_gslice<GATED>(gs, g, gate, cur.tok0, cur.valid, r0, cur.h, H, d);
     float beta_cur = tid < cur.valid ? beta_of(cur.tok0 + tid, cur.h) : 0.0f;
@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
         nxt = prep_item(item + gridDim.x, H, chunk_off, seq_start, seq_len, n_seqs);
 
     uint32_t qkphase = 0, vphase = 0, mphase = 0;
-    bool qkpend = true, vpend = true, mpend = false;
+    bool qkpend = true, vpend = false, mpend = false;
     bool ok = true;
     KDA_PHASE_START();
     for (; item < n_items; item += gridDim.x) {
@@ -351,7 +351,9 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
         }
         KDA_PHASE(0, 1);
         // 2. row norms of q and k (raw tiles in the A operand's K-major
-        //    layout): one (row, 64-channel half) per thread, two threads per row
+        //    layout): one (row, 64-channel half) per thread, two threads per row;
+        //    step c reads the row's 16-byte unit c ^ (row % 8), so that eight
+        //    consecutive rows cover all 32 banks
         {
             const int R = tid >> 1, half = tid & 1;  // R: 0..63 q rows, 64..127 k rows
             const unsigned char *row = sXL + half * 16384 + R * 128;
@@ -359,7 +361,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 float x[8];
-                unpack8(*reinterpret_cast<const uint4 *>(row + (c << 4)), x);
+                unpack8(*reinterpret_cast<const uint4 *>(row + ((c ^ (R & 7)) << 4)), x);
 #pragma unroll
                 for (int t = 0; t < 8; ++t) ss = fmaf(x[t], x[t], ss);
             }
@@ -376,84 +378,118 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
         }
         KDA_PHASE(0, 2);
 
-        // 3. per row of the slice: G_r - G_31 (the reference is row 31, the
-        //    middle of the chunk; log2 units), x = exp(G_r - G_31), and from
-        //    them the operands q_hat x, k_hat x (in place over the raw tiles),
-        //    k_hat / x (hi + lo), E = k_hat x e^{G_31}, QG = q_hat x e^{G_31}
-        //    and KD = (k_hat / x) e^{G_63 - G_31}.  A chunk with any
-        //    |G_r - G_31| beyond the limit is deferred as a whole (its outputs
-        //    here are discarded: the strong-decay prep rewrites its record).
+        // 3. per row of the slice, with the reference row m of its half
+        //    (m = 15 for rows 0..31, 47 for rows 32..63; log2 units): G_r - G_m,
+        //    x = exp(G_r - G_m), and from them the operands q_hat x, k_hat x
+        //    (in place over the raw tiles) and the column operand k_hat / x
+        //    (hi + lo), so that exp(G_r - G_j) = x_r / x_j for r, j in one half;
+        //    rows of the first half also give k_hat e^{G_47 - G_j} = (k_hat / x)
+        //    e^{G_47 - G_15} (<= 1), the columns that rows of the second half
+        //    pair with them.  E = k_hat x e^{G_m} and QG = q_hat x e^{G_m} (both
+        //    k_hat e^{G_r}, q_hat e^{G_r}), KD = (k_hat / x) e^{G_63 - G_m}.  A
+        //    chunk with any |G_r - G_m| beyond the limit is deferred as a whole
+        //    (its outputs here are discarded: the strong-decay prep rewrites its
+        //    record).
         bool wide = false;
         {
-            float4 before = make_float4(0.f, 0.f, 0.f, 0.f), c2 = before, tot = before;
+            const int hf = warp >> 2;  // this warp's half of the chunk
+            float4 before = make_float4(0.f, 0.f, 0.f, 0.f), g15 = before, g47 = before, tot = before;
 #pragma unroll
             for (int o = 0; o < 8; ++o) {
                 const float4 s = *reinterpret_cast<const float4 *>(sQS + o * D + d);
                 if (o < warp) {
                     before.x += s.x; before.y += s.y; before.z += s.z; before.w += s.w;
                 }
-                if (o < 4) {
-                    c2.x += s.x; c2.y += s.y; c2.z += s.z; c2.w += s.w;
+                if (o < 2) {
+                    g15.x += s.x; g15.y += s.y; g15.z += s.z; g15.w += s.w;
+                }
+                if (o < 6) {
+                    g47.x += s.x; g47.y += s.y; g47.z += s.z; g47.w += s.w;
                 }
                 tot.x += s.x; tot.y += s.y; tot.z += s.z; tot.w += s.w;
             }
-            const float4 off = make_float4(before.x - c2.x, before.y - c2.y, before.z - c2.z, before.w - c2.w);
-            const float4 tail = make_float4(tot.x - c2.x, tot.y - c2.y, tot.z - c2.z, tot.w - c2.w);
+            const float4 ref = hf ? g47 : g15;
+            const float4 tail = make_float4(tot.x - ref.x, tot.y - ref.y, tot.z - ref.z, tot.w - ref.w);
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {  // pre becomes G_r - G_m
+                pre[i].x += before.x - ref.x;
+                pre[i].y += before.y - ref.y;
+                pre[i].z += before.z - ref.z;
+                pre[i].w += before.w - ref.w;
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(pre[i].x), fabsf(pre[i].y)),
+                                         fmaxf(fabsf(pre[i].z), fabsf(pre[i].w))));
+            }
+            wide = !(amax <= kRelLimit2);  // also catches a non-finite decay
+            // thread bases: XL (K-major, 128 rows), the column operand (96 rows),
+            // 64-row tiles (E, KD), QG rows of WQ
+            unsigned char *xl = sXL + kb * 16384 + r0 * 128 + hb;
+            unsigned char *cop = sm + P_COLH + kb * (NCOL * 128) + r0 * 128 + hb;
+            unsigned char *e64 = sE + kb * 8192 + r0 * 128 + hb;
+            unsigned char *qg = rec + TcRec::WQ + kb * 16384 + (C + r0) * 128 + hb;
+            unsigned char *kd = rec + TcRec::KD + kb * 8192 + r0 * 128 + hb;
+            constexpr int kLo = P_COLL - P_COLH;
+            // hi + lo bf16 parts of four column values at byte offset `at`
+            auto put_col = [&](int at, const float (&c)[4]) {
+                const uint2 hi = make_uint2(pack2(c[0], c[1]), pack2(c[2], c[3]));
+                const float2 h01 = unpack2(hi.x), h23 = unpack2(hi.y);
+                *reinterpret_cast<uint2 *>(cop + at) = hi;
+                *reinterpret_cast<uint2 *>(cop + kLo + at) =
+                    make_uint2(pack2(c[0] - h01.x, c[1] - h01.y), pack2(c[2] - h23.x, c[3] - h23.y));
+            };
+            if (hf == 0) {
+                // first-half columns again, referenced to row 47, from the raw
+                // k tile (before it is overwritten below): k_hat e^{G_47 - G_j},
+                // <= 1, its exponent formed directly so that it underflows only
+                // where the products it enters are negligible
+                const float4 d47 = make_float4(g15.x - g47.x, g15.y - g47.y, g15.z - g47.z, g15.w - g47.w);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int o16 = i * 128 + ((cw ^ i) << 4);
+                    const uint2 kraw = *reinterpret_cast<const uint2 *>(xl + 8192 + o16);
+                    const bool live = r0 + i < valid;
+                    const float2 k01 = unpack2(live ? kraw.x : 0u), k23 = unpack2(live ? kraw.y : 0u);
+                    const float rk = sRk[r0 + i];
+                    const float c2[4] = {k01.x * rk * ex2(-(pre[i].x + d47.x)), k01.y * rk * ex2(-(pre[i].y + d47.y)),
+                                         k23.x * rk * ex2(-(pre[i].z + d47.z)), k23.y * rk * ex2(-(pre[i].w + d47.w))};
+                    put_col(o16 + C * 128, c2);
+                }
+            }
             if (warp == 0)
                 *reinterpret_cast<float4 *>(rec + TcRec::GC + 4 * d) =
                     make_float4(ex2(tot.x), ex2(tot.y), ex2(tot.z), ex2(tot.w));
-            const float ec[4] = {ex2(c2.x), ex2(c2.y), ex2(c2.z), ex2(c2.w)};
+            const float ec[4] = {ex2(ref.x), ex2(ref.y), ex2(ref.z), ex2(ref.w)};
             const float el[4] = {ex2(tail.x), ex2(tail.y), ex2(tail.z), ex2(tail.w)};
-            const float4 rq03 = *reinterpret_cast<const float4 *>(sRq + r0);
-            const float4 rq47 = *reinterpret_cast<const float4 *>(sRq + r0 + 4);
-            const float4 rk03 = *reinterpret_cast<const float4 *>(sRk + r0);
-            const float4 rk47 = *reinterpret_cast<const float4 *>(sRk + r0 + 4);
-            const float rqs[8] = {rq03.x, rq03.y, rq03.z, rq03.w, rq47.x, rq47.y, rq47.z, rq47.w};
-            const float rks[8] = {rk03.x, rk03.y, rk03.z, rk03.w, rk47.x, rk47.y, rk47.z, rk47.w};
-            // thread bases: XL (K-major, 128 rows), 64-row tiles (COL, E, KD), QG rows of WQ
-            unsigned char *xl = sXL + kb * 16384 + r0 * 128 + hb;
-            unsigned char *c64 = sm + P_COLH + kb * 8192 + r0 * 128 + hb;
-            unsigned char *qg = rec + TcRec::WQ + kb * 16384 + (C + r0) * 128 + hb;
-            unsigned char *kd = rec + TcRec::KD + kb * 8192 + r0 * 128 + hb;
-            float amax = 0.0f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int o16 = i * 128 + ((cw ^ i) << 4);  // row r0 + i, this thread's 8 bytes
-                const float rel[4] = {pre[i].x + off.x, pre[i].y + off.y, pre[i].z + off.z, pre[i].w + off.w};
+                const float rel[4] = {pre[i].x, pre[i].y, pre[i].z, pre[i].w};
                 const uint2 qraw = *reinterpret_cast<const uint2 *>(xl + o16);
                 const uint2 kraw = *reinterpret_cast<const uint2 *>(xl + 8192 + o16);
                 const bool live = r0 + i < valid;  // rows past the sequence end: zero
                 const float2 q01 = unpack2(live ? qraw.x : 0u), q23 = unpack2(live ? qraw.y : 0u);
                 const float2 k01 = unpack2(live ? kraw.x : 0u), k23 = unpack2(live ? kraw.y : 0u);
                 const float qv[4] = {q01.x, q01.y, q23.x, q23.y}, kv[4] = {k01.x, k01.y, k23.x, k23.y};
-                float qx[4], kx[4], col[4], lo[4];
+                const float rq = sRq[r0 + i], rk = sRk[r0 + i];
+                float qx[4], kx[4], col[4];
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
-                    amax = fmaxf(amax, fabsf(rel[t]));
                     const float x = ex2(rel[t]), ir = ex2(-rel[t]);
-                    const float kh = kv[t] * rks[i];
-                    qx[t] = qv[t] * rqs[i] * x;
+                    const float kh = kv[t] * rk;
+                    qx[t] = qv[t] * rq * x;
                     kx[t] = kh * x;
                     col[t] = kh * ir;
                 }
-                const uint2 hi = make_uint2(pack2(col[0], col[1]), pack2(col[2], col[3]));
-                {
-                    const float2 h01 = unpack2(hi.x), h23 = unpack2(hi.y);
-                    lo[0] = col[0] - h01.x; lo[1] = col[1] - h01.y;
-                    lo[2] = col[2] - h23.x; lo[3] = col[3] - h23.y;
-                }
                 *reinterpret_cast<uint2 *>(xl + o16) = make_uint2(pack2(qx[0], qx[1]), pack2(qx[2], qx[3]));
                 *reinterpret_cast<uint2 *>(xl + 8192 + o16) = make_uint2(pack2(kx[0], kx[1]), pack2(kx[2], kx[3]));
-                *reinterpret_cast<uint2 *>(c64 + o16) = hi;
-                *reinterpret_cast<uint2 *>(c64 + 16384 + o16) = make_uint2(pack2(lo[0], lo[1]), pack2(lo[2], lo[3]));
-                *reinterpret_cast<uint2 *>(c64 + 32768 + o16) =
+                put_col(o16, col);
+                *reinterpret_cast<uint2 *>(e64 + o16) =
                     make_uint2(pack2(kx[0] * ec[0], kx[1] * ec[1]), pack2(kx[2] * ec[2], kx[3] * ec[3]));
                 *reinterpret_cast<uint2 *>(qg + o16) =
                     make_uint2(pack2(qx[0] * ec[0], qx[1] * ec[1]), pack2(qx[2] * ec[2], qx[3] * ec[3]));
                 *reinterpret_cast<uint2 *>(kd + o16) =
                     make_uint2(pack2(col[0] * el[0], col[1] * el[1]), pack2(col[2] * el[2], col[3] * el[3]));
             }
-            wide = !(amax <= kRelLimit2);  // also catches a non-finite decay
         }
         KDA_PHASE(0, 3);
         fence_async_smem();
@@ -463,22 +499,14 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
         float beta_nxt = 0.0f, alog_nxt = 0.0f;
         float4 bias_nxt = make_float4(0.f, 0.f, 0.f, 0.f);
         if (defer) {
-            // hand the item to the strong-decay prep; the next item's tiles go
-            // out at once (its v load once this item's v copy has landed)
+            // hand the item to the strong-decay prep; the next item's q and k
+            // tiles go out at once
             if (tid == 0) {
                 defer_list[atomicAdd(defer_count, 1)] = item;
                 atomicOr(status, kStrongDecay);
                 if (has_next) load_qk(sm, maps, nxt.h, nxt.tok0, full_qk);
             }
             qkpend = has_next;
-            if (mbar_wait(full_v, vphase)) {
-                vphase ^= 1;
-                vpend = false;
-            } else {
-                ok = false;
-            }
-            if (tid == 0 && has_next && ok) load_v(sm, maps, nxt.h, nxt.tok0, full_v);
-            vpend = has_next && ok;
             if (has_next) {
                 load_gslice<GATED>(gs, g, gate, nxt.tok0, nxt.valid, r0, nxt.h, H, d);
                 if (tid < nxt.valid) beta_nxt = beta_of(nxt.tok0 + tid, nxt.h);
@@ -496,8 +524,8 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
         } else {
         if (tid == 0) {
             tc_fence_after();
-            mma_tile<128, C, 128, 128, C>(tmem, smem_u32(sXL), smem_u32(sm + P_COLH), false);
-            mma_tile<128, C, 128, 128, C>(tmem, smem_u32(sXL), smem_u32(sm + P_COLL), true);
+            mma_tile<128, NCOL, 128, 128, NCOL>(tmem, smem_u32(sXL), smem_u32(sm + P_COLH), false);
+            mma_tile<128, NCOL, 128, 128, NCOL>(tmem, smem_u32(sXL), smem_u32(sm + P_COLL), true);
             mma_commit(mbar);
         }
         mpend = true;
@@ -509,7 +537,10 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
         // 4. causal scores A (j <= r, to the record) and the beta-scaled
         //    strictly lower L (to shared fp32 for the inverse): TMEM lanes
         //    0..63 hold A's rows, 64..127 L's; warp w reads the 32 lanes of
-        //    quarter w % 4 and columns 32 (w / 4) .. +31.
+        //    quarter w % 4 for output columns j0 = 32 (w / 4) .. +31, which a
+        //    row of the first half finds at TMEM columns j (j < 32), a row of
+        //    the second half at 64 + j (j < 32) and at j (j >= 32).  The v tile
+        //    goes out as soon as the column operand has been read.
         float *sL = reinterpret_cast<float *>(sm + P_L);
         if (mbar_wait(mbar, mphase)) {
             mphase ^= 1;
@@ -518,12 +549,22 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
             ok = false;
         }
         tc_fence_after();
+        if (tid == 0 && ok) {
+            load_v(sm, maps, cur.h, cur.tok0, full_v);
+            vpend = true;
+        }
         KDA_PHASE(0, 5);
         {
             const int quarter = warp & 3, j0 = 32 * (warp >> 2);
+            const bool second = quarter & 1;  // rows 32..63 of A or L
             float x[32];
-            tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + j0, x);
-            tmem_ld_wait();
+            if (second || j0 == 0) {
+                tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (second && j0 == 0 ? 64 : j0), x);
+                tmem_ld_wait();
+            } else {
+#pragma unroll
+                for (int t = 0; t < 32; ++t) x[t] = 0.0f;  // right of the diagonal
+            }
             if (quarter < 2) {
                 const int r = 32 * quarter + lane;
 #pragma unroll
@@ -673,8 +714,8 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
             }
         }
         KDA_PHASE(0, 8);
-        // the v tile (requested with q and k, or at the end of the previous
-        // item): rows past the sequence end are zeroed
+        // the v tile (requested after the A/L MMA): rows past the sequence
+        // end are zeroed
         if (mbar_wait(full_v, vphase)) {
             vphase ^= 1;
             vpend = false;
@@ -722,9 +763,6 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
             ok = false;
         }
         tc_fence_after();
-        // v is consumed: the next item's v load goes out
-        if (tid == 0 && has_next) load_v(sm, maps, nxt.h, nxt.tok0, full_v);
-        vpend = has_next;
         KDA_PHASE(0, 10);
 
         // 7. W rows and U: TMEM lanes 0..63 (warps of quarters 0, 1; warps

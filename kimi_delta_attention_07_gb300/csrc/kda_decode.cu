@@ -150,7 +150,10 @@ __global__ void __launch_bounds__(kDecodeThreads)
                                 const int32_t *__restrict__ state_indices,
                                 const int32_t *__restrict__ num_accepted, int64_t n_slots,
                                 T *__restrict__ o, int S, int H, int rows_per_cta, float scale) {
-    __shared__ float s_part[kWarps];  // epilogue: per-warp sums of o^2
+    // epilogue: per-warp sums of o^2 of token t in buffer t & 1, so that one
+    // barrier per token suffices (token t + 2 rewrites a buffer only after
+    // every warp has passed token t + 1's barrier, i.e. finished reading it)
+    __shared__ float s_part[2][kWarps];
     // GATED: the decay factors of token t in buffer t & 1, activated once per CTA
     // (16 channels per warp) at the end of token t - 1
     __shared__ __align__(16) float s_dec[2][kHeadDim];
@@ -291,15 +294,14 @@ __global__ void __launch_bounds__(kDecodeThreads)
         // top of token t - 1, before the barrier that ended it)
         if (GATED && t + 1 < S) activate(nxt, (t + 1) & 1);
         if (EPI) {  // rows_per_cta == 128: this CTA holds the head's whole output row
-            if (lane == 0) s_part[warp] = ss;
-            __syncthreads();
+            if (lane == 0) s_part[t & 1][warp] = ss;
+            __syncthreads();  // also publishes the next token's decays
             float tot = 0.0f;
 #pragma unroll
-            for (int w2 = 0; w2 < kWarps; ++w2) tot += s_part[w2];
+            for (int w2 = 0; w2 < kWarps; ++w2) tot += s_part[t & 1][w2];
             const float rn = 1.0f / sqrtf(tot * (1.0f / kHeadDim) + epi.eps);
             if (lane < rpw)
                 o[io_k + row0 + warp + kWarps * lane] = from_f32<T>(my_o * rn * w_o * gate_beta(gate_o));
-            __syncthreads();  // s_part is rewritten by the next token
         } else if (GATED && t + 1 < S) {
             __syncthreads();  // the next token's decays are in place
         }

@@ -210,13 +210,13 @@ def run_chunk_status(kda, x, **kw):
 
 
 # (g range, whether chunks go to the strong-decay prep, whether diagonal
-# blocks are computed from exact pairwise exponentials; None = either).  At
-# -2.45..-2.0 every chunk stays inside the main prep's factorised range
-# (|G_r - G_31| <= 32 * 2.45 = 78.4, right at its edge); at -5..-3 every
-# chunk leaves it; at -20..-5 every 16-token block leaves the strong-decay
-# prep's diagonal range too.
-STRONG = [((-2.45, -2.0), False, False), ((-3.0, -1.0), None, False),
-          ((-5.0, -3.0), True, None), ((-20.0, -5.0), True, True)]
+# blocks are computed from exact pairwise exponentials; None = either).  Up to
+# -5 per token every chunk stays inside the main prep's factorised range
+# (|G_r - G_m| <= 16 * 5 = 80 with m the reference row of r's 32-token half,
+# -4.9..-4.5 right at its edge); at -20..-5 every chunk leaves it, and every
+# 16-token block leaves the strong-decay prep's diagonal range too.
+STRONG = [((-3.0, -1.0), False, False), ((-4.9, -4.5), False, False),
+          ((-20.0, -5.0), True, True), ((-7.0, -5.5), True, None)]
 
 
 @pytest.mark.parametrize("scan", SCANS)
