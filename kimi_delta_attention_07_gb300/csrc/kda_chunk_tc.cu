@@ -304,7 +304,6 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
     uint32_t qkphase = 0, vphase = 0, mphase = 0;
     bool qkpend = true, vpend = false, mpend = false;
     bool ok = true;
-    KDA_PHASE_START();
     for (; item < n_items; item += gridDim.x) {
         const bool has_next = item + (int)gridDim.x < n_items;
         if (!has_next) griddep_launch_dependents();  // last item: the next kernel may be scheduled
@@ -342,14 +341,12 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
             }
             *reinterpret_cast<float4 *>(sQS + warp * D + d) = acc;
         }
-        KDA_PHASE(0, 0);
         if (mbar_wait(full_qk, qkphase)) {
             qkphase ^= 1;
             qkpend = false;
         } else {
             ok = false;
         }
-        KDA_PHASE(0, 1);
         // 2. row norms of q and k (raw tiles in the A operand's K-major
         //    layout): one (row, 64-channel half) per thread, two threads per row;
         //    step c reads the row's 16-byte unit c ^ (row % 8), so that eight
@@ -376,7 +373,6 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
             ok = false;  // uniform from here on: every thread takes the exit path
             break;
         }
-        KDA_PHASE(0, 2);
 
         // 3. per row of the slice, with the reference row m of its half
         //    (m = 15 for rows 0..31, 47 for rows 32..63; log2 units): G_r - G_m,
@@ -491,11 +487,9 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
                     make_uint2(pack2(col[0] * el[0], col[1] * el[1]), pack2(col[2] * el[2], col[3] * el[3]));
             }
         }
-        KDA_PHASE(0, 3);
         fence_async_smem();
         tc_fence_before();
         const bool defer = __syncthreads_or((int)wide) != 0;
-        KDA_PHASE(0, 4);
         float beta_nxt = 0.0f, alog_nxt = 0.0f;
         float4 bias_nxt = make_float4(0.f, 0.f, 0.f, 0.f);
         if (defer) {
@@ -553,7 +547,6 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
             load_v(sm, maps, cur.h, cur.tok0, full_v);
             vpend = true;
         }
-        KDA_PHASE(0, 5);
         {
             const int quarter = warp & 3, j0 = 32 * (warp >> 2);
             const bool second = quarter & 1;  // rows 32..63 of A or L
@@ -594,7 +587,6 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
             ok = false;  // uniform from here on: every thread takes the exit path
             break;
         }
-        KDA_PHASE(0, 6);
 
         // 5. X = (I + L)^-1 with L strictly lower (beta-scaled rows), in 16x16
         //    blocks, and T = X diag(beta) written straight into the bf16 hi + lo
@@ -657,7 +649,6 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
                 for (int r = 0; r < 16; ++r) dst[r * MS + c] = x[r];
             }
             __syncthreads();
-            KDA_PHASE(0, 7);
             for (int s = tid; s < 576; s += kPrepThreads) {  // warp-uniform slot ranges
                 const int ii = (s >> 2) & 15, c4 = s & 3;
                 if (s < 192) {  // X_{q+1,q} = -M_{q+1,q} X_qq
@@ -713,7 +704,6 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
                 }
             }
         }
-        KDA_PHASE(0, 8);
         // the v tile (requested after the A/L MMA): rows past the sequence
         // end are zeroed
         if (mbar_wait(full_v, vphase)) {
@@ -755,7 +745,6 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
                 alog_nxt = gate.a_log[nxt.h];
             }
         }
-        KDA_PHASE(0, 9);
         if (mbar_wait(mbar, mphase)) {
             mphase ^= 1;
             mpend = false;
@@ -763,7 +752,6 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
             ok = false;
         }
         tc_fence_after();
-        KDA_PHASE(0, 10);
 
         // 7. W rows and U: TMEM lanes 0..63 (warps of quarters 0, 1; warps
         //    0, 1 take W, warps 4, 5 take U) -> shared memory in the record's
@@ -805,7 +793,6 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
             bulk_commit();
         }
         }
-        KDA_PHASE(0, 11);
         cur = nxt;
         if (item + 2 * (int)gridDim.x < n_items) nxt = *sNext;
         beta_cur = beta_nxt;
@@ -824,7 +811,6 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
         }
         __syncthreads();
     }
-    KDA_PHASE_FLUSH(0);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
@@ -959,7 +945,6 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     if (tid == kIssuer)
         for (int ck = 0; ck < kStages - 1 && ck < nck; ++ck, ++loads_issued) issue(ck);
     bool ok = true;
-    KDA_PHASE_START();
     for (int ck = 0; ck < nck; ++ck) {
         const uint32_t fpar = (uint32_t)((ck / kStages) & 1), cpar = (uint32_t)(ck & 1);
         unsigned char *st = stage_of(ck);
@@ -982,11 +967,9 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 }
             }
         } else if (warp < 2) {
-            KDA_PHASE(1, 0);
             ok = mbar_wait(&full[ck % kStages], fpar) && ok;  // U of this stage
             ok = mbar_wait(bar_ws, cpar) && ok;
             tc_fence_after();
-            KDA_PHASE(1, 1);
             float x[32], u[32];  // Vn = U - W S, row tid
             tmem_ld32(tD1 + lane_base, x);
             const uint4 *up = reinterpret_cast<const uint4 *>(st + kImageBytes + tid * 64);
@@ -1003,7 +986,6 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             store_row_n32(sVn, tid, x);
             fence_async_smem();
             tc_fence_before();
-            KDA_PHASE(1, 2);
         } else if (warp < 4) {
             ok = mbar_wait(&full[ck % kStages], fpar) && ok;  // gC of this stage
             if (ck > 0) {
@@ -1024,10 +1006,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             mma_tile_n32<128, 64, 128>(tD1, smem_u32(st + TcRec::A) - 8192, smem_u32(sVn), true);
             mma_commit(bar_out);
         } else if (warp < 4) {
-            KDA_PHASE(1, 3);
             ok = mbar_wait(bar_d3, cpar) && ok;
             tc_fence_after();
-            KDA_PHASE(1, 4);
             float x[32];  // S = diag(gC) S + KD^T Vn
             tmem_ld32(tD3 + lane_base, x);
             const float gc = reinterpret_cast<const float *>(st + TcRec::GC)[tid];
@@ -1037,13 +1017,11 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             store_row_n32(sS, tid, S);
             fence_async_smem();
             tc_fence_before();
-            KDA_PHASE(1, 5);
         }
         if (!named_bar_and(kBarS, kScanThreads, ok)) {
             ok = false;
             break;
         }
-        KDA_PHASE(1, 6);
     }
     if (ok && nck > 0 && (warp == 2 || warp == 3)) {
         ok = mbar_wait(bar_out, (uint32_t)((nck - 1) & 1));
@@ -1065,7 +1043,6 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 #pragma unroll
         for (int x = 0; x < BV; ++x) final_state[st_off + (int64_t)(v0 + x) * D + tid] = S[x];
     }
-    KDA_PHASE_FLUSH(1);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kScanTmemCols);
@@ -1360,13 +1337,3 @@ cudaError_t launch_chunk_scan_tc(const float *initial_state, float *final_state,
 }
 
 }  // namespace kda
-
-#ifdef KDA_PHASE_TRACE
-extern "C" int kda_phase_read(unsigned long long *out) {
-    return (int)cudaMemcpyFromSymbol(out, kda_phase_cycles, sizeof(unsigned long long) * 64);
-}
-extern "C" int kda_phase_reset() {
-    unsigned long long z[64] = {0};
-    return (int)cudaMemcpyToSymbol(kda_phase_cycles, z, sizeof(z));
-}
-#endif

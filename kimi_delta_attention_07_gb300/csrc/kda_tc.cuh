@@ -6,38 +6,6 @@
 
 #include <stdint.h>
 
-// Phase markers for cycle accounting: cycles between markers accumulate in
-// registers and the first CTA's thread 0 adds them to a device array at the
-// end.  They compile to nothing unless KDA_PHASE_TRACE is defined (this
-// header is then included by a single translation unit, which owns it).
-#ifdef KDA_PHASE_TRACE
-__device__ unsigned long long kda_phase_cycles[2][32];
-#define KDA_PHASE_START()                 \
-    long long kda_tprev_ = clock64();     \
-    unsigned long long kda_acc_[16] = {0}
-#define KDA_PHASE(kind, idx)                                   \
-    do {                                                       \
-        const long long t_ = clock64();                        \
-        kda_acc_[idx] += (unsigned long long)(t_ - kda_tprev_); \
-        kda_tprev_ = t_;                                       \
-    } while (0)
-#define KDA_PHASE_FLUSH(kind)                                                              \
-    do {                                                                                   \
-        if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0)     \
-            for (int i_ = 0; i_ < 16; ++i_) kda_phase_cycles[kind][i_] += kda_acc_[i_];   \
-    } while (0)
-#else
-#define KDA_PHASE_START() \
-    do {                  \
-    } while (0)
-#define KDA_PHASE(kind, idx) \
-    do {                     \
-    } while (0)
-#define KDA_PHASE_FLUSH(kind) \
-    do {                      \
-    } while (0)
-#endif
-
 namespace kda {
 namespace tc {
 
