@@ -69,11 +69,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 // half) the factorised exponentials take: both factors stay inside fp32 /
 // bf16 range.  Chunks beyond it are deferred to the strong-decay prep.
 constexpr float kRelLimit2 = 80.0f * kLog2e;
-constexpr int NCOL = 96;  // B operand rows of the A/L MMA: 32 per (column half, reference)
+constexpr int NCOL = 96;  // column-operand rows of the A/L MMA: 32 per (column half, reference)
 // shared memory plan (offsets from a 1024-aligned base)
 constexpr int P_XL = 0;             // 32 KB: raw [q ; k] (TMA) -> [q_hat x ; k_hat x]
-constexpr int P_COLH = 32768;       // 24 KB: the column operand, hi part (B operand of A/L)
-constexpr int P_COLL = 57344;       // 24 KB: its lo part
+constexpr int P_COL = 32768;        // 48 KB: B operand of the A/L MMA, 2 NCOL rows: the
+                                    // column operand's hi part (rows 0..95), then its lo part
 constexpr int P_E = 81920;          // 16 KB: E = k_hat exp(G), MN-major [j][d]
 constexpr int P_RQ = 98304;         // fp32 [64]: scale / |q_r|
 constexpr int P_RK = P_RQ + 256;    // fp32 [64]: 1 / |k_r|
@@ -95,7 +95,7 @@ static_assert(P_SMEM * kPrepMinBlocks + 2048 <= 233472, "two prep CTAs per SM");
 static_assert(P_L + C * LSTRIDE * 4 <= P_SCR && P_SCR + 14 * MBLK * 4 <= P_T, "L, scratch, T");
 static_assert(P_T + 16384 <= P_V && P_V + 16384 <= P_E && P_STAGE + 32768 <= P_E,
               "T, v and staging below E");
-static_assert(P_COLL + NCOL * 256 <= P_E, "column operand");
+static_assert(P_COL + 2 * NCOL * 256 <= P_E, "column operand");
 
 struct PrepItem {
     int64_t tok0;
@@ -420,11 +420,11 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
             // thread bases: XL (K-major, 128 rows), the column operand (96 rows),
             // 64-row tiles (E, KD), QG rows of WQ
             unsigned char *xl = sXL + kb * 16384 + r0 * 128 + hb;
-            unsigned char *cop = sm + P_COLH + kb * (NCOL * 128) + r0 * 128 + hb;
+            unsigned char *cop = sm + P_COL + kb * (2 * NCOL * 128) + r0 * 128 + hb;
             unsigned char *e64 = sE + kb * 8192 + r0 * 128 + hb;
             unsigned char *qg = rec + TcRec::WQ + kb * 16384 + (C + r0) * 128 + hb;
             unsigned char *kd = rec + TcRec::KD + kb * 8192 + r0 * 128 + hb;
-            constexpr int kLo = P_COLL - P_COLH;
+            constexpr int kLo = NCOL * 128;  // the lo part's rows follow the hi part's
             // hi + lo bf16 parts of four column values at byte offset `at`
             auto put_col = [&](int at, const float (&c)[4]) {
                 const uint2 hi = make_uint2(pack2(c[0], c[1]), pack2(c[2], c[3]));
@@ -518,8 +518,8 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
         } else {
         if (tid == 0) {
             tc_fence_after();
-            mma_tile<128, NCOL, 128, 128, NCOL>(tmem, smem_u32(sXL), smem_u32(sm + P_COLH), false);
-            mma_tile<128, NCOL, 128, 128, NCOL>(tmem, smem_u32(sXL), smem_u32(sm + P_COLL), true);
+            // hi and lo parts side by side in N: TMEM columns 0..95 and 96..191
+            mma_tile<128, 2 * NCOL, 128, 128, 2 * NCOL>(tmem, smem_u32(sXL), smem_u32(sm + P_COL), false);
             mma_commit(mbar);
         }
         mpend = true;
@@ -533,8 +533,9 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
         //    0..63 hold A's rows, 64..127 L's; warp w reads the 32 lanes of
         //    quarter w % 4 for output columns j0 = 32 (w / 4) .. +31, which a
         //    row of the first half finds at TMEM columns j (j < 32), a row of
-        //    the second half at 64 + j (j < 32) and at j (j >= 32).  The v tile
-        //    goes out as soon as the column operand has been read.
+        //    the second half at 64 + j (j < 32) and at j (j >= 32); the lo
+        //    part's products sit NCOL columns further and are added.  The v
+        //    tile goes out as soon as the column operand has been read.
         float *sL = reinterpret_cast<float *>(sm + P_L);
         if (mbar_wait(mbar, mphase)) {
             mphase ^= 1;
@@ -552,8 +553,13 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
             const bool second = quarter & 1;  // rows 32..63 of A or L
             float x[32];
             if (second || j0 == 0) {
-                tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (second && j0 == 0 ? 64 : j0), x);
+                const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16) + (second && j0 == 0 ? 64 : j0);
+                float xl[32];
+                tmem_ld32(ta, x);
+                tmem_ld32(ta + NCOL, xl);
                 tmem_ld_wait();
+#pragma unroll
+                for (int t = 0; t < 32; ++t) x[t] += xl[t];
             } else {
 #pragma unroll
                 for (int t = 0; t < 32; ++t) x[t] = 0.0f;  // right of the diagonal
