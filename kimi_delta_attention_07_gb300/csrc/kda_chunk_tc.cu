@@ -842,7 +842,10 @@ constexpr int S_SMEM = S_BYTES + 1024;
 static_assert(kStageBytes <= (uint32_t)S_STAGE, "stage too small");
 static_assert(kImageBytes % 16 == 0 && TcRec::UBLK % 16 == 0, "bulk copy size");
 static_assert(8 * (kStages + 4) + 4 <= 64, "scan barrier block");
-constexpr uint32_t kBarS = 1, kBarV = 2;  // named barriers (160 threads): S operand ready, Vn ready
+// named barriers: S operand ready (every warp), Vn ready (the Vn warps and the
+// issuer only: the output warps store the previous chunk's rows meanwhile and are
+// held by the next "S ready" instead)
+constexpr uint32_t kBarS = 1, kBarV = 2;
 
 // This thread's 32 values x[v] as row k of an N = 32 operand (MN-major,
 // 64-byte swizzle, see sw64_off): four 16-byte stores, conflict-free across
@@ -1001,17 +1004,18 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             }
             tc_fence_before();
         }
-        if (!named_bar_and(kBarV, kScanThreads, ok)) {
-            ok = false;
-            break;
-        }
+        // (a failure seen here is carried to the "S ready" barrier below, which
+        // every warp reaches; the output warps' D3 wait then gives up on its own)
+        if (warp < 2 || warp == 4) ok = named_bar_and(kBarV, 96, ok);
         if (tid == kIssuer) {
             tc_fence_after();
-            mma_tile_n32<128, 64, 64, true>(tD3, smem_u32(st + TcRec::KD), smem_u32(sVn), false);
-            mma_commit(bar_d3);
-            mma_tile_n32<128, 64, 128>(tD1, smem_u32(st + TcRec::A) - 8192, smem_u32(sVn), true);
-            mma_commit(bar_out);
-        } else if (warp < 4) {
+            if (ok) {
+                mma_tile_n32<128, 64, 64, true>(tD3, smem_u32(st + TcRec::KD), smem_u32(sVn), false);
+                mma_commit(bar_d3);
+                mma_tile_n32<128, 64, 128>(tD1, smem_u32(st + TcRec::A) - 8192, smem_u32(sVn), true);
+                mma_commit(bar_out);
+            }
+        } else if (warp < 4 && ok) {
             ok = mbar_wait(bar_d3, cpar) && ok;
             tc_fence_after();
             float x[32];  // S = diag(gC) S + KD^T Vn
@@ -1228,17 +1232,18 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             }
             tc_fence_before();
         }
-        if (!named_bar_and(kBarV, kWideThreads, ok)) {
-            ok = false;
-            break;
-        }
+        // (a failure seen here is carried to the "S ready" barrier below, which
+        // every warp reaches; the output warps' D3 wait then gives up on its own)
+        if (q < 2 || warp == 8) ok = named_bar_and(kBarV, 160, ok);
         if (tid == kWideIssuer) {
             tc_fence_after();
-            mma_tile<128, 128, 64, 64, 64, true, true>(tD3, smem_u32(st + TcRec::KD), smem_u32(sVn), false);
-            mma_commit(bar_d3);
-            mma_tile<128, 128, 64, 128, 64, false, true>(tD1, smem_u32(st + TcRec::A) - 8192, smem_u32(sVn), true);
-            mma_commit(bar_out);
-        } else if (warp < 8) {
+            if (ok) {
+                mma_tile<128, 128, 64, 64, 64, true, true>(tD3, smem_u32(st + TcRec::KD), smem_u32(sVn), false);
+                mma_commit(bar_d3);
+                mma_tile<128, 128, 64, 128, 64, false, true>(tD1, smem_u32(st + TcRec::A) - 8192, smem_u32(sVn), true);
+                mma_commit(bar_out);
+            }
+        } else if (warp < 8 && ok) {
             ok = mbar_wait(bar_d3, cpar) && ok;
             tc_fence_after();
             const float gc = reinterpret_cast<const float *>(st + TcRec::GC)[d];
