@@ -84,16 +84,19 @@ constexpr int P_BYTES = P_BAR + 128;
 constexpr int P_SMEM = P_BYTES + 1024;
 // reuse of [0, 64 KB) once the A/L MMA has read its operands
 constexpr int P_L = 0;              // fp32 [64][LSTRIDE]: beta-scaled L
-constexpr int P_SCR = 17408;        // inverse scratch: 14 16x16 fp32 blocks
-constexpr int P_T = 36864;          // T operand, hi (8 KB) and lo (8 KB)
-constexpr int P_V = 53248;          // 16 KB: v, MN-major (two 64-column boxes), loaded after A/L
+constexpr int P_SCR = 17408;        // inverse scratch: X_aa and M_ab (10 16x16 fp32 blocks);
+                                    // C30, C31, X_10, X_21 reuse L's space once L is consumed
+constexpr int P_T = 32768;          // T operand: [T_hi ; T_hi] then [T_lo ; T_lo], 16 KB each
+constexpr int P_V = 65536;          // 16 KB: v, MN-major (two 64-column boxes), loaded after A/L
 constexpr int P_STAGE = 32768;      // W and U staged for the record after the W/U MMA
 constexpr int LSTRIDE = 68;         // row stride (floats) of L in shared memory
 constexpr int MS = 20;              // row stride (floats) of 16x16 scratch matrices
 constexpr int MBLK = 16 * MS;       // floats per 16x16 scratch matrix
 static_assert(P_SMEM * kPrepMinBlocks + 2048 <= 233472, "two prep CTAs per SM");
-static_assert(P_L + C * LSTRIDE * 4 <= P_SCR && P_SCR + 14 * MBLK * 4 <= P_T, "L, scratch, T");
-static_assert(P_T + 16384 <= P_V && P_V + 16384 <= P_E && P_STAGE + 32768 <= P_E,
+static_assert(P_L + C * LSTRIDE * 4 <= P_SCR && P_SCR + 10 * MBLK * 4 <= P_XL + 32768 &&
+                  4 * MBLK * 4 <= C * LSTRIDE * 4,
+              "L and inverse scratch inside the q/k region");
+static_assert(P_T + 32768 <= P_V && P_V + 16384 <= P_E && P_STAGE + 32768 <= P_E,
               "T, v and staging below E");
 static_assert(P_COL + 2 * NCOL * 256 <= P_E, "column operand");
 
@@ -242,7 +245,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
     unsigned char *sm = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     unsigned char *sXL = sm + P_XL;
     unsigned char *sE = sm + P_E;
-    unsigned char *sT = sm + P_T;  // T_hi; T_lo follows 8 KB later
+    unsigned char *sT = sm + P_T;  // [T_hi ; T_hi], then [T_lo ; T_lo] 16 KB later
     float *sRq = reinterpret_cast<float *>(sm + P_RQ);
     float *sRk = reinterpret_cast<float *>(sm + P_RK);
     float *sB = reinterpret_cast<float *>(sm + P_BETA);
@@ -612,7 +615,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
             const float *cL = sL;
             float *XD = reinterpret_cast<float *>(sm + P_SCR);  // X_aa, a = 0..3
             float *Mb = XD + 4 * MBLK;                         // M_ab, pairs p = 0..5
-            float *Cb = Mb + 6 * MBLK;                         // C30, C31
+            float *Cb = reinterpret_cast<float *>(sm + P_L);  // C30, C31 (stage B on: L is consumed)
             float *Xo = Cb + 2 * MBLK;                         // X_10, X_21
             // Block pairs (a, b), a > b, index p: (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
             auto pair_a = [](int p_) { return p_ < 1 ? 1 : (p_ < 3 ? 2 : 3); };
@@ -624,9 +627,14 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
                 const uint32_t h01 = pack2(y0, y1), h23 = pack2(y2, y3);
                 const float2 f01 = unpack2(h01), f23 = unpack2(h23);
                 const uint32_t off = sw128_off(row, col, 64);
-                *reinterpret_cast<uint2 *>(sT + off) = make_uint2(h01, h23);
-                *reinterpret_cast<uint2 *>(sT + 8192 + off) =
-                    make_uint2(pack2(y0 - f01.x, y1 - f01.y), pack2(y2 - f23.x, y3 - f23.y));
+                const uint2 hi = make_uint2(h01, h23);
+                const uint2 lo = make_uint2(pack2(y0 - f01.x, y1 - f01.y), pack2(y2 - f23.x, y3 - f23.y));
+                // rows 64..127 repeat rows 0..63, so that W and U land in both
+                // halves of TMEM and all eight warps share their readout
+                *reinterpret_cast<uint2 *>(sT + off) = hi;
+                *reinterpret_cast<uint2 *>(sT + 8192 + off) = hi;
+                *reinterpret_cast<uint2 *>(sT + 16384 + off) = lo;
+                *reinterpret_cast<uint2 *>(sT + 24576 + off) = lo;
             };
             if (warp < 5) {
                 const int sl = 32 * warp + lane;
@@ -705,8 +713,9 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
                     const int pz = sl >> 6, i = (sl >> 2) & 15, h = (sl >> 1) & 1, hl = sl & 1;
                     const int a = pz < 3 ? 0 : (pz < 5 ? 1 : 2);
                     const int b = pz < 3 ? pz + 1 : (pz < 5 ? pz - 1 : 3);
-                    *reinterpret_cast<uint4 *>(sT + hl * 8192 + sw128_off(16 * a + i, 16 * b + 8 * h, 64)) =
-                        make_uint4(0, 0, 0, 0);
+                    unsigned char *z = sT + hl * 16384 + sw128_off(16 * a + i, 16 * b + 8 * h, 64);
+                    *reinterpret_cast<uint4 *>(z) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(z + 8192) = make_uint4(0, 0, 0, 0);
                 }
             }
         }
@@ -735,9 +744,9 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
         if (tid == 0) {
             tc_fence_after();
             mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 0, smem_u32(sT), smem_u32(sE), false);
-            mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 0, smem_u32(sT + 8192), smem_u32(sE), true);
+            mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 0, smem_u32(sT + 16384), smem_u32(sE), true);
             mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 128, smem_u32(sT), smem_u32(sm + P_V), false);
-            mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 128, smem_u32(sT + 8192), smem_u32(sm + P_V), true);
+            mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 128, smem_u32(sT + 16384), smem_u32(sm + P_V), true);
             mma_commit(mbar);
             if (has_next) load_qk(sm, maps, nxt.h, nxt.tok0, full_qk);
         }
@@ -759,29 +768,32 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
         }
         tc_fence_after();
 
-        // 7. W rows and U: TMEM lanes 0..63 (warps of quarters 0, 1; warps
-        //    0, 1 take W, warps 4, 5 take U) -> shared memory in the record's
-        //    own layout -> three bulk copies to the record.  U rows are stored
-        //    with their 16-byte chunks rotated (chunk c of row i at
-        //    c ^ ((i / 2) % 4)), which keeps these writes and the scan's reads
-        //    free of bank conflicts.
+        // 7. W and U rows (TMEM lanes 0..63, repeated in lanes 64..127): warp
+        //    w reads lane quarter w % 4, i.e. rows 32 (w % 2) .. +31, columns
+        //    64 ((w % 4) / 2) .. +63 of W (w < 4) or U (w >= 4) -> shared
+        //    memory in the record's own layout -> three bulk copies to the
+        //    record.  U rows are stored with their 16-byte chunks rotated
+        //    (chunk c of row i at c ^ ((i / 2) % 4)), which keeps these writes
+        //    and the scan's reads free of bank conflicts.
         unsigned char *stg = sm + P_STAGE;
-        if ((warp & 3) < 2) {
-            const int i = 32 * (warp & 3) + lane, part = warp >> 2;
-            const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 128 * part;
+        {
+            const int quarter = warp & 3, part = warp >> 2;
+            const int i = 32 * (quarter & 1) + lane, c0 = 64 * (quarter >> 1);
+            const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16) + 128 * part + c0;
 #pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
+            for (int cb = 0; cb < 2; ++cb) {
                 float x[32];
                 tmem_ld32(ta + 32 * cb, x);
                 tmem_ld_wait();
+                const int col = c0 + 32 * cb;
 #pragma unroll
                 for (int c8 = 0; c8 < 4; ++c8) {
                     float y[8];
 #pragma unroll
                     for (int t = 0; t < 8; ++t) y[t] = x[8 * c8 + t];
                     unsigned char *dst = part == 0
-                        ? stg + sw128_off(i, 32 * cb + 8 * c8, 64)
-                        : stg + 16384 + cb * TcRec::UBLK + i * 64 + ((c8 ^ ((i >> 1) & 3)) << 4);
+                        ? stg + sw128_off(i, col + 8 * c8, 64)
+                        : stg + 16384 + (col >> 5) * TcRec::UBLK + i * 64 + ((c8 ^ ((i >> 1) & 3)) << 4);
                     *reinterpret_cast<uint4 *>(dst) = pack8(y);
                 }
             }

@@ -28,20 +28,34 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *p, float4 x
 }
 
 template <typename T>
+__device__ __forceinline__ float4 gated_row(float4 x, float4 gt, float4 w, float eps) {
+    const float ms = warp_sum(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w) * (1.0f / kHeadDim);
+    const float rn = 1.0f / sqrtf(ms + eps);
+    return make_float4(x.x * rn * w.x * gate_beta(gt.x), x.y * rn * w.y * gate_beta(gt.y),
+                       x.z * rn * w.z * gate_beta(gt.z), x.w * rn * w.w * gate_beta(gt.w));
+}
+
+// One warp per row; a warp takes two rows (r and r + warps) per step and
+// issues all four loads before the first store, so that two rows of each
+// warp are in flight.  The grid is the resident one (a grid-stride loop).
+template <typename T>
 __global__ void __launch_bounds__(kEpiThreads)
     output_gate_norm_kernel(T *__restrict__ o, const EpiArgs epi, int64_t rows) {
     const int lane = threadIdx.x & 31;
     const float4 w = *reinterpret_cast<const float4 *>(epi.weight + 4 * lane);
-    const T *gate = reinterpret_cast<const T *>(epi.out_gate);
+    const T *__restrict__ gate = reinterpret_cast<const T *>(epi.out_gate);
     const int64_t warps = (int64_t)gridDim.x * (kEpiThreads / 32);
-    for (int64_t r = blockIdx.x * (int64_t)(kEpiThreads / 32) + (threadIdx.x >> 5); r < rows; r += warps) {
+    int64_t r = blockIdx.x * (int64_t)(kEpiThreads / 32) + (threadIdx.x >> 5);
+    for (; r + warps < rows; r += 2 * warps) {
+        const int64_t e0 = r * kHeadDim + 4 * lane, e1 = e0 + warps * kHeadDim;
+        const float4 x0 = load4(o + e0), g0 = load4(gate + e0);
+        const float4 x1 = load4(o + e1), g1 = load4(gate + e1);
+        store4(o + e0, gated_row<T>(x0, g0, w, epi.eps));
+        store4(o + e1, gated_row<T>(x1, g1, w, epi.eps));
+    }
+    if (r < rows) {
         const int64_t e = r * kHeadDim + 4 * lane;
-        const float4 x = load4(o + e);
-        const float4 gt = load4(gate + e);
-        const float ms = warp_sum(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w) * (1.0f / kHeadDim);
-        const float rn = 1.0f / sqrtf(ms + epi.eps);
-        store4(o + e, make_float4(x.x * rn * w.x * gate_beta(gt.x), x.y * rn * w.y * gate_beta(gt.y),
-                                  x.z * rn * w.z * gate_beta(gt.z), x.w * rn * w.w * gate_beta(gt.w)));
+        store4(o + e, gated_row<T>(load4(o + e), load4(gate + e), w, epi.eps));
     }
 }
 
@@ -51,12 +65,24 @@ cudaError_t launch_output_gate_norm(void *o, const EpiArgs &epi, int64_t rows, i
                                     cudaStream_t stream) {
     if (rows == 0) return cudaSuccess;
     const int64_t blocks = (rows + (kEpiThreads / 32) - 1) / (kEpiThreads / 32);
-    const int grid = (int)std::min<int64_t>(blocks, 152 * 16);
-    if (dtype == KDA_BF16)
-        output_gate_norm_kernel<__nv_bfloat16><<<grid, kEpiThreads, 0, stream>>>(
-            (__nv_bfloat16 *)o, epi, rows);
-    else
-        output_gate_norm_kernel<float><<<grid, kEpiThreads, 0, stream>>>((float *)o, epi, rows);
+    // one wave of resident blocks, so that no block waits for a second wave
+    auto one_wave = [&](auto kernel) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kEpiThreads, 0) !=
+                cudaSuccess ||
+            per_sm < 1) {
+            cudaGetLastError();
+            per_sm = 1;
+        }
+        return (int)std::min<int64_t>(blocks, (int64_t)sm_count() * per_sm);
+    };
+    if (dtype == KDA_BF16) {
+        auto kern = output_gate_norm_kernel<__nv_bfloat16>;
+        kern<<<one_wave(kern), kEpiThreads, 0, stream>>>((__nv_bfloat16 *)o, epi, rows);
+    } else {
+        auto kern = output_gate_norm_kernel<float>;
+        kern<<<one_wave(kern), kEpiThreads, 0, stream>>>((float *)o, epi, rows);
+    }
     return cudaGetLastError();
 }
 
