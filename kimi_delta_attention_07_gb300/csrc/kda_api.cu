@@ -145,12 +145,13 @@ int chunk_call(int phase, const void *q, const void *k, const void *v, const flo
                    : launch_chunk_prep_f32(q, k, v, g, beta, dtype, n_seqs, total_tokens, H,
                                            scale, workspace, s);
     }
+    bool epi_applied = false;
     if (e == cudaSuccess && (phase & kScan))
         e = tc ? launch_chunk_scan_tc(initial_state, final_state, state_indices, o, n_seqs,
-                                      total_tokens, H, flags, workspace, s)
+                                      total_tokens, H, flags, epi, &epi_applied, workspace, s)
                : launch_chunk_scan_f32(initial_state, final_state, state_indices, o, dtype,
                                        n_seqs, total_tokens, H, workspace, s);
-    if (e == cudaSuccess && (phase & kScan) && epi && epi->out_gate)
+    if (e == cudaSuccess && (phase & kScan) && epi && epi->out_gate && !epi_applied)
         e = launch_output_gate_norm(o, *epi, total_tokens * H, dtype, s);
     if (e != cudaSuccess) {
         cudaGetLastError();

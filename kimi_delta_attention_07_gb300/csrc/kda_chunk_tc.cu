@@ -262,6 +262,12 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
     int32_t *status = ws_at<int32_t>(workspace, L.status_off);
     int32_t *defer_count = ws_at<int32_t>(workspace, L.defer_count_off);
     int32_t *defer_list = ws_at<int32_t>(workspace, L.defer_off);
+    {  // clear the scan's row-sum exchange ring (its tags) for this call
+        uint4 *ring = ws_at<uint4>(workspace, L.epi_part_off);
+        const int n16 = min(n_seqs * H, kEpiPairs) * kEpiRing * 4 * C / 2;
+        for (int i = blockIdx.x * kPrepThreads + threadIdx.x; i < n16; i += gridDim.x * kPrepThreads)
+            ring[i] = make_uint4(0, 0, 0, 0);
+    }
     const int n_items = chunk_off[n_seqs] * H;
     if ((int)blockIdx.x >= n_items) return;
 
@@ -848,12 +854,12 @@ constexpr uint32_t kStageBytes = kImageBytes + TcRec::UBLK;  // + this CTA's U b
 constexpr int S_STAGE = 62464;                               // kStageBytes rounded up to 1024
 constexpr int S_SOP = kStages * S_STAGE;                     // S operand [128 keys][32] bf16, 8 KB
 constexpr int S_VOP = S_SOP + 8192;                          // Vn operand [64 rows][32] bf16, 4 KB
-constexpr int S_BAR = S_VOP + 4096;                          // full[kStages], ws, d3, out, drain, tmem slot
-constexpr int S_BYTES = S_BAR + 64;
+constexpr int S_BAR = S_VOP + 4096;                          // mbarriers, tmem slot
+constexpr int S_BYTES = S_BAR + 128;
 constexpr int S_SMEM = S_BYTES + 1024;
 static_assert(kStageBytes <= (uint32_t)S_STAGE, "stage too small");
 static_assert(kImageBytes % 16 == 0 && TcRec::UBLK % 16 == 0, "bulk copy size");
-static_assert(8 * (kStages + 4) + 4 <= 64, "scan barrier block");
+static_assert(8 * (kStages + 4) + 4 <= 128, "scan barrier block");
 // named barriers: S operand ready (every warp), Vn ready (the Vn warps and the
 // issuer only: the output warps store the previous chunk's rows meanwhile and are
 // held by the next "S ready" instead)
@@ -1068,6 +1074,391 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kScanTmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// split scan with the output epilogue
+//   o <- o / sqrt(mean(o^2) + eps) * weight * sigmoid(gate)   per 128-value row
+// The chain of warps 0-4 is the one above; the output rows leave through two
+// warps of their own (6 and 7: TMEM lane quarters 2 and 3, rows 64..127 of
+// D1), which trail the chain by up to three chunks: D1 has four buffers, and
+// the issuer reuses one only after they have read it.  The four CTAs of a
+// (sequence, head) hold 32 values of a row each.  Every output thread
+// publishes its row's sum of squares as one tagged word (tag = chunk + 1 in
+// the low half, the fp32 sum in the high half, written and read whole) in a
+// ring in the workspace that the prep clears.  Warp 5 collects the four CTAs'
+// words of each row (polling two chunks at a time, so that the L2 round trip
+// stays off the output warps) and hands the row totals to the output warps
+// through shared memory.  Output step c publishes chunk c and finishes chunk
+// c - 1 with warp 5's totals.  So a thread publishes chunk c + 2 only after
+// its CTA has finished chunk c, i.e. after every CTA has published chunk c,
+// which each does only after finishing chunk c - 2, i.e. after its warp 5 has
+// read chunk c - 2's words: in a ring of 4 slots chunk c + 2 takes chunk
+// c - 2's slot once nobody reads it any more.  The grid is launched
+// cooperatively, so that the four are resident together.
+constexpr int kEpiScanThreads = 256;  // warps 0-4 as above; warp 5 row-sum exchange; warps 6-7 output rows
+constexpr int kOutWarp0 = 6;
+constexpr int kD1Bufs = 4;
+constexpr uint32_t kEpiTmemCols = 256;  // D1 (4 x 32 columns), D3 (32)
+static_assert(32 * kD1Bufs + BV <= (int)kEpiTmemCols, "scan TMEM columns");
+static_assert(kEpiRing == 4, "the ring argument above needs four slots");
+constexpr int kTotSlots = 4;                        // row totals handed from warp 5 to the output warps
+constexpr int E_BAR_BYTES = 256;                    // mbarriers and the TMEM slot
+static_assert(8 * (kStages + 3 + 2 * kD1Bufs + 2 * kTotSlots) + 4 <= E_BAR_BYTES, "epilogue scan barrier block");
+constexpr int kGateSlots = 4;                       // gate rows prefetched two chunks ahead
+constexpr int S_GATE = S_BAR + E_BAR_BYTES;         // [kGateSlots][64 rows][64 B] bf16
+constexpr int S_TOT = S_GATE + kGateSlots * C * 64;  // fp32 [kTotSlots][64 rows]
+constexpr int S_EPI_SMEM = S_TOT + kTotSlots * C * 4 + 1024;
+static_assert(S_EPI_SMEM <= 232448, "epilogue scan shared memory");
+
+// 16-byte copy global -> shared that completes asynchronously (commit groups)
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_gpu_u64(uint64_t *p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_relaxed_gpu_u64(const uint64_t *p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__global__ void __launch_bounds__(kEpiScanThreads, 1)
+    chunk_scan_tc_epi_kernel(const float *__restrict__ initial_state, float *__restrict__ final_state,
+                             const int32_t *__restrict__ state_indices, __nv_bfloat16 *__restrict__ o,
+                             int n_seqs, int H, void *workspace, WsLayout L, EpiArgs epi) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char *sS = sm + S_SOP;
+    unsigned char *sVn = sm + S_VOP;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + S_BAR);
+    uint64_t *bar_ws = full + kStages;          // D1 = WQ S done
+    uint64_t *bar_d3 = bar_ws + 1;              // D3 = KD^T Vn done
+    uint64_t *bar_out = bar_d3 + 1;             // [kD1Bufs] D1 += A Vn done: the chunk's output rows
+    uint64_t *bar_free = bar_out + kD1Bufs;     // [kD1Bufs] the output warps have read D1
+    uint64_t *tot_full = bar_free + kD1Bufs;     // [kTotSlots] warp 5 has written a chunk's row totals
+    uint64_t *tot_empty = tot_full + kTotSlots;  // [kTotSlots] the output warps have read them
+    uint64_t *bar_drain = tot_empty + kTotSlots;  // exit path: every MMA issued so far is done
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_drain + 1);
+    float *sTot = reinterpret_cast<float *>(sm + S_TOT);
+    griddep_wait();  // the records (previous kernel) are complete
+
+    const int n = blockIdx.x, h = blockIdx.y, vb = blockIdx.z, v0 = vb * BV;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t start = ws_at<const int32_t>(workspace, L.seq_start_off)[n];
+    if (start < 0) return;  // sequence skipped (bad cu_seqlens or slot)
+    const int len = ws_at<const int32_t>(workspace, L.seq_len_off)[n];
+    const int c0 = ws_at<const int32_t>(workspace, L.chunk_off_off)[n];
+    const int nck = (len + C - 1) / C;
+    const int64_t slot = state_indices ? (int64_t)state_indices[n] : (int64_t)n;
+    const int64_t st_off = (slot * H + h) * (int64_t)D * D;  // [V][K] block of (slot, h)
+    int32_t *status = ws_at<int32_t>(workspace, L.status_off);
+    const unsigned char *recs = ws_at<const unsigned char>(workspace, L.records_off);
+    auto rec_of = [&](int ck) { return recs + ((size_t)(c0 + ck) * H + h) * TcRec::bytes; };
+    auto stage_of = [&](int ck) { return sm + (ck % kStages) * S_STAGE; };
+    auto issue = [&](int ck) {  // the issuing thread
+        unsigned char *dst = stage_of(ck);
+        uint64_t *b = &full[ck % kStages];
+        mbar_arrive_expect_tx(b, kStageBytes);
+        bulk_g2s(dst, rec_of(ck), kImageBytes, b);
+        bulk_g2s(dst + kImageBytes, rec_of(ck) + TcRec::U + vb * TcRec::UBLK, TcRec::UBLK, b);
+    };
+
+    if (warp == 0) tmem_alloc(tmem_slot, kEpiTmemCols);
+    if (tid == kIssuer) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+        mbar_init(bar_ws, 1);
+        mbar_init(bar_d3, 1);
+        for (int b = 0; b < kD1Bufs; ++b) {
+            mbar_init(&bar_out[b], 1);
+            mbar_init(&bar_free[b], 2);  // one arrival per output warp
+        }
+        for (int b = 0; b < kTotSlots; ++b) {
+            mbar_init(&tot_full[b], 1);
+            mbar_init(&tot_empty[b], 2);  // one arrival per output warp
+        }
+        mbar_init(bar_drain, 1);
+        fence_mbar_init();
+    }
+    // state row d = tid (warps 0-3), columns v0 .. v0+31, fp32 in registers
+    float S[BV];
+    if (tid < D) {
+#pragma unroll
+        for (int x = 0; x < BV; ++x)
+            S[x] = initial_state ? initial_state[st_off + (int64_t)(v0 + x) * D + tid] : 0.0f;
+        store_row_n32(sS, tid, S);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tD3 = tmem + 32 * kD1Bufs;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+
+    // stage loads issued / waited for by the issuer, for the exit path
+    int loads_issued = 0, loads_done = 0;
+    bool ok = true;
+    if (warp < 5) {
+        if (tid == kIssuer)
+            for (int ck = 0; ck < kStages - 1 && ck < nck; ++ck, ++loads_issued) issue(ck);
+        for (int ck = 0; ck < nck; ++ck) {
+            const uint32_t fpar = (uint32_t)((ck / kStages) & 1), cpar = (uint32_t)(ck & 1);
+            const int b = ck % kD1Bufs;
+            unsigned char *st = stage_of(ck);
+            const uint32_t tD1 = tmem + 32 * b;
+            if (tid == kIssuer) {
+                ok = mbar_wait(&full[ck % kStages], fpar) && ok;
+                if (ok) loads_done = ck + 1;
+                tc_fence_after();
+                if (ok) {
+                    mma_tile_n32<128, 128, 128>(tD1, smem_u32(st + TcRec::WQ), smem_u32(sS), false);
+                    mma_commit(bar_ws);
+                }
+                // the next chunk's D1 buffer last held chunk ck - 3: the output
+                // warps must have read it (waited for here, while Vn is formed)
+                const int cn = ck + 1;
+                if (ok && cn < nck && cn >= kD1Bufs)
+                    ok = mbar_wait(&bar_free[cn % kD1Bufs], (uint32_t)(((cn / kD1Bufs) - 1) & 1)) && ok;
+                // refill the stage of chunk ck-1 once its last MMA (D1 += A Vn) is done
+                const int t = ck + kStages - 1;
+                if (ok && t < nck) {
+                    if (ck > 0)
+                        ok = mbar_wait(&bar_out[(ck - 1) % kD1Bufs], (uint32_t)(((ck - 1) / kD1Bufs) & 1)) && ok;
+                    if (ok) {
+                        issue(t);
+                        ++loads_issued;
+                    }
+                }
+            } else if (warp < 2) {
+                ok = mbar_wait(&full[ck % kStages], fpar) && ok;  // U of this stage
+                ok = mbar_wait(bar_ws, cpar) && ok;
+                tc_fence_after();
+                float x[32], u[32];  // Vn = U - W S, row tid
+                tmem_ld32(tD1 + lane_base, x);
+                const uint4 *up = reinterpret_cast<const uint4 *>(st + kImageBytes + tid * 64);
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    float y[8];
+                    unpack8(up[c8 ^ ((tid >> 1) & 3)], y);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) u[8 * c8 + t] = y[t];
+                }
+                tmem_ld_wait();
+#pragma unroll
+                for (int vv = 0; vv < BV; ++vv) x[vv] = u[vv] - x[vv];
+                store_row_n32(sVn, tid, x);
+                fence_async_smem();
+                tc_fence_before();
+            } else if (warp < 4) {
+                ok = mbar_wait(&full[ck % kStages], fpar) && ok;  // gC of this stage
+            }
+            // (a failure seen here is carried to the "S ready" barrier below, which
+            // every state warp reaches; warps 2-3's D3 wait then gives up on its own)
+            if (warp < 2 || warp == 4) ok = named_bar_and(kBarV, 96, ok);
+            if (tid == kIssuer) {
+                tc_fence_after();
+                if (ok) {
+                    mma_tile_n32<128, 64, 64, true>(tD3, smem_u32(st + TcRec::KD), smem_u32(sVn), false);
+                    mma_commit(bar_d3);
+                    mma_tile_n32<128, 64, 128>(tD1, smem_u32(st + TcRec::A) - 8192, smem_u32(sVn), true);
+                    mma_commit(&bar_out[b]);
+                }
+            } else if (warp < 4 && ok) {
+                ok = mbar_wait(bar_d3, cpar) && ok;
+                tc_fence_after();
+                float x[32];  // S = diag(gC) S + KD^T Vn
+                tmem_ld32(tD3 + lane_base, x);
+                const float gc = reinterpret_cast<const float *>(st + TcRec::GC)[tid];
+                tmem_ld_wait();
+#pragma unroll
+                for (int vv = 0; vv < BV; ++vv) S[vv] = fmaf(gc, S[vv], x[vv]);
+                store_row_n32(sS, tid, S);
+                fence_async_smem();
+                tc_fence_before();
+            }
+            if (!named_bar_and(kBarS, kScanThreads, ok)) {
+                ok = false;
+                break;
+            }
+        }
+    } else if (warp == 5) {
+
+        // row totals: lane l takes rows l and l + 32 of every chunk; each round
+        // reads the words of the next two chunks not yet complete
+        const uint64_t *ring = ws_at<const uint64_t>(workspace, L.epi_part_off) +
+                               (size_t)(n * H + h) * kEpiRing * 4 * C;  // [slot][CTA][row]
+        long long tlast = clock64();  // last progress
+        int cdone = 0;
+        while (cdone < nck) {
+            bool comp[2] = {false, false};
+            float tot[2][2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int c = cdone + k;
+                if (c >= nck) break;
+                const uint64_t *slot = ring + (size_t)(c % kEpiRing) * 4 * C + lane;
+                uint64_t wd[2][4];
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) wd[hr][j] = ld_relaxed_gpu_u64(slot + j * C + 32 * hr);
+                bool all = true;
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    float t = 0.0f;  // summed in CTA order: the same rounding in all four
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        all = all && (uint32_t)wd[hr][j] == (uint32_t)(c + 1);
+                        t += __uint_as_float((uint32_t)(wd[hr][j] >> 32));
+                    }
+                    tot[k][hr] = t;
+                }
+                comp[k] = __all_sync(0xffffffffu, all);
+            }
+            // hand over, in order, the chunks found complete
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                if (!comp[k] || (k == 1 && !comp[0])) break;
+                const int c = cdone, sl = c % kTotSlots;
+                if (c >= kTotSlots) ok = mbar_wait(&tot_empty[sl], (uint32_t)(((c / kTotSlots) - 1) & 1)) && ok;
+                if (!ok) break;
+                sTot[sl * C + lane] = tot[k][0];
+                sTot[sl * C + lane + 32] = tot[k][1];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tot_full[sl]);
+                ++cdone;
+            }
+            if (!ok) break;
+            if (comp[0]) {
+                tlast = clock64();
+            } else if (clock64() - tlast > 4000000000LL) {  // no word for ~2 s
+                ok = false;
+                break;
+            } else {
+                __nanosleep(64);
+            }
+        }
+    } else if (warp >= kOutWarp0) {
+        // output rows: row r of each chunk is TMEM lane 64 + r of its D1 buffer
+        const int r = tid - 32 * kOutWarp0;
+        const __nv_bfloat16 *gate = reinterpret_cast<const __nv_bfloat16 *>(epi.out_gate);
+        uint64_t *ring = ws_at<uint64_t>(workspace, L.epi_part_off) +
+                         (size_t)(n * H + h) * kEpiRing * 4 * C + r;  // [slot][CTA][row]
+        float w[BV];
+#pragma unroll
+        for (int c4 = 0; c4 < BV / 4; ++c4) {
+            const float4 wv = *reinterpret_cast<const float4 *>(epi.weight + v0 + 4 * c4);
+            w[4 * c4] = wv.x;
+            w[4 * c4 + 1] = wv.y;
+            w[4 * c4 + 2] = wv.z;
+            w[4 * c4 + 3] = wv.w;
+        }
+        auto row_of = [&](int ck) { return ((int64_t)start + (int64_t)ck * C + r) * H + h; };
+        auto live_of = [&](int ck) { return r < min(C, len - ck * C); };
+        // this thread's gate row of chunk ck: four 16-byte units in slot ck % 4,
+        // unit c at c ^ ((r / 2) % 4) (conflict-free reads across the warp)
+        unsigned char *grow = sm + S_GATE + r * 64;
+        auto gate_unit = [&](int ck, int c8) {
+            return grow + (ck % kGateSlots) * (C * 64) + ((c8 ^ ((r >> 1) & 3)) << 4);
+        };
+        auto fetch_gate = [&](int ck) {  // one commit group per call, empty past the end
+            if (ck < nck && live_of(ck)) {
+                const uint4 *gq = reinterpret_cast<const uint4 *>(gate + row_of(ck) * D + v0);
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) cp_async16(gate_unit(ck, c8), gq + c8);
+            }
+            cp_async_commit();
+        };
+        fetch_gate(0);
+        fetch_gate(1);
+        // Step ck: chunk ck's rows into x, its sum published, chunk ck + 2's
+        // gate row requested; chunk ck - 1 finished from xp with warp 5's row
+        // total.  Called with the two register sets swapped on alternate
+        // steps.
+        auto step = [&](int ck, float (&x)[BV], float (&xp)[BV]) -> bool {
+            fetch_gate(ck + 2);
+            if (ck > 0) {
+                cp_async_wait<3>();  // chunk ck - 1's gate row (groups ck, ck + 1, ck + 2 may be pending)
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    float gv[8];
+                    unpack8(live_of(ck - 1) ? *reinterpret_cast<const uint4 *>(gate_unit(ck - 1, c8))
+                                            : make_uint4(0, 0, 0, 0),
+                            gv);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t)  // sigmoid(g) = 1 / (1 + e^-g)
+                        xp[8 * c8 + t] *= w[8 * c8 + t] * __fdividef(1.0f, 1.0f + __expf(-gv[t]));
+                }
+            }
+            if (ck < nck) {
+                const int b = ck % kD1Bufs;
+                if (!mbar_wait(&bar_out[b], (uint32_t)((ck / kD1Bufs) & 1))) return false;
+                tc_fence_after();
+                tmem_ld32(tmem + 32 * b + lane_base, x);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_free[b]);  // D1[b] may be reused
+                float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // rows past the sequence end are zero
+#pragma unroll
+                for (int vv = 0; vv < BV; ++vv) s4[vv & 3] = fmaf(x[vv], x[vv], s4[vv & 3]);
+                const float ss = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                st_relaxed_gpu_u64(ring + (size_t)(ck % kEpiRing) * 4 * C + vb * C,
+                                   ((uint64_t)__float_as_uint(ss) << 32) | (uint32_t)(ck + 1));
+            }
+            if (ck > 0) {
+                const int sl = (ck - 1) % kTotSlots;
+                if (!mbar_wait(&tot_full[sl], (uint32_t)(((ck - 1) / kTotSlots) & 1))) return false;
+                const float tot = sTot[sl * C + r];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tot_empty[sl]);
+                const float rn = rsqrtf(tot * (1.0f / D) + epi.eps);
+                if (live_of(ck - 1)) {
+                    uint4 *op = reinterpret_cast<uint4 *>(o + row_of(ck - 1) * D + v0);
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        float y[8];
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) y[t] = xp[8 * c8 + t] * rn;
+                        op[c8] = pack8(y);
+                    }
+                }
+            }
+            return true;
+        };
+        float xa[BV], xb[BV];
+        for (int ck = 0; ck <= nck && ok; ck += 2) {
+            ok = step(ck, xa, xb);
+            if (ok && ck + 1 <= nck) ok = step(ck + 1, xb, xa);
+        }
+        cp_async_wait<0>();  // nothing in flight into shared memory at exit
+    }
+    ok = __syncthreads_and(ok);
+    if (!ok) {
+        // let copies and MMAs still in flight land before the shared memory
+        // and the TMEM are released
+        if (tid == kIssuer) {
+            atomicOr(status, kStatusTimeout);
+            for (int t = loads_done; t < loads_issued; ++t)
+                mbar_wait(&full[t % kStages], (uint32_t)((t / kStages) & 1), 400000000LL);
+            mma_commit(bar_drain);
+            mbar_wait(bar_drain, 0, 400000000LL);
+        }
+    } else if (final_state && tid < D) {
+#pragma unroll
+        for (int x = 0; x < BV; ++x) final_state[st_off + (int64_t)(v0 + x) * D + tid] = S[x];
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kEpiTmemCols);
 }
 
 // ---------------------------------------------------------------------------
@@ -1335,9 +1726,10 @@ cudaError_t launch_chunk_prep_tc(const void *q, const void *k, const void *v, co
 
 cudaError_t launch_chunk_scan_tc(const float *initial_state, float *final_state,
                                  const int32_t *state_indices, void *o, int n_seqs,
-                                 int64_t total_tokens, int H, int flags, void *workspace,
-                                 cudaStream_t stream) {
+                                 int64_t total_tokens, int H, int flags, const EpiArgs *epi,
+                                 bool *epi_applied, void *workspace, cudaStream_t stream) {
     const WsLayout L = ws_layout(total_tokens, n_seqs, H, TcRec::bytes);
+    *epi_applied = false;
     // wide scan once four CTAs per (sequence, head) would not fit in one wave
     const bool wide = (flags & KDA_CHUNK_SCAN_WIDE) ||
                       (!(flags & KDA_CHUNK_SCAN_SPLIT) && (int64_t)n_seqs * H * (D / BV) > sm_count());
@@ -1348,14 +1740,37 @@ cudaError_t launch_chunk_scan_tc(const float *initial_state, float *final_state,
                                                stream, initial_state, final_state, state_indices,
                                                (__nv_bfloat16 *)o, n_seqs, H, workspace, L);
         if (e != cudaSuccess) return e;
-    } else {
-        const dim3 grid((unsigned)n_seqs, (unsigned)H, D / BV);
-        cudaFuncSetAttribute(chunk_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S_SMEM);
-        const cudaError_t e = launch_dependent(chunk_scan_tc_kernel, grid, dim3(kScanThreads), S_SMEM,
-                                               stream, initial_state, final_state, state_indices,
-                                               (__nv_bfloat16 *)o, n_seqs, H, workspace, L);
-        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
     }
+    const dim3 grid((unsigned)n_seqs, (unsigned)H, D / BV);
+    const int64_t ctas = (int64_t)n_seqs * H * (D / BV);
+    // the epilogue in the scan: 16-byte aligned gate rows, exchange room for
+    // every (sequence, head), and the whole grid resident at once
+    bool fuse = epi && epi->out_gate && ((uintptr_t)epi->out_gate % 16 == 0) &&
+                (int64_t)n_seqs * H <= kEpiPairs;
+    if (fuse) {
+        int per_sm = 0;
+        cudaFuncSetAttribute(chunk_scan_tc_epi_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S_EPI_SMEM);
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chunk_scan_tc_epi_kernel, kEpiScanThreads,
+                                                          S_EPI_SMEM) != cudaSuccess) {
+            cudaGetLastError();
+            per_sm = 0;
+        }
+        fuse = ctas <= (int64_t)per_sm * sm_count();
+    }
+    if (fuse) {
+        const cudaError_t e = launch_dependent_coop(chunk_scan_tc_epi_kernel, grid, dim3(kEpiScanThreads),
+                                                    S_EPI_SMEM, stream, initial_state, final_state, state_indices,
+                                                    (__nv_bfloat16 *)o, n_seqs, H, workspace, L, *epi);
+        if (e != cudaSuccess) return e;
+        *epi_applied = true;
+        return cudaGetLastError();
+    }
+    cudaFuncSetAttribute(chunk_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S_SMEM);
+    const cudaError_t e = launch_dependent(chunk_scan_tc_kernel, grid, dim3(kScanThreads), S_SMEM, stream,
+                                           initial_state, final_state, state_indices, (__nv_bfloat16 *)o,
+                                           n_seqs, H, workspace, L);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

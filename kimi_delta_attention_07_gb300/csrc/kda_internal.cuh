@@ -73,9 +73,16 @@ __host__ __device__ inline int64_t max_chunks(int64_t total_tokens, int n_seqs) 
     return total_tokens / kChunk + n_seqs;
 }
 
+// Row sums of squares exchanged between the four value-column CTAs of a
+// (sequence, head) when the split scan applies the output epilogue itself: a
+// ring of kEpiRing chunks x 4 CTAs x 64 rows of tagged 8-byte words per
+// (sequence, head), for at most kEpiPairs pairs.
+constexpr int kEpiPairs = 64;
+constexpr int kEpiRing = 4;
+
 struct WsLayout {
-    size_t status_off, defer_count_off, seq_start_off, seq_len_off, chunk_off_off, defer_off,
-        records_off, record_bytes, total;
+    size_t status_off, defer_count_off, seq_start_off, seq_len_off, chunk_off_off, epi_part_off,
+        defer_off, records_off, record_bytes, total;
 };
 
 __host__ __device__ inline WsLayout ws_layout(int64_t total_tokens, int n_seqs, int H,
@@ -87,7 +94,8 @@ __host__ __device__ inline WsLayout ws_layout(int64_t total_tokens, int n_seqs, 
     L.seq_start_off = 256;
     L.seq_len_off = L.seq_start_off + arr;
     L.chunk_off_off = L.seq_len_off + arr;
-    L.defer_off = L.chunk_off_off + arr;
+    L.epi_part_off = align_up(L.chunk_off_off + arr, 256);  // u64 [kEpiPairs][kEpiRing][4][64]
+    L.defer_off = L.epi_part_off + sizeof(uint64_t) * kEpiPairs * kEpiRing * 4 * kChunk;
     const size_t items = (size_t)max_chunks(total_tokens, n_seqs) * (size_t)H;
     L.records_off = align_up(L.defer_off + sizeof(int32_t) * items, 256);
     L.record_bytes = record_bytes;
@@ -159,6 +167,34 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// The same for a grid whose CTAs wait on one another: a cooperative launch,
+// which fails rather than start a grid that cannot be resident at once.
+// Where programmatic serialization cannot be combined with it, the launch is
+// repeated as a plain cooperative one.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent_coop(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                  cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    }
+    return e;
 }
 
 // SM count of the current device (cached per device; host only)
@@ -248,10 +284,13 @@ cudaError_t launch_chunk_prep_tc_strong(const void *q, const void *k, const void
 cudaError_t launch_gate_activation(const GateArgs &gate, int dtype, int64_t total_tokens, int H,
                                    float *g_out, float *beta_out, cudaStream_t stream);
 
+// epi (may be nullptr): the output epilogue, applied in the scan where the
+// layout allows it (*epi_applied then true; otherwise the caller runs
+// launch_output_gate_norm after it).
 cudaError_t launch_chunk_scan_tc(const float *initial_state, float *final_state,
                                  const int32_t *state_indices, void *o, int n_seqs,
-                                 int64_t total_tokens, int H, int flags, void *workspace,
-                                 cudaStream_t stream);
+                                 int64_t total_tokens, int H, int flags, const EpiArgs *epi,
+                                 bool *epi_applied, void *workspace, cudaStream_t stream);
 
 // Block-wide helper used by the chunk kernels: find the sequence that owns
 // global chunk `c` (largest n with chunk_off[n] <= c; chunk_off non-decreasing).

@@ -764,6 +764,37 @@ def test_gated_chunk_epilogue_split_scan_ragged(kda, lengths):
     assert rel_l2(vk_to_kv(sf), s_ref) < TOL_BF16
 
 
+@pytest.mark.parametrize("case", ["gate_8_byte_aligned", "pairs_beyond_exchange"])
+def test_gated_chunk_epilogue_split_scan_separate_pass(kda, case):
+    """Split-layout calls that the scan cannot apply the epilogue to itself
+    (gate rows not 16-byte aligned; more (sequence, head) pairs than its
+    exchange ring holds) take the standalone pass, with the same result."""
+    lengths, H = ([130, 65], 2) if case == "gate_8_byte_aligned" else ([70, 1, 64], 24)
+    x = kda_inputs.prefill(lengths, H=H, seed=64, init_std=0.02)
+    y, g_ref, b_ref = _gated(x, 64, "lower_bound")
+    y = kda_inputs.with_output_gate(y, seed=64)
+    d = dev(y, names=("q", "k", "v", "raw_gate", "raw_beta", "a_log", "dt_bias", "cu_seqlens",
+                      "initial_state", "out_gate", "norm_weight"))
+    gate = d["out_gate"]
+    if case == "gate_8_byte_aligned":
+        buf = torch.empty(gate.numel() + 8, dtype=gate.dtype, device=gate.device)
+        gate = buf[4:4 + gate.numel()].view(gate.shape)
+        gate.copy_(d["out_gate"])
+        assert gate.data_ptr() % 16 == 8
+    o, sf = kda.kda_chunk_fwd_gated(d["q"], d["k"], d["v"], d["raw_gate"], d["raw_beta"], d["a_log"],
+                                    d["dt_bias"], lower_bound=y["lower_bound"], out_gate=gate,
+                                    norm_weight=d["norm_weight"], norm_eps=y["norm_eps"],
+                                    cu_seqlens=d["cu_seqlens"], initial_state=d["initial_state"],
+                                    scan="split")
+    torch.cuda.synchronize()
+    s0 = np.swapaxes(y["initial_state"].double().numpy(), -1, -2)
+    o_ref, s_ref = oracle.recurrence(y["q"], y["k"], y["v"], g_ref, b_ref,
+                                     cu_seqlens=y["cu_seqlens"].numpy(), initial_state=s0)
+    out_ref = oracle.output_gate_norm(o_ref, y["out_gate"], y["norm_weight"], y["norm_eps"])
+    assert rel_l2(to_np(o), out_ref) < TOL_BF16
+    assert rel_l2(vk_to_kv(sf), s_ref) < TOL_BF16
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_output_gate_norm_standalone(kda, dtype):
     gen = torch.Generator().manual_seed(63)
