@@ -1222,11 +1222,6 @@ __global__ void __launch_bounds__(kEpiScanThreads, 1)
                     mma_tile_n32<128, 128, 128>(tD1, smem_u32(st + TcRec::WQ), smem_u32(sS), false);
                     mma_commit(bar_ws);
                 }
-                // the next chunk's D1 buffer last held chunk ck - 3: the output
-                // warps must have read it (waited for here, while Vn is formed)
-                const int cn = ck + 1;
-                if (ok && cn < nck && cn >= kD1Bufs)
-                    ok = mbar_wait(&bar_free[cn % kD1Bufs], (uint32_t)(((cn / kD1Bufs) - 1) & 1)) && ok;
                 // refill the stage of chunk ck-1 once its last MMA (D1 += A Vn) is done
                 const int t = ck + kStages - 1;
                 if (ok && t < nck) {
@@ -1271,6 +1266,11 @@ __global__ void __launch_bounds__(kEpiScanThreads, 1)
                     mma_tile_n32<128, 64, 128>(tD1, smem_u32(st + TcRec::A) - 8192, smem_u32(sVn), true);
                     mma_commit(&bar_out[b]);
                 }
+                // the next chunk's D1 buffer last held chunk ck - 3: the output
+                // warps must have read it (waited for while the state is updated)
+                const int cn = ck + 1;
+                if (ok && cn < nck && cn >= kD1Bufs)
+                    ok = mbar_wait(&bar_free[cn % kD1Bufs], (uint32_t)(((cn / kD1Bufs) - 1) & 1)) && ok;
             } else if (warp < 4 && ok) {
                 ok = mbar_wait(bar_d3, cpar) && ok;
                 tc_fence_after();
@@ -1337,14 +1337,14 @@ __global__ void __launch_bounds__(kEpiScanThreads, 1)
                 ++cdone;
             }
             if (!ok) break;
+            // a chunk's words come about one state step apart: poll sparingly
             if (comp[0]) {
                 tlast = clock64();
             } else if (clock64() - tlast > 4000000000LL) {  // no word for ~2 s
                 ok = false;
                 break;
-            } else {
-                __nanosleep(64);
             }
+            __nanosleep(comp[0] ? 400 : 200);
         }
     } else if (warp >= kOutWarp0) {
         // output rows: row r of each chunk is TMEM lane 64 + r of its D1 buffer
