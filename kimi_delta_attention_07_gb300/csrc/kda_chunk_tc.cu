@@ -96,8 +96,8 @@ static_assert(P_SMEM * kPrepMinBlocks + 2048 <= 233472, "two prep CTAs per SM");
 static_assert(P_L + C * LSTRIDE * 4 <= P_SCR && P_SCR + 10 * MBLK * 4 <= P_XL + 32768 &&
                   4 * MBLK * 4 <= C * LSTRIDE * 4,
               "L and inverse scratch inside the q/k region");
-static_assert(P_T + 32768 <= P_V && P_V + 16384 <= P_E && P_STAGE + 32768 <= P_E,
-              "T, v and staging below E");
+static_assert(P_T + 32768 <= P_V && P_V + 16384 == P_E && P_STAGE + 32768 <= P_E,
+              "T and staging below [v | E], one N = 256 operand of four 8 KB column blocks");
 static_assert(P_COL + 2 * NCOL * 256 <= P_E, "column operand");
 
 struct PrepItem {
@@ -667,61 +667,66 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
                 float *dst = unit ? XD + a * MBLK : Mb + p_ * MBLK;
 #pragma unroll
                 for (int r = 0; r < 16; ++r) dst[r * MS + c] = x[r];
-            }
-            __syncthreads();
-            for (int s = tid; s < 576; s += kPrepThreads) {  // warp-uniform slot ranges
-                const int ii = (s >> 2) & 15, c4 = s & 3;
-                if (s < 192) {  // X_{q+1,q} = -M_{q+1,q} X_qq
-                    const int q_ = s >> 6;
-                    const int pm = q_ == 0 ? 0 : (q_ == 1 ? 2 : 5);
-                    float4 x = mm16_row4(Mb + pm * MBLK, MS, XD + q_ * MBLK, MS, ii, c4);
-                    x = make_float4(-x.x, -x.y, -x.z, -x.w);
-                    if (q_ < 2) *reinterpret_cast<float4 *>(Xo + q_ * MBLK + ii * MS + 4 * c4) = x;
-                    put_t(q_ + 1, q_, ii, c4, x);
-                } else if (s < 320) {  // C30 = M_32 M_20 - M_30, C31 = M_32 M_21 - M_31
-                    const int k_ = (s - 192) >> 6;
-                    float4 x = mm16_row4(Mb + 5 * MBLK, MS, Mb + (k_ == 0 ? 1 : 2) * MBLK, MS, ii, c4);
-                    const float4 m = *reinterpret_cast<const float4 *>(Mb + (3 + k_) * MBLK + ii * MS + 4 * c4);
-                    *reinterpret_cast<float4 *>(Cb + k_ * MBLK + ii * MS + 4 * c4) =
-                        make_float4(x.x - m.x, x.y - m.y, x.z - m.z, x.w - m.w);
-                } else {  // diagonal blocks of T
-                    const int a = (s - 320) >> 6;
-                    put_t(a, a, ii, c4, *reinterpret_cast<const float4 *>(XD + a * MBLK + ii * MS + 4 * c4));
-                }
-            }
-            __syncthreads();
-            for (int s = tid; s < 576; s += kPrepThreads) {
-                if (s < 192) {
-                    const int q_ = s >> 6, ii = (s >> 2) & 15, c4 = s & 3;
-                    float a16[16];
-                    float4 x, y;
-                    if (q_ == 0) {         // X_20 = -(M_20 X_00 + M_21 X_10)
-                        row16(Mb + 1 * MBLK, MS, ii, a16);
-                        x = row4_times(a16, XD, c4);
-                        row16(Mb + 2 * MBLK, MS, ii, a16);
-                        y = row4_times(a16, Xo, c4);
-                        put_t(2, 0, ii, c4, make_float4(-(x.x + y.x), -(x.y + y.y), -(x.z + y.z), -(x.w + y.w)));
-                    } else if (q_ == 1) {  // X_31 = -(M_31 X_11 + M_32 X_21)
-                        row16(Mb + 4 * MBLK, MS, ii, a16);
-                        x = row4_times(a16, XD + MBLK, c4);
-                        row16(Mb + 5 * MBLK, MS, ii, a16);
-                        y = row4_times(a16, Xo + MBLK, c4);
-                        put_t(3, 1, ii, c4, make_float4(-(x.x + y.x), -(x.y + y.y), -(x.z + y.z), -(x.w + y.w)));
-                    } else {               // X_30 = C30 X_00 + C31 X_10
-                        row16(Cb, MS, ii, a16);
-                        x = row4_times(a16, XD, c4);
-                        row16(Cb + MBLK, MS, ii, a16);
-                        y = row4_times(a16, Xo, c4);
-                        put_t(3, 0, ii, c4, make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w));
-                    }
-                } else {  // zeros above the block diagonal: 6 blocks x 16 rows x 2 chunks x hi, lo
-                    const int sl = s - 192;
+            } else {
+                // meanwhile warps 5-7: zeros above the block diagonal of T, 6
+                // blocks x 16 rows x 2 chunks x hi, lo (4 slots per thread)
+                for (int sl = tid - 160; sl < 384; sl += 96) {
                     const int pz = sl >> 6, i = (sl >> 2) & 15, h = (sl >> 1) & 1, hl = sl & 1;
                     const int a = pz < 3 ? 0 : (pz < 5 ? 1 : 2);
                     const int b = pz < 3 ? pz + 1 : (pz < 5 ? pz - 1 : 3);
                     unsigned char *z = sT + hl * 16384 + sw128_off(16 * a + i, 16 * b + 8 * h, 64);
                     *reinterpret_cast<uint4 *>(z) = make_uint4(0, 0, 0, 0);
                     *reinterpret_cast<uint4 *>(z + 8192) = make_uint4(0, 0, 0, 0);
+                }
+            }
+            __syncthreads();
+            if (tid < 192) {  // X_{q+1,q} = -M_{q+1,q} X_qq, one (row, 4 columns) slot per thread
+                const int ii = (tid >> 2) & 15, c4 = tid & 3, q_ = tid >> 6;
+                const int pm = q_ == 0 ? 0 : (q_ == 1 ? 2 : 5);
+                float4 x = mm16_row4(Mb + pm * MBLK, MS, XD + q_ * MBLK, MS, ii, c4);
+                x = make_float4(-x.x, -x.y, -x.z, -x.w);
+                if (q_ < 2) *reinterpret_cast<float4 *>(Xo + q_ * MBLK + ii * MS + 4 * c4) = x;
+                put_t(q_ + 1, q_, ii, c4, x);
+            } else {  // C30 = M_32 M_20 - M_30, C31 = M_32 M_21 - M_31: two slots per thread
+#pragma unroll 1
+                for (int k_ = 0; k_ < 2; ++k_) {
+                    const int sl = tid - 192, ii = (sl >> 2) & 15, c4 = sl & 3;
+                    float4 x = mm16_row4(Mb + 5 * MBLK, MS, Mb + (k_ == 0 ? 1 : 2) * MBLK, MS, ii, c4);
+                    const float4 m = *reinterpret_cast<const float4 *>(Mb + (3 + k_) * MBLK + ii * MS + 4 * c4);
+                    *reinterpret_cast<float4 *>(Cb + k_ * MBLK + ii * MS + 4 * c4) =
+                        make_float4(x.x - m.x, x.y - m.y, x.z - m.z, x.w - m.w);
+                }
+            }
+            __syncthreads();
+            if (tid < 192) {
+                const int q_ = tid >> 6, ii = (tid >> 2) & 15, c4 = tid & 3;
+                float a16[16];
+                float4 x, y;
+                if (q_ == 0) {         // X_20 = -(M_20 X_00 + M_21 X_10)
+                    row16(Mb + 1 * MBLK, MS, ii, a16);
+                    x = row4_times(a16, XD, c4);
+                    row16(Mb + 2 * MBLK, MS, ii, a16);
+                    y = row4_times(a16, Xo, c4);
+                    put_t(2, 0, ii, c4, make_float4(-(x.x + y.x), -(x.y + y.y), -(x.z + y.z), -(x.w + y.w)));
+                } else if (q_ == 1) {  // X_31 = -(M_31 X_11 + M_32 X_21)
+                    row16(Mb + 4 * MBLK, MS, ii, a16);
+                    x = row4_times(a16, XD + MBLK, c4);
+                    row16(Mb + 5 * MBLK, MS, ii, a16);
+                    y = row4_times(a16, Xo + MBLK, c4);
+                    put_t(3, 1, ii, c4, make_float4(-(x.x + y.x), -(x.y + y.y), -(x.z + y.z), -(x.w + y.w)));
+                } else {               // X_30 = C30 X_00 + C31 X_10
+                    row16(Cb, MS, ii, a16);
+                    x = row4_times(a16, XD, c4);
+                    row16(Cb + MBLK, MS, ii, a16);
+                    y = row4_times(a16, Xo, c4);
+                    put_t(3, 0, ii, c4, make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w));
+                }
+            } else {  // the diagonal blocks of T: 4 blocks x 16 rows x 4 column groups, 4 per thread
+#pragma unroll 1
+                for (int k_ = 0; k_ < 4; ++k_) {
+                    const int sl = tid - 192 + 64 * k_;
+                    const int a = sl >> 6, ii = (sl >> 2) & 15, c4 = sl & 3;
+                    put_t(a, a, ii, c4, *reinterpret_cast<const float4 *>(XD + a * MBLK + ii * MS + 4 * c4));
                 }
             }
         }
@@ -749,10 +754,9 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
         //    slice and beta are fetched into registers while the MMA runs.
         if (tid == 0) {
             tc_fence_after();
-            mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 0, smem_u32(sT), smem_u32(sE), false);
-            mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 0, smem_u32(sT + 16384), smem_u32(sE), true);
-            mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 128, smem_u32(sT), smem_u32(sm + P_V), false);
-            mma_tile<128, 128, 64, 128, 64, false, true>(tmem + 128, smem_u32(sT + 16384), smem_u32(sm + P_V), true);
+            // [U | W] = T [v | E]: one N = 256 group (TMEM columns 0..127 U, 128..255 W)
+            mma_tile<128, 256, 64, 128, 64, false, true>(tmem, smem_u32(sT), smem_u32(sm + P_V), false);
+            mma_tile<128, 256, 64, 128, 64, false, true>(tmem, smem_u32(sT + 16384), smem_u32(sm + P_V), true);
             mma_commit(mbar);
             if (has_next) load_qk(sm, maps, nxt.h, nxt.tok0, full_qk);
         }
@@ -785,7 +789,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
         {
             const int quarter = warp & 3, part = warp >> 2;
             const int i = 32 * (quarter & 1) + lane, c0 = 64 * (quarter >> 1);
-            const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16) + 128 * part + c0;
+            const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16) + 128 * (1 - part) + c0;
 #pragma unroll 1
             for (int cb = 0; cb < 2; ++cb) {
                 float x[32];
