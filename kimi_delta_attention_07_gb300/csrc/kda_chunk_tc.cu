@@ -849,6 +849,9 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
 // ---------------------------------------------------------------------------
 constexpr int kScanThreads = 160;  // warps 0-3: state rows, Vn, output rows; warp 4: MMAs and loads
 constexpr int kIssuer = 128;       // lane 0 of warp 4
+constexpr int kSplitThreads = 192;  // the split scan: warp 5 issues the second key half of D1
+constexpr int kIssuer2 = 160;       // lane 0 of warp 5
+constexpr uint32_t kSplitTmemCols = 256;  // D1 (2 buffers x 2 key halves x 32 columns), D3 (32)
 constexpr int BV = 32;
 constexpr uint32_t kScanTmemCols = 128;  // D1 double-buffered (2 x 32 columns), D3 (32)
 constexpr int kStages = 3;
@@ -883,14 +886,17 @@ __device__ __forceinline__ void store_row_n32(unsigned char *op, int k, const fl
 }
 
 // Per chunk ck (records staged by bulk copies, kStages deep), D1 = D1[ck & 1]:
-//   issuer:     D1 = [W ; QG] S                         after "S ready"
-//   warps 0-1:  Vn = U - D1[0:64] -> Vn operand          -> "Vn ready"
+//   issuers:    D1 = [W ; QG] S, keys 0..63 from warp 4 and keys 64..127 from
+//               warp 5 into two accumulators              after "S ready"
+//   warps 0-1:  Vn = U - (D1a + D1b)[0:64] -> Vn operand  -> "Vn ready"
 //   warps 2-3:  output rows of chunk ck-1 from D1[(ck-1) & 1]
-//   issuer:     D3 = KD^T Vn, then D1[64:128] += A Vn    after "Vn ready"
-//   warps 0-3:  S = diag(gC) S + D3 -> S operand         -> "S ready"
-// A dedicated issuing warp keeps the (slow to issue) MMAs off the threads that
-// own state rows; the output MMA runs while the state is updated.
-__global__ void __launch_bounds__(kScanThreads, 1)
+//   issuer:     D3 = KD^T Vn, then D1a[64:128] += A Vn    after "Vn ready"
+//   warps 0-3:  S = diag(gC) S + D3 -> S operand          -> "S ready"
+// Dedicated issuing warps keep the (slow to issue) MMAs off the threads that
+// own state rows; a tcgen05.mma costs its issuing thread ~60 cycles, so D1's
+// eight instructions go out as two groups of four at once (scan 76 -> 74 us
+// on the 4k workload).  The output MMA runs while the state is updated.
+__global__ void __launch_bounds__(kSplitThreads, 1)
     chunk_scan_tc_kernel(const float *__restrict__ initial_state, float *__restrict__ final_state,
                          const int32_t *__restrict__ state_indices, __nv_bfloat16 *__restrict__ o,
                          int n_seqs, int H, void *workspace, WsLayout L) {
@@ -927,13 +933,13 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         bulk_g2s(dst + kImageBytes, rec_of(ck) + TcRec::U + vb * TcRec::UBLK, TcRec::UBLK, b);
     };
 
-    if (warp == 0) tmem_alloc(tmem_slot, kScanTmemCols);
+    if (warp == 0) tmem_alloc(tmem_slot, kSplitTmemCols);
     if (tid == kIssuer) {
         for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
-        mbar_init(bar_ws, 1);
+        mbar_init(bar_ws, 2);  // both key halves of D1
         mbar_init(bar_d3, 1);
         mbar_init(bar_out, 1);
-        mbar_init(bar_drain, 1);
+        mbar_init(bar_drain, 2);  // both issuers
         fence_mbar_init();
     }
     // state row d = tid (warps 0-3), columns v0 .. v0+31, fp32 in registers
@@ -949,14 +955,18 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tD3 = tmem + 64;
+    const uint32_t tD3 = tmem + 128;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
 
-    // Output rows of chunk ck (TMEM D1 buffer ck & 1, lanes 64..127) -> o (warps 2-3).
+    // Output rows of chunk ck (TMEM D1 buffer ck & 1, both key halves, lanes 64..127) -> o
+    // (warps 2-3).
     auto store_output = [&](int ck) {
-        float x[32];
+        float x[32], x2[32];
         tmem_ld32(tmem + 32 * (ck & 1) + lane_base, x);
+        tmem_ld32(tmem + 64 + 32 * (ck & 1) + lane_base, x2);
         tmem_ld_wait();
+#pragma unroll
+        for (int t = 0; t < 32; ++t) x[t] += x2[t];
         const int r = tid - 64;
         if (r < min(C, len - ck * C)) {
             const int64_t tok = (int64_t)start + (int64_t)ck * C + r;
@@ -984,8 +994,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             ok = mbar_wait(&full[ck % kStages], fpar) && ok;
             if (ok) loads_done = ck + 1;
             tc_fence_after();
-            if (ok) {
-                mma_tile_n32<128, 128, 128>(tD1, smem_u32(st + TcRec::WQ), smem_u32(sS), false);
+            if (ok) {  // keys 0..63 of D1 = [W ; QG] S
+                mma_tile_n32<128, 64, 128>(tD1, smem_u32(st + TcRec::WQ), smem_u32(sS), false);
                 mma_commit(bar_ws);
             }
             // refill the stage of chunk ck-1 once its last MMA (D1 += A Vn) is done
@@ -997,12 +1007,21 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                     ++loads_issued;
                 }
             }
+        } else if (tid == kIssuer2) {
+            ok = mbar_wait(&full[ck % kStages], fpar) && ok;
+            tc_fence_after();
+            if (ok) {  // keys 64..127 of D1, issued at the same time from a second thread
+                mma_tile_n32<128, 64, 128>(tD1 + 64, smem_u32(st + TcRec::WQ + 16384), smem_u32(sS + 4096),
+                                           false);
+                mma_commit(bar_ws);
+            }
         } else if (warp < 2) {
             ok = mbar_wait(&full[ck % kStages], fpar) && ok;  // U of this stage
             ok = mbar_wait(bar_ws, cpar) && ok;
             tc_fence_after();
-            float x[32], u[32];  // Vn = U - W S, row tid
+            float x[32], x2[32], u[32];  // Vn = U - W S, row tid
             tmem_ld32(tD1 + lane_base, x);
+            tmem_ld32(tD1 + 64 + lane_base, x2);
             const uint4 *up = reinterpret_cast<const uint4 *>(st + kImageBytes + tid * 64);
 #pragma unroll
             for (int c8 = 0; c8 < 4; ++c8) {
@@ -1013,7 +1032,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             }
             tmem_ld_wait();
 #pragma unroll
-            for (int vv = 0; vv < BV; ++vv) x[vv] = u[vv] - x[vv];
+            for (int vv = 0; vv < BV; ++vv) x[vv] = u[vv] - (x[vv] + x2[vv]);
             store_row_n32(sVn, tid, x);
             fence_async_smem();
             tc_fence_before();
@@ -1050,7 +1069,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             fence_async_smem();
             tc_fence_before();
         }
-        if (!named_bar_and(kBarS, kScanThreads, ok)) {
+        if (!named_bar_and(kBarS, kSplitThreads, ok)) {
             ok = false;
             break;
         }
@@ -1064,6 +1083,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     if (!ok) {
         // let copies and MMAs still in flight land before the shared memory
         // and the TMEM are released
+        if (tid == kIssuer2) mma_commit(bar_drain);
         if (tid == kIssuer) {
             atomicOr(status, kStatusTimeout);
             for (int t = loads_done; t < loads_issued; ++t)
@@ -1077,7 +1097,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kScanTmemCols);
+    if (warp == 0) tmem_dealloc(tmem, kSplitTmemCols);
 }
 
 // ---------------------------------------------------------------------------
@@ -1771,7 +1791,7 @@ cudaError_t launch_chunk_scan_tc(const float *initial_state, float *final_state,
         return cudaGetLastError();
     }
     cudaFuncSetAttribute(chunk_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S_SMEM);
-    const cudaError_t e = launch_dependent(chunk_scan_tc_kernel, grid, dim3(kScanThreads), S_SMEM, stream,
+    const cudaError_t e = launch_dependent(chunk_scan_tc_kernel, grid, dim3(kSplitThreads), S_SMEM, stream,
                                            initial_state, final_state, state_indices, (__nv_bfloat16 *)o,
                                            n_seqs, H, workspace, L);
     if (e != cudaSuccess) return e;
