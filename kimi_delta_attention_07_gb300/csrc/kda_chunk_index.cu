@@ -18,7 +18,11 @@ __global__ void __launch_bounds__(kIndexThreads)
     chunk_index_kernel(const int32_t *__restrict__ cu_seqlens, int n_seqs, int64_t total_tokens,
                        const int32_t *__restrict__ state_indices, int64_t n_slots,
                        void *workspace, WsLayout L) {
-    griddep_launch_dependents();  // the prep may be scheduled now; it waits for this grid to finish
+    // the previous kernel of the stream (e.g. the previous forward's scan, which
+    // reads the index rewritten below) is complete before anything is written;
+    // the prep may be scheduled now, and waits for this grid to finish
+    griddep_wait();
+    griddep_launch_dependents();
     int32_t *seq_start = ws_at<int32_t>(workspace, L.seq_start_off);
     int32_t *seq_len = ws_at<int32_t>(workspace, L.seq_len_off);
     int32_t *chunk_off = ws_at<int32_t>(workspace, L.chunk_off_off);
@@ -93,9 +97,10 @@ cudaError_t launch_chunk_index(const int32_t *cu_seqlens, int n_seqs, int64_t to
                                const int32_t *state_indices, int64_t n_slots, void *workspace,
                                cudaStream_t stream) {
     const WsLayout L = ws_layout(total_tokens, n_seqs, 1, 0);
-    chunk_index_kernel<<<1, kIndexThreads, 0, stream>>>(cu_seqlens, n_seqs, total_tokens,
-                                                        state_indices, n_slots, workspace, L);
-    return cudaGetLastError();
+    const cudaError_t e = launch_dependent(chunk_index_kernel, dim3(1), dim3(kIndexThreads), 0, stream,
+                                           cu_seqlens, n_seqs, total_tokens, state_indices, n_slots,
+                                           workspace, L);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace kda

@@ -911,6 +911,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     uint64_t *bar_drain = bar_out + 1;  // exit path: every MMA issued so far is done
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_drain + 1);
     griddep_wait();  // the records (previous kernel) are complete
+    // the next forward's chunk index may be scheduled (one CTA; it waits for
+    // this grid to complete before it writes anything)
+    griddep_launch_dependents();
 
     const int n = blockIdx.x, h = blockIdx.y, vb = blockIdx.z, v0 = vb * BV;
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -1173,6 +1176,9 @@ __global__ void __launch_bounds__(kEpiScanThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_drain + 1);
     float *sTot = reinterpret_cast<float *>(sm + S_TOT);
     griddep_wait();  // the records (previous kernel) are complete
+    // the next forward's chunk index may be scheduled (one CTA; it waits for
+    // this grid to complete before it writes anything)
+    griddep_launch_dependents();
 
     const int n = blockIdx.x, h = blockIdx.y, vb = blockIdx.z, v0 = vb * BV;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1510,6 +1516,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                            const int32_t *__restrict__ state_indices, __nv_bfloat16 *__restrict__ o,
                            int n_seqs, int H, void *workspace, WsLayout L) {
     griddep_wait();  // the records (previous kernel) are complete
+    // the next forward's chunk index may be scheduled (one CTA; it waits for
+    // this grid to complete before it writes anything)
+    griddep_launch_dependents();
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     unsigned char *sS = sm + W_SOP;
