@@ -401,8 +401,14 @@ int kda_recurrent_multi_step(const void *q, const void *k, const void *v, const 
  *   norm_weight device fp32 [V];  norm_eps > 0
  * replaces each output row of V values by
  *   o / sqrt(mean(o^2) + norm_eps) * norm_weight * sigmoid(out_gate).
- * Decode applies it in the step; the chunked forward applies it as a final
- * pass over o (kda_output_gate_norm).
+ * Decode applies it in the step.  The chunked forward applies it inside its
+ * state scan where it can (tensor-core path, one CTA per 32 value columns,
+ * out_gate 16-byte aligned, at most 64 (sequence, head) pairs: the row's four
+ * CTAs exchange their sums of squares through the workspace, and the grid is
+ * launched cooperatively, so it must fit the GPU at once), normalising the
+ * unrounded o; otherwise as a final pass over the stored o
+ * (kda_output_gate_norm).  The two agree within the rounding of o to its
+ * dtype.
  */
 int kda_chunk_fwd_gated(const void *q, const void *k, const void *v, const void *raw_gate,
                         const void *raw_beta, const float *a_log, const float *dt_bias,
