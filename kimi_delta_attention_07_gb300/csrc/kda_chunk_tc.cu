@@ -853,7 +853,6 @@ constexpr int kSplitThreads = 192;  // the split scan: warp 5 issues the second 
 constexpr int kIssuer2 = 160;       // lane 0 of warp 5
 constexpr uint32_t kSplitTmemCols = 256;  // D1 (2 buffers x 2 key halves x 32 columns), D3 (32)
 constexpr int BV = 32;
-constexpr uint32_t kScanTmemCols = 128;  // D1 double-buffered (2 x 32 columns), D3 (32)
 constexpr int kStages = 3;
 static_assert(BV == 32, "S and Vn are N = 32 operands");
 constexpr uint32_t kImageBytes = TcRec::U;                   // WQ | KD | A | gC
