@@ -1794,9 +1794,13 @@ cudaError_t launch_chunk_scan_tc(const float *initial_state, float *final_state,
         const cudaError_t e = launch_dependent_coop(chunk_scan_tc_epi_kernel, grid, dim3(kEpiScanThreads),
                                                     S_EPI_SMEM, stream, initial_state, final_state, state_indices,
                                                     (__nv_bfloat16 *)o, n_seqs, H, workspace, L, *epi);
-        if (e != cudaSuccess) return e;
-        *epi_applied = true;
-        return cudaGetLastError();
+        if (e == cudaSuccess) {
+            *epi_applied = true;
+            return cudaGetLastError();
+        }
+        // a cooperative launch refused here (nothing was launched): the plain
+        // split scan below, and the separate pass after it
+        cudaGetLastError();
     }
     cudaFuncSetAttribute(chunk_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S_SMEM);
     const cudaError_t e = launch_dependent(chunk_scan_tc_kernel, grid, dim3(kSplitThreads), S_SMEM, stream,
