@@ -13,6 +13,7 @@ namespace kda {
 namespace {
 
 constexpr int kIndexThreads = 1024;
+constexpr int kMaxSortedSeqs = 256;  // beyond this, sequences keep their order
 
 __global__ void __launch_bounds__(kIndexThreads)
     chunk_index_kernel(const int32_t *__restrict__ cu_seqlens, int n_seqs, int64_t total_tokens,
@@ -83,6 +84,28 @@ __global__ void __launch_bounds__(kIndexThreads)
         if (n < n_seqs) chunk_off[n] = carry + before;
         carry += warp_tot[kIndexThreads / 32 - 1];
         __syncthreads();
+    }
+    // sequences by decreasing length (ties: lower index first), so that a
+    // scan grid walking this order starts its longest chains first; the
+    // quadratic count runs for batches of up to kMaxSortedSeqs sequences
+    int32_t *order = ws_at<int32_t>(workspace, L.seq_order_off);
+    __shared__ int len_s[kMaxSortedSeqs];
+    __syncthreads();  // seq_len of every sequence is written
+    const bool sorted = n_seqs <= kMaxSortedSeqs;
+    if (sorted)
+        for (int n = threadIdx.x; n < n_seqs; n += kIndexThreads) len_s[n] = seq_len[n];
+    __syncthreads();
+    for (int n = threadIdx.x; n < n_seqs; n += kIndexThreads) {
+        int rank = n;
+        if (sorted) {
+            const int ln = len_s[n];
+            rank = 0;
+            for (int m = 0; m < n_seqs; ++m) {
+                const int lm = len_s[m];
+                rank += (lm > ln) || (lm == ln && m < n);
+            }
+        }
+        order[rank] = n;
     }
     if (threadIdx.x == 0) {
         chunk_off[n_seqs] = carry;

@@ -1529,7 +1529,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     uint64_t *bar_drain = bar_out + 1;      // exit path: every MMA issued so far is done
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_drain + 1);
 
-    const int n = blockIdx.x, h = blockIdx.y;
+    // longest sequences first: the grid walks the sequences by decreasing
+    // length, all heads of one sequence before the next
+    const int n = ws_at<const int32_t>(workspace, L.seq_order_off)[blockIdx.x / H], h = blockIdx.x % H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q = warp & 3, half = (warp >> 2) & 1;  // TMEM lane quarter, value-column half
     const int32_t start = ws_at<const int32_t>(workspace, L.seq_start_off)[n];
@@ -1766,7 +1768,7 @@ cudaError_t launch_chunk_scan_tc(const float *initial_state, float *final_state,
     const bool wide = (flags & KDA_CHUNK_SCAN_WIDE) ||
                       (!(flags & KDA_CHUNK_SCAN_SPLIT) && (int64_t)n_seqs * H * (D / BV) > sm_count());
     if (wide) {
-        const dim3 grid((unsigned)n_seqs, (unsigned)H, 1);
+        const dim3 grid((unsigned)((int64_t)n_seqs * H), 1, 1);
         cudaFuncSetAttribute(chunk_scan_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, W_SMEM);
         const cudaError_t e = launch_dependent(chunk_scan_wide_kernel, grid, dim3(kWideThreads), W_SMEM,
                                                stream, initial_state, final_state, state_indices,

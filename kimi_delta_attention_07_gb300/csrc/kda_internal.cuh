@@ -81,8 +81,8 @@ constexpr int kEpiPairs = 64;
 constexpr int kEpiRing = 4;
 
 struct WsLayout {
-    size_t status_off, defer_count_off, seq_start_off, seq_len_off, chunk_off_off, epi_part_off,
-        defer_off, records_off, record_bytes, total;
+    size_t status_off, defer_count_off, seq_start_off, seq_len_off, chunk_off_off, seq_order_off,
+        epi_part_off, defer_off, records_off, record_bytes, total;
 };
 
 __host__ __device__ inline WsLayout ws_layout(int64_t total_tokens, int n_seqs, int H,
@@ -94,7 +94,8 @@ __host__ __device__ inline WsLayout ws_layout(int64_t total_tokens, int n_seqs, 
     L.seq_start_off = 256;
     L.seq_len_off = L.seq_start_off + arr;
     L.chunk_off_off = L.seq_len_off + arr;
-    L.epi_part_off = align_up(L.chunk_off_off + arr, 256);  // u64 [kEpiPairs][kEpiRing][4][64]
+    L.seq_order_off = L.chunk_off_off + arr;  // int32 [n_seqs]: sequences by decreasing length
+    L.epi_part_off = align_up(L.seq_order_off + arr, 256);  // u64 [kEpiPairs][kEpiRing][4][64]
     L.defer_off = L.epi_part_off + sizeof(uint64_t) * kEpiPairs * kEpiRing * 4 * kChunk;
     const size_t items = (size_t)max_chunks(total_tokens, n_seqs) * (size_t)H;
     L.records_off = align_up(L.defer_off + sizeof(int32_t) * items, 256);
