@@ -1019,19 +1019,21 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
             }
         } else if (warp < 2) {
             ok = mbar_wait(&full[ck % kStages], fpar) && ok;  // U of this stage
+            float x[32], x2[32], u[32];  // Vn = U - W S, row tid
+            {  // U first, while D1 is formed
+                const uint4 *up = reinterpret_cast<const uint4 *>(st + kImageBytes + tid * 64);
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    float y[8];
+                    unpack8(up[c8 ^ ((tid >> 1) & 3)], y);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) u[8 * c8 + t] = y[t];
+                }
+            }
             ok = mbar_wait(bar_ws, cpar) && ok;
             tc_fence_after();
-            float x[32], x2[32], u[32];  // Vn = U - W S, row tid
             tmem_ld32(tD1 + lane_base, x);
             tmem_ld32(tD1 + 64 + lane_base, x2);
-            const uint4 *up = reinterpret_cast<const uint4 *>(st + kImageBytes + tid * 64);
-#pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-                float y[8];
-                unpack8(up[c8 ^ ((tid >> 1) & 3)], y);
-#pragma unroll
-                for (int t = 0; t < 8; ++t) u[8 * c8 + t] = y[t];
-            }
             tmem_ld_wait();
 #pragma unroll
             for (int vv = 0; vv < BV; ++vv) x[vv] = u[vv] - (x[vv] + x2[vv]);
@@ -1059,11 +1061,11 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
                 mma_commit(bar_out);
             }
         } else if (warp < 4 && ok) {
+            const float gc = reinterpret_cast<const float *>(st + TcRec::GC)[tid];
             ok = mbar_wait(bar_d3, cpar) && ok;
             tc_fence_after();
             float x[32];  // S = diag(gC) S + KD^T Vn
             tmem_ld32(tD3 + lane_base, x);
-            const float gc = reinterpret_cast<const float *>(st + TcRec::GC)[tid];
             tmem_ld_wait();
 #pragma unroll
             for (int vv = 0; vv < BV; ++vv) S[vv] = fmaf(gc, S[vv], x[vv]);
@@ -1263,18 +1265,20 @@ __global__ void __launch_bounds__(kEpiScanThreads, 1)
                 }
             } else if (warp < 2) {
                 ok = mbar_wait(&full[ck % kStages], fpar) && ok;  // U of this stage
+                float x[32], u[32];  // Vn = U - W S, row tid
+                {  // U first, while D1 is formed
+                    const uint4 *up = reinterpret_cast<const uint4 *>(st + kImageBytes + tid * 64);
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        float y[8];
+                        unpack8(up[c8 ^ ((tid >> 1) & 3)], y);
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) u[8 * c8 + t] = y[t];
+                    }
+                }
                 ok = mbar_wait(bar_ws, cpar) && ok;
                 tc_fence_after();
-                float x[32], u[32];  // Vn = U - W S, row tid
                 tmem_ld32(tD1 + lane_base, x);
-                const uint4 *up = reinterpret_cast<const uint4 *>(st + kImageBytes + tid * 64);
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    float y[8];
-                    unpack8(up[c8 ^ ((tid >> 1) & 3)], y);
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) u[8 * c8 + t] = y[t];
-                }
                 tmem_ld_wait();
 #pragma unroll
                 for (int vv = 0; vv < BV; ++vv) x[vv] = u[vv] - x[vv];
@@ -1301,11 +1305,11 @@ __global__ void __launch_bounds__(kEpiScanThreads, 1)
                 if (ok && cn < nck && cn >= kD1Bufs)
                     ok = mbar_wait(&bar_free[cn % kD1Bufs], (uint32_t)(((cn / kD1Bufs) - 1) & 1)) && ok;
             } else if (warp < 4 && ok) {
+                const float gc = reinterpret_cast<const float *>(st + TcRec::GC)[tid];
                 ok = mbar_wait(bar_d3, cpar) && ok;
                 tc_fence_after();
                 float x[32];  // S = diag(gC) S + KD^T Vn
                 tmem_ld32(tD3 + lane_base, x);
-                const float gc = reinterpret_cast<const float *>(st + TcRec::GC)[tid];
                 tmem_ld_wait();
 #pragma unroll
                 for (int vv = 0; vv < BV; ++vv) S[vv] = fmaf(gc, S[vv], x[vv]);
@@ -1681,9 +1685,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                 mma_commit(bar_out);
             }
         } else if (warp < 8 && ok) {
+            const float gc = reinterpret_cast<const float *>(st + TcRec::GC)[d];
             ok = mbar_wait(bar_d3, cpar) && ok;
             tc_fence_after();
-            const float gc = reinterpret_cast<const float *>(st + TcRec::GC)[d];
 #pragma unroll
             for (int p = 0; p < 2; ++p) {  // S = diag(gC) S + KD^T Vn
                 float x[32];
