@@ -40,7 +40,8 @@ METRIC = "KDA prefill tokens/s (T=4096,H=32,K=V=128) & decode step us; % rooflin
 T_4K, H, K, V = 4096, 32, 128, 128
 DEC_N, DEC_STEPS = 256, 64
 L2_BYTES = 129 * 1024 * 1024
-KERNELS_PER_PREFILL = 3   # chunk index, intra-chunk, state scan
+KERNELS_PER_PREFILL = 4   # chunk index, main prep, strong-decay prep (exits at once when
+                          # nothing is deferred), state scan
 KERNELS_PER_DECODE = 1
 
 
