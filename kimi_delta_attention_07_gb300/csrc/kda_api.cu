@@ -127,9 +127,16 @@ int chunk_call(int phase, const void *q, const void *k, const void *v, const flo
     cudaGetLastError();  // clear a stale error so the checks below see only ours
     cudaError_t e = cudaSuccess;
     const bool tc = use_tensor_cores(dtype, flags);
+    // tensor-core path, whole forward: the split scan goes first and runs
+    // alongside the prep, record by record (scan_ctas of its CTAs; 0 = it runs
+    // after the prep)
+    int scan_ctas = 0;
     if (phase & kIntra) {
-        e = launch_chunk_index(cu_seqlens, n_seqs, total_tokens, state_indices, n_slots,
+        e = launch_chunk_index(cu_seqlens, n_seqs, total_tokens, H, state_indices, n_slots,
                                workspace, s);
+        if (e == cudaSuccess && tc && (phase & kScan))
+            scan_ctas = launch_chunk_scan_tc_ahead(initial_state, final_state, state_indices, o, n_seqs,
+                                                   total_tokens, H, flags, epi, workspace, s, &e);
         if (e == cudaSuccess && gate && !tc) {  // fp32 path: activate into the workspace
             const WsGate W = ws_gate(ws_layout(total_tokens, n_seqs, H, record_bytes(dtype, flags)),
                                      total_tokens, H);
@@ -141,12 +148,12 @@ int chunk_call(int phase, const void *q, const void *k, const void *v, const flo
         }
         if (e == cudaSuccess)
             e = tc ? launch_chunk_prep_tc(q, k, v, g, beta, gate, n_seqs, total_tokens, H, scale,
-                                          workspace, s)
+                                          scan_ctas, workspace, s)
                    : launch_chunk_prep_f32(q, k, v, g, beta, dtype, n_seqs, total_tokens, H,
                                            scale, workspace, s);
     }
     bool epi_applied = false;
-    if (e == cudaSuccess && (phase & kScan))
+    if (e == cudaSuccess && (phase & kScan) && !scan_ctas)
         e = tc ? launch_chunk_scan_tc(initial_state, final_state, state_indices, o, n_seqs,
                                       total_tokens, H, flags, epi, &epi_applied, workspace, s)
                : launch_chunk_scan_f32(initial_state, final_state, state_indices, o, dtype,

@@ -17,11 +17,12 @@ constexpr int kMaxSortedSeqs = 256;  // beyond this, sequences keep their order
 
 __global__ void __launch_bounds__(kIndexThreads)
     chunk_index_kernel(const int32_t *__restrict__ cu_seqlens, int n_seqs, int64_t total_tokens,
-                       const int32_t *__restrict__ state_indices, int64_t n_slots,
+                       int H, const int32_t *__restrict__ state_indices, int64_t n_slots,
                        void *workspace, WsLayout L) {
-    // the previous kernel of the stream (e.g. the previous forward's scan, which
-    // reads the index rewritten below) is complete before anything is written;
-    // the prep may be scheduled now, and waits for this grid to finish
+    // the previous kernel of the stream (e.g. the previous forward's scan, or
+    // its strong-decay prep, which finishes only after a scan running beside it)
+    // is complete before anything is written; the next kernel may be scheduled
+    // now, and waits for this grid to finish
     griddep_wait();
     griddep_launch_dependents();
     int32_t *seq_start = ws_at<int32_t>(workspace, L.seq_start_off);
@@ -107,22 +108,39 @@ __global__ void __launch_bounds__(kIndexThreads)
         }
         order[rank] = n;
     }
+    // no (chunk, head) record of this call is written yet
+    {
+        const int64_t n_items = (int64_t)carry * H;
+        int4 *ready4 = ws_at<int4>(workspace, L.ready_off);
+        for (int64_t i = threadIdx.x; i < n_items / 4; i += kIndexThreads) ready4[i] = make_int4(0, 0, 0, 0);
+        int32_t *ready = ws_at<int32_t>(workspace, L.ready_off);
+        for (int64_t i = n_items / 4 * 4 + threadIdx.x; i < n_items; i += kIndexThreads) ready[i] = 0;
+    }
     if (threadIdx.x == 0) {
         chunk_off[n_seqs] = carry;
         *ws_at<int32_t>(workspace, L.status_off) = status_s;
         *ws_at<int32_t>(workspace, L.defer_count_off) = 0;  // no item deferred yet
+        *ws_at<int32_t>(workspace, L.item_ctr_off) = 0;     // no item handed out yet
+        *ws_at<int32_t>(workspace, L.scan_done_off) = 0;
+        *ws_at<int32_t>(workspace, L.strong_done_off) = 0;
+        *ws_at<int32_t>(workspace, L.prep_done_off) = 0;
     }
 }
 
 }  // namespace
 
-cudaError_t launch_chunk_index(const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens,
+void preload_chunk_index_kernel() {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, chunk_index_kernel) != cudaSuccess) cudaGetLastError();
+}
+
+cudaError_t launch_chunk_index(const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens, int H,
                                const int32_t *state_indices, int64_t n_slots, void *workspace,
                                cudaStream_t stream) {
-    const WsLayout L = ws_layout(total_tokens, n_seqs, 1, 0);
+    const WsLayout L = ws_layout(total_tokens, n_seqs, H, 0);
     const cudaError_t e = launch_dependent(chunk_index_kernel, dim3(1), dim3(kIndexThreads), 0, stream,
-                                           cu_seqlens, n_seqs, total_tokens, state_indices, n_slots,
-                                           workspace, L);
+                                           cu_seqlens, n_seqs, total_tokens, H, state_indices,
+                                           n_slots, workspace, L);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -104,7 +104,7 @@ struct PrepItem {
     int64_t tok0;
     int valid, h, c;
 };
-static_assert(32 + sizeof(PrepItem) <= 128, "barrier block");
+static_assert(32 + sizeof(PrepItem) <= 64, "barrier block");
 
 __device__ __forceinline__ PrepItem prep_item(int item, int H, const int32_t *chunk_off,
                                               const int32_t *seq_start, const int32_t *seq_len,
@@ -239,8 +239,11 @@ template <bool GATED>
 __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
     chunk_prep_tc_kernel(const __grid_constant__ RawMaps maps, const float *__restrict__ g,
                          const float *__restrict__ beta, const GateArgs gate, int n_seqs, int H,
-                         float scale, void *workspace, WsLayout L) {
-    griddep_wait();  // the chunk index (previous kernel) is complete
+                         float scale, int scan_ctas, void *workspace, WsLayout L) {
+    // the chunk index (previous kernel) is complete; launched after a scan
+    // that runs alongside, whose completion is not waited for, the index
+    // finished before that scan was let go
+    if (!scan_ctas) griddep_wait();
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     unsigned char *sXL = sm + P_XL;
@@ -255,6 +258,8 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
     uint64_t *mbar = full_qk + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(full_qk + 3);
     PrepItem *sNext = reinterpret_cast<PrepItem *>(sm + P_BAR + 32);  // metadata two items ahead
+    int *sFirst = reinterpret_cast<int *>(sm + P_BAR + 64);            // this CTA's first item
+    int *sPub = sFirst + 1;  // thread 0: the item whose record waits for its ready flag, or -1
 
     const int32_t *chunk_off = ws_at<const int32_t>(workspace, L.chunk_off_off);
     const int32_t *seq_start = ws_at<const int32_t>(workspace, L.seq_start_off);
@@ -269,7 +274,45 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
             ring[i] = make_uint4(0, 0, 0, 0);
     }
     const int n_items = chunk_off[n_seqs] * H;
-    if ((int)blockIdx.x >= n_items) return;
+    // Items go out in (chunk, head) order as CTAs ask for them (two at the
+    // start, then one per item, two items ahead), so that records are written
+    // chunk by chunk whichever CTAs are resident; each record's ready flag is
+    // raised once it is written (the previous item's, when the next item finds
+    // its bulk copies done; the last one's at exit).
+    if (threadIdx.x == 0) {
+        *sFirst = atomicAdd(ws_at<int32_t>(workspace, L.item_ctr_off), 2);
+        *sPub = -1;
+    }
+    __syncthreads();
+    const int first = *sFirst;
+    // this CTA's writes (records, deferred-item list) are done: with a scan
+    // running alongside, the strong-decay prep counts finished CTAs instead of
+    // waiting for this grid
+    int32_t *prep_done = ws_at<int32_t>(workspace, L.prep_done_off);
+    if (first >= n_items) {
+        if (threadIdx.x == 0) count_release(prep_done);
+        return;
+    }
+    // "no item" is an item of no rows (valid = 0, token 0, head 0): its loads
+    // (a tile that is read but never used, no g or beta) go out like a real
+    // item's, so that nothing below branches on whether there is a next item
+    auto no_item = []() {
+        PrepItem p;
+        p.tok0 = 0;
+        p.valid = 0;
+        p.h = 0;
+        p.c = 0;
+        return p;
+    };
+    auto take_item = [&]() {  // one thread
+        const int id = atomicAdd(ws_at<int32_t>(workspace, L.item_ctr_off), 1);
+        return id < n_items ? prep_item(id, H, chunk_off, seq_start, seq_len, n_seqs) : no_item();
+    };
+    auto publish = [&]() {  // thread 0, once the copies of the pending record are done
+        const int pub = *sPub;
+        if (pub >= 0) flag_publish(ws_at<int32_t>(workspace, L.ready_off) + pub);
+        *sPub = -1;
+    };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // transform-pass slice of this thread: key channels d .. d+3 of the 8
@@ -294,8 +337,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
                            reinterpret_cast<const __nv_bfloat16 *>(gate.raw_beta)[tok * H + hh]))
                      : beta[tok * H + hh];
     };
-    int item = blockIdx.x;
-    PrepItem cur = prep_item(item, H, chunk_off, seq_start, seq_len, n_seqs);
+    PrepItem cur = prep_item(first, H, chunk_off, seq_start, seq_len, n_seqs);
     if (tid == 0) load_qk(sm, maps, cur.h, cur.tok0, full_qk);
     GSlice<GATED> gs;
     load_gslice<GATED>(gs, g, gate, cur.tok0, cur.valid, r0, cur.h, H, d);
@@ -306,16 +348,14 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
         bias_cur = *reinterpret_cast<const float4 *>(gate.dt_bias + cur.h * D + d);
         alog_cur = gate.a_log[cur.h];
     }
-    PrepItem nxt = cur;
-    if (item + (int)gridDim.x < n_items)
-        nxt = prep_item(item + gridDim.x, H, chunk_off, seq_start, seq_len, n_seqs);
+    PrepItem nxt = first + 1 < n_items ? prep_item(first + 1, H, chunk_off, seq_start, seq_len, n_seqs)
+                                       : no_item();
 
     uint32_t qkphase = 0, vphase = 0, mphase = 0;
     bool qkpend = true, vpend = false, mpend = false;
     bool ok = true;
-    for (; item < n_items; item += gridDim.x) {
-        const bool has_next = item + (int)gridDim.x < n_items;
-        if (!has_next) griddep_launch_dependents();  // last item: the next kernel may be scheduled
+    for (;;) {
+        if (!nxt.valid) griddep_launch_dependents();  // last item: the next kernel may be scheduled
         unsigned char *rec = ws_at<unsigned char>(workspace, L.records_off + ((size_t)cur.c * H + cur.h) * TcRec::bytes);
         const int valid = cur.valid;
         if (tid < C) sB[tid] = tid < valid ? beta_cur : 0.0f;
@@ -377,7 +417,10 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
                 else sRk[R - C] = R - C < valid ? rsqrtf(ss + 1e-6f) : 0.0f;
             }
         }
-        if (tid == 0) bulk_wait_read();  // the previous item's W/U staging has been read
+        if (tid == 0) {  // the previous item's W/U copies are done: its record is complete
+            bulk_wait_all();
+            publish();
+        }
         if (!__syncthreads_and(ok)) {
             ok = false;  // uniform from here on: every thread takes the exit path
             break;
@@ -505,21 +548,18 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
             // hand the item to the strong-decay prep; the next item's q and k
             // tiles go out at once
             if (tid == 0) {
-                defer_list[atomicAdd(defer_count, 1)] = item;
+                defer_list[atomicAdd(defer_count, 1)] = cur.c * H + cur.h;
                 atomicOr(status, kStrongDecay);
-                if (has_next) load_qk(sm, maps, nxt.h, nxt.tok0, full_qk);
+                load_qk(sm, maps, nxt.h, nxt.tok0, full_qk);
             }
-            qkpend = has_next;
-            if (has_next) {
-                load_gslice<GATED>(gs, g, gate, nxt.tok0, nxt.valid, r0, nxt.h, H, d);
-                if (tid < nxt.valid) beta_nxt = beta_of(nxt.tok0 + tid, nxt.h);
-                if (GATED) {
-                    bias_nxt = *reinterpret_cast<const float4 *>(gate.dt_bias + nxt.h * D + d);
-                    alog_nxt = gate.a_log[nxt.h];
-                }
+            qkpend = true;
+            load_gslice<GATED>(gs, g, gate, nxt.tok0, nxt.valid, r0, nxt.h, H, d);
+            if (tid < nxt.valid) beta_nxt = beta_of(nxt.tok0 + tid, nxt.h);
+            if (GATED) {
+                bias_nxt = *reinterpret_cast<const float4 *>(gate.dt_bias + nxt.h * D + d);
+                alog_nxt = gate.a_log[nxt.h];
             }
-            if (tid == kPrepThreads - 1 && item + 2 * (int)gridDim.x < n_items)
-                *sNext = prep_item(item + 2 * gridDim.x, H, chunk_off, seq_start, seq_len, n_seqs);
+            if (tid == kPrepThreads - 1 && nxt.valid) *sNext = take_item();
             if (!__syncthreads_and(ok)) {
                 ok = false;
                 break;
@@ -534,8 +574,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
         mpend = true;
         // metadata of the item after next, fetched by one thread whose
         // dependent loads stall only its own warp, handed over in shared memory
-        if (tid == kPrepThreads - 1 && item + 2 * (int)gridDim.x < n_items)
-            *sNext = prep_item(item + 2 * gridDim.x, H, chunk_off, seq_start, seq_len, n_seqs);
+        if (tid == kPrepThreads - 1 && nxt.valid) *sNext = take_item();
 
         // 4. causal scores A (j <= r, to the record) and the beta-scaled
         //    strictly lower L (to shared fp32 for the inverse): TMEM lanes
@@ -758,17 +797,15 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
             mma_tile<128, 256, 64, 128, 64, false, true>(tmem, smem_u32(sT), smem_u32(sm + P_V), false);
             mma_tile<128, 256, 64, 128, 64, false, true>(tmem, smem_u32(sT + 16384), smem_u32(sm + P_V), true);
             mma_commit(mbar);
-            if (has_next) load_qk(sm, maps, nxt.h, nxt.tok0, full_qk);
+            load_qk(sm, maps, nxt.h, nxt.tok0, full_qk);
         }
         mpend = true;
-        qkpend = has_next;
-        if (has_next) {
-            load_gslice<GATED>(gs, g, gate, nxt.tok0, nxt.valid, r0, nxt.h, H, d);
-            if (tid < nxt.valid) beta_nxt = beta_of(nxt.tok0 + tid, nxt.h);
-            if (GATED) {
-                bias_nxt = *reinterpret_cast<const float4 *>(gate.dt_bias + nxt.h * D + d);
-                alog_nxt = gate.a_log[nxt.h];
-            }
+        qkpend = true;
+        load_gslice<GATED>(gs, g, gate, nxt.tok0, nxt.valid, r0, nxt.h, H, d);
+        if (tid < nxt.valid) beta_nxt = beta_of(nxt.tok0 + tid, nxt.h);
+        if (GATED) {
+            bias_nxt = *reinterpret_cast<const float4 *>(gate.dt_bias + nxt.h * D + d);
+            alog_nxt = gate.a_log[nxt.h];
         }
         if (mbar_wait(mbar, mphase)) {
             mphase ^= 1;
@@ -819,29 +856,33 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
             bulk_s2g(rec + TcRec::WQ + 16384, stg + 8192, 8192);   // W, key columns 64..127
             bulk_s2g(rec + TcRec::U, stg + 16384, 4 * TcRec::UBLK);
             bulk_commit();
+            *sPub = cur.c * H + cur.h;
         }
         }
+        if (!nxt.valid) break;
         cur = nxt;
-        if (item + 2 * (int)gridDim.x < n_items) nxt = *sNext;
+        nxt = *sNext;
         beta_cur = beta_nxt;
         bias_cur = bias_nxt;
         alog_cur = alog_nxt;
     }
-    if (tid == 0) bulk_wait_all();  // the last record's W and U are written
-    if (!ok) {
-        if (tid == 0) {
+    if (tid == 0) {
+        bulk_wait_all();  // the last record's W and U are written
+        publish();
+        // the tiles requested for the item of no rows after the last one (or,
+        // on the exit path, whatever copies and MMAs are still in flight) land
+        // before the shared memory and the TMEM are released
+        if (qkpend) mbar_wait(full_qk, qkphase, 400000000LL);
+        if (!ok) {
             atomicOr(status, kStatusTimeout);
-            // let copies and MMAs still in flight land before the shared memory
-            // and the TMEM are released
-            if (qkpend) mbar_wait(full_qk, qkphase, 400000000LL);
             if (vpend) mbar_wait(full_v, vphase, 400000000LL);
             if (mpend) mbar_wait(mbar, mphase, 400000000LL);
         }
-        __syncthreads();
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
+    if (tid == 0) count_release(prep_done);
 }
 
 // ---------------------------------------------------------------------------
@@ -870,6 +911,30 @@ static_assert(8 * (kStages + 4) + 4 <= 128, "scan barrier block");
 // issuer only: the output warps store the previous chunk's rows meanwhile and are
 // held by the next "S ready" instead)
 constexpr uint32_t kBarS = 1, kBarV = 2;
+
+// The split scan's shared memory: two "front" slots (the part a chunk step
+// needs first: WQ for D1, U for Vn, gC for the state update) and one KD | A
+// slot (read only by the step's last two MMAs), so that a CTA fits beside a
+// prep CTA on one SM and runs alongside the prep.
+constexpr uint32_t kFBytes = 32768 + 512 + TcRec::UBLK;  // WQ | gC | this CTA's U block
+constexpr uint32_t kKBytes = TcRec::GC - TcRec::KD;     // KD | A, contiguous in the record
+constexpr int SP_F = 37888;                             // front slot (kFBytes rounded up to 1024)
+constexpr int SP_FGC = 32768;                           // gC in a front slot
+constexpr int SP_FU = SP_FGC + 512;                     // U block in a front slot
+constexpr int SP_K = 2 * SP_F;                          // KD | A slot, 24 KB
+constexpr int SP_SOP = SP_K + 24576;                    // S operand [128 keys][32] bf16, 8 KB
+constexpr int SP_VOP = SP_SOP + 8192;                   // Vn operand [64 rows][32] bf16, 4 KB
+constexpr int SP_BAR = SP_VOP + 4096;                   // mbarriers, tmem slot
+constexpr int SP_BYTES = SP_BAR + 128;
+// more than half of an SM's 228 KB (with the 1 KB each CTA reserves), so that
+// the scan's CTAs spread one per SM, and room for one prep CTA beside each
+constexpr int SP_SMEM = 116736;
+static_assert(kFBytes <= (uint32_t)SP_F && TcRec::A - TcRec::KD == 16384 && kKBytes == 24576,
+              "split scan slots");
+static_assert(SP_BYTES + 1024 <= SP_SMEM && 2 * (SP_SMEM + 1024) > 233472 &&
+                  SP_SMEM + 1024 + P_SMEM + 1024 <= 233472,
+              "one split-scan CTA per SM, beside one prep CTA");
+static_assert(8 * 7 + 4 <= 128, "split scan barrier block");
 
 // This thread's 32 values x[v] as row k of an N = 32 operand (MN-major,
 // 64-byte swizzle, see sw64_off): four 16-byte stores, conflict-free across
@@ -1102,6 +1167,276 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kSplitTmemCols);
+}
+
+// Per chunk ck, D1 = D1[ck & 1]:
+//   issuers:    D1 = [W ; QG] S, keys 0..63 from warp 4 and keys 64..127 from
+//               warp 5 into two accumulators              after "S ready"
+//   warps 0-1:  Vn = U - (D1a + D1b)[0:64] -> Vn operand  -> "Vn ready"
+//   warps 2-3:  output rows of chunk ck-1 from D1[(ck-1) & 1]
+//   issuer:     D3 = KD^T Vn, then D1a[64:128] += A Vn    after "Vn ready"
+//   warps 0-3:  S = diag(gC) S + D3 -> S operand          -> "S ready"
+// Dedicated issuing warps keep the (slow to issue) MMAs off the threads that
+// own state rows; a tcgen05.mma costs its issuing thread ~60 cycles, so D1's
+// eight instructions go out as two groups of four at once.  The output MMA
+// runs while the state is updated.
+// Loads (all from the issuer): the front part of chunk ck+1 (WQ, gC, U) right
+// after D1 of chunk ck, into the front slot chunk ck-1 used; its KD | A once
+// D1 += A Vn of chunk ck has read the single KD | A slot.  Each waits for the
+// record's ready flag, so the scan can run alongside the prep that writes the
+// records (launched after it); with the records already written the flags
+// are up.  Registers are capped at 128 per thread (TMEM read in 16-column
+// halves where three 32-column rows would be live): an SM sub-partition holds
+// 16 K registers, and a scan CTA (6 warps, two on each of two sub-partitions)
+// shares its SM with a prep CTA (8 warps of 128 registers, two per
+// sub-partition).
+__global__ void __maxnreg__(128)
+    chunk_scan_tc_overlap_kernel(const float *__restrict__ initial_state, float *__restrict__ final_state,
+                         const int32_t *__restrict__ state_indices, __nv_bfloat16 *__restrict__ o,
+                         int n_seqs, int H, void *workspace, WsLayout L) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char *sK = sm + SP_K;
+    unsigned char *sS = sm + SP_SOP;
+    unsigned char *sVn = sm + SP_VOP;
+    uint64_t *full_f = reinterpret_cast<uint64_t *>(sm + SP_BAR);  // front slots 0, 1
+    uint64_t *full_k = full_f + 2;      // the KD | A slot
+    uint64_t *bar_ws = full_k + 1;      // D1 = WQ S done
+    uint64_t *bar_d3 = bar_ws + 1;      // D3 = KD^T Vn done
+    uint64_t *bar_out = bar_d3 + 1;     // D1 += A Vn done: the chunk's output rows
+    uint64_t *bar_drain = bar_out + 1;  // exit path: every MMA issued so far is done
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_drain + 1);
+    griddep_wait();  // the chunk index (and, launched after the prep, the records) is complete
+    // the next kernel may be scheduled: the prep, when it runs alongside (it
+    // waits for no part of this grid), or the next forward's chunk index (one
+    // CTA, which waits for this grid to complete before it writes anything)
+    griddep_launch_dependents();
+
+    const int n = blockIdx.x, h = blockIdx.y, vb = blockIdx.z, v0 = vb * BV;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    int32_t *scan_done = ws_at<int32_t>(workspace, L.scan_done_off);
+    const int32_t start = ws_at<const int32_t>(workspace, L.seq_start_off)[n];
+    if (start < 0) {  // sequence skipped (bad cu_seqlens or slot)
+        if (tid == 0) count_release(scan_done);
+        return;
+    }
+    const int len = ws_at<const int32_t>(workspace, L.seq_len_off)[n];
+    const int c0 = ws_at<const int32_t>(workspace, L.chunk_off_off)[n];
+    const int nck = (len + C - 1) / C;
+    const int64_t slot = state_indices ? (int64_t)state_indices[n] : (int64_t)n;
+    const int64_t st_off = (slot * H + h) * (int64_t)D * D;  // [V][K] block of (slot, h)
+    int32_t *status = ws_at<int32_t>(workspace, L.status_off);
+    const unsigned char *recs = ws_at<const unsigned char>(workspace, L.records_off);
+    const int32_t *ready = ws_at<const int32_t>(workspace, L.ready_off);
+    auto rec_of = [&](int ck) { return recs + ((size_t)(c0 + ck) * H + h) * TcRec::bytes; };
+    auto flag_of = [&](int ck) { return ready + (size_t)(c0 + ck) * H + h; };
+    auto fslot = [&](int ck) { return sm + (ck & 1) * SP_F; };
+    auto issue_f = [&](int ck) {  // the issuer, after the record's flag
+        unsigned char *dst = fslot(ck);
+        uint64_t *b = &full_f[ck & 1];
+        const unsigned char *r = rec_of(ck);
+        mbar_arrive_expect_tx(b, kFBytes);
+        bulk_g2s(dst, r + TcRec::WQ, 32768, b);
+        bulk_g2s(dst + SP_FGC, r + TcRec::GC, 512, b);
+        bulk_g2s(dst + SP_FU, r + TcRec::U + vb * TcRec::UBLK, TcRec::UBLK, b);
+    };
+    auto issue_k = [&](int ck) {  // the issuer, after the record's flag
+        mbar_arrive_expect_tx(full_k, kKBytes);
+        bulk_g2s(sK, rec_of(ck) + TcRec::KD, kKBytes, full_k);
+    };
+
+    if (warp == 0) tmem_alloc(tmem_slot, kSplitTmemCols);
+    if (tid == kIssuer) {
+        mbar_init(&full_f[0], 1);
+        mbar_init(&full_f[1], 1);
+        mbar_init(full_k, 1);
+        mbar_init(bar_ws, 2);  // both key halves of D1
+        mbar_init(bar_d3, 1);
+        mbar_init(bar_out, 1);
+        mbar_init(bar_drain, 2);  // both issuers
+        fence_mbar_init();
+    }
+    // state row d = tid (warps 0-3), columns v0 .. v0+31, fp32 in registers
+    float S[BV];
+    if (tid < D) {
+#pragma unroll
+        for (int x = 0; x < BV; ++x)
+            S[x] = initial_state ? initial_state[st_off + (int64_t)(v0 + x) * D + tid] : 0.0f;
+        store_row_n32(sS, tid, S);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tD3 = tmem + 128;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+
+    // Output rows of chunk ck (TMEM D1 buffer ck & 1, both key halves, lanes 64..127) -> o
+    // (warps 2-3), 16 columns at a time.
+    auto store_output = [&](int ck) {
+        const int r = tid - 64;
+        const bool live = r < min(C, len - ck * C);
+        uint4 *op = reinterpret_cast<uint4 *>(o + (((int64_t)start + (int64_t)ck * C + r) * H + h) * (int64_t)D + v0);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            float x[16], x2[16];
+            tmem_ld16(tmem + 32 * (ck & 1) + 16 * hf + lane_base, x);
+            tmem_ld16(tmem + 64 + 32 * (ck & 1) + 16 * hf + lane_base, x2);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c8 = 0; c8 < 2; ++c8) {
+                float y[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) y[t] = x[8 * c8 + t] + x2[8 * c8 + t];
+                if (live) op[2 * hf + c8] = pack8(y);
+            }
+        }
+    };
+
+    // loads issued / waited for, for the exit path (all from the issuer)
+    int f_issued = 0, f_done = 0, k_issued = 0;
+    bool ok = true;
+    if (nck > 0 && tid == kIssuer) {
+        ok = flag_wait(flag_of(0));
+        if (ok) {
+            issue_f(0);
+            issue_k(0);
+            f_issued = 1;
+            k_issued = 1;
+        }
+    }
+    for (int ck = 0; ck < nck; ++ck) {
+        const uint32_t fpar = (uint32_t)((ck >> 1) & 1), cpar = (uint32_t)(ck & 1);
+        unsigned char *fs = fslot(ck);
+        const uint32_t tD1 = tmem + 32 * (ck & 1);
+        const bool more = ck + 1 < nck;
+        if (tid == kIssuer) {
+            ok = mbar_wait(&full_f[ck & 1], fpar) && ok;
+            if (ok) f_done = ck + 1;
+            tc_fence_after();
+            if (ok) {  // keys 0..63 of D1 = [W ; QG] S
+                mma_tile_n32<128, 64, 128>(tD1, smem_u32(fs), smem_u32(sS), false);
+                mma_commit(bar_ws);
+            }
+            // the next chunk's front part, into the slot of chunk ck-1 (whose
+            // readers have all passed "S ready" of chunk ck-1)
+            if (ok && more) {
+                ok = flag_wait(flag_of(ck + 1));
+                if (ok) {
+                    issue_f(ck + 1);
+                    ++f_issued;
+                }
+            }
+        } else if (tid == kIssuer2) {
+            ok = mbar_wait(&full_f[ck & 1], fpar) && ok;
+            tc_fence_after();
+            if (ok) {  // keys 64..127 of D1, issued at the same time from a second thread
+                mma_tile_n32<128, 64, 128>(tD1 + 64, smem_u32(fs + 16384), smem_u32(sS + 4096), false);
+                mma_commit(bar_ws);
+            }
+        } else if (warp < 2) {
+            ok = mbar_wait(&full_f[ck & 1], fpar) && ok;  // U of this chunk
+            uint4 up[4];  // U row tid (bf16), read while D1 is formed
+            {
+                const uint4 *ur = reinterpret_cast<const uint4 *>(fs + SP_FU + tid * 64);
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) up[c8] = ur[c8 ^ ((tid >> 1) & 3)];
+            }
+            ok = mbar_wait(bar_ws, cpar) && ok;
+            tc_fence_after();
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {  // Vn = U - W S, row tid, 16 columns at a time
+                float x[16], x2[16];
+                tmem_ld16(tD1 + 16 * hf + lane_base, x);
+                tmem_ld16(tD1 + 64 + 16 * hf + lane_base, x2);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    float y[8];
+                    unpack8(up[2 * hf + c], y);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) y[t] -= x[8 * c + t] + x2[8 * c + t];
+                    *reinterpret_cast<uint4 *>(sVn + sw64_off(tid, 16 * hf + 8 * c)) = pack8(y);
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+        } else if (warp < 4) {
+            ok = mbar_wait(&full_f[ck & 1], fpar) && ok;  // gC of this chunk
+            if (ck > 0) {
+                ok = mbar_wait(bar_out, cpar ^ 1) && ok;
+                tc_fence_after();
+                if (ok) store_output(ck - 1);
+            }
+            tc_fence_before();
+        }
+        // (a failure seen here is carried to the "S ready" barrier below, which
+        // every warp reaches; the output warps' D3 wait then gives up on its own)
+        if (warp < 2 || warp == 4) ok = named_bar_and(kBarV, 96, ok);
+        if (tid == kIssuer) {
+            if (ok) ok = mbar_wait(full_k, cpar);  // KD | A of this chunk
+            tc_fence_after();
+            if (ok) {
+                mma_tile_n32<128, 64, 64, true>(tD3, smem_u32(sK), smem_u32(sVn), false);
+                mma_commit(bar_d3);
+                mma_tile_n32<128, 64, 128>(tD1, smem_u32(sK + 16384) - 8192, smem_u32(sVn), true);
+                mma_commit(bar_out);
+            }
+            // the next chunk's KD | A (its flag seen above), once this chunk's
+            // last MMA has read the slot
+            if (ok && more) {
+                ok = mbar_wait(bar_out, cpar);
+                if (ok) {
+                    issue_k(ck + 1);
+                    ++k_issued;
+                }
+            }
+        } else if (warp < 4 && ok) {
+            const float gc = reinterpret_cast<const float *>(fs + SP_FGC)[tid];
+            ok = mbar_wait(bar_d3, cpar) && ok;
+            tc_fence_after();
+            float x[32];  // S = diag(gC) S + KD^T Vn
+            tmem_ld32(tD3 + lane_base, x);
+            tmem_ld_wait();
+#pragma unroll
+            for (int vv = 0; vv < BV; ++vv) S[vv] = fmaf(gc, S[vv], x[vv]);
+            store_row_n32(sS, tid, S);
+            fence_async_smem();
+            tc_fence_before();
+        }
+        if (!named_bar_and(kBarS, kSplitThreads, ok)) {
+            ok = false;
+            break;
+        }
+    }
+    if (ok && nck > 0 && (warp == 2 || warp == 3)) {
+        ok = mbar_wait(bar_out, (uint32_t)((nck - 1) & 1));
+        tc_fence_after();
+        if (ok) store_output(nck - 1);
+    }
+    ok = __syncthreads_and(ok);
+    if (!ok) {
+        // let copies and MMAs still in flight land before the shared memory
+        // and the TMEM are released (at most one KD | A copy is in flight: a
+        // new one goes out only after the previous one was consumed)
+        if (tid == kIssuer2) mma_commit(bar_drain);
+        if (tid == kIssuer) {
+            atomicOr(status, kStatusTimeout);
+            for (int t = f_done; t < f_issued; ++t)
+                mbar_wait(&full_f[t & 1], (uint32_t)((t >> 1) & 1), 400000000LL);
+            if (k_issued > 0) mbar_wait(full_k, (uint32_t)((k_issued - 1) & 1), 400000000LL);
+            mma_commit(bar_drain);
+            mbar_wait(bar_drain, 0, 400000000LL);
+        }
+    } else if (final_state && tid < D) {
+#pragma unroll
+        for (int x = 0; x < BV; ++x) final_state[st_off + (int64_t)(v0 + x) * D + tid] = S[x];
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kSplitTmemCols);
+    if (tid == 0) count_release(scan_done);  // this CTA's outputs are written
 }
 
 // ---------------------------------------------------------------------------
@@ -1732,8 +2067,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 
 cudaError_t launch_chunk_prep_tc(const void *q, const void *k, const void *v, const float *g,
                                  const float *beta, const GateArgs *gate, int n_seqs,
-                                 int64_t total_tokens, int H, float scale, void *workspace,
-                                 cudaStream_t stream) {
+                                 int64_t total_tokens, int H, float scale, int scan_ctas,
+                                 void *workspace, cudaStream_t stream) {
     const WsLayout L = ws_layout(total_tokens, n_seqs, H, TcRec::bytes);
     const int64_t items_max = max_chunks(total_tokens, n_seqs) * (int64_t)H;
     const int grid = (int)std::min<int64_t>(items_max, (int64_t)kPrepMinBlocks * sm_count());
@@ -1753,12 +2088,12 @@ cudaError_t launch_chunk_prep_tc(const void *q, const void *k, const void *v, co
     cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                          cudaSharedmemCarveoutMaxShared);
     cudaError_t e = launch_dependent(kern, dim3(grid), dim3(kPrepThreads), P_SMEM, stream, maps, g,
-                                     beta, ga, n_seqs, H, scale, workspace, L);
+                                     beta, ga, n_seqs, H, scale, scan_ctas, workspace, L);
     if (e == cudaSuccess) e = cudaGetLastError();
     // the items deferred above (none in most workloads: its CTAs then exit at once)
     if (e == cudaSuccess)
         e = launch_chunk_prep_tc_strong(q, k, v, g, beta, gate, n_seqs, total_tokens, H, scale,
-                                        workspace, stream);
+                                        scan_ctas, grid, workspace, stream);
     return e;
 }
 
@@ -1814,6 +2149,58 @@ cudaError_t launch_chunk_scan_tc(const float *initial_state, float *final_state,
                                            n_seqs, H, workspace, L);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+void preload_chunk_tc_kernels() {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, chunk_prep_tc_kernel<true>) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, chunk_prep_tc_kernel<false>) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, chunk_scan_tc_overlap_kernel) != cudaSuccess)
+        cudaGetLastError();
+}
+
+int launch_chunk_scan_tc_ahead(const float *initial_state, float *final_state,
+                               const int32_t *state_indices, void *o, int n_seqs,
+                               int64_t total_tokens, int H, int flags, const EpiArgs *epi,
+                               void *workspace, cudaStream_t stream, cudaError_t *err) {
+    (void)epi;  // with an epilogue, the separate pass follows the step
+    *err = cudaSuccess;
+    const int64_t ctas = (int64_t)n_seqs * H * (D / BV);
+    // the split layout, one CTA per SM, and SMs left over for the strong-decay
+    // prep (which cannot share an SM with a scan CTA) and for prep CTAs in pairs
+    if ((flags & KDA_CHUNK_SCAN_WIDE) || ctas + 8 > sm_count()) return 0;
+    {  // every kernel launched while this scan runs is loaded first (once per device)
+        static bool loaded[64] = {false};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+            cudaGetLastError();
+            return 0;
+        }
+        if (!loaded[dev]) {
+            preload_chunk_tc_kernels();
+            preload_chunk_tc_strong_kernels();
+            preload_chunk_index_kernel();
+            preload_output_gate_norm_kernels();
+            loaded[dev] = true;
+        }
+    }
+    const WsLayout L = ws_layout(total_tokens, n_seqs, H, TcRec::bytes);
+    const dim3 grid((unsigned)n_seqs, (unsigned)H, D / BV);
+    cudaFuncSetAttribute(chunk_scan_tc_overlap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SP_SMEM);
+    // the whole 228 KB as shared memory, so that a prep CTA fits beside a scan CTA
+    cudaFuncSetAttribute(chunk_scan_tc_overlap_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
+    // cooperative: every CTA is resident before the prep (launched next, and
+    // let go once every scan CTA has started) takes the rest of the GPU
+    const cudaError_t e = launch_dependent_coop(chunk_scan_tc_overlap_kernel, grid, dim3(kSplitThreads), SP_SMEM,
+                                                stream, initial_state, final_state, state_indices,
+                                                (__nv_bfloat16 *)o, n_seqs, H, workspace, L);
+    if (e != cudaSuccess) {  // refused (nothing was launched): the scan runs after the prep
+        cudaGetLastError();
+        return 0;
+    }
+    *err = cudaGetLastError();
+    return (int)ctas;
 }
 
 }  // namespace kda

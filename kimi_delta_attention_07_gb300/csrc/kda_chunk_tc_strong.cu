@@ -189,10 +189,19 @@ __device__ __forceinline__ float4 mm16_row4(const float *A, int lda, const float
 template <bool GATED>
 __global__ void __launch_bounds__(kPrepThreads, 1)
     chunk_prep_tc_strong_kernel(const __grid_constant__ RawMaps maps, const float *__restrict__ beta,
-                         const GateArgs gate, int n_seqs, int H, float scale, void *workspace,
-                         WsLayout L) {
+                         const GateArgs gate, int n_seqs, int H, float scale, int scan_ctas,
+                         int prep_ctas, void *workspace, WsLayout L) {
     constexpr uint32_t kGBytes = GATED ? 16384u : 32768u;
-    griddep_wait();  // the chunk index (previous kernel) is complete
+    if (!scan_ctas) {
+        griddep_wait();  // the prep (previous kernel) is complete
+    } else {
+        // the prep's CTAs have all finished (their deferred items listed); the
+        // kernel before this one is not waited for, as that would wait for the
+        // scan running alongside, which waits for the items listed here
+        if (threadIdx.x == 0 && !count_wait(ws_at<const int32_t>(workspace, L.prep_done_off), prep_ctas))
+            atomicOr(ws_at<int32_t>(workspace, L.status_off), kStatusTimeout);
+        __syncthreads();
+    }
     auto beta_of = [&](int64_t tok, int hh) {
         return GATED ? gate_beta(__bfloat162float(
                            reinterpret_cast<const __nv_bfloat16 *>(gate.raw_beta)[tok * H + hh]))
@@ -229,7 +238,22 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     int32_t *status = ws_at<int32_t>(workspace, L.status_off);
     const int32_t *list = ws_at<const int32_t>(workspace, L.defer_off);
     const int n_list = *ws_at<const int32_t>(workspace, L.defer_count_off);
-    if ((int)blockIdx.x >= n_list) return;
+    int32_t *ready = ws_at<int32_t>(workspace, L.ready_off);
+    // With a scan running alongside (scan_ctas of them), the CTA that finishes
+    // last waits for the scan to finish too: whatever follows on the stream
+    // waits for this grid, so it then sees the scan's outputs.
+    auto finish = [&]() {  // one thread per CTA, at exit
+        if (!scan_ctas) return;
+        if (atomicAdd(ws_at<int32_t>(workspace, L.strong_done_off), 1) == (int)gridDim.x - 1) {
+            griddep_launch_dependents();
+            if (!count_wait(ws_at<const int32_t>(workspace, L.scan_done_off), scan_ctas))
+                atomicOr(status, kStatusTimeout);
+        }
+    };
+    if ((int)blockIdx.x >= n_list) {
+        if (threadIdx.x == 0) finish();
+        return;
+    }
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (warp == 0) tmem_alloc(tmem_slot, kPrepTmemCols);
@@ -833,6 +857,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             bulk_s2g(rec + TcRec::WQ + 16384, sXL + 8192, 8192);   // W, key columns 64..127
             bulk_s2g(rec + TcRec::U, sXL + 16384, 4 * TcRec::UBLK);
             bulk_commit();
+            bulk_wait_all();  // the record is complete (the other parts precede the barrier above)
+            flag_publish(ready + (size_t)cur.c * H + cur.h);
         }
         cur = nxt;
         if (li + 2 * (int)gridDim.x < n_list) nxt = *sNext;
@@ -853,14 +879,23 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         __syncthreads();
     }
     if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
+    if (tid == kLoader) finish();
 }
 
 }  // namespace
 
+void preload_chunk_tc_strong_kernels() {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, chunk_prep_tc_strong_kernel<true>) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, chunk_prep_tc_strong_kernel<false>) != cudaSuccess)
+        cudaGetLastError();
+}
+
 cudaError_t launch_chunk_prep_tc_strong(const void *q, const void *k, const void *v,
                                         const float *g, const float *beta, const GateArgs *gate,
                                         int n_seqs, int64_t total_tokens, int H, float scale,
-                                        void *workspace, cudaStream_t stream) {
+                                        int scan_ctas, int prep_ctas, void *workspace,
+                                        cudaStream_t stream) {
     const WsLayout L = ws_layout(total_tokens, n_seqs, H, TcRec::bytes);
     const int64_t items_max = max_chunks(total_tokens, n_seqs) * (int64_t)H;
     const int grid = (int)std::min<int64_t>(items_max, (int64_t)sm_count());
@@ -882,7 +917,8 @@ cudaError_t launch_chunk_prep_tc_strong(const void *q, const void *k, const void
     auto kern = gate ? chunk_prep_tc_strong_kernel<true> : chunk_prep_tc_strong_kernel<false>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
     const cudaError_t e = launch_dependent(kern, dim3(grid), dim3(kPrepThreads), P_SMEM, stream,
-                                           maps, beta, ga, n_seqs, H, scale, workspace, L);
+                                           maps, beta, ga, n_seqs, H, scale, scan_ctas, prep_ctas,
+                                           workspace, L);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

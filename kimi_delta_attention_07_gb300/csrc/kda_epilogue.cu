@@ -61,6 +61,13 @@ __global__ void __launch_bounds__(kEpiThreads)
 
 }  // namespace
 
+void preload_output_gate_norm_kernels() {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, output_gate_norm_kernel<__nv_bfloat16>) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, output_gate_norm_kernel<float>) != cudaSuccess)
+        cudaGetLastError();
+}
+
 cudaError_t launch_output_gate_norm(void *o, const EpiArgs &epi, int64_t rows, int dtype,
                                     cudaStream_t stream) {
     if (rows == 0) return cudaSuccess;

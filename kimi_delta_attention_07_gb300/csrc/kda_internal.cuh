@@ -47,12 +47,16 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 // ---- workspace layout -----------------------------------------------------
 //
-//   [0, 256)      status word (int32, StatusBits), deferred-item count (int32,
-//                 tensor-core path) + padding
+//   [0, 256)      status word (int32, StatusBits), deferred-item count, and the
+//                 counters of the tensor-core path (items handed out by the prep,
+//                 scan CTAs finished, strong-decay prep CTAs finished, prep CTAs
+//                 finished), int32 each
 //   [256, ...)    seq_start[N] int32 (-1 = sequence skipped), seq_len[N] int32,
 //                 chunk_off[N+1] int32 (exclusive prefix sum of chunks per seq)
 //   aligned(16)   deferred (chunk, head) items, int32 [max chunks * H]
 //                 (tensor-core path: the items handed to the strong-decay prep)
+//   aligned(16)   ready flags, int32 [max chunks * H]: record written (cleared by
+//                 the chunk index, raised by the prep that writes the record)
 //   aligned(256)  per-(chunk, head) records, index chunk * H + head
 //
 // The record contents depend on the chunk path (fp32 CUDA-core path or bf16
@@ -81,8 +85,9 @@ constexpr int kEpiPairs = 64;
 constexpr int kEpiRing = 4;
 
 struct WsLayout {
-    size_t status_off, defer_count_off, seq_start_off, seq_len_off, chunk_off_off, seq_order_off,
-        epi_part_off, defer_off, records_off, record_bytes, total;
+    size_t status_off, defer_count_off, item_ctr_off, scan_done_off, strong_done_off, prep_done_off,
+        seq_start_off, seq_len_off, chunk_off_off, seq_order_off, epi_part_off, defer_off,
+        ready_off, records_off, record_bytes, total;
 };
 
 __host__ __device__ inline WsLayout ws_layout(int64_t total_tokens, int n_seqs, int H,
@@ -91,6 +96,10 @@ __host__ __device__ inline WsLayout ws_layout(int64_t total_tokens, int n_seqs, 
     const size_t arr = align_up(sizeof(int32_t) * (size_t)(n_seqs + 1), 16);
     L.status_off = 0;
     L.defer_count_off = 4;
+    L.item_ctr_off = 8;
+    L.scan_done_off = 12;
+    L.strong_done_off = 16;
+    L.prep_done_off = 20;
     L.seq_start_off = 256;
     L.seq_len_off = L.seq_start_off + arr;
     L.chunk_off_off = L.seq_len_off + arr;
@@ -98,7 +107,8 @@ __host__ __device__ inline WsLayout ws_layout(int64_t total_tokens, int n_seqs, 
     L.epi_part_off = align_up(L.seq_order_off + arr, 256);  // u64 [kEpiPairs][kEpiRing][4][64]
     L.defer_off = L.epi_part_off + sizeof(uint64_t) * kEpiPairs * kEpiRing * 4 * kChunk;
     const size_t items = (size_t)max_chunks(total_tokens, n_seqs) * (size_t)H;
-    L.records_off = align_up(L.defer_off + sizeof(int32_t) * items, 256);
+    L.ready_off = align_up(L.defer_off + sizeof(int32_t) * items, 16);
+    L.records_off = align_up(L.ready_off + sizeof(int32_t) * items, 256);
     L.record_bytes = record_bytes;
     L.total = L.records_off + items * record_bytes;
     return L;
@@ -253,7 +263,8 @@ __host__ __device__ inline WsGate ws_gate(const WsLayout &L, int64_t total_token
 
 // ---- launchers (return cudaGetLastError() of the launch) ------------------
 
-cudaError_t launch_chunk_index(const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens,
+// Also clears the ready flags and the counters of the tensor-core path.
+cudaError_t launch_chunk_index(const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens, int H,
                                const int32_t *state_indices, int64_t n_slots, void *workspace,
                                cudaStream_t stream);
 
@@ -267,19 +278,35 @@ cudaError_t launch_chunk_scan_f32(const float *initial_state, float *final_state
                                   cudaStream_t stream);
 
 // gate == nullptr: g, beta are activated fp32; otherwise g, beta are unused
-// and the raw gates of *gate are activated on chip.
+// and the raw gates of *gate are activated on chip.  scan_ctas > 0: the split
+// scan (that many CTAs) was launched just before and runs alongside, waiting
+// for each record's ready flag; the prep then does not wait for the kernel
+// before it, and the strong-decay prep's last CTA waits for the scan to finish
+// (so that whatever follows on the stream sees the scan complete).
 cudaError_t launch_chunk_prep_tc(const void *q, const void *k, const void *v, const float *g,
                                  const float *beta, const GateArgs *gate, int n_seqs,
-                                 int64_t total_tokens, int H, float scale, void *workspace,
-                                 cudaStream_t stream);
+                                 int64_t total_tokens, int H, float scale, int scan_ctas,
+                                 void *workspace, cudaStream_t stream);
 
 // The strong-decay prep of the tensor-core path: the (chunk, head) items that
 // chunk_prep_tc deferred (listed in the workspace), with per-16-token decay
 // references.  Launched right after launch_chunk_prep_tc, same arguments.
+// prep_ctas: the grid of the prep before it (with a scan running alongside,
+// this grid waits for that many prep CTAs to finish instead of waiting for
+// the kernel before it, which would wait for the scan as well).
 cudaError_t launch_chunk_prep_tc_strong(const void *q, const void *k, const void *v,
                                         const float *g, const float *beta, const GateArgs *gate,
                                         int n_seqs, int64_t total_tokens, int H, float scale,
-                                        void *workspace, cudaStream_t stream);
+                                        int scan_ctas, int prep_ctas, void *workspace,
+                                        cudaStream_t stream);
+
+// Load every kernel that a forward with the scan running alongside the prep
+// launches, once per device: a kernel loaded lazily while the scan waits for
+// the prep could wait for the running scan itself.
+void preload_chunk_tc_kernels();
+void preload_chunk_tc_strong_kernels();
+void preload_chunk_index_kernel();
+void preload_output_gate_norm_kernels();
 
 // Activated g and beta of a gated call into fp32 buffers (the fp32 path).
 cudaError_t launch_gate_activation(const GateArgs &gate, int dtype, int64_t total_tokens, int H,
@@ -292,6 +319,17 @@ cudaError_t launch_chunk_scan_tc(const float *initial_state, float *final_state,
                                  const int32_t *state_indices, void *o, int n_seqs,
                                  int64_t total_tokens, int H, int flags, const EpiArgs *epi,
                                  bool *epi_applied, void *workspace, cudaStream_t stream);
+
+// The split scan launched BEFORE the prep, to run alongside it: cooperatively
+// (every CTA resident, at most one per SM, leaving room for a prep CTA beside
+// each and for the strong-decay prep on the SMs left over).  Returns the
+// number of scan CTAs launched, 0 if this layout does not apply (the wide scan
+// is wanted, the epilogue would be fused, or the grid does not fit); a launch
+// error is returned in *err.
+int launch_chunk_scan_tc_ahead(const float *initial_state, float *final_state,
+                               const int32_t *state_indices, void *o, int n_seqs,
+                               int64_t total_tokens, int H, int flags, const EpiArgs *epi,
+                               void *workspace, cudaStream_t stream, cudaError_t *err);
 
 // Block-wide helper used by the chunk kernels: find the sequence that owns
 // global chunk `c` (largest n with chunk_off[n] <= c; chunk_off non-decreasing).

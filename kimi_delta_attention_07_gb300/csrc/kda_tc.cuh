@@ -127,6 +127,59 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// ---- ready flags between kernels that run at the same time ---------------------------
+// The writer publishes once its data is written: its own bulk copies complete
+// (bulk_wait_all) and the other threads' stores ordered before it by a CTA
+// barrier; the proxy fence orders the bulk copies' writes before the release.
+__device__ __forceinline__ void flag_publish(int32_t *p) {
+    asm volatile("fence.proxy.async.global;\n\tst.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(1)
+                 : "memory");
+}
+__device__ __forceinline__ int32_t flag_peek(const int32_t *p) {
+    int32_t v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ int32_t flag_load_acquire(const int32_t *p) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// The reader: once a relaxed read has seen the flag, this fence makes it an
+// acquire, and the proxy fence orders the bulk copies issued next after it.
+__device__ __forceinline__ void flag_acquire() {
+    asm volatile("fence.acq_rel.gpu;\n\tfence.proxy.async.global;" ::: "memory");
+}
+// Wait until *p is nonzero with acquiring reads (an acquiring read costs its
+// thread one L2 round trip; a fence after a relaxed read costs about twice
+// that, more with copies in flight), giving up after ~max_cycles SM clocks;
+// the proxy fence orders the bulk copies issued next after it.  False on
+// timeout.
+__device__ __forceinline__ bool flag_wait(const int32_t *p, long long max_cycles = 4000000000LL) {
+    if (!flag_load_acquire(p)) {
+        const long long t0 = clock64();
+        while (!flag_load_acquire(p)) {
+            if (clock64() - t0 > max_cycles) return false;
+        }
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+}
+// A counter that kernels running at the same time raise as they finish.
+__device__ __forceinline__ void count_release(int32_t *p) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(1) : "memory");
+}
+__device__ __forceinline__ bool count_wait(const int32_t *p, int32_t target,
+                                           long long max_cycles = 4000000000LL) {
+    const long long t0 = clock64();
+    while (flag_peek(p) < target) {
+        if (clock64() - t0 > max_cycles) return false;
+        __nanosleep(256);
+    }
+    flag_acquire();
+    return true;
+}
+
 // ---- TMEM ---------------------------------------------------------------------------
 // Executed by one full warp; the TMEM base address is written to *dst.
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {

@@ -405,6 +405,23 @@ def test_chunk_wide_and_split_scans_agree(kda):
     assert rel_l2(to_np(s2), to_np(s1)) < 2e-3
 
 
+@pytest.mark.parametrize("n_seqs", [256, 300])
+def test_chunk_wide_scan_many_short_sequences(kda, n_seqs):
+    """The wide scan visits sequences longest first; at 256 sequences the
+    index kernel ranks them (ties included), beyond that it keeps their order.
+    Either way each output row and final state belongs to its own sequence."""
+    gen = torch.Generator().manual_seed(47 + n_seqs)
+    lengths = torch.randint(1, 101, (n_seqs,), generator=gen).tolist()
+    lengths[3] = lengths[7] = lengths[200] = 64  # ties across a chunk boundary
+    lengths[11] = 0
+    x = kda_inputs.prefill(lengths, H=2, dtype=torch.bfloat16, seed=48, init_std=0.02)
+    o, sf = run_chunk(kda, x, scan="wide")
+    o_ref, s_ref = oracle_prefill(x)
+    assert rel_l2(to_np(o), o_ref) < TOL_BF16
+    assert rel_l2(vk_to_kv(sf), s_ref) < TOL_BF16
+    assert np.array_equal(vk_to_kv(sf)[11], s_ref[11])  # the empty sequence keeps its state
+
+
 def test_chunk_bad_cu_seqlens_are_flagged_and_skipped(kda):
     x = kda_inputs.prefill([64, 64], H=1, dtype=torch.float32, seed=37)
     d = dev(x)
