@@ -61,7 +61,16 @@ def parse():
     p.add_argument("--no-varlen", action="store_true", help="skip the varlen_8 prefill sub-run")
     p.add_argument("--no-long", action="store_true",
                    help="skip the long_131k prefill + hand-off decode sub-run")
-    return p.parse_args()
+    p.add_argument("--phases", action="store_true",
+                   help="run each step as its two phases (the prep, then the scan after it) "
+                        "instead of one forward, and skip the sub-runs that need the whole "
+                        "forward: the form a kernel profiler can capture (it serialises "
+                        "kernels, and the forward's scan waits for records of a prep that "
+                        "runs beside it)")
+    a = p.parse_args()
+    if a.phases:
+        a.no_e2e = a.no_gated = a.no_varlen = a.no_long = True
+    return a
 
 
 # ---- distributed plumbing --------------------------------------------------
@@ -566,8 +575,12 @@ def run_ours(args, rank, ws):
     sf = torch.empty((1, H, V, K), dtype=torch.float32, device=dev)
     kw = dict(o=o, final_state=sf, workspace=work, precise=args.precise, stream=stream)
 
-    def step():  # the whole forward: one kda_chunk_fwd call
-        kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], **kw)
+    def step():  # the whole forward: one kda_chunk_fwd call (or its two phases)
+        if args.phases:
+            kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], phase="intra", **kw)
+            kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], phase="scan", **kw)
+        else:
+            kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], **kw)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -645,7 +658,9 @@ def run_ours(args, rank, ws):
                        "chunk": 64, "io_dtype": "bf16", "g_beta_state": "fp32",
                        "global_batch_tokens": T_4K * ws, "parallelism": f"replicas{ws}",
                        "l2": "inputs + workspace > 129 MB L2, no flush",
-                       "path": "fp32 CUDA-core (precise)" if args.precise else "default"},
+                       "path": "fp32 CUDA-core (precise)" if args.precise else "default",
+                       "step": ("the two phases run one after the other" if args.phases else
+                                "one forward: the scan runs alongside the prep")},
             "roofline": roofline, "step_roofline": step_roofline, "kernels": kernels,
             "e2e": e2e, "gpu_launches": launches, "clocks": clk,
             "decode": dec, "gated": gated, "short_conv": conv, "varlen_8": varlen,

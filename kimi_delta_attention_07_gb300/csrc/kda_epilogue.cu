@@ -41,6 +41,11 @@ __device__ __forceinline__ float4 gated_row(float4 x, float4 gt, float4 w, float
 template <typename T>
 __global__ void __launch_bounds__(kEpiThreads)
     output_gate_norm_kernel(T *__restrict__ o, const EpiArgs epi, int64_t rows) {
+    // launched as a dependent of the kernel before it (the scan, or the
+    // strong-decay prep that finishes after the scan): scheduled early, it
+    // reads o once that kernel has completed
+    griddep_wait();
+    griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const float4 w = *reinterpret_cast<const float4 *>(epi.weight + 4 * lane);
     const T *__restrict__ gate = reinterpret_cast<const T *>(epi.out_gate);
@@ -83,13 +88,17 @@ cudaError_t launch_output_gate_norm(void *o, const EpiArgs &epi, int64_t rows, i
         }
         return (int)std::min<int64_t>(blocks, (int64_t)sm_count() * per_sm);
     };
+    cudaError_t e;
     if (dtype == KDA_BF16) {
         auto kern = output_gate_norm_kernel<__nv_bfloat16>;
-        kern<<<one_wave(kern), kEpiThreads, 0, stream>>>((__nv_bfloat16 *)o, epi, rows);
+        e = launch_dependent(kern, dim3(one_wave(kern)), dim3(kEpiThreads), 0, stream,
+                             (__nv_bfloat16 *)o, epi, rows);
     } else {
         auto kern = output_gate_norm_kernel<float>;
-        kern<<<one_wave(kern), kEpiThreads, 0, stream>>>((float *)o, epi, rows);
+        e = launch_dependent(kern, dim3(one_wave(kern)), dim3(kEpiThreads), 0, stream, (float *)o, epi,
+                             rows);
     }
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
