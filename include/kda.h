@@ -136,7 +136,17 @@ size_t kda_chunk_workspace_bytes(int64_t total_tokens, int n_seqs, int H, int K,
  *               in one wave on the device, else the second.
  *               KDA_CHUNK_SCAN_SPLIT / KDA_CHUNK_SCAN_WIDE force one (not
  *               both; ignored on the fp32 path).  Results agree within
- *               rounding of the summation order.
+ *               rounding of the summation order.  In kda_chunk_fwd the
+ *               four-CTA scan, when its CTAs number at most the SM count
+ *               less 8, is launched before the intra-chunk phase and runs
+ *               alongside it (cooperatively, one CTA per SM beside one prep
+ *               CTA), waiting for each (chunk, head) record as it is
+ *               written; the results are those of the two phases run one
+ *               after the other, bit for bit.  Chunks that need the
+ *               strong-decay path (KDA_WS_STRONG_DECAY) are then redone
+ *               only on the SMs that host no scan CTA, so a call where most
+ *               chunks need it runs several times slower than with
+ *               KDA_CHUNK_SCAN_WIDE or the two phases called separately.
  *   workspace   device, 256-byte aligned, kda_chunk_workspace_bytes(...)
  *               bytes; its contents are scratch and may be anything.
  *
@@ -190,8 +200,10 @@ int kda_chunk_scan(const void *q, const void *k, const void *v, const float *g,
 #define KDA_WS_BAD_SEQLENS 1 /* cu_seqlens decreasing or outside [0, T]: those sequences skipped */
 #define KDA_WS_BAD_SLOT 2    /* a state_indices entry outside [0, n_slots): that sequence skipped */
 #define KDA_WS_TIMEOUT 4     /* a bounded wait of a kernel (a copy or an MMA that never
-                                completed, ~2 s) gave up: the CTA left its remaining chunks
-                                unwritten and exited; outputs of that call are incomplete */
+                                completed, or a record of the intra-chunk phase that a scan
+                                running alongside it never saw written, ~2 s) gave up: the
+                                CTA left its remaining chunks unwritten and exited; outputs of
+                                that call are incomplete */
 #define KDA_WS_EXACT_DECAY 8 /* informational, not an error: on the tensor-core path some
                                 16-token block decayed by more than 75 in a key channel (per-token
                                 decays below about -5) and its diagonal 16 x 16 scores were
@@ -401,14 +413,15 @@ int kda_recurrent_multi_step(const void *q, const void *k, const void *v, const 
  *   norm_weight device fp32 [V];  norm_eps > 0
  * replaces each output row of V values by
  *   o / sqrt(mean(o^2) + norm_eps) * norm_weight * sigmoid(out_gate).
- * Decode applies it in the step.  The chunked forward applies it inside its
- * state scan where it can (tensor-core path, one CTA per 32 value columns,
- * out_gate 16-byte aligned, at most 64 (sequence, head) pairs: the row's four
- * CTAs exchange their sums of squares through the workspace, and the grid is
+ * Decode applies it in the step.  The chunked forward applies it as a final
+ * pass over the stored o (kda_output_gate_norm) when its scan runs alongside
+ * the intra-chunk phase (see kda_chunk_fwd); otherwise inside its state scan
+ * where it can (tensor-core path, one CTA per 32 value columns, out_gate
+ * 16-byte aligned, at most 64 (sequence, head) pairs: the row's four CTAs
+ * exchange their sums of squares through the workspace, and the grid is
  * launched cooperatively, so it must fit the GPU at once), normalising the
- * unrounded o; otherwise as a final pass over the stored o
- * (kda_output_gate_norm).  The two agree within the rounding of o to its
- * dtype.
+ * unrounded o; else as the final pass.  The two agree within the rounding of
+ * o to its dtype.
  */
 int kda_chunk_fwd_gated(const void *q, const void *k, const void *v, const void *raw_gate,
                         const void *raw_beta, const float *a_log, const float *dt_bias,

@@ -736,9 +736,10 @@ def test_gated_chunk_with_output_epilogue(kda, dtype, precise, scan):
 
 def test_gated_prefill_4k_with_output_epilogue(kda):
     """The bench's gated 4k workload with the output epilogue (split-layout
-    scan): sampled heads against the oracle, and every head equal, within bf16
-    rounding of o, to the forward without the epilogue followed by the
-    standalone pass (a fused epilogue would normalise the unrounded o)."""
+    scan, run alongside the prep, then the epilogue pass): sampled heads
+    against the oracle, and every head equal, within bf16 rounding of o, to
+    the forward without the epilogue followed by the standalone pass (an
+    epilogue inside the scan would normalise the unrounded o)."""
     y = kda_inputs.with_output_gate(kda_inputs.prefill_4k_gated(), seed=6)
     d = dev(y, names=("q", "k", "v", "raw_gate", "raw_beta", "a_log", "dt_bias", "cu_seqlens",
                       "out_gate", "norm_weight"))
@@ -810,6 +811,29 @@ def test_gated_chunk_epilogue_split_scan_separate_pass(kda, case):
     out_ref = oracle.output_gate_norm(o_ref, y["out_gate"], y["norm_weight"], y["norm_eps"])
     assert rel_l2(to_np(o), out_ref) < TOL_BF16
     assert rel_l2(vk_to_kv(sf), s_ref) < TOL_BF16
+
+
+def test_gated_chunk_epilogue_in_the_split_scan(kda):
+    """37 (sequence, head) pairs: 148 scan CTAs fit one wave of a 152-SM GB300
+    but leave too few SMs to run the scan alongside the prep, so the scan runs
+    after it and applies the epilogue itself (its four CTAs per row exchanging
+    sums of squares); on another SM count another path, with the same result."""
+    x = kda_inputs.prefill([200], H=37, seed=65, init_std=0.02)
+    y, g_ref, b_ref = _gated(x, 65, "lower_bound")
+    y = kda_inputs.with_output_gate(y, seed=65)
+    d = dev(y, names=("q", "k", "v", "raw_gate", "raw_beta", "a_log", "dt_bias", "cu_seqlens",
+                      "initial_state", "out_gate", "norm_weight"))
+    o, sf = kda.kda_chunk_fwd_gated(d["q"], d["k"], d["v"], d["raw_gate"], d["raw_beta"], d["a_log"],
+                                    d["dt_bias"], lower_bound=y["lower_bound"], out_gate=d["out_gate"],
+                                    norm_weight=d["norm_weight"], norm_eps=y["norm_eps"],
+                                    cu_seqlens=d["cu_seqlens"], initial_state=d["initial_state"])
+    torch.cuda.synchronize()
+    s0 = np.swapaxes(y["initial_state"].double().numpy(), -1, -2)
+    o_ref, s_ref = oracle.recurrence(y["q"], y["k"], y["v"], g_ref, b_ref,
+                                     cu_seqlens=y["cu_seqlens"].numpy(), initial_state=s0)
+    out_ref = oracle.output_gate_norm(o_ref, y["out_gate"], y["norm_weight"], y["norm_eps"])
+    check_heads(to_np(o), out_ref, TOL_BF16, "o (37 heads, epilogue)")
+    check_heads(vk_to_kv(sf), s_ref, TOL_BF16, "S (37 heads)", axis=1)
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
