@@ -147,6 +147,9 @@ size_t kda_chunk_workspace_bytes(int64_t total_tokens, int n_seqs, int H, int K,
  *               only on the SMs that host no scan CTA, so a call where most
  *               chunks need it runs several times slower than with
  *               KDA_CHUNK_SCAN_WIDE or the two phases called separately.
+ *               The scan waits for each record for at most ~2 s: work on
+ *               other streams that holds the GPU's SMs that long makes the
+ *               call report KDA_WS_TIMEOUT.
  *   workspace   device, 256-byte aligned, kda_chunk_workspace_bytes(...)
  *               bytes; its contents are scratch and may be anything.
  *
