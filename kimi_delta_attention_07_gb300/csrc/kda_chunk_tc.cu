@@ -2071,7 +2071,8 @@ cudaError_t launch_chunk_prep_tc(const void *q, const void *k, const void *v, co
                                  void *workspace, cudaStream_t stream) {
     const WsLayout L = ws_layout(total_tokens, n_seqs, H, TcRec::bytes);
     const int64_t items_max = max_chunks(total_tokens, n_seqs) * (int64_t)H;
-    const int grid = (int)std::min<int64_t>(items_max, (int64_t)kPrepMinBlocks * sm_count());
+    // two CTAs per SM; beside a scan that runs alongside, one on each of its SMs
+    const int grid = (int)std::min<int64_t>(items_max, (int64_t)kPrepMinBlocks * sm_count() - scan_ctas);
     RawMaps maps;
     memset(&maps, 0, sizeof(maps));
     if (total_tokens > 0) {
