@@ -126,6 +126,7 @@ __device__ __forceinline__ PrepItem prep_item(int item, int H, const int32_t *ch
 // Rows past the end of the tensor arrive as zeros.
 struct RawMaps {
     CUtensorMap q, k, v;
+    CUtensorMap g;  // g fp32, or the raw bf16 gate: only prefetched into L2
 };
 
 __device__ __forceinline__ void load_qk(unsigned char *sm, const RawMaps &m, int h, int64_t tok0,
@@ -356,6 +357,22 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
     bool ok = true;
     for (;;) {
         if (!nxt.valid) griddep_launch_dependents();  // last item: the next kernel may be scheduled
+        // the next item's tiles and beta into L2 now, so that its loads (issued
+        // late in this item, where their shared memory and registers free up)
+        // find them there
+        if (tid == 0 && nxt.valid) {
+            tma_prefetch_3d(&maps.q, 0, nxt.h, (int)nxt.tok0);
+            tma_prefetch_3d(&maps.q, 64, nxt.h, (int)nxt.tok0);
+            tma_prefetch_3d(&maps.k, 0, nxt.h, (int)nxt.tok0);
+            tma_prefetch_3d(&maps.k, 64, nxt.h, (int)nxt.tok0);
+            tma_prefetch_3d(&maps.v, 0, nxt.h, (int)nxt.tok0);
+            tma_prefetch_3d(&maps.v, 64, nxt.h, (int)nxt.tok0);
+            tma_prefetch_3d(&maps.g, 0, nxt.h, (int)nxt.tok0);
+        } else if (tid >= 192 && tid - 192 < nxt.valid) {
+            const int64_t bt = (nxt.tok0 + (tid - 192)) * H + nxt.h;
+            prefetch_l2(GATED ? (const void *)(reinterpret_cast<const __nv_bfloat16 *>(gate.raw_beta) + bt)
+                              : (const void *)(beta + bt));
+        }
         unsigned char *rec = ws_at<unsigned char>(workspace, L.records_off + ((size_t)cur.c * H + cur.h) * TcRec::bytes);
         const int valid = cur.valid;
         if (tid < C) sB[tid] = tid < valid ? beta_cur : 0.0f;
@@ -2078,7 +2095,9 @@ cudaError_t launch_chunk_prep_tc(const void *q, const void *k, const void *v, co
     if (total_tokens > 0) {
         if (!encode_rows(&maps.q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, total_tokens, true) ||
             !encode_rows(&maps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, total_tokens, true) ||
-            !encode_rows(&maps.v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, total_tokens, true))
+            !encode_rows(&maps.v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, total_tokens, true) ||
+            !(gate ? encode_rows(&maps.g, gate->raw_gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, total_tokens)
+                   : encode_rows(&maps.g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, total_tokens)))
             return cudaErrorInvalidValue;
     }
     GateArgs ga;

@@ -95,6 +95,16 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int c0,
         : "memory");
 }
 
+// Prefetch the same tile into L2 only (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
 // ---- named barrier `id` (1..15; 0 is __syncthreads): returns once `count`
 // threads (whole warps) have arrived at it.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
