@@ -926,9 +926,9 @@ constexpr int S_SMEM = S_BYTES + 1024;
 static_assert(kStageBytes <= (uint32_t)S_STAGE, "stage too small");
 static_assert(kImageBytes % 16 == 0 && TcRec::UBLK % 16 == 0, "bulk copy size");
 static_assert(8 * (kStages + 4) + 4 <= 128, "scan barrier block");
-// named barriers: S operand ready (every warp), Vn ready (the Vn warps and the
-// issuer only: the output warps store the previous chunk's rows meanwhile and are
-// held by the next "S ready" instead)
+// named barriers: S operand ready (every warp), Vn ready (warps 0-4: the Vn
+// warps, the issuer, and the output warps once they have stored the previous
+// chunk's rows)
 constexpr uint32_t kBarS = 1, kBarV = 2;
 
 // The split scan's shared memory: two "front" slots (the part a chunk step
@@ -1134,8 +1134,11 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
             tc_fence_before();
         }
         // (a failure seen here is carried to the "S ready" barrier below, which
-        // every warp reaches; the output warps' D3 wait then gives up on its own)
-        if (warp < 2 || warp == 4) ok = named_bar_and(kBarV, 96, ok);
+        // every warp reaches.)  The output warps meet "Vn ready" too: they wait
+        // on bar_out's phase of chunk ck-1 by parity, so the issuer must not
+        // complete chunk ck's phase (D1 += A Vn, issued after this barrier)
+        // before they have seen the previous one.
+        if (warp < 5) ok = named_bar_and(kBarV, 160, ok);
         if (tid == kIssuer) {
             tc_fence_after();
             if (ok) {
@@ -1391,8 +1394,11 @@ __global__ void __maxnreg__(128)
             tc_fence_before();
         }
         // (a failure seen here is carried to the "S ready" barrier below, which
-        // every warp reaches; the output warps' D3 wait then gives up on its own)
-        if (warp < 2 || warp == 4) ok = named_bar_and(kBarV, 96, ok);
+        // every warp reaches.)  The output warps meet "Vn ready" too: they wait
+        // on bar_out's phase of chunk ck-1 by parity, so the issuer must not
+        // complete chunk ck's phase (D1 += A Vn, issued after this barrier)
+        // before they have seen the previous one.
+        if (warp < 5) ok = named_bar_and(kBarV, 160, ok);
         if (tid == kIssuer) {
             if (ok) ok = mbar_wait(full_k, cpar);  // KD | A of this chunk
             tc_fence_after();
@@ -2028,8 +2034,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             tc_fence_before();
         }
         // (a failure seen here is carried to the "S ready" barrier below, which
-        // every warp reaches; the output warps' D3 wait then gives up on its own)
-        if (q < 2 || warp == 8) ok = named_bar_and(kBarV, 160, ok);
+        // every warp reaches.)  The output warps meet "Vn ready" too: they wait
+        // on bar_out's phase of chunk ck-1 by parity, so the issuer must not
+        // complete chunk ck's phase (D1 += A Vn, issued after this barrier)
+        // before they have seen the previous one.
+        ok = named_bar_and(kBarV, kWideThreads, ok);
         if (tid == kWideIssuer) {
             tc_fence_after();
             if (ok) {

@@ -422,6 +422,30 @@ def test_chunk_wide_scan_many_short_sequences(kda, n_seqs):
     assert np.array_equal(vk_to_kv(sf)[11], s_ref[11])  # the empty sequence keeps its state
 
 
+def test_chunk_back_to_back_forwards_do_not_wait_out(kda):
+    """3000 forwards of the 4k workload back to back on one workspace (the
+    scan running alongside the prep): none may sit in a bounded device wait
+    until it gives up (~2 s).  A scan whose output warps could fall a whole
+    chunk behind the issuer once did so about once in 3000 calls."""
+    import time
+    x = kda_inputs.prefill_4k()
+    d = dev(x)
+    work = torch.empty(kda.kda_chunk_workspace_bytes(4096, 1, 32), dtype=torch.uint8, device="cuda")
+    o = torch.empty((4096, 32, 128), dtype=torch.bfloat16, device="cuda")
+    sf = torch.empty((1, 32, 128, 128), dtype=torch.float32, device="cuda")
+    kw = dict(o=o, final_state=sf, workspace=work)
+    for _ in range(3):
+        kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], **kw)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for _ in range(3000):
+        kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], **kw)
+    torch.cuda.synchronize()
+    dt = time.time() - t0
+    assert kda.kda_workspace_status(work) == 0
+    assert dt < 1.5, f"3000 forwards took {dt:.2f} s"
+
+
 def test_chunk_bad_cu_seqlens_are_flagged_and_skipped(kda):
     x = kda_inputs.prefill([64, 64], H=1, dtype=torch.float32, seed=37)
     d = dev(x)
