@@ -29,10 +29,67 @@ namespace {
 constexpr int kDecodeThreads = 256;  // 8 warps
 constexpr int kWarps = kDecodeThreads / 32;
 constexpr int kMaxRowsPerWarp = kHeadDim / kWarps;  // 16: a whole head per CTA
+constexpr int kTokBlk = 8;  // speculative decode: tokens per block of gate tables
+constexpr int kTabPer = kTokBlk * kHeadDim / kDecodeThreads;  // table entries per thread
+
+// One butterfly level of a reduce-scatter over the warp: a lane holding N
+// partial sums passes the half its partner keeps (across lane bit N/2) and
+// adds the partner's share of the half it keeps.
+template <int N>
+__device__ __forceinline__ void scatter_level(float (&p)[16], int lane) {
+    constexpr int M = N / 2;
+    const bool hi = (lane & M) != 0;
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        const float send = hi ? p[i] : p[i + M];
+        const float keep = hi ? p[i + M] : p[i];
+        p[i] = keep + __shfl_xor_sync(0xffffffffu, send, M);
+    }
+}
+
+// One token's update of a warp's 16 state rows when its CTA holds a whole
+// head (row j of the warp is head row warp + 8 j; dst points at lane's four
+// key channels of row 0 in the destination).  The 32 dot products of the
+// rows, a_j = s_j . k_hat and c_j = s_j . q_hat, are summed over the lanes by
+// a reduce-scatter: at each butterfly level a lane keeps half of its partial
+// sums and hands the other half to its partner, so lane l ends with the whole
+// sum of product l (a_l below 16, c_{l-16} above) after 31 shuffles, where
+// one lane-wide reduction per product takes 160.  Returns u_j on lane j < 16
+// and o_j = c_j + u_j (k_hat . q_hat) on lane 16 + j.
+__device__ __forceinline__ float whole_head_token(float4 (&s)[kMaxRowsPerWarp], float4 dec,
+                                                  float4 kh, float4 qh, float kq, float b,
+                                                  float vrow, float *dst, int lane) {
+    float p[16];
+    const bool hi = (lane & 16) != 0;  // the first level pairs a_j with c_j of the same row
+#pragma unroll
+    for (int j = 0; j < kMaxRowsPerWarp; ++j) {
+        float4 x = s[j];
+        x.x *= dec.x; x.y *= dec.y; x.z *= dec.z; x.w *= dec.w;
+        s[j] = x;
+        const float a = x.x * kh.x + x.y * kh.y + x.z * kh.z + x.w * kh.w;
+        const float c = x.x * qh.x + x.y * qh.y + x.z * qh.z + x.w * qh.w;
+        p[j] = (hi ? c : a) + __shfl_xor_sync(0xffffffffu, hi ? a : c, 16);
+    }
+    scatter_level<16>(p, lane);
+    scatter_level<8>(p, lane);
+    scatter_level<4>(p, lane);
+    scatter_level<2>(p, lane);
+    const float u = b * (vrow - p[0]);  // lanes 0-15 (vrow: v of row `lane`)
+    const float uo = __shfl_sync(0xffffffffu, u, lane & 15);
+#pragma unroll
+    for (int j = 0; j < kMaxRowsPerWarp; ++j) {
+        const float uj = __shfl_sync(0xffffffffu, u, j);
+        float4 x = s[j];
+        x.x += uj * kh.x; x.y += uj * kh.y; x.z += uj * kh.z; x.w += uj * kh.w;
+        s[j] = x;
+        *reinterpret_cast<float4 *>(dst + (int64_t)(kWarps * j) * kHeadDim) = x;
+    }
+    return hi ? p[0] + uo * kq : u;
+}
 
 // One token per sequence (the common decode step).
 template <typename T, bool GATED, bool EPI>
-__global__ void __launch_bounds__(kDecodeThreads)
+__global__ void __launch_bounds__(kDecodeThreads, 2)
     recurrent_step_kernel(const T *__restrict__ q, const T *__restrict__ k,
                           const T *__restrict__ v, const float *__restrict__ g,
                           const float *__restrict__ beta, const GateArgs gate, const EpiArgs epi,
@@ -103,28 +160,39 @@ __global__ void __launch_bounds__(kDecodeThreads)
     const float kq = warp_sum(kh.x * qh.x + kh.y * qh.y + kh.z * qh.z + kh.w * qh.w);
 
     float my_o = 0.0f, ss = 0.0f;  // epilogue: o of row `lane`, sum of o^2 over the warp's rows
-#pragma unroll
-    for (int j = 0; j < kMaxRowsPerWarp; ++j) {
-        if (j >= rpw) break;
-        const int r = row0 + warp + kWarps * j;
-        float4 x = s[j];
-        x.x *= dec.x; x.y *= dec.y; x.z *= dec.z; x.w *= dec.w;
-        float a = x.x * kh.x + x.y * kh.y + x.z * kh.z + x.w * kh.w;
-        float c = x.x * qh.x + x.y * qh.y + x.z * qh.z + x.w * qh.w;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            a += __shfl_xor_sync(0xffffffffu, a, off);
-            c += __shfl_xor_sync(0xffffffffu, c, off);
-        }
-        const float u = b * (__shfl_sync(0xffffffffu, vrow, j) - a);
-        x.x += u * kh.x; x.y += u * kh.y; x.z += u * kh.z; x.w += u * kh.w;
-        *reinterpret_cast<float4 *>(S + (int64_t)r * kHeadDim + 4 * lane) = x;
-        const float ov = c + u * kq;
+    if (rpw == kMaxRowsPerWarp) {
+        const float ov = whole_head_token(s, dec, kh, qh, kq, b, vrow,
+                                          S + (int64_t)(row0 + warp) * kHeadDim + 4 * lane, lane);
         if (EPI) {
-            ss = fmaf(ov, ov, ss);
-            if (lane == j) my_o = ov;
-        } else if (lane == 0) {
-            o[io_k + r] = from_f32<T>(ov);
+            my_o = __shfl_sync(0xffffffffu, ov, (lane & 15) + 16);  // lanes 0-15: o of row `lane`
+            ss = warp_sum(lane < 16 ? my_o * my_o : 0.0f);
+        } else if (lane >= 16) {
+            o[io_k + row0 + warp + kWarps * (lane - 16)] = from_f32<T>(ov);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < kMaxRowsPerWarp; ++j) {
+            if (j >= rpw) break;
+            const int r = row0 + warp + kWarps * j;
+            float4 x = s[j];
+            x.x *= dec.x; x.y *= dec.y; x.z *= dec.z; x.w *= dec.w;
+            float a = x.x * kh.x + x.y * kh.y + x.z * kh.z + x.w * kh.w;
+            float c = x.x * qh.x + x.y * qh.y + x.z * qh.z + x.w * qh.w;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                a += __shfl_xor_sync(0xffffffffu, a, off);
+                c += __shfl_xor_sync(0xffffffffu, c, off);
+            }
+            const float u = b * (__shfl_sync(0xffffffffu, vrow, j) - a);
+            x.x += u * kh.x; x.y += u * kh.y; x.z += u * kh.z; x.w += u * kh.w;
+            *reinterpret_cast<float4 *>(S + (int64_t)r * kHeadDim + 4 * lane) = x;
+            const float ov = c + u * kq;
+            if (EPI) {
+                ss = fmaf(ov, ov, ss);
+                if (lane == j) my_o = ov;
+            } else if (lane == 0) {
+                o[io_k + r] = from_f32<T>(ov);
+            }
         }
     }
     if (EPI) {  // rows_per_cta == 128: this CTA holds the head's whole output row
@@ -142,7 +210,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
 // Speculative decode: S tokens per sequence, per-token destination slots,
 // the starting slot picked by the accepted count (see launch_recurrent_step).
 template <typename T, bool GATED, bool EPI>
-__global__ void __launch_bounds__(kDecodeThreads)
+__global__ void __launch_bounds__(kDecodeThreads, 2)
     recurrent_multi_step_kernel(const T *__restrict__ q, const T *__restrict__ k,
                                 const T *__restrict__ v, const float *__restrict__ g,
                                 const float *__restrict__ beta, const GateArgs gate,
@@ -150,13 +218,16 @@ __global__ void __launch_bounds__(kDecodeThreads)
                                 const int32_t *__restrict__ state_indices,
                                 const int32_t *__restrict__ num_accepted, int64_t n_slots,
                                 T *__restrict__ o, int S, int H, int rows_per_cta, float scale) {
-    // epilogue: per-warp sums of o^2 of token t in buffer t & 1, so that one
-    // barrier per token suffices (token t + 2 rewrites a buffer only after
-    // every warp has passed token t + 1's barrier, i.e. finished reading it)
-    __shared__ float s_part[2][kWarps];
-    // GATED: the decay factors of token t in buffer t & 1, activated once per CTA
-    // (16 channels per warp) at the end of token t - 1
-    __shared__ __align__(16) float s_dec[2][kHeadDim];
+    // Tokens go in blocks of up to kTokBlk.  At the start of a block the CTA
+    // activates the block's raw gates (GATED: e^g of every key channel) and
+    // output gates (EPI: sigmoid) into shared tables, behind one barrier; the
+    // tokens then run without a barrier, the epilogue keeping each token's raw
+    // output row and per-warp sums of o^2 in shared memory until the block's
+    // end, where one barrier lets the CTA finish the block's rows.
+    __shared__ __align__(16) float s_dec[GATED ? kTokBlk : 1][kHeadDim];
+    __shared__ float s_og[EPI ? kTokBlk : 1][kHeadDim];    // sigmoid(out_gate)
+    __shared__ float s_o[EPI ? kTokBlk : 1][kHeadDim];     // o before the epilogue
+    __shared__ float s_part[EPI ? kTokBlk : 1][kWarps];    // per-warp sums of o^2
     const int pair = blockIdx.x;  // n * H + h
     const int n = pair / H;
     const int h = pair - n * H;
@@ -187,8 +258,50 @@ __global__ void __launch_bounds__(kDecodeThreads)
     }
     const int64_t slot_in = slot_of(acc - 1);
 
-    // This warp's state rows are requested first, so that their latency
-    // overlaps the setup below; they stay in registers across the tokens.
+    // The raw gates of a block of tokens (kTabPer entries of the tables per
+    // thread), and their activation into the tables.
+    struct TabIn {
+        float gx[kTabPer];  // GATED: raw gate + dt_bias
+        float og[kTabPer];  // EPI: raw output gate
+    };
+    auto tab_load = [&](int t0, int nb) {
+        TabIn in;
+#pragma unroll
+        for (int u = 0; u < kTabPer; ++u) {
+            const int i = threadIdx.x + u * kDecodeThreads;
+            in.gx[u] = 0.0f;
+            in.og[u] = 0.0f;
+            if (i < nb * kHeadDim) {
+                const int tt = i / kHeadDim, c = i % kHeadDim;
+                const int64_t e = io_of(t0 + tt) + c;
+                if (GATED)
+                    in.gx[u] = to_f32(reinterpret_cast<const T *>(gate.raw_gate)[e]) +
+                               gate.dt_bias[(int64_t)h * kHeadDim + c];
+                if (EPI) in.og[u] = to_f32(reinterpret_cast<const T *>(epi.out_gate)[e]);
+            }
+        }
+        return in;
+    };
+    auto tab_store = [&](const TabIn &in, int nb, float gscale) {
+#pragma unroll
+        for (int u = 0; u < kTabPer; ++u) {
+            const int i = threadIdx.x + u * kDecodeThreads;
+            if (i < nb * kHeadDim) {
+                const int tt = i / kHeadDim, c = i % kHeadDim;
+                if (GATED)
+                    s_dec[GATED ? tt : 0][c] =
+                        expf(gate_decay(in.gx[u], gscale, gate.lower_bound, gate.use_lower_bound != 0));
+                if (EPI) s_og[EPI ? tt : 0][c] = gate_beta(in.og[u]);
+            }
+        }
+    };
+    // The first block's raw gates are requested before the state, so that the
+    // tables are in place (behind the block's barrier) while the state rows
+    // are still on their way.
+    TabIn tab;
+    if (GATED || EPI) tab = tab_load(0, min(kTokBlk, S));
+
+    // This warp's state rows; they stay in registers across the tokens.
     const float *S0 = pool + ((slot_in * H + h) * (int64_t)kHeadDim) * kHeadDim;  // [V][K]
     float4 s[kMaxRowsPerWarp];
 #pragma unroll
@@ -200,28 +313,16 @@ __global__ void __launch_bounds__(kDecodeThreads)
     // the previous token's row updates.
     struct TokIn {
         float4 q4, k4, g4;  // g4: g (not GATED)
-        float gx;           // GATED: raw gate + dt_bias of channel 16 warp + lane (lanes 0-15)
         float vrow, b;      // vrow: v of the warp's row `lane`; b: beta (raw when GATED)
-        float gate_o, w_o;  // epilogue: output gate and norm weight of row `lane`
     };
     auto fetch = [&](int t) {
         TokIn in;
         const int64_t io_k = io_of(t);
         const int64_t pt = (int64_t)(n * S + t) * H + h;  // beta / raw beta index
         in.vrow = lane < rpw ? to_f32(v[io_k + row0 + warp + kWarps * lane]) : 0.0f;
-        in.gate_o = 0.0f;
-        in.w_o = 0.0f;
-        if (EPI && lane < rpw) {
-            const int r = row0 + warp + kWarps * lane;
-            in.gate_o = to_f32(reinterpret_cast<const T *>(epi.out_gate)[io_k + r]);
-            in.w_o = epi.weight[r];
-        }
         in.q4 = load4(q + io_k + 4 * lane);
         in.k4 = load4(k + io_k + 4 * lane);
         if (GATED) {
-            const int c = 16 * warp + (lane & 15);
-            in.gx = to_f32(reinterpret_cast<const T *>(gate.raw_gate)[io_k + c]) +
-                    gate.dt_bias[(int64_t)h * kHeadDim + c];
             in.b = to_f32(reinterpret_cast<const T *>(gate.raw_beta)[pt]);
         } else {
             in.g4 = load4(g + io_k + 4 * lane);
@@ -231,79 +332,85 @@ __global__ void __launch_bounds__(kDecodeThreads)
     };
     TokIn nxt = fetch(0);
     const float gscale = GATED ? expf(gate.a_log[h]) : 0.0f;
-    auto activate = [&](const TokIn &in, int buf) {  // GATED: one channel per lane 0-15
-        if (lane < 16)
-            s_dec[buf][16 * warp + lane] =
-                expf(gate_decay(in.gx, gscale, gate.lower_bound, gate.use_lower_bound != 0));
-    };
-    if (GATED) {
-        activate(nxt, 0);
-        __syncthreads();
-    }
-    for (int t = 0; t < S; ++t) {
-        const TokIn cur = nxt;
-        if (t + 1 < S) nxt = fetch(t + 1);
-        const int64_t io_k = io_of(t);
-        const float vrow = cur.vrow, gate_o = cur.gate_o, w_o = cur.w_o;
-        const float4 q4 = cur.q4, k4 = cur.k4;
-        float4 dec;
-        float b;
-        if (GATED) {
-            dec = *reinterpret_cast<const float4 *>(&s_dec[t & 1][4 * lane]);
-            b = gate_beta(cur.b);
-        } else {
-            dec = make_float4(expf(cur.g4.x), expf(cur.g4.y), expf(cur.g4.z), expf(cur.g4.w));
-            b = cur.b;
+    for (int t0 = 0; t0 < S; t0 += kTokBlk) {
+        const int nb = min(kTokBlk, S - t0);
+        if (GATED || EPI) {  // the tables of tokens t0 .. t0 + nb - 1
+            if (t0 > 0) {
+                __syncthreads();  // every thread is done with the previous block's tables
+                tab = tab_load(t0, nb);
+            }
+            tab_store(tab, nb, gscale);
+            __syncthreads();
         }
-        const float sq = warp_sum(q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w);
-        const float sk = warp_sum(k4.x * k4.x + k4.y * k4.y + k4.z * k4.z + k4.w * k4.w);
-        const float rq = scale / sqrtf(sq + 1e-6f);
-        const float rk = 1.0f / sqrtf(sk + 1e-6f);
-        const float4 qh = make_float4(q4.x * rq, q4.y * rq, q4.z * rq, q4.w * rq);
-        const float4 kh = make_float4(k4.x * rk, k4.y * rk, k4.z * rk, k4.w * rk);
-        const float kq = warp_sum(kh.x * qh.x + kh.y * qh.y + kh.z * qh.z + kh.w * qh.w);
+        for (int tt = 0; tt < nb; ++tt) {
+            const int t = t0 + tt;
+            const TokIn cur = nxt;
+            if (t + 1 < S) nxt = fetch(t + 1);
+            const int64_t io_k = io_of(t);
+            const float vrow = cur.vrow;
+            const float4 q4 = cur.q4, k4 = cur.k4;
+            float4 dec;
+            float b;
+            if (GATED) {
+                dec = *reinterpret_cast<const float4 *>(&s_dec[GATED ? tt : 0][4 * lane]);
+                b = gate_beta(cur.b);
+            } else {
+                dec = make_float4(expf(cur.g4.x), expf(cur.g4.y), expf(cur.g4.z), expf(cur.g4.w));
+                b = cur.b;
+            }
+            const float sq = warp_sum(q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w);
+            const float sk = warp_sum(k4.x * k4.x + k4.y * k4.y + k4.z * k4.z + k4.w * k4.w);
+            const float rq = scale / sqrtf(sq + 1e-6f);
+            const float rk = 1.0f / sqrtf(sk + 1e-6f);
+            const float4 qh = make_float4(q4.x * rq, q4.y * rq, q4.z * rq, q4.w * rq);
+            const float4 kh = make_float4(k4.x * rk, k4.y * rk, k4.z * rk, k4.w * rk);
+            const float kq = warp_sum(kh.x * qh.x + kh.y * qh.y + kh.z * qh.z + kh.w * qh.w);
 
-        float *Sd = pool + ((slot_of(t) * H + h) * (int64_t)kHeadDim) * kHeadDim;  // destination
-        float my_o = 0.0f, ss = 0.0f;  // epilogue: o of row `lane`, sum of o^2 over the warp's rows
-#pragma unroll
-        for (int j = 0; j < kMaxRowsPerWarp; ++j) {
-            if (j >= rpw) break;
-            const int r = row0 + warp + kWarps * j;
-            float4 x = s[j];
-            x.x *= dec.x; x.y *= dec.y; x.z *= dec.z; x.w *= dec.w;
-            float a = x.x * kh.x + x.y * kh.y + x.z * kh.z + x.w * kh.w;
-            float c = x.x * qh.x + x.y * qh.y + x.z * qh.z + x.w * qh.w;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                a += __shfl_xor_sync(0xffffffffu, a, off);
-                c += __shfl_xor_sync(0xffffffffu, c, off);
+            float *Sd = pool + ((slot_of(t) * H + h) * (int64_t)kHeadDim) * kHeadDim;  // destination
+            if (rpw == kMaxRowsPerWarp) {
+                const float ov = whole_head_token(s, dec, kh, qh, kq, b, vrow,
+                                                  Sd + (int64_t)(row0 + warp) * kHeadDim + 4 * lane, lane);
+                if (EPI) {  // rows_per_cta == 128: this CTA holds the head's whole output row
+                    const float my_o = __shfl_sync(0xffffffffu, ov, (lane & 15) + 16);  // o of row `lane`
+                    const float ss = warp_sum(lane < 16 ? my_o * my_o : 0.0f);
+                    if (lane < 16) s_o[EPI ? tt : 0][warp + kWarps * lane] = my_o;
+                    if (lane == 0) s_part[EPI ? tt : 0][warp] = ss;
+                } else if (lane >= 16) {
+                    o[io_k + row0 + warp + kWarps * (lane - 16)] = from_f32<T>(ov);
+                }
+                continue;
             }
-            const float u = b * (__shfl_sync(0xffffffffu, vrow, j) - a);
-            x.x += u * kh.x; x.y += u * kh.y; x.z += u * kh.z; x.w += u * kh.w;
-            s[j] = x;
-            *reinterpret_cast<float4 *>(Sd + (int64_t)r * kHeadDim + 4 * lane) = x;
-            const float ov = c + u * kq;
-            if (EPI) {
-                ss = fmaf(ov, ov, ss);
-                if (lane == j) my_o = ov;
-            } else if (lane == 0) {
-                o[io_k + r] = from_f32<T>(ov);
+#pragma unroll
+            for (int j = 0; j < kMaxRowsPerWarp; ++j) {  // (never with the epilogue)
+                if (j >= rpw) break;
+                const int r = row0 + warp + kWarps * j;
+                float4 x = s[j];
+                x.x *= dec.x; x.y *= dec.y; x.z *= dec.z; x.w *= dec.w;
+                float a = x.x * kh.x + x.y * kh.y + x.z * kh.z + x.w * kh.w;
+                float c = x.x * qh.x + x.y * qh.y + x.z * qh.z + x.w * qh.w;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    a += __shfl_xor_sync(0xffffffffu, a, off);
+                    c += __shfl_xor_sync(0xffffffffu, c, off);
+                }
+                const float u = b * (__shfl_sync(0xffffffffu, vrow, j) - a);
+                x.x += u * kh.x; x.y += u * kh.y; x.z += u * kh.z; x.w += u * kh.w;
+                s[j] = x;
+                *reinterpret_cast<float4 *>(Sd + (int64_t)r * kHeadDim + 4 * lane) = x;
+                if (lane == 0) o[io_k + r] = from_f32<T>(c + u * kq);
             }
         }
-        // the next token's decays into the other buffer (read by every warp at the
-        // top of token t - 1, before the barrier that ended it)
-        if (GATED && t + 1 < S) activate(nxt, (t + 1) & 1);
-        if (EPI) {  // rows_per_cta == 128: this CTA holds the head's whole output row
-            if (lane == 0) s_part[t & 1][warp] = ss;
-            __syncthreads();  // also publishes the next token's decays
-            float tot = 0.0f;
+        if (EPI) {  // the block's output rows, normalised and gated
+            __syncthreads();
+            for (int i = threadIdx.x; i < nb * kHeadDim; i += kDecodeThreads) {
+                const int tt = i / kHeadDim, r = i % kHeadDim;
+                float tot = 0.0f;
 #pragma unroll
-            for (int w2 = 0; w2 < kWarps; ++w2) tot += s_part[t & 1][w2];
-            const float rn = 1.0f / sqrtf(tot * (1.0f / kHeadDim) + epi.eps);
-            if (lane < rpw)
-                o[io_k + row0 + warp + kWarps * lane] = from_f32<T>(my_o * rn * w_o * gate_beta(gate_o));
-        } else if (GATED && t + 1 < S) {
-            __syncthreads();  // the next token's decays are in place
+                for (int w2 = 0; w2 < kWarps; ++w2) tot += s_part[EPI ? tt : 0][w2];
+                const float rn = 1.0f / sqrtf(tot * (1.0f / kHeadDim) + epi.eps);
+                o[io_of(t0 + tt) + r] =
+                    from_f32<T>(s_o[EPI ? tt : 0][r] * rn * epi.weight[r] * s_og[EPI ? tt : 0][r]);
+            }
         }
     }
 }

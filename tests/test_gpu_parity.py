@@ -934,6 +934,37 @@ def test_gated_multi_step_matches_oracle(kda, dtype, gate, epilogue):
     assert rel_l2(vk_to_kv(pool_d), pool_ref) < TOL_F32
 
 
+@pytest.mark.parametrize("epilogue", [False, True])
+def test_gated_multi_step_past_one_table_block(kda, epilogue):
+    """A verify width of 11 draft tokens: the kernel activates the gates of
+    eight tokens at a time, so the second block (three tokens) reuses the
+    tables; accepted counts 11, 1 and 6, against the oracle."""
+    N, S, H = 3, 11, 2
+    tok = kda_inputs.spec_tokens(N, S, H=H, dtype=torch.bfloat16, seed=76)
+    y, g_ref, b_ref = _gated(tok, 76, "softplus")
+    y = kda_inputs.with_output_gate(y, seed=76)
+    pool = kda_inputs.decode_pool(N * S + 2, H=H, seed=76)
+    idx = torch.randperm(N * S + 2, generator=torch.Generator().manual_seed(76))[:N * S]
+    idx = idx.to(torch.int32).view(N, S)
+    acc = torch.tensor([11, 1, 6], dtype=torch.int32)
+    pool_d = pool.cuda()
+    names = ("q", "k", "v", "raw_gate", "raw_beta", "a_log", "dt_bias")
+    o = kda.kda_recurrent_multi_step_gated(
+        *(y[n].cuda() for n in names), pool_d, idx.cuda(), num_accepted=acc.cuda(),
+        lower_bound=y["lower_bound"], out_gate=y["out_gate"].cuda() if epilogue else None,
+        norm_weight=y["norm_weight"].cuda() if epilogue else None, norm_eps=y["norm_eps"])
+    torch.cuda.synchronize()
+    p0 = np.swapaxes(pool.double().numpy(), -1, -2)
+    o_ref, pool_ref = oracle.multi_step(y["q"], y["k"], y["v"], g_ref, b_ref, p0, idx.numpy(),
+                                        num_accepted=acc.numpy())
+    if epilogue:
+        o_ref = oracle.output_gate_norm(o_ref, y["out_gate"], y["norm_weight"], y["norm_eps"])
+    assert rel_l2(to_np(o), o_ref) < TOL_BF16
+    assert rel_l2(vk_to_kv(pool_d), pool_ref) < TOL_F32
+    for t in range(S):  # every token's rows against the oracle's, so no block is hidden
+        assert rel_l2(to_np(o[:, t]), o_ref[:, t]) < TOL_BF16, t
+
+
 def test_multi_step_with_one_token_equals_the_step(kda):
     N, H = 5, 3
     tok = kda_inputs.decode_tokens(N, H=H, seed=72)
