@@ -115,14 +115,22 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
         return;
     }
 
-    // This warp's state rows are requested first, so that their latency
-    // overlaps the setup below; lane j also fetches v of the warp's row j.
-    float *S = pool + ((slot * H + h) * (int64_t)kHeadDim) * kHeadDim;  // [V][K] of (slot, h)
-    float4 s[kMaxRowsPerWarp];
-#pragma unroll
-    for (int j = 0; j < kMaxRowsPerWarp; ++j)
-        if (j < rpw)
-            s[j] = *reinterpret_cast<const float4 *>(S + (int64_t)(row0 + warp + kWarps * j) * kHeadDim + 4 * lane);
+    // The token's inputs are requested before the state rows, so that the
+    // decays and norms are ready when the rows arrive; lane j fetches v of the
+    // warp's row j.
+    const float4 q4 = load4(q + io_k + 4 * lane);
+    const float4 k4 = load4(k + io_k + 4 * lane);
+    float4 g4, r4, c4;
+    float braw, gs = 0.0f;
+    if (GATED) {
+        r4 = load4(reinterpret_cast<const T *>(gate.raw_gate) + io_k + 4 * lane);
+        c4 = load4(gate.dt_bias + (int64_t)h * kHeadDim + 4 * lane);
+        gs = expf(gate.a_log[h]);
+        braw = to_f32(reinterpret_cast<const T *>(gate.raw_beta)[pair]);
+    } else {
+        g4 = load4(g + io_k + 4 * lane);
+        braw = beta[pair];
+    }
     const float vrow = lane < rpw ? to_f32(v[io_k + row0 + warp + kWarps * lane]) : 0.0f;
     float gate_o = 0.0f, w_o = 0.0f;  // epilogue: output gate and norm weight of row `lane`
     if (EPI && lane < rpw) {
@@ -130,25 +138,24 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
         gate_o = to_f32(reinterpret_cast<const T *>(epi.out_gate)[io_k + r]);
         w_o = epi.weight[r];
     }
+    float *S = pool + ((slot * H + h) * (int64_t)kHeadDim) * kHeadDim;  // [V][K] of (slot, h)
+    float4 s[kMaxRowsPerWarp];
+#pragma unroll
+    for (int j = 0; j < kMaxRowsPerWarp; ++j)
+        if (j < rpw)
+            s[j] = *reinterpret_cast<const float4 *>(S + (int64_t)(row0 + warp + kWarps * j) * kHeadDim + 4 * lane);
 
     // L2 norms of q and k over the key dim (eps inside the root), scale on q.
-    const float4 q4 = load4(q + io_k + 4 * lane);
-    const float4 k4 = load4(k + io_k + 4 * lane);
-    float4 g4;
     float b;
     if (GATED) {
-        const float4 r4 = load4(reinterpret_cast<const T *>(gate.raw_gate) + io_k + 4 * lane);
-        const float4 c4 = load4(gate.dt_bias + (int64_t)h * kHeadDim + 4 * lane);
-        const float gs = expf(gate.a_log[h]);
         const bool lb = gate.use_lower_bound != 0;
         g4 = make_float4(gate_decay(r4.x + c4.x, gs, gate.lower_bound, lb),
                          gate_decay(r4.y + c4.y, gs, gate.lower_bound, lb),
                          gate_decay(r4.z + c4.z, gs, gate.lower_bound, lb),
                          gate_decay(r4.w + c4.w, gs, gate.lower_bound, lb));
-        b = gate_beta(to_f32(reinterpret_cast<const T *>(gate.raw_beta)[pair]));
+        b = gate_beta(braw);
     } else {
-        g4 = load4(g + io_k + 4 * lane);
-        b = beta[pair];
+        b = braw;
     }
     const float sq = warp_sum(q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w);
     const float sk = warp_sum(k4.x * k4.x + k4.y * k4.y + k4.z * k4.z + k4.w * k4.w);
