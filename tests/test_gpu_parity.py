@@ -446,6 +446,46 @@ def test_chunk_back_to_back_forwards_do_not_wait_out(kda):
     assert dt < 1.5, f"3000 forwards took {dt:.2f} s"
 
 
+def test_gated_epilogue_forwards_alternate_on_one_workspace(kda):
+    """The gated 4k forward with the output epilogue (the scan running
+    alongside the prep, then the epilogue pass launched as its dependent), on
+    two inputs in turn, 100 times each, on one workspace: the last outputs
+    equal the first bit for bit, no bounded wait ran out, and the epilogue
+    forward equals the forward followed by the standalone pass."""
+    ins = []
+    for seed in (6, 7):
+        y = kda_inputs.with_output_gate(kda_inputs.with_raw_gates(
+            kda_inputs.prefill([4096], H=32, dtype=torch.bfloat16, seed=seed), seed=seed), seed=seed)
+        ins.append(dev(y, names=("q", "k", "v", "raw_gate", "raw_beta", "a_log", "dt_bias",
+                                 "out_gate", "norm_weight")))
+    eps = 1e-5
+    work = torch.empty(kda.kda_chunk_workspace_bytes(4096, 1, 32), dtype=torch.uint8, device="cuda")
+    outs = [torch.empty((4096, 32, 128), dtype=torch.bfloat16, device="cuda") for _ in ins]
+
+    def call(i):
+        d = ins[i]
+        return kda.kda_chunk_fwd_gated(d["q"], d["k"], d["v"], d["raw_gate"], d["raw_beta"], d["a_log"],
+                                       d["dt_bias"], lower_bound=-5.0, out_gate=d["out_gate"],
+                                       norm_weight=d["norm_weight"], norm_eps=eps, workspace=work,
+                                       o=outs[i])[0]
+
+    first = [call(i).clone() for i in range(2)]
+    for _ in range(100):
+        for i in range(2):
+            call(i)
+    torch.cuda.synchronize()
+    assert kda.kda_workspace_status(work) == 0
+    for i in range(2):
+        assert torch.equal(outs[i], first[i]), i
+    # and the same rows as the forward without the epilogue followed by the pass
+    d = ins[0]
+    o2, _ = kda.kda_chunk_fwd_gated(d["q"], d["k"], d["v"], d["raw_gate"], d["raw_beta"], d["a_log"],
+                                    d["dt_bias"], lower_bound=-5.0)
+    kda.kda_output_gate_norm(o2, d["out_gate"], d["norm_weight"], eps)
+    torch.cuda.synchronize()
+    assert torch.equal(first[0], o2)
+
+
 def test_chunk_bad_cu_seqlens_are_flagged_and_skipped(kda):
     x = kda_inputs.prefill([64, 64], H=1, dtype=torch.float32, seed=37)
     d = dev(x)
