@@ -591,9 +591,6 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
             mma_commit(mbar);
         }
         mpend = true;
-        // metadata of the item after next, fetched by one thread whose
-        // dependent loads stall only its own warp, handed over in shared memory
-        if (tid == kPrepThreads - 1 && nxt.valid) *sNext = take_item();
 
         // 4. causal scores A (j <= r, to the record) and the beta-scaled
         //    strictly lower L (to shared fp32 for the inverse): TMEM lanes
@@ -736,6 +733,11 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
                     *reinterpret_cast<uint4 *>(z) = make_uint4(0, 0, 0, 0);
                     *reinterpret_cast<uint4 *>(z + 8192) = make_uint4(0, 0, 0, 0);
                 }
+                // and the item after next, claimed here, where these warps wait
+                // for the substitutions anyway (the later an item is claimed,
+                // the less the CTAs' ends spread when the items run out);
+                // handed over in shared memory
+                if (tid == kPrepThreads - 1 && nxt.valid) *sNext = take_item();
             }
             __syncthreads();
             if (tid < 192) {  // X_{q+1,q} = -M_{q+1,q} X_qq, one (row, 4 columns) slot per thread
