@@ -436,9 +436,13 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
                 else sRk[R - C] = R - C < valid ? rsqrtf(ss + 1e-6f) : 0.0f;
             }
         }
-        if (tid == 0) {  // the previous item's W/U copies are done: its record is complete
-            bulk_wait_all();
-            publish();
+        if (tid == 0) {
+            if (scan_ctas) {  // the previous item's W/U copies are done: its record is
+                bulk_wait_all();  // complete, and the scan running alongside may read it
+                publish();
+            } else {  // (no one reads the flags before this kernel ends) its W/U staging,
+                bulk_wait_read();  // under the column operand written next, has been read
+            }
         }
         if (!__syncthreads_and(ok)) {
             ok = false;  // uniform from here on: every thread takes the exit path
