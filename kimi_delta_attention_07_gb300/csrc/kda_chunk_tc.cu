@@ -63,6 +63,10 @@ constexpr int D = kHeadDim;  // 128
 // ---------------------------------------------------------------------------
 constexpr int kPrepThreads = 256;
 constexpr int kPrepMinBlocks = 2;        // two CTAs per SM overlap each other's phases
+// the thread that copies W and U to the record and raises its ready flag,
+// with a scan running alongside: a lane of warp 4, whose warps finish the
+// transform pass ahead of warps 0-3 (without one, thread 0 copies them)
+constexpr int kStoreThread = 128;
 constexpr uint32_t kPrepTmemCols = 256;  // A/L result 0..63; then W 0..127, U 128..255
 constexpr float kLog2e = 1.4426950408889634f;
 // Largest |G_r - G_ref| (natural log units, ref = the reference row of r's
@@ -260,7 +264,8 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(full_qk + 3);
     PrepItem *sNext = reinterpret_cast<PrepItem *>(sm + P_BAR + 32);  // metadata two items ahead
     int *sFirst = reinterpret_cast<int *>(sm + P_BAR + 64);            // this CTA's first item
-    int *sPub = sFirst + 1;  // thread 0: the item whose record waits for its ready flag, or -1
+    int *sPub = sFirst + 1;  // store thread: the item whose record waits for its ready flag, or -1
+    const int store_tid = scan_ctas ? kStoreThread : 0;
 
     const int32_t *chunk_off = ws_at<const int32_t>(workspace, L.chunk_off_off);
     const int32_t *seq_start = ws_at<const int32_t>(workspace, L.seq_start_off);
@@ -309,7 +314,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
         const int id = atomicAdd(ws_at<int32_t>(workspace, L.item_ctr_off), 1);
         return id < n_items ? prep_item(id, H, chunk_off, seq_start, seq_len, n_seqs) : no_item();
     };
-    auto publish = [&]() {  // thread 0, once the copies of the pending record are done
+    auto publish = [&]() {  // the store thread, once the copies of the pending record are done
         const int pub = *sPub;
         if (pub >= 0) flag_publish(ws_at<int32_t>(workspace, L.ready_off) + pub);
         *sPub = -1;
@@ -436,14 +441,9 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
                 else sRk[R - C] = R - C < valid ? rsqrtf(ss + 1e-6f) : 0.0f;
             }
         }
-        if (tid == 0) {
-            if (scan_ctas) {  // the previous item's W/U copies are done: its record is
-                bulk_wait_all();  // complete, and the scan running alongside may read it
-                publish();
-            } else {  // (no one reads the flags before this kernel ends) its W/U staging,
-                bulk_wait_read();  // under the column operand written next, has been read
-            }
-        }
+        // the previous item's W/U staging, under the column operand written
+        // next, has been read by its copies
+        if (tid == store_tid) bulk_wait_read();
         if (!__syncthreads_and(ok)) {
             ok = false;  // uniform from here on: every thread takes the exit path
             break;
@@ -561,6 +561,13 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
                 *reinterpret_cast<uint2 *>(kd + o16) =
                     make_uint2(pack2(col[0] * el[0], col[1] * el[1]), pack2(col[2] * el[2], col[3] * el[3]));
             }
+        }
+        // with a scan running alongside (the only reader of the ready flags),
+        // the previous item's record is complete once its W/U copies are: its
+        // flag goes up here, where warps 4-7 wait for warps 0-3 anyway
+        if (scan_ctas && tid == store_tid) {
+            bulk_wait_all();
+            publish();
         }
         fence_async_smem();
         tc_fence_before();
@@ -876,7 +883,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
             ok = false;  // uniform from here on: every thread takes the exit path
             break;
         }
-        if (tid == 0) {
+        if (tid == store_tid) {
             bulk_s2g(rec + TcRec::WQ, stg, 8192);                  // W, key columns 0..63
             bulk_s2g(rec + TcRec::WQ + 16384, stg + 8192, 8192);   // W, key columns 64..127
             bulk_s2g(rec + TcRec::U, stg + 16384, 4 * TcRec::UBLK);
@@ -891,9 +898,11 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
         bias_cur = bias_nxt;
         alog_cur = alog_nxt;
     }
-    if (tid == 0) {
+    if (tid == store_tid) {
         bulk_wait_all();  // the last record's W and U are written
         publish();
+    }
+    if (tid == 0) {
         // the tiles requested for the item of no rows after the last one (or,
         // on the exit path, whatever copies and MMAs are still in flight) land
         // before the shared memory and the TMEM are released
