@@ -365,8 +365,8 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepMinBlocks)
         // the next item's tiles and beta into L2 now, so that its loads (issued
         // late in this item, where their shared memory and registers free up)
         // find them there
-        // (from warp 2: thread 0's release of the previous record's flag, in the
-        // norms below, would wait for these)
+        // (from warp 2: a release of a record's flag by the thread that copies
+        // the records would wait for these)
         if (tid == 64 && nxt.valid) {
             tma_prefetch_3d(&maps.q, 0, nxt.h, (int)nxt.tok0);
             tma_prefetch_3d(&maps.q, 64, nxt.h, (int)nxt.tok0);
