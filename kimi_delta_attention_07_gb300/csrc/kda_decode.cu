@@ -13,12 +13,14 @@
 //
 // The state is streamed once in and once out (HBM bound): each warp owns
 // whole 512-byte rows, a lane holds 4 consecutive key channels (one 128-bit
-// load and one 128-bit store per lane per row), and the two dot products are
-// warp-shuffle reductions.  Rows of one head are split over CTAs when there
-// are too few (sequence, head) pairs to fill the GPU.  The gated variant
-// activates the model's raw gate and beta on the way in (see GateArgs); the
-// epilogue variant (one CTA per head) normalises each head's output row and
-// applies the output gate before storing it (see EpiArgs).
+// load and one 128-bit store per lane per row), and the two dot products per
+// row are summed over the lanes (for a whole head per CTA, all of a warp's
+// rows at once by one reduce-scatter; see whole_head_token).  Rows of one head
+// are split over CTAs when there are too few (sequence, head) pairs to fill
+// the GPU.  The gated variant activates the model's raw gate and beta on the
+// way in (see GateArgs); the epilogue variant (one CTA per head) normalises
+// each head's output row and applies the output gate before storing it (see
+// EpiArgs).
 #include <string.h>
 
 #include "kda_internal.cuh"
