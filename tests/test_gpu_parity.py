@@ -1005,6 +1005,51 @@ def test_gated_multi_step_past_one_table_block(kda, epilogue):
         assert rel_l2(to_np(o[:, t]), o_ref[:, t]) < TOL_BF16, t
 
 
+def test_gated_decode_whole_heads_without_epilogue(kda):
+    """40 sequences x 32 heads: enough (sequence, head) pairs that every CTA
+    keeps a whole head (the warps' row products summed by one reduce-scatter),
+    from raw gates and without the epilogue, for the one-token step and the
+    verify-width-4 step; the oracle follows a sample of pairs."""
+    N, H, S = 40, 32, 4
+    rng = np.random.default_rng(7)
+    seqs = np.sort(rng.choice(N, 4, replace=False))
+    heads = np.sort(rng.choice(H, 3, replace=False))
+    names = ("q", "k", "v", "raw_gate", "raw_beta", "a_log", "dt_bias")
+    # one token per sequence
+    tok = kda_inputs.decode_tokens(N, H=H, seed=81)
+    y, _, _ = _gated(tok, 81, "softplus")
+    pool = kda_inputs.decode_pool(N, H=H, seed=81)
+    pool_d = pool.cuda()
+    o = kda.kda_recurrent_step_gated(*(y[n].cuda() for n in names), pool_d, lower_bound=y["lower_bound"])
+    torch.cuda.synchronize()
+    g_ref, b_ref = oracle.gate_activation(y["raw_gate"][seqs][:, heads], y["raw_beta"][seqs][:, heads],
+                                          y["a_log"][heads], y["dt_bias"][heads], y["lower_bound"])
+    sub = {n: y[n][seqs][:, heads] for n in ("q", "k", "v")}
+    o_ref, pool_ref = oracle.step(sub["q"], sub["k"], sub["v"], g_ref, b_ref,
+                                  np.swapaxes(pool[seqs][:, heads].double().numpy(), -1, -2))
+    assert rel_l2(to_np(o[seqs][:, heads]), o_ref) < TOL_BF16
+    assert rel_l2(vk_to_kv(pool_d[seqs][:, heads]), pool_ref) < TOL_F32
+    # S draft tokens per sequence, per-token slots
+    tok = kda_inputs.spec_tokens(N, S, H=H, seed=82)
+    y, _, _ = _gated(tok, 82, "softplus")
+    pool = kda_inputs.decode_pool(N * S, H=H, seed=82)
+    idx = torch.arange(N * S, dtype=torch.int32).view(N, S)
+    acc = (torch.arange(N, dtype=torch.int32) % S) + 1
+    pool_d = pool.cuda()
+    o = kda.kda_recurrent_multi_step_gated(*(y[n].cuda() for n in names), pool_d, idx.cuda(),
+                                           num_accepted=acc.cuda(), lower_bound=y["lower_bound"])
+    torch.cuda.synchronize()
+    g_ref, b_ref = oracle.gate_activation(y["raw_gate"][seqs][:, :, heads], y["raw_beta"][seqs][:, :, heads],
+                                          y["a_log"][heads], y["dt_bias"][heads], y["lower_bound"])
+    sub = {n: y[n][seqs][:, :, heads] for n in ("q", "k", "v")}
+    p0 = np.swapaxes(pool[:, heads].double().numpy(), -1, -2)
+    o_ref, pool_ref = oracle.multi_step(sub["q"], sub["k"], sub["v"], g_ref, b_ref, p0, idx.numpy()[seqs],
+                                        num_accepted=acc.numpy()[seqs])
+    assert rel_l2(to_np(o[seqs][:, :, heads]), o_ref) < TOL_BF16
+    written = idx[seqs].reshape(-1).long()
+    assert rel_l2(vk_to_kv(pool_d[written][:, heads]), pool_ref[written.numpy()]) < TOL_F32
+
+
 def test_multi_step_with_one_token_equals_the_step(kda):
     N, H = 5, 3
     tok = kda_inputs.decode_tokens(N, H=H, seed=72)
