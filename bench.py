@@ -313,7 +313,8 @@ def time_phases(kda, d, steps, **kw):
 
 def time_prefill(kda, d, cu, init, steps, warmup, stream, ws, fin=None, idx=None):
     """Device time of the chunked forward on resident inputs (one call per
-    step, CUDA events on the launch stream), ms per call, and of its two
+    step, CUDA events on the launch stream between steps), ms per call as the
+    median step (so that one disturbed step does not move it), and of its two
     phases run alone."""
     T, Hh, _ = d["q"].shape
     N = cu.numel() - 1
@@ -331,15 +332,16 @@ def time_prefill(kda, d, cu, init, steps, warmup, stream, ws, fin=None, idx=None
     for _ in range(max(3, warmup)):
         step()
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     barrier(ws)
     torch.cuda.synchronize()
-    a.record(stream)
-    for _ in range(steps):
+    evs[0].record(stream)
+    for i in range(steps):
         step()
-    b.record(stream)
+        evs[i + 1].record(stream)
     torch.cuda.synchronize()
-    ms = max_over_ranks(a.elapsed_time(b) / steps, ws, d["q"].device)
+    per = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(steps))
+    ms = max_over_ranks(per[steps // 2], ws, d["q"].device)
     status = kda.kda_workspace_status(work, stream)
     intra, scan = time_phases(kda, d, steps, **kw)
     del work
