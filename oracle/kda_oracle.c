@@ -1,7 +1,7 @@
 /*
  * KDA oracle: plain fp64 token-by-token recurrence of Kimi Delta Attention.
  *
- * TEST INFRASTRUCTURE ONLY.  This file is the parity checker for the CUDA
+ * TEST INFRASTRUCTURE ONLY.  This file is the parity oracle for the CUDA
  * library; it shares no code, header, table or helper with it.  Only the
  * tests, the smoke check and the benchmark's CPU-baseline leg may build,
  * load or call it.
